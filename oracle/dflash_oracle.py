@@ -1,0 +1,331 @@
+"""Plain CPU oracle of the DFlash 2 draft-verify hot path.
+
+TEST INFRASTRUCTURE ONLY.  This module is imported by tests/, by
+``__graft_entry__.smoke()`` and by the CPU-baseline / reference legs of
+``bench.py``, nowhere else.  It shares no code with the CUDA library and
+never imports it.  It is deliberately slow: float64 numpy, one library
+primitive per step (a matmul, a sort, a cumulative sum), loops over
+sequences and positions written out.
+
+Sources (page title, section):
+  [DC]  "DFlash 2: Block diffusion, wearing a drafter's coat"
+  [2B]  "A 2B Drafter Made a 27B Model 3.4x Faster. Same Exact Output."
+  [KP]  "DFlash 2: Keep Drafting Parallel"
+  [QW]  "Qwen3.8-27B-DFlash2" (aiany.app item page)
+
+Readings where the pages are silent or garbled (each also listed in the
+design notes):
+  * conv: ``w_j(h) = W_j h`` (linear, no bias), ``x_t = h_t``, causal zero
+    pad ``h_{-1} = 0``, no residual; y rounded to the storage dtype.
+  * pair score: ``S_t(a, b) = U_t(b) + <E_in(a), G(h_t) * E_out(b)>`` with
+    ``G(h) = sigmoid(W_g h)``; the page's own equation did not survive
+    extraction, only its description ([KP] "A Lightweight Path Selector").
+  * U_t(b) is the raw drafter logit of candidate b (not the log-prob).
+  * the walk starts from the verified (anchor) token; greedy takes the best
+    successor, sampling draws from softmax(S_t(prev, .)/T) over the 16
+    candidates, and that conditional is the draft distribution q_t used by
+    the verifier (zero off the candidates).
+  * inverse CDF: the smallest index whose running sum is strictly greater
+    than u * total.
+  * accept test ``u * q(x) < p(x)`` (= ``u < min(1, p/q)``).
+  * degenerate residual (all weights zero): sample from p instead.
+  * bonus token when all K drafts are accepted: drawn from target row K.
+  * T = 0: greedy walk, accept iff the draft equals the target argmax, emit
+    the target argmax at the first mismatch / bonus slot.
+  * decisions (ranking, argmax, accept, inverse CDF) compare their operands
+    rounded to fp32, the precision the CUDA kernels decide in; the operands
+    themselves are computed in float64 from the exact input values.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from . import philox
+
+C = 16  # candidates per position ([DC] "Sixteen candidates per position")
+
+
+# --------------------------------------------------------------------------
+# storage rounding
+# --------------------------------------------------------------------------
+def round_bf16(x) -> np.ndarray:
+    """Round to the nearest bfloat16 (ties to even), via float32.
+
+    bfloat16 is the upper 16 bits of an IEEE float32; rounding adds
+    0x7FFF plus the lowest kept bit before truncating the low half.
+    Returns float32 values that are exactly representable in bf16.
+    """
+    f = np.ascontiguousarray(np.asarray(x, dtype=np.float32))
+    u = f.view(np.uint32).astype(np.uint64)
+    u = (u + np.uint64(0x7FFF) + ((u >> np.uint64(16)) & np.uint64(1))) \
+        & np.uint64(0xFFFF0000)
+    return u.astype(np.uint32).view(np.float32)
+
+
+def to_storage(x, dtype: str) -> np.ndarray:
+    """float64 -> the storage dtype's values (float32 array)."""
+    return round_bf16(x) if dtype == "bf16" else np.asarray(x, np.float32)
+
+
+# --------------------------------------------------------------------------
+# a1: two-tap dynamic depthwise convolution
+# --------------------------------------------------------------------------
+def conv2tap(h: np.ndarray, w_conv) -> np.ndarray:
+    """y_t = w0(h_t) * x_t + w1(h_t) * x_{t-1}, per channel, in float64.
+
+    [DC] "Suffix-decay convolution": a two-tap dynamic depthwise conv that
+    mixes each position with its predecessor; [2B] "The two fixes": "mixes
+    each position's representation with its immediate predecessor's".
+    h: [B, K, H]; w_conv: [2H, H] (rows 0..H-1 = W0, H..2H-1 = W1) or None,
+    in which case y = h.  The predecessor of the first block position is
+    zero (causal pad); positions never mix across sequences.
+    """
+    h = np.asarray(h, dtype=np.float64)
+    if w_conv is None:
+        return h.copy()
+    B, K, H = h.shape
+    W = np.asarray(w_conv, dtype=np.float64)
+    W0, W1 = W[:H], W[H:]
+    y = np.empty_like(h)
+    for b in range(B):
+        for t in range(K):
+            w0 = W0 @ h[b, t]            # dynamic tap weights from h_t
+            w1 = W1 @ h[b, t]
+            prev = h[b, t - 1] if t > 0 else np.zeros(H)
+            y[b, t] = w0 * h[b, t] + w1 * prev
+    return y
+
+
+# --------------------------------------------------------------------------
+# a2: LM head, logsumexp, top-16
+# --------------------------------------------------------------------------
+def lmhead_topk(y: np.ndarray, w_lm: np.ndarray, want_logits=False):
+    """Drafter logits U = y W^T, their logsumexp and the top-16 per row.
+
+    [DC] "Sixteen candidates per position"; [2B] "What a block-diffusion
+    drafter is": the drafter keeps its 16 best tokens per block slot;
+    [KP] "A Lightweight Path Selector": U_t is the drafter's own logit.
+    y: [M, H]; w_lm: [V, H].  Returns topv f32 [M,16], topi i32 [M,16]
+    (descending value, ties to the lower token id, padding -inf / -1 when
+    V < 16), lse f64 [M]; with want_logits also U f64 [M, V].
+    """
+    y = np.asarray(y, dtype=np.float64)
+    W = np.asarray(w_lm, dtype=np.float64)
+    U = y @ W.T                                   # [M, V] float64
+    M, V = U.shape
+    m = U.max(axis=1, keepdims=True)
+    lse = (m + np.log(np.exp(U - m).sum(axis=1, keepdims=True)))[:, 0]
+    U32 = U.astype(np.float32)                    # ranking precision
+    order = np.argsort(-U32, axis=1, kind="stable")[:, :C]
+    n = min(C, V)
+    topi = np.full((M, C), -1, np.int32)
+    topv = np.full((M, C), -np.inf, np.float32)
+    topi[:, :n] = order[:, :n]
+    topv[:, :n] = np.take_along_axis(U32, order[:, :n], axis=1)
+    out = (topv, topi, lse)
+    return out + (U,) if want_logits else out
+
+
+# --------------------------------------------------------------------------
+# a3: context gate + low-rank bilinear pair scores
+# --------------------------------------------------------------------------
+def gate(h: np.ndarray, w_gate: np.ndarray) -> np.ndarray:
+    """G(h_t) = sigmoid(W_g h_t) in float64.  h: [..., H]; w_gate [r, H].
+
+    [KP] "A Lightweight Path Selector": embeddings are matched under a
+    context gate of h_t.
+    """
+    z = np.asarray(h, np.float64) @ np.asarray(w_gate, np.float64).T
+    return 1.0 / (1.0 + np.exp(-z))
+
+
+def pair_score(topv, topi, anchor, g, e_in, e_out) -> np.ndarray:
+    """S[b,t,i,j] = U_t(c_j) + sum_k E_in[a_i,k] G_t[k] E_out[c_j,k].
+
+    [KP] "A Lightweight Path Selector" (every adjacent pair of candidates is
+    scored, predecessor a and current candidate b, low-rank bilinear over a
+    256-dim embedding, no backbone or LM-head pass); [DC] "A path selector".
+    Position 0's predecessor is the anchor (last verified) token for every
+    row i; position t >= 1 uses the candidates of position t-1.  Invalid
+    (-1) candidates or predecessors give -inf.
+    topv/topi: [B,K,16]; anchor [B]; g [B,K,r]; e_in/e_out [V,r].
+    Returns float64 [B,K,16,16].
+    """
+    topv = np.asarray(topv, np.float64)
+    topi = np.asarray(topi)
+    Ein = np.asarray(e_in, np.float64)
+    Eout = np.asarray(e_out, np.float64)
+    B, K, _ = topv.shape
+    S = np.full((B, K, C, C), -np.inf)
+    for b in range(B):
+        for t in range(K):
+            preds = (np.full(C, int(anchor[b])) if t == 0
+                     else topi[b, t - 1])
+            cands = topi[b, t]
+            for i in range(C):
+                if preds[i] < 0:
+                    continue
+                ein = Ein[preds[i]]
+                for j in range(C):
+                    if cands[j] < 0:
+                        continue
+                    S[b, t, i, j] = topv[b, t, j] + np.dot(
+                        ein * g[b, t], Eout[cands[j]])
+    return S
+
+
+# --------------------------------------------------------------------------
+# a4: walk through the K x 16 lattice
+# --------------------------------------------------------------------------
+def _inverse_cdf(w: np.ndarray, u: float):
+    """Smallest index whose running sum is strictly greater than u*total,
+    decided on fp32-rounded operands.  Returns (index, relative margin)."""
+    cum = np.cumsum(w)
+    tot = cum[-1]
+    thr32 = np.float32(u) * np.float32(tot)
+    above = np.nonzero(cum.astype(np.float32) > thr32)[0]
+    j = int(above[0]) if above.size else int(np.nonzero(w > 0)[0][-1])
+    thr = u * tot
+    lo = cum[j - 1] if j > 0 else 0.0
+    margin = min(abs(cum[j] - thr), abs(thr - lo)) / tot
+    return j, margin
+
+
+def path_walk(S, topi, T: float, u_walk):
+    """Walk one path through the candidate lattice per sequence.
+
+    [KP] "A Lightweight Path Selector": starting from the verified token,
+    greedy follows the best successor and sampling draws from the scores;
+    [2B] "The two fixes": one coherent route through the grid.
+    S: [B,K,16,16] (row = predecessor slot, column = candidate slot);
+    topi [B,K,16]; u_walk [B,K] uniforms (unused at T = 0).
+    Returns slot [B,K] i32, draft [B,K] i32, q [B,K,16] f64 and the
+    per-step decision margin [B,K] (score gap at T=0, CDF distance at T>0).
+    """
+    S = np.asarray(S, np.float64)
+    B, K = S.shape[:2]
+    slot = np.zeros((B, K), np.int32)
+    draft = np.zeros((B, K), np.int32)
+    q = np.zeros((B, K, C))
+    margin = np.zeros((B, K))
+    for b in range(B):
+        prev = 0            # every row of position 0 is the anchor's row
+        for t in range(K):
+            row = S[b, t, prev]
+            if T == 0.0:
+                r32 = row.astype(np.float32)
+                j = int(np.argmax(r32))           # first maximum
+                others = np.delete(row, j)
+                fin = others[np.isfinite(others)]
+                margin[b, t] = row[j] - fin.max() if fin.size else np.inf
+                q[b, t, j] = 1.0
+            else:
+                mx = row.max()
+                w = np.where(np.isfinite(row), np.exp((row - mx) / T), 0.0)
+                j, margin[b, t] = _inverse_cdf(w, u_walk[b, t])
+                q[b, t] = w / w.sum()
+            slot[b, t] = j
+            draft[b, t] = topi[b, t, j]
+            prev = j
+    return slot, draft, q, margin
+
+
+# --------------------------------------------------------------------------
+# a5 + a6: rejection-sampling verify with residual / bonus resample
+# --------------------------------------------------------------------------
+def _softmax(z: np.ndarray):
+    m = z.max()
+    lse = m + np.log(np.exp(z - m).sum())
+    return np.exp(z - lse), lse
+
+
+def verify(L, draft, topi, q, T: float, u_acc, u_res):
+    """Verify K drafts per sequence against the target's K+1 logit rows.
+
+    [DC] "Lossless, with conditions I did not used to state": accept a
+    draft token with probability min(1, p/q) and resample from the residual
+    on rejection; [KP] "A Lightweight Path Selector": rejection sampling
+    restores the exact target distribution; [2B] "Caveats": greedy output
+    matches the target exactly.
+    L: [B,K+1,V] target logits; draft [B,K]; topi/q [B,K,16] (q = the
+    walk's draft distribution, zero off the candidates); u_acc [B,K];
+    u_res [B].  Returns n [B] (accepted drafts), out [B,K+1] (accepted
+    drafts, then the resampled / bonus token, then -1) and a dict of
+    decision margins.
+    """
+    L = np.asarray(L, np.float64)
+    B, K1, V = L.shape
+    K = K1 - 1
+    n_acc = np.zeros(B, np.int32)
+    out = np.full((B, K1), -1, np.int32)
+    acc_margin = np.full((B, K), np.inf)
+    res_margin = np.full(B, np.inf)
+    degenerate = np.zeros(B, bool)
+    for b in range(B):
+        n = K
+        for t in range(K):
+            d = int(draft[b, t])
+            if T == 0.0:
+                a = int(np.argmax(L[b, t].astype(np.float32)))
+                ok = (d == a)
+            else:
+                p, _ = _softmax(L[b, t] / T)
+                js = np.nonzero(topi[b, t] == d)[0]
+                qd = float(q[b, t, js[0]]) if js.size else 0.0
+                ok = bool(np.float32(u_acc[b, t]) * np.float32(qd)
+                          < np.float32(p[d]))
+                acc_margin[b, t] = abs(p[d] - u_acc[b, t] * qd) / max(p[d],
+                                                                      1e-300)
+            if not ok:
+                n = t
+                break
+        n_acc[b] = n
+        out[b, :n] = draft[b, :n]
+        if T == 0.0:
+            out[b, n] = int(np.argmax(L[b, n].astype(np.float32)))
+            continue
+        p, _ = _softmax(L[b, n] / T)
+        if n < K:
+            qf = np.zeros(V)
+            ok = topi[b, n] >= 0
+            qf[topi[b, n][ok]] = q[b, n][ok]
+            r = np.maximum(0.0, p - qf)
+        else:
+            r = p
+        if not r.sum() > 0.0:
+            r = p
+            degenerate[b] = True
+        v, res_margin[b] = _inverse_cdf(r, u_res[b])
+        out[b, n] = v
+    return n_acc, out, {"accept": acc_margin, "resample": res_margin,
+                        "degenerate": degenerate}
+
+
+# --------------------------------------------------------------------------
+# one whole draft-verify cycle
+# --------------------------------------------------------------------------
+def draft_verify_cycle(h, w_conv, w_lm, w_gate, e_in, e_out, anchor, L,
+                       T: float, seed: int, cycle: int, dtype: str):
+    """All five steps for B sequences, each stage fed by the previous one.
+
+    h: [B,K,H] drafter hidden states (values of the storage dtype);
+    L: [B,K+1,V] target logits.  Returns a dict of every intermediate.
+    """
+    h = np.asarray(h, np.float64)
+    B, K, H = h.shape
+    y = to_storage(conv2tap(h, w_conv), dtype).astype(np.float64)
+    topv, topi, lse = lmhead_topk(y.reshape(B * K, H), w_lm)
+    topv = topv.reshape(B, K, C)
+    topi = topi.reshape(B, K, C)
+    g = gate(h, w_gate)
+    S = pair_score(topv, topi, anchor, g, e_in, e_out)
+    S32 = S.astype(np.float32)
+    slot, draft, q, _ = path_walk(S32, topi, T,
+                                  philox.walk_uniforms(seed, cycle, B, K))
+    q32 = q.astype(np.float32)
+    n, out, _ = verify(L, draft, topi, q32, T,
+                       philox.accept_uniforms(seed, cycle, B, K),
+                       philox.resample_uniforms(seed, cycle, B, K))
+    return {"y": y, "topv": topv, "topi": topi, "lse": lse.reshape(B, K),
+            "g": g, "S": S32, "slot": slot, "draft": draft, "q": q32,
+            "n": n, "out": out}

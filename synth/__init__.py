@@ -1,0 +1,193 @@
+"""Seeded synthetic workloads for the DFlash 2 draft-verify hot path.
+
+This module only draws numbers. It holds none of the path's arithmetic
+(no convolution, no LM head, no scoring, walk or verify): both the CPU
+oracle and the CUDA path consume what it returns, and neither imports
+the other.
+
+Every tensor comes from ``numpy.random.Generator(PCG64)`` seeded with
+``SeedSequence([seed, tensor_id])``, so each tensor has its own stream and
+the values are identical on x86 and Arm hosts.  bf16 tensors are drawn in
+fp32 and rounded to bf16 (round-to-nearest-even) by torch's dtype cast.
+
+Shapes (row-major, contiguous):
+  h       [B, K+1, H]  drafter final hidden states.  The drafter path uses
+                       rows 0..K-1; row K exists only so that the target's
+                       bonus row K can be synthesised from a drafter logit.
+  w_conv  [2H, H]      two-tap dynamic conv weights, rows 0..H-1 = W0.
+  w_lm    [V, H]       drafter LM head.
+  w_gate  [r, H]       selector context gate.
+  e_in    [V, r]       selector embedding of the predecessor token.
+  e_out   [V, r]       selector embedding of the current candidate.
+  anchor  [B] int32    last verified token of each sequence.
+
+The target model's logits are defined by the workloads in terms of the
+drafter's own fp32 logits (``target = 0.9 * draft + noise`` and the like),
+so :func:`target_logits` takes those drafter logits as an argument and only
+applies the workload's transform and noise.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, replace
+from typing import Optional
+
+import numpy as np
+import torch
+
+__all__ = ["Workload", "CONFIGS", "get", "make_inputs", "target_logits",
+           "sweep_points"]
+
+# Tensor ids for the per-tensor streams.
+_TID = {"h": 1, "w_conv": 2, "w_lm": 3, "w_gate": 4, "e_in": 5, "e_out": 6,
+        "anchor": 7, "target": 8}
+
+
+@dataclass(frozen=True)
+class Workload:
+    """One synthetic draft-verify workload.
+
+    B sequences, K drafted positions each, vocabulary V, drafter hidden H,
+    selector rank r.  ``dtype`` is the storage type of the drafter-side
+    tensors ("bf16" or "fp32").  ``T`` is the sampling temperature (0 =
+    greedy).  ``target`` is (kind, a, noise_sd): kind "affine" gives
+    ``a*draft + N(0, noise_sd)``; kind "zipf" gives
+    ``-a*log(rank) + N(0, noise_sd)`` with rank the 1-based rank of the
+    token in the drafter's row (descending, ties to the lower id).
+    """
+    name: str
+    B: int
+    K: int
+    V: int
+    H: int
+    r: int
+    dtype: str
+    T: float
+    seed: int
+    w_lm_sd: float
+    conv_sd: Optional[float]
+    sel_sd: float
+    target: tuple
+
+    @property
+    def M(self) -> int:
+        return self.B * self.K
+
+    def with_(self, **kw) -> "Workload":
+        return replace(self, **kw)
+
+
+# The five workloads of the benchmark definition.  "tiny" has no conv
+# (y = h); "tiny_conv" is the same with a N(0, 0.05) conv.  The selector
+# scale of the bf16 workloads is not stated there; the tiny workload's
+# N(0, 0.1) is carried over.
+CONFIGS = {
+    "tiny": Workload("tiny", B=1, K=4, V=1024, H=64, r=32, dtype="fp32",
+                     T=0.0, seed=0, w_lm_sd=0.1, conv_sd=None, sel_sd=0.1,
+                     target=("affine", 1.0, 1.0)),
+    "tiny_conv": Workload("tiny_conv", B=1, K=4, V=1024, H=64, r=32,
+                          dtype="fp32", T=0.0, seed=0, w_lm_sd=0.1,
+                          conv_sd=0.05, sel_sd=0.1,
+                          target=("affine", 1.0, 1.0)),
+    "b1k8": Workload("b1k8", B=1, K=8, V=151936, H=2048, r=256, dtype="bf16",
+                     T=0.0, seed=1, w_lm_sd=0.02, conv_sd=0.05, sel_sd=0.1,
+                     target=("affine", 1.0, 0.5)),
+    "b32k8": Workload("b32k8", B=32, K=8, V=151936, H=2048, r=256,
+                      dtype="bf16", T=1.0, seed=2, w_lm_sd=0.02,
+                      conv_sd=0.05, sel_sd=0.1,
+                      target=("affine", 0.9, 1.0)),
+    "b128k16zipf": Workload("b128k16zipf", B=128, K=16, V=151936, H=2560,
+                            r=256, dtype="bf16", T=1.0, seed=3,
+                            w_lm_sd=0.02, conv_sd=0.05, sel_sd=0.1,
+                            target=("zipf", 1.1, 0.5)),
+}
+
+
+def sweep_points():
+    """The sweep grid: K in {4,8,16} x B in {1,8,32,128,256} x T in {0,1},
+    V=262144, H=3072, r=256, same generators as b32k8 (seed 4)."""
+    out = []
+    for K in (4, 8, 16):
+        for B in (1, 8, 32, 128, 256):
+            for T in (0.0, 1.0):
+                out.append(Workload(f"sweep_k{K}_b{B}_t{int(T)}", B=B, K=K,
+                                    V=262144, H=3072, r=256, dtype="bf16",
+                                    T=T, seed=4, w_lm_sd=0.02, conv_sd=0.05,
+                                    sel_sd=0.1, target=("affine", 0.9, 1.0)))
+    return out
+
+
+def get(name: str, **overrides) -> Workload:
+    w = CONFIGS[name]
+    return w.with_(**overrides) if overrides else w
+
+
+def _rng(seed: int, tensor: str) -> np.random.Generator:
+    return np.random.Generator(np.random.PCG64(
+        np.random.SeedSequence([int(seed), _TID[tensor]])))
+
+
+def _normal(seed, tensor, shape, sd, dtype) -> torch.Tensor:
+    x = _rng(seed, tensor).standard_normal(size=shape, dtype=np.float32)
+    if sd != 1.0:
+        x *= np.float32(sd)
+    t = torch.from_numpy(x)
+    return t.to(torch.bfloat16) if dtype == "bf16" else t
+
+
+def make_inputs(w: Workload) -> dict:
+    """All drafter-side inputs of workload ``w`` as CPU torch tensors."""
+    B, K, V, H, r = w.B, w.K, w.V, w.H, w.r
+    out = {
+        "h": _normal(w.seed, "h", (B, K + 1, H), 1.0, w.dtype),
+        "w_lm": _normal(w.seed, "w_lm", (V, H), w.w_lm_sd, w.dtype),
+        "w_gate": _normal(w.seed, "w_gate", (r, H), w.sel_sd, w.dtype),
+        "e_in": _normal(w.seed, "e_in", (V, r), w.sel_sd, w.dtype),
+        "e_out": _normal(w.seed, "e_out", (V, r), w.sel_sd, w.dtype),
+        "anchor": torch.from_numpy(
+            _rng(w.seed, "anchor").integers(0, V, size=B).astype(np.int32)),
+        "w_conv": None,
+    }
+    if w.conv_sd is not None:
+        out["w_conv"] = _normal(w.seed, "w_conv", (2 * H, H), w.conv_sd,
+                                w.dtype)
+    return out
+
+
+def target_logits(w: Workload, draft_logits: np.ndarray) -> torch.Tensor:
+    """Target logits [B, K+1, V] fp32 from the drafter's fp32 logits.
+
+    ``draft_logits`` are the drafter's logits for rows 0..K of every
+    sequence (row K uses the hidden state h[:, K]); the caller computes
+    them.  Only the workload's transform and seeded noise are applied here.
+    """
+    d = np.asarray(draft_logits, dtype=np.float32)
+    B, K1, V = d.shape
+    kind, a, sd = w.target
+    noise = _rng(w.seed, "target").standard_normal(size=d.shape,
+                                                   dtype=np.float32)
+    noise *= np.float32(sd)
+    if kind == "affine":
+        out = np.float32(a) * d + noise
+    elif kind == "zipf":
+        flat = d.reshape(-1, V)
+        # rank 1 = largest logit; ties go to the lower token id
+        order = np.argsort(-flat, axis=1, kind="stable")
+        rank = np.empty_like(order)
+        rows = np.arange(flat.shape[0])[:, None]
+        rank[rows, order] = np.arange(1, V + 1)[None, :]
+        out = (-np.float32(a) * np.log(rank.astype(np.float32))).reshape(
+            d.shape) + noise
+    else:
+        raise ValueError(f"unknown target kind {kind!r}")
+    return torch.from_numpy(np.ascontiguousarray(out, dtype=np.float32))
+
+
+def describe(w: Workload) -> str:
+    conv = "none" if w.conv_sd is None else f"N(0,{w.conv_sd})"
+    kind, a, sd = w.target
+    tgt = (f"{a}*draft+N(0,{sd})" if kind == "affine"
+           else f"-{a}*log(rank)+N(0,{sd})")
+    return (f"B={w.B} K={w.K} V={w.V} H={w.H} r={w.r} {w.dtype} T={w.T} "
+            f"seed={w.seed} h~N(0,1) W_lm~N(0,{w.w_lm_sd}) conv={conv} "
+            f"sel~N(0,{w.sel_sd}) target={tgt}")
+

@@ -1,0 +1,537 @@
+"""Pins of the CPU oracle against what the pages and the mathematics fix.
+
+Each test checks an oracle function against something other than itself:
+a closed form, a special case that reduces to a textbook or library routine,
+brute-force enumeration, or a statistical property the pages state (the
+sampler is lossless).  No GPU.
+"""
+import math
+import os
+import subprocess
+import sys
+import textwrap
+
+import numpy as np
+import pytest
+import torch
+from scipy import stats
+
+import oracle
+from oracle import philox
+
+C = 16
+
+
+# --------------------------------------------------------------------------
+# bf16 rounding
+# --------------------------------------------------------------------------
+def test_round_bf16_matches_torch_cast():
+    rng = np.random.default_rng(0)
+    x = np.concatenate([
+        rng.standard_normal(200000).astype(np.float32) * 10,
+        # exact ties between two bf16 neighbours: low half = 0x8000
+        (rng.integers(0, 2**15, 5000, dtype=np.uint32) << 16 | 0x8000)
+        .astype(np.uint32).view(np.float32),
+    ])
+    x = x[np.isfinite(x)]
+    ref = torch.from_numpy(x).to(torch.bfloat16).float().numpy()
+    got = oracle.round_bf16(x)
+    assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
+
+
+# --------------------------------------------------------------------------
+# Philox4x32-10
+# --------------------------------------------------------------------------
+_TRITON_PHILOX = textwrap.dedent("""
+    import os, sys, json
+    os.environ["TRITON_INTERPRET"] = "1"
+    import numpy as np, torch, triton, triton.language as tl
+
+    @triton.jit
+    def kern(c_ptr, k_ptr, o_ptr, N: tl.constexpr):
+        i = tl.arange(0, N)
+        c0 = tl.load(c_ptr + 4 * i + 0)
+        c1 = tl.load(c_ptr + 4 * i + 1)
+        c2 = tl.load(c_ptr + 4 * i + 2)
+        c3 = tl.load(c_ptr + 4 * i + 3)
+        k0 = tl.load(k_ptr + 2 * i + 0)
+        k1 = tl.load(k_ptr + 2 * i + 1)
+        a, b, c, d = tl.philox_impl(c0, c1, c2, c3, k0, k1, 10)
+        tl.store(o_ptr + 4 * i + 0, a)
+        tl.store(o_ptr + 4 * i + 1, b)
+        tl.store(o_ptr + 4 * i + 2, c)
+        tl.store(o_ptr + 4 * i + 3, d)
+
+    data = np.load(sys.argv[1])
+    ctr = torch.from_numpy(data["ctr"].astype(np.uint32).view(np.int32))
+    key = torch.from_numpy(data["key"].astype(np.uint32).view(np.int32))
+    ctr = ctr.view(torch.uint32); key = key.view(torch.uint32)
+    out = torch.zeros_like(ctr)
+    kern[(1,)](ctr, key, out, N=ctr.shape[0] // 4)
+    np.save(sys.argv[2], out.view(torch.int32).numpy().view(np.uint32))
+""")
+
+
+def test_philox_matches_independent_implementation(tmp_path):
+    """Triton's philox (run on the CPU by its interpreter) is an independent
+    implementation of the same published generator."""
+    pytest.importorskip("triton")
+    rng = np.random.default_rng(1)
+    n = 256
+    ctr = rng.integers(0, 2**32, size=(n, 4), dtype=np.uint64)
+    key = rng.integers(0, 2**32, size=(n, 2), dtype=np.uint64)
+    ctr[0] = 0
+    key[0] = 0
+    ctr[1] = 2**32 - 1
+    key[1] = 2**32 - 1
+    inp = tmp_path / "in.npz"
+    outp = tmp_path / "out.npy"
+    np.savez(inp, ctr=ctr.reshape(-1), key=key.reshape(-1))
+    script = tmp_path / "tphilox.py"
+    script.write_text(_TRITON_PHILOX)
+    env = dict(os.environ, TRITON_INTERPRET="1")
+    r = subprocess.run([sys.executable, str(script), str(inp), str(outp)],
+                       env=env, capture_output=True, text=True, timeout=600)
+    if r.returncode != 0:
+        pytest.skip("triton interpreter unavailable: " + r.stderr[-300:])
+    ref = np.load(outp).reshape(n, 4)
+    got = philox.philox4x32_10(ctr, key)
+    assert np.array_equal(got, ref)
+
+
+def test_philox_vector_and_scalar_agree():
+    rng = np.random.default_rng(2)
+    ctr = rng.integers(0, 2**32, size=(64, 4), dtype=np.uint64)
+    key = rng.integers(0, 2**32, size=(64, 2), dtype=np.uint64)
+    vec = philox.philox4x32_10(ctr, key)
+    for i in range(64):
+        assert tuple(int(x) for x in vec[i]) == philox.philox_scalar(ctr[i],
+                                                                     key[i])
+
+
+def test_philox_uniforms_are_uniform():
+    u = philox.uniforms(12345, 7, np.arange(1_000_000), 3, 1)
+    assert u.min() >= 0.0 and u.max() < 1.0
+    assert np.all(u * 2**24 == np.floor(u * 2**24))
+    counts = np.histogram(u, bins=256, range=(0, 1))[0]
+    assert stats.chisquare(counts).pvalue > 1e-4
+    # distinct streams are distinct
+    u2 = philox.uniforms(12345, 8, np.arange(1000), 3, 1)
+    assert not np.array_equal(u[:1000], u2)
+
+
+# --------------------------------------------------------------------------
+# a1 conv
+# --------------------------------------------------------------------------
+def _h(B, K, H, seed=0):
+    return np.random.default_rng(seed).standard_normal((B, K, H))
+
+
+def test_conv_zero_weights_give_zero():
+    h = _h(2, 3, 8)
+    assert np.all(oracle.conv2tap(h, np.zeros((16, 8))) == 0.0)
+
+
+def test_conv_first_tap_only_is_elementwise_square():
+    h = _h(2, 4, 8)
+    a = 0.75
+    W = np.concatenate([a * np.eye(8), np.zeros((8, 8))])
+    np.testing.assert_allclose(oracle.conv2tap(h, W), a * h * h, rtol=1e-15)
+
+
+def test_conv_second_tap_reads_predecessor_with_causal_zero():
+    h = _h(3, 5, 6)
+    bcoef = -1.5
+    W = np.concatenate([np.zeros((6, 6)), bcoef * np.eye(6)])
+    y = oracle.conv2tap(h, W)
+    assert np.all(y[:, 0] == 0.0)                 # h_{-1} = 0
+    np.testing.assert_allclose(y[:, 1:], bcoef * h[:, 1:] * h[:, :-1],
+                               rtol=1e-15)
+
+
+def test_conv_weight_orientation():
+    """W0[c, k] multiplies h[k] into channel c (not the transpose)."""
+    H = 5
+    h = _h(1, 2, H)
+    W = np.zeros((2 * H, H))
+    W[1, 3] = 2.0          # w0[1] = 2 h[3]
+    W[H + 4, 0] = 1.0      # w1[4] = h[0]
+    y = oracle.conv2tap(h, W)
+    exp = np.zeros_like(h)
+    exp[0, :, 1] = 2.0 * h[0, :, 3] * h[0, :, 1]
+    exp[0, 1, 4] = h[0, 1, 0] * h[0, 0, 4]
+    np.testing.assert_allclose(y, exp, rtol=1e-15, atol=0)
+
+
+def test_conv_none_is_identity():
+    h = _h(1, 3, 4)
+    assert np.array_equal(oracle.conv2tap(h, None), h)
+
+
+# --------------------------------------------------------------------------
+# a2 LM head / logsumexp / top-16
+# --------------------------------------------------------------------------
+def test_lmhead_zero_weights():
+    V = 1000
+    topv, topi, lse = oracle.lmhead_topk(_h(1, 3, 8)[0], np.zeros((V, 8)))
+    np.testing.assert_allclose(lse, math.log(V), rtol=1e-15)
+    assert np.array_equal(topi, np.tile(np.arange(C), (3, 1)))
+    assert np.all(topv == 0.0)
+
+
+def test_lmhead_geometric_closed_form():
+    """U[v] = -delta * rank(v) for a permutation rank: the top-16 are the
+    tokens of rank 0..15 in order and lse is a geometric series."""
+    V, H, delta = 5000, 4, 0.37
+    rng = np.random.default_rng(3)
+    perm = rng.permutation(V)                     # perm[k] = token of rank k
+    rank = np.empty(V)
+    rank[perm] = np.arange(V)
+    W = np.zeros((V, H))
+    W[:, 2] = -delta * rank
+    y = np.zeros((2, H))
+    y[0, 2] = 1.0
+    y[1, 2] = 2.0                                 # doubles every logit
+    topv, topi, lse = oracle.lmhead_topk(y, W)
+    for row, s in ((0, 1.0), (1, 2.0)):
+        d = delta * s
+        assert np.array_equal(topi[row], perm[:C])
+        np.testing.assert_allclose(topv[row], -d * np.arange(C), rtol=1e-6)
+        closed = math.log((1 - math.exp(-V * d)) / (1 - math.exp(-d)))
+        np.testing.assert_allclose(lse[row], closed, rtol=1e-12)
+
+
+def test_lmhead_ties_go_to_lower_id_and_padding():
+    W = np.zeros((40, 2))
+    W[[5, 7, 30], 0] = 1.0                        # three equal maxima
+    topv, topi, _ = oracle.lmhead_topk(np.array([[1.0, 0.0]]), W)
+    assert list(topi[0, :3]) == [5, 7, 30]
+    assert list(topi[0, 3:6]) == [0, 1, 2]        # then the zeros by id
+    Ws = np.arange(5, dtype=float)[:, None]
+    topv, topi, lse = oracle.lmhead_topk(np.array([[1.0]]), Ws)
+    assert list(topi[0]) == [4, 3, 2, 1, 0] + [-1] * 11
+    assert np.all(np.isneginf(topv[0, 5:]))
+    np.testing.assert_allclose(lse[0], math.log(sum(math.exp(v)
+                                                    for v in range(5))))
+
+
+def test_lmhead_topk_matches_library_topk():
+    rng = np.random.default_rng(4)
+    y = rng.standard_normal((6, 32))
+    W = rng.standard_normal((3000, 32)) * 0.2
+    topv, topi, lse = oracle.lmhead_topk(y, W)
+    U = torch.from_numpy(y) @ torch.from_numpy(W).T
+    ref = torch.topk(U, C, dim=1)
+    for m in range(6):
+        assert set(topi[m].tolist()) == set(ref.indices[m].tolist())
+    np.testing.assert_allclose(lse, torch.logsumexp(U, 1).numpy(),
+                               rtol=1e-13)
+
+
+# --------------------------------------------------------------------------
+# a3 gate + pair score
+# --------------------------------------------------------------------------
+def test_gate_closed_forms():
+    h = np.array([[1.0, 2.0]])
+    assert np.all(oracle.gate(h, np.zeros((3, 2))) == 0.5)
+    w = np.array([[math.log(3.0), 0.0], [0.0, -math.log(3.0) / 2]])
+    np.testing.assert_allclose(oracle.gate(h, w), [[0.75, 0.25]],
+                               rtol=1e-15)
+
+
+def _lattice(B, K, V, seed=0, r=8):
+    rng = np.random.default_rng(seed)
+    topi = np.stack([np.stack([rng.choice(V, C, replace=False)
+                               for _ in range(K)]) for _ in range(B)])
+    topv = -np.sort(-rng.standard_normal((B, K, C)), axis=2)
+    anchor = rng.integers(0, V, B)
+    g = rng.random((B, K, r))
+    return topv.astype(np.float32), topi.astype(np.int32), anchor, g
+
+
+def test_pair_score_zero_embeddings_is_drafter_logit():
+    topv, topi, anchor, g = _lattice(2, 3, 100)
+    E = np.zeros((100, 8))
+    S = oracle.pair_score(topv, topi, anchor, g, E, E)
+    np.testing.assert_array_equal(S, np.broadcast_to(topv[:, :, None, :],
+                                                      S.shape))
+
+
+def test_pair_score_one_hot_embeddings_closed_form():
+    """E_in[v] = e_{v mod r}, E_out[v] = c e_{(v+1) mod r}: the bilinear
+    term is c * g[a mod r] when predecessor a = candidate b + 1 (mod r),
+    else 0.  Pins which table takes the predecessor (the tables are not
+    symmetric), the anchor at t=0, and the i/j orientation."""
+    V, r, cc = 64, 8, 0.5
+    topv, topi, anchor, g = _lattice(2, 3, V, seed=5, r=r)
+    Ein = np.zeros((V, r))
+    Ein[np.arange(V), np.arange(V) % r] = 1.0
+    Eout = np.zeros((V, r))
+    Eout[np.arange(V), (np.arange(V) + 1) % r] = cc
+    S = oracle.pair_score(topv, topi, anchor, g, Ein, Eout)
+    hits = 0
+    for b in range(2):
+        for t in range(3):
+            preds = [anchor[b]] * C if t == 0 else topi[b, t - 1]
+            for i in range(C):
+                for j in range(C):
+                    a, c = int(preds[i]), int(topi[b, t, j])
+                    match = a % r == (c + 1) % r
+                    hits += match
+                    exp = topv[b, t, j] + (cc * g[b, t, a % r]
+                                           if match else 0.0)
+                    assert abs(S[b, t, i, j] - exp) < 1e-12
+    assert hits > 50
+    # the tables are not interchangeable: scaling only E_in by 2 doubles
+    S2 = oracle.pair_score(topv, topi, anchor, g, 2 * Ein, Eout)
+    np.testing.assert_allclose(S2 - topv[:, :, None, :],
+                               2 * (S - topv[:, :, None, :]), atol=1e-12)
+
+
+def test_pair_score_padding_is_neg_inf():
+    topv, topi, anchor, g = _lattice(1, 2, 50, seed=6)
+    topi[0, 0, 10:] = -1
+    topv[0, 0, 10:] = -np.inf
+    E = np.random.default_rng(0).standard_normal((50, 8))
+    S = oracle.pair_score(topv, topi, anchor, g, E, E)
+    assert np.all(np.isneginf(S[0, 0, :, 10:]))   # invalid candidates
+    assert np.all(np.isneginf(S[0, 1, 10:, :]))   # invalid predecessors
+    assert np.all(np.isfinite(S[0, 1, :10, :]))
+
+
+# --------------------------------------------------------------------------
+# a4 walk
+# --------------------------------------------------------------------------
+def test_walk_zero_selector_is_independent_top1():
+    topv, topi, anchor, g = _lattice(3, 5, 200, seed=7)
+    E = np.zeros((200, 8))
+    S = oracle.pair_score(topv, topi, anchor, g, E, E).astype(np.float32)
+    slot, draft, q, _ = oracle.path_walk(S, topi, 0.0, None)
+    assert np.all(slot == 0)
+    assert np.array_equal(draft, topi[:, :, 0])
+    assert np.all(q[:, :, 0] == 1.0)
+
+
+def _all_paths(S, K):
+    """Enumerate every path (x_0..x_{K-1}) of the 16^K lattice."""
+    grids = np.meshgrid(*[np.arange(C)] * K, indexing="ij")
+    paths = np.stack([g.reshape(-1) for g in grids], 1)     # lexicographic
+    steps = [S[0, 0, paths[:, 0]]]                          # anchor row
+    for t in range(1, K):
+        steps.append(S[t, paths[:, t - 1], paths[:, t]])
+    return paths, np.stack(steps, 1)
+
+
+def test_walk_greedy_equals_brute_force_lexicographic_max():
+    rng = np.random.default_rng(8)
+    K = 3
+    for trial in range(20):
+        S = rng.standard_normal((1, K, C, C)).astype(np.float32)
+        S[0, 0] = S[0, 0, 0]                      # position 0: anchor rows
+        if trial % 4 == 0:                        # force ties
+            S = np.round(S * 2) / 2
+        topi = np.tile(np.arange(C, dtype=np.int32), (1, K, 1))
+        slot, _, _, _ = oracle.path_walk(S, topi, 0.0, None)
+        paths, steps = _all_paths(S[0], K)
+        # best successor with ties to the lowest slot, step by step, is the
+        # lexicographic maximum of (s_0, -x_0, s_1, -x_1, s_2, -x_2)
+        key = lambda i: tuple(v for t in range(K)
+                              for v in (float(steps[i, t]), -paths[i, t]))
+        best = max(range(len(paths)), key=key)
+        assert list(slot[0]) == list(paths[best])
+
+
+def test_walk_sampled_path_probabilities():
+    """Exact path probabilities by enumeration sum to one and match the
+    frequencies of the oracle's seeded walk (chi-square)."""
+    rng = np.random.default_rng(9)
+    K, T = 3, 0.8
+    S = (rng.standard_normal((K, C, C)) * 1.5).astype(np.float32)
+    S[0] = S[0, 0]
+    S[:, :, 4:] = -np.inf                         # 4 live candidates
+    paths, steps = _all_paths(S, K)
+    logp = np.zeros(len(paths))
+    for t in range(K):
+        prev = np.zeros(len(paths), int) if t == 0 else paths[:, t - 1]
+        rows = S[t, prev].astype(np.float64) / T
+        m = rows.max(1, keepdims=True)
+        lz = (m + np.log(np.exp(rows - m).sum(1, keepdims=True)))[:, 0]
+        logp += rows[np.arange(len(paths)), paths[:, t]] - lz
+    p = np.exp(logp)
+    np.testing.assert_allclose(p.sum(), 1.0, rtol=1e-12)
+    live = p > 0
+    N = 60000
+    Sb = np.broadcast_to(S, (N,) + S.shape)
+    topi = np.broadcast_to(np.arange(C, dtype=np.int32), (N, K, C))
+    u = philox.walk_uniforms(99, 0, N, K)
+    slot, _, q, _ = oracle.path_walk(Sb, topi, T, u)
+    code = slot[:, 0] * C * C + slot[:, 1] * C + slot[:, 2]
+    counts = np.bincount(code, minlength=C ** K)
+    assert counts[~live].sum() == 0
+    res = stats.chisquare(counts[live], p[live] * N)
+    assert res.pvalue > 1e-3
+    np.testing.assert_allclose(q.sum(-1), 1.0, rtol=1e-12)
+
+
+# --------------------------------------------------------------------------
+# a5/a6 verify
+# --------------------------------------------------------------------------
+def _cands(V, K, B=1):
+    """Candidates = all V tokens (V <= 16), padded with -1."""
+    topi = np.full((B, K, C), -1, np.int32)
+    topi[:, :, :V] = np.arange(V)
+    return topi
+
+
+def test_verify_greedy_is_target_argmax_prefix():
+    V, K = 50, 6
+    rng = np.random.default_rng(10)
+    L = rng.standard_normal((2, K + 1, V)).astype(np.float32)
+    am = L.argmax(-1)
+    draft = am[:, :K].copy()
+    draft[0, 3] = (am[0, 3] + 1) % V             # seq 0 mismatches at t=3
+    topi = np.zeros((2, K, C), np.int32)
+    topi[:, :, 0] = draft
+    q = np.zeros((2, K, C), np.float32)
+    q[:, :, 0] = 1.0
+    n, out, _ = oracle.verify(L, draft, topi, q, 0.0, None, None)
+    assert list(n) == [3, K]
+    assert list(out[0]) == list(am[0, :4]) + [-1] * (K - 3)
+    assert list(out[1]) == list(am[1, :K + 1])   # bonus = argmax of row K
+
+
+def test_verify_p_equals_q_accepts_everything():
+    V, K, B = 10, 4, 200
+    rng = np.random.default_rng(11)
+    qv = rng.dirichlet(np.ones(V), size=(B, K))
+    topi = _cands(V, K, B)
+    q = np.zeros((B, K, C), np.float32)
+    q[:, :, :V] = qv
+    L = np.zeros((B, K + 1, V), np.float32)
+    L[:, :K] = np.log(q[:, :, :V])               # target = draft dist.
+    L[:, K] = rng.standard_normal((B, V))
+    draft = np.array([[rng.choice(V, p=qv[b, t] / qv[b, t].sum())
+                       for t in range(K)] for b in range(B)], np.int32)
+    n, out, _ = oracle.verify(L, draft, topi, q, 1.0,
+                              philox.accept_uniforms(0, 0, B, K),
+                              philox.resample_uniforms(0, 0, B, K))
+    assert np.all(n == K)
+    assert np.array_equal(out[:, :K], draft)
+
+
+def test_verify_zero_target_mass_on_candidates_rejects_at_zero():
+    V, K, B = 8, 3, 4000
+    topi = np.zeros((B, K, C), np.int32) - 1
+    topi[:, :, :3] = [0, 1, 2]                   # candidates 0..2
+    q = np.zeros((B, K, C), np.float32)
+    q[:, :, :3] = [0.5, 0.3, 0.2]
+    L = np.zeros((B, K + 1, V), np.float32)
+    L[:, 0, :3] = -np.inf                        # target never emits 0..2
+    L[:, 0, 3:] = np.log(np.arange(1, 6))        # p0 ~ 1..5 on tokens 3..7
+    draft = np.zeros((B, K), np.int32)
+    n, out, _ = oracle.verify(L, draft, topi, q, 1.0,
+                              philox.accept_uniforms(1, 0, B, K),
+                              philox.resample_uniforms(1, 0, B, K))
+    assert np.all(n == 0)
+    counts = np.bincount(out[:, 0], minlength=V)
+    assert counts[:3].sum() == 0
+    assert stats.chisquare(counts[3:], np.arange(1, 6) / 15 * B).pvalue > 1e-3
+
+
+def _sampled_drafts(q0, B, seed):
+    """Draft tokens drawn from q0 by the oracle's own walk."""
+    V = len(q0)
+    S = np.full((B, 1, C, C), -np.inf, np.float32)
+    S[:, 0, :, :V] = np.log(q0)
+    topi = _cands(V, 1, B)
+    slot, draft, q, _ = oracle.path_walk(S, topi, 1.0,
+                                         philox.walk_uniforms(seed, 0, B, 1))
+    return draft, q.astype(np.float32), topi
+
+
+def test_verify_accept_rate_is_sum_min_p_q():
+    """K = 1: P(accept) = E[n] = sum_v min(p(v), q(v))  (binomial, 4 sigma)."""
+    V, B = 8, 40000
+    rng = np.random.default_rng(12)
+    q0 = rng.dirichlet(np.ones(V))
+    p0 = rng.dirichlet(np.ones(V))
+    draft, q, topi = _sampled_drafts(q0, B, seed=5)
+    L = np.zeros((B, 2, V), np.float32)
+    L[:, 0] = np.log(p0)
+    n, out, _ = oracle.verify(L, draft, topi, q, 1.0,
+                              philox.accept_uniforms(6, 0, B, 1),
+                              philox.resample_uniforms(6, 0, B, 1))
+    pa = np.minimum(p0, q0).sum()
+    sd = math.sqrt(pa * (1 - pa) / B)
+    assert abs(n.mean() - pa) < 4 * sd
+
+
+def test_verify_is_lossless_chi_square():
+    """The emitted first token follows the target's p0 whatever q is, and
+    the second token, given the first draft was accepted, follows p1.  At
+    T = 0.7 the target distribution is softmax(L / T)."""
+    V, B, K, T = 8, 40000, 2, 0.7
+    rng = np.random.default_rng(13)
+    q0 = rng.dirichlet(np.ones(V) * 0.7)
+    p0 = rng.dirichlet(np.ones(V) * 0.7)
+    p1 = rng.dirichlet(np.ones(V))
+    d0, qa, topi0 = _sampled_drafts(q0, B, seed=7)
+    d1, qb, _ = _sampled_drafts(q0[::-1].copy(), B, seed=8)
+    draft = np.concatenate([d0, d1], 1)
+    q = np.concatenate([qa, qb], 1)
+    topi = np.concatenate([topi0, topi0], 1)
+    L = np.zeros((B, K + 1, V), np.float32)
+    L[:, 0] = T * np.log(p0)
+    L[:, 1] = T * np.log(p1)
+    L[:, 2] = 0.0
+    n, out, _ = oracle.verify(L, draft, topi, q, T,
+                              philox.accept_uniforms(9, 0, B, K),
+                              philox.resample_uniforms(9, 0, B, K))
+    c0 = np.bincount(out[:, 0], minlength=V)
+    assert stats.chisquare(c0, p0 * B).pvalue > 1e-3
+    sel = n >= 1
+    c1 = np.bincount(out[sel, 1], minlength=V)
+    assert stats.chisquare(c1, p1 * sel.sum()).pvalue > 1e-3
+
+
+def test_verify_output_layout():
+    V, K, B = 30, 5, 50
+    rng = np.random.default_rng(14)
+    L = rng.standard_normal((B, K + 1, V)).astype(np.float32) * 2
+    topi = np.stack([np.stack([rng.choice(V, C, replace=False)
+                               for _ in range(K)]) for _ in range(B)])
+    q = rng.dirichlet(np.ones(C), size=(B, K)).astype(np.float32)
+    slot = rng.integers(0, C, (B, K))
+    draft = np.take_along_axis(topi, slot[..., None], 2)[..., 0]
+    n, out, _ = oracle.verify(L, draft, topi.astype(np.int32), q, 0.8,
+                              philox.accept_uniforms(2, 3, B, K),
+                              philox.resample_uniforms(2, 3, B, K))
+    for b in range(B):
+        assert list(out[b, :n[b]]) == list(draft[b, :n[b]])
+        assert 0 <= out[b, n[b]] < V
+        assert np.all(out[b, n[b] + 1:] == -1)
+
+
+# --------------------------------------------------------------------------
+# whole cycle on the tiny workload
+# --------------------------------------------------------------------------
+def test_tiny_cycle_runs_and_is_consistent():
+    import synth
+    w = synth.get("tiny_conv")
+    x = synth.make_inputs(w)
+    f = lambda t: None if t is None else t.double().numpy()
+    h = f(x["h"])
+    y = oracle.to_storage(oracle.conv2tap(h, f(x["w_conv"])), w.dtype)
+    _, _, _, U = oracle.lmhead_topk(y.reshape(-1, w.H), f(x["w_lm"]),
+                                    want_logits=True)
+    L = synth.target_logits(w, U.reshape(w.B, w.K + 1, w.V)).numpy()
+    r = oracle.draft_verify_cycle(h[:, :w.K], f(x["w_conv"]), f(x["w_lm"]),
+                                  f(x["w_gate"]), f(x["e_in"]),
+                                  f(x["e_out"]), x["anchor"].numpy(), L,
+                                  w.T, w.seed, 0, w.dtype)
+    assert np.array_equal(r["draft"], np.take_along_axis(
+        r["topi"], r["slot"][..., None], 2)[..., 0])
+    n = int(r["n"][0])
+    assert list(r["out"][0, :n]) == list(r["draft"][0, :n])
+    # greedy: the emitted token after the accepted prefix is the argmax
+    assert r["out"][0, n] == int(np.argmax(L[0, n]))
