@@ -1,0 +1,490 @@
+"""Benchmark of one DFlash 2 draft-verify cycle on GB300.
+
+A step is one whole cycle for B sequences: conv + LM head + top-16 +
+logsumexp, pair scores, lattice walk, verify with residual / bonus draw —
+the four calls of the C ABI.  Default workload: B=32, K=8, V=151936,
+H=2048, r=256, bf16, T=1 (the b32k8 synthetic workload).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME]
+                    [--impl ours|reference]
+
+Prints one JSON line.  ``value`` = draft-verify cycles/s over all ranks
+(device-timed, inputs resident in HBM); ``e2e`` = the same through the
+public API with host buffers (H2D of the step's inputs and D2H of its
+results inside the timed region).  Under torchrun each rank runs its own
+batch (replicas, weak scaling) and rank 0 reports.  ``--impl reference``
+times the CPU oracle on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+C = 16
+METRIC = ("draft-verify cycles/s and verified tokens/s at B=32,K=8,V=151936;"
+          " % HBM/TC roofline")
+UNIT = "cycles/s"
+
+
+def parse(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default="b32k8")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=None)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0,
+                    help="bounded CPU work for the oracle baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args(argv)
+
+
+# --------------------------------------------------------------------------
+# distributed plumbing (replicas: no data-path collective)
+# --------------------------------------------------------------------------
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def rank_seed(base: int, rank: int) -> int:
+    """Philox seed of a rank: every replica draws its own uniforms."""
+    return base * 1000003 + rank
+
+
+def aggregate(cycles_per_rank: int, seconds_per_rank, world: int):
+    """Whole-job throughput: all ranks' cycles over the slowest rank."""
+    t = max(seconds_per_rank)
+    return world * cycles_per_rank / t, t
+
+
+def max_over_ranks(x: float, device=None) -> float:
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+# --------------------------------------------------------------------------
+# peaks and clocks
+# --------------------------------------------------------------------------
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0,
+            "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,"
+             "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+             "clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,"
+             "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.file = None
+
+    def __enter__(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv",
+                                                    delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index),
+                 f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=self.file, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or self.file is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [],
+                    "samples": 0}
+        self.file.flush()
+        with open(self.file.name) as f:
+            rows = [r.split(",") for r in f.read().strip().splitlines() if r]
+        os.unlink(self.file.name)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        for r in rows:
+            r = [x.strip() for x in r]
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------
+# workload synthesis (outside every timed region)
+# --------------------------------------------------------------------------
+def synth_target_torch(w, x, dev):
+    """Target logits of workload ``w``: its transform of the drafter's fp32
+    logits, which are computed here with plain torch ops on the device
+    (input synthesis only)."""
+    import torch
+    torch.backends.cuda.matmul.allow_tf32 = False
+    h = x["h"].to(dev).float()                       # [B, K+1, H]
+    H = w.H
+    if x["w_conv"] is not None:
+        wc = x["w_conv"].to(dev).float()
+        w0 = h @ wc[:H].T
+        w1 = h @ wc[H:].T
+        prev = torch.zeros_like(h)
+        prev[:, 1:] = h[:, :-1]
+        y = w0 * h + w1 * prev
+    else:
+        y = h
+    if w.dtype == "bf16":
+        y = y.to(torch.bfloat16)
+    y = y.float().reshape(-1, H)
+    wl = x["w_lm"].to(dev)
+    U = torch.empty(y.shape[0], w.V, dtype=torch.float32, device=dev)
+    step = 16384
+    for v0 in range(0, w.V, step):
+        U[:, v0:v0 + step] = y @ wl[v0:v0 + step].float().T
+    d = U.reshape(w.B, w.K + 1, w.V).cpu().numpy()
+    return synth.target_logits(w, d)
+
+
+# --------------------------------------------------------------------------
+# algorithmic bytes and flops per launch
+# --------------------------------------------------------------------------
+def lmhead_algorithmic(w):
+    """Bytes and flops of one LM-head launch (the step's dominant kernel):
+    read W_lm and y once, write topv/topi/lse."""
+    es = 2 if w.dtype == "bf16" else 4
+    M = w.M
+    by = w.V * w.H * es + M * w.H * es + M * (C * 8 + 4)
+    fl = 2.0 * M * w.V * w.H
+    return by, fl
+
+
+def verify_algorithmic(w, n_mean):
+    """Bytes the verify needs: target rows 0..n of each sequence, the draw
+    row once more, plus the small draft arrays."""
+    rows_needed = w.B * (n_mean + 1)
+    return rows_needed * w.V * 4 * (2 if w.T > 0 else 1) + w.M * C * 8
+
+
+# --------------------------------------------------------------------------
+# CPU oracle timing (bounded sample of the same workload)
+# --------------------------------------------------------------------------
+def time_oracle(w, x, L, seconds: float, seed: int):
+    """Whole cycles of the oracle on the first sequences of the workload,
+    one sequence at a time, until ``seconds`` of work; returns cycles/s
+    scaled to the full batch, and a description of the sample."""
+    import oracle
+    f64 = lambda t: None if t is None else t.float().numpy().astype(np.float64)
+    W = {k: f64(x[k]) for k in ("w_conv", "w_lm", "w_gate", "e_in", "e_out")}
+    h = f64(x["h"])[:, :w.K]
+    Lc = L.numpy() if hasattr(L, "numpy") else L
+    anchor = x["anchor"].numpy()
+    done, t0 = 0, time.perf_counter()
+    while True:
+        b = done % w.B
+        oracle.draft_verify_cycle(h[b:b + 1], W["w_conv"], W["w_lm"],
+                                  W["w_gate"], W["e_in"], W["e_out"],
+                                  anchor[b:b + 1], Lc[b:b + 1], w.T, seed, 0,
+                                  w.dtype)
+        done += 1
+        el = time.perf_counter() - t0
+        if el >= seconds or done >= w.B:
+            break
+    seq_per_s = done / el
+    return {"value": seq_per_s / w.B, "unit": UNIT,
+            "cores": os.cpu_count(), "kind": "oracle",
+            "sample": (f"{done} of {w.B} sequences of one cycle ({el:.1f} s, "
+                       f"float64 numpy; cycles/s = sequences/s / B)")}
+
+
+# --------------------------------------------------------------------------
+# the reference arm: the CPU oracle
+# --------------------------------------------------------------------------
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    w = synth.get(args.config)
+    x = synth.make_inputs(w)
+    import oracle
+    from oracle import dflash_oracle as _o  # noqa: F401
+    f64 = lambda t: None if t is None else t.float().numpy().astype(np.float64)
+    h_all = f64(x["h"])
+    y = oracle.to_storage(oracle.conv2tap(h_all, f64(x["w_conv"])), w.dtype)
+    # the target logits of the sampled sequences only
+    nseq = max(1, min(w.B, 2))
+    _, _, _, U = oracle.lmhead_topk(
+        y[:nseq].reshape(-1, w.H).astype(np.float64), f64(x["w_lm"]),
+        want_logits=True)
+    d = np.zeros((w.B, w.K + 1, w.V), np.float32)
+    d[:nseq] = U.reshape(nseq, w.K + 1, w.V)
+    L = synth.target_logits(w, d)
+    per = max(2.0, args.cpu_seconds / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        time_oracle(w, x, L, per, w.seed)
+    vals = [time_oracle(w, x, L, per, w.seed) for _ in range(args.steps)]
+    v = statistics.median(r["value"] for r in vals)
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 / v, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": w.name,
+                                            "recipe": synth.describe(w)},
+            "cpu_baseline": {"value": v, "unit": UNIT,
+                             "cores": vals[0]["cores"], "kind": "oracle",
+                             "sample": vals[0]["sample"]},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+# --------------------------------------------------------------------------
+# our arm
+# --------------------------------------------------------------------------
+def run_ours(args):
+    import torch
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    import block_drafter_verify_gb300 as dv_mod
+
+    w = synth.get(args.config)
+    x = synth.make_inputs(w)
+    L_cpu = synth_target_torch(w, x, dev)
+    weights = {k: (None if x[k] is None else x[k].to(dev).contiguous())
+               for k in ("w_conv", "w_lm", "w_gate", "e_in", "e_out")}
+    h = x["h"][:, :w.K].contiguous().to(dev)
+    anchor = x["anchor"].to(dev)
+    L = L_cpu.to(dev)
+    seed = rank_seed(w.seed, rank)
+    dv = dv_mod.DraftVerify(w.B, w.K, w.H, w.V, w.r, weights, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    # per-stage events, re-registered every timed step
+    stages = dv_mod.STAGES
+    K = args.steps
+
+    def mk():
+        e = torch.cuda.Event(enable_timing=True)
+        e.record(stream)
+        return e
+    ev = [[(mk(), mk()) for _ in stages] for _ in range(K)]
+    torch.cuda.synchronize(dev)
+
+    for i in range(args.warmup):
+        dv.cycle(h, anchor, L, w.T, seed, i)
+    torch.cuda.synchronize(dev)
+    dv_mod.dflash_check()
+
+    n_hist = []
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_stop = torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(dev.index or 0) as clk:
+        t_start.record(stream)
+        for i in range(K):
+            for si in range(len(stages)):
+                dv_mod.dflash_profile_stage(si, ev[i][si][0], ev[i][si][1])
+            dv.cycle(h, anchor, L, w.T, seed, args.warmup + i)
+        t_stop.record(stream)
+        torch.cuda.synchronize(dev)
+    for si in range(len(stages)):
+        dv_mod.dflash_profile_stage(si, None, None)
+    barrier()
+    dv_mod.dflash_check()
+    secs = t_start.elapsed_time(t_stop) / 1e3
+    secs_max = max_over_ranks(secs, dev)
+    value, _ = aggregate(K, [secs_max], world)
+    n_last = dv.n.cpu().numpy()
+    n_hist.append(float(n_last.mean()))
+
+    stage_us = {}
+    for si, name in enumerate(stages):
+        ts = []
+        for i in range(K):
+            b, e = ev[i][si]
+            try:
+                ts.append(b.elapsed_time(e) * 1e3)
+            except RuntimeError:
+                ts = []
+                break
+        if ts and (w.conv_sd is not None or name != "conv") and \
+                (w.T > 0 or name != "verify_draw"):
+            stage_us[name] = statistics.mean(ts)
+
+    # roofline of the dominant kernel (the LM head)
+    pk = peaks()
+    by, fl = lmhead_algorithmic(w)
+    t_lm = stage_us["lmhead"] * 1e-6
+    ridge = pk["bf16_tflops"] * 1e12 / (pk["hbm_gbs"] * 1e9)
+    hbm_bound = (fl / by) < ridge
+    traffic = None
+    tr_file = os.path.join(ROOT, "profiles", "lmhead_traffic.json")
+    if os.path.exists(tr_file):
+        with open(tr_file) as f:
+            tr = json.load(f)
+        if tr.get("workload") == w.name and tr.get("kernel_rev") == \
+                lmhead_kernel_rev():
+            traffic = tr.get("bytes_per_launch")
+    if hbm_bound:
+        achieved = by / t_lm / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"],
+                "unit": "GB/s", "frac": achieved / pk["hbm_gbs"],
+                "traffic": traffic, "peak_source": pk["source"],
+                "kernel": "lmhead",
+                "tensor_frac": fl / t_lm / 1e12 / pk["bf16_tflops"]}
+    else:
+        achieved = fl / t_lm / 1e12
+        roof = {"bound": "tensor", "achieved": achieved,
+                "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": achieved / pk["bf16_tflops"], "traffic": traffic,
+                "peak_source": pk["source"], "kernel": "lmhead",
+                "hbm_frac": by / t_lm / 1e9 / pk["hbm_gbs"]}
+
+    # end to end through the public API with host buffers
+    e2e_steps = args.e2e_steps or max(3, min(K, 20))
+    h_host = x["h"][:, :w.K].contiguous().pin_memory()
+    a_host = x["anchor"].pin_memory()
+    L_host = L_cpu.pin_memory()
+    n_host = torch.empty(w.B, dtype=torch.int32).pin_memory()
+    o_host = torch.empty(w.B, w.K + 1, dtype=torch.int32).pin_memory()
+    h_d, a_d, L_d = torch.empty_like(h), torch.empty_like(anchor), \
+        torch.empty_like(L)
+    barrier()
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(e2e_steps):
+        h_d.copy_(h_host, non_blocking=True)
+        a_d.copy_(a_host, non_blocking=True)
+        L_d.copy_(L_host, non_blocking=True)
+        n, out = dv.cycle(h_d, a_d, L_d, w.T, seed, 10**6 + i)
+        n_host.copy_(n, non_blocking=True)
+        o_host.copy_(out, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_secs = max_over_ranks(e0.elapsed_time(e1) / 1e3, dev)
+    e2e_value = world * e2e_steps / e2e_secs
+    h2d = h_host.numel() * h_host.element_size() + a_host.numel() * 4 + \
+        L_host.numel() * 4
+    d2h = n_host.numel() * 4 + o_host.numel() * 4
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = time_oracle(w, x, L_cpu, args.cpu_seconds, seed)
+
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank != 0:
+        return 0
+    n_mean = float(np.mean(n_hist))
+    launches_per_step = (3 if w.conv_sd is not None else 2) + 2 + \
+        (2 if w.T > 0 else 1)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": 1e3 * secs_max / K,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": w.dtype, "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "K": w.K, "V": w.V,
+                   "H": w.H, "r": w.r, "T": w.T, "parallelism":
+                   f"replicas x{world}",
+                   "l2": "inputs larger than L2 (W_lm streamed each cycle)",
+                   "recipe": synth.describe(w)},
+        "verified_tokens_per_s": value * w.B * (n_mean + 1),
+        "mean_accepted": n_mean,
+        "stage_us": stage_us,
+        "clocks": clk.summary(),
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * K,
+        "roofline": roof,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def lmhead_kernel_rev() -> str:
+    """Revision tag of the LM-head kernel source (hash of its file), so that
+    a stored ncu traffic figure is only used for the kernel it measured."""
+    import hashlib
+    p = os.path.join(ROOT, "block_drafter_verify_gb300", "csrc")
+    h = hashlib.sha1()
+    for name in sorted(os.listdir(p)):
+        if name.startswith("lmhead"):
+            with open(os.path.join(p, name), "rb") as f:
+                h.update(f.read())
+    return h.hexdigest()[:12]
+
+
+def main(argv=None):
+    args = parse(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

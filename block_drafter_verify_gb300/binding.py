@@ -1,0 +1,261 @@
+"""ctypes binding of libdflash: the C ABI of include/dflash.h under the same
+names, taking torch CUDA tensors.  Argument marshalling only — every step of
+the path runs in the library's CUDA kernels.  Importing works without a GPU;
+calling needs the built library and a CUDA device, and fails loudly if
+either is missing.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+BF16, FP32 = 0, 1
+C = 16
+STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported",
+          3: "CUDA runtime error", 4: "non-finite target logit",
+          5: "device wait timed out", 6: "token index out of range"}
+
+EXPORTS = ("dflash_workspace_bytes", "dflash_lmhead_topk", "dflash_pair_score",
+           "dflash_path_walk", "dflash_verify", "dflash_philox4x32",
+           "dflash_profile_stage", "dflash_check", "dflash_status_string")
+STAGES = ("conv", "lmhead", "merge", "pair_score", "walk", "verify_rows",
+          "verify_draw")
+
+
+class DFlashError(RuntimeError):
+    def __init__(self, fn, status):
+        self.status = int(status)
+        super().__init__(f"{fn}: {STATUS.get(self.status, self.status)}")
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(path: str | None = None):
+    """Load libdflash.so (built by ``build.build()``) and declare its ABI."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or _build.LIB
+    if not os.path.exists(p):
+        raise RuntimeError(
+            f"{p} is missing: build it with block_drafter_verify_gb300.build"
+            ".build() (or __graft_entry__.build()); there is no fallback")
+    L = ctypes.CDLL(p)
+    vp, i32, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    u64, sz, i64 = ctypes.c_uint64, ctypes.c_size_t, ctypes.c_int64
+    sig = {
+        "dflash_workspace_bytes": (sz, [i32, i32, i32, i32, i32]),
+        "dflash_lmhead_topk": (i32, [vp, vp, vp, i32, i32, i32, i32, i32, vp,
+                                     vp, vp, vp, sz, vp]),
+        "dflash_pair_score": (i32, [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32,
+                                    i32, i32, i32, vp, vp]),
+        "dflash_path_walk": (i32, [vp, vp, i32, i32, f32, u64, u64, vp, vp,
+                                   vp, vp]),
+        "dflash_verify": (i32, [vp, vp, vp, vp, i32, i32, i32, f32, u64, u64,
+                                vp, vp, vp, sz, vp]),
+        "dflash_philox4x32": (i32, [vp, u64, vp, i64, vp]),
+        "dflash_profile_stage": (i32, [i32, vp, vp]),
+        "dflash_check": (i32, [vp]),
+        "dflash_status_string": (ctypes.c_char_p, [i32]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(L, name)
+        fn.restype = res
+        fn.argtypes = args
+    if path is None:
+        _lib = L
+    return L
+
+
+# --------------------------------------------------------------------------
+# marshalling helpers
+# --------------------------------------------------------------------------
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _dtype(t):
+    if t.dtype == torch.bfloat16:
+        return BF16
+    if t.dtype == torch.float32:
+        return FP32
+    raise ValueError(f"unsupported storage dtype {t.dtype}")
+
+
+def _want(t, dtype, name):
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+
+
+def _call(name, *args):
+    st = getattr(load(), name)(*args)
+    if st != 0:
+        raise DFlashError(name, st)
+
+
+# --------------------------------------------------------------------------
+# the ABI, one function per entry point
+# --------------------------------------------------------------------------
+def dflash_workspace_bytes(which: int, B: int, K: int, H: int, V: int) -> int:
+    return int(load().dflash_workspace_bytes(which, B, K, H, V))
+
+
+def dflash_lmhead_topk(h, conv_w, w_lm, topv, topi, lse, ws, stream=None):
+    """h [B,K,H]; conv_w [2H,H] or None; w_lm [V,H] (same dtype);
+    topv [B*K,16] f32, topi [B*K,16] i32, lse [B*K] f32 outputs; ws uint8."""
+    B, K, H = h.shape
+    V = w_lm.shape[0]
+    dt = _dtype(h)
+    for t, n in ((w_lm, "w_lm"), (conv_w, "conv_w")):
+        if t is not None:
+            _want(t, h.dtype, n)
+    _want(topv, torch.float32, "topv")
+    _want(topi, torch.int32, "topi")
+    _want(lse, torch.float32, "lse")
+    _call("dflash_lmhead_topk", _ptr(h), _ptr(conv_w), _ptr(w_lm), B, K, H, V,
+          dt, _ptr(topv), _ptr(topi), _ptr(lse), _ptr(ws), ws.numel(),
+          _stream(stream))
+
+
+def dflash_pair_score(topv, topi, anchor, h, w_gate, e_in, e_out, scores,
+                      stream=None):
+    """topv/topi [B,K,16]; anchor [B] i32; h [B,K,H]; w_gate [r,H];
+    e_in/e_out [V,r]; scores [B,K,16,16] f32 output."""
+    B, K, H = h.shape
+    V, r = e_in.shape
+    _want(anchor, torch.int32, "anchor")
+    _want(scores, torch.float32, "scores")
+    _call("dflash_pair_score", _ptr(topv), _ptr(topi), _ptr(anchor), _ptr(h),
+          _ptr(w_gate), _ptr(e_in), _ptr(e_out), B, K, H, V, r, _dtype(h),
+          _ptr(scores), _stream(stream))
+
+
+def dflash_path_walk(scores, topi, T, seed, cycle, slot, draft, q,
+                     stream=None):
+    """scores [B,K,16,16]; topi [B,K,16]; slot/draft [B,K] i32 and
+    q [B,K,16] f32 outputs."""
+    B, K = scores.shape[:2]
+    _call("dflash_path_walk", _ptr(scores), _ptr(topi), B, K, float(T),
+          int(seed) & (2**64 - 1), int(cycle) & (2**64 - 1), _ptr(slot),
+          _ptr(draft), _ptr(q), _stream(stream))
+
+
+def dflash_verify(target_logits, draft, topi, q, T, seed, cycle, n_accepted,
+                  out_tok, ws, stream=None):
+    """target_logits [B,K+1,V] f32; draft [B,K]; topi/q [B,K,16];
+    n_accepted [B] and out_tok [B,K+1] i32 outputs; ws uint8."""
+    B, K1, V = target_logits.shape
+    _want(target_logits, torch.float32, "target_logits")
+    _call("dflash_verify", _ptr(target_logits), _ptr(draft), _ptr(topi),
+          _ptr(q), B, K1 - 1, V, float(T), int(seed) & (2**64 - 1),
+          int(cycle) & (2**64 - 1), _ptr(n_accepted), _ptr(out_tok),
+          _ptr(ws), ws.numel(), _stream(stream))
+
+
+def dflash_philox4x32(ctr, seed, out, stream=None):
+    """ctr [n,4] and out [n,4] int32 tensors holding uint32 words."""
+    _call("dflash_philox4x32", _ptr(ctr), int(seed) & (2**64 - 1), _ptr(out),
+          ctr.shape[0], _stream(stream))
+
+
+def dflash_profile_stage(stage, begin=None, end=None):
+    """Record torch.cuda.Event ``begin``/``end`` around the kernel of
+    ``stage`` (index or name in STAGES) on every later call; None stops.
+    The events must already exist on the device (record them once)."""
+    if isinstance(stage, str):
+        stage = STAGES.index(stage)
+    b = None if begin is None else ctypes.c_void_p(begin.cuda_event)
+    e = None if end is None else ctypes.c_void_p(end.cuda_event)
+    _call("dflash_profile_stage", int(stage), b, e)
+
+
+def dflash_check(stream=None):
+    """Synchronise and raise if a kernel flagged a problem."""
+    _call("dflash_check", _stream(stream))
+
+
+# --------------------------------------------------------------------------
+# one cycle with its buffers (still marshalling: four ABI calls)
+# --------------------------------------------------------------------------
+class DraftVerify:
+    """Device buffers for one workload shape plus the four calls of a cycle.
+
+    weights: dict with w_conv (or None), w_lm, w_gate, e_in, e_out as CUDA
+    tensors of one storage dtype.  ``cycle(h, anchor, L, T, seed, c)`` runs
+    conv + LM head + top-16, pair scores, walk and verify on the current
+    stream and returns the (device) n_accepted and out_tok tensors.
+    """
+
+    def __init__(self, B, K, H, V, r, weights, device="cuda"):
+        self.B, self.K, self.H, self.V, self.r = B, K, H, V, r
+        self.w = weights
+        dev = torch.device(device)
+        M = B * K
+        f32, i32 = torch.float32, torch.int32
+        self.topv = torch.empty(M, C, dtype=f32, device=dev)
+        self.topi = torch.empty(M, C, dtype=i32, device=dev)
+        self.lse = torch.empty(M, dtype=f32, device=dev)
+        self.scores = torch.empty(B, K, C, C, dtype=f32, device=dev)
+        self.slot = torch.empty(B, K, dtype=i32, device=dev)
+        self.draft = torch.empty(B, K, dtype=i32, device=dev)
+        self.q = torch.empty(B, K, C, dtype=f32, device=dev)
+        self.n = torch.empty(B, dtype=i32, device=dev)
+        self.out = torch.empty(B, K + 1, dtype=i32, device=dev)
+        self.ws_lm = torch.empty(dflash_workspace_bytes(0, B, K, H, V),
+                                 dtype=torch.uint8, device=dev)
+        self.ws_v = torch.empty(dflash_workspace_bytes(1, B, K, H, V),
+                                dtype=torch.uint8, device=dev)
+
+    def lmhead(self, h, stream=None):
+        dflash_lmhead_topk(h, self.w["w_conv"], self.w["w_lm"], self.topv,
+                           self.topi, self.lse, self.ws_lm, stream)
+
+    def pair_score(self, h, anchor, stream=None):
+        B, K = self.B, self.K
+        dflash_pair_score(self.topv.view(B, K, C), self.topi.view(B, K, C),
+                          anchor, h, self.w["w_gate"], self.w["e_in"],
+                          self.w["e_out"], self.scores, stream)
+
+    def walk(self, T, seed, cycle, stream=None):
+        dflash_path_walk(self.scores, self.topi.view(self.B, self.K, C), T,
+                         seed, cycle, self.slot, self.draft, self.q, stream)
+
+    def verify(self, L, T, seed, cycle, stream=None):
+        dflash_verify(L, self.draft, self.topi.view(self.B, self.K, C),
+                      self.q, T, seed, cycle, self.n, self.out, self.ws_v,
+                      stream)
+
+    def cycle(self, h, anchor, L, T, seed, cycle, stream=None):
+        self.lmhead(h, stream)
+        self.pair_score(h, anchor, stream)
+        self.walk(T, seed, cycle, stream)
+        self.verify(L, T, seed, cycle, stream)
+        return self.n, self.out
+
+    def y(self):
+        """y written by the last lmhead call (conv output, storage dtype)."""
+        dt = self.w["w_lm"].dtype
+        n = self.B * self.K * self.H
+        return self.ws_lm[: n * (2 if dt == torch.bfloat16 else 4)].view(
+            dt).view(self.B, self.K, self.H)

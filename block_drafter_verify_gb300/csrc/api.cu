@@ -1,0 +1,312 @@
+// The C ABI declared in include/dflash.h: host-side argument checks,
+// workspace carving and kernel launches.  Nothing here allocates memory.
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "kernels.h"
+
+using namespace dflash;
+
+namespace {
+
+__device__ int g_err_word;  // sticky device error bits (kErr*)
+
+struct DeviceState {
+  bool ready = false;
+  int sms = 0;
+  int* err = nullptr;
+};
+constexpr int kMaxDevices = 64;
+DeviceState g_dev[kMaxDevices];
+std::mutex g_mu;
+
+dflash_status device_state(DeviceState** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return DFLASH_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return DFLASH_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState& d = g_dev[dev];
+  if (!d.ready) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return DFLASH_ERR_CUDA;
+    if (major != 10 || minor != 3) return DFLASH_ERR_UNSUPPORTED;  // sm_103a only
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_err_word) != cudaSuccess) return DFLASH_ERR_CUDA;
+    d.err = static_cast<int*>(p);
+    d.ready = true;
+  }
+  *out = &d;
+  return DFLASH_OK;
+}
+
+// Caller-supplied timing events per stage (dflash_profile_stage).
+enum Stage { kStConv = 0, kStLmhead, kStMerge, kStPair, kStWalk, kStVerifyRows,
+             kStVerifyDraw, kNumStages };
+cudaEvent_t g_prof[kNumStages][2] = {};
+
+struct StageTimer {
+  int st;
+  cudaStream_t s;
+  StageTimer(int stage, cudaStream_t stream) : st(stage), s(stream) {
+    if (g_prof[st][0]) cudaEventRecord(g_prof[st][0], s);
+  }
+  ~StageTimer() {
+    if (g_prof[st][1]) cudaEventRecord(g_prof[st][1], s);
+  }
+};
+
+inline bool aligned(const void* p, uintptr_t a) {
+  return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0;
+}
+inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+#define REQUIRE(cond)                                   \
+  do {                                                  \
+    if (!(cond)) return DFLASH_ERR_INVALID_ARG;         \
+  } while (0)
+
+inline dflash_status cuda_status(cudaError_t e) {
+  return e == cudaSuccess ? DFLASH_OK : DFLASH_ERR_CUDA;
+}
+
+bool sizes_ok(int B, int K, int H, int V) {
+  if (B < 1 || K < 1 || K > DFLASH_MAX_K || V < 1 || H < 0) return false;
+  const long long M = (long long)B * K;
+  return M <= (1 << 20) && (long long)V <= (1LL << 30) &&
+         M * (long long)(H > 0 ? H : 1) <= (1LL << 40);
+}
+
+// Workspace of dflash_lmhead_topk: y (room for fp32), then the per-strip
+// top-16 partials of every row.
+size_t lmhead_ws_layout(int B, int K, int H, int V, void* base, void** y,
+                        TopkPartials* P) {
+  (void)V;
+  const size_t M = (size_t)B * K;
+  char* p = static_cast<char*>(base);
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    off = align256(off);
+    char* r = p ? p + off : nullptr;
+    off += bytes;
+    return r;
+  };
+  void* yy = take(M * H * sizeof(float));
+  TopkPartials pp;
+  pp.v = reinterpret_cast<float*>(take((size_t)kMaxStrips * M * kC * sizeof(float)));
+  pp.i = reinterpret_cast<int*>(take((size_t)kMaxStrips * M * kC * sizeof(int)));
+  pp.m = reinterpret_cast<float*>(take((size_t)kMaxStrips * M * sizeof(float)));
+  pp.s = reinterpret_cast<float*>(take((size_t)kMaxStrips * M * sizeof(float)));
+  if (y) *y = yy;
+  if (P) *P = pp;
+  return align256(off);
+}
+
+template <typename T>
+dflash_status lmhead_impl(const T* h, const T* conv_w, const T* w_lm, int B,
+                          int K, int H, int V, float* topv, int* topi,
+                          float* lse, void* ws, const DeviceState& d,
+                          cudaStream_t s) {
+  void* yv = nullptr;
+  TopkPartials P;
+  lmhead_ws_layout(B, K, H, V, ws, &yv, &P);
+  const int M = B * K;
+  const T* a = h;
+  cudaError_t e;
+  if (conv_w) {
+    T* y = static_cast<T*>(yv);
+    {
+      StageTimer tm(kStConv, s);
+      e = launch_conv_simt<T>(h, conv_w, B, K, H, y, s);
+    }
+    if (e != cudaSuccess) return DFLASH_ERR_CUDA;
+    a = y;
+  }
+  const int ns = lmhead_simt_strips(M, V, d.sms);
+  {
+    StageTimer tm(kStLmhead, s);
+    e = launch_lmhead_simt<T>(a, w_lm, M, H, V, ns, P, s);
+  }
+  if (e != cudaSuccess) return DFLASH_ERR_CUDA;
+  StageTimer tm(kStMerge, s);
+  return cuda_status(launch_topk_merge(P, ns, M, topv, topi, lse, s));
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t dflash_workspace_bytes(int which, int B, int K, int H, int V) {
+  if (!sizes_ok(B, K, which == 0 ? H : 0, V)) return 0;
+  if (which == 0) {
+    if (H < 8) return 0;
+    return lmhead_ws_layout(B, K, H, V, nullptr, nullptr, nullptr);
+  }
+  if (which == 1) return verify_ws_layout(B, K, V, nullptr, nullptr);
+  return 0;
+}
+
+dflash_status dflash_lmhead_topk(const void* h, const void* conv_w,
+                                 const void* w_lm, int B, int K, int H, int V,
+                                 dflash_dtype dt, float* topv, int32_t* topi,
+                                 float* lse, void* ws, size_t ws_bytes,
+                                 dflash_stream_t stream) {
+  REQUIRE(h && w_lm && topv && topi && lse && ws);
+  REQUIRE(sizes_ok(B, K, H, V) && H >= 8 && H % 8 == 0);
+  REQUIRE(dt == DFLASH_BF16 || dt == DFLASH_FP32);
+  REQUIRE(aligned(ws, 256) && aligned(h, 16) && aligned(w_lm, 16));
+  REQUIRE(!conv_w || aligned(conv_w, 16));
+  REQUIRE(ws_bytes >= lmhead_ws_layout(B, K, H, V, nullptr, nullptr, nullptr));
+  DeviceState* d = nullptr;
+  dflash_status st = device_state(&d);
+  if (st != DFLASH_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (dt == DFLASH_FP32)
+    return lmhead_impl<float>(static_cast<const float*>(h),
+                              static_cast<const float*>(conv_w),
+                              static_cast<const float*>(w_lm), B, K, H, V,
+                              topv, topi, lse, ws, *d, s);
+  return lmhead_impl<__nv_bfloat16>(
+      static_cast<const __nv_bfloat16*>(h),
+      static_cast<const __nv_bfloat16*>(conv_w),
+      static_cast<const __nv_bfloat16*>(w_lm), B, K, H, V, topv, topi, lse, ws,
+      *d, s);
+}
+
+dflash_status dflash_pair_score(const float* topv, const int32_t* topi,
+                                const int32_t* anchor, const void* h,
+                                const void* w_gate, const void* e_in,
+                                const void* e_out, int B, int K, int H, int V,
+                                int r, dflash_dtype dt, float* scores,
+                                dflash_stream_t stream) {
+  REQUIRE(topv && topi && anchor && h && w_gate && e_in && e_out && scores);
+  REQUIRE(sizes_ok(B, K, H, V) && H >= 1 && r >= 1 && r <= DFLASH_MAX_RANK);
+  REQUIRE(dt == DFLASH_BF16 || dt == DFLASH_FP32);
+  DeviceState* d = nullptr;
+  dflash_status st = device_state(&d);
+  if (st != DFLASH_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  StageTimer tm(kStPair, s);
+  if (dt == DFLASH_FP32)
+    e = launch_pair_score<float>(topv, topi, anchor,
+                                 static_cast<const float*>(h),
+                                 static_cast<const float*>(w_gate),
+                                 static_cast<const float*>(e_in),
+                                 static_cast<const float*>(e_out), B, K, H, V,
+                                 r, scores, d->err, s);
+  else
+    e = launch_pair_score<__nv_bfloat16>(
+        topv, topi, anchor, static_cast<const __nv_bfloat16*>(h),
+        static_cast<const __nv_bfloat16*>(w_gate),
+        static_cast<const __nv_bfloat16*>(e_in),
+        static_cast<const __nv_bfloat16*>(e_out), B, K, H, V, r, scores,
+        d->err, s);
+  return cuda_status(e);
+}
+
+dflash_status dflash_path_walk(const float* scores, const int32_t* topi,
+                               int B, int K, float T, uint64_t seed,
+                               uint64_t cycle, int32_t* slot, int32_t* draft,
+                               float* q, dflash_stream_t stream) {
+  REQUIRE(scores && topi && slot && draft && q);
+  REQUIRE(B >= 1 && K >= 1 && K <= DFLASH_MAX_K && B <= (1 << 20));
+  REQUIRE(T >= 0.f && T < INFINITY);
+  REQUIRE(aligned(scores, 16));
+  DeviceState* d = nullptr;
+  dflash_status st = device_state(&d);
+  if (st != DFLASH_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  StageTimer tm(kStWalk, s);
+  return cuda_status(launch_path_walk(scores, topi, B, K, T, seed, cycle,
+                                      slot, draft, q, d->err, s));
+}
+
+dflash_status dflash_verify(const float* target_logits, const int32_t* draft,
+                            const int32_t* topi, const float* q, int B, int K,
+                            int V, float T, uint64_t seed, uint64_t cycle,
+                            int32_t* n_accepted, int32_t* out_tok, void* ws,
+                            size_t ws_bytes, dflash_stream_t stream) {
+  REQUIRE(target_logits && draft && topi && q && n_accepted && out_tok && ws);
+  REQUIRE(sizes_ok(B, K, 0, V));
+  REQUIRE(T >= 0.f && T < INFINITY);
+  REQUIRE(aligned(ws, 256) && aligned(target_logits, 16));
+  REQUIRE(ws_bytes >= verify_ws_layout(B, K, V, nullptr, nullptr));
+  DeviceState* d = nullptr;
+  dflash_status st = device_state(&d);
+  if (st != DFLASH_OK) return st;
+  VerifyWs w;
+  verify_ws_layout(B, K, V, ws, &w);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(w.counters, 0, w.counter_bytes, s) != cudaSuccess)
+    return DFLASH_ERR_CUDA;
+  cudaError_t e;
+  {
+    StageTimer tm(kStVerifyRows, s);
+    e = launch_verify_rows(target_logits, draft, topi, q, B, K, V, T, seed,
+                           cycle, n_accepted, out_tok, w, d->sms, d->err, s);
+  }
+  if (e != cudaSuccess || T == 0.f) return cuda_status(e);
+  StageTimer tm(kStVerifyDraw, s);
+  return cuda_status(launch_verify_resample(target_logits, topi, q, B, K, V, T,
+                                            seed, cycle, out_tok, w, d->sms,
+                                            d->err, s));
+}
+
+dflash_status dflash_philox4x32(const uint32_t* ctr, uint64_t seed,
+                                uint32_t* out, int64_t n,
+                                dflash_stream_t stream) {
+  REQUIRE(n >= 0 && (n == 0 || (ctr && out)));
+  REQUIRE(aligned(ctr, 16) && aligned(out, 16));
+  DeviceState* d = nullptr;
+  dflash_status st = device_state(&d);
+  if (st != DFLASH_OK) return st;
+  return cuda_status(launch_philox(ctr, seed, out, n,
+                                   reinterpret_cast<cudaStream_t>(stream)));
+}
+
+dflash_status dflash_profile_stage(int stage, void* begin, void* end) {
+  REQUIRE(stage >= 0 && stage < kNumStages);
+  REQUIRE((begin == nullptr) == (end == nullptr));
+  g_prof[stage][0] = static_cast<cudaEvent_t>(begin);
+  g_prof[stage][1] = static_cast<cudaEvent_t>(end);
+  return DFLASH_OK;
+}
+
+dflash_status dflash_check(dflash_stream_t stream) {
+  DeviceState* d = nullptr;
+  dflash_status st = device_state(&d);
+  if (st != DFLASH_OK) return st;
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return DFLASH_ERR_CUDA;
+  int word = 0;
+  if (cudaMemcpy(&word, d->err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return DFLASH_ERR_CUDA;
+  if (word) {
+    const int zero = 0;
+    if (cudaMemcpy(d->err, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+      return DFLASH_ERR_CUDA;
+  }
+  if (word & kErrTimeout) return DFLASH_ERR_DEVICE_TIMEOUT;
+  if (word & kErrNonfinite) return DFLASH_ERR_NONFINITE;
+  if (word & kErrBadIndex) return DFLASH_ERR_BAD_INDEX;
+  return DFLASH_OK;
+}
+
+const char* dflash_status_string(dflash_status st) {
+  switch (st) {
+    case DFLASH_OK: return "ok";
+    case DFLASH_ERR_INVALID_ARG: return "invalid argument";
+    case DFLASH_ERR_UNSUPPORTED: return "unsupported";
+    case DFLASH_ERR_CUDA: return "CUDA runtime error";
+    case DFLASH_ERR_NONFINITE: return "non-finite target logit";
+    case DFLASH_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+    case DFLASH_ERR_BAD_INDEX: return "token index out of range";
+  }
+  return "unknown status";
+}
+
+}  // extern "C"

@@ -1,0 +1,68 @@
+// Host-side launchers of every kernel; the C ABI in api.cu calls these.
+// Each returns the cudaError_t of its launch(es).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace dflash {
+
+// conv.cu -----------------------------------------------------------------
+template <typename T>
+cudaError_t launch_conv_simt(const T* h, const T* w_conv, int B, int K, int H,
+                             T* y, cudaStream_t s);
+
+// lmhead_simt.cu ----------------------------------------------------------
+template <typename T>
+cudaError_t launch_lmhead_simt(const T* y, const T* w_lm, int M, int H, int V,
+                               int nstrip, TopkPartials P, cudaStream_t s);
+int lmhead_simt_strips(int M, int V, int num_sms);
+cudaError_t launch_topk_merge(TopkPartials P, int nstrip, int M, float* topv,
+                              int* topi, float* lse, cudaStream_t s);
+
+// pair_score.cu -----------------------------------------------------------
+template <typename T>
+cudaError_t launch_pair_score(const float* topv, const int* topi,
+                              const int* anchor, const T* h, const T* w_gate,
+                              const T* e_in, const T* e_out, int B, int K,
+                              int H, int V, int r, float* scores, int* err,
+                              cudaStream_t s);
+
+// walk.cu -----------------------------------------------------------------
+cudaError_t launch_path_walk(const float* scores, const int* topi, int B,
+                             int K, float T, uint64_t seed, uint64_t cycle,
+                             int* slot, int* draft, float* q, int* err,
+                             cudaStream_t s);
+
+// verify.cu ---------------------------------------------------------------
+struct VerifyWs {
+  float2* chunk_part;             // [rows][nchunk]
+  float* row_m;                   // [rows]
+  float* row_z;                   // [rows]
+  int* row_arg;                   // [rows]
+  int* n_row;                     // [B]
+  unsigned long long* res_part;   // [B][nchunk2][2]
+  unsigned* counters;             // rows + 2B counters, zeroed per call
+  size_t counter_bytes;
+};
+constexpr int kVerifyMaxChunks = 64;
+size_t verify_ws_layout(int B, int K, int V, void* base, VerifyWs* out);
+cudaError_t launch_verify_rows(const float* L, const int* draft,
+                               const int* topi, const float* q, int B, int K,
+                               int V, float T, uint64_t seed, uint64_t cycle,
+                               int* n_accepted, int* out_tok,
+                               const VerifyWs& ws, int num_sms, int* err,
+                               cudaStream_t s);
+cudaError_t launch_verify_resample(const float* L, const int* topi,
+                                   const float* q, int B, int K, int V,
+                                   float T, uint64_t seed, uint64_t cycle,
+                                   int* out_tok, const VerifyWs& ws,
+                                   int num_sms, int* err, cudaStream_t s);
+
+// philox --------------------------------------------------------------------
+cudaError_t launch_philox(const uint32_t* ctr, uint64_t seed, uint32_t* out,
+                          int64_t n, cudaStream_t s);
+
+}  // namespace dflash

@@ -1,0 +1,224 @@
+/*
+ * dflash.h — C ABI of the DFlash 2 draft-verify hot path on one GB300 GPU.
+ *
+ * One draft-verify cycle is four calls, in this order, on one stream:
+ *
+ *   dflash_lmhead_topk  two-tap conv + drafter LM head + logsumexp + top-16
+ *   dflash_pair_score   context gate + low-rank bilinear scores of the
+ *                       16 x 16 candidate pairs of adjacent positions
+ *   dflash_path_walk    greedy or sampled walk through the K x 16 lattice
+ *   dflash_verify       rejection-sampling verify, residual / bonus draw
+ *
+ * Sources (page title, section):
+ *   "DFlash 2: Block diffusion, wearing a drafter's coat" — "Sixteen
+ *     candidates per position", "A path selector", "Suffix-decay
+ *     convolution", "Lossless, with conditions I did not used to state".
+ *   "A 2B Drafter Made a 27B Model 3.4x Faster. Same Exact Output." —
+ *     "The two fixes", "Running it", "Caveats before you rebuild your
+ *     serving stack".
+ *   "DFlash 2: Keep Drafting Parallel" — "What Comes Next", "A Lightweight
+ *     Path Selector".
+ *
+ * Conventions shared by every call:
+ *   - Shapes: B sequences, K drafted positions per sequence (1..16), V
+ *     vocabulary, H drafter hidden size, r selector rank (1..256), C = 16
+ *     candidates per position.  M = B*K rows.  All arrays are row-major and
+ *     contiguous.
+ *   - Every pointer argument except `seed`-like scalars is DEVICE memory
+ *     owned by the caller (for example a torch CUDA tensor).  The library
+ *     allocates nothing on these paths; scratch comes from the caller's
+ *     workspace `ws` of at least dflash_workspace_bytes(...) bytes.
+ *   - Calls are asynchronous on stream `s` (NULL = legacy default stream).
+ *     Arguments are checked on the host before anything is launched; a bad
+ *     argument returns DFLASH_ERR_INVALID_ARG (or _UNSUPPORTED) and
+ *     launches nothing.
+ *   - Problems found on the device (an index out of range, a non-finite
+ *     target logit, a draft that is not among its candidates) set a sticky
+ *     device error word; kernels never trap.  dflash_check() synchronises
+ *     the stream, reads and clears that word and returns the matching
+ *     status.
+ *   - dtype (DFLASH_BF16 or DFLASH_FP32) is the storage type of the
+ *     drafter-side tensors (hidden states, weights, embeddings).  All
+ *     accumulation is fp32.  Scores, probabilities and target logits are
+ *     fp32 whatever dtype is.
+ *   - When V < 16 the candidate lists are padded with index -1 and value
+ *     -inf (q = 0).
+ *   - Randomness: uniforms are Philox4x32-10 (Salmon et al., SC'11) with
+ *     key (seed lo, seed hi) and counter (b, t, purpose, cycle mod 2^32);
+ *     purpose 0 = walk draw of position t, 1 = accept draw of position t,
+ *     2 = residual / bonus draw (t = K); u = (word0 >> 8) * 2^-24.  Give
+ *     each cycle a new `cycle` value.  T = 0 selects the greedy forms and
+ *     ignores seed and cycle.
+ */
+#ifndef DFLASH_H_
+#define DFLASH_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t / CUstream. */
+typedef struct CUstream_st* dflash_stream_t;
+
+typedef enum {
+  DFLASH_OK = 0,
+  DFLASH_ERR_INVALID_ARG = 1,    /* bad pointer, size, alignment or value */
+  DFLASH_ERR_UNSUPPORTED = 2,    /* valid request this build cannot run  */
+  DFLASH_ERR_CUDA = 3,           /* a CUDA runtime call failed           */
+  DFLASH_ERR_NONFINITE = 4,      /* device: NaN or +inf target logit     */
+  DFLASH_ERR_DEVICE_TIMEOUT = 5, /* device: a bounded wait ran out       */
+  DFLASH_ERR_BAD_INDEX = 6       /* device: token id outside [0, V), or a
+                                    draft not among its candidates        */
+} dflash_status;
+
+typedef enum { DFLASH_BF16 = 0, DFLASH_FP32 = 1 } dflash_dtype;
+
+#define DFLASH_CANDIDATES 16
+#define DFLASH_MAX_K 16
+#define DFLASH_MAX_RANK 256
+
+/* Workspace needed by dflash_lmhead_topk (which = 0) or dflash_verify
+ * (which = 1) for these sizes, in bytes; an upper bound over both dtypes.
+ * Returns 0 for invalid sizes. */
+size_t dflash_workspace_bytes(int which, int B, int K, int H, int V);
+
+/*
+ * Steps a1 + a2: two-tap dynamic depthwise conv, drafter LM head, online
+ * logsumexp and per-position top-16.
+ *
+ * "Suffix-decay convolution" (drafter's coat page) and "The two fixes"
+ * (2B-drafter page): each position is mixed with its predecessor,
+ *     w0_t = W0 h_t,  w1_t = W1 h_t,  y_t = w0_t * h_t + w1_t * h_{t-1},
+ * per channel, h_{-1} = 0 at the first block position of every sequence,
+ * y rounded to dtype.  "Sixteen candidates per position" and "A Lightweight
+ * Path Selector": U_t = y_t W_lm^T is the drafter's own logit; the call
+ * keeps its 16 largest entries and log(sum_v exp U_t(v)) without writing
+ * U_t to memory.
+ *
+ *   h      [B, K, H] dtype        drafter final hidden states
+ *   conv_w [2H, H]   dtype        rows 0..H-1 = W0, rows H..2H-1 = W1;
+ *                                 NULL skips the conv (y = h)
+ *   w_lm   [V, H]    dtype        LM head
+ *   topv   [B*K, 16] fp32  out    U_t of the candidates, descending
+ *   topi   [B*K, 16] int32 out    their token ids (ties: lower id first)
+ *   lse    [B*K]     fp32  out    logsumexp of U_t over the vocabulary
+ *   ws     >= dflash_workspace_bytes(0, B, K, H, V) bytes, 256-B aligned.
+ *          On return its first B*K*H elements (dtype) hold y when conv_w
+ *          is not NULL.
+ * Requirements: 1 <= K <= 16, B >= 1, H % 8 == 0, V >= 1; bf16 operand
+ * pointers 16-byte aligned.
+ */
+dflash_status dflash_lmhead_topk(const void* h, const void* conv_w,
+                                 const void* w_lm, int B, int K, int H,
+                                 int V, dflash_dtype dt, float* topv,
+                                 int32_t* topi, float* lse, void* ws,
+                                 size_t ws_bytes, dflash_stream_t s);
+
+/*
+ * Step a3: context gate and low-rank bilinear pair scores.
+ *
+ * "A Lightweight Path Selector" (Keep Drafting Parallel page) and "A path
+ * selector" (drafter's coat page): for predecessor a and current candidate
+ * b of adjacent positions,
+ *     S_t(a, b) = U_t(b) + < E_in(a), G(h_t) * E_out(b) >,
+ *     G(h_t) = sigmoid(W_g h_t)   (gate form: this library's reading),
+ * every pair scored at once, with no backbone or LM-head pass.  The
+ * predecessor of position 0 is the anchor (last verified) token, so all 16
+ * rows of S[b, 0] are equal.
+ *
+ *   topv, topi [B, K, 16]  from dflash_lmhead_topk
+ *   anchor     [B] int32   last verified token of each sequence
+ *   h          [B, K, H] dtype   (the same hidden states, pre-conv)
+ *   w_gate     [r, H] dtype;  e_in, e_out [V, r] dtype
+ *   scores     [B, K, 16, 16] fp32 out: scores[b,t,i,j] = S_t(pred_i,
+ *              cand_j); -inf where either index is -1.
+ * Requirements: 1 <= r <= 256, 1 <= K <= 16.
+ */
+dflash_status dflash_pair_score(const float* topv, const int32_t* topi,
+                                const int32_t* anchor, const void* h,
+                                const void* w_gate, const void* e_in,
+                                const void* e_out, int B, int K, int H, int V,
+                                int r, dflash_dtype dt, float* scores,
+                                dflash_stream_t s);
+
+/*
+ * Step a4: walk one path through the K x 16 candidate lattice.
+ *
+ * "A Lightweight Path Selector": starting from the verified token, greedy
+ * follows the best successor; sampling draws from the scores.  With
+ * prev = 0 (the anchor row) and for t = 0..K-1:
+ *   T == 0: j = argmax_j scores[b,t,prev,j] (lowest j on ties), q one-hot;
+ *   T >  0: w_j = exp((scores[b,t,prev,j] - max) / T), q = w / sum(w),
+ *           j = the smallest j with w_0 + .. + w_j > u * sum(w),
+ *           u = walk uniform (b, t);
+ *   prev = j.
+ *   slot  [B, K] int32 out   chosen candidate slot
+ *   draft [B, K] int32 out   topi[b, t, slot]
+ *   q     [B, K, 16] fp32 out the draft distribution the verifier needs
+ */
+dflash_status dflash_path_walk(const float* scores, const int32_t* topi,
+                               int B, int K, float T, uint64_t seed,
+                               uint64_t cycle, int32_t* slot, int32_t* draft,
+                               float* q, dflash_stream_t s);
+
+/*
+ * Steps a5 + a6: rejection-sampling verify with residual or bonus draw.
+ *
+ * "Lossless, with conditions I did not used to state" (drafter's coat
+ * page): accept a draft token x with probability min(1, p(x)/q(x)), and on
+ * the first rejection resample from normalize(max(0, p - q)); the emitted
+ * tokens then follow the target distribution exactly.  p_t =
+ * softmax(L[b,t] / T).  For t = 0..K-1 in order, draft t is accepted iff
+ * u_t * q_t(x) < p_t(x) (u_t = accept uniform (b, t)); n = the number
+ * accepted before the first rejection.  If n < K the token at n is drawn
+ * from max(0, p_n - q_n) (q_n zero off the candidates; p_n if that is all
+ * zero); if n = K a bonus token is drawn from p_K.  A draw takes the
+ * smallest token v whose running weight sum exceeds u * total (u =
+ * residual uniform (b, K)).  T == 0: accept iff the draft equals
+ * argmax L[b,t] (lowest id on ties) and emit argmax L[b,n].
+ *
+ *   target_logits [B, K+1, V] fp32   target model logits, rows 0..K
+ *   draft [B, K], topi [B, K, 16], q [B, K, 16]   from the walk
+ *   n_accepted [B] int32 out
+ *   out_tok [B, K+1] int32 out   draft[0..n-1], the drawn token, then -1
+ *   ws >= dflash_workspace_bytes(1, B, K, 0, V) bytes, 256-B aligned
+ * Requirements: target_logits 16-byte aligned; T >= 0.  A NaN or +inf
+ * target logit sets DFLASH_ERR_NONFINITE in the device error word.
+ */
+dflash_status dflash_verify(const float* target_logits, const int32_t* draft,
+                            const int32_t* topi, const float* q, int B, int K,
+                            int V, float T, uint64_t seed, uint64_t cycle,
+                            int32_t* n_accepted, int32_t* out_tok, void* ws,
+                            size_t ws_bytes, dflash_stream_t s);
+
+/* Philox4x32-10 of n counters (ctr [n, 4] uint32, device) under key
+ * (seed lo, seed hi) into out [n, 4] uint32 (device): the generator the
+ * walk and verify draw from, exposed so callers can reproduce draws. */
+dflash_status dflash_philox4x32(const uint32_t* ctr, uint64_t seed,
+                                uint32_t* out, int64_t n, dflash_stream_t s);
+
+/* Per-stage timing.  While set, the library records the caller's CUDA
+ * events `begin` and `end` (cudaEvent_t, created by the caller) on the
+ * call's stream right before and right after it launches the kernel of
+ * `stage`:
+ *   0 conv, 1 LM head with top-16 / logsumexp epilogue, 2 top-16 merge,
+ *   3 pair score, 4 walk, 5 verify row pass, 6 verify residual / bonus draw.
+ * Pass NULL for both to stop.  Process-wide host state; set it from the
+ * thread that makes the calls, not while other threads call the library.
+ * Returns DFLASH_ERR_INVALID_ARG for an unknown stage or a lone NULL. */
+dflash_status dflash_profile_stage(int stage, void* begin, void* end);
+
+/* Synchronise `s`, read and clear the device error word of the current
+ * device; DFLASH_OK if no kernel reported a problem since the last call. */
+dflash_status dflash_check(dflash_stream_t s);
+
+/* Static, human-readable name of a status. */
+const char* dflash_status_string(dflash_status st);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DFLASH_H_ */
