@@ -105,6 +105,45 @@ size_t lmhead_ws_layout(int B, int K, int H, int V, void* base, void** y,
   return align256(off);
 }
 
+// bf16 storage: conv and LM head on the tensor cores (tcgen05 + TMA).
+dflash_status lmhead_bf16(const __nv_bfloat16* h, const __nv_bfloat16* conv_w,
+                          const __nv_bfloat16* w_lm, int B, int K, int H,
+                          int V, float* topv, int* topi, float* lse, void* ws,
+                          const DeviceState& d, cudaStream_t s) {
+  void* yv = nullptr;
+  TopkPartials P;
+  lmhead_ws_layout(B, K, H, V, ws, &yv, &P);
+  const int M = B * K;
+  const __nv_bfloat16* a = h;
+  cudaError_t e;
+  if (conv_w) {
+    CUtensorMap mh, mw;
+    if (!make_tmap_bf16_2d(&mh, h, H, M, 64, 128) ||
+        !make_tmap_bf16_2d(&mw, conv_w, H, 2 * (uint64_t)H, 64, 32))
+      return DFLASH_ERR_CUDA;
+    __nv_bfloat16* y = static_cast<__nv_bfloat16*>(yv);
+    {
+      StageTimer tm(kStConv, s);
+      e = launch_conv_tc(mh, mw, h, B, K, H, y, d.err, s);
+    }
+    if (e != cudaSuccess) return DFLASH_ERR_CUDA;
+    a = y;
+  }
+  CUtensorMap my, mw;
+  if (!make_tmap_bf16_2d(&my, a, H, M, 64, 128) ||
+      !make_tmap_bf16_2d(&mw, w_lm, H, V, 64, 256))
+    return DFLASH_ERR_CUDA;
+  int strips = 0;
+  {
+    StageTimer tm(kStLmhead, s);
+    e = launch_lmhead_tc(my, mw, M, H, V, d.sms, P, d.err, &strips, s);
+  }
+  if (e != cudaSuccess) return DFLASH_ERR_CUDA;
+  StageTimer tm(kStMerge, s);
+  return cuda_status(launch_topk_merge(P, strips, M, topv, topi, lse, s));
+}
+
+// fp32 storage: exact fp32 products on the CUDA cores.
 template <typename T>
 dflash_status lmhead_impl(const T* h, const T* conv_w, const T* w_lm, int B,
                           int K, int H, int V, float* topv, int* topi,
@@ -169,11 +208,10 @@ dflash_status dflash_lmhead_topk(const void* h, const void* conv_w,
                               static_cast<const float*>(conv_w),
                               static_cast<const float*>(w_lm), B, K, H, V,
                               topv, topi, lse, ws, *d, s);
-  return lmhead_impl<__nv_bfloat16>(
-      static_cast<const __nv_bfloat16*>(h),
-      static_cast<const __nv_bfloat16*>(conv_w),
-      static_cast<const __nv_bfloat16*>(w_lm), B, K, H, V, topv, topi, lse, ws,
-      *d, s);
+  return lmhead_bf16(static_cast<const __nv_bfloat16*>(h),
+                     static_cast<const __nv_bfloat16*>(conv_w),
+                     static_cast<const __nv_bfloat16*>(w_lm), B, K, H, V, topv,
+                     topi, lse, ws, *d, s);
 }
 
 dflash_status dflash_pair_score(const float* topv, const int32_t* topi,

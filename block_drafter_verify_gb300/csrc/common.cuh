@@ -92,9 +92,10 @@ __device__ __forceinline__ float philox_uniform(uint64_t seed, uint32_t b,
   return (float)philox_u24(seed, b, t, purpose, cycle) * 0x1p-24f;
 }
 
-// Top-16 candidate partials written per (vocab strip, row) by the LM-head
-// kernels and folded by the merge kernel.  Layout [strip][row][16] and
-// [strip][row]; each list sorted by (value desc, id asc).
+// Top-16 candidate partials written per (row, vocab strip) by the LM-head
+// kernels and folded by the merge kernel.  Layout [row][strip][16] and
+// [row][strip]; each list sorted by (value desc, id asc), padded with
+// (-inf, -1).
 struct TopkPartials {
   float* v;
   int* i;

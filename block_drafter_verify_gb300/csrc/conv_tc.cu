@@ -1,0 +1,201 @@
+// Step a1 on the 5th-generation tensor cores: the two-tap dynamic depthwise
+// convolution for bf16 storage, fused into the GEMM that computes its taps.
+//
+// "Suffix-decay convolution" (DFlash 2: Block diffusion, wearing a drafter's
+// coat): each position is mixed with its predecessor through per-channel
+// taps computed from the position, y_t = (W0 h_t) * h_t + (W1 h_t) * h_{t-1}
+// with h_{-1} = 0.
+//
+// One CTA per (128-row tile, 32-channel tile), 192 threads.  The B operand
+// of each stage stacks W0 rows [c0, c0+32) over W1 rows [c0, c0+32), so one
+// tcgen05.mma M=128 N=64 yields both taps of 32 channels (TMEM columns 0-31
+// = W0 h, 32-63 = W1 h).  The epilogue (warps 2-5, thread = row) reads both
+// halves, loads h_t and h_{t-1} for the 32 channels, applies the taps in
+// fp32 and writes y rounded to bf16 — the A operand of the LM head.
+#include "kernels.h"
+#include "tc_ptx.cuh"
+
+namespace dflash {
+namespace {
+
+constexpr int BM = 128, BC = 32, BK = 64, STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;        // 16 KB
+constexpr int B_BYTES = 2 * BC * BK * 2;    // 8 KB (W0 part, then W1 part)
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int THREADS = 192;
+constexpr uint32_t TMEM_COLS = 64;
+constexpr uint64_t WAIT_NS = 2000000000ull;
+
+struct Bars {
+  uint64_t full[STAGES];
+  uint64_t empty[STAGES];
+  uint64_t tfull;
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+};
+constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + sizeof(Bars);
+
+__device__ __forceinline__ bool wait_timeout(uint64_t* bar, uint32_t parity) {
+  int never = 0;
+  return tc::mbar_wait_bounded(bar, parity, &never, WAIT_NS);
+}
+
+__device__ __forceinline__ void bf16x8_to_f32(const uint4& u, float* f) {
+  const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 t = __bfloat1622float2(p[i]);
+    f[2 * i] = t.x;
+    f[2 * i + 1] = t.y;
+  }
+}
+
+__global__ void __launch_bounds__(THREADS)
+    conv_tc_kernel(const __grid_constant__ CUtensorMap map_h,
+                   const __grid_constant__ CUtensorMap map_wc,
+                   const __nv_bfloat16* __restrict__ h, int M, int K, int H,
+                   __nv_bfloat16* __restrict__ y, int* err) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sa = smem;
+  uint8_t* sb = smem + STAGES * A_BYTES;
+  Bars* bars = reinterpret_cast<Bars*>(smem + STAGES * STAGE_BYTES);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int c0 = blockIdx.x * BC, mtile = blockIdx.y;
+  const int kblocks = (H + BK - 1) / BK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      tc::mbar_init(&bars->full[s], 1);
+      tc::mbar_init(&bars->empty[s], 1);
+    }
+    tc::mbar_init(&bars->tfull, 1);
+    tc::mbar_init(&bars->drain, 1);
+    bars->abort = 0;
+    tc::fence_mbar_init();
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(&bars->tmem_base, TMEM_COLS);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = bars->tmem_base;
+  volatile int* abort = &bars->abort;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0, issued = 0, last_par = 0;
+      for (int kb = 0; kb < kblocks; ++kb) {
+        if (!tc::mbar_wait_bounded(&bars->empty[stage], phase ^ 1, abort,
+                                   WAIT_NS))
+          break;
+        tc::mbar_arrive_expect_tx(&bars->full[stage], STAGE_BYTES);
+        uint8_t* b = sb + stage * B_BYTES;
+        tc::tma_load_2d(sa + stage * A_BYTES, &map_h, &bars->full[stage],
+                        kb * BK, mtile * BM);
+        tc::tma_load_2d(b, &map_wc, &bars->full[stage], kb * BK, c0);
+        tc::tma_load_2d(b + BC * BK * 2, &map_wc, &bars->full[stage], kb * BK,
+                        H + c0);
+        issued |= 1u << stage;
+        last_par = (last_par & ~(1u << stage)) | (phase << stage);
+        if (++stage == STAGES) { stage = 0; phase ^= 1; }
+      }
+      for (int s = 0; s < STAGES; ++s)
+        if ((issued >> s) & 1) wait_timeout(&bars->full[s], (last_par >> s) & 1);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = tc::idesc_bf16_f32(BM, 2 * BC);
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int kb = 0; kb < kblocks; ++kb) {
+        if (!tc::mbar_wait_bounded(&bars->full[stage], phase, abort,
+                                   WAIT_NS)) {
+          ok = false;
+          break;
+        }
+        tc::fence_after_sync();
+        const uint32_t a0 = tc::smem_u32(sa + stage * A_BYTES);
+        const uint32_t b0 = tc::smem_u32(sb + stage * B_BYTES);
+#pragma unroll
+        for (int k = 0; k < BK / 16; ++k)
+          tc::mma_bf16(tmem, tc::sdesc_k_sw128(a0 + k * 32),
+                       tc::sdesc_k_sw128(b0 + k * 32), idesc, (kb | k) != 0);
+        tc::mma_commit(&bars->empty[stage]);
+        if (++stage == STAGES) { stage = 0; phase ^= 1; }
+      }
+      if (ok) tc::mma_commit(&bars->tfull);
+      tc::mma_commit(&bars->drain);
+      wait_timeout(&bars->drain, 0);
+    }
+  } else {
+    const int q = warp & 3;
+    const int m = mtile * BM + q * 32 + lane;
+    const bool got = tc::mbar_wait_bounded(&bars->tfull, 0, abort, WAIT_NS);
+    if (__all_sync(0xffffffffu, got)) {
+      tc::fence_after_sync();
+      const uint32_t tb = tmem + (static_cast<uint32_t>(q * 32) << 16);
+      float w0[32], w1[32];
+      tc::tmem_ld_x32(tb, w0);
+      tc::tmem_ld_x32(tb + BC, w1);
+      if (m < M) {
+        const bool has_prev = (m % K) != 0;
+        const __nv_bfloat16* hr = h + (size_t)m * H + c0;
+        __nv_bfloat16* yr = y + (size_t)m * H + c0;
+#pragma unroll
+        for (int g = 0; g < BC / 8; ++g) {
+          if (c0 + g * 8 >= H) break;
+          float hc[8], hp[8];
+          bf16x8_to_f32(*reinterpret_cast<const uint4*>(hr + g * 8), hc);
+          if (has_prev)
+            bf16x8_to_f32(*reinterpret_cast<const uint4*>(hr - H + g * 8), hp);
+          uint4 out;
+          __nv_bfloat162* o = reinterpret_cast<__nv_bfloat162*>(&out);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int j = g * 8 + 2 * i;
+            const float y0 = w0[j] * hc[2 * i] + (has_prev ? w1[j] * hp[2 * i] : 0.f);
+            const float y1 = w0[j + 1] * hc[2 * i + 1] +
+                             (has_prev ? w1[j + 1] * hp[2 * i + 1] : 0.f);
+            o[i] = __floats2bfloat162_rn(y0, y1);
+          }
+          *reinterpret_cast<uint4*>(yr + g * 8) = out;
+        }
+      }
+    } else {
+      *abort = 1;
+    }
+  }
+
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, TMEM_COLS);
+  }
+  if (threadIdx.x == 0 && bars->abort) raise_error(err, kErrTimeout);
+}
+
+}  // namespace
+
+cudaError_t launch_conv_tc(const CUtensorMap& map_h, const CUtensorMap& map_wc,
+                           const __nv_bfloat16* h, int B, int K, int H,
+                           __nv_bfloat16* y, int* err, cudaStream_t s) {
+  const int M = B * K;
+  cudaError_t e = cudaFuncSetAttribute(
+      conv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      (int)SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  const dim3 grid((H + BC - 1) / BC, (M + BM - 1) / BM);
+  conv_tc_kernel<<<grid, THREADS, SMEM_BYTES, s>>>(map_h, map_wc, h, M, K, H,
+                                                   y, err);
+  return cudaGetLastError();
+}
+
+}  // namespace dflash

@@ -2,6 +2,7 @@
 // Each returns the cudaError_t of its launch(es).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -13,6 +14,21 @@ namespace dflash {
 template <typename T>
 cudaError_t launch_conv_simt(const T* h, const T* w_conv, int B, int K, int H,
                              T* y, cudaStream_t s);
+
+// conv_tc.cu / lmhead_tc.cu: tensor-core (tcgen05) kernels for bf16 ------
+// TMA descriptor of a row-major bf16 [rows, inner] matrix, 128-byte swizzle.
+bool make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner,
+                       uint64_t rows, uint32_t box_inner, uint32_t box_rows);
+// map_h: h [B*K, H] box {64, 128}; map_wc: conv_w [2H, H] box {64, 32}.
+cudaError_t launch_conv_tc(const CUtensorMap& map_h, const CUtensorMap& map_wc,
+                           const __nv_bfloat16* h, int B, int K, int H,
+                           __nv_bfloat16* y, int* err, cudaStream_t s);
+// map_y: y [M, H] box {64, 128}; map_w: w_lm [V, H] box {64, 256}.
+// Writes `*strips` partial lists per row.
+cudaError_t launch_lmhead_tc(const CUtensorMap& map_y, const CUtensorMap& map_w,
+                             int M, int H, int V, int num_sms, TopkPartials P,
+                             int* err, int* strips, cudaStream_t s);
+int lmhead_tc_grid(int M, int V, int num_sms, int* row_tiles, int* strips);
 
 // lmhead_simt.cu ----------------------------------------------------------
 template <typename T>

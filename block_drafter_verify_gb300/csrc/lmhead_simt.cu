@@ -91,7 +91,7 @@ __global__ void __launch_bounds__(kThreads)
       list_insert(tv, ti, xv, xi, pos, lane);
     }
   }
-  const size_t pr = (size_t)strip * M + m;
+  const size_t pr = (size_t)m * gridDim.y + strip;
   if (lane < kC) {
     P.v[pr * kC + lane] = tv;
     P.i[pr * kC + lane] = ti;
@@ -102,54 +102,89 @@ __global__ void __launch_bounds__(kThreads)
   }
 }
 
-__global__ void __launch_bounds__(kThreads)
+// One warp per row.  The row's strip lists are staged in shared memory;
+// (max, sum) pairs are folded per lane in strip order and then across lanes
+// in a fixed tree; the top-16 is a 16-round tournament of the strips' list
+// heads (lane l owns strips l, l+32, ...), so the result does not depend on
+// timing.
+constexpr int kMergeWarps = 4;
+constexpr int kMaxOwned = (kMaxStrips + 31) / 32;
+
+__global__ void __launch_bounds__(kMergeWarps * 32)
     topk_merge_kernel(TopkPartials P, int nstrip, int M, float* topv,
                       int* topi, float* lse) {
-  const int m = blockIdx.x, tid = threadIdx.x, lane = tid & 31,
-            warp = tid >> 5;
-  __shared__ float s_v[kRowsPerCta][kC], s_m[kRowsPerCta], s_s[kRowsPerCta];
-  __shared__ int s_i[kRowsPerCta][kC];
-  float tv = -INFINITY;
-  int ti = -1;
-  float rm = -INFINITY, rs = 0.f;
-  for (int st = warp; st < nstrip; st += kRowsPerCta) {
-    const size_t pr = (size_t)st * M + m;
-    const float ev = lane < kC ? P.v[pr * kC + lane] : -INFINITY;
-    const int ei = lane < kC ? P.i[pr * kC + lane] : -1;
-    for (int k = 0; k < kC; ++k) {
-      const float xv = __shfl_sync(0xffffffffu, ev, k);
-      const int xi = __shfl_sync(0xffffffffu, ei, k);
-      if (!ranks_ahead(xv, xi, __shfl_sync(0xffffffffu, tv, 15),
-                       __shfl_sync(0xffffffffu, ti, 15)))
-        break;  // the strip's list is sorted: nothing further gets in
-      const int pos = __popc(__ballot_sync(
-          0xffffffffu, lane < kC && ranks_ahead(tv, ti, xv, xi)));
-      list_insert(tv, ti, xv, xi, pos, lane);
-    }
-    lse_combine(rm, rs, P.m[pr], P.s[pr], 1.f);
+  extern __shared__ float4 msm4[];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int m = blockIdx.x * kMergeWarps + warp;
+  if (m >= M) return;
+  float* sv = reinterpret_cast<float*>(msm4) + (size_t)warp * nstrip * kC;
+  int* si = reinterpret_cast<int*>(reinterpret_cast<float*>(msm4) +
+                                   (size_t)kMergeWarps * nstrip * kC) +
+            (size_t)warp * nstrip * kC;
+  const size_t base = (size_t)m * nstrip * kC;
+  const float4* gv = reinterpret_cast<const float4*>(P.v + base);
+  const int4* gi = reinterpret_cast<const int4*>(P.i + base);
+  for (int i = lane; i < nstrip * kC / 4; i += 32) {
+    reinterpret_cast<float4*>(sv)[i] = gv[i];
+    reinterpret_cast<int4*>(si)[i] = gi[i];
   }
-  if (lane < kC) { s_v[warp][lane] = tv; s_i[warp][lane] = ti; }
-  if (lane == 0) { s_m[warp] = rm; s_s[warp] = rs; }
-  __syncthreads();
-  if (warp != 0) return;
-  for (int w2 = 1; w2 < kRowsPerCta; ++w2) {
-    const float ev = lane < kC ? s_v[w2][lane] : -INFINITY;
-    const int ei = lane < kC ? s_i[w2][lane] : -1;
-    for (int k = 0; k < kC; ++k) {
-      const float xv = __shfl_sync(0xffffffffu, ev, k);
-      const int xi = __shfl_sync(0xffffffffu, ei, k);
-      if (!ranks_ahead(xv, xi, __shfl_sync(0xffffffffu, tv, 15),
-                       __shfl_sync(0xffffffffu, ti, 15)))
-        break;
-      const int pos = __popc(__ballot_sync(
-          0xffffffffu, lane < kC && ranks_ahead(tv, ti, xv, xi)));
-      list_insert(tv, ti, xv, xi, pos, lane);
+  // logsumexp: per-lane fold in strip order, then a fixed butterfly
+  float rm = -INFINITY, rs = 0.f;
+  for (int st = lane; st < nstrip; st += 32)
+    lse_combine(rm, rs, P.m[(size_t)m * nstrip + st],
+                P.s[(size_t)m * nstrip + st], 1.f);
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float om = __shfl_xor_sync(0xffffffffu, rm, o);
+    const float os = __shfl_xor_sync(0xffffffffu, rs, o);
+    if (lane & o) {  // the higher lane folds the lower lane's value first
+      float am = om, as = os;
+      lse_combine(am, as, rm, rs, 1.f);
+      rm = am; rs = as;
+    } else {
+      lse_combine(rm, rs, om, os, 1.f);
     }
-    lse_combine(rm, rs, s_m[w2], s_s[w2], 1.f);
+  }
+  __syncwarp();
+  // tournament over list heads
+  int head[kMaxOwned];
+#pragma unroll
+  for (int j = 0; j < kMaxOwned; ++j) head[j] = 0;
+  float outv = -INFINITY;
+  int outi = -1;
+  for (int r = 0; r < kC; ++r) {
+    float bv = -INFINITY;
+    int bi = -1, bj = -1;
+#pragma unroll
+    for (int j = 0; j < kMaxOwned; ++j) {
+      const int st = lane + 32 * j;
+      if (st < nstrip && head[j] < kC) {
+        const float v = sv[st * kC + head[j]];
+        const int id = si[st * kC + head[j]];
+        if (bj < 0 || ranks_ahead(v, id, bv, bi)) { bv = v; bi = id; bj = j; }
+      }
+    }
+    int bl = lane;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      const int ol = __shfl_xor_sync(0xffffffffu, bl, o);
+      const int oj = __shfl_xor_sync(0xffffffffu, bj, o);
+      const bool take = (oj >= 0) && (bj < 0 || ranks_ahead(ov, oi, bv, bi) ||
+                                      (ov == bv && oi == bi && ol < bl));
+      if (take) { bv = ov; bi = oi; bl = ol; bj = oj; }
+    }
+    if (lane == r) { outv = bv; outi = bi; }
+    if (lane == bl && bj >= 0) {
+#pragma unroll
+      for (int j = 0; j < kMaxOwned; ++j)
+        if (j == bj) ++head[j];
+    }
   }
   if (lane < kC) {
-    topv[(size_t)m * kC + lane] = tv;
-    topi[(size_t)m * kC + lane] = ti;
+    topv[(size_t)m * kC + lane] = outv;
+    topi[(size_t)m * kC + lane] = outi;
   }
   if (lane == 0) lse[m] = rm + logf(rs);
 }
@@ -181,7 +216,13 @@ cudaError_t launch_lmhead_simt(const T* y, const T* w_lm, int M, int H, int V,
 
 cudaError_t launch_topk_merge(TopkPartials P, int nstrip, int M, float* topv,
                               int* topi, float* lse, cudaStream_t s) {
-  topk_merge_kernel<<<M, kThreads, 0, s>>>(P, nstrip, M, topv, topi, lse);
+  const size_t smem = (size_t)kMergeWarps * nstrip * kC * 8;
+  cudaError_t e = cudaFuncSetAttribute(
+      topk_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      (int)smem);
+  if (e != cudaSuccess) return e;
+  topk_merge_kernel<<<(M + kMergeWarps - 1) / kMergeWarps, kMergeWarps * 32,
+                      smem, s>>>(P, nstrip, M, topv, topi, lse);
   return cudaGetLastError();
 }
 

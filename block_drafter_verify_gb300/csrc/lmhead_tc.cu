@@ -1,0 +1,303 @@
+// Step a2 on the 5th-generation tensor cores: drafter LM head
+// U = y W_lm^T (bf16 x bf16 -> fp32) with an epilogue that keeps, per row,
+// an online logsumexp and the 16 largest logits, so U never reaches HBM.
+//
+// "Sixteen candidates per position" (DFlash 2: Block diffusion, wearing a
+// drafter's coat) and "A Lightweight Path Selector" (DFlash 2: Keep Drafting
+// Parallel): U_t is the drafter's own logit; 16 candidates are kept per slot.
+//
+// Persistent kernel, one CTA per SM, 192 threads:
+//   warp 0      TMA producer: y tile [128 x 64] and W tile [256 x 64] per
+//               stage, 4 stages, 128-byte swizzle;
+//   warp 1      MMA issuer (one thread): tcgen05.mma M=128 N=256 K=16 into
+//               one of two TMEM accumulators (2 x 256 fp32 columns);
+//   warps 2-5   epilogue: thread = one row (TMEM lane), reads 32 columns at
+//               a time with tcgen05.ld, folds them into (max, sum exp) and a
+//               register-resident sorted top-16, while the MMA fills the
+//               other accumulator.
+// CTA c owns row tile (c mod row_tiles) and the vocab tiles strip, strip +
+// strips, ... (strip = c / row_tiles), so the CTAs that share a vocab tile
+// run it at the same time and W_lm is read from HBM about once.  Each CTA
+// writes one top-16 / (max, sum) partial per row; topk_merge folds them.
+// Every wait is time-bounded; on a timeout the CTA stops issuing, drains
+// its copies and MMAs, frees TMEM, flags the error word and exits.
+#include <algorithm>
+
+#include "kernels.h"
+#include "tc_ptx.cuh"
+
+namespace dflash {
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;  // 16 KB
+constexpr int B_BYTES = BN * BK * 2;  // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int THREADS = 192;
+constexpr uint32_t TMEM_COLS = 2 * BN;
+constexpr uint64_t WAIT_NS = 2000000000ull;  // 2 s: far beyond any real wait
+constexpr float LOG2E = 1.4426950408889634f;
+
+struct Bars {
+  uint64_t full[STAGES];
+  uint64_t empty[STAGES];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+};
+constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + sizeof(Bars);
+
+__device__ __forceinline__ bool wait_timeout(uint64_t* bar, uint32_t parity) {
+  int never = 0;
+  return tc::mbar_wait_bounded(bar, parity, &never, WAIT_NS);
+}
+
+// Insert xv (> tv[15], id larger than every held id) into the sorted list.
+__device__ __forceinline__ void topk_insert(float (&tv)[kC], int (&ti)[kC],
+                                            float xv, int xi) {
+#pragma unroll
+  for (int p = kC - 1; p >= 1; --p) {
+    const bool shift = xv > tv[p - 1];
+    const bool here = !shift && (xv > tv[p]);
+    tv[p] = shift ? tv[p - 1] : (here ? xv : tv[p]);
+    ti[p] = shift ? ti[p - 1] : (here ? xi : ti[p]);
+  }
+  if (xv > tv[0]) { tv[0] = xv; ti[0] = xi; }
+}
+
+// Fold 32 logits (columns col0..col0+31) of this thread's row.
+__device__ __forceinline__ void epilogue_chunk(float (&x)[32], int col0,
+                                               int V, float (&tv)[kC],
+                                               int (&ti)[kC], float& run_m,
+                                               float& run_s) {
+  if (col0 + 32 > V) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (col0 + i >= V) x[i] = -INFINITY;
+  }
+  float t16[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) t16[i] = fmaxf(x[i], x[i + 16]);
+#pragma unroll
+  for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+    for (int i = 0; i < w; ++i) t16[i] = fmaxf(t16[i], t16[i + w]);
+  const float cm = t16[0];
+  if (cm > run_m) {
+    run_s *= tc::ex2_approx((run_m - cm) * LOG2E);
+    run_m = cm;
+  }
+  const float nb = -run_m * LOG2E;
+  float s[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int i = 0; i < 32; ++i) s[i & 3] += tc::ex2_approx(fmaf(x[i], LOG2E, nb));
+  run_s += (s[0] + s[1]) + (s[2] + s[3]);
+  if (cm > tv[kC - 1]) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (x[i] > tv[kC - 1]) topk_insert(tv, ti, x[i], col0 + i);
+  }
+}
+
+__global__ void __launch_bounds__(THREADS, 1)
+    lmhead_tc_kernel(const __grid_constant__ CUtensorMap map_y,
+                     const __grid_constant__ CUtensorMap map_w, int M, int H,
+                     int V, int row_tiles, int strips, TopkPartials P,
+                     int* err) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sa = smem;
+  uint8_t* sb = smem + STAGES * A_BYTES;
+  Bars* bars = reinterpret_cast<Bars*>(smem + STAGES * STAGE_BYTES);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int mtile = blockIdx.x % row_tiles, strip = blockIdx.x / row_tiles;
+  const int vtiles = (V + BN - 1) / BN;
+  const int kblocks = (H + BK - 1) / BK;
+  const int my_tiles =
+      strip < vtiles ? (vtiles - strip + strips - 1) / strips : 0;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      tc::mbar_init(&bars->full[s], 1);
+      tc::mbar_init(&bars->empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      tc::mbar_init(&bars->tfull[b], 1);
+      tc::mbar_init(&bars->tempty[b], 4);
+    }
+    tc::mbar_init(&bars->drain, 1);
+    bars->abort = 0;
+    tc::fence_mbar_init();
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(&bars->tmem_base, TMEM_COLS);
+    tc::tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    tc::tma_prefetch_map(&map_y);
+    tc::tma_prefetch_map(&map_w);
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = bars->tmem_base;
+  volatile int* abort = &bars->abort;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0, issued = 0, last_par = 0;
+      bool ok = true;
+      for (int it = 0; it < my_tiles && ok; ++it) {
+        const int vt = strip + it * strips;
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!tc::mbar_wait_bounded(&bars->empty[stage], phase ^ 1, abort,
+                                     WAIT_NS)) {
+            ok = false;
+            break;
+          }
+          tc::mbar_arrive_expect_tx(&bars->full[stage], STAGE_BYTES);
+          tc::tma_load_2d(sa + stage * A_BYTES, &map_y, &bars->full[stage],
+                          kb * BK, mtile * BM);
+          tc::tma_load_2d(sb + stage * B_BYTES, &map_w, &bars->full[stage],
+                          kb * BK, vt * BN);
+          issued |= 1u << stage;
+          last_par = (last_par & ~(1u << stage)) | (phase << stage);
+          if (++stage == STAGES) { stage = 0; phase ^= 1; }
+        }
+      }
+      // leave no copy in flight
+      for (int s = 0; s < STAGES; ++s)
+        if ((issued >> s) & 1) wait_timeout(&bars->full[s], (last_par >> s) & 1);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA
+    if (lane == 0) {
+      constexpr uint32_t idesc = tc::idesc_bf16_f32(BM, BN);
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int it = 0; it < my_tiles && ok; ++it) {
+        const int b = it & 1;
+        const uint32_t aph = (it >> 1) & 1;
+        if (!tc::mbar_wait_bounded(&bars->tempty[b], aph ^ 1, abort, WAIT_NS)) {
+          ok = false;
+          break;
+        }
+        tc::fence_after_sync();
+        const uint32_t d = tmem + b * BN;
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!tc::mbar_wait_bounded(&bars->full[stage], phase, abort,
+                                     WAIT_NS)) {
+            ok = false;
+            break;
+          }
+          tc::fence_after_sync();
+          const uint32_t a0 = tc::smem_u32(sa + stage * A_BYTES);
+          const uint32_t b0 = tc::smem_u32(sb + stage * B_BYTES);
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k)
+            tc::mma_bf16(d, tc::sdesc_k_sw128(a0 + k * 32),
+                         tc::sdesc_k_sw128(b0 + k * 32), idesc,
+                         (kb | k) != 0);
+          tc::mma_commit(&bars->empty[stage]);
+          if (++stage == STAGES) { stage = 0; phase ^= 1; }
+        }
+        if (ok) tc::mma_commit(&bars->tfull[b]);
+      }
+      // every MMA issued completes before TMEM is released
+      tc::mma_commit(&bars->drain);
+      wait_timeout(&bars->drain, 0);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int m = mtile * BM + q * 32 + lane;
+    float tv[kC];
+    int ti[kC];
+#pragma unroll
+    for (int k = 0; k < kC; ++k) { tv[k] = -INFINITY; ti[k] = -1; }
+    float run_m = -INFINITY, run_s = 0.f;
+    bool ok = true;
+    for (int it = 0; it < my_tiles; ++it) {
+      const int vt = strip + it * strips;
+      const int b = it & 1;
+      const uint32_t aph = (it >> 1) & 1;
+      const bool got = tc::mbar_wait_bounded(&bars->tfull[b], aph, abort,
+                                             WAIT_NS);
+      if (!__all_sync(0xffffffffu, got)) {
+        *abort = 1;
+        ok = false;
+        break;
+      }
+      tc::fence_after_sync();
+      const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16) +
+                             static_cast<uint32_t>(b * BN);
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        __syncwarp();
+        float x[32];
+        tc::tmem_ld_x32(tbase + c * 32, x);
+        epilogue_chunk(x, vt * BN + c * 32, V, tv, ti, run_m, run_s);
+      }
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&bars->tempty[b]);
+    }
+    if (ok && m < M) {
+      const size_t pr = (size_t)m * strips + strip;
+      float4* pv = reinterpret_cast<float4*>(P.v + pr * kC);
+      int4* pi = reinterpret_cast<int4*>(P.i + pr * kC);
+#pragma unroll
+      for (int k = 0; k < kC / 4; ++k) {
+        pv[k] = make_float4(tv[4 * k], tv[4 * k + 1], tv[4 * k + 2],
+                            tv[4 * k + 3]);
+        pi[k] = make_int4(ti[4 * k], ti[4 * k + 1], ti[4 * k + 2],
+                          ti[4 * k + 3]);
+      }
+      P.m[pr] = run_m;
+      P.s[pr] = run_s;
+    }
+  }
+
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, TMEM_COLS);
+  }
+  if (threadIdx.x == 0 && bars->abort) raise_error(err, kErrTimeout);
+}
+
+}  // namespace
+
+int lmhead_tc_grid(int M, int V, int num_sms, int* row_tiles, int* strips) {
+  const int rt = (M + BM - 1) / BM;
+  const int vt = (V + BN - 1) / BN;
+  int st = std::max(1, num_sms / rt);
+  st = std::min(std::min(st, vt), kMaxStrips);
+  *row_tiles = rt;
+  *strips = st;
+  return rt * st;
+}
+
+cudaError_t launch_lmhead_tc(const CUtensorMap& map_y, const CUtensorMap& map_w,
+                             int M, int H, int V, int num_sms, TopkPartials P,
+                             int* err, int* strips_out, cudaStream_t s) {
+  int rt = 0, st = 0;
+  const int grid = lmhead_tc_grid(M, V, num_sms, &rt, &st);
+  *strips_out = st;
+  cudaError_t e = cudaFuncSetAttribute(
+      lmhead_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      (int)SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  lmhead_tc_kernel<<<grid, THREADS, SMEM_BYTES, s>>>(map_y, map_w, M, H, V,
+                                                     rt, st, P, err);
+  return cudaGetLastError();
+}
+
+}  // namespace dflash

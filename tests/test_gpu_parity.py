@@ -39,8 +39,9 @@ def run_stagewise(lib, w, x, L, seed=7, cycle=3):
     h64 = f64(h)
     if x["w_conv"] is not None:
         y = dv.y()
-        ties["y"] = check_y(y, oracle.conv2tap(h64, f64(x["w_conv"])),
-                            w.dtype)
+        W = f64(x["w_conv"])
+        ties["y"] = check_y(y, oracle.conv2tap(h64, W),
+                            oracle.conv2tap(np.abs(h64), np.abs(W)), w.dtype)
         y64 = f64(y).reshape(-1, H)
     else:
         y64 = h64.reshape(-1, H)
