@@ -221,8 +221,11 @@ dflash_status dflash_pair_score(const float* topv, const int32_t* topi,
                                 int r, dflash_dtype dt, float* scores,
                                 dflash_stream_t stream) {
   REQUIRE(topv && topi && anchor && h && w_gate && e_in && e_out && scores);
-  REQUIRE(sizes_ok(B, K, H, V) && H >= 1 && r >= 1 && r <= DFLASH_MAX_RANK);
+  REQUIRE(sizes_ok(B, K, H, V) && H >= 8 && H % 8 == 0 && r >= 1 &&
+          r <= DFLASH_MAX_RANK);
   REQUIRE(dt == DFLASH_BF16 || dt == DFLASH_FP32);
+  REQUIRE(aligned(h, 16) && aligned(w_gate, 16) && aligned(e_in, 16) &&
+          aligned(e_out, 16));
   DeviceState* d = nullptr;
   dflash_status st = device_state(&d);
   if (st != DFLASH_OK) return st;

@@ -18,7 +18,7 @@
 namespace dflash {
 namespace {
 
-constexpr int BM = 128, BC = 32, BK = 64, STAGES = 4;
+constexpr int BM = 128, BC = 32, BK = 64, STAGES = 8;
 constexpr int A_BYTES = BM * BK * 2;        // 16 KB
 constexpr int B_BYTES = 2 * BC * BK * 2;    // 8 KB (W0 part, then W1 part)
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;

@@ -63,7 +63,8 @@ struct VerifyWs {
   unsigned* counters;             // rows + 2B counters, zeroed per call
   size_t counter_bytes;
 };
-constexpr int kVerifyMaxChunks = 64;
+constexpr int kVerifyMaxChunks = 64;     // row-pass chunks per target row
+constexpr int kResampleMaxChunks = 256;  // draw-pass chunks per sequence
 size_t verify_ws_layout(int B, int K, int V, void* base, VerifyWs* out);
 cudaError_t launch_verify_rows(const float* L, const int* draft,
                                const int* topi, const float* q, int B, int K,

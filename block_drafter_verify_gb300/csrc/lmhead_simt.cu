@@ -124,9 +124,12 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
   const size_t base = (size_t)m * nstrip * kC;
   const float4* gv = reinterpret_cast<const float4*>(P.v + base);
   const int4* gi = reinterpret_cast<const int4*>(P.i + base);
+#pragma unroll 4
   for (int i = lane; i < nstrip * kC / 4; i += 32) {
-    reinterpret_cast<float4*>(sv)[i] = gv[i];
-    reinterpret_cast<int4*>(si)[i] = gi[i];
+    const float4 fv = gv[i];
+    const int4 iv = gi[i];
+    reinterpret_cast<float4*>(sv)[i] = fv;
+    reinterpret_cast<int4*>(si)[i] = iv;
   }
   // logsumexp: per-lane fold in strip order, then a fixed butterfly
   float rm = -INFINITY, rs = 0.f;

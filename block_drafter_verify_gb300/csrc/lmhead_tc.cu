@@ -47,7 +47,10 @@ struct Bars {
   uint32_t tmem_base;
   int abort;
 };
-constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + sizeof(Bars);
+constexpr int XS_STRIDE = 33;  // padded row of the per-thread chunk stage
+constexpr size_t XS_BYTES = 4 * 32 * XS_STRIDE * sizeof(float);
+constexpr size_t SMEM_BYTES =
+    1024 + (size_t)STAGES * STAGE_BYTES + sizeof(Bars) + XS_BYTES;
 
 __device__ __forceinline__ bool wait_timeout(uint64_t* bar, uint32_t parity) {
   int never = 0;
@@ -67,11 +70,13 @@ __device__ __forceinline__ void topk_insert(float (&tv)[kC], int (&ti)[kC],
   if (xv > tv[0]) { tv[0] = xv; ti[0] = xi; }
 }
 
-// Fold 32 logits (columns col0..col0+31) of this thread's row.
-__device__ __forceinline__ void epilogue_chunk(float (&x)[32], int col0,
-                                               int V, float (&tv)[kC],
-                                               int (&ti)[kC], float& run_m,
-                                               float& run_s) {
+// Fold 32 logits (columns col0..col0+31) of this thread's row into its
+// running (max, sum exp); returns the bitmask of columns that beat the
+// row's current 16th value (their values are staged in xs).
+__device__ __forceinline__ unsigned epilogue_chunk(float (&x)[32], int col0,
+                                                   int V, float thr,
+                                                   float& run_m, float& run_s,
+                                                   float* xs) {
   if (col0 + 32 > V) {
 #pragma unroll
     for (int i = 0; i < 32; ++i)
@@ -94,11 +99,15 @@ __device__ __forceinline__ void epilogue_chunk(float (&x)[32], int col0,
 #pragma unroll
   for (int i = 0; i < 32; ++i) s[i & 3] += tc::ex2_approx(fmaf(x[i], LOG2E, nb));
   run_s += (s[0] + s[1]) + (s[2] + s[3]);
-  if (cm > tv[kC - 1]) {
+  unsigned mask = 0;
+  if (cm > thr) {
 #pragma unroll
-    for (int i = 0; i < 32; ++i)
-      if (x[i] > tv[kC - 1]) topk_insert(tv, ti, x[i], col0 + i);
+    for (int i = 0; i < 32; ++i) {
+      mask |= (x[i] > thr ? 1u : 0u) << i;
+      xs[i] = x[i];
+    }
   }
+  return mask;
 }
 
 __global__ void __launch_bounds__(THREADS, 1)
@@ -112,6 +121,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint8_t* sa = smem;
   uint8_t* sb = smem + STAGES * A_BYTES;
   Bars* bars = reinterpret_cast<Bars*>(smem + STAGES * STAGE_BYTES);
+  float* xs_all = reinterpret_cast<float*>(smem + STAGES * STAGE_BYTES +
+                                           ((sizeof(Bars) + 15) & ~size_t(15)));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int mtile = blockIdx.x % row_tiles, strip = blockIdx.x / row_tiles;
   const int vtiles = (V + BN - 1) / BN;
@@ -217,6 +228,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int m = mtile * BM + q * 32 + lane;
+    float* xs = xs_all + ((warp - 2) * 32 + lane) * XS_STRIDE;
     float tv[kC];
     int ti[kC];
 #pragma unroll
@@ -242,7 +254,18 @@ __global__ void __launch_bounds__(THREADS, 1)
         __syncwarp();
         float x[32];
         tc::tmem_ld_x32(tbase + c * 32, x);
-        epilogue_chunk(x, vt * BN + c * 32, V, tv, ti, run_m, run_s);
+        const int col0 = vt * BN + c * 32;
+        unsigned mask =
+            epilogue_chunk(x, col0, V, tv[kC - 1], run_m, run_s, xs);
+        // insert the chunk's candidates, every lane its own row in step
+        while (__any_sync(0xffffffffu, mask != 0)) {
+          if (mask) {
+            const int i = __ffs(mask) - 1;
+            mask &= mask - 1;
+            const float xv = xs[i];
+            if (xv > tv[kC - 1]) topk_insert(tv, ti, xv, col0 + i);
+          }
+        }
       }
       tc::fence_before_sync();
       __syncwarp();

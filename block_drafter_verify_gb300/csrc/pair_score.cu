@@ -8,7 +8,7 @@
 // One launch, no scratch memory: a cluster of 8 CTAs owns 8 rows (b, t).
 //   1. gate pre-activations: CTA k of the cluster computes z = W_g h for the
 //      8 rows over its eighth of the hidden dimension (W_g staged through
-//      shared memory in coalesced 32-column panels);
+//      shared memory in 64-column panels with 16-byte loads);
 //   2. the partial sums are added over the cluster through distributed
 //      shared memory, in cluster-rank order, and CTA k keeps row k's gate
 //      g = sigmoid(z);
@@ -25,15 +25,32 @@ namespace {
 
 constexpr int kCluster = 8;
 constexpr int kThreads = 256;
-constexpr int kPanel = 32;  // W_g columns per staged panel
+constexpr int kPanel = 64;           // W_g columns per staged panel
+constexpr int kPanelStride = kPanel + 4;  // 16-byte rows, no bank conflicts
 
-struct PairSmem {
-  // phase 1-2 (cluster-visible)
-  float* part;   // [kCluster rows][256]
-  float* hsl;    // [kCluster rows][hs]
-  float* panel;  // [256][kPanel + 1]  (reused as E tiles in phase 3)
-  float* gate;   // [256]
+// 16-byte vector of storage elements converted to fp32.
+template <typename T>
+struct Vec16 {
+  static constexpr int N = 16 / sizeof(T);
+  __device__ __forceinline__ static void to_f32(const uint4& u, float* f);
 };
+template <>
+__device__ __forceinline__ void Vec16<float>::to_f32(const uint4& u,
+                                                     float* f) {
+  f[0] = __uint_as_float(u.x); f[1] = __uint_as_float(u.y);
+  f[2] = __uint_as_float(u.z); f[3] = __uint_as_float(u.w);
+}
+template <>
+__device__ __forceinline__ void Vec16<__nv_bfloat16>::to_f32(const uint4& u,
+                                                             float* f) {
+  const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 t = __bfloat1622float2(p[i]);
+    f[2 * i] = t.x;
+    f[2 * i + 1] = t.y;
+  }
+}
 
 template <typename T>
 __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads)
@@ -43,6 +60,8 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads)
                       const T* __restrict__ w_gate, const T* __restrict__ e_in,
                       const T* __restrict__ e_out, int B, int K, int H, int V,
                       int r, int hs, float* __restrict__ scores, int* err) {
+  constexpr int EPV = Vec16<T>::N;            // elements per 16-byte vector
+  constexpr int VPR = kPanel / EPV;           // vectors per panel row
   extern __shared__ float4 smem4[];
   float* smem = reinterpret_cast<float*>(smem4);
   cg::cluster_group cluster = cg::this_cluster();
@@ -53,10 +72,10 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads)
   const int k0 = crank * hs, k1 = min(H, k0 + hs);
   const int klen = max(0, k1 - k0);
 
-  float* part = smem;                          // kCluster * 256
-  float* hsl = part + kCluster * 256;          // kCluster * hs
-  float* panel = hsl + kCluster * hs;          // 256 * (kPanel + 1)
-  float* gate = panel + 256 * (kPanel + 1);    // 256
+  float* part = smem;                           // kCluster * 256
+  float* hsl = part + kCluster * 256;           // kCluster * hs
+  float* panel = hsl + kCluster * hs;           // 256 * kPanelStride
+  float* gate = panel + 256 * kPanelStride;     // 256
 
   // ---- phase 1: partial z[row][k] over this CTA's hidden slice ----------
   for (int i = tid; i < kCluster * hs; i += kThreads) {
@@ -67,22 +86,44 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads)
   float acc[kCluster];
 #pragma unroll
   for (int rr = 0; rr < kCluster; ++rr) acc[rr] = 0.f;
+  constexpr int kLoads = 256 * VPR / kThreads;  // 16-byte loads per thread
   for (int p0 = 0; p0 < klen; p0 += kPanel) {
-    __syncthreads();
     const int pw = min(kPanel, klen - p0);
-    for (int i = tid; i < r * kPanel; i += kThreads) {
-      const int g = i / kPanel, cc = i % kPanel;
-      panel[g * (kPanel + 1) + cc] =
-          cc < pw ? to_f32(w_gate[(size_t)g * H + k0 + p0 + cc]) : 0.f;
+    uint4 buf[kLoads];
+#pragma unroll
+    for (int u = 0; u < kLoads; ++u) {
+      const int i = tid + u * kThreads;
+      const int g = i / VPR, cv = i % VPR;
+      buf[u] = (g < r && cv * EPV < pw)
+                   ? *reinterpret_cast<const uint4*>(
+                         w_gate + (size_t)g * H + k0 + p0 + cv * EPV)
+                   : make_uint4(0, 0, 0, 0);
+    }
+    __syncthreads();  // previous panel fully consumed
+#pragma unroll
+    for (int u = 0; u < kLoads; ++u) {
+      const int i = tid + u * kThreads;
+      const int g = i / VPR, cv = i % VPR;
+      float f[EPV];
+      Vec16<T>::to_f32(buf[u], f);
+#pragma unroll
+      for (int e = 0; e < EPV; ++e) panel[g * kPanelStride + cv * EPV + e] = f[e];
     }
     __syncthreads();
     if (tid < r) {
-      const float* wrow = panel + tid * (kPanel + 1);
-      for (int cc = 0; cc < pw; ++cc) {
-        const float w = wrow[cc];
+      // four columns per step: one 16-byte load of W_g, one per row of h
+      const float4* wrow = reinterpret_cast<const float4*>(panel + tid * kPanelStride);
+      for (int c4 = 0; c4 < pw / 4; ++c4) {
+        const float4 w = wrow[c4];
 #pragma unroll
-        for (int rr = 0; rr < kCluster; ++rr)
-          acc[rr] = fmaf(w, hsl[rr * hs + p0 + cc], acc[rr]);
+        for (int rr = 0; rr < kCluster; ++rr) {
+          const float4 hv =
+              *reinterpret_cast<const float4*>(hsl + rr * hs + p0 + 4 * c4);
+          acc[rr] = fmaf(w.x, hv.x, acc[rr]);
+          acc[rr] = fmaf(w.y, hv.y, acc[rr]);
+          acc[rr] = fmaf(w.z, hv.z, acc[rr]);
+          acc[rr] = fmaf(w.w, hv.w, acc[rr]);
+        }
       }
     }
   }
@@ -121,12 +162,33 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads)
   const int rs = r + 1;  // padded row stride
   float* ein_s = panel;             // [16][rs]
   float* eout_s = panel + kC * rs;  // [16][rs], scaled by the gate
-  for (int i = tid; i < kC * r; i += kThreads) {
-    const int row = i / r, k = i % r;
-    const int a = s_pred[row], c = s_cand[row];
-    ein_s[row * rs + k] = a >= 0 ? to_f32(e_in[(size_t)a * r + k]) : 0.f;
-    eout_s[row * rs + k] =
-        c >= 0 ? to_f32(e_out[(size_t)c * r + k]) * gate[k] : 0.f;
+  const int vpr = (r + EPV - 1) / EPV;  // vectors per embedding row
+  if (r % EPV == 0) {
+    for (int i = tid; i < 2 * kC * vpr; i += kThreads) {
+      const int tab = i / (kC * vpr), rem = i % (kC * vpr);
+      const int row = rem / vpr, cv = rem % vpr;
+      const int tok = tab == 0 ? s_pred[row] : s_cand[row];
+      float f[EPV];
+      if (tok >= 0) {
+        const T* src = (tab == 0 ? e_in : e_out) + (size_t)tok * r + cv * EPV;
+        Vec16<T>::to_f32(*reinterpret_cast<const uint4*>(src), f);
+      } else {
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) f[e] = 0.f;
+      }
+      float* dst = (tab == 0 ? ein_s : eout_s) + row * rs + cv * EPV;
+#pragma unroll
+      for (int e = 0; e < EPV; ++e)
+        dst[e] = tab == 0 ? f[e] : f[e] * gate[cv * EPV + e];
+    }
+  } else {
+    for (int i = tid; i < kC * r; i += kThreads) {
+      const int row = i / r, k = i % r;
+      const int a = s_pred[row], c = s_cand[row];
+      ein_s[row * rs + k] = a >= 0 ? to_f32(e_in[(size_t)a * r + k]) : 0.f;
+      eout_s[row * rs + k] =
+          c >= 0 ? to_f32(e_out[(size_t)c * r + k]) * gate[k] : 0.f;
+    }
   }
   __syncthreads();
   const int i = tid / kC, j = tid % kC;
@@ -148,12 +210,10 @@ cudaError_t launch_pair_score(const float* topv, const int* topi,
                               int H, int V, int r, float* scores, int* err,
                               cudaStream_t s) {
   const int M = B * K;
-  const int hs = (H + kCluster - 1) / kCluster;
-  const size_t floats = (size_t)kCluster * 256 + (size_t)kCluster * hs +
-                        (size_t)256 * (kPanel + 1) + 256;
-  const size_t smem = std::max(floats, (size_t)kCluster * 256 +
-                                           (size_t)kCluster * hs +
-                                           2 * kC * (DFLASH_MAX_RANK + 1) + 256) *
+  // hidden slice per cluster rank, a multiple of 8 so 16-byte loads align
+  const int hs = ((H + kCluster - 1) / kCluster + 7) & ~7;
+  const size_t smem = ((size_t)kCluster * 256 + (size_t)kCluster * hs +
+                       (size_t)256 * kPanelStride + 256) *
                       sizeof(float);
   cudaError_t e = cudaFuncSetAttribute(
       pair_score_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -8,15 +8,20 @@
 //   verify_rows      grid (B*(K+1), chunks): every target row is split into
 //                    chunks; a CTA reduces its chunk to (max, sum exp) at
 //                    T > 0 or (max, first argmax) at T = 0.  The last CTA of
-//                    a row folds the chunk partials in chunk order; the last
-//                    row of a sequence runs the accept chain for it.
-//   verify_resample  (T > 0 only) grid (B, chunks2): every CTA sums the
-//                    fixed-point residual weights of one chunk of row n_b;
-//                    the last CTA of the sequence finds the chunk holding
-//                    the draw and scans it.
+//                    a row folds the chunk partials in a fixed order; the
+//                    last row of a sequence runs the accept tests of all K
+//                    positions in parallel (one lane each) and keeps the
+//                    prefix before the first rejection.
+//   verify_resample  (T > 0 only) grid (B, chunks of whole 4096-token
+//                    slabs): every CTA sums the fixed-point residual weights
+//                    of one chunk of row n_b; the last CTA of the sequence
+//                    finds the chunk that holds the draw with a block scan
+//                    and scans it slab by slab, 16 tokens per thread held in
+//                    registers.
 // Residual weights are integers (units of 2^-40 of the row maximum's
 // weight), so their sums are exact and the draw does not depend on the
 // grid.  "Last CTA" is found with an atomic ticket: nothing ever waits.
+// Every loop keeps several independent loads in flight.
 #include <algorithm>
 
 #include "kernels.h"
@@ -26,6 +31,8 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
+constexpr int kSeg = 16;                // tokens per thread per slab
+constexpr int kSlab = kThreads * kSeg;  // 4096 tokens
 
 __device__ __forceinline__ bool arg_better(float v1, int i1, float v2,
                                            int i2) {
@@ -58,6 +65,39 @@ __device__ __forceinline__ void online_lse(float x, float& m, float& s,
   } else if (x != -INFINITY) {
     s += __expf((x - m) * invT);
   }
+}
+
+// Fold a second (max, sum) or (max, argmax) partial into the first.
+__device__ __forceinline__ void fold(bool greedy, float& a, float& s, int& i,
+                                     float a2, float s2, int i2, float invT) {
+  if (greedy) {
+    if (arg_better(a2, i2, a, i)) { a = a2; i = i2; }
+  } else {
+    lse_combine(a, s, a2, s2, invT);
+  }
+}
+
+// Inclusive block scan of one uint64 per thread; also returns the block
+// total.  `s_red` holds kWarps values.
+__device__ __forceinline__ unsigned long long block_incl_scan(
+    unsigned long long v, unsigned long long* s_red,
+    unsigned long long* total) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long t = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += t;
+  }
+  __syncthreads();
+  if (lane == 31) s_red[wid] = v;
+  __syncthreads();
+  unsigned long long pre = 0, tot = 0;
+  for (int w = 0; w < kWarps; ++w) {
+    if (w < wid) pre += s_red[w];
+    tot += s_red[w];
+  }
+  *total = tot;
+  return v + pre;
 }
 
 __global__ void __launch_bounds__(kThreads)
@@ -106,7 +146,15 @@ __global__ void __launch_bounds__(kThreads)
       take(f.x, v); take(f.y, v + 1); take(f.z, v + 2); take(f.w, v + 3);
     }
   } else {
-    for (int v = v0 + tid; v < v1; v += kThreads) take(x[v], v);
+    int v = v0 + tid;
+    for (; v + 3 * kThreads < v1; v += 4 * kThreads) {
+      float f[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) f[u] = x[v + u * kThreads];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) take(f[u], v + u * kThreads);
+    }
+    for (; v < v1; v += kThreads) take(x[v], v);
   }
   if (__any_sync(0xffffffffu, bad) && (tid & 31) == 0)
     raise_error(err, kErrNonfinite);
@@ -120,62 +168,64 @@ __global__ void __launch_bounds__(kThreads)
     const float oa = __shfl_xor_sync(0xffffffffu, a, o);
     const float os = __shfl_xor_sync(0xffffffffu, sacc, o);
     const int oi = __shfl_xor_sync(0xffffffffu, ai, o);
-    if (greedy) {
-      if (arg_better(oa, oi, a, ai)) { a = oa; ai = oi; }
-    } else {
-      lse_combine(a, sacc, oa, os, invT);
-    }
+    fold(greedy, a, sacc, ai, oa, os, oi, invT);
   }
-  if ((tid & 31) == 0) { s_a[tid >> 5] = a; s_s[tid >> 5] = sacc; s_i[tid >> 5] = ai; }
+  if ((tid & 31) == 0) {
+    s_a[tid >> 5] = a;
+    s_s[tid >> 5] = sacc;
+    s_i[tid >> 5] = ai;
+  }
   __syncthreads();
   if (tid == 0) {
     float ra = s_a[0], rs = s_s[0];
     int ri = s_i[0];
-    for (int w = 1; w < kWarps; ++w) {
-      if (greedy) {
-        if (arg_better(s_a[w], s_i[w], ra, ri)) { ra = s_a[w]; ri = s_i[w]; }
-      } else {
-        lse_combine(ra, rs, s_a[w], s_s[w], invT);
-      }
-    }
+    for (int w = 1; w < kWarps; ++w)
+      fold(greedy, ra, rs, ri, s_a[w], s_s[w], s_i[w], invT);
     ws.chunk_part[(size_t)row * nchunk + c] =
         make_float2(ra, greedy ? __int_as_float(ri) : rs);
     __threadfence();
     s_last = (atomicAdd(&ws.counters[row], 1u) == (unsigned)(nchunk - 1));
   }
   __syncthreads();
-  if (!s_last || tid != 0) return;
+  if (!s_last || tid >= 32) return;
 
-  // ---- last CTA of this row: fold the chunks in order -------------------
+  // ---- last CTA of this row (warp 0): fold the chunks in a fixed tree ---
   __threadfence();
-  float rm = -INFINITY, rz = 0.f;
+  const int lane = tid;
+  float ra = -INFINITY, rs = 0.f;
   int ri = 0x7fffffff;
-  for (int cc = 0; cc < nchunk; ++cc) {
+  for (int cc = lane; cc < nchunk; cc += 32) {  // nchunk <= 64
     const float2 p = __ldcg(&ws.chunk_part[(size_t)row * nchunk + cc]);
-    if (greedy) {
-      const int pi = __float_as_int(p.y);
-      if (arg_better(p.x, pi, rm, ri)) { rm = p.x; ri = pi; }
-    } else {
-      lse_combine(rm, rz, p.x, p.y, invT);
+    fold(greedy, ra, rs, ri, p.x, p.y, __float_as_int(p.y), invT);
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    const float oa = __shfl_xor_sync(0xffffffffu, ra, o);
+    const float os = __shfl_xor_sync(0xffffffffu, rs, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, ri, o);
+    fold(greedy, ra, rs, ri, oa, os, oi, invT);
+  }
+  int last_row = 0;
+  if (lane == 0) {
+    if (ra == -INFINITY) {  // every logit of the row is -inf: no distribution
+      raise_error(err, kErrNonfinite);
+      ri = 0; ra = 0.f; rs = 1.f;
     }
+    ws.row_m[row] = ra;
+    ws.row_z[row] = rs;
+    ws.row_arg[row] = ri;
+    __threadfence();
+    last_row = (atomicAdd(&ws.counters[rows + b], 1u) == (unsigned)K);
   }
-  if (rm == -INFINITY) {  // every logit of the row is -inf: no distribution
-    raise_error(err, kErrNonfinite);
-    ri = 0; rm = 0.f; rz = 1.f;
-  }
-  ws.row_m[row] = rm;
-  ws.row_z[row] = rz;
-  ws.row_arg[row] = ri;
-  __threadfence();
-  if (atomicAdd(&ws.counters[rows + b], 1u) != (unsigned)K) return;
+  if (!__shfl_sync(0xffffffffu, last_row, 0)) return;
 
-  // ---- last row of sequence b: the accept chain --------------------------
+  // ---- last row of sequence b: the K accept tests, one lane each --------
   __threadfence();
-  int n = K;
-  for (int t = 0; t < K; ++t) {
+  bool ok = true;
+  if (lane < K) {
+    const int t = lane;
     const int d = draft[b * K + t];
     const int rr = b * K1 + t;
-    bool ok;
     if (d < 0 || d >= V) {
       raise_error(err, kErrBadIndex);
       ok = false;
@@ -184,12 +234,11 @@ __global__ void __launch_bounds__(kThreads)
     } else {
       float qd = 0.f;
       bool found = false;
+#pragma unroll
       for (int j = 0; j < kC; ++j) {
-        if (topi[(b * K + t) * kC + j] == d) {
-          qd = q[(b * K + t) * kC + j];
-          found = true;
-          break;
-        }
+        const int cj = topi[(b * K + t) * kC + j];
+        const float qj = q[(b * K + t) * kC + j];
+        if (!found && cj == d) { qd = qj; found = true; }
       }
       if (!found) raise_error(err, kErrBadIndex);
       const float pd = rel_weight(L[(size_t)rr * V + d],
@@ -198,13 +247,53 @@ __global__ void __launch_bounds__(kThreads)
       const float u = philox_uniform(seed, b, t, kPurposeAccept, cycle);
       ok = u * qd < pd;
     }
-    if (!ok) { n = t; break; }
   }
-  n_accepted[b] = n;
-  for (int t = 0; t <= K; ++t)
-    out_tok[b * K1 + t] = t < n ? draft[b * K + t] : -1;
-  if (greedy) out_tok[b * K1 + n] = __ldcg(&ws.row_arg[b * K1 + n]);
-  ws.n_row[b] = n;
+  const unsigned rej = __ballot_sync(0xffffffffu, lane < K && !ok);
+  const int n = rej ? __ffs(rej) - 1 : K;
+  if (lane == 0) {
+    n_accepted[b] = n;
+    ws.n_row[b] = n;
+  }
+  if (lane <= K) {
+    int tok = lane < n ? draft[b * K + lane] : -1;
+    if (greedy && lane == n) tok = __ldcg(&ws.row_arg[b * K1 + n]);
+    out_tok[b * K1 + lane] = tok;  // at T > 0 slot n is drawn next launch
+  }
+}
+
+// Fixed-point weight of token v: the residual max(0, e - q Z) for a
+// candidate of the rejected row, e itself otherwise (and for every token
+// when drawing from p).
+__device__ __forceinline__ unsigned long long token_weight(
+    float xv, int v, float m, float invT, bool use_raw, const int* s_ci,
+    const float* s_qz) {
+  const float e = rel_weight(xv, m, invT);
+  float w = e;
+  if (!use_raw) {
+#pragma unroll
+    for (int j = 0; j < kC; ++j)
+      if (s_ci[j] == v) w = fmaxf(e - s_qz[j], 0.f);
+  }
+  return quant(w);
+}
+
+// Load kSeg consecutive logits starting at v (-inf past v1).
+__device__ __forceinline__ void load_seg(const float* x, int v, int v1,
+                                         int vec4, float (&f)[kSeg]) {
+  if (vec4 && v + kSeg <= v1) {
+    const float4* p = reinterpret_cast<const float4*>(x + v);
+#pragma unroll
+    for (int u = 0; u < kSeg / 4; ++u) {
+      const float4 t = p[u];
+      f[4 * u] = t.x;
+      f[4 * u + 1] = t.y;
+      f[4 * u + 2] = t.z;
+      f[4 * u + 3] = t.w;
+    }
+  } else {
+#pragma unroll
+    for (int u = 0; u < kSeg; ++u) f[u] = (v + u < v1) ? x[v + u] : -INFINITY;
+  }
 }
 
 __global__ void __launch_bounds__(kThreads)
@@ -222,10 +311,9 @@ __global__ void __launch_bounds__(kThreads)
   const float* x = L + (size_t)rr * V;
   __shared__ int s_ci[kC];
   __shared__ float s_qz[kC];
-  __shared__ unsigned long long s_red[kWarps];
-  __shared__ int s_last, s_use_raw;
+  __shared__ unsigned long long s_red[kWarps], s_red2[kWarps];
+  __shared__ int s_last, s_use_raw, s_cstar;
   __shared__ unsigned long long s_theta, s_cum;
-  __shared__ int s_cstar;
   if (tid < kC) {
     if (n < K) {
       s_ci[tid] = topi[(b * K + n) * kC + tid];
@@ -240,16 +328,11 @@ __global__ void __launch_bounds__(kThreads)
   // ---- chunk sums: raw weights quant(e), residual = raw + corrections ----
   const int v0 = c * chunk2, v1 = min(V, v0 + chunk2);
   unsigned long long raw = 0;
-  if (vec4) {
-    const float4* x4 = reinterpret_cast<const float4*>(x);
-    for (int v = v0 + tid * 4; v < v1; v += kThreads * 4) {
-      const float4 f = x4[v >> 2];
-      raw += quant(rel_weight(f.x, m, invT)) + quant(rel_weight(f.y, m, invT)) +
-             quant(rel_weight(f.z, m, invT)) + quant(rel_weight(f.w, m, invT));
-    }
-  } else {
-    for (int v = v0 + tid; v < v1; v += kThreads)
-      raw += quant(rel_weight(x[v], m, invT));
+  for (int s0 = v0; s0 < v1; s0 += kSlab) {
+    float f[kSeg];
+    load_seg(x, s0 + tid * kSeg, v1, vec4, f);
+#pragma unroll
+    for (int u = 0; u < kSeg; ++u) raw += quant(rel_weight(f[u], m, invT));
   }
   long long corr = 0;
   if (tid < kC) {
@@ -276,75 +359,83 @@ __global__ void __launch_bounds__(kThreads)
   __syncthreads();
   if (!s_last) return;
 
-  // ---- last CTA of the sequence: locate the draw -------------------------
+  // ---- last CTA of the sequence: locate the chunk of the draw ------------
+  __threadfence();
+  unsigned long long p_res = 0, p_raw = 0;
+  if (tid < nchunk2) {  // nchunk2 <= kThreads
+    p_raw = __ldcg(&ws.res_part[((size_t)b * nchunk2 + tid) * 2 + 0]);
+    p_res = __ldcg(&ws.res_part[((size_t)b * nchunk2 + tid) * 2 + 1]);
+  }
+  const unsigned long long wres = warp_sum_u64(p_res);
+  const unsigned long long wraw = warp_sum_u64(p_raw);
+  if ((tid & 31) == 0) {
+    s_red[tid >> 5] = wres;
+    s_red2[tid >> 5] = wraw;
+  }
+  __syncthreads();
   if (tid == 0) {
-    __threadfence();
-    unsigned long long R = 0;
-    for (int cc = 0; cc < nchunk2; ++cc)
-      R += __ldcg(&ws.res_part[((size_t)b * nchunk2 + cc) * 2 + 1]);
-    int use_raw = 0;
-    if (R == 0) {  // degenerate residual: draw from p itself
-      use_raw = 1;
-      for (int cc = 0; cc < nchunk2; ++cc)
-        R += __ldcg(&ws.res_part[((size_t)b * nchunk2 + cc) * 2]);
+    unsigned long long R = 0, R0 = 0;
+    for (int w = 0; w < kWarps; ++w) {
+      R += s_red[w];
+      R0 += s_red2[w];
     }
+    const int use_raw = (R == 0);  // degenerate residual: draw from p
+    if (use_raw) R = R0;
     const unsigned long long u24 =
         philox_u24(seed, b, K, kPurposeResample, cycle);
     // theta = floor(u24 * R / 2^24); the product needs up to 82 bits
     const unsigned long long hi = __umul64hi(R, u24), lo = R * u24;
-    const unsigned long long theta = (hi << 40) | (lo >> 24);
-    unsigned long long cum = 0;
-    int cstar = -1;
-    for (int cc = 0; cc < nchunk2; ++cc) {
-      const unsigned long long p =
-          __ldcg(&ws.res_part[((size_t)b * nchunk2 + cc) * 2 + (use_raw ? 0 : 1)]);
-      if (cum + p > theta) { cstar = cc; break; }
-      cum += p;
-    }
-    if (cstar < 0) { raise_error(err, kErrBadIndex); cstar = 0; cum = 0; }
-    s_theta = theta;
-    s_cum = cum;
-    s_cstar = cstar;
+    s_theta = (hi << 40) | (lo >> 24);
     s_use_raw = use_raw;
+    s_cstar = -1;
   }
   __syncthreads();
-  const int w0 = s_cstar * chunk2, w1 = min(V, w0 + chunk2);
-  const int seg = (w1 - w0 + kThreads - 1) / kThreads;
-  const int a0 = min(w1, w0 + tid * seg), a1 = min(w1, a0 + seg);
   const bool use_raw = s_use_raw;
-  auto weight = [&](int v) -> unsigned long long {
-    const float e = rel_weight(x[v], m, invT);
-    if (!use_raw) {
-#pragma unroll
-      for (int j = 0; j < kC; ++j)
-        if (s_ci[j] == v) return quant(fmaxf(e - s_qz[j], 0.f));
+  const unsigned long long theta = s_theta;
+  {
+    const unsigned long long p = use_raw ? p_raw : p_res;
+    unsigned long long tot;
+    const unsigned long long incl = block_incl_scan(p, s_red, &tot);
+    if (tid < nchunk2 && incl - p <= theta && theta < incl) {
+      s_cstar = tid;
+      s_cum = incl - p;
     }
-    return quant(e);
-  };
-  unsigned long long tsum = 0;
-  for (int v = a0; v < a1; ++v) tsum += weight(v);
-  // exclusive block scan of tsum
-  const int lane = tid & 31, wid = tid >> 5;
-  unsigned long long incl = tsum;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const unsigned long long t = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += t;
   }
   __syncthreads();
-  if (lane == 31) s_red[wid] = incl;
-  __syncthreads();
-  unsigned long long pre = incl - tsum;
-  for (int w = 0; w < wid; ++w) pre += s_red[w];
-  const unsigned long long lo_b = s_cum + pre, theta = s_theta;
-  if (tsum > 0 && lo_b <= theta && theta < lo_b + tsum) {
-    unsigned long long acc = lo_b;
-    int pick = a1 - 1;
-    for (int v = a0; v < a1; ++v) {
-      acc += weight(v);
-      if (acc > theta) { pick = v; break; }
+  if (s_cstar < 0) {  // cannot happen: theta is below the total
+    if (tid == 0) raise_error(err, kErrBadIndex);
+    return;
+  }
+  // ---- scan chunk c* slab by slab, 16 tokens per thread in registers -----
+  const int w0 = s_cstar * chunk2, w1 = min(V, w0 + chunk2);
+  unsigned long long base = s_cum;
+  for (int s0 = w0; s0 < w1; s0 += kSlab) {
+    float f[kSeg];
+    const int v = s0 + tid * kSeg;
+    load_seg(x, v, w1, vec4, f);
+    unsigned long long wts[kSeg], tsum = 0;
+#pragma unroll
+    for (int u = 0; u < kSeg; ++u) {
+      wts[u] = (v + u < w1)
+                   ? token_weight(f[u], v + u, m, invT, use_raw, s_ci, s_qz)
+                   : 0ull;
+      tsum += wts[u];
     }
-    out_tok[b * K1 + n] = pick;
+    unsigned long long tot;
+    const unsigned long long incl = block_incl_scan(tsum, s_red, &tot);
+    const unsigned long long lo_b = base + incl - tsum;
+    if (tsum > 0 && lo_b <= theta && theta < lo_b + tsum) {
+      unsigned long long acc = lo_b;
+      int pick = -1;
+#pragma unroll
+      for (int u = 0; u < kSeg; ++u) {
+        acc += wts[u];
+        if (pick < 0 && acc > theta) pick = v + u;
+      }
+      out_tok[b * K1 + n] = pick;
+    }
+    if (theta < base + tot) break;  // uniform across the block
+    base += tot;
   }
 }
 
@@ -360,6 +451,14 @@ __global__ void philox_kernel(const uint32_t* __restrict__ ctr, uint64_t seed,
 
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
+int verify_chunks(int parts, int V, int target_ctas, int* chunk) {
+  const int max_chunks =
+      std::min(kVerifyMaxChunks, std::max(1, (V + 1023) / 1024));
+  int n = std::min(max_chunks, std::max(1, (target_ctas + parts - 1) / parts));
+  *chunk = (((V + n - 1) / n) + 3) & ~3;
+  return (V + *chunk - 1) / *chunk;
+}
+
 }  // namespace
 
 size_t verify_ws_layout(int B, int K, int V, void* base, VerifyWs* o) {
@@ -374,28 +473,19 @@ size_t verify_ws_layout(int B, int K, int V, void* base, VerifyWs* o) {
     return r;
   };
   VerifyWs w{};
-  w.chunk_part = reinterpret_cast<float2*>(take(rows * kVerifyMaxChunks * sizeof(float2)));
+  w.chunk_part =
+      reinterpret_cast<float2*>(take(rows * kVerifyMaxChunks * sizeof(float2)));
   w.row_m = reinterpret_cast<float*>(take(rows * sizeof(float)));
   w.row_z = reinterpret_cast<float*>(take(rows * sizeof(float)));
   w.row_arg = reinterpret_cast<int*>(take(rows * sizeof(int)));
   w.n_row = reinterpret_cast<int*>(take((size_t)B * sizeof(int)));
-  w.res_part = reinterpret_cast<unsigned long long*>(
-      take((size_t)B * kVerifyMaxChunks * 2 * sizeof(unsigned long long)));
+  w.res_part = reinterpret_cast<unsigned long long*>(take(
+      (size_t)B * kResampleMaxChunks * 2 * sizeof(unsigned long long)));
   w.counter_bytes = (rows + 2 * (size_t)B) * sizeof(unsigned);
   w.counters = reinterpret_cast<unsigned*>(take(w.counter_bytes));
   if (o) *o = w;
   return align256(off);
 }
-
-namespace {
-int verify_chunks(int parts, int V, int num_sms, int* chunk) {
-  const int max_chunks =
-      std::min(kVerifyMaxChunks, std::max(1, (V + 1023) / 1024));
-  int n = std::min(max_chunks, std::max(1, (num_sms + parts - 1) / parts));
-  *chunk = (((V + n - 1) / n) + 3) & ~3;
-  return (V + *chunk - 1) / *chunk;
-}
-}  // namespace
 
 // The caller zeroes ws.counters on the stream before this launch.
 cudaError_t launch_verify_rows(const float* L, const int* draft,
@@ -420,8 +510,12 @@ cudaError_t launch_verify_resample(const float* L, const int* topi,
                                    float T, uint64_t seed, uint64_t cycle,
                                    int* out_tok, const VerifyWs& ws,
                                    int num_sms, int* err, cudaStream_t s) {
-  int chunk2 = 0;
-  const int nchunk2 = verify_chunks(B, V, 2 * num_sms, &chunk2);
+  (void)num_sms;
+  // chunks are whole slabs of 4096 tokens, at most kResampleMaxChunks
+  const int slabs = (V + kSlab - 1) / kSlab;
+  const int per = (slabs + kResampleMaxChunks - 1) / kResampleMaxChunks;
+  const int chunk2 = per * kSlab;
+  const int nchunk2 = (V + chunk2 - 1) / chunk2;
   const int vec4 = (V % 4 == 0) && ((reinterpret_cast<uintptr_t>(L) & 15) == 0);
   const float invT = 1.f / T;
   verify_resample_kernel<<<dim3(B, nchunk2), kThreads, 0, s>>>(

@@ -4,16 +4,20 @@
 // sequential step; starting from the verified token, greedy follows the best
 // successor and sampling draws from the pair scores.
 //
-// One warp per sequence.  The sequence's K x 16 x 16 scores are staged in
-// shared memory with 16-byte loads first, so the K dependent steps read
-// on-chip memory only.  Lane j < 16 owns candidate slot j; argmax, max, the
-// exp weights' prefix sum and the draw are warp shuffles and one ballot.
+// One CTA of 128 threads per sequence.  All four warps stage the
+// sequence's K x 16 x 16 scores in shared memory with 16-byte loads (at most
+// eight per thread, all in flight at once), then warp 0 walks: the K
+// dependent steps read on-chip memory only.  Lane j < 16 owns candidate
+// slot j; argmax, max, the exp weights' prefix sum and the draw are warp
+// shuffles and one ballot.
 #include "kernels.h"
 
 namespace dflash {
 namespace {
 
-__global__ void __launch_bounds__(32)
+constexpr int kWalkThreads = 128;
+
+__global__ void __launch_bounds__(kWalkThreads)
     path_walk_kernel(const float* __restrict__ scores,
                      const int* __restrict__ topi, int B, int K, float T,
                      float invT, uint64_t seed, uint64_t cycle,
@@ -21,11 +25,26 @@ __global__ void __launch_bounds__(32)
                      float* __restrict__ q, int* err) {
   extern __shared__ float4 s_scores4[];
   const float* s_scores = reinterpret_cast<const float*>(s_scores4);
+  __shared__ int s_topi[DFLASH_MAX_K * kC];
   const int b = blockIdx.x, lane = threadIdx.x;
+  for (int i = threadIdx.x; i < K * kC; i += kWalkThreads)
+    s_topi[i] = topi[(size_t)b * K * kC + i];
   const float4* src =
       reinterpret_cast<const float4*>(scores + (size_t)b * K * kC * kC);
-  for (int i = lane; i < K * kC * kC / 4; i += 32) s_scores4[i] = src[i];
-  __syncwarp();
+  const int n4 = K * kC * kC / 4;  // <= 1024: eight per thread
+  float4 st[8];
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    const int i = threadIdx.x + u * kWalkThreads;
+    if (i < n4) st[u] = src[i];
+  }
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    const int i = threadIdx.x + u * kWalkThreads;
+    if (i < n4) s_scores4[i] = st[u];
+  }
+  __syncthreads();
+  if (threadIdx.x >= 32) return;
 
   int prev = 0;  // row 0 of position 0 is the anchor's row
   for (int t = 0; t < K; ++t) {
@@ -66,7 +85,7 @@ __global__ void __launch_bounds__(32)
     }
     if (lane < kC) q[rowbase + lane] = qj;
     if (lane == 0) {
-      const int tok = topi[rowbase + j];
+      const int tok = s_topi[t * kC + j];
       slot[b * K + t] = j;
       draft[b * K + t] = tok;
       if (tok < 0) raise_error(err, kErrBadIndex);
@@ -83,8 +102,9 @@ cudaError_t launch_path_walk(const float* scores, const int* topi, int B,
                              cudaStream_t s) {
   const size_t smem = (size_t)K * kC * kC * sizeof(float);
   const float invT = T > 0.f ? 1.f / T : 0.f;
-  path_walk_kernel<<<B, 32, smem, s>>>(scores, topi, B, K, T, invT, seed,
-                                       cycle, slot, draft, q, err);
+  path_walk_kernel<<<B, kWalkThreads, smem, s>>>(scores, topi, B, K, T, invT,
+                                                 seed, cycle, slot, draft, q,
+                                                 err);
   return cudaGetLastError();
 }
 

@@ -135,7 +135,8 @@ dflash_status dflash_lmhead_topk(const void* h, const void* conv_w,
  *   w_gate     [r, H] dtype;  e_in, e_out [V, r] dtype
  *   scores     [B, K, 16, 16] fp32 out: scores[b,t,i,j] = S_t(pred_i,
  *              cand_j); -inf where either index is -1.
- * Requirements: 1 <= r <= 256, 1 <= K <= 16.
+ * Requirements: 1 <= r <= 256, 1 <= K <= 16, H % 8 == 0; h, w_gate, e_in
+ * and e_out 16-byte aligned.
  */
 dflash_status dflash_pair_score(const float* topv, const int32_t* topi,
                                 const int32_t* anchor, const void* h,

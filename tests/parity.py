@@ -15,9 +15,8 @@ import oracle
 from oracle import philox
 
 C = 16
-# Tie epsilons (absolute logit gap / relative CDF distance).
-EPS_LOGIT_BF16 = 1e-4
-EPS_LOGIT_FP32 = 1e-5
+# Tie epsilons of the sampled decisions (relative CDF distance / relative
+# accept-test margin).
 EPS_CDF = 1e-5
 EPS_ACCEPT = 1e-5
 
@@ -32,38 +31,56 @@ def np_(t):
     return t.detach().cpu().numpy()
 
 
+def _ulp_bf16(x):
+    e = np.floor(np.log2(np.maximum(np.abs(x), 2.0 ** -126)))
+    return 2.0 ** (e - 7)
+
+
 def check_y(y_gpu, y_ref64, y_abs64, dtype):
-    """y: bf16 results equal the oracle's rounding except at rounding
-    near-ties; fp32 within the accumulation bound.  ``y_abs64`` is the same
-    conv of |h| with |W| (the sum of the magnitudes of every term), which
-    bounds the fp32 accumulation error.  Returns the tie count."""
+    """Conv output y.  The exact value y_ref is known to float64; the CUDA
+    value may differ by its fp32 accumulation error, at most 1e-6 of the sum
+    of term magnitudes y_abs (measured on GB300: 1.25e-7).  A bf16 result
+    must therefore be the correct rounding of some value within that band:
+    |y - y_ref| <= band + ulp(y)/2.  Where the two taps cancel, the band can
+    span several bf16 steps.  Returns the count of results that differ from
+    the round-to-nearest-even of y_ref (legitimate near-ties)."""
     g = np_(y_gpu.float()).astype(np.float64)
-    band = 1e-5 * y_abs64 + 1e-30
+    band = 1e-6 * y_abs64 + 1e-30
     if dtype == "fp32":
         assert np.all(np.abs(g - y_ref64) <= band)
         return 0
-    o = oracle.round_bf16(y_ref64).astype(np.float64)
-    diff = g != o
-    if not diff.any():
-        return 0
-    # a mismatch is allowed only when the exact value sits on the rounding
-    # boundary between the two neighbouring bf16 values
-    mid = 0.5 * (g[diff] + o[diff])
-    near = np.abs(y_ref64[diff] - mid) <= band[diff]
-    step = np.abs(g[diff] - o[diff]) <= np.abs(o[diff]) * 2.0 ** -7 + 1e-30
-    assert np.all(near & step), (
-        f"{int((~(near & step)).sum())} y values differ beyond rounding ties")
-    return int(diff.sum())
+    half = 0.5 * np.maximum(_ulp_bf16(g), _ulp_bf16(y_ref64))
+    ok = np.abs(g - y_ref64) <= band + half
+    if not np.all(ok):
+        idx = np.nonzero(~ok.reshape(-1))[0][:5]
+        gv, rv, bv = g.reshape(-1), y_ref64.reshape(-1), band.reshape(-1)
+        det = "; ".join(f"#{i}: gpu {gv[i]!r} exact {rv[i]!r} band {bv[i]:.3g}"
+                        for i in idx)
+        raise AssertionError(f"{int((~ok).sum())} y values outside the "
+                             f"accumulation band: {det}")
+    return int((g != oracle.round_bf16(y_ref64)).sum())
 
 
-def check_topk(topv, topi, lse, ref, eps, lse_rtol):
+# Error model of a logit computed with fp32 accumulation: |error| <= c *
+# sum_k |y_k W_vk|.  Measured on GB300 for the tensor-core path: at most
+# 6.6e-7 of that sum (b32k8); c = 2e-6 leaves a 3x margin.  Sequential fp32
+# accumulation over H <= 64 terms is bounded by H * 2^-24 < 4e-6.
+ERR_C = {"bf16": 2e-6, "fp32": 4e-6}
+
+
+def check_topk(topv, topi, lse, ref, A, c):
     """Compare the CUDA top-16 / lse with the oracle's ``ref`` = (topv, topi,
-    lse, U) computed from the CUDA path's own y (U = float64 logits [M, V]).
-    Returns the number of rows whose lists differ by near-ties."""
+    lse, U) computed from the CUDA path's own y.  ``A`` = |y| |W|^T (the
+    sum of term magnitudes per logit) scales the accumulation bound c * A.
+    Two tokens may trade ranks only if their exact logits are within the sum
+    of their bounds.  Returns the number of rows whose lists differ."""
     topv, topi, lse = np_(topv), np_(topi), np_(lse)
     _, o_i, o_lse, U = ref
     M, V = U.shape
-    np.testing.assert_allclose(lse, o_lse, rtol=lse_rtol, atol=0)
+    lse_tol = c * A.max(axis=1) + 1e-6 * np.abs(o_lse)
+    bad = np.abs(lse - o_lse) > lse_tol
+    assert not bad.any(), (f"lse rows {np.nonzero(bad)[0][:5]}: "
+                           f"{lse[bad][:5]} vs {o_lse[bad][:5]}")
     n = min(C, V)
     ties = 0
     for m in range(M):
@@ -71,14 +88,13 @@ def check_topk(topv, topi, lse, ref, eps, lse_rtol):
         assert np.all((gi >= 0) & (gi < V)), f"row {m}: index out of range"
         assert len(set(gi.tolist())) == n, f"row {m}: repeated index"
         assert np.all(topi[m, n:] == -1) and np.all(np.isneginf(topv[m, n:]))
-        # reported values belong to their indices
-        np.testing.assert_allclose(topv[m, :n], U[m, gi], rtol=1e-5,
-                                   atol=eps * 0.1)
+        eg = c * A[m, gi] + 1e-7
+        assert np.all(np.abs(topv[m, :n] - U[m, gi]) <= eg), (
+            f"row {m}: topv off by {np.abs(topv[m, :n] - U[m, gi]).max()}")
         if not np.array_equal(gi, oi):
             ties += 1
-            # rank by rank, the chosen tokens' exact logits agree within eps
             gap = np.abs(U[m, gi] - U[m, oi])
-            assert np.all(gap <= eps), (
+            assert np.all(gap <= eg + c * A[m, oi] + 1e-7), (
                 f"row {m}: top-16 differs beyond ties: {gi} vs {oi}, gap "
                 f"{gap.max()}")
     return ties
@@ -154,10 +170,8 @@ def draft_logits_oracle(x, w):
     return U.reshape(w.B, w.K + 1, w.V).astype(np.float32)
 
 
-def tie_eps(dtype):
-    return EPS_LOGIT_BF16 if dtype == "bf16" else EPS_LOGIT_FP32
 
 
-__all__ = ["check_y", "check_topk", "check_scores", "check_walk",
+__all__ = ["ERR_C", "check_y", "check_topk", "check_scores", "check_walk",
            "check_verify", "to_dev", "draft_logits_oracle", "f64", "np_",
-           "tie_eps", "torch"]
+           "torch"]

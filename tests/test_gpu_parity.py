@@ -11,8 +11,8 @@ import oracle
 import synth
 from golden import lattice
 from oracle import philox
-from parity import (check_scores, check_topk, check_verify, check_walk,
-                    check_y, draft_logits_oracle, f64, np_, tie_eps, to_dev)
+from parity import (ERR_C, check_scores, check_topk, check_verify,
+                    check_walk, check_y, draft_logits_oracle, f64, np_, to_dev)
 
 pytestmark = pytest.mark.gpu
 C = 16
@@ -45,10 +45,10 @@ def run_stagewise(lib, w, x, L, seed=7, cycle=3):
         y64 = f64(y).reshape(-1, H)
     else:
         y64 = h64.reshape(-1, H)
-    ref = oracle.lmhead_topk(y64, f64(x["w_lm"]), want_logits=True)
-    bf16 = w.dtype == "bf16"
-    ties["topk"] = check_topk(dv.topv, dv.topi, dv.lse, ref, tie_eps(w.dtype),
-                              1e-5 if bf16 else 1e-6)
+    W_lm = f64(x["w_lm"])
+    ref = oracle.lmhead_topk(y64, W_lm, want_logits=True)
+    A = np.abs(y64) @ np.abs(W_lm).T
+    ties["topk"] = check_topk(dv.topv, dv.topi, dv.lse, ref, A, ERR_C[w.dtype])
     dv.pair_score(h, anchor)
     torch.cuda.synchronize()
     topv = np_(dv.topv).reshape(B, K, C)
