@@ -7,10 +7,11 @@ from .binding import (BF16, C, FP32, STAGES, DFlashError, DraftVerify,
                       EXPORTS, dflash_check, dflash_lmhead_topk,
                       dflash_pair_score, dflash_path_walk, dflash_philox4x32,
                       dflash_profile_stage, dflash_verify,
-                      dflash_workspace_bytes, library_path, load)
+                      dflash_verify_noalloc, dflash_workspace_bytes,
+                      library_path, load)
 
 __all__ = ["BF16", "C", "FP32", "STAGES", "DFlashError", "DraftVerify",
            "EXPORTS", "dflash_check", "dflash_lmhead_topk",
            "dflash_pair_score", "dflash_path_walk", "dflash_philox4x32",
-           "dflash_profile_stage", "dflash_verify", "dflash_workspace_bytes",
-           "library_path", "load"]
+           "dflash_profile_stage", "dflash_verify", "dflash_verify_noalloc",
+           "dflash_workspace_bytes", "library_path", "load"]

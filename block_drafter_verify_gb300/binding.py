@@ -20,8 +20,9 @@ STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported",
           5: "device wait timed out", 6: "token index out of range"}
 
 EXPORTS = ("dflash_workspace_bytes", "dflash_lmhead_topk", "dflash_pair_score",
-           "dflash_path_walk", "dflash_verify", "dflash_philox4x32",
-           "dflash_profile_stage", "dflash_check", "dflash_status_string")
+           "dflash_path_walk", "dflash_verify", "dflash_verify_noalloc",
+           "dflash_philox4x32", "dflash_profile_stage", "dflash_check",
+           "dflash_status_string")
 STAGES = ("conv", "lmhead", "merge", "pair_score", "walk", "verify_rows",
           "verify_draw")
 
@@ -62,6 +63,8 @@ def load(path: str | None = None):
                                    vp, vp]),
         "dflash_verify": (i32, [vp, vp, vp, vp, i32, i32, i32, f32, u64, u64,
                                 vp, vp, vp, sz, vp]),
+        "dflash_verify_noalloc": (i32, [vp, vp, vp, vp, i32, i32, i32, f32,
+                                        u64, u64, vp, vp, vp]),
         "dflash_philox4x32": (i32, [vp, u64, vp, i64, vp]),
         "dflash_profile_stage": (i32, [i32, vp, vp]),
         "dflash_check": (i32, [vp]),
@@ -171,6 +174,18 @@ def dflash_verify(target_logits, draft, topi, q, T, seed, cycle, n_accepted,
           _ptr(q), B, K1 - 1, V, float(T), int(seed) & (2**64 - 1),
           int(cycle) & (2**64 - 1), _ptr(n_accepted), _ptr(out_tok),
           _ptr(ws), ws.numel(), _stream(stream))
+
+
+def dflash_verify_noalloc(target_logits, draft, topi, q, T, seed, cycle,
+                          n_accepted, out_tok, stream=None):
+    """dflash_verify with the library's own fixed scratch, for callers that
+    cannot allocate device memory; same arguments minus the workspace."""
+    B, K1, V = target_logits.shape
+    _want(target_logits, torch.float32, "target_logits")
+    _call("dflash_verify_noalloc", _ptr(target_logits), _ptr(draft),
+          _ptr(topi), _ptr(q), B, K1 - 1, V, float(T),
+          int(seed) & (2**64 - 1), int(cycle) & (2**64 - 1),
+          _ptr(n_accepted), _ptr(out_tok), _stream(stream))
 
 
 def dflash_philox4x32(ctr, seed, out, stream=None):

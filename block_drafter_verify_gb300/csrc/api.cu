@@ -176,6 +176,19 @@ dflash_status lmhead_impl(const T* h, const T* conv_w, const T* w_lm, int B,
 
 }  // namespace
 
+namespace dflash {
+// SM count and device error word of the current device, for entry points
+// defined in other files.
+dflash_status current_device_info(int* sms, int** err) {
+  DeviceState* d = nullptr;
+  const dflash_status st = device_state(&d);
+  if (st != DFLASH_OK) return st;
+  *sms = d->sms;
+  *err = d->err;
+  return DFLASH_OK;
+}
+}  // namespace dflash
+
 extern "C" {
 
 size_t dflash_workspace_bytes(int which, int B, int K, int H, int V) {

@@ -195,6 +195,33 @@ dflash_status dflash_verify(const float* target_logits, const int32_t* draft,
                             int32_t* n_accepted, int32_t* out_tok, void* ws,
                             size_t ws_bytes, dflash_stream_t s);
 
+/*
+ * dflash_verify without any caller-provided scratch, for callers that
+ * cannot allocate device memory at the time they verify: serving loops whose
+ * device memory belongs to another engine's allocator, code running where
+ * allocation (and the synchronisation it can bring) is not allowed, and C
+ * callers with no allocator of their own.  This entry point has no
+ * counterpart in the pages; it exists for those callers only.
+ *
+ * Same arguments, semantics and results as dflash_verify, minus ws and
+ * ws_bytes.  The scratch is a fixed 4 MiB array the library holds in device
+ * memory on every GPU that loads it, until the process exits; sizes whose
+ * scratch (dflash_workspace_bytes(1, B, K, 0, V)) exceeds 4 MiB are refused
+ * with DFLASH_ERR_UNSUPPORTED (B = 256 with K = 16 fits; B = 512 with
+ * K = 16 does not).  The first call on a device looks up the array's device
+ * address
+ * (so make that first call before any stream capture).  All calls share the
+ * array: each clears what must start at zero itself, and calls whose
+ * kernels overlap on the GPU (several streams or threads on one device)
+ * race on it and must be serialised by the caller.  Allocates nothing.
+ */
+dflash_status dflash_verify_noalloc(const float* target_logits,
+                                   const int32_t* draft, const int32_t* topi,
+                                   const float* q, int B, int K, int V,
+                                   float T, uint64_t seed, uint64_t cycle,
+                                   int32_t* n_accepted, int32_t* out_tok,
+                                   dflash_stream_t s);
+
 /* Philox4x32-10 of n counters (ctr [n, 4] uint32, device) under key
  * (seed lo, seed hi) into out [n, 4] uint32 (device): the generator the
  * walk and verify draw from, exposed so callers can reproduce draws. */

@@ -1,0 +1,67 @@
+"""dflash_verify_noalloc: verify for callers that cannot allocate device
+memory (serving loops whose memory belongs to another engine's allocator,
+code where allocating is not allowed, C callers without an allocator).  It
+keeps its scratch in the library's own fixed device array; its results must
+equal dflash_verify's, call after call, since every call reuses (and must
+re-clear) that array.  This file is collected last."""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from parity import draft_logits_oracle, np_, to_dev
+
+pytestmark = pytest.mark.gpu
+C = 16
+
+
+def _drafts(lib, w, x):
+    """Candidates, drafts and q from the library's own first three steps."""
+    dv = lib.DraftVerify(w.B, w.K, w.H, w.V, w.r,
+                         {k: to_dev(x[k]) for k in ("w_conv", "w_lm", "w_gate",
+                                                    "e_in", "e_out")})
+    h = to_dev(x["h"][:, :w.K])
+    dv.lmhead(h)
+    dv.pair_score(h, to_dev(x["anchor"]))
+    dv.walk(w.T, 17, 4)
+    return dv
+
+
+@pytest.mark.parametrize("T", [1.0, 0.0])
+def test_noalloc_verify_matches_verify_on_consecutive_calls(lib, T):
+    w = synth.Workload("noalloc", B=6, K=5, V=4099, H=128, r=32, dtype="bf16",
+                       T=T, seed=21, w_lm_sd=0.2, conv_sd=0.05, sel_sd=0.1,
+                       target=("affine", 0.9, 0.7))
+    x = synth.make_inputs(w)
+    L = to_dev(synth.target_logits(w, draft_logits_oracle(x, w)))
+    dv = _drafts(lib, w, x)
+    topi = dv.topi.view(w.B, w.K, C)
+    i32 = dict(dtype=torch.int32, device="cuda")
+    for call in range(2):                       # two calls in a row
+        cyc = 100 + call
+        n_ref = torch.empty(w.B, **i32)
+        out_ref = torch.empty(w.B, w.K + 1, **i32)
+        ws = torch.empty(lib.dflash_workspace_bytes(1, w.B, w.K, w.H, w.V),
+                         dtype=torch.uint8, device="cuda")
+        lib.dflash_verify(L, dv.draft, topi, dv.q, T, 7, cyc, n_ref, out_ref,
+                          ws)
+        n = torch.full((w.B,), -7, **i32)
+        out = torch.full((w.B, w.K + 1), -7, **i32)
+        lib.dflash_verify_noalloc(L, dv.draft, topi, dv.q, T, 7, cyc, n, out)
+        torch.cuda.synchronize()
+        lib.dflash_check()
+        assert np.array_equal(np_(n), np_(n_ref))
+        assert np.array_equal(np_(out), np_(out_ref))
+
+
+def test_noalloc_verify_refuses_sizes_beyond_its_scratch(lib):
+    B, K, V = 512, 16, 64
+    L = torch.zeros(B, K + 1, V, device="cuda")
+    draft = torch.zeros(B, K, dtype=torch.int32, device="cuda")
+    topi = torch.zeros(B, K, C, dtype=torch.int32, device="cuda")
+    q = torch.zeros(B, K, C, device="cuda")
+    n = torch.empty(B, dtype=torch.int32, device="cuda")
+    out = torch.empty(B, K + 1, dtype=torch.int32, device="cuda")
+    with pytest.raises(lib.DFlashError) as e:
+        lib.dflash_verify_noalloc(L, draft, topi, q, 1.0, 0, 0, n, out)
+    assert e.value.status == 2      # DFLASH_ERR_UNSUPPORTED
