@@ -367,8 +367,7 @@ def run_ours(args):
             except RuntimeError:
                 ts = []
                 break
-        if ts and (w.conv_sd is not None or name != "conv") and \
-                (w.T > 0 or name != "verify_draw"):
+        if ts and (w.conv_sd is not None or name != "conv"):
             stage_us[name] = statistics.mean(ts)
 
     # roofline of the dominant kernel (the LM head)
@@ -440,8 +439,7 @@ def run_ours(args):
     if rank != 0:
         return 0
     n_mean = float(np.mean(n_hist))
-    launches_per_step = (3 if w.conv_sd is not None else 2) + 2 + \
-        (2 if w.T > 0 else 1)
+    launches_per_step = (3 if w.conv_sd is not None else 2) + 3
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": 1e3 * secs_max / K,

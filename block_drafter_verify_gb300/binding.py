@@ -23,8 +23,7 @@ EXPORTS = ("dflash_workspace_bytes", "dflash_lmhead_topk", "dflash_pair_score",
            "dflash_path_walk", "dflash_verify", "dflash_verify_noalloc",
            "dflash_philox4x32", "dflash_profile_stage", "dflash_check",
            "dflash_status_string")
-STAGES = ("conv", "lmhead", "merge", "pair_score", "walk", "verify_rows",
-          "verify_draw")
+STAGES = ("conv", "lmhead", "merge", "pair_score", "walk", "verify")
 
 
 class DFlashError(RuntimeError):

@@ -45,7 +45,7 @@ dflash_status device_state(DeviceState** out) {
 
 // Caller-supplied timing events per stage (dflash_profile_stage).
 enum Stage { kStConv = 0, kStLmhead, kStMerge, kStPair, kStWalk, kStVerifyRows,
-             kStVerifyDraw, kNumStages };
+             kNumStages };
 cudaEvent_t g_prof[kNumStages][2] = {};
 
 struct StageTimer {
@@ -297,17 +297,10 @@ dflash_status dflash_verify(const float* target_logits, const int32_t* draft,
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(w.counters, 0, w.counter_bytes, s) != cudaSuccess)
     return DFLASH_ERR_CUDA;
-  cudaError_t e;
-  {
-    StageTimer tm(kStVerifyRows, s);
-    e = launch_verify_rows(target_logits, draft, topi, q, B, K, V, T, seed,
-                           cycle, n_accepted, out_tok, w, d->sms, d->err, s);
-  }
-  if (e != cudaSuccess || T == 0.f) return cuda_status(e);
-  StageTimer tm(kStVerifyDraw, s);
-  return cuda_status(launch_verify_resample(target_logits, topi, q, B, K, V, T,
-                                            seed, cycle, out_tok, w, d->sms,
-                                            d->err, s));
+  StageTimer tm(kStVerifyRows, s);
+  return cuda_status(launch_verify(target_logits, draft, topi, q, B, K, V, T,
+                                   seed, cycle, n_accepted, out_tok, w, d->sms,
+                                   d->err, s));
 }
 
 dflash_status dflash_philox4x32(const uint32_t* ctr, uint64_t seed,

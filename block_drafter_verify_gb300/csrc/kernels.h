@@ -54,29 +54,22 @@ cudaError_t launch_path_walk(const float* scores, const int* topi, int B,
 
 // verify.cu ---------------------------------------------------------------
 struct VerifyWs {
-  float2* chunk_part;             // [rows][nchunk]
-  float* row_m;                   // [rows]
-  float* row_z;                   // [rows]
-  int* row_arg;                   // [rows]
-  int* n_row;                     // [B]
-  unsigned long long* res_part;   // [B][nchunk2][2]
-  unsigned* counters;             // rows + 2B counters, zeroed per call
+  float2* part;        // [rows][max(segments, 64)]: segment (max, sum) pairs
+                       // at T > 0, chunk (max, argmax) at T = 0
+  float* row_m;        // [rows] row max
+  float* row_z;        // [rows] sum of exp((x - max) / T)
+  int* row_arg;        // [rows] first argmax
+  unsigned* counters;  // rows + B tickets, zeroed before every launch
   size_t counter_bytes;
 };
-constexpr int kVerifyMaxChunks = 64;     // row-pass chunks per target row
-constexpr int kResampleMaxChunks = 256;  // draw-pass chunks per sequence
+constexpr int kVerifyMaxChunks = 64;  // row chunks (CTAs) per target row
 size_t verify_ws_layout(int B, int K, int V, void* base, VerifyWs* out);
-cudaError_t launch_verify_rows(const float* L, const int* draft,
-                               const int* topi, const float* q, int B, int K,
-                               int V, float T, uint64_t seed, uint64_t cycle,
-                               int* n_accepted, int* out_tok,
-                               const VerifyWs& ws, int num_sms, int* err,
-                               cudaStream_t s);
-cudaError_t launch_verify_resample(const float* L, const int* topi,
-                                   const float* q, int B, int K, int V,
-                                   float T, uint64_t seed, uint64_t cycle,
-                                   int* out_tok, const VerifyWs& ws,
-                                   int num_sms, int* err, cudaStream_t s);
+// The caller zeroes ws.counters on stream s first.
+cudaError_t launch_verify(const float* L, const int* draft, const int* topi,
+                          const float* q, int B, int K, int V, float T,
+                          uint64_t seed, uint64_t cycle, int* n_accepted,
+                          int* out_tok, const VerifyWs& ws, int num_sms,
+                          int* err, cudaStream_t s);
 
 // philox --------------------------------------------------------------------
 cudaError_t launch_philox(const uint32_t* ctr, uint64_t seed, uint32_t* out,

@@ -10,8 +10,8 @@
 // logit of column v0 + l, the warp folds the 32 logits into its running
 // (max, sum exp) and into a top-16 list held by lanes 0..15, sorted by
 // (value desc, id asc).  Logits never leave registers.
-// topk_merge: one CTA per row folds the strips' lists and (max, sum) pairs
-// in strip order and writes topv / topi / lse.
+// topk_merge: one CTA per row merges the strips' lists and (max, sum)
+// pairs and writes topv / topi / lse.
 #include <algorithm>
 #include <climits>
 
@@ -102,92 +102,87 @@ __global__ void __launch_bounds__(kThreads)
   }
 }
 
-// One warp per row.  The row's strip lists are staged in shared memory;
-// (max, sum) pairs are folded per lane in strip order and then across lanes
-// in a fixed tree; the top-16 is a 16-round tournament of the strips' list
-// heads (lane l owns strips l, l+32, ...), so the result does not depend on
-// timing.
-constexpr int kMergeWarps = 4;
-constexpr int kMaxOwned = (kMaxStrips + 31) / 32;
+// One CTA of eight warps per row.  Warp w prefetches the lists of strips
+// w, w+8, ... (all loads in flight at once) and folds each into a sorted
+// top-16 held by lanes 0..15 with a bitonic merge: lanes 0..15 hold the
+// current list best-first, lanes 16..31 the new list worst-first, and five
+// compare-exchange steps (distance 16, 8, 4, 2, 1) sort the 32 entries.  A
+// list whose best entry does not beat the current 16th is skipped.  Warp 0
+// then merges the eight warp lists in warp order; (max, sum) pairs are
+// folded per warp in strip order and then in warp order.  The result does
+// not depend on timing.
+constexpr int kMergeWarps = 8;
+constexpr int kMaxPerWarp = (kMaxStrips + kMergeWarps - 1) / kMergeWarps;
+
+// One bitonic merge: (v, i) on lanes 0..15 = current list, lanes 16..31 =
+// candidate list reversed; returns with lanes 0..15 = the best 16, sorted.
+__device__ __forceinline__ void bitonic_merge32(float& v, int& i, int lane) {
+#pragma unroll
+  for (int d = 16; d; d >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, v, d);
+    const int oi = __shfl_xor_sync(0xffffffffu, i, d);
+    const bool lower = (lane & d) == 0;
+    if (lower == ranks_ahead(ov, oi, v, i)) { v = ov; i = oi; }
+  }
+}
 
 __global__ void __launch_bounds__(kMergeWarps * 32)
     topk_merge_kernel(TopkPartials P, int nstrip, int M, float* topv,
                       int* topi, float* lse) {
-  extern __shared__ float4 msm4[];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int m = blockIdx.x * kMergeWarps + warp;
-  if (m >= M) return;
-  float* sv = reinterpret_cast<float*>(msm4) + (size_t)warp * nstrip * kC;
-  int* si = reinterpret_cast<int*>(reinterpret_cast<float*>(msm4) +
-                                   (size_t)kMergeWarps * nstrip * kC) +
-            (size_t)warp * nstrip * kC;
-  const size_t base = (size_t)m * nstrip * kC;
-  const float4* gv = reinterpret_cast<const float4*>(P.v + base);
-  const int4* gi = reinterpret_cast<const int4*>(P.i + base);
-#pragma unroll 4
-  for (int i = lane; i < nstrip * kC / 4; i += 32) {
-    const float4 fv = gv[i];
-    const int4 iv = gi[i];
-    reinterpret_cast<float4*>(sv)[i] = fv;
-    reinterpret_cast<int4*>(si)[i] = iv;
+  const int m = blockIdx.x;
+  __shared__ float s_v[kMergeWarps][kC], s_m[kMergeWarps], s_s[kMergeWarps];
+  __shared__ int s_i[kMergeWarps][kC];
+  const size_t base = (size_t)m * nstrip;
+  const int k = lane < kC ? lane : 31 - lane;  // lanes 16..31: reversed
+  float nv[kMaxPerWarp];
+  int ni[kMaxPerWarp];
+#pragma unroll
+  for (int j = 0; j < kMaxPerWarp; ++j) {
+    const int st = warp + j * kMergeWarps;
+    nv[j] = -INFINITY;
+    ni[j] = -1;
+    if (st < nstrip) {
+      nv[j] = P.v[(base + st) * kC + k];
+      ni[j] = P.i[(base + st) * kC + k];
+    }
   }
-  // logsumexp: per-lane fold in strip order, then a fixed butterfly
+  float tv = -INFINITY;
+  int ti = -1;
   float rm = -INFINITY, rs = 0.f;
-  for (int st = lane; st < nstrip; st += 32)
-    lse_combine(rm, rs, P.m[(size_t)m * nstrip + st],
-                P.s[(size_t)m * nstrip + st], 1.f);
 #pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const float om = __shfl_xor_sync(0xffffffffu, rm, o);
-    const float os = __shfl_xor_sync(0xffffffffu, rs, o);
-    if (lane & o) {  // the higher lane folds the lower lane's value first
-      float am = om, as = os;
-      lse_combine(am, as, rm, rs, 1.f);
-      rm = am; rs = as;
-    } else {
-      lse_combine(rm, rs, om, os, 1.f);
-    }
+  for (int j = 0; j < kMaxPerWarp; ++j) {
+    const int st = warp + j * kMergeWarps;
+    if (st >= nstrip) break;
+    if (lane == 0) lse_combine(rm, rs, P.m[base + st], P.s[base + st], 1.f);
+    const float bv = __shfl_sync(0xffffffffu, nv[j], 0);
+    const int bi = __shfl_sync(0xffffffffu, ni[j], 0);
+    if (!ranks_ahead(bv, bi, __shfl_sync(0xffffffffu, tv, kC - 1),
+                     __shfl_sync(0xffffffffu, ti, kC - 1)))
+      continue;  // nothing in this list enters the top 16
+    float v = lane < kC ? tv : nv[j];
+    int i = lane < kC ? ti : ni[j];
+    bitonic_merge32(v, i, lane);
+    tv = v;
+    ti = i;
   }
-  __syncwarp();
-  // tournament over list heads
-  int head[kMaxOwned];
-#pragma unroll
-  for (int j = 0; j < kMaxOwned; ++j) head[j] = 0;
-  float outv = -INFINITY;
-  int outi = -1;
-  for (int r = 0; r < kC; ++r) {
-    float bv = -INFINITY;
-    int bi = -1, bj = -1;
-#pragma unroll
-    for (int j = 0; j < kMaxOwned; ++j) {
-      const int st = lane + 32 * j;
-      if (st < nstrip && head[j] < kC) {
-        const float v = sv[st * kC + head[j]];
-        const int id = si[st * kC + head[j]];
-        if (bj < 0 || ranks_ahead(v, id, bv, bi)) { bv = v; bi = id; bj = j; }
-      }
-    }
-    int bl = lane;
-#pragma unroll
-    for (int o = 16; o; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-      const int ol = __shfl_xor_sync(0xffffffffu, bl, o);
-      const int oj = __shfl_xor_sync(0xffffffffu, bj, o);
-      const bool take = (oj >= 0) && (bj < 0 || ranks_ahead(ov, oi, bv, bi) ||
-                                      (ov == bv && oi == bi && ol < bl));
-      if (take) { bv = ov; bi = oi; bl = ol; bj = oj; }
-    }
-    if (lane == r) { outv = bv; outi = bi; }
-    if (lane == bl && bj >= 0) {
-#pragma unroll
-      for (int j = 0; j < kMaxOwned; ++j)
-        if (j == bj) ++head[j];
-    }
+  if (lane < kC) { s_v[warp][lane] = tv; s_i[warp][lane] = ti; }
+  if (lane == 0) { s_m[warp] = rm; s_s[warp] = rs; }
+  __syncthreads();
+  if (warp != 0) return;
+  for (int w2 = 1; w2 < kMergeWarps; ++w2) {
+    if (lane == 0) lse_combine(rm, rs, s_m[w2], s_s[w2], 1.f);
+    const float cv = s_v[w2][k];
+    const int ci = s_i[w2][k];
+    float v = lane < kC ? tv : cv;
+    int i = lane < kC ? ti : ci;
+    bitonic_merge32(v, i, lane);
+    tv = v;
+    ti = i;
   }
   if (lane < kC) {
-    topv[(size_t)m * kC + lane] = outv;
-    topi[(size_t)m * kC + lane] = outi;
+    topv[(size_t)m * kC + lane] = tv;
+    topi[(size_t)m * kC + lane] = ti;
   }
   if (lane == 0) lse[m] = rm + logf(rs);
 }
@@ -219,13 +214,8 @@ cudaError_t launch_lmhead_simt(const T* y, const T* w_lm, int M, int H, int V,
 
 cudaError_t launch_topk_merge(TopkPartials P, int nstrip, int M, float* topv,
                               int* topi, float* lse, cudaStream_t s) {
-  const size_t smem = (size_t)kMergeWarps * nstrip * kC * 8;
-  cudaError_t e = cudaFuncSetAttribute(
-      topk_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-      (int)smem);
-  if (e != cudaSuccess) return e;
-  topk_merge_kernel<<<(M + kMergeWarps - 1) / kMergeWarps, kMergeWarps * 32,
-                      smem, s>>>(P, nstrip, M, topv, topi, lse);
+  topk_merge_kernel<<<M, kMergeWarps * 32, 0, s>>>(P, nstrip, M, topv, topi,
+                                                   lse);
   return cudaGetLastError();
 }
 

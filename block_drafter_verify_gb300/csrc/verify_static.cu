@@ -96,12 +96,8 @@ extern "C" dflash_status dflash_verify_noalloc(
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(w.counters, 0, w.counter_bytes, s) != cudaSuccess)
     return DFLASH_ERR_CUDA;
-  cudaError_t e = launch_verify_rows(target_logits, draft, topi, q, B, K, V, T,
-                                     seed, cycle, n_accepted, out_tok, w, sms,
-                                     err, s);
-  if (e != cudaSuccess) return DFLASH_ERR_CUDA;
-  if (T == 0.f) return DFLASH_OK;
-  e = launch_verify_resample(target_logits, topi, q, B, K, V, T, seed, cycle,
-                             out_tok, w, sms, err, s);
+  const cudaError_t e =
+      launch_verify(target_logits, draft, topi, q, B, K, V, T, seed, cycle,
+                    n_accepted, out_tok, w, sms, err, s);
   return e == cudaSuccess ? DFLASH_OK : DFLASH_ERR_CUDA;
 }

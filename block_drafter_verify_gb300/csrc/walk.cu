@@ -45,6 +45,10 @@ __global__ void __launch_bounds__(kWalkThreads)
   }
   __syncthreads();
   if (threadIdx.x >= 32) return;
+  // lane t draws position t's uniform up front (off the serial chain)
+  const float u_lane = (T > 0.f && lane < K)
+                           ? philox_uniform(seed, b, lane, kPurposeWalk, cycle)
+                           : 0.f;
 
   int prev = 0;  // row 0 of position 0 is the anchor's row
   for (int t = 0; t < K; ++t) {
@@ -74,7 +78,7 @@ __global__ void __launch_bounds__(kWalkThreads)
         if (lane >= o) cum += n;
       }
       const float tot = __shfl_sync(0xffffffffu, cum, 31);
-      const float u = philox_uniform(seed, b, t, kPurposeWalk, cycle);
+      const float u = __shfl_sync(0xffffffffu, u_lane, t);
       const float thr = u * tot;
       const unsigned above = __ballot_sync(0xffffffffu, lane < kC && cum > thr);
       const unsigned live = __ballot_sync(0xffffffffu, w > 0.f);

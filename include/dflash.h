@@ -233,7 +233,7 @@ dflash_status dflash_philox4x32(const uint32_t* ctr, uint64_t seed,
  * call's stream right before and right after it launches the kernel of
  * `stage`:
  *   0 conv, 1 LM head with top-16 / logsumexp epilogue, 2 top-16 merge,
- *   3 pair score, 4 walk, 5 verify row pass, 6 verify residual / bonus draw.
+ *   3 pair score, 4 walk, 5 verify (row pass, accept tests and draw).
  * Pass NULL for both to stop.  Process-wide host state; set it from the
  * thread that makes the calls, not while other threads call the library.
  * Returns DFLASH_ERR_INVALID_ARG for an unknown stage or a lone NULL. */
