@@ -18,6 +18,7 @@ times the CPU oracle on a bounded sample of the same workload.
 from __future__ import annotations
 
 import argparse
+import datetime
 import json
 import os
 import statistics
@@ -34,6 +35,7 @@ sys.path.insert(0, ROOT)
 import synth  # noqa: E402
 
 C = 16
+GRAPH_STEPS = 100    # cycles captured per CUDA graph in the timed region
 METRIC = ("draft-verify cycles/s and verified tokens/s at B=32,K=8,V=151936;"
           " % HBM/TC roofline")
 UNIT = "cycles/s"
@@ -42,7 +44,7 @@ UNIT = "cycles/s"
 def parse(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=3000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--config", default="b32k8")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
@@ -106,9 +108,11 @@ def peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle sampling while the timed region runs."""
+    """nvidia-smi clock / throttle sampling, started ahead of the timed
+    region; only samples whose own timestamps fall inside [mark_start(),
+    mark_end()] are summarised."""
 
-    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,"
+    QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,"
              "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
              "clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,"
@@ -118,6 +122,7 @@ class ClockSampler:
         self.index = index
         self.proc = None
         self.file = None
+        self.t0 = self.t1 = None
 
     def __enter__(self):
         try:
@@ -126,10 +131,16 @@ class ClockSampler:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index),
                  f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=self.file, stderr=subprocess.DEVNULL)
+                 "-lms", "50"], stdout=self.file, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
         return self
+
+    def mark_start(self):
+        self.t0 = datetime.datetime.now()
+
+    def mark_end(self):
+        self.t1 = datetime.datetime.now()
 
     def __exit__(self, *a):
         if self.proc is not None:
@@ -152,14 +163,17 @@ class ClockSampler:
                  "sw_power_cap"]
         for r in rows:
             r = [x.strip() for x in r]
-            if len(r) < 9:
+            if len(r) < 10:
                 continue
             try:
-                sm.append(float(r[1]))
-                smax.append(float(r[2]))
+                ts = datetime.datetime.strptime(r[0], "%Y/%m/%d %H:%M:%S.%f")
+                if self.t0 and self.t1 and not (self.t0 <= ts <= self.t1):
+                    continue
+                sm.append(float(r[2]))
+                smax.append(float(r[3]))
             except ValueError:
                 continue
-            for n, v in zip(names, r[5:9]):
+            for n, v in zip(names, r[6:10]):
                 if v.lower() == "active":
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None,
@@ -318,57 +332,85 @@ def run_ours(args):
     dv = dv_mod.DraftVerify(w.B, w.K, w.H, w.V, w.r, weights, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    # per-stage events, re-registered every timed step
+    # Warm-up, then the timed region: the K cycles are captured into CUDA
+    # graphs (at most GRAPH_STEPS cycles per graph, each cycle with its own
+    # Philox cycle counter) and replayed, so host launch overhead is not
+    # timed; the work on the device is exactly the eager path's.
     stages = dv_mod.STAGES
     K = args.steps
-
-    def mk():
-        e = torch.cuda.Event(enable_timing=True)
-        e.record(stream)
-        return e
-    ev = [[(mk(), mk()) for _ in stages] for _ in range(K)]
-    torch.cuda.synchronize(dev)
-
     for i in range(args.warmup):
         dv.cycle(h, anchor, L, w.T, seed, i)
     torch.cuda.synchronize(dev)
     dv_mod.dflash_check()
 
-    n_hist = []
+    def capture(first, count):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for i in range(count):
+                dv.cycle(h, anchor, L, w.T, seed, first + i)
+        return g
+
+    clk = ClockSampler(dev.index or 0).__enter__()
+    G = min(K, GRAPH_STEPS)
+    graphs = []
+    use_graph, graph_error = True, ""
+    try:
+        g_full = capture(args.warmup, G)
+        graphs = [g_full] * (K // G)
+        if K % G:
+            graphs.append(capture(args.warmup + (K // G) * G, K % G))
+        graphs[0].replay()            # one untimed replay of the captured work
+        torch.cuda.synchronize(dev)
+    except RuntimeError as exc:       # capture refused: time the eager calls
+        use_graph = False
+        graph_error = str(exc).splitlines()[0][:200]
     t_start = torch.cuda.Event(enable_timing=True)
     t_stop = torch.cuda.Event(enable_timing=True)
     barrier()
     torch.cuda.synchronize(dev)
-    with ClockSampler(dev.index or 0) as clk:
-        t_start.record(stream)
+    clk.mark_start()
+    t_start.record(stream)
+    if use_graph:
+        for g in graphs:
+            g.replay()
+    else:
         for i in range(K):
-            for si in range(len(stages)):
-                dv_mod.dflash_profile_stage(si, ev[i][si][0], ev[i][si][1])
             dv.cycle(h, anchor, L, w.T, seed, args.warmup + i)
-        t_stop.record(stream)
-        torch.cuda.synchronize(dev)
-    for si in range(len(stages)):
-        dv_mod.dflash_profile_stage(si, None, None)
+    t_stop.record(stream)
+    torch.cuda.synchronize(dev)
+    clk.mark_end()
+    clk.__exit__(None, None, None)
     barrier()
     dv_mod.dflash_check()
     secs = t_start.elapsed_time(t_stop) / 1e3
     secs_max = max_over_ranks(secs, dev)
     value, _ = aggregate(K, [secs_max], world)
-    n_last = dv.n.cpu().numpy()
-    n_hist.append(float(n_last.mean()))
+    n_hist = [float(dv.n.cpu().numpy().mean())]
 
+    # per-kernel times: CUDA events the library records around each launch,
+    # on the launching stream, over eager cycles (not part of the timed K)
+    KS = min(K, 20)
+
+    def mk():
+        e = torch.cuda.Event(enable_timing=True)
+        e.record(stream)
+        return e
+    ev = [[(mk(), mk()) for _ in stages] for _ in range(KS)]
+    torch.cuda.synchronize(dev)
+    for i in range(KS):
+        for si in range(len(stages)):
+            dv_mod.dflash_profile_stage(si, ev[i][si][0], ev[i][si][1])
+        dv.cycle(h, anchor, L, w.T, seed, args.warmup + i)
+    torch.cuda.synchronize(dev)
+    for si in range(len(stages)):
+        dv_mod.dflash_profile_stage(si, None, None)
+    dv_mod.dflash_check()
     stage_us = {}
     for si, name in enumerate(stages):
-        ts = []
-        for i in range(K):
-            b, e = ev[i][si]
-            try:
-                ts.append(b.elapsed_time(e) * 1e3)
-            except RuntimeError:
-                ts = []
-                break
-        if ts and (w.conv_sd is not None or name != "conv"):
-            stage_us[name] = statistics.mean(ts)
+        if name == "conv" and w.conv_sd is None:
+            continue
+        stage_us[name] = statistics.mean(
+            ev[i][si][0].elapsed_time(ev[i][si][1]) * 1e3 for i in range(KS))
 
     # roofline of the dominant kernel (the LM head)
     pk = peaks()
@@ -449,6 +491,8 @@ def run_ours(args):
                    "H": w.H, "r": w.r, "T": w.T, "parallelism":
                    f"replicas x{world}",
                    "l2": "inputs larger than L2 (W_lm streamed each cycle)",
+                   "timing": ("CUDA graph replay of the K cycles" if use_graph
+                              else "eager calls: " + graph_error),
                    "recipe": synth.describe(w)},
         "verified_tokens_per_s": value * w.B * (n_mean + 1),
         "mean_accepted": n_mean,

@@ -135,16 +135,20 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
   __shared__ int s_i[kMergeWarps][kC];
   const size_t base = (size_t)m * nstrip;
   const int k = lane < kC ? lane : 31 - lane;  // lanes 16..31: reversed
-  float nv[kMaxPerWarp];
+  float nv[kMaxPerWarp], pm[kMaxPerWarp], ps[kMaxPerWarp];
   int ni[kMaxPerWarp];
 #pragma unroll
-  for (int j = 0; j < kMaxPerWarp; ++j) {
+  for (int j = 0; j < kMaxPerWarp; ++j) {  // every load in flight at once
     const int st = warp + j * kMergeWarps;
     nv[j] = -INFINITY;
     ni[j] = -1;
+    pm[j] = -INFINITY;
+    ps[j] = 0.f;
     if (st < nstrip) {
       nv[j] = P.v[(base + st) * kC + k];
       ni[j] = P.i[(base + st) * kC + k];
+      pm[j] = P.m[base + st];
+      ps[j] = P.s[base + st];
     }
   }
   float tv = -INFINITY;
@@ -154,7 +158,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
   for (int j = 0; j < kMaxPerWarp; ++j) {
     const int st = warp + j * kMergeWarps;
     if (st >= nstrip) break;
-    if (lane == 0) lse_combine(rm, rs, P.m[base + st], P.s[base + st], 1.f);
+    lse_combine(rm, rs, pm[j], ps[j], 1.f);
     const float bv = __shfl_sync(0xffffffffu, nv[j], 0);
     const int bi = __shfl_sync(0xffffffffu, ni[j], 0);
     if (!ranks_ahead(bv, bi, __shfl_sync(0xffffffffu, tv, kC - 1),
