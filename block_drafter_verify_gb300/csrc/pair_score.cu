@@ -81,10 +81,33 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads)
   float* gate = panel + 256 * kPanelStride;     // kRowsPerCta * 256
 
   // ---- phase 1: partial z[row][k] over this CTA's hidden slice ----------
-  for (int i = tid; i < kRows * hs; i += kThreads) {
-    const int rr = i / hs, kk = i % hs;
-    const int m = m0 + rr;
-    hsl[i] = (m < M && kk < klen) ? to_f32(h[(size_t)m * H + k0 + kk]) : 0.f;
+  {  // h slice of the 16 rows: 16-byte loads, a batch issued before use
+    const int vrow = hs / EPV;                 // vectors per row slice
+    constexpr int kBatch = 8;                  // loads in flight per thread
+    for (int i0 = 0; i0 < kRows * vrow; i0 += kBatch * kThreads) {
+      uint4 hv[kBatch];
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int i = i0 + tid + u * kThreads;
+        const int rr = i / vrow, cv = i % vrow;
+        const int m = m0 + rr;
+        hv[u] = (rr < kRows && m < M && cv * EPV < klen)
+                    ? *reinterpret_cast<const uint4*>(h + (size_t)m * H + k0 +
+                                                      cv * EPV)
+                    : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int i = i0 + tid + u * kThreads;
+        const int rr = i / vrow, cv = i % vrow;
+        if (rr < kRows) {
+          float f[EPV];
+          Vec16<T>::to_f32(hv[u], f);
+#pragma unroll
+          for (int e = 0; e < EPV; ++e) hsl[rr * hs + cv * EPV + e] = f[e];
+        }
+      }
+    }
   }
   float acc[kRows];
 #pragma unroll
@@ -176,22 +199,36 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads)
     float* eout_s = panel + kC * rs;  // [16][rs], scaled by the gate
     const int vpr = (r + EPV - 1) / EPV;  // vectors per embedding row
     if (r % EPV == 0) {
-      for (int i = tid; i < 2 * kC * vpr; i += kThreads) {
-        const int tab = i / (kC * vpr), rem = i % (kC * vpr);
-        const int row = rem / vpr, cv = rem % vpr;
-        const int tok = tab == 0 ? s_pred[row] : s_cand[row];
-        float f[EPV];
-        if (tok >= 0) {
-          const T* src = (tab == 0 ? e_in : e_out) + (size_t)tok * r + cv * EPV;
-          Vec16<T>::to_f32(*reinterpret_cast<const uint4*>(src), f);
-        } else {
-  #pragma unroll
-          for (int e = 0; e < EPV; ++e) f[e] = 0.f;
+      // 2 tables x 16 rows x vpr vectors: every load issued before any use
+      constexpr int kMaxE =
+          (2 * kC * DFLASH_MAX_RANK / 4 + kThreads - 1) / kThreads;
+      uint4 ev[kMaxE];
+#pragma unroll
+      for (int u = 0; u < kMaxE; ++u) {
+        const int i = tid + u * kThreads;
+        ev[u] = make_uint4(0, 0, 0, 0);
+        if (i < 2 * kC * vpr) {
+          const int tab = i / (kC * vpr), rem = i % (kC * vpr);
+          const int row = rem / vpr, cv = rem % vpr;
+          const int tok = tab == 0 ? s_pred[row] : s_cand[row];
+          if (tok >= 0)
+            ev[u] = *reinterpret_cast<const uint4*>(
+                (tab == 0 ? e_in : e_out) + (size_t)tok * r + cv * EPV);
         }
-        float* dst = (tab == 0 ? ein_s : eout_s) + row * rs + cv * EPV;
-  #pragma unroll
-        for (int e = 0; e < EPV; ++e)
-          dst[e] = tab == 0 ? f[e] : f[e] * g_row[cv * EPV + e];
+      }
+#pragma unroll
+      for (int u = 0; u < kMaxE; ++u) {
+        const int i = tid + u * kThreads;
+        if (i < 2 * kC * vpr) {
+          const int tab = i / (kC * vpr), rem = i % (kC * vpr);
+          const int row = rem / vpr, cv = rem % vpr;
+          float f[EPV];
+          Vec16<T>::to_f32(ev[u], f);
+          float* dst = (tab == 0 ? ein_s : eout_s) + row * rs + cv * EPV;
+#pragma unroll
+          for (int e = 0; e < EPV; ++e)
+            dst[e] = tab == 0 ? f[e] : f[e] * g_row[cv * EPV + e];
+        }
       }
     } else {
       for (int i = tid; i < kC * r; i += kThreads) {

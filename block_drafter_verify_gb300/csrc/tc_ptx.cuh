@@ -89,6 +89,18 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* m,
       : "memory");
 }
 
+// Bulk (non-tensor) copy of `bytes` (a multiple of 16, both addresses
+// 16-byte aligned) from global to this CTA's shared memory; completion is
+// signalled on `bar` as transaction bytes.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src,
+                                          uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes "
+      "[%0], [%1], %2, [%3];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // ---- TMEM -----------------------------------------------------------------
 __device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
   asm volatile(

@@ -7,10 +7,12 @@
 // One launch, grid (B*(K+1) target rows, chunks of each row), 256 threads:
 //   main pass   a CTA walks its chunk in blocks of 16384 tokens; warp w of
 //               the CTA owns the contiguous 2048-token segment w of each
-//               block (lane l: 16-byte loads at 4l + 128u, u < 16).  At
-//               T > 0 a warp reduces its segment to (max, sum 2^((x-max)/T
-//               log2 e)) with one max shuffle and one sum shuffle, and
-//               writes that pair; at T = 0 the CTA keeps the first argmax.
+//               block and streams its segments through a 3-stage ring of
+//               8 KB bulk async copies in shared memory (lane l reads the
+//               16-byte words 4l + 128u, u < 16).  At T > 0 a warp reduces
+//               a segment to (max, sum 2^((x-max)/T log2 e)) with one max
+//               shuffle and one sum shuffle and writes that pair; at T = 0
+//               the CTA keeps the first argmax.
 //   row fold    the last CTA to finish a row folds the row's segment pairs
 //               (or chunk argmaxes) in a fixed tree: row max, Z, argmax.
 //   accept      the last row of a sequence to finish runs the K accept tests
@@ -26,6 +28,7 @@
 #include <algorithm>
 
 #include "kernels.h"
+#include "tc_ptx.cuh"
 
 namespace dflash {
 namespace {
@@ -35,6 +38,10 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kSegTokens = 2048;                 // one warp's segment
 constexpr int kBlockTokens = kWarps * kSegTokens;  // 16384
 constexpr float kLog2e = 1.4426950408889634f;
+// Bulk-copy ring of the main pass: kStages segment copies in flight per warp.
+constexpr int kStages = 3;
+constexpr size_t kRingBytes = (size_t)kWarps * kStages * kSegTokens * 4;
+constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s: far beyond any real wait
 
 __device__ __forceinline__ float ex2f(float x) {
   float y;
@@ -109,14 +116,60 @@ __global__ void __launch_bounds__(kThreads)
   __shared__ float s_qz[kC], s_corr[kC];
 
   // ---- main pass ------------------------------------------------------
+  // Segments of this chunk: sc0 .. sc1-1; warp w takes sc0 + w + 8 j.  With
+  // 16-byte aligned rows (vec4) each warp streams its segments through a
+  // ring of kStages bulk copies in shared memory, so copies stay in flight
+  // while it computes; otherwise it loads into registers directly.
+  extern __shared__ float4 ring4[];
+  __shared__ uint64_t s_bar[kWarps][kStages];
+  __shared__ int s_abort;
   bool bad = false;
   float ga = -INFINITY;   // T = 0: this thread's best value ...
   int gi = 0x7fffffff;    // ... and its (first) index
-  for (int blk = 0; blk < bpc; ++blk) {
-    const int base = (c * bpc + blk) * kBlockTokens + wid * kSegTokens;
-    if (base >= V) break;
+  const int sc0 = c * bpc * kWarps;
+  const int sc1 = min(nseg, (c + 1) * bpc * kWarps);
+  const int nmine = sc0 + wid < sc1 ? (sc1 - (sc0 + wid) + kWarps - 1) / kWarps : 0;
+  float* ring = reinterpret_cast<float*>(ring4) + (size_t)wid * kStages * kSegTokens;
+  if (vec4) {
+    if (tid == 0) s_abort = 0;
+    if (lane == 0) {
+      for (int st = 0; st < kStages; ++st) tc::mbar_init(&s_bar[wid][st], 1);
+      tc::fence_mbar_init();
+    }
+    __syncthreads();
+  }
+  auto issue = [&](int j) {  // lane 0: copy segment j of this warp
+    const int base = (sc0 + wid + kWarps * j) * kSegTokens;
+    const int st = j % kStages;
+    const uint32_t bytes = (uint32_t)min(kSegTokens, V - base) * 4u;
+    // the warp's earlier reads of this stage come before the copy's writes
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    tc::mbar_arrive_expect_tx(&s_bar[wid][st], bytes);
+    tc::bulk_load(ring + st * kSegTokens, x + base, bytes, &s_bar[wid][st]);
+  };
+  if (vec4 && lane == 0)
+    for (int j = 0; j < min(kStages, nmine); ++j) issue(j);
+  for (int j = 0; j < nmine; ++j) {
+    const int base = (sc0 + wid + kWarps * j) * kSegTokens;
     float4 f[16];
-    load_segment(x, base, V, lane, vec4, f);
+    if (vec4) {
+      const int st = j % kStages;
+      const bool got = tc::mbar_wait_bounded(&s_bar[wid][st], (j / kStages) & 1,
+                                             &s_abort, kWaitNs);
+      if (!got && lane == 0) raise_error(err, kErrTimeout);
+      const float* seg = ring + st * kSegTokens;
+#pragma unroll
+      for (int u = 0; u < 16; ++u) {
+        const int i = 4 * lane + 128 * u;
+        f[u] = base + i < V
+                   ? *reinterpret_cast<const float4*>(seg + i)
+                   : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+      }
+      __syncwarp();  // every lane has read the stage: refill it
+      if (lane == 0 && j + kStages < nmine) issue(j + kStages);
+    } else {
+      load_segment(x, base, V, lane, vec4, f);
+    }
     if (greedy) {
       float chk = 0.f;
 #pragma unroll
@@ -460,17 +513,26 @@ cudaError_t launch_verify(const float* L, const int* draft, const int* topi,
                           int* err, cudaStream_t s) {
   const int rows = B * (K + 1);
   const int blocks_per_row = (V + kBlockTokens - 1) / kBlockTokens;
-  // chunks of whole 16384-token blocks: about four CTAs per SM in total,
-  // at most kVerifyMaxChunks per row
+  const int vec4 = (V % 4 == 0) && ((reinterpret_cast<uintptr_t>(L) & 15) == 0);
+  // chunks of whole 16384-token blocks: about two CTAs per SM in total with
+  // the shared-memory ring (one CTA fits an SM), four without; at most
+  // kVerifyMaxChunks per row
+  const long long per_sm = vec4 ? 2 : 4;
   const long long total_blocks = (long long)rows * blocks_per_row;
   int bpc = (int)std::max<long long>(
-      1, (total_blocks + 4LL * num_sms - 1) / (4LL * num_sms));
+      1, (total_blocks + per_sm * num_sms - 1) / (per_sm * num_sms));
   bpc = std::max(bpc, (blocks_per_row + kVerifyMaxChunks - 1) / kVerifyMaxChunks);
   bpc = std::min(bpc, blocks_per_row);
   const int nchunk = (blocks_per_row + bpc - 1) / bpc;
-  const int vec4 = (V % 4 == 0) && ((reinterpret_cast<uintptr_t>(L) & 15) == 0);
   const float s2 = T > 0.f ? kLog2e / T : 0.f;
-  verify_kernel<<<dim3(rows, nchunk), kThreads, 0, s>>>(
+  const size_t smem = vec4 ? kRingBytes : 0;
+  if (vec4) {
+    const cudaError_t e = cudaFuncSetAttribute(
+        verify_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        (int)kRingBytes);
+    if (e != cudaSuccess) return e;
+  }
+  verify_kernel<<<dim3(rows, nchunk), kThreads, smem, s>>>(
       L, draft, topi, q, B, K, V, nchunk, bpc, T, s2, seed, cycle, n_accepted,
       out_tok, ws, err, vec4);
   return cudaGetLastError();

@@ -112,6 +112,7 @@ def test_tiny_fp32(lib, name, T):
     (2, 16, 256, 3000, 256, 0.7),
     (4, 1, 64, 777, 16, 1.0),       # K = 1
     (9, 3, 128, 2051, 32, 1.5),     # M not a multiple of 8
+    (5, 3, 200, 1999, 48, 1.0),     # H not a multiple of 64 (ragged K tail)
 ])
 def test_small_bf16(lib, B, K, H, V, r, T):
     w = synth.Workload("small", B=B, K=K, V=V, H=H, r=r, dtype="bf16", T=T,
