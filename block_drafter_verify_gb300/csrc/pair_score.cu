@@ -6,9 +6,12 @@
 // gate of h_t — no backbone or LM-head pass.
 //
 // One launch, no scratch memory: a cluster of 8 CTAs owns 16 rows (b, t).
-//   1. gate pre-activations: CTA k of the cluster computes z = W_g h for the
-//      16 rows over its eighth of the hidden dimension (W_g staged through
-//      shared memory in 64-column panels with 16-byte loads and stores);
+//   1. gate pre-activations z = W_g h of the 16 rows over this CTA's eighth
+//      of the hidden dimension.  bf16 storage: the h rows and W_g rows are
+//      staged unconverted with cp.async (zero-filled past the slice) and
+//      contracted on the tensor cores (mma.sync m16n8k16, bf16 x bf16 ->
+//      fp32; warp w owns gate columns 32w .. 32w+31).  fp32 storage: exact
+//      fp32 products on the CUDA cores, W_g staged in 64-column panels;
 //   2. the partial sums are added over the cluster through distributed
 //      shared memory, in cluster-rank order, and CTA k keeps the gates
 //      g = sigmoid(z) of rows 2k and 2k+1;
@@ -16,6 +19,9 @@
 //      rows of E_out (scaled by g) and writes the 16 x 16 scores of each of
 //      its two rows.
 #include <cooperative_groups.h>
+
+#include <algorithm>
+#include <type_traits>
 
 #include "kernels.h"
 
@@ -28,8 +34,16 @@ constexpr int kCluster = 8;     // CTAs per cluster (split of the hidden dim)
 constexpr int kRows = 16;       // rows (b, t) per cluster
 constexpr int kRowsPerCta = kRows / kCluster;
 constexpr int kThreads = 256;
-constexpr int kPanel = 64;           // W_g columns per staged panel
+constexpr int kPanel = 64;           // fp32 path: W_g columns per panel
 constexpr int kPanelStride = kPanel + 4;  // 16-byte rows, no bank conflicts
+constexpr int kKP = 128;             // bf16 path: hidden columns per panel
+constexpr int kLdsB = kKP + 8;       // padded bf16 row: conflict-free reads
+
+// Shared memory of phase 1, in floats (phase 3 reuses the same region).
+__host__ __device__ constexpr size_t work_floats(int hs, bool bf16) {
+  return bf16 ? (size_t)(kRows + 256) * kLdsB / 2
+              : (size_t)kRows * hs + (size_t)256 * kPanelStride;
+}
 
 // 16-byte vector of storage elements converted to fp32.
 template <typename T>
@@ -55,32 +69,103 @@ __device__ __forceinline__ void Vec16<__nv_bfloat16>::to_f32(const uint4& u,
   }
 }
 
-template <typename T>
-__global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads)
-    pair_score_kernel(const float* __restrict__ topv,
-                      const int* __restrict__ topi,
-                      const int* __restrict__ anchor, const T* __restrict__ h,
-                      const T* __restrict__ w_gate, const T* __restrict__ e_in,
-                      const T* __restrict__ e_out, int B, int K, int H, int V,
-                      int r, int hs, float* __restrict__ scores, int* err) {
-  constexpr int EPV = Vec16<T>::N;            // elements per 16-byte vector
-  constexpr int VPR = kPanel / EPV;           // vectors per panel row
-  extern __shared__ float4 smem4[];
-  float* smem = reinterpret_cast<float*>(smem4);
-  cg::cluster_group cluster = cg::this_cluster();
-  const int crank = (int)cluster.block_rank();
+// 16-byte asynchronous copy global -> shared; src_bytes = 0 writes zeros.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src,
+                                           int src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(
+                   static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
+               "l"(src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
+// D += A B for one 16 x 8 x 16 tile, bf16 inputs, fp32 accumulators.
+__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0,
+                                          uint32_t a1, uint32_t a2,
+                                          uint32_t a3, uint32_t b0,
+                                          uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+      "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t ld_b32(const __nv_bfloat16* p) {
+  return *reinterpret_cast<const uint32_t*>(p);
+}
+
+// Phase 1, bf16 storage: part[row][n] = sum over this CTA's slice of
+// h[m0 + row][k] * W_g[n][k], on the tensor cores.  The slice length is a
+// multiple of 8 (H is), so every 16-byte copy is either whole or skipped.
+__device__ __forceinline__ void gate_partial_mma(
+    const __nv_bfloat16* __restrict__ h, const __nv_bfloat16* __restrict__ w,
+    int M, int H, int r, int m0, int k0, int klen, float* part, float* work) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g = lane >> 2, c = lane & 3;
+  __nv_bfloat16* hs_ = reinterpret_cast<__nv_bfloat16*>(work);  // [16][kLdsB]
+  __nv_bfloat16* ws_ = hs_ + kRows * kLdsB;                      // [256][kLdsB]
+  float acc[4][4];
+#pragma unroll
+  for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
+  constexpr int kChunks = kKP / 8;  // 16-byte chunks per staged row
+  for (int p0 = 0; p0 < klen; p0 += kKP) {
+    const int pw = min(kKP, klen - p0);
+    __syncthreads();  // the previous panel is consumed
+    for (int i = tid; i < kRows * kChunks; i += kThreads) {
+      const int row = i / kChunks, ch = i % kChunks;
+      const bool ok = m0 + row < M && ch * 8 < pw;
+      cp_async16(hs_ + row * kLdsB + ch * 8,
+                 ok ? h + (size_t)(m0 + row) * H + k0 + p0 + ch * 8 : h,
+                 ok ? 16 : 0);
+    }
+    for (int i = tid; i < 256 * kChunks; i += kThreads) {
+      const int n = i / kChunks, ch = i % kChunks;
+      const bool ok = n < r && ch * 8 < pw;
+      cp_async16(ws_ + n * kLdsB + ch * 8,
+                 ok ? w + (size_t)n * H + k0 + p0 + ch * 8 : w, ok ? 16 : 0);
+    }
+    cp_async_wait_all();
+    __syncthreads();
+    const int ksteps = (pw + 15) / 16;  // columns past pw are zeros
+    for (int kk = 0; kk < ksteps; ++kk) {
+      const int kc = kk * 16 + 2 * c;
+      const uint32_t a0 = ld_b32(hs_ + g * kLdsB + kc);
+      const uint32_t a1 = ld_b32(hs_ + (g + 8) * kLdsB + kc);
+      const uint32_t a2 = ld_b32(hs_ + g * kLdsB + kc + 8);
+      const uint32_t a3 = ld_b32(hs_ + (g + 8) * kLdsB + kc + 8);
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt) {
+        const __nv_bfloat16* wr = ws_ + ((warp * 4 + nt) * 8 + g) * kLdsB + kc;
+        mma_16816(acc[nt], a0, a1, a2, a3, ld_b32(wr), ld_b32(wr + 8));
+      }
+    }
+  }
+#pragma unroll
+  for (int nt = 0; nt < 4; ++nt) {
+    const int n = (warp * 4 + nt) * 8 + 2 * c;
+    part[g * 256 + n] = acc[nt][0];
+    part[g * 256 + n + 1] = acc[nt][1];
+    part[(g + 8) * 256 + n] = acc[nt][2];
+    part[(g + 8) * 256 + n + 1] = acc[nt][3];
+  }
+}
+
+// Phase 1, fp32 storage: exact fp32 products on the CUDA cores.
+__device__ __forceinline__ void gate_partial_simt(
+    const float* __restrict__ h, const float* __restrict__ w_gate, int M,
+    int H, int r, int m0, int k0, int klen, int hs, float* part,
+    float* work) {
+  using T = float;
+  constexpr int EPV = 4;               // elements per 16-byte vector
+  constexpr int VPR = kPanel / EPV;    // vectors per panel row
   const int tid = threadIdx.x;
-  const int M = B * K;
-  const int m0 = (blockIdx.x / kCluster) * kRows;
-  const int k0 = crank * hs, k1 = min(H, k0 + hs);
-  const int klen = max(0, k1 - k0);
-
-  float* part = smem;                           // kRows * 256
-  float* hsl = part + kRows * 256;              // kRows * hs
-  float* panel = hsl + kRows * hs;              // 256 * kPanelStride
-  float* gate = panel + 256 * kPanelStride;     // kRowsPerCta * 256
-
-  // ---- phase 1: partial z[row][k] over this CTA's hidden slice ----------
+  float* hsl = work;                   // kRows * hs
+  float* panel = hsl + kRows * hs;     // 256 * kPanelStride
   {  // h slice of the 16 rows: 16-byte loads, a batch issued before use
     const int vrow = hs / EPV;                 // vectors per row slice
     constexpr int kBatch = 8;                  // loads in flight per thread
@@ -159,6 +244,36 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads)
 #pragma unroll
     for (int rr = 0; rr < kRows; ++rr) part[rr * 256 + tid] = acc[rr];
   }
+}
+
+template <typename T>
+__global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads)
+    pair_score_kernel(const float* __restrict__ topv,
+                      const int* __restrict__ topi,
+                      const int* __restrict__ anchor, const T* __restrict__ h,
+                      const T* __restrict__ w_gate, const T* __restrict__ e_in,
+                      const T* __restrict__ e_out, int B, int K, int H, int V,
+                      int r, int hs, float* __restrict__ scores, int* err) {
+  constexpr int EPV = Vec16<T>::N;            // elements per 16-byte vector
+  extern __shared__ float4 smem4[];
+  float* smem = reinterpret_cast<float*>(smem4);
+  cg::cluster_group cluster = cg::this_cluster();
+  const int crank = (int)cluster.block_rank();
+  const int tid = threadIdx.x;
+  const int M = B * K;
+  const int m0 = (blockIdx.x / kCluster) * kRows;
+  const int k0 = crank * hs, k1 = min(H, k0 + hs);
+  const int klen = max(0, k1 - k0);
+
+  float* part = smem;                           // kRows * 256
+  float* gate = part + kRows * 256;             // kRowsPerCta * 256
+  float* work = gate + kRowsPerCta * 256;       // phase 1, then phase 3
+
+  // ---- phase 1: partial z[row][k] over this CTA's hidden slice ----------
+  if constexpr (std::is_same<T, __nv_bfloat16>::value)
+    gate_partial_mma(h, w_gate, M, H, r, m0, k0, klen, part, work);
+  else
+    gate_partial_simt(h, w_gate, M, H, r, m0, k0, klen, hs, part, work);
   cluster.sync();
 
   // ---- phase 2: add the 8 slices (rank order) for this CTA's two rows ---
@@ -195,8 +310,8 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads)
     }
     __syncthreads();
     const int rs = r + 1;  // padded row stride
-    float* ein_s = panel;             // [16][rs]
-    float* eout_s = panel + kC * rs;  // [16][rs], scaled by the gate
+    float* ein_s = work;              // [16][rs]
+    float* eout_s = work + kC * rs;   // [16][rs], scaled by the gate
     const int vpr = (r + EPV - 1) / EPV;  // vectors per embedding row
     if (r % EPV == 0) {
       // 2 tables x 16 rows x vpr vectors: every load issued before any use
@@ -262,9 +377,11 @@ cudaError_t launch_pair_score(const float* topv, const int* topi,
   const int M = B * K;
   // hidden slice per cluster rank, a multiple of 8 so 16-byte loads align
   const int hs = ((H + kCluster - 1) / kCluster + 7) & ~7;
-  const size_t smem = ((size_t)kRows * 256 + (size_t)kRows * hs +
-                       (size_t)256 * kPanelStride + kRowsPerCta * 256) *
-                      sizeof(float);
+  const size_t work =
+      std::max(work_floats(hs, std::is_same<T, __nv_bfloat16>::value),
+               (size_t)2 * kC * (DFLASH_MAX_RANK + 1));
+  const size_t smem =
+      ((size_t)kRows * 256 + (size_t)kRowsPerCta * 256 + work) * sizeof(float);
   cudaError_t e = cudaFuncSetAttribute(
       pair_score_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
       (int)smem);

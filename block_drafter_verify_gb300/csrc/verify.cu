@@ -110,7 +110,7 @@ __global__ void __launch_bounds__(kThreads)
 
   __shared__ float s_a[kWarps], s_s[kWarps];
   __shared__ int s_i[kWarps];
-  __shared__ int s_flag, s_n, s_seg, s_lastpos, s_use_raw;
+  __shared__ int s_flag, s_n, s_seg, s_use_raw;
   __shared__ float s_W[64], s_rem;
   __shared__ int s_ci[kC];
   __shared__ float s_qz[kC], s_corr[kC];
@@ -342,75 +342,74 @@ __global__ void __launch_bounds__(kThreads)
     s_corr[tid] = corr;
   }
   __syncthreads();
-  // Segment weights of row n, 64 segments per group: thread k < 64 turns
-  // the pair of segment k0 + k into sum_v 2^((x_v - m) s2); thread 0 then
-  // applies the candidates' residual corrections in candidate order and
-  // either adds the group to the total (locate == false) or walks it to
-  // find the segment holding theta.  Every loop bound and exit flag below
-  // is the same for all threads.
-  const float u = philox_uniform(seed, b, K, kPurposeResample, cycle);
-  auto group = [&](int k0, bool raw, bool locate, float& acc, float theta) {
-    if (tid < 64) {
-      const int k = k0 + tid;
-      float w = 0.f;
-      if (k < nseg) {
-        const float2 p = __ldcg(&ws.part[(size_t)rn * nseg + k]);
-        w = (p.x == -INFINITY) ? 0.f : p.y * ex2f((p.x - m) * s2);
-      }
-      s_W[tid] = w;
-    }
-    __syncthreads();
-    if (tid == 0) {
-      const int kn = min(64, nseg - k0);
+  // Warp 0 locates the segment holding the draw.  Lane l owns the
+  // contiguous segments l*per .. l*per+per-1; a segment's weight is its
+  // (max, sum) pair rescaled to the row max, plus the corrections of the
+  // candidates inside it (in candidate order), clamped at zero.  One
+  // inclusive scan of the lane totals and one ballot find the lane, which
+  // walks its segments.  A zero residual total switches to p itself.
+  if (wid == 0) {
+    const int per = (nseg + 31) / 32;
+    const float u = philox_uniform(seed, b, K, kPurposeResample, cycle);
+    auto seg_weight = [&](int k, bool raw) -> float {
+      if (k >= nseg) return 0.f;
+      const float2 p = __ldcg(&ws.part[(size_t)rn * nseg + k]);
+      float w = (p.x == -INFINITY) ? 0.f : p.y * ex2f((p.x - m) * s2);
       if (!raw) {
-        for (int j = 0; j < kC; ++j) {
-          const int cj = s_ci[j];
-          const int k = cj / kSegTokens - k0;
-          if (cj >= 0 && k >= 0 && k < kn) s_W[k] += s_corr[j];
-        }
+#pragma unroll
+        for (int j = 0; j < kC; ++j)
+          if (s_ci[j] >= 0 && s_ci[j] / kSegTokens == k) w += s_corr[j];
       }
-      for (int k = 0; k < kn; ++k) {
-        const float w = fmaxf(s_W[k], 0.f);
-        if (!locate) {
-          acc += w;
-        } else if (s_seg < 0) {
-          if (w > 0.f) s_lastpos = k0 + k;
+      return fmaxf(w, 0.f);
+    };
+    int f_seg = -1, f_raw = 0;
+    float f_rem = 0.f;
+    for (int raw = 0; raw < 2 && f_seg < 0; ++raw) {
+      float ltot = 0.f;
+#pragma unroll 4
+      for (int i = 0; i < per; ++i) ltot += seg_weight(lane * per + i, raw);
+      float incl = ltot;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+      }
+      const float total = __shfl_sync(0xffffffffu, incl, 31);
+      if (!(total > 0.f)) continue;  // degenerate residual: draw from p
+      const float theta = u * total;
+      const unsigned hit = __ballot_sync(0xffffffffu, ltot > 0.f && incl > theta);
+      const unsigned live = __ballot_sync(0xffffffffu, ltot > 0.f);
+      // u * total rounded up to the total: the last lane with weight
+      const int L = hit ? __ffs(hit) - 1 : 31 - __clz(live);
+      if (lane == L) {
+        float acc = incl - ltot;
+        int last = -1;
+        for (int i = 0; i < per; ++i) {
+          const float w = seg_weight(lane * per + i, raw);
+          if (w > 0.f) last = lane * per + i;
           if (w > 0.f && acc + w > theta) {
-            s_seg = k0 + k;
-            s_rem = theta - acc;
-          } else {
-            acc += w;
+            f_seg = lane * per + i;
+            f_rem = theta - acc;
+            break;
           }
+          acc += w;
+        }
+        if (f_seg < 0) {
+          f_seg = last;
+          f_rem = INFINITY;
         }
       }
+      f_seg = __shfl_sync(0xffffffffu, f_seg, L);
+      f_rem = __shfl_sync(0xffffffffu, f_rem, L);
+      f_raw = raw;
     }
-    __syncthreads();
-  };
-  if (tid == 0) { s_seg = -1; s_lastpos = -1; s_use_raw = 0; }
-  for (int raw = 0; raw < 2; ++raw) {
-    float total = 0.f;  // meaningful in thread 0
-    for (int k0 = 0; k0 < nseg; k0 += 64) group(k0, raw, false, total, 0.f);
-    if (tid == 0) {
-      s_rem = total;  // broadcast the total
-      s_use_raw = raw;
+    if (lane == 0) {
+      s_seg = f_seg;
+      s_rem = f_rem;
+      s_use_raw = f_raw;
     }
-    __syncthreads();
-    const float tot = s_rem;
-    __syncthreads();
-    if (!(tot > 0.f)) continue;  // degenerate residual: draw from p
-    float cum = 0.f;
-    const float theta = u * tot;
-    for (int k0 = 0; k0 < nseg; k0 += 64) {
-      group(k0, raw, true, cum, theta);
-      if (s_seg >= 0) break;
-    }
-    if (s_seg < 0 && tid == 0) {  // u * total rounded up to the total:
-      s_seg = s_lastpos;          // the last segment with weight, whose
-      s_rem = INFINITY;           // last weighted token is then drawn
-    }
-    __syncthreads();
-    break;
   }
+  __syncthreads();
   int seg = s_seg;
   if (seg < 0) {  // cannot happen: the row maximum has weight 1
     if (tid == 0) raise_error(err, kErrBadIndex);
