@@ -131,7 +131,7 @@ dflash_status lmhead_bf16(const __nv_bfloat16* h, const __nv_bfloat16* conv_w,
   }
   CUtensorMap my, mw;
   if (!make_tmap_bf16_2d(&my, a, H, M, 64, 128) ||
-      !make_tmap_bf16_2d(&mw, w_lm, H, V, 64, 256))
+      !make_tmap_bf16_2d(&mw, w_lm, H, V, 64, lmhead_tc_pairs(M) ? 128 : 256))
     return DFLASH_ERR_CUDA;
   int strips = 0;
   {

@@ -23,12 +23,14 @@ bool make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner,
 cudaError_t launch_conv_tc(const CUtensorMap& map_h, const CUtensorMap& map_wc,
                            const __nv_bfloat16* h, int B, int K, int H,
                            __nv_bfloat16* y, int* err, cudaStream_t s);
-// map_y: y [M, H] box {64, 128}; map_w: w_lm [V, H] box {64, 256}.
+// map_y: y [M, H] box {64, 128}; map_w: w_lm [V, H] box {64, 256}, or
+// {64, 128} when lmhead_tc_pairs(M) (CTA pairs, two or more row tiles).
 // Writes `*strips` partial lists per row.
 cudaError_t launch_lmhead_tc(const CUtensorMap& map_y, const CUtensorMap& map_w,
                              int M, int H, int V, int num_sms, TopkPartials P,
                              int* err, int* strips, cudaStream_t s);
-int lmhead_tc_grid(int M, int V, int num_sms, int* row_tiles, int* strips);
+bool lmhead_tc_pairs(int M);
+int lmhead_tc_grid(int M, int V, int num_sms, int* row_groups, int* strips);
 
 // lmhead_simt.cu ----------------------------------------------------------
 template <typename T>

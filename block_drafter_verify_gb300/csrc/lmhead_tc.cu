@@ -7,20 +7,31 @@
 // Parallel): U_t is the drafter's own logit; 16 candidates are kept per slot.
 //
 // Persistent kernel, one CTA per SM, 192 threads:
-//   warp 0      TMA producer: y tile [128 x 64] and W tile [256 x 64] per
-//               stage, 4 stages, 128-byte swizzle;
-//   warp 1      MMA issuer (one thread): tcgen05.mma M=128 N=256 K=16 into
-//               one of two TMEM accumulators (2 x 256 fp32 columns);
+//   warp 0      TMA producer: y tile [128 x 64] and W tile per stage,
+//               128-byte swizzle;
+//   warp 1      MMA issuer (one thread): tcgen05.mma N=256 K=16 into one of
+//               two TMEM accumulators (2 x 256 fp32 columns);
 //   warps 2-5   epilogue: thread = one row (TMEM lane), reads 32 columns at
 //               a time with tcgen05.ld, folds them into (max, sum exp) and a
 //               register-resident sorted top-16, while the MMA fills the
 //               other accumulator.
-// CTA c owns row tile (c mod row_tiles) and the vocab tiles strip, strip +
-// strips, ... (strip = c / row_tiles), so the CTAs that share a vocab tile
-// run it at the same time and W_lm is read from HBM about once.  Each CTA
-// writes one top-16 / (max, sum) partial per row; topk_merge folds them.
-// Every wait is time-bounded; on a timeout the CTA stops issuing, drains
-// its copies and MMAs, frees TMEM, flags the error word and exits.
+// Two variants:
+//   single  (one row tile, M <= 128): W tile [256 x 64] per stage, 4 stages,
+//           M=128 MMAs (cta_group::1);
+//   pair    (two or more row tiles): a cluster of two CTAs computes the rows
+//           of two row tiles against one W tile with M=256 MMAs
+//           (cta_group::2).  Each CTA loads its own y tile and one half
+//           [128 x 64] of the W tile, so W crosses L2 -> SM once per pair
+//           instead of once per row tile and a stage is 32 KB: 6 stages.
+//           The even CTA issues the MMAs; its full barriers count both
+//           CTAs' copies, and its commits arrive on both CTAs' barriers.
+// Unit u (a CTA, or a pair) owns row group (u mod row_groups) and the vocab
+// tiles strip, strip + strips, ... (strip = u / row_groups), so the units
+// that share a vocab tile run it at the same time and W_lm is read from HBM
+// about once.  Each CTA writes one top-16 / (max, sum) partial per row;
+// topk_merge folds them.  Every wait is time-bounded; on a timeout the CTA
+// stops issuing, drains its copies and MMAs, frees TMEM, flags the error
+// word and exits.
 #include <algorithm>
 
 #include "kernels.h"
@@ -29,28 +40,39 @@
 namespace dflash {
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr int BM = 128, BN = 256, BK = 64;
 constexpr int A_BYTES = BM * BK * 2;  // 16 KB
-constexpr int B_BYTES = BN * BK * 2;  // 32 KB
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int THREADS = 192;
 constexpr uint32_t TMEM_COLS = 2 * BN;
 constexpr uint64_t WAIT_NS = 2000000000ull;  // 2 s: far beyond any real wait
 constexpr float LOG2E = 1.4426950408889634f;
 
+template <bool kPair>
+struct Cfg {
+  static constexpr int STAGES = kPair ? 6 : 4;
+  static constexpr int B_ROWS = kPair ? BN / 2 : BN;  // W rows per CTA
+  static constexpr int B_BYTES = B_ROWS * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int CTAS = kPair ? 2 : 1;
+};
+
+template <int STAGES>
 struct Bars {
-  uint64_t full[STAGES];
+  uint64_t full[STAGES];   // pair: only the even CTA's are used
   uint64_t empty[STAGES];
   uint64_t tfull[2];
-  uint64_t tempty[2];
+  uint64_t tempty[2];      // pair: only the even CTA's are used
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
 };
 constexpr int XS_STRIDE = 33;  // padded row of the per-thread chunk stage
 constexpr size_t XS_BYTES = 4 * 32 * XS_STRIDE * sizeof(float);
-constexpr size_t SMEM_BYTES =
-    1024 + (size_t)STAGES * STAGE_BYTES + sizeof(Bars) + XS_BYTES;
+template <bool kPair>
+constexpr size_t smem_bytes() {
+  return 1024 + (size_t)Cfg<kPair>::STAGES * Cfg<kPair>::STAGE_BYTES +
+         ((sizeof(Bars<Cfg<kPair>::STAGES>) + 15) & ~size_t(15)) + XS_BYTES;
+}
 
 __device__ __forceinline__ bool wait_timeout(uint64_t* bar, uint32_t parity) {
   int never = 0;
@@ -110,21 +132,31 @@ __device__ __forceinline__ unsigned epilogue_chunk(float (&x)[32], int col0,
   return mask;
 }
 
+template <bool kPair>
 __global__ void __launch_bounds__(THREADS, 1)
     lmhead_tc_kernel(const __grid_constant__ CUtensorMap map_y,
                      const __grid_constant__ CUtensorMap map_w, int M, int H,
-                     int V, int row_tiles, int strips, TopkPartials P,
+                     int V, int row_groups, int strips, TopkPartials P,
                      int* err) {
+  using C = Cfg<kPair>;
+  constexpr int STAGES = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sa = smem;
   uint8_t* sb = smem + STAGES * A_BYTES;
-  Bars* bars = reinterpret_cast<Bars*>(smem + STAGES * STAGE_BYTES);
-  float* xs_all = reinterpret_cast<float*>(smem + STAGES * STAGE_BYTES +
-                                           ((sizeof(Bars) + 15) & ~size_t(15)));
+  Bars<STAGES>* bars =
+      reinterpret_cast<Bars<STAGES>*>(smem + STAGES * C::STAGE_BYTES);
+  float* xs_all = reinterpret_cast<float*>(
+      smem + STAGES * C::STAGE_BYTES +
+      ((sizeof(Bars<STAGES>) + 15) & ~size_t(15)));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int mtile = blockIdx.x % row_tiles, strip = blockIdx.x / row_tiles;
+  // a pair is a cluster of two consecutive blocks; rank 0 leads
+  const int rank = kPair ? (int)(blockIdx.x & 1) : 0;
+  const bool leader = rank == 0;
+  const int unit = kPair ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  const int group = unit % row_groups, strip = unit / row_groups;
+  const int mtile = kPair ? 2 * group + rank : group;
   const int vtiles = (V + BN - 1) / BN;
   const int kblocks = (H + BK - 1) / BK;
   const int my_tiles =
@@ -137,22 +169,30 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     for (int b = 0; b < 2; ++b) {
       tc::mbar_init(&bars->tfull[b], 1);
-      tc::mbar_init(&bars->tempty[b], 4);
+      tc::mbar_init(&bars->tempty[b], 4 * C::CTAS);
     }
     tc::mbar_init(&bars->drain, 1);
     bars->abort = 0;
     tc::fence_mbar_init();
   }
   if (warp == 1) {
-    tc::tmem_alloc(&bars->tmem_base, TMEM_COLS);
-    tc::tmem_relinquish();
+    if constexpr (kPair) {
+      tc::tmem_alloc_pair(&bars->tmem_base, TMEM_COLS);
+      tc::tmem_relinquish_pair();
+    } else {
+      tc::tmem_alloc(&bars->tmem_base, TMEM_COLS);
+      tc::tmem_relinquish();
+    }
   }
   if (warp == 0 && lane == 0) {
     tc::tma_prefetch_map(&map_y);
     tc::tma_prefetch_map(&map_w);
   }
   tc::fence_before_sync();
-  __syncthreads();
+  if constexpr (kPair)
+    tc::cluster_sync();  // both CTAs' barriers exist before any copy lands
+  else
+    __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = bars->tmem_base;
   volatile int* abort = &bars->abort;
@@ -160,6 +200,10 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
+      // full barriers of the MMA-issuing CTA, as cluster addresses
+      const uint32_t full0 =
+          kPair ? tc::mapa_shared(tc::smem_u32(&bars->full[0]), 0)
+                : tc::smem_u32(&bars->full[0]);
       int stage = 0;
       uint32_t phase = 0, issued = 0, last_par = 0;
       bool ok = true;
@@ -171,24 +215,39 @@ __global__ void __launch_bounds__(THREADS, 1)
             ok = false;
             break;
           }
-          tc::mbar_arrive_expect_tx(&bars->full[stage], STAGE_BYTES);
-          tc::tma_load_2d(sa + stage * A_BYTES, &map_y, &bars->full[stage],
-                          kb * BK, mtile * BM);
-          tc::tma_load_2d(sb + stage * B_BYTES, &map_w, &bars->full[stage],
-                          kb * BK, vt * BN);
+          uint8_t* a_dst = sa + stage * A_BYTES;
+          uint8_t* b_dst = sb + stage * C::B_BYTES;
+          if constexpr (kPair) {
+            if (leader)
+              tc::mbar_arrive_expect_tx(&bars->full[stage],
+                                        2 * C::STAGE_BYTES);
+            const uint32_t fb = full0 + stage * 8;
+            tc::tma_load_2d_pair(a_dst, &map_y, fb, kb * BK, mtile * BM);
+            tc::tma_load_2d_pair(b_dst, &map_w, fb, kb * BK,
+                                 vt * BN + rank * C::B_ROWS);
+          } else {
+            tc::mbar_arrive_expect_tx(&bars->full[stage], C::STAGE_BYTES);
+            tc::tma_load_2d(a_dst, &map_y, &bars->full[stage], kb * BK,
+                            mtile * BM);
+            tc::tma_load_2d(b_dst, &map_w, &bars->full[stage], kb * BK,
+                            vt * BN);
+          }
           issued |= 1u << stage;
           last_par = (last_par & ~(1u << stage)) | (phase << stage);
           if (++stage == STAGES) { stage = 0; phase ^= 1; }
         }
       }
-      // leave no copy in flight
-      for (int s = 0; s < STAGES; ++s)
-        if ((issued >> s) & 1) wait_timeout(&bars->full[s], (last_par >> s) & 1);
+      // leave no copy in flight (a pair's full barriers count both CTAs'
+      // copies; the closing cluster barrier keeps the odd CTA until then)
+      if (leader)
+        for (int s = 0; s < STAGES; ++s)
+          if ((issued >> s) & 1)
+            wait_timeout(&bars->full[s], (last_par >> s) & 1);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA
-    if (lane == 0) {
-      constexpr uint32_t idesc = tc::idesc_bf16_f32(BM, BN);
+    if (lane == 0 && leader) {
+      constexpr uint32_t idesc = tc::idesc_bf16_f32(BM * C::CTAS, BN);
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
@@ -209,19 +268,34 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
           tc::fence_after_sync();
           const uint32_t a0 = tc::smem_u32(sa + stage * A_BYTES);
-          const uint32_t b0 = tc::smem_u32(sb + stage * B_BYTES);
+          const uint32_t b0 = tc::smem_u32(sb + stage * C::B_BYTES);
 #pragma unroll
-          for (int k = 0; k < BK / 16; ++k)
-            tc::mma_bf16(d, tc::sdesc_k_sw128(a0 + k * 32),
-                         tc::sdesc_k_sw128(b0 + k * 32), idesc,
-                         (kb | k) != 0);
-          tc::mma_commit(&bars->empty[stage]);
+          for (int k = 0; k < BK / 16; ++k) {
+            const uint64_t ad = tc::sdesc_k_sw128(a0 + k * 32);
+            const uint64_t bd = tc::sdesc_k_sw128(b0 + k * 32);
+            if constexpr (kPair)
+              tc::mma_bf16_pair(d, ad, bd, idesc, (kb | k) != 0);
+            else
+              tc::mma_bf16(d, ad, bd, idesc, (kb | k) != 0);
+          }
+          if constexpr (kPair)
+            tc::mma_commit_pair_mc(&bars->empty[stage], 3);
+          else
+            tc::mma_commit(&bars->empty[stage]);
           if (++stage == STAGES) { stage = 0; phase ^= 1; }
         }
-        if (ok) tc::mma_commit(&bars->tfull[b]);
+        if (ok) {
+          if constexpr (kPair)
+            tc::mma_commit_pair_mc(&bars->tfull[b], 3);
+          else
+            tc::mma_commit(&bars->tfull[b]);
+        }
       }
       // every MMA issued completes before TMEM is released
-      tc::mma_commit(&bars->drain);
+      if constexpr (kPair)
+        tc::mma_commit_pair_mc(&bars->drain, 1);
+      else
+        tc::mma_commit(&bars->drain);
       wait_timeout(&bars->drain, 0);
     }
   } else {
@@ -229,6 +303,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int m = mtile * BM + q * 32 + lane;
     float* xs = xs_all + ((warp - 2) * 32 + lane) * XS_STRIDE;
+    // accumulator-free barriers of the MMA-issuing CTA
+    const uint32_t tempty0 =
+        kPair ? tc::mapa_shared(tc::smem_u32(&bars->tempty[0]), 0)
+              : tc::smem_u32(&bars->tempty[0]);
     float tv[kC];
     int ti[kC];
 #pragma unroll
@@ -269,7 +347,12 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       tc::fence_before_sync();
       __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&bars->tempty[b]);
+      if (lane == 0) {
+        if constexpr (kPair)
+          tc::mbar_arrive_cluster(tempty0 + b * 8);
+        else
+          tc::mbar_arrive(&bars->tempty[b]);
+      }
     }
     if (ok && m < M) {
       const size_t pr = (size_t)m * strips + strip;
@@ -288,39 +371,105 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 
   tc::fence_before_sync();
-  __syncthreads();
+  if constexpr (kPair)
+    tc::cluster_sync();  // the pair's MMAs and copies are done in both CTAs
+  else
+    __syncthreads();
   if (warp == 1) {
     tc::fence_after_sync();
-    tc::tmem_dealloc(tmem, TMEM_COLS);
+    if constexpr (kPair)
+      tc::tmem_dealloc_pair(tmem, TMEM_COLS);
+    else
+      tc::tmem_dealloc(tmem, TMEM_COLS);
   }
   if (threadIdx.x == 0 && bars->abort) raise_error(err, kErrTimeout);
 }
 
 }  // namespace
 
-int lmhead_tc_grid(int M, int V, int num_sms, int* row_tiles, int* strips) {
+bool lmhead_tc_pairs(int M) { return (M + BM - 1) / BM >= 2; }
+
+namespace {
+// Pairs the device can hold at once (a pair needs two SMs of one TPC).
+int max_resident_pairs(int num_sms) {
+  static int cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+    return num_sms / 2;
+  if (cached[dev] > 0) return cached[dev];
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(num_sms);
+  cfg.blockDim = dim3(THREADS);
+  cfg.dynamicSmemBytes = smem_bytes<true>();
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaFuncSetAttribute(lmhead_tc_kernel<true>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)smem_bytes<true>()) != cudaSuccess ||
+      cudaOccupancyMaxActiveClusters(&n, lmhead_tc_kernel<true>, &cfg) !=
+          cudaSuccess ||
+      n < 1) {
+    (void)cudaGetLastError();
+    n = num_sms / 2;
+  }
+  cached[dev] = n;
+  return n;
+}
+}  // namespace
+
+int lmhead_tc_grid(int M, int V, int num_sms, int* row_groups, int* strips) {
+  const bool pairs = lmhead_tc_pairs(M);
+  const int ctas = pairs ? 2 : 1;
   const int rt = (M + BM - 1) / BM;
+  const int rg = (rt + ctas - 1) / ctas;  // units per vocab strip
   const int vt = (V + BN - 1) / BN;
-  int st = std::max(1, num_sms / rt);
+  const int units = pairs ? max_resident_pairs(num_sms) : num_sms;
+  int st = std::max(1, units / rg);
   st = std::min(std::min(st, vt), kMaxStrips);
-  *row_tiles = rt;
+  *row_groups = rg;
   *strips = st;
-  return rt * st;
+  return rg * st * ctas;
 }
 
 cudaError_t launch_lmhead_tc(const CUtensorMap& map_y, const CUtensorMap& map_w,
                              int M, int H, int V, int num_sms, TopkPartials P,
                              int* err, int* strips_out, cudaStream_t s) {
-  int rt = 0, st = 0;
-  const int grid = lmhead_tc_grid(M, V, num_sms, &rt, &st);
+  int rg = 0, st = 0;
+  const int grid = lmhead_tc_grid(M, V, num_sms, &rg, &st);
   *strips_out = st;
+  if (!lmhead_tc_pairs(M)) {
+    cudaError_t e = cudaFuncSetAttribute(
+        lmhead_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        (int)smem_bytes<false>());
+    if (e != cudaSuccess) return e;
+    lmhead_tc_kernel<false><<<grid, THREADS, smem_bytes<false>(), s>>>(
+        map_y, map_w, M, H, V, rg, st, P, err);
+    return cudaGetLastError();
+  }
   cudaError_t e = cudaFuncSetAttribute(
-      lmhead_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-      (int)SMEM_BYTES);
+      lmhead_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      (int)smem_bytes<true>());
   if (e != cudaSuccess) return e;
-  lmhead_tc_kernel<<<grid, THREADS, SMEM_BYTES, s>>>(map_y, map_w, M, H, V,
-                                                     rt, st, P, err);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(THREADS);
+  cfg.dynamicSmemBytes = smem_bytes<true>();
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, lmhead_tc_kernel<true>, map_y, map_w, M, H,
+                            V, rg, st, P, err);
 }
 
 }  // namespace dflash

@@ -108,7 +108,7 @@ __global__ void __launch_bounds__(kThreads)
   const float* x = L + (size_t)row * V;
   const bool greedy = (T == 0.f);
 
-  __shared__ float s_a[kWarps], s_s[kWarps];
+  __shared__ float s_a[kWarps];
   __shared__ int s_i[kWarps];
   __shared__ int s_flag, s_n, s_seg, s_use_raw;
   __shared__ float s_W[64], s_rem;

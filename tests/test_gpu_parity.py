@@ -113,6 +113,8 @@ def test_tiny_fp32(lib, name, T):
     (4, 1, 64, 777, 16, 1.0),       # K = 1
     (9, 3, 128, 2051, 32, 1.5),     # M not a multiple of 8
     (5, 3, 200, 1999, 48, 1.0),     # H not a multiple of 64 (ragged K tail)
+    (16, 16, 256, 3000, 256, 0.0),  # M = 256: two row tiles (CTA pair)
+    (20, 15, 136, 4099, 64, 1.0),   # M = 300: pair with an empty odd tile
 ])
 def test_small_bf16(lib, B, K, H, V, r, T):
     w = synth.Workload("small", B=B, K=K, V=V, H=H, r=r, dtype="bf16", T=T,
