@@ -56,11 +56,11 @@ cudaError_t launch_path_walk(const float* scores, const int* topi, int B,
 
 // verify.cu ---------------------------------------------------------------
 struct VerifyWs {
-  float2* part;        // [rows][max(segments, 64)]: segment (max, sum) pairs
-                       // at T > 0, chunk (max, argmax) at T = 0
-  float* row_m;        // [rows] row max
-  float* row_z;        // [rows] sum of exp((x - max) / T)
-  int* row_arg;        // [rows] first argmax
+  float2* part;        // [rows][segments]: segment (max, sum) pairs at
+                       // T > 0, chunk (max, argmax) at T = 0
+  int* row_acc;        // [rows] accept decision of position t (t < K)
+  int* row_tok;        // [rows] token emitted if t is the first rejection
+                       // (t = K: the bonus token)
   unsigned* counters;  // rows + B tickets, zeroed before every launch
   size_t counter_bytes;
 };

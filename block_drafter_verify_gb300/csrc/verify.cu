@@ -7,41 +7,40 @@
 // One launch, grid (B*(K+1) target rows, chunks of each row), 256 threads:
 //   main pass   a CTA walks its chunk in blocks of 16384 tokens; warp w of
 //               the CTA owns the contiguous 2048-token segment w of each
-//               block and streams its segments through a 3-stage ring of
-//               8 KB bulk async copies in shared memory (lane l reads the
-//               16-byte words 4l + 128u, u < 16).  At T > 0 a warp reduces
-//               a segment to (max, sum 2^((x-max)/T log2 e)) with one max
-//               shuffle and one sum shuffle and writes that pair; at T = 0
-//               the CTA keeps the first argmax.
-//   row fold    the last CTA to finish a row folds the row's segment pairs
-//               (or chunk argmaxes) in a fixed tree: row max, Z, argmax.
-//   accept      the last row of a sequence to finish runs the K accept tests
-//               at once, one lane per position, and keeps the prefix before
-//               the first rejection.
-//   draw        (T > 0) the same CTA turns the segment pairs of row n into
-//               residual weights (the drafter's q subtracted at the <= 16
-//               candidates), finds the segment that holds u * total, reads
-//               its 2048 tokens once more and draws the token with a block
-//               prefix sum.
+//               block and reads it with 16-byte loads straight into
+//               registers (lane l holds the words 4l + 128u, u < 16).  No
+//               shared-memory staging: every CTA of the grid is resident
+//               at once and keeps its loads in flight.  At T > 0 a warp
+//               reduces a segment to (max, sum 2^((x-max)/T log2 e)); at
+//               T = 0 the CTA keeps the first argmax.
+//   row work    the last CTA to finish row (b, t) (atomic ticket) folds the
+//               row in a fixed tree (row max, Z, argmax) and then settles
+//               everything that depends on that row alone: the accept test
+//               of position t, and at T > 0 the token to emit if position t
+//               turns out to be the first rejection (a draw from the
+//               residual max(0, p - q) over the <= 16 candidates) or, for
+//               t = K, the bonus draw from p.  All draws of sequence b share
+//               its one resample uniform, so drawing every row ahead of time
+//               gives the same token as drawing only the rejected one.  The
+//               drafter's inputs of row t (draft, candidates, q and the
+//               target logits at those tokens) are fetched at the start of
+//               the CTA, so none of this waits on another launch or row.
+//   sequence    the last row of a sequence to finish keeps the prefix before
+//               the first rejection n and emits row n's token.
 // "Last CTA" is an atomic ticket; nothing ever waits.  All folds and sums
 // run in a fixed order, so results are identical run to run.
 #include <algorithm>
 
 #include "kernels.h"
-#include "tc_ptx.cuh"
 
 namespace dflash {
 namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kSegTokens = 2048;                 // one warp's segment
+constexpr int kSegTokens = 2048;                   // one warp's segment
 constexpr int kBlockTokens = kWarps * kSegTokens;  // 16384
 constexpr float kLog2e = 1.4426950408889634f;
-// Bulk-copy ring of the main pass: kStages segment copies in flight per warp.
-constexpr int kStages = 3;
-constexpr size_t kRingBytes = (size_t)kWarps * kStages * kSegTokens * 4;
-constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s: far beyond any real wait
 
 __device__ __forceinline__ float ex2f(float x) {
   float y;
@@ -103,73 +102,50 @@ __global__ void __launch_bounds__(kThreads)
   const int row = blockIdx.x, c = blockIdx.y, tid = threadIdx.x;
   const int lane = tid & 31, wid = tid >> 5;
   const int K1 = K + 1, rows = B * K1;
-  const int b = row / K1;
+  const int b = row / K1, t = row % K1;
   const int nseg = (V + kSegTokens - 1) / kSegTokens;
   const float* x = L + (size_t)row * V;
   const bool greedy = (T == 0.f);
+  // the row's pairs: written here when one CTA covers the row, else loaded
+  extern __shared__ float2 s_pair[];
 
   __shared__ float s_a[kWarps];
   __shared__ int s_i[kWarps];
-  __shared__ int s_flag, s_n, s_seg, s_use_raw;
-  __shared__ float s_W[64], s_rem;
+  __shared__ int s_flag, s_seg, s_use_raw, s_acc;
+  __shared__ float s_W[kWarps], s_rem, s_m;
   __shared__ int s_ci[kC];
   __shared__ float s_qz[kC], s_corr[kC];
 
+  // ---- the drafter's inputs of this row, in flight during the main pass --
+  // lanes 0-15 of warp 0: candidate j (token, q, target logit); lane 16:
+  // the draft token.  Loaded into registers now, stored after the pass.
+  const bool has_draft = t < K;
+  int r_tok = -1;
+  float r_q = 0.f;
+  if (wid == 0 && has_draft) {
+    if (lane < kC) {
+      r_tok = topi[(b * K + t) * kC + lane];
+      r_q = q[(b * K + t) * kC + lane];
+    } else if (lane == kC) {
+      r_tok = draft[b * K + t];
+    }
+  }
+
   // ---- main pass ------------------------------------------------------
-  // Segments of this chunk: sc0 .. sc1-1; warp w takes sc0 + w + 8 j.  With
-  // 16-byte aligned rows (vec4) each warp streams its segments through a
-  // ring of kStages bulk copies in shared memory, so copies stay in flight
-  // while it computes; otherwise it loads into registers directly.
-  extern __shared__ float4 ring4[];
-  __shared__ uint64_t s_bar[kWarps][kStages];
-  __shared__ int s_abort;
+  // Segments of this chunk: sc0 .. sc1-1; warp w takes sc0 + w + 8 j.
   bool bad = false;
   float ga = -INFINITY;   // T = 0: this thread's best value ...
   int gi = 0x7fffffff;    // ... and its (first) index
   const int sc0 = c * bpc * kWarps;
   const int sc1 = min(nseg, (c + 1) * bpc * kWarps);
   const int nmine = sc0 + wid < sc1 ? (sc1 - (sc0 + wid) + kWarps - 1) / kWarps : 0;
-  float* ring = reinterpret_cast<float*>(ring4) + (size_t)wid * kStages * kSegTokens;
-  if (vec4) {
-    if (tid == 0) s_abort = 0;
-    if (lane == 0) {
-      for (int st = 0; st < kStages; ++st) tc::mbar_init(&s_bar[wid][st], 1);
-      tc::fence_mbar_init();
-    }
-    __syncthreads();
-  }
-  auto issue = [&](int j) {  // lane 0: copy segment j of this warp
-    const int base = (sc0 + wid + kWarps * j) * kSegTokens;
-    const int st = j % kStages;
-    const uint32_t bytes = (uint32_t)min(kSegTokens, V - base) * 4u;
-    // the warp's earlier reads of this stage come before the copy's writes
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    tc::mbar_arrive_expect_tx(&s_bar[wid][st], bytes);
-    tc::bulk_load(ring + st * kSegTokens, x + base, bytes, &s_bar[wid][st]);
-  };
-  if (vec4 && lane == 0)
-    for (int j = 0; j < min(kStages, nmine); ++j) issue(j);
+  float r_x = 0.f;  // target logit at r_tok (fetched after the first segment)
   for (int j = 0; j < nmine; ++j) {
-    const int base = (sc0 + wid + kWarps * j) * kSegTokens;
+    const int seg = sc0 + wid + kWarps * j;
+    const int base = seg * kSegTokens;
     float4 f[16];
-    if (vec4) {
-      const int st = j % kStages;
-      const bool got = tc::mbar_wait_bounded(&s_bar[wid][st], (j / kStages) & 1,
-                                             &s_abort, kWaitNs);
-      if (!got && lane == 0) raise_error(err, kErrTimeout);
-      const float* seg = ring + st * kSegTokens;
-#pragma unroll
-      for (int u = 0; u < 16; ++u) {
-        const int i = 4 * lane + 128 * u;
-        f[u] = base + i < V
-                   ? *reinterpret_cast<const float4*>(seg + i)
-                   : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-      }
-      __syncwarp();  // every lane has read the stage: refill it
-      if (lane == 0 && j + kStages < nmine) issue(j + kStages);
-    } else {
-      load_segment(x, base, V, lane, vec4, f);
-    }
+    load_segment(x, base, V, lane, vec4, f);
+    if (j == 0 && wid == 0 && r_tok >= 0 && r_tok < V) r_x = x[r_tok];
     if (greedy) {
       float chk = 0.f;
 #pragma unroll
@@ -203,10 +179,14 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
       for (int o = 16; o; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
       bad |= (sum != sum) || mx == INFINITY;
-      if (lane == 0)
-        ws.part[(size_t)row * nseg + base / kSegTokens] = make_float2(mx, sum);
+      if (lane == 0) {
+        const float2 pr = make_float2(mx, sum);
+        if (nchunk == 1) s_pair[seg] = pr;
+        else ws.part[(size_t)row * nseg + seg] = pr;
+      }
     }
   }
+  if (wid == 0 && nmine == 0 && r_tok >= 0 && r_tok < V) r_x = x[r_tok];
   if (__any_sync(0xffffffffu, bad) && lane == 0) raise_error(err, kErrNonfinite);
   if (greedy) {  // chunk argmax: lanes, then warps, in a fixed tree
 #pragma unroll
@@ -224,28 +204,48 @@ __global__ void __launch_bounds__(kThreads)
       int ri = s_i[0];
       for (int w = 1; w < kWarps; ++w)
         if (arg_better(s_a[w], s_i[w], ra, ri)) { ra = s_a[w]; ri = s_i[w]; }
-      ws.part[(size_t)row * nseg + c] = make_float2(ra, __int_as_float(ri));
+      s_a[0] = ra;
+      s_i[0] = ri;
+      if (nchunk > 1)
+        ws.part[(size_t)row * nseg + c] = make_float2(ra, __int_as_float(ri));
     }
-    __threadfence();
-    s_flag = (atomicAdd(&ws.counters[row], 1u) == (unsigned)(nchunk - 1));
+    if (nchunk > 1) {
+      __threadfence();
+      s_flag = (atomicAdd(&ws.counters[row], 1u) == (unsigned)(nchunk - 1));
+    } else {
+      s_flag = 1;
+    }
   }
   __syncthreads();
   if (!s_flag) return;
 
-  // ---- last CTA of this row: fold the row (warp 0, fixed tree) ----------
-  if (wid == 0) {
+  // ---- last CTA of row (b, t): fold it ----------------------------------
+  if (nchunk > 1) {
     __threadfence();
+    const int nparts = greedy ? nchunk : nseg;
+    for (int k = tid; k < nparts; k += kThreads)
+      s_pair[k] = __ldcg(&ws.part[(size_t)row * nseg + k]);
+    __syncthreads();
+  }
+  if (wid == 0) {
     float ra = -INFINITY, rs = 0.f;
     int ri = 0x7fffffff;
-    const int nparts = greedy ? nchunk : nseg;
-    for (int k = lane; k < nparts; k += 32) {
-      const float2 p = __ldcg(&ws.part[(size_t)row * nseg + k]);
-      if (greedy) {
-        if (arg_better(p.x, __float_as_int(p.y), ra, ri)) {
-          ra = p.x;
-          ri = __float_as_int(p.y);
-        }
+    if (greedy) {
+      if (nchunk == 1) {
+        ra = s_a[0];
+        ri = s_i[0];
       } else {
+        for (int k = lane; k < nchunk; k += 32) {
+          const float2 p = s_pair[k];
+          if (arg_better(p.x, __float_as_int(p.y), ra, ri)) {
+            ra = p.x;
+            ri = __float_as_int(p.y);
+          }
+        }
+      }
+    } else {
+      for (int k = lane; k < nseg; k += 32) {
+        const float2 p = s_pair[k];
         fold_lse(ra, rs, p.x, p.y, s2);
       }
     }
@@ -260,209 +260,203 @@ __global__ void __launch_bounds__(kThreads)
         fold_lse(ra, rs, oa, os, s2);
       }
     }
-    if (lane == 0) {
-      if (ra == -INFINITY) {  // every logit of the row is -inf
-        raise_error(err, kErrNonfinite);
-        ri = 0; ra = 0.f; rs = 1.f;
-      }
-      ws.row_m[row] = ra;
-      ws.row_z[row] = rs;
-      ws.row_arg[row] = ri;
-      __threadfence();
-      s_flag = (atomicAdd(&ws.counters[rows + b], 1u) == (unsigned)K);
+    if (ra == -INFINITY) {  // every logit of the row is -inf
+      if (lane == 0) raise_error(err, kErrNonfinite);
+      ri = 0; ra = 0.f; rs = 1.f;
     }
-  }
-  __syncthreads();
-  if (!s_flag) return;
-
-  // ---- last row of sequence b: the K accept tests, one lane each --------
-  if (wid == 0) {
-    __threadfence();
-    bool ok = true;
-    if (lane < K) {
-      const int t = lane;
-      const int d = draft[b * K + t];
-      const int rr = b * K1 + t;
+    // accept test of position t (t < K), lane 16 holding the draft token
+    const int d = __shfl_sync(0xffffffffu, r_tok, kC);
+    const float xd = __shfl_sync(0xffffffffu, r_x, kC);
+    int acc = 1;
+    if (has_draft) {
       if (d < 0 || d >= V) {
-        raise_error(err, kErrBadIndex);
-        ok = false;
+        if (lane == 0) raise_error(err, kErrBadIndex);
+        acc = 0;
       } else if (greedy) {
-        ok = (d == __ldcg(&ws.row_arg[rr]));
+        acc = (d == ri);
       } else {
-        float qd = 0.f;
-        bool found = false;
-#pragma unroll
-        for (int j = 0; j < kC; ++j) {
-          const int cj = topi[(b * K + t) * kC + j];
-          const float qj = q[(b * K + t) * kC + j];
-          if (!found && cj == d) { qd = qj; found = true; }
-        }
-        if (!found) raise_error(err, kErrBadIndex);
-        const float m = __ldcg(&ws.row_m[rr]);
-        const float pd = weight(L[(size_t)rr * V + d], s2, -m * s2) /
-                         __ldcg(&ws.row_z[rr]);
+        // q of the draft: its first match among the candidates
+        const unsigned hit = __ballot_sync(0xffffffffu, lane < kC && r_tok == d);
+        const float qd = hit ? __shfl_sync(0xffffffffu, r_q, __ffs(hit) - 1) : 0.f;
+        if (!hit && lane == 0) raise_error(err, kErrBadIndex);
+        const float pd = weight(xd, s2, -ra * s2) / rs;
         const float u = philox_uniform(seed, b, t, kPurposeAccept, cycle);
-        ok = u * qd < pd;
+        acc = (u * qd < pd);
       }
     }
-    const unsigned rej = __ballot_sync(0xffffffffu, lane < K && !ok);
-    const int n = rej ? __ffs(rej) - 1 : K;
-    if (lane == 0) {
-      n_accepted[b] = n;
-      s_n = n;
-    }
-    if (lane <= K) {
-      int tok = lane < n ? draft[b * K + lane] : -1;
-      if (greedy && lane == n) tok = __ldcg(&ws.row_arg[b * K1 + n]);
-      if (!greedy && lane == n) tok = -2;  // replaced by the draw below
-      out_tok[b * K1 + lane] = tok;
+    if (greedy) {
+      if (lane == 0) {
+        ws.row_acc[row] = acc;
+        ws.row_tok[row] = ri;
+      }
+    } else {
+      // residual corrections of the candidates: -min(p_j Z, q_j Z)
+      if (lane < kC) {
+        int cj = has_draft ? r_tok : -1;
+        float qz = 0.f, corr = 0.f;
+        if (cj >= 0 && cj < V) {
+          qz = r_q * rs;
+          corr = -fminf(weight(r_x, s2, -ra * s2), qz);
+        } else {
+          cj = -1;
+        }
+        s_ci[lane] = cj;
+        s_qz[lane] = qz;
+        s_corr[lane] = corr;
+      }
+      if (lane == 0) {
+        s_m = ra;
+        s_acc = acc;
+      }
     }
   }
-  if (greedy) return;
-  __syncthreads();
-
-  // ---- draw: row n, residual max(0, p - q) (or p for the bonus row) -----
-  const int n = s_n;
-  const int rn = b * K1 + n;
-  const float* xr = L + (size_t)rn * V;
-  const float m = __ldcg(&ws.row_m[rn]);
-  const float Z = __ldcg(&ws.row_z[rn]);
-  const float nb = -m * s2;
-  if (tid < kC) {  // the rejected position's candidates
-    int cj = -1;
-    float qz = 0.f, corr = 0.f;
-    if (n < K) {
-      cj = topi[(b * K + n) * kC + tid];
-      qz = q[(b * K + n) * kC + tid] * Z;
-      if (cj >= 0 && cj < V) corr = -fminf(weight(xr[cj], s2, nb), qz);
-      else cj = -1;
-    }
-    s_ci[tid] = cj;
-    s_qz[tid] = qz;
-    s_corr[tid] = corr;
-  }
-  __syncthreads();
-  // Warp 0 locates the segment holding the draw.  Lane l owns the
-  // contiguous segments l*per .. l*per+per-1; a segment's weight is its
-  // (max, sum) pair rescaled to the row max, plus the corrections of the
-  // candidates inside it (in candidate order), clamped at zero.  One
-  // inclusive scan of the lane totals and one ballot find the lane, which
-  // walks its segments.  A zero residual total switches to p itself.
-  if (wid == 0) {
-    const int per = (nseg + 31) / 32;
-    const float u = philox_uniform(seed, b, K, kPurposeResample, cycle);
-    auto seg_weight = [&](int k, bool raw) -> float {
-      if (k >= nseg) return 0.f;
-      const float2 p = __ldcg(&ws.part[(size_t)rn * nseg + k]);
-      float w = (p.x == -INFINITY) ? 0.f : p.y * ex2f((p.x - m) * s2);
-      if (!raw) {
+  if (!greedy) {
+    __syncthreads();
+    // ---- draw of row (b, t): residual max(0, p - q), or p for t = K ------
+    // Warp 0 locates the segment.  Lane l owns the contiguous segments
+    // l*per .. l*per+per-1; a segment's weight is its (max, sum) pair
+    // rescaled to the row max, plus the corrections of the candidates
+    // inside it (in candidate order), clamped at zero.  One inclusive scan
+    // of the lane totals and one ballot find the lane, which walks its
+    // segments.  A zero residual total switches to p itself.
+    const float m = s_m;
+    const float nb = -m * s2;
+    if (wid == 0) {
+      const int per = (nseg + 31) / 32;
+      const float u = philox_uniform(seed, b, K, kPurposeResample, cycle);
+      auto seg_weight = [&](int k, bool raw) -> float {
+        if (k >= nseg) return 0.f;
+        const float2 p = s_pair[k];
+        float w = (p.x == -INFINITY) ? 0.f : p.y * ex2f((p.x - m) * s2);
+        if (!raw) {
 #pragma unroll
-        for (int j = 0; j < kC; ++j)
-          if (s_ci[j] >= 0 && s_ci[j] / kSegTokens == k) w += s_corr[j];
-      }
-      return fmaxf(w, 0.f);
-    };
-    int f_seg = -1, f_raw = 0;
-    float f_rem = 0.f;
-    for (int raw = 0; raw < 2 && f_seg < 0; ++raw) {
-      float ltot = 0.f;
-#pragma unroll 4
-      for (int i = 0; i < per; ++i) ltot += seg_weight(lane * per + i, raw);
-      float incl = ltot;
+          for (int j = 0; j < kC; ++j)
+            if (s_ci[j] >= 0 && s_ci[j] / kSegTokens == k) w += s_corr[j];
+        }
+        return fmaxf(w, 0.f);
+      };
+      int f_seg = -1, f_raw = 0;
+      float f_rem = 0.f;
+      for (int raw = 0; raw < 2 && f_seg < 0; ++raw) {
+        float ltot = 0.f;
+        for (int i = 0; i < per; ++i) ltot += seg_weight(lane * per + i, raw);
+        float incl = ltot;
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const float t = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += t;
-      }
-      const float total = __shfl_sync(0xffffffffu, incl, 31);
-      if (!(total > 0.f)) continue;  // degenerate residual: draw from p
-      const float theta = u * total;
-      const unsigned hit = __ballot_sync(0xffffffffu, ltot > 0.f && incl > theta);
-      const unsigned live = __ballot_sync(0xffffffffu, ltot > 0.f);
-      // u * total rounded up to the total: the last lane with weight
-      const int L = hit ? __ffs(hit) - 1 : 31 - __clz(live);
-      if (lane == L) {
-        float acc = incl - ltot;
-        int last = -1;
-        for (int i = 0; i < per; ++i) {
-          const float w = seg_weight(lane * per + i, raw);
-          if (w > 0.f) last = lane * per + i;
-          if (w > 0.f && acc + w > theta) {
-            f_seg = lane * per + i;
-            f_rem = theta - acc;
-            break;
+        for (int o = 1; o < 32; o <<= 1) {
+          const float tt = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += tt;
+        }
+        const float total = __shfl_sync(0xffffffffu, incl, 31);
+        if (!(total > 0.f)) continue;  // degenerate residual: draw from p
+        const float theta = u * total;
+        const unsigned hit = __ballot_sync(0xffffffffu, ltot > 0.f && incl > theta);
+        const unsigned live = __ballot_sync(0xffffffffu, ltot > 0.f);
+        // u * total rounded up to the total: the last lane with weight
+        const int Ls = hit ? __ffs(hit) - 1 : 31 - __clz(live);
+        if (lane == Ls) {
+          float a = incl - ltot;
+          int last = -1;
+          for (int i = 0; i < per; ++i) {
+            const float w = seg_weight(lane * per + i, raw);
+            if (w > 0.f) last = lane * per + i;
+            if (w > 0.f && a + w > theta) {
+              f_seg = lane * per + i;
+              f_rem = theta - a;
+              break;
+            }
+            a += w;
           }
-          acc += w;
+          if (f_seg < 0) {
+            f_seg = last;
+            f_rem = INFINITY;
+          }
         }
-        if (f_seg < 0) {
-          f_seg = last;
-          f_rem = INFINITY;
-        }
+        f_seg = __shfl_sync(0xffffffffu, f_seg, Ls);
+        f_rem = __shfl_sync(0xffffffffu, f_rem, Ls);
+        f_raw = raw;
       }
-      f_seg = __shfl_sync(0xffffffffu, f_seg, L);
-      f_rem = __shfl_sync(0xffffffffu, f_rem, L);
-      f_raw = raw;
-    }
-    if (lane == 0) {
-      s_seg = f_seg;
-      s_rem = f_rem;
-      s_use_raw = f_raw;
-    }
-  }
-  __syncthreads();
-  int seg = s_seg;
-  if (seg < 0) {  // cannot happen: the row maximum has weight 1
-    if (tid == 0) raise_error(err, kErrBadIndex);
-    seg = 0;
-  }
-  // the 2048 tokens of the segment: 8 contiguous tokens per thread
-  const bool use_raw = s_use_raw;
-  const int t0 = seg * kSegTokens + tid * 8;
-  float w8[8];
-  float tsum = 0.f;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int v = t0 + i;
-    float wv = 0.f;
-    if (v < V) {
-      wv = weight(xr[v], s2, nb);
-      if (!use_raw) {
-#pragma unroll
-        for (int j = 0; j < kC; ++j)
-          if (s_ci[j] == v) wv = fmaxf(wv - s_qz[j], 0.f);
+      if (lane == 0) {
+        s_seg = f_seg;
+        s_rem = f_rem;
+        s_use_raw = f_raw;
       }
     }
-    w8[i] = wv;
-    tsum += wv;
-  }
-  // block exclusive scan of tsum (fixed tree)
-  float incl = tsum;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const float t = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += t;
-  }
-  __syncthreads();
-  if (lane == 31) s_W[wid] = incl;
-  __syncthreads();
-  float pre = 0.f, segtot = 0.f;
-  for (int w = 0; w < kWarps; ++w) {
-    if (w < wid) pre += s_W[w];
-    segtot += s_W[w];
-  }
-  const float excl = pre + incl - tsum;
-  // rounding may leave the target at or past the recomputed total
-  const float rem = fminf(s_rem, segtot * (1.f - 0x1p-22f));
-  if (tsum > 0.f && excl <= rem && rem < excl + tsum) {
-    float acc = excl;
-    int pick = -1, last = -1;
+    __syncthreads();
+    int seg = s_seg;
+    if (seg < 0) {  // cannot happen: the row maximum has weight 1
+      if (tid == 0) raise_error(err, kErrBadIndex);
+      seg = 0;
+    }
+    // the 2048 tokens of the segment: 8 contiguous tokens per thread
+    const bool use_raw = s_use_raw;
+    const int t0 = seg * kSegTokens + tid * 8;
+    float w8[8];
+    float tsum = 0.f;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      if (w8[i] > 0.f) last = t0 + i;
-      acc += w8[i];
-      if (pick < 0 && acc > rem) pick = t0 + i;
+      const int v = t0 + i;
+      float wv = 0.f;
+      if (v < V) {
+        wv = weight(x[v], s2, nb);
+        if (!use_raw) {
+#pragma unroll
+          for (int j = 0; j < kC; ++j)
+            if (s_ci[j] == v) wv = fmaxf(wv - s_qz[j], 0.f);
+        }
+      }
+      w8[i] = wv;
+      tsum += wv;
     }
-    out_tok[b * K1 + n] = pick >= 0 ? pick : last;
+    // block exclusive scan of tsum (fixed tree)
+    float incl = tsum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float tt = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += tt;
+    }
+    if (lane == 31) s_W[wid] = incl;
+    __syncthreads();
+    float pre = 0.f, segtot = 0.f;
+    for (int w = 0; w < kWarps; ++w) {
+      if (w < wid) pre += s_W[w];
+      segtot += s_W[w];
+    }
+    const float excl = pre + incl - tsum;
+    // rounding may leave the target at or past the recomputed total
+    const float rem = fminf(s_rem, segtot * (1.f - 0x1p-22f));
+    if (tsum > 0.f && excl <= rem && rem < excl + tsum) {
+      float a = excl;
+      int pick = -1, last = -1;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        if (w8[i] > 0.f) last = t0 + i;
+        a += w8[i];
+        if (pick < 0 && a > rem) pick = t0 + i;
+      }
+      ws.row_tok[row] = pick >= 0 ? pick : last;
+      __threadfence();  // before the sequence ticket below
+    }
+    if (tid == 0) ws.row_acc[row] = s_acc;
+  }
+
+  // ---- ticket of sequence b; its last row emits the tokens --------------
+  __syncthreads();
+  if (tid == 0) {
+    __threadfence();
+    s_flag = (atomicAdd(&ws.counters[rows + b], 1u) == (unsigned)K);
+  }
+  __syncthreads();
+  if (!s_flag || wid != 0) return;
+  __threadfence();
+  const int acc = lane < K ? __ldcg(&ws.row_acc[b * K1 + lane]) : 1;
+  const unsigned rej = __ballot_sync(0xffffffffu, lane < K && !acc);
+  const int n = rej ? __ffs(rej) - 1 : K;
+  if (lane == 0) n_accepted[b] = n;
+  if (lane <= K) {
+    int tok = -1;
+    if (lane < n) tok = draft[b * K + lane];
+    else if (lane == n) tok = __ldcg(&ws.row_tok[b * K1 + n]);
+    out_tok[b * K1 + lane] = tok;
   }
 }
 
@@ -483,8 +477,6 @@ inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 size_t verify_ws_layout(int B, int K, int V, void* base, VerifyWs* o) {
   const size_t rows = (size_t)B * (K + 1);
   const size_t nseg = ((size_t)V + kSegTokens - 1) / kSegTokens;
-  // per row: segment pairs (T > 0) or chunk argmaxes (T = 0, <= 64)
-  const size_t per_row = std::max<size_t>(nseg, kVerifyMaxChunks);
   char* p = static_cast<char*>(base);
   size_t off = 0;
   auto take = [&](size_t bytes) {
@@ -494,10 +486,10 @@ size_t verify_ws_layout(int B, int K, int V, void* base, VerifyWs* o) {
     return r;
   };
   VerifyWs w{};
-  w.part = reinterpret_cast<float2*>(take(rows * per_row * sizeof(float2)));
-  w.row_m = reinterpret_cast<float*>(take(rows * sizeof(float)));
-  w.row_z = reinterpret_cast<float*>(take(rows * sizeof(float)));
-  w.row_arg = reinterpret_cast<int*>(take(rows * sizeof(int)));
+  // per row: segment pairs (T > 0) or chunk argmaxes (T = 0, <= nseg)
+  w.part = reinterpret_cast<float2*>(take(rows * nseg * sizeof(float2)));
+  w.row_acc = reinterpret_cast<int*>(take(rows * sizeof(int)));
+  w.row_tok = reinterpret_cast<int*>(take(rows * sizeof(int)));
   w.counter_bytes = (rows + (size_t)B) * sizeof(unsigned);
   w.counters = reinterpret_cast<unsigned*>(take(w.counter_bytes));
   if (o) *o = w;
@@ -511,12 +503,13 @@ cudaError_t launch_verify(const float* L, const int* draft, const int* topi,
                           int* out_tok, const VerifyWs& ws, int num_sms,
                           int* err, cudaStream_t s) {
   const int rows = B * (K + 1);
+  const int nseg = (V + kSegTokens - 1) / kSegTokens;
   const int blocks_per_row = (V + kBlockTokens - 1) / kBlockTokens;
   const int vec4 = (V % 4 == 0) && ((reinterpret_cast<uintptr_t>(L) & 15) == 0);
-  // chunks of whole 16384-token blocks: about two CTAs per SM in total with
-  // the shared-memory ring (one CTA fits an SM), four without; at most
-  // kVerifyMaxChunks per row
-  const long long per_sm = vec4 ? 2 : 4;
+  // chunks of whole 16384-token blocks: about two CTAs per SM in total (so
+  // a large batch keeps one chunk per row and its pairs in shared memory),
+  // at most kVerifyMaxChunks per row
+  const long long per_sm = 2;
   const long long total_blocks = (long long)rows * blocks_per_row;
   int bpc = (int)std::max<long long>(
       1, (total_blocks + per_sm * num_sms - 1) / (per_sm * num_sms));
@@ -524,11 +517,10 @@ cudaError_t launch_verify(const float* L, const int* draft, const int* topi,
   bpc = std::min(bpc, blocks_per_row);
   const int nchunk = (blocks_per_row + bpc - 1) / bpc;
   const float s2 = T > 0.f ? kLog2e / T : 0.f;
-  const size_t smem = vec4 ? kRingBytes : 0;
-  if (vec4) {
+  const size_t smem = (size_t)nseg * sizeof(float2);
+  if (smem > 48 * 1024) {
     const cudaError_t e = cudaFuncSetAttribute(
-        verify_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-        (int)kRingBytes);
+        verify_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
   verify_kernel<<<dim3(rows, nchunk), kThreads, smem, s>>>(

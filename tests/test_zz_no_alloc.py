@@ -55,7 +55,10 @@ def test_noalloc_verify_matches_verify_on_consecutive_calls(lib, T):
 
 
 def test_noalloc_verify_refuses_sizes_beyond_its_scratch(lib):
-    B, K, V = 512, 16, 64
+    # 278,528 target rows: their per-row results and tickets alone outgrow
+    # the 4 MiB array
+    B, K, V = 16384, 16, 64
+    assert lib.dflash_workspace_bytes(1, B, K, 0, V) > 4 << 20
     L = torch.zeros(B, K + 1, V, device="cuda")
     draft = torch.zeros(B, K, dtype=torch.int32, device="cuda")
     topi = torch.zeros(B, K, C, dtype=torch.int32, device="cuda")
