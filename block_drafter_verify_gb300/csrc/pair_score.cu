@@ -15,9 +15,11 @@
 //   2. the partial sums are added over the cluster through distributed
 //      shared memory, in cluster-rank order, and CTA k keeps the gates
 //      g = sigmoid(z) of rows 2k and 2k+1;
-//   3. CTA k gathers the 16 predecessor rows of E_in and the 16 candidate
-//      rows of E_out (scaled by g) and writes the 16 x 16 scores of each of
-//      its two rows.
+//   3. CTA k writes the 16 x 16 scores of each of its two rows from the 16
+//      predecessor rows of E_in and the 16 candidate rows of E_out (scaled
+//      by g).  Those 64 embedding rows are fetched with cp.async while step
+//      1 runs: right after the first W_g panel's copies are issued, the CTA
+//      reads its rows' candidate lists and starts the gathers.
 #include <cooperative_groups.h>
 
 #include <algorithm>
@@ -34,6 +36,7 @@ constexpr int kCluster = 8;     // CTAs per cluster (split of the hidden dim)
 constexpr int kRows = 16;       // rows (b, t) per cluster
 constexpr int kRowsPerCta = kRows / kCluster;
 constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
 constexpr int kPanel = 64;           // fp32 path: W_g columns per panel
 constexpr int kPanelStride = kPanel + 4;  // 16-byte rows, no bank conflicts
 constexpr int kKP = 128;             // bf16 path: hidden columns per panel
@@ -48,7 +51,6 @@ __host__ __device__ constexpr size_t work_floats(int hs, bool bf16) {
 // 16-byte vector of storage elements converted to fp32.
 template <typename T>
 struct Vec16 {
-  static constexpr int N = 16 / sizeof(T);
   __device__ __forceinline__ static void to_f32(const uint4& u, float* f);
 };
 template <>
@@ -100,9 +102,11 @@ __device__ __forceinline__ uint32_t ld_b32(const __nv_bfloat16* p) {
 // Phase 1, bf16 storage: part[row][n] = sum over this CTA's slice of
 // h[m0 + row][k] * W_g[n][k], on the tensor cores.  The slice length is a
 // multiple of 8 (H is), so every 16-byte copy is either whole or skipped.
+template <typename Prologue>
 __device__ __forceinline__ void gate_partial_mma(
     const __nv_bfloat16* __restrict__ h, const __nv_bfloat16* __restrict__ w,
-    int M, int H, int r, int m0, int k0, int klen, float* part, float* work) {
+    int M, int H, int r, int m0, int k0, int klen, float* part, float* work,
+    Prologue&& after_first_issue) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, c = lane & 3;
   __nv_bfloat16* hs_ = reinterpret_cast<__nv_bfloat16*>(work);  // [16][kLdsB]
@@ -129,6 +133,7 @@ __device__ __forceinline__ void gate_partial_mma(
       cp_async16(ws_ + n * kLdsB + ch * 8,
                  ok ? w + (size_t)n * H + k0 + p0 + ch * 8 : w, ok ? 16 : 0);
     }
+    if (p0 == 0) after_first_issue();
     cp_async_wait_all();
     __syncthreads();
     const int ksteps = (pw + 15) / 16;  // columns past pw are zeros
@@ -145,6 +150,8 @@ __device__ __forceinline__ void gate_partial_mma(
       }
     }
   }
+  if (klen <= 0) after_first_issue();
+  __syncthreads();  // part aliases the staged tiles
 #pragma unroll
   for (int nt = 0; nt < 4; ++nt) {
     const int n = (warp * 4 + nt) * 8 + 2 * c;
@@ -240,6 +247,7 @@ __device__ __forceinline__ void gate_partial_simt(
       }
     }
   }
+  __syncthreads();  // part aliases the staged slice and panel
   if (tid < r) {
 #pragma unroll
     for (int rr = 0; rr < kRows; ++rr) part[rr * 256 + tid] = acc[rr];
@@ -253,8 +261,8 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads)
                       const int* __restrict__ anchor, const T* __restrict__ h,
                       const T* __restrict__ w_gate, const T* __restrict__ e_in,
                       const T* __restrict__ e_out, int B, int K, int H, int V,
-                      int r, int hs, float* __restrict__ scores, int* err) {
-  constexpr int EPV = Vec16<T>::N;            // elements per 16-byte vector
+                      int r, int hs, int work_len, float* __restrict__ scores,
+                      int* err) {
   extern __shared__ float4 smem4[];
   float* smem = reinterpret_cast<float*>(smem4);
   cg::cluster_group cluster = cg::this_cluster();
@@ -265,15 +273,55 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads)
   const int k0 = crank * hs, k1 = min(H, k0 + hs);
   const int klen = max(0, k1 - k0);
 
-  float* part = smem;                           // kRows * 256
-  float* gate = part + kRows * 256;             // kRowsPerCta * 256
+  float* gate = smem;                           // kRowsPerCta * 256
   float* work = gate + kRowsPerCta * 256;       // phase 1, then phase 3
+  float* part = work;  // [kRows][256]: written once phase 1's tiles are done
+  // raw embedding rows [row j][table (0 = E_in, 1 = E_out)][16][r]
+  T* estage = reinterpret_cast<T*>(work + work_len);
+  __shared__ int s_tok[kRowsPerCta][2][kC];
+  // the embedding rows come in by 16-byte copies when rows are whole
+  // 16-byte vectors (the tables are 16-byte aligned)
+  const bool vec = (r * (int)sizeof(T)) % 16 == 0;
+
+  // Indices of this CTA's rows (b, t): candidates topi[b,t,:] and their
+  // predecessors (the anchor at t = 0, else topi[b,t-1,:]); then the
+  // gathers of their embedding rows, in flight during phase 1.
+  auto fetch_rows = [&]() {
+    if (tid < kRowsPerCta * 2 * kC) {
+      const int j = tid / (2 * kC), tab = (tid / kC) & 1, i = tid % kC;
+      const int m = m0 + crank * kRowsPerCta + j;
+      int tok = -1;
+      if (m < M) {
+        const int b = m / K, t = m % K;
+        tok = tab == 1 ? topi[(size_t)m * kC + i]
+                       : (t == 0 ? anchor[b] : topi[(size_t)(m - 1) * kC + i]);
+        if (tok < -1 || tok >= V) { raise_error(err, kErrBadIndex); tok = -1; }
+      }
+      s_tok[j][tab][i] = tok;
+    }
+    __syncthreads();
+    if (vec) {
+      const int cpr = r * (int)sizeof(T) / 16;  // 16-byte chunks per row
+      const int total = kRowsPerCta * 2 * kC * cpr;
+      for (int idx = tid; idx < total; idx += kThreads) {
+        const int rowi = idx / cpr, ch = idx % cpr;  // rowi = (j*2+tab)*16+i
+        const int tab = (rowi / kC) & 1;
+        const int tok = s_tok[rowi / (2 * kC)][tab][rowi % kC];
+        const T* src = (tab == 0 ? e_in : e_out) + (size_t)max(tok, 0) * r;
+        cp_async16(estage + (size_t)rowi * r + ch * (16 / sizeof(T)),
+                   reinterpret_cast<const char*>(src) + ch * 16,
+                   tok >= 0 ? 16 : 0);
+      }
+    }
+  };
 
   // ---- phase 1: partial z[row][k] over this CTA's hidden slice ----------
-  if constexpr (std::is_same<T, __nv_bfloat16>::value)
-    gate_partial_mma(h, w_gate, M, H, r, m0, k0, klen, part, work);
-  else
+  if constexpr (std::is_same<T, __nv_bfloat16>::value) {
+    gate_partial_mma(h, w_gate, M, H, r, m0, k0, klen, part, work, fetch_rows);
+  } else {
+    fetch_rows();
     gate_partial_simt(h, w_gate, M, H, r, m0, k0, klen, hs, part, work);
+  }
   cluster.sync();
 
   // ---- phase 2: add the 8 slices (rank order) for this CTA's two rows ---
@@ -289,66 +337,44 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads)
       gate[j * 256 + tid] = 1.f / (1.f + __expf(-z));
     }
   }
-  cluster.sync();  // peers are done reading this CTA's partials
+  cp_async_wait_all();  // the embedding rows (normally long since landed)
+  cluster.sync();       // peers are done reading this CTA's partials
 
+  // ---- phase 3: 16 x 16 scores of each row --------------------------------
+  // fp32 tiles with 16-byte aligned rows when r allows (float4 reads)
+  const bool r4 = (r % 4) == 0;
+  const int rs = r4 ? r + 4 : r + 1;
+  float* ein_s = work;              // [16][rs]
+  float* eout_s = work + kC * rs;   // [16][rs], scaled by the gate
+  const int lane = tid & 31, warp = tid >> 5;
   for (int j = 0; j < kRowsPerCta; ++j) {
     const int m = m0 + crank * kRowsPerCta + j;
     if (m >= M) break;
-    const int b = m / K, t = m % K;
     const float* g_row = gate + j * 256;
-    __syncthreads();  // the previous row's tiles are consumed
-
-    // ---- phase 3: 16 x 16 scores of row m ---------------------------------
-    __shared__ int s_pred[kC], s_cand[kC];
-    if (tid < kC) {
-      int cand = topi[(size_t)m * kC + tid];
-      int pred = (t == 0) ? anchor[b] : topi[(size_t)(m - 1) * kC + tid];
-      if (cand < -1 || cand >= V) { raise_error(err, kErrBadIndex); cand = -1; }
-      if (pred < -1 || pred >= V) { raise_error(err, kErrBadIndex); pred = -1; }
-      s_cand[tid] = cand;
-      s_pred[tid] = pred;
-    }
-    __syncthreads();
-    const int rs = r + 1;  // padded row stride
-    float* ein_s = work;              // [16][rs]
-    float* eout_s = work + kC * rs;   // [16][rs], scaled by the gate
-    const int vpr = (r + EPV - 1) / EPV;  // vectors per embedding row
-    if (r % EPV == 0) {
-      // 2 tables x 16 rows x vpr vectors: every load issued before any use
-      constexpr int kMaxE =
-          (2 * kC * DFLASH_MAX_RANK / 4 + kThreads - 1) / kThreads;
-      uint4 ev[kMaxE];
+    if (j > 0) __syncthreads();  // the previous row's tiles are consumed
+    const int* pred = s_tok[j][0];
+    const int* cand = s_tok[j][1];
+    if (vec) {
+      // warp w converts staged rows w, w + 8, ...; lane l its 16-byte chunks
+      constexpr int epc = 16 / sizeof(T);  // elements per chunk
+      const int cpr = r / epc;
+      const T* st = estage + (size_t)j * 2 * kC * r;
+      for (int rowi = warp; rowi < 2 * kC; rowi += kWarps) {
+        const bool out = rowi >= kC;
+        float* dst = (out ? eout_s : ein_s) + (rowi % kC) * rs;
+        const T* srow = st + (size_t)rowi * r;
+        for (int ch = lane; ch < cpr; ch += 32) {
+          float f[epc > 4 ? 8 : 4];
+          Vec16<T>::to_f32(*reinterpret_cast<const uint4*>(srow + ch * epc), f);
 #pragma unroll
-      for (int u = 0; u < kMaxE; ++u) {
-        const int i = tid + u * kThreads;
-        ev[u] = make_uint4(0, 0, 0, 0);
-        if (i < 2 * kC * vpr) {
-          const int tab = i / (kC * vpr), rem = i % (kC * vpr);
-          const int row = rem / vpr, cv = rem % vpr;
-          const int tok = tab == 0 ? s_pred[row] : s_cand[row];
-          if (tok >= 0)
-            ev[u] = *reinterpret_cast<const uint4*>(
-                (tab == 0 ? e_in : e_out) + (size_t)tok * r + cv * EPV);
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < kMaxE; ++u) {
-        const int i = tid + u * kThreads;
-        if (i < 2 * kC * vpr) {
-          const int tab = i / (kC * vpr), rem = i % (kC * vpr);
-          const int row = rem / vpr, cv = rem % vpr;
-          float f[EPV];
-          Vec16<T>::to_f32(ev[u], f);
-          float* dst = (tab == 0 ? ein_s : eout_s) + row * rs + cv * EPV;
-#pragma unroll
-          for (int e = 0; e < EPV; ++e)
-            dst[e] = tab == 0 ? f[e] : f[e] * g_row[cv * EPV + e];
+          for (int e = 0; e < epc; ++e)
+            dst[ch * epc + e] = out ? f[e] * g_row[ch * epc + e] : f[e];
         }
       }
     } else {
       for (int i = tid; i < kC * r; i += kThreads) {
         const int row = i / r, k = i % r;
-        const int a = s_pred[row], c = s_cand[row];
+        const int a = pred[row], c = cand[row];
         ein_s[row * rs + k] = a >= 0 ? to_f32(e_in[(size_t)a * r + k]) : 0.f;
         eout_s[row * rs + k] =
             c >= 0 ? to_f32(e_out[(size_t)c * r + k]) * g_row[k] : 0.f;
@@ -356,13 +382,24 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads)
     }
     __syncthreads();
     const int i = tid / kC, jj = tid % kC;
-    float s = 0.f;
+    float sc = 0.f;
     const float* ea = ein_s + i * rs;
     const float* eb = eout_s + jj * rs;
-    for (int k = 0; k < r; ++k) s = fmaf(ea[k], eb[k], s);
-    const bool valid = s_pred[i] >= 0 && s_cand[jj] >= 0;
+    int k = 0;
+    if (r4) {
+      for (; k < r; k += 4) {
+        const float4 a4 = *reinterpret_cast<const float4*>(ea + k);
+        const float4 b4 = *reinterpret_cast<const float4*>(eb + k);
+        sc = fmaf(a4.x, b4.x, sc);
+        sc = fmaf(a4.y, b4.y, sc);
+        sc = fmaf(a4.z, b4.z, sc);
+        sc = fmaf(a4.w, b4.w, sc);
+      }
+    }
+    for (; k < r; ++k) sc = fmaf(ea[k], eb[k], sc);
+    const bool valid = pred[i] >= 0 && cand[jj] >= 0;
     scores[(size_t)m * kC * kC + tid] =
-        valid ? topv[(size_t)m * kC + jj] + s : -INFINITY;
+        valid ? topv[(size_t)m * kC + jj] + sc : -INFINITY;
   }
 }
 
@@ -377,19 +414,20 @@ cudaError_t launch_pair_score(const float* topv, const int* topi,
   const int M = B * K;
   // hidden slice per cluster rank, a multiple of 8 so 16-byte loads align
   const int hs = ((H + kCluster - 1) / kCluster + 7) & ~7;
-  const size_t work =
-      std::max(work_floats(hs, std::is_same<T, __nv_bfloat16>::value),
-               (size_t)2 * kC * (DFLASH_MAX_RANK + 1));
+  const size_t work = std::max(
+      {work_floats(hs, std::is_same<T, __nv_bfloat16>::value),
+       (size_t)kRows * 256, (size_t)2 * kC * (r + 4)});
+  const size_t estage = (size_t)kRowsPerCta * 2 * kC * r * sizeof(T);
   const size_t smem =
-      ((size_t)kRows * 256 + (size_t)kRowsPerCta * 256 + work) * sizeof(float);
+      ((size_t)kRowsPerCta * 256 + work) * sizeof(float) + estage;
   cudaError_t e = cudaFuncSetAttribute(
       pair_score_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
       (int)smem);
   if (e != cudaSuccess) return e;
   const int clusters = (M + kRows - 1) / kRows;
   pair_score_kernel<T><<<clusters * kCluster, kThreads, smem, s>>>(
-      topv, topi, anchor, h, w_gate, e_in, e_out, B, K, H, V, r, hs, scores,
-      err);
+      topv, topi, anchor, h, w_gate, e_in, e_out, B, K, H, V, r, hs,
+      (int)work, scores, err);
   return cudaGetLastError();
 }
 
