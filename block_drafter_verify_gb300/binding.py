@@ -20,7 +20,8 @@ STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported",
           5: "device wait timed out", 6: "token index out of range"}
 
 EXPORTS = ("dflash_workspace_bytes", "dflash_lmhead_topk", "dflash_pair_score",
-           "dflash_path_walk", "dflash_verify", "dflash_verify_noalloc",
+           "dflash_path_walk", "dflash_draft", "dflash_verify",
+           "dflash_verify_noalloc",
            "dflash_philox4x32", "dflash_profile_stage", "dflash_check",
            "dflash_status_string")
 STAGES = ("conv", "lmhead", "merge", "pair_score", "walk", "verify")
@@ -60,6 +61,9 @@ def load(path: str | None = None):
                                     i32, i32, i32, vp, vp]),
         "dflash_path_walk": (i32, [vp, vp, i32, i32, f32, u64, u64, vp, vp,
                                    vp, vp]),
+        "dflash_draft": (i32, [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32,
+                               i32, i32, f32, u64, u64, vp, vp, vp, vp, vp,
+                               vp, vp, vp, sz, vp]),
         "dflash_verify": (i32, [vp, vp, vp, vp, i32, i32, i32, f32, u64, u64,
                                 vp, vp, vp, sz, vp]),
         "dflash_verify_noalloc": (i32, [vp, vp, vp, vp, i32, i32, i32, f32,
@@ -163,6 +167,23 @@ def dflash_path_walk(scores, topi, T, seed, cycle, slot, draft, q,
           _ptr(draft), _ptr(q), _stream(stream))
 
 
+def dflash_draft(h, conv_w, w_lm, w_gate, e_in, e_out, anchor, T, seed,
+                 cycle, topv, topi, lse, scores, slot, draft, q, ws,
+                 stream=None):
+    """Steps a1-a4 in one call: h [B,K,H]; conv_w [2H,H] or None; w_lm
+    [V,H]; w_gate [r,H]; e_in/e_out [V,r] (one storage dtype); anchor [B]
+    i32; outputs topv/topi [B*K,16], lse [B*K], scores [B,K,16,16], slot and
+    draft [B,K] i32, q [B,K,16]; ws uint8 (workspace kind 2)."""
+    B, K, H = h.shape
+    V = w_lm.shape[0]
+    r = w_gate.shape[0]
+    _call("dflash_draft", _ptr(h), _ptr(conv_w), _ptr(w_lm), _ptr(w_gate),
+          _ptr(e_in), _ptr(e_out), _ptr(anchor), B, K, H, V, r, _dtype(h),
+          float(T), int(seed) & (2**64 - 1), int(cycle) & (2**64 - 1),
+          _ptr(topv), _ptr(topi), _ptr(lse), _ptr(scores), _ptr(slot),
+          _ptr(draft), _ptr(q), _ptr(ws), ws.numel(), _stream(stream))
+
+
 def dflash_verify(target_logits, draft, topi, q, T, seed, cycle, n_accepted,
                   out_tok, ws, stream=None):
     """target_logits [B,K+1,V] f32; draft [B,K]; topi/q [B,K,16];
@@ -240,6 +261,8 @@ class DraftVerify:
                                  dtype=torch.uint8, device=dev)
         self.ws_v = torch.empty(dflash_workspace_bytes(1, B, K, H, V),
                                 dtype=torch.uint8, device=dev)
+        self.ws_d = torch.empty(dflash_workspace_bytes(2, B, K, H, V),
+                                dtype=torch.uint8, device=dev)
 
     def lmhead(self, h, stream=None):
         dflash_lmhead_topk(h, self.w["w_conv"], self.w["w_lm"], self.topv,
@@ -260,16 +283,25 @@ class DraftVerify:
                       self.q, T, seed, cycle, self.n, self.out, self.ws_v,
                       stream)
 
+    def draft_all(self, h, anchor, T, seed, cycle, stream=None):
+        """Steps a1-a4 in one dflash_draft call (gate inside the conv)."""
+        B, K = self.B, self.K
+        dflash_draft(h, self.w["w_conv"], self.w["w_lm"], self.w["w_gate"],
+                     self.w["e_in"], self.w["e_out"], anchor, T, seed, cycle,
+                     self.topv, self.topi, self.lse, self.scores, self.slot,
+                     self.draft, self.q, self.ws_d, stream)
+
     def cycle(self, h, anchor, L, T, seed, cycle, stream=None):
-        self.lmhead(h, stream)
-        self.pair_score(h, anchor, stream)
-        self.walk(T, seed, cycle, stream)
+        """One draft-verify cycle: dflash_draft + dflash_verify."""
+        self.draft_all(h, anchor, T, seed, cycle, stream)
         self.verify(L, T, seed, cycle, stream)
         return self.n, self.out
 
-    def y(self):
-        """y written by the last lmhead call (conv output, storage dtype)."""
+    def y(self, fused=False):
+        """y written by the last lmhead (or, fused=True, draft_all) call:
+        the conv output in the storage dtype."""
         dt = self.w["w_lm"].dtype
         n = self.B * self.K * self.H
-        return self.ws_lm[: n * (2 if dt == torch.bfloat16 else 4)].view(
+        ws = self.ws_d if fused else self.ws_lm
+        return ws[: n * (2 if dt == torch.bfloat16 else 4)].view(
             dt).view(self.B, self.K, self.H)

@@ -105,11 +105,25 @@ size_t lmhead_ws_layout(int B, int K, int H, int V, void* base, void** y,
   return align256(off);
 }
 
-// bf16 storage: conv and LM head on the tensor cores (tcgen05 + TMA).
+// Workspace of dflash_draft: the LM-head workspace, then the gate
+// [B*K, DFLASH_MAX_RANK] fp32.
+size_t draft_ws_layout(int B, int K, int H, int V, void* base, float** gate) {
+  const size_t lm = align256(lmhead_ws_layout(B, K, H, V, nullptr, nullptr,
+                                              nullptr));
+  if (gate)
+    *gate = reinterpret_cast<float*>(static_cast<char*>(base) + lm);
+  return align256(lm + (size_t)B * K * DFLASH_MAX_RANK * sizeof(float));
+}
+
+// bf16 storage: conv and LM head on the tensor cores (tcgen05 + TMA).  With
+// w_gate (and conv_w) the conv launch also writes the pair selector's gate
+// [B*K, r] fp32 to `gate`.
 dflash_status lmhead_bf16(const __nv_bfloat16* h, const __nv_bfloat16* conv_w,
                           const __nv_bfloat16* w_lm, int B, int K, int H,
                           int V, float* topv, int* topi, float* lse, void* ws,
-                          const DeviceState& d, cudaStream_t s) {
+                          const DeviceState& d, cudaStream_t s,
+                          const __nv_bfloat16* w_gate = nullptr, int r = 0,
+                          float* gate = nullptr) {
   void* yv = nullptr;
   TopkPartials P;
   lmhead_ws_layout(B, K, H, V, ws, &yv, &P);
@@ -117,14 +131,17 @@ dflash_status lmhead_bf16(const __nv_bfloat16* h, const __nv_bfloat16* conv_w,
   const __nv_bfloat16* a = h;
   cudaError_t e;
   if (conv_w) {
-    CUtensorMap mh, mw;
+    CUtensorMap mh, mw, mg;
     if (!make_tmap_bf16_2d(&mh, h, H, M, 64, 128) ||
         !make_tmap_bf16_2d(&mw, conv_w, H, 2 * (uint64_t)H, 64, 32))
+      return DFLASH_ERR_CUDA;
+    if (w_gate && !make_tmap_bf16_2d(&mg, w_gate, H, r, 64, 32))
       return DFLASH_ERR_CUDA;
     __nv_bfloat16* y = static_cast<__nv_bfloat16*>(yv);
     {
       StageTimer tm(kStConv, s);
-      e = launch_conv_tc(mh, mw, h, B, K, H, y, d.err, s);
+      e = launch_conv_tc(mh, mw, w_gate ? &mg : nullptr, h, B, K, H, r, y,
+                         gate, d.err, s);
     }
     if (e != cudaSuccess) return DFLASH_ERR_CUDA;
     a = y;
@@ -198,6 +215,10 @@ size_t dflash_workspace_bytes(int which, int B, int K, int H, int V) {
     return lmhead_ws_layout(B, K, H, V, nullptr, nullptr, nullptr);
   }
   if (which == 1) return verify_ws_layout(B, K, V, nullptr, nullptr);
+  if (which == 2) {
+    if (H < 8) return 0;
+    return draft_ws_layout(B, K, H, V, nullptr, nullptr);
+  }
   return 0;
 }
 
@@ -277,6 +298,58 @@ dflash_status dflash_path_walk(const float* scores, const int32_t* topi,
   StageTimer tm(kStWalk, s);
   return cuda_status(launch_path_walk(scores, topi, B, K, T, seed, cycle,
                                       slot, draft, q, d->err, s));
+}
+
+dflash_status dflash_draft(const void* h, const void* conv_w, const void* w_lm,
+                           const void* w_gate, const void* e_in,
+                           const void* e_out, const int32_t* anchor, int B,
+                           int K, int H, int V, int r, dflash_dtype dt,
+                           float T, uint64_t seed, uint64_t cycle, float* topv,
+                           int32_t* topi, float* lse, float* scores,
+                           int32_t* slot, int32_t* draft, float* q, void* ws,
+                           size_t ws_bytes, dflash_stream_t stream) {
+  REQUIRE(h && w_lm && w_gate && e_in && e_out && anchor && topv && topi &&
+          lse && scores && slot && draft && q && ws);
+  REQUIRE(sizes_ok(B, K, H, V) && H >= 8 && H % 8 == 0 && r >= 1 &&
+          r <= DFLASH_MAX_RANK);
+  REQUIRE(dt == DFLASH_BF16 || dt == DFLASH_FP32);
+  REQUIRE(T >= 0.f && T < INFINITY);
+  REQUIRE(aligned(ws, 256) && aligned(h, 16) && aligned(w_lm, 16) &&
+          aligned(w_gate, 16) && aligned(e_in, 16) && aligned(e_out, 16) &&
+          aligned(scores, 16));
+  REQUIRE(!conv_w || aligned(conv_w, 16));
+  REQUIRE(ws_bytes >= draft_ws_layout(B, K, H, V, nullptr, nullptr));
+  DeviceState* d = nullptr;
+  dflash_status st = device_state(&d);
+  if (st != DFLASH_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  float* gate = nullptr;
+  draft_ws_layout(B, K, H, V, ws, &gate);
+  cudaError_t e;
+  if (dt == DFLASH_BF16 && conv_w) {
+    // the gate rides along with the conv: pair scores only gather and score
+    using bf = __nv_bfloat16;
+    st = lmhead_bf16(static_cast<const bf*>(h), static_cast<const bf*>(conv_w),
+                     static_cast<const bf*>(w_lm), B, K, H, V, topv, topi, lse,
+                     ws, *d, s, static_cast<const bf*>(w_gate), r, gate);
+    if (st != DFLASH_OK) return st;
+    StageTimer tm(kStPair, s);
+    e = launch_pair_score_gated<bf>(topv, topi, anchor, gate,
+                                    static_cast<const bf*>(e_in),
+                                    static_cast<const bf*>(e_out), B, K, V, r,
+                                    scores, d->err, s);
+  } else {
+    st = dflash_lmhead_topk(h, conv_w, w_lm, B, K, H, V, dt, topv, topi, lse,
+                            ws, ws_bytes, stream);
+    if (st != DFLASH_OK) return st;
+    st = dflash_pair_score(topv, topi, anchor, h, w_gate, e_in, e_out, B, K, H,
+                           V, r, dt, scores, stream);
+    if (st != DFLASH_OK) return st;
+    e = cudaSuccess;
+  }
+  if (e != cudaSuccess) return DFLASH_ERR_CUDA;
+  return dflash_path_walk(scores, topi, B, K, T, seed, cycle, slot, draft, q,
+                          stream);
 }
 
 dflash_status dflash_verify(const float* target_logits, const int32_t* draft,

@@ -12,6 +12,12 @@
 // = W0 h, 32-63 = W1 h).  The epilogue (warps 2-5, thread = row) reads both
 // halves, loads h_t and h_{t-1} for the 32 channels, applies the taps in
 // fp32 and writes y rounded to bf16 — the A operand of the LM head.
+//
+// Optionally the same launch also computes the pair selector's context gate
+// g_t = sigmoid(W_g h_t) ("A Lightweight Path Selector", DFlash 2: Keep
+// Drafting Parallel), which reads the same h tiles: extra CTAs after the
+// channel tiles take 64 gate rows each as their B operand (W_g rows
+// [g0, g0+64) in two 32-row boxes) and write g in fp32.
 #include "kernels.h"
 #include "tc_ptx.cuh"
 
@@ -54,8 +60,10 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4& u, float* f) {
 __global__ void __launch_bounds__(THREADS)
     conv_tc_kernel(const __grid_constant__ CUtensorMap map_h,
                    const __grid_constant__ CUtensorMap map_wc,
+                   const __grid_constant__ CUtensorMap map_wg,
                    const __nv_bfloat16* __restrict__ h, int M, int K, int H,
-                   __nv_bfloat16* __restrict__ y, int* err) {
+                   int r, __nv_bfloat16* __restrict__ y,
+                   float* __restrict__ gate, int* err) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -63,7 +71,12 @@ __global__ void __launch_bounds__(THREADS)
   uint8_t* sb = smem + STAGES * A_BYTES;
   Bars* bars = reinterpret_cast<Bars*>(smem + STAGES * STAGE_BYTES);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int c0 = blockIdx.x * BC, mtile = blockIdx.y;
+  // blocks [0, H/32): conv channel tiles; after them: 64-row gate tiles
+  const int conv_tiles = (H + BC - 1) / BC;
+  const bool is_gate = (int)blockIdx.x >= conv_tiles;
+  const int c0 = is_gate ? ((int)blockIdx.x - conv_tiles) * 2 * BC
+                         : (int)blockIdx.x * BC;
+  const int mtile = blockIdx.y;
   const int kblocks = (H + BK - 1) / BK;
 
   if (threadIdx.x == 0) {
@@ -98,9 +111,15 @@ __global__ void __launch_bounds__(THREADS)
         uint8_t* b = sb + stage * B_BYTES;
         tc::tma_load_2d(sa + stage * A_BYTES, &map_h, &bars->full[stage],
                         kb * BK, mtile * BM);
-        tc::tma_load_2d(b, &map_wc, &bars->full[stage], kb * BK, c0);
-        tc::tma_load_2d(b + BC * BK * 2, &map_wc, &bars->full[stage], kb * BK,
-                        H + c0);
+        if (is_gate) {
+          tc::tma_load_2d(b, &map_wg, &bars->full[stage], kb * BK, c0);
+          tc::tma_load_2d(b + BC * BK * 2, &map_wg, &bars->full[stage],
+                          kb * BK, c0 + BC);
+        } else {
+          tc::tma_load_2d(b, &map_wc, &bars->full[stage], kb * BK, c0);
+          tc::tma_load_2d(b + BC * BK * 2, &map_wc, &bars->full[stage],
+                          kb * BK, H + c0);
+        }
         issued |= 1u << stage;
         last_par = (last_par & ~(1u << stage)) | (phase << stage);
         if (++stage == STAGES) { stage = 0; phase ^= 1; }
@@ -144,7 +163,26 @@ __global__ void __launch_bounds__(THREADS)
       float w0[32], w1[32];
       tc::tmem_ld_x32(tb, w0);
       tc::tmem_ld_x32(tb + BC, w1);
-      if (m < M) {
+      if (is_gate) {
+        // columns 0-63 of the accumulator are z for gate rows c0 .. c0+63
+        if (m < M) {
+          float* gr = gate + (size_t)m * r + c0;
+          float g[2 * BC];
+#pragma unroll
+          for (int j = 0; j < 2 * BC; ++j)
+            g[j] = 1.f / (1.f + __expf(-(j < BC ? w0[j] : w1[j - BC])));
+          if (r % 4 == 0 && c0 + 2 * BC <= r) {
+#pragma unroll
+            for (int j = 0; j < 2 * BC; j += 4)
+              *reinterpret_cast<float4*>(gr + j) =
+                  make_float4(g[j], g[j + 1], g[j + 2], g[j + 3]);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 2 * BC; ++j)
+              if (c0 + j < r) gr[j] = g[j];
+          }
+        }
+      } else if (m < M) {
         const bool has_prev = (m % K) != 0;
         const __nv_bfloat16* hr = h + (size_t)m * H + c0;
         __nv_bfloat16* yr = y + (size_t)m * H + c0;
@@ -185,16 +223,18 @@ __global__ void __launch_bounds__(THREADS)
 }  // namespace
 
 cudaError_t launch_conv_tc(const CUtensorMap& map_h, const CUtensorMap& map_wc,
-                           const __nv_bfloat16* h, int B, int K, int H,
-                           __nv_bfloat16* y, int* err, cudaStream_t s) {
+                           const CUtensorMap* map_wg, const __nv_bfloat16* h,
+                           int B, int K, int H, int r, __nv_bfloat16* y,
+                           float* gate, int* err, cudaStream_t s) {
   const int M = B * K;
   cudaError_t e = cudaFuncSetAttribute(
       conv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
       (int)SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  const dim3 grid((H + BC - 1) / BC, (M + BM - 1) / BM);
-  conv_tc_kernel<<<grid, THREADS, SMEM_BYTES, s>>>(map_h, map_wc, h, M, K, H,
-                                                   y, err);
+  const int gate_tiles = map_wg ? (r + 2 * BC - 1) / (2 * BC) : 0;
+  const dim3 grid((H + BC - 1) / BC + gate_tiles, (M + BM - 1) / BM);
+  conv_tc_kernel<<<grid, THREADS, SMEM_BYTES, s>>>(
+      map_h, map_wc, map_wg ? *map_wg : map_wc, h, M, K, H, r, y, gate, err);
   return cudaGetLastError();
 }
 

@@ -254,6 +254,105 @@ __device__ __forceinline__ void gate_partial_simt(
   }
 }
 
+// The 16 x 16 scores of one row (b, t), whole CTA:
+//   S[i][j] = topv[j] + sum_k E_in[pred_i, k] g[k] E_out[cand_j, k]
+// (-inf where pred_i or cand_j is padding).  The embedding rows are staged
+// raw in st ([table][16][r], 0 = E_in) when `vec`, else read from the
+// tables here.  work holds two fp32 tiles of 16 rows; thread tid writes
+// S[tid / 16][tid % 16].
+template <typename T>
+__device__ __forceinline__ void score_row(
+    const T* st, bool vec, const int* pred, const int* cand,
+    const float* g_row, const T* __restrict__ e_in,
+    const T* __restrict__ e_out, int r, float* work,
+    const float* __restrict__ topv_row, float* __restrict__ out) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // fp32 tiles with 16-byte aligned rows when r allows (float4 reads)
+  const bool r4 = (r % 4) == 0;
+  const int rs = r4 ? r + 4 : r + 1;
+  float* ein_s = work;              // [16][rs]
+  float* eout_s = work + kC * rs;   // [16][rs], scaled by the gate
+  if (vec) {
+    // warp w converts staged rows w, w + 8, ...; lane l its 16-byte chunks
+    constexpr int epc = 16 / sizeof(T);  // elements per chunk
+    const int cpr = r / epc;
+    for (int rowi = warp; rowi < 2 * kC; rowi += kWarps) {
+      const bool outt = rowi >= kC;
+      float* dst = (outt ? eout_s : ein_s) + (rowi % kC) * rs;
+      const T* srow = st + (size_t)rowi * r;
+      for (int ch = lane; ch < cpr; ch += 32) {
+        float f[epc > 4 ? 8 : 4];
+        Vec16<T>::to_f32(*reinterpret_cast<const uint4*>(srow + ch * epc), f);
+#pragma unroll
+        for (int e = 0; e < epc; ++e)
+          dst[ch * epc + e] = outt ? f[e] * g_row[ch * epc + e] : f[e];
+      }
+    }
+  } else {
+    for (int i = tid; i < kC * r; i += kThreads) {
+      const int row = i / r, k = i % r;
+      const int a = pred[row], c = cand[row];
+      ein_s[row * rs + k] = a >= 0 ? to_f32(e_in[(size_t)a * r + k]) : 0.f;
+      eout_s[row * rs + k] =
+          c >= 0 ? to_f32(e_out[(size_t)c * r + k]) * g_row[k] : 0.f;
+    }
+  }
+  __syncthreads();
+  const int i = tid / kC, jj = tid % kC;
+  float sc = 0.f;
+  const float* ea = ein_s + i * rs;
+  const float* eb = eout_s + jj * rs;
+  int k = 0;
+  if (r4) {
+    for (; k < r; k += 4) {
+      const float4 a4 = *reinterpret_cast<const float4*>(ea + k);
+      const float4 b4 = *reinterpret_cast<const float4*>(eb + k);
+      sc = fmaf(a4.x, b4.x, sc);
+      sc = fmaf(a4.y, b4.y, sc);
+      sc = fmaf(a4.z, b4.z, sc);
+      sc = fmaf(a4.w, b4.w, sc);
+    }
+  }
+  for (; k < r; ++k) sc = fmaf(ea[k], eb[k], sc);
+  const bool valid = pred[i] >= 0 && cand[jj] >= 0;
+  out[tid] = valid ? topv_row[jj] + sc : -INFINITY;
+}
+
+// Token of (table, slot i) for row m: candidates topi[m, i] (table 1) or
+// their predecessors, the anchor at t = 0 else topi[m - 1, i] (table 0);
+// -1 for padding, and out-of-range ids are flagged and treated as padding.
+__device__ __forceinline__ int row_token(const int* __restrict__ topi,
+                                         const int* __restrict__ anchor, int m,
+                                         int K, int V, int tab, int i,
+                                         int* err) {
+  const int b = m / K, t = m % K;
+  int tok = tab == 1 ? topi[(size_t)m * kC + i]
+                     : (t == 0 ? anchor[b] : topi[(size_t)(m - 1) * kC + i]);
+  if (tok < -1 || tok >= V) {
+    raise_error(err, kErrBadIndex);
+    tok = -1;
+  }
+  return tok;
+}
+
+// Gathers of the 2 x 16 embedding rows of tokens tok[tab][i] into st
+// ([table][16][r]) by 16-byte asynchronous copies; padding rows are zeros.
+template <typename T>
+__device__ __forceinline__ void gather_rows(T* st, const int (*tok)[kC],
+                                            const T* __restrict__ e_in,
+                                            const T* __restrict__ e_out,
+                                            int r) {
+  const int cpr = r * (int)sizeof(T) / 16;  // 16-byte chunks per row
+  for (int idx = threadIdx.x; idx < 2 * kC * cpr; idx += kThreads) {
+    const int rowi = idx / cpr, ch = idx % cpr;  // rowi = tab * 16 + i
+    const int tab = rowi / kC;
+    const int t = tok[tab][rowi % kC];
+    const T* src = (tab == 0 ? e_in : e_out) + (size_t)max(t, 0) * r;
+    cp_async16(st + (size_t)rowi * r + ch * (16 / sizeof(T)),
+               reinterpret_cast<const char*>(src) + ch * 16, t >= 0 ? 16 : 0);
+  }
+}
+
 template <typename T>
 __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads)
     pair_score_kernel(const float* __restrict__ topv,
@@ -290,29 +389,13 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads)
     if (tid < kRowsPerCta * 2 * kC) {
       const int j = tid / (2 * kC), tab = (tid / kC) & 1, i = tid % kC;
       const int m = m0 + crank * kRowsPerCta + j;
-      int tok = -1;
-      if (m < M) {
-        const int b = m / K, t = m % K;
-        tok = tab == 1 ? topi[(size_t)m * kC + i]
-                       : (t == 0 ? anchor[b] : topi[(size_t)(m - 1) * kC + i]);
-        if (tok < -1 || tok >= V) { raise_error(err, kErrBadIndex); tok = -1; }
-      }
-      s_tok[j][tab][i] = tok;
+      s_tok[j][tab][i] = m < M ? row_token(topi, anchor, m, K, V, tab, i, err)
+                               : -1;
     }
     __syncthreads();
-    if (vec) {
-      const int cpr = r * (int)sizeof(T) / 16;  // 16-byte chunks per row
-      const int total = kRowsPerCta * 2 * kC * cpr;
-      for (int idx = tid; idx < total; idx += kThreads) {
-        const int rowi = idx / cpr, ch = idx % cpr;  // rowi = (j*2+tab)*16+i
-        const int tab = (rowi / kC) & 1;
-        const int tok = s_tok[rowi / (2 * kC)][tab][rowi % kC];
-        const T* src = (tab == 0 ? e_in : e_out) + (size_t)max(tok, 0) * r;
-        cp_async16(estage + (size_t)rowi * r + ch * (16 / sizeof(T)),
-                   reinterpret_cast<const char*>(src) + ch * 16,
-                   tok >= 0 ? 16 : 0);
-      }
-    }
+    if (vec)
+      for (int j = 0; j < kRowsPerCta; ++j)
+        gather_rows(estage + (size_t)j * 2 * kC * r, s_tok[j], e_in, e_out, r);
   };
 
   // ---- phase 1: partial z[row][k] over this CTA's hidden slice ----------
@@ -341,66 +424,51 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads)
   cluster.sync();       // peers are done reading this CTA's partials
 
   // ---- phase 3: 16 x 16 scores of each row --------------------------------
-  // fp32 tiles with 16-byte aligned rows when r allows (float4 reads)
-  const bool r4 = (r % 4) == 0;
-  const int rs = r4 ? r + 4 : r + 1;
-  float* ein_s = work;              // [16][rs]
-  float* eout_s = work + kC * rs;   // [16][rs], scaled by the gate
-  const int lane = tid & 31, warp = tid >> 5;
   for (int j = 0; j < kRowsPerCta; ++j) {
     const int m = m0 + crank * kRowsPerCta + j;
     if (m >= M) break;
-    const float* g_row = gate + j * 256;
     if (j > 0) __syncthreads();  // the previous row's tiles are consumed
-    const int* pred = s_tok[j][0];
-    const int* cand = s_tok[j][1];
-    if (vec) {
-      // warp w converts staged rows w, w + 8, ...; lane l its 16-byte chunks
-      constexpr int epc = 16 / sizeof(T);  // elements per chunk
-      const int cpr = r / epc;
-      const T* st = estage + (size_t)j * 2 * kC * r;
-      for (int rowi = warp; rowi < 2 * kC; rowi += kWarps) {
-        const bool out = rowi >= kC;
-        float* dst = (out ? eout_s : ein_s) + (rowi % kC) * rs;
-        const T* srow = st + (size_t)rowi * r;
-        for (int ch = lane; ch < cpr; ch += 32) {
-          float f[epc > 4 ? 8 : 4];
-          Vec16<T>::to_f32(*reinterpret_cast<const uint4*>(srow + ch * epc), f);
-#pragma unroll
-          for (int e = 0; e < epc; ++e)
-            dst[ch * epc + e] = out ? f[e] * g_row[ch * epc + e] : f[e];
-        }
-      }
-    } else {
-      for (int i = tid; i < kC * r; i += kThreads) {
-        const int row = i / r, k = i % r;
-        const int a = pred[row], c = cand[row];
-        ein_s[row * rs + k] = a >= 0 ? to_f32(e_in[(size_t)a * r + k]) : 0.f;
-        eout_s[row * rs + k] =
-            c >= 0 ? to_f32(e_out[(size_t)c * r + k]) * g_row[k] : 0.f;
-      }
-    }
-    __syncthreads();
-    const int i = tid / kC, jj = tid % kC;
-    float sc = 0.f;
-    const float* ea = ein_s + i * rs;
-    const float* eb = eout_s + jj * rs;
-    int k = 0;
-    if (r4) {
-      for (; k < r; k += 4) {
-        const float4 a4 = *reinterpret_cast<const float4*>(ea + k);
-        const float4 b4 = *reinterpret_cast<const float4*>(eb + k);
-        sc = fmaf(a4.x, b4.x, sc);
-        sc = fmaf(a4.y, b4.y, sc);
-        sc = fmaf(a4.z, b4.z, sc);
-        sc = fmaf(a4.w, b4.w, sc);
-      }
-    }
-    for (; k < r; ++k) sc = fmaf(ea[k], eb[k], sc);
-    const bool valid = pred[i] >= 0 && cand[jj] >= 0;
-    scores[(size_t)m * kC * kC + tid] =
-        valid ? topv[(size_t)m * kC + jj] + sc : -INFINITY;
+    score_row(estage + (size_t)j * 2 * kC * r, vec, s_tok[j][0], s_tok[j][1],
+              gate + j * 256, e_in, e_out, r, work, topv + (size_t)m * kC,
+              scores + (size_t)m * kC * kC);
   }
+}
+
+// Pair scores of one row (b, t) per CTA from a precomputed gate: the
+// candidate and predecessor ids, the gate row and the 32 embedding rows
+// come in by asynchronous copies, then score_row.
+template <typename T>
+__global__ void __launch_bounds__(kThreads)
+    pair_score_gated_kernel(const float* __restrict__ topv,
+                            const int* __restrict__ topi,
+                            const int* __restrict__ anchor,
+                            const float* __restrict__ gate,
+                            const T* __restrict__ e_in,
+                            const T* __restrict__ e_out, int K, int V, int r,
+                            float* __restrict__ scores, int* err) {
+  extern __shared__ float4 smem4[];
+  float* g_row = reinterpret_cast<float*>(smem4);        // [256]
+  float* work = g_row + DFLASH_MAX_RANK;                  // two 16-row tiles
+  T* st = reinterpret_cast<T*>(work + 2 * kC * (DFLASH_MAX_RANK + 4));
+  __shared__ int s_tok[2][kC];
+  const int m = blockIdx.x, tid = threadIdx.x;
+  const bool vec = (r * (int)sizeof(T)) % 16 == 0;
+  const float* grow = gate + (size_t)m * r;
+  if (r % 4 == 0) {
+    for (int c = tid; c < r / 4; c += kThreads)
+      cp_async16(g_row + 4 * c, grow + 4 * c, 16);
+  } else {
+    for (int k = tid; k < r; k += kThreads) g_row[k] = grow[k];
+  }
+  if (tid < 2 * kC)
+    s_tok[tid / kC][tid % kC] =
+        row_token(topi, anchor, m, K, V, tid / kC, tid % kC, err);
+  __syncthreads();
+  if (vec) gather_rows(st, s_tok, e_in, e_out, r);
+  cp_async_wait_all();
+  __syncthreads();
+  score_row(st, vec, s_tok[0], s_tok[1], g_row, e_in, e_out, r, work,
+            topv + (size_t)m * kC, scores + (size_t)m * kC * kC);
 }
 
 }  // namespace
@@ -430,6 +498,31 @@ cudaError_t launch_pair_score(const float* topv, const int* topi,
       (int)work, scores, err);
   return cudaGetLastError();
 }
+
+template <typename T>
+cudaError_t launch_pair_score_gated(const float* topv, const int* topi,
+                                    const int* anchor, const float* gate,
+                                    const T* e_in, const T* e_out, int B,
+                                    int K, int V, int r, float* scores,
+                                    int* err, cudaStream_t s) {
+  const size_t smem = (size_t)(DFLASH_MAX_RANK + 2 * kC * (DFLASH_MAX_RANK + 4)) *
+                          sizeof(float) +
+                      (size_t)2 * kC * r * sizeof(T);
+  cudaError_t e = cudaFuncSetAttribute(
+      pair_score_gated_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      (int)smem);
+  if (e != cudaSuccess) return e;
+  pair_score_gated_kernel<T><<<B * K, kThreads, smem, s>>>(
+      topv, topi, anchor, gate, e_in, e_out, K, V, r, scores, err);
+  return cudaGetLastError();
+}
+
+template cudaError_t launch_pair_score_gated<float>(
+    const float*, const int*, const int*, const float*, const float*,
+    const float*, int, int, int, int, float*, int*, cudaStream_t);
+template cudaError_t launch_pair_score_gated<__nv_bfloat16>(
+    const float*, const int*, const int*, const float*, const __nv_bfloat16*,
+    const __nv_bfloat16*, int, int, int, int, float*, int*, cudaStream_t);
 
 template cudaError_t launch_pair_score<float>(const float*, const int*,
                                               const int*, const float*,

@@ -9,6 +9,9 @@
  *   dflash_path_walk    greedy or sampled walk through the K x 16 lattice
  *   dflash_verify       rejection-sampling verify, residual / bonus draw
  *
+ * or two: dflash_draft (the first three in one call, with the context gate
+ * computed inside the conv launch) and dflash_verify.
+ *
  * Sources (page title, section):
  *   "DFlash 2: Block diffusion, wearing a drafter's coat" — "Sixteen
  *     candidates per position", "A path selector", "Suffix-decay
@@ -80,9 +83,9 @@ typedef enum { DFLASH_BF16 = 0, DFLASH_FP32 = 1 } dflash_dtype;
 #define DFLASH_MAX_K 16
 #define DFLASH_MAX_RANK 256
 
-/* Workspace needed by dflash_lmhead_topk (which = 0) or dflash_verify
- * (which = 1) for these sizes, in bytes; an upper bound over both dtypes.
- * Returns 0 for invalid sizes. */
+/* Workspace needed by dflash_lmhead_topk (which = 0), dflash_verify
+ * (which = 1) or dflash_draft (which = 2) for these sizes, in bytes; an
+ * upper bound over both dtypes and every r.  Returns 0 for invalid sizes. */
 size_t dflash_workspace_bytes(int which, int B, int K, int H, int V);
 
 /*
@@ -189,6 +192,38 @@ dflash_status dflash_path_walk(const float* scores, const int32_t* topi,
  * Requirements: target_logits 16-byte aligned; T >= 0.  A NaN or +inf
  * target logit sets DFLASH_ERR_NONFINITE in the device error word.
  */
+/*
+ * Steps a1-a4 in one call: dflash_lmhead_topk, dflash_pair_score and
+ * dflash_path_walk with the same arguments and outputs as those three
+ * calls, in that order ("Suffix-decay convolution" and "Sixteen candidates
+ * per position" of "DFlash 2: Block diffusion, wearing a drafter's coat";
+ * "A Lightweight Path Selector" of "DFlash 2: Keep Drafting Parallel").
+ * For bf16 storage with a conv, the context gate g_t = sigmoid(W_g h_t)
+ * reads the same h tiles as the conv, so it is computed by the conv launch
+ * on the tensor cores and kept in the workspace; the pair scores then only
+ * gather embedding rows.  Otherwise the three steps run as the separate
+ * calls do.
+ *   inputs   h, conv_w (may be NULL: no conv), w_lm, w_gate, e_in, e_out,
+ *            anchor, sizes, dt, T, seed, cycle: as in the three calls
+ *   outputs  topv, topi, lse (dflash_lmhead_topk), scores
+ *            (dflash_pair_score), slot, draft, q (dflash_path_walk)
+ *   ws       >= dflash_workspace_bytes(2, B, K, H, V) bytes, 256-byte
+ *            aligned, caller-owned; holds y, the LM-head partials and the
+ *            gate.
+ * Requirements: the union of the three calls' (h, w_lm, w_gate, e_in,
+ * e_out, scores 16-byte aligned; H % 8 == 0; 1 <= r <= 256; T >= 0).
+ * Results equal the three calls' up to the order of fp32 accumulation in
+ * the gate.
+ */
+dflash_status dflash_draft(const void* h, const void* conv_w, const void* w_lm,
+                           const void* w_gate, const void* e_in,
+                           const void* e_out, const int32_t* anchor, int B,
+                           int K, int H, int V, int r, dflash_dtype dt,
+                           float T, uint64_t seed, uint64_t cycle, float* topv,
+                           int32_t* topi, float* lse, float* scores,
+                           int32_t* slot, int32_t* draft, float* q, void* ws,
+                           size_t ws_bytes, dflash_stream_t s);
+
 dflash_status dflash_verify(const float* target_logits, const int32_t* draft,
                             const int32_t* topi, const float* q, int B, int K,
                             int V, float T, uint64_t seed, uint64_t cycle,

@@ -70,6 +70,49 @@ def run_stagewise(lib, w, x, L, seed=7, cycle=3):
     return {"ties": ties, "n": np_(dv.n), "out": np_(dv.out), "dv": dv}
 
 
+def run_fused(lib, w, x, L, seed=7, cycle=3):
+    """dflash_draft (steps a1-a4 in one call, the gate computed inside the
+    conv launch for bf16) then dflash_verify; every output is checked
+    against the oracle fed with the CUDA path's own upstream outputs."""
+    B, K, H, V, r = w.B, w.K, w.H, w.V, w.r
+    h = to_dev(x["h"][:, :K])
+    anchor = to_dev(x["anchor"])
+    Ld = to_dev(L)
+    dv = lib.DraftVerify(B, K, H, V, r, _weights(x))
+    ties = {}
+    dv.draft_all(h, anchor, w.T, seed, cycle)
+    torch.cuda.synchronize()
+    lib.dflash_check()
+    h64 = f64(h)
+    if x["w_conv"] is not None:
+        y = dv.y(fused=True)
+        W = f64(x["w_conv"])
+        ties["y"] = check_y(y, oracle.conv2tap(h64, W),
+                            oracle.conv2tap(np.abs(h64), np.abs(W)), w.dtype)
+        y64 = f64(y).reshape(-1, H)
+    else:
+        y64 = h64.reshape(-1, H)
+    W_lm = f64(x["w_lm"])
+    ref = oracle.lmhead_topk(y64, W_lm, want_logits=True)
+    A = np.abs(y64) @ np.abs(W_lm).T
+    ties["topk"] = check_topk(dv.topv, dv.topi, dv.lse, ref, A, ERR_C[w.dtype])
+    topv = np_(dv.topv).reshape(B, K, C)
+    topi = np_(dv.topi).reshape(B, K, C)
+    g = oracle.gate(h64, f64(x["w_gate"]))
+    S = oracle.pair_score(topv, topi, np_(anchor), g, f64(x["e_in"]),
+                          f64(x["e_out"]))
+    check_scores(dv.scores, S)
+    S32 = np_(dv.scores)
+    ties["walk"] = check_walk(dv.slot, dv.draft, dv.q, S32, topi, w.T, seed,
+                              cycle, 1e-5)
+    dv.verify(Ld, w.T, seed, cycle)
+    torch.cuda.synchronize()
+    lib.dflash_check()
+    ties["verify"], _, _ = check_verify(dv.n, dv.out, np_(Ld), np_(dv.draft),
+                                        topi, np_(dv.q), w.T, seed, cycle)
+    return {"ties": ties, "n": np_(dv.n), "out": np_(dv.out), "dv": dv}
+
+
 def _make(w):
     x = synth.make_inputs(w)
     L = synth.target_logits(w, draft_logits_oracle(x, w))
@@ -312,3 +355,57 @@ def test_full_size_workload(lib, name):
     x, L = _make(w)
     r = run_stagewise(lib, w, x, L, seed=w.seed, cycle=0)
     print(name, "ties", r["ties"], "mean accepted", r["n"].mean())
+
+
+# --------------------------------------------------------------------------
+# dflash_draft: steps a1-a4 in one call
+@pytest.mark.parametrize("B,K,H,V,r,T", [
+    (3, 5, 192, 5003, 64, 1.0),     # ragged V, one row tile
+    (9, 3, 128, 2051, 40, 1.5),     # r not a multiple of 64 (partial gate tile)
+    (5, 3, 200, 1999, 48, 0.0),     # ragged K tail, greedy
+    (20, 15, 136, 4099, 256, 1.0),  # M = 300: CTA pairs, full rank
+])
+def test_fused_draft_bf16(lib, B, K, H, V, r, T):
+    w = synth.Workload("small", B=B, K=K, V=V, H=H, r=r, dtype="bf16", T=T,
+                       seed=31 + B, w_lm_sd=0.1, conv_sd=0.05, sel_sd=0.1,
+                       target=("affine", 0.9, 1.0))
+    x, L = _make(w)
+    run_fused(lib, w, x, L)
+
+
+@pytest.mark.parametrize("name,T", [("tiny", 1.0), ("tiny_conv", 0.0)])
+def test_fused_draft_fp32(lib, name, T):
+    """fp32 storage (and no conv) take the separate kernels inside the call."""
+    w = synth.get(name, T=T)
+    x, L = _make(w)
+    r = run_fused(lib, w, x, L)
+    assert r["ties"]["topk"] == 0
+
+
+def test_fused_draft_matches_separate_calls(lib):
+    """Same LM head kernels: identical candidates; scores within the fp32
+    tolerance (the gate's accumulation order differs)."""
+    w = synth.Workload("small", B=6, K=8, V=3001, H=256, r=256, dtype="bf16",
+                       T=1.0, seed=5, w_lm_sd=0.1, conv_sd=0.05, sel_sd=0.1,
+                       target=("affine", 0.9, 1.0))
+    x = synth.make_inputs(w)
+    h = to_dev(x["h"][:, :w.K])
+    anchor = to_dev(x["anchor"])
+    a = lib.DraftVerify(w.B, w.K, w.H, w.V, w.r, _weights(x))
+    b = lib.DraftVerify(w.B, w.K, w.H, w.V, w.r, _weights(x))
+    a.lmhead(h)
+    a.pair_score(h, anchor)
+    b.draft_all(h, anchor, w.T, 7, 3)
+    torch.cuda.synchronize()
+    lib.dflash_check()
+    assert torch.equal(a.topi, b.topi) and torch.equal(a.topv, b.topv)
+    assert torch.equal(a.lse, b.lse)
+    np.testing.assert_allclose(np_(b.scores), np_(a.scores), rtol=1e-5,
+                               atol=1e-5)
+
+
+def test_fused_draft_full_size_b32k8(lib):
+    w = synth.get("b32k8")
+    x, L = _make(w)
+    r = run_fused(lib, w, x, L, seed=w.seed, cycle=0)
+    print("b32k8 fused ties", r["ties"], "mean accepted", r["n"].mean())
