@@ -405,11 +405,21 @@ def run_ours(args):
     for si in range(len(stages)):
         dv_mod.dflash_profile_stage(si, None, None)
     dv_mod.dflash_check()
+    # dflash_draft with bf16 storage and a conv runs three kernels: the conv
+    # (with the context gate), the LM head, and one launch that merges the
+    # LM head's partials, scores the pairs and walks (recorded as the
+    # pair-score stage); otherwise the per-step kernels
+    fused = w.dtype == "bf16" and w.conv_sd is not None
+    names = ({"conv": "conv+gate", "lmhead": "lmhead",
+              "pair_score": "merge+pair_score+walk", "verify": "verify"}
+             if fused else {n: n for n in stages})
     stage_us = {}
     for si, name in enumerate(stages):
         if name == "conv" and w.conv_sd is None:
             continue
-        stage_us[name] = statistics.mean(
+        if name not in names:
+            continue
+        stage_us[names[name]] = statistics.mean(
             ev[i][si][0].elapsed_time(ev[i][si][1]) * 1e3 for i in range(KS))
 
     # roofline of the dominant kernel (the LM head)
@@ -481,7 +491,8 @@ def run_ours(args):
     if rank != 0:
         return 0
     n_mean = float(np.mean(n_hist))
-    launches_per_step = (3 if w.conv_sd is not None else 2) + 3
+    launches_per_step = (4 if w.dtype == "bf16" and w.conv_sd is not None
+                         else (3 if w.conv_sd is not None else 2) + 3)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": 1e3 * secs_max / K,

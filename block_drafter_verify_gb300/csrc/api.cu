@@ -106,13 +106,17 @@ size_t lmhead_ws_layout(int B, int K, int H, int V, void* base, void** y,
 }
 
 // Workspace of dflash_draft: the LM-head workspace, then the gate
-// [B*K, DFLASH_MAX_RANK] fp32.
-size_t draft_ws_layout(int B, int K, int H, int V, void* base, float** gate) {
+// [B*K, DFLASH_MAX_RANK] fp32, then one walk ticket per sequence.
+size_t draft_ws_layout(int B, int K, int H, int V, void* base, float** gate,
+                       unsigned** tickets = nullptr) {
   const size_t lm = align256(lmhead_ws_layout(B, K, H, V, nullptr, nullptr,
                                               nullptr));
+  const size_t g = align256((size_t)B * K * DFLASH_MAX_RANK * sizeof(float));
   if (gate)
     *gate = reinterpret_cast<float*>(static_cast<char*>(base) + lm);
-  return align256(lm + (size_t)B * K * DFLASH_MAX_RANK * sizeof(float));
+  if (tickets)
+    *tickets = reinterpret_cast<unsigned*>(static_cast<char*>(base) + lm + g);
+  return align256(lm + g + (size_t)B * sizeof(unsigned));
 }
 
 // bf16 storage: conv and LM head on the tensor cores (tcgen05 + TMA).  With
@@ -123,7 +127,9 @@ dflash_status lmhead_bf16(const __nv_bfloat16* h, const __nv_bfloat16* conv_w,
                           int V, float* topv, int* topi, float* lse, void* ws,
                           const DeviceState& d, cudaStream_t s,
                           const __nv_bfloat16* w_gate = nullptr, int r = 0,
-                          float* gate = nullptr) {
+                          float* gate = nullptr, unsigned* tickets = nullptr,
+                          TopkPartials* P_out = nullptr,
+                          int* strips_out = nullptr) {
   void* yv = nullptr;
   TopkPartials P;
   lmhead_ws_layout(B, K, H, V, ws, &yv, &P);
@@ -141,7 +147,7 @@ dflash_status lmhead_bf16(const __nv_bfloat16* h, const __nv_bfloat16* conv_w,
     {
       StageTimer tm(kStConv, s);
       e = launch_conv_tc(mh, mw, w_gate ? &mg : nullptr, h, B, K, H, r, y,
-                         gate, d.err, s);
+                         gate, tickets, d.err, s);
     }
     if (e != cudaSuccess) return DFLASH_ERR_CUDA;
     a = y;
@@ -156,6 +162,11 @@ dflash_status lmhead_bf16(const __nv_bfloat16* h, const __nv_bfloat16* conv_w,
     e = launch_lmhead_tc(my, mw, M, H, V, d.sms, P, d.err, &strips, s);
   }
   if (e != cudaSuccess) return DFLASH_ERR_CUDA;
+  if (P_out) {  // the caller merges (draft tail)
+    *P_out = P;
+    *strips_out = strips;
+    return DFLASH_OK;
+  }
   StageTimer tm(kStMerge, s);
   return cuda_status(launch_topk_merge(P, strips, M, topv, topi, lse, s));
 }
@@ -324,20 +335,26 @@ dflash_status dflash_draft(const void* h, const void* conv_w, const void* w_lm,
   if (st != DFLASH_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   float* gate = nullptr;
-  draft_ws_layout(B, K, H, V, ws, &gate);
+  unsigned* tickets = nullptr;
+  draft_ws_layout(B, K, H, V, ws, &gate, &tickets);
   cudaError_t e;
   if (dt == DFLASH_BF16 && conv_w) {
-    // the gate rides along with the conv: pair scores only gather and score
+    // The gate rides along with the conv (which also zeroes the walk
+    // tickets); one launch after the LM head merges its partials, scores
+    // the pairs and walks each sequence.
     using bf = __nv_bfloat16;
+    TopkPartials P;
+    int strips = 0;
     st = lmhead_bf16(static_cast<const bf*>(h), static_cast<const bf*>(conv_w),
                      static_cast<const bf*>(w_lm), B, K, H, V, topv, topi, lse,
-                     ws, *d, s, static_cast<const bf*>(w_gate), r, gate);
+                     ws, *d, s, static_cast<const bf*>(w_gate), r, gate,
+                     tickets, &P, &strips);
     if (st != DFLASH_OK) return st;
     StageTimer tm(kStPair, s);
-    e = launch_pair_score_gated<bf>(topv, topi, anchor, gate,
-                                    static_cast<const bf*>(e_in),
-                                    static_cast<const bf*>(e_out), B, K, V, r,
-                                    scores, d->err, s);
+    return cuda_status(launch_draft_tail<bf>(
+        P, strips, anchor, gate, static_cast<const bf*>(e_in),
+        static_cast<const bf*>(e_out), B, K, V, r, T, seed, cycle, topv, topi,
+        lse, scores, slot, draft, q, tickets, d->err, s));
   } else {
     st = dflash_lmhead_topk(h, conv_w, w_lm, B, K, H, V, dt, topv, topi, lse,
                             ws, ws_bytes, stream);

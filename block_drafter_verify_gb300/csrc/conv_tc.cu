@@ -63,7 +63,8 @@ __global__ void __launch_bounds__(THREADS)
                    const __grid_constant__ CUtensorMap map_wg,
                    const __nv_bfloat16* __restrict__ h, int M, int K, int H,
                    int r, __nv_bfloat16* __restrict__ y,
-                   float* __restrict__ gate, int* err) {
+                   float* __restrict__ gate, unsigned* __restrict__ tickets,
+                   int ntickets, int* err) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -79,6 +80,8 @@ __global__ void __launch_bounds__(THREADS)
   const int mtile = blockIdx.y;
   const int kblocks = (H + BK - 1) / BK;
 
+  if (tickets && blockIdx.x == 0 && blockIdx.y == 0)
+    for (int i = threadIdx.x; i < ntickets; i += THREADS) tickets[i] = 0u;
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       tc::mbar_init(&bars->full[s], 1);
@@ -225,7 +228,8 @@ __global__ void __launch_bounds__(THREADS)
 cudaError_t launch_conv_tc(const CUtensorMap& map_h, const CUtensorMap& map_wc,
                            const CUtensorMap* map_wg, const __nv_bfloat16* h,
                            int B, int K, int H, int r, __nv_bfloat16* y,
-                           float* gate, int* err, cudaStream_t s) {
+                           float* gate, unsigned* tickets, int* err,
+                           cudaStream_t s) {
   const int M = B * K;
   cudaError_t e = cudaFuncSetAttribute(
       conv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -234,7 +238,8 @@ cudaError_t launch_conv_tc(const CUtensorMap& map_h, const CUtensorMap& map_wc,
   const int gate_tiles = map_wg ? (r + 2 * BC - 1) / (2 * BC) : 0;
   const dim3 grid((H + BC - 1) / BC + gate_tiles, (M + BM - 1) / BM);
   conv_tc_kernel<<<grid, THREADS, SMEM_BYTES, s>>>(
-      map_h, map_wc, map_wg ? *map_wg : map_wc, h, M, K, H, r, y, gate, err);
+      map_h, map_wc, map_wg ? *map_wg : map_wc, h, M, K, H, r, y, gate,
+      tickets, B, err);
   return cudaGetLastError();
 }
 

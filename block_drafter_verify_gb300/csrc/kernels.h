@@ -21,11 +21,13 @@ bool make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner,
                        uint64_t rows, uint32_t box_inner, uint32_t box_rows);
 // map_h: h [B*K, H] box {64, 128}; map_wc: conv_w [2H, H] box {64, 32}.
 // With map_wg (w_gate [r, H], box {64, 32}) the launch also writes the pair
-// selector's gate g = sigmoid(W_g h) as gate [B*K, r] fp32.
+// selector's gate g = sigmoid(W_g h) as gate [B*K, r] fp32.  tickets (B
+// words, may be NULL) are zeroed for a later launch of the same call.
 cudaError_t launch_conv_tc(const CUtensorMap& map_h, const CUtensorMap& map_wc,
                            const CUtensorMap* map_wg, const __nv_bfloat16* h,
                            int B, int K, int H, int r, __nv_bfloat16* y,
-                           float* gate, int* err, cudaStream_t s);
+                           float* gate, unsigned* tickets, int* err,
+                           cudaStream_t s);
 // map_y: y [M, H] box {64, 128}; map_w: w_lm [V, H] box {64, 256}, or
 // {64, 128} when lmhead_tc_pairs(M) (CTA pairs, two or more row tiles).
 // Writes `*strips` partial lists per row.
@@ -44,6 +46,17 @@ cudaError_t launch_topk_merge(TopkPartials P, int nstrip, int M, float* topv,
                               int* topi, float* lse, cudaStream_t s);
 
 // pair_score.cu -----------------------------------------------------------
+// After the LM head, for a precomputed gate [B*K, r] fp32: merge of the
+// strip partials, pair scores and walk in one launch (tickets [B], zeroed
+// by the conv launch, pick each sequence's walker).
+template <typename T>
+cudaError_t launch_draft_tail(TopkPartials P, int nstrip, const int* anchor,
+                              const float* gate, const T* e_in,
+                              const T* e_out, int B, int K, int V, int r,
+                              float T_, uint64_t seed, uint64_t cycle,
+                              float* topv, int* topi, float* lse,
+                              float* scores, int* slot, int* draft, float* q,
+                              unsigned* tickets, int* err, cudaStream_t s);
 // Pair scores from a precomputed gate [B*K, r] fp32 (gathers + bilinear).
 template <typename T>
 cudaError_t launch_pair_score_gated(const float* topv, const int* topi,

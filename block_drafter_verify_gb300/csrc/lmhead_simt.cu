@@ -16,6 +16,7 @@
 #include <climits>
 
 #include "kernels.h"
+#include "merge.cuh"
 
 namespace dflash {
 namespace {
@@ -33,11 +34,6 @@ __device__ __forceinline__ void list_insert(float& tv, int& ti, float xv,
     if (lane > pos) { tv = pv; ti = pi; }
     else if (lane == pos) { tv = xv; ti = xi; }
   }
-}
-
-__device__ __forceinline__ bool ranks_ahead(float v1, int i1, float v2,
-                                            int i2) {
-  return v1 > v2 || (v1 == v2 && (unsigned)i1 < (unsigned)i2);
 }
 
 template <typename T>
@@ -102,30 +98,7 @@ __global__ void __launch_bounds__(kThreads)
   }
 }
 
-// One CTA of eight warps per row.  Warp w prefetches the lists of strips
-// w, w+8, ... (all loads in flight at once) and folds each into a sorted
-// top-16 held by lanes 0..15 with a bitonic merge: lanes 0..15 hold the
-// current list best-first, lanes 16..31 the new list worst-first, and five
-// compare-exchange steps (distance 16, 8, 4, 2, 1) sort the 32 entries.  A
-// list whose best entry does not beat the current 16th is skipped.  Warp 0
-// then merges the eight warp lists in warp order; (max, sum) pairs are
-// folded per warp in strip order and then in warp order.  The result does
-// not depend on timing.
-constexpr int kMergeWarps = 8;
-constexpr int kMaxPerWarp = (kMaxStrips + kMergeWarps - 1) / kMergeWarps;
-
-// One bitonic merge: (v, i) on lanes 0..15 = current list, lanes 16..31 =
-// candidate list reversed; returns with lanes 0..15 = the best 16, sorted.
-__device__ __forceinline__ void bitonic_merge32(float& v, int& i, int lane) {
-#pragma unroll
-  for (int d = 16; d; d >>= 1) {
-    const float ov = __shfl_xor_sync(0xffffffffu, v, d);
-    const int oi = __shfl_xor_sync(0xffffffffu, i, d);
-    const bool lower = (lane & d) == 0;
-    if (lower == ranks_ahead(ov, oi, v, i)) { v = ov; i = oi; }
-  }
-}
-
+// One CTA of eight warps per row: the merge of merge.cuh.
 __global__ void __launch_bounds__(kMergeWarps * 32)
     topk_merge_kernel(TopkPartials P, int nstrip, int M, float* topv,
                       int* topi, float* lse) {
@@ -133,57 +106,14 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
   const int m = blockIdx.x;
   __shared__ float s_v[kMergeWarps][kC], s_m[kMergeWarps], s_s[kMergeWarps];
   __shared__ int s_i[kMergeWarps][kC];
-  const size_t base = (size_t)m * nstrip;
-  const int k = lane < kC ? lane : 31 - lane;  // lanes 16..31: reversed
-  float nv[kMaxPerWarp], pm[kMaxPerWarp], ps[kMaxPerWarp];
-  int ni[kMaxPerWarp];
-#pragma unroll
-  for (int j = 0; j < kMaxPerWarp; ++j) {  // every load in flight at once
-    const int st = warp + j * kMergeWarps;
-    nv[j] = -INFINITY;
-    ni[j] = -1;
-    pm[j] = -INFINITY;
-    ps[j] = 0.f;
-    if (st < nstrip) {
-      nv[j] = P.v[(base + st) * kC + k];
-      ni[j] = P.i[(base + st) * kC + k];
-      pm[j] = P.m[base + st];
-      ps[j] = P.s[base + st];
-    }
-  }
-  float tv = -INFINITY;
-  int ti = -1;
-  float rm = -INFINITY, rs = 0.f;
-#pragma unroll
-  for (int j = 0; j < kMaxPerWarp; ++j) {
-    const int st = warp + j * kMergeWarps;
-    if (st >= nstrip) break;
-    lse_combine(rm, rs, pm[j], ps[j], 1.f);
-    const float bv = __shfl_sync(0xffffffffu, nv[j], 0);
-    const int bi = __shfl_sync(0xffffffffu, ni[j], 0);
-    if (!ranks_ahead(bv, bi, __shfl_sync(0xffffffffu, tv, kC - 1),
-                     __shfl_sync(0xffffffffu, ti, kC - 1)))
-      continue;  // nothing in this list enters the top 16
-    float v = lane < kC ? tv : nv[j];
-    int i = lane < kC ? ti : ni[j];
-    bitonic_merge32(v, i, lane);
-    tv = v;
-    ti = i;
-  }
+  float tv, rm, rs;
+  int ti;
+  merge_fold_warp(P, nstrip, m, warp, lane, tv, ti, rm, rs);
   if (lane < kC) { s_v[warp][lane] = tv; s_i[warp][lane] = ti; }
   if (lane == 0) { s_m[warp] = rm; s_s[warp] = rs; }
   __syncthreads();
   if (warp != 0) return;
-  for (int w2 = 1; w2 < kMergeWarps; ++w2) {
-    if (lane == 0) lse_combine(rm, rs, s_m[w2], s_s[w2], 1.f);
-    const float cv = s_v[w2][k];
-    const int ci = s_i[w2][k];
-    float v = lane < kC ? tv : cv;
-    int i = lane < kC ? ti : ci;
-    bitonic_merge32(v, i, lane);
-    tv = v;
-    ti = i;
-  }
+  merge_combine(s_v, s_i, s_m, s_s, lane, tv, ti, rm, rs);
   if (lane < kC) {
     topv[(size_t)m * kC + lane] = tv;
     topi[(size_t)m * kC + lane] = ti;

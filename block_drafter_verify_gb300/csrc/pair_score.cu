@@ -26,6 +26,7 @@
 #include <type_traits>
 
 #include "kernels.h"
+#include "merge.cuh"
 
 namespace cg = cooperative_groups;
 
@@ -77,6 +78,13 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src,
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(
                    static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
                "l"(src), "r"(src_bytes)
+               : "memory");
+}
+// 4-byte asynchronous copy global -> shared.
+__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(
+                   static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
+               "l"(src)
                : "memory");
 }
 __device__ __forceinline__ void cp_async_wait_all() {
@@ -258,9 +266,9 @@ __device__ __forceinline__ void gate_partial_simt(
 //   S[i][j] = topv[j] + sum_k E_in[pred_i, k] g[k] E_out[cand_j, k]
 // (-inf where pred_i or cand_j is padding).  The embedding rows are staged
 // raw in st ([table][16][r], 0 = E_in) when `vec`, else read from the
-// tables here.  work holds two fp32 tiles of 16 rows; thread tid writes
-// S[tid / 16][tid % 16].
-template <typename T>
+// tables here.  work holds two fp32 tiles of 16 rows; thread tid < 128
+// writes S[tid / 16][tid % 16] and S[tid / 16 + 8][tid % 16].
+template <int NT, typename T>
 __device__ __forceinline__ void score_row(
     const T* st, bool vec, const int* pred, const int* cand,
     const float* g_row, const T* __restrict__ e_in,
@@ -276,20 +284,33 @@ __device__ __forceinline__ void score_row(
     // warp w converts staged rows w, w + 8, ...; lane l its 16-byte chunks
     constexpr int epc = 16 / sizeof(T);  // elements per chunk
     const int cpr = r / epc;
-    for (int rowi = warp; rowi < 2 * kC; rowi += kWarps) {
+    for (int rowi = warp; rowi < 2 * kC; rowi += NT / 32) {
       const bool outt = rowi >= kC;
       float* dst = (outt ? eout_s : ein_s) + (rowi % kC) * rs;
       const T* srow = st + (size_t)rowi * r;
       for (int ch = lane; ch < cpr; ch += 32) {
         float f[epc > 4 ? 8 : 4];
         Vec16<T>::to_f32(*reinterpret_cast<const uint4*>(srow + ch * epc), f);
+        if (r4) {  // 16-byte stores (rows are 16-byte aligned)
 #pragma unroll
-        for (int e = 0; e < epc; ++e)
-          dst[ch * epc + e] = outt ? f[e] * g_row[ch * epc + e] : f[e];
+          for (int e = 0; e < epc; e += 4) {
+            float4 o = make_float4(f[e], f[e + 1], f[e + 2], f[e + 3]);
+            if (outt) {
+              const float4 g4 =
+                  *reinterpret_cast<const float4*>(g_row + ch * epc + e);
+              o.x *= g4.x; o.y *= g4.y; o.z *= g4.z; o.w *= g4.w;
+            }
+            *reinterpret_cast<float4*>(dst + ch * epc + e) = o;
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < epc; ++e)
+            dst[ch * epc + e] = outt ? f[e] * g_row[ch * epc + e] : f[e];
+        }
       }
     }
   } else {
-    for (int i = tid; i < kC * r; i += kThreads) {
+    for (int i = tid; i < kC * r; i += NT) {
       const int row = i / r, k = i % r;
       const int a = pred[row], c = cand[row];
       ein_s[row * rs + k] = a >= 0 ? to_f32(e_in[(size_t)a * r + k]) : 0.f;
@@ -298,24 +319,41 @@ __device__ __forceinline__ void score_row(
     }
   }
   __syncthreads();
+  // thread tid < 128: outputs (i, jj) and (i + 8, jj), sharing eb's loads
+  if (tid >= kC * kC / 2) return;
   const int i = tid / kC, jj = tid % kC;
-  float sc = 0.f;
   const float* ea = ein_s + i * rs;
+  const float* ea8 = ein_s + (i + 8) * rs;
   const float* eb = eout_s + jj * rs;
+  float sc = 0.f, sd = 0.f;
   int k = 0;
-  if (r4) {
+  if (r4) {  // four partial sums (k mod 4) per output, added at the end
+    float s1 = 0.f, s2 = 0.f, s3 = 0.f, d1 = 0.f, d2 = 0.f, d3 = 0.f;
+#pragma unroll 4
     for (; k < r; k += 4) {
-      const float4 a4 = *reinterpret_cast<const float4*>(ea + k);
       const float4 b4 = *reinterpret_cast<const float4*>(eb + k);
+      const float4 a4 = *reinterpret_cast<const float4*>(ea + k);
+      const float4 c4 = *reinterpret_cast<const float4*>(ea8 + k);
       sc = fmaf(a4.x, b4.x, sc);
-      sc = fmaf(a4.y, b4.y, sc);
-      sc = fmaf(a4.z, b4.z, sc);
-      sc = fmaf(a4.w, b4.w, sc);
+      s1 = fmaf(a4.y, b4.y, s1);
+      s2 = fmaf(a4.z, b4.z, s2);
+      s3 = fmaf(a4.w, b4.w, s3);
+      sd = fmaf(c4.x, b4.x, sd);
+      d1 = fmaf(c4.y, b4.y, d1);
+      d2 = fmaf(c4.z, b4.z, d2);
+      d3 = fmaf(c4.w, b4.w, d3);
     }
+    sc = (sc + s1) + (s2 + s3);
+    sd = (sd + d1) + (d2 + d3);
   }
-  for (; k < r; ++k) sc = fmaf(ea[k], eb[k], sc);
-  const bool valid = pred[i] >= 0 && cand[jj] >= 0;
-  out[tid] = valid ? topv_row[jj] + sc : -INFINITY;
+  for (; k < r; ++k) {
+    sc = fmaf(ea[k], eb[k], sc);
+    sd = fmaf(ea8[k], eb[k], sd);
+  }
+  const float tj = topv_row[jj];
+  const bool cj = cand[jj] >= 0;
+  out[i * kC + jj] = (pred[i] >= 0 && cj) ? tj + sc : -INFINITY;
+  out[(i + 8) * kC + jj] = (pred[i + 8] >= 0 && cj) ? tj + sd : -INFINITY;
 }
 
 // Token of (table, slot i) for row m: candidates topi[m, i] (table 1) or
@@ -337,13 +375,13 @@ __device__ __forceinline__ int row_token(const int* __restrict__ topi,
 
 // Gathers of the 2 x 16 embedding rows of tokens tok[tab][i] into st
 // ([table][16][r]) by 16-byte asynchronous copies; padding rows are zeros.
-template <typename T>
+template <typename T, int NT = kThreads>
 __device__ __forceinline__ void gather_rows(T* st, const int (*tok)[kC],
                                             const T* __restrict__ e_in,
                                             const T* __restrict__ e_out,
                                             int r) {
   const int cpr = r * (int)sizeof(T) / 16;  // 16-byte chunks per row
-  for (int idx = threadIdx.x; idx < 2 * kC * cpr; idx += kThreads) {
+  for (int idx = threadIdx.x; idx < 2 * kC * cpr; idx += NT) {
     const int rowi = idx / cpr, ch = idx % cpr;  // rowi = tab * 16 + i
     const int tab = rowi / kC;
     const int t = tok[tab][rowi % kC];
@@ -428,7 +466,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads)
     const int m = m0 + crank * kRowsPerCta + j;
     if (m >= M) break;
     if (j > 0) __syncthreads();  // the previous row's tiles are consumed
-    score_row(estage + (size_t)j * 2 * kC * r, vec, s_tok[j][0], s_tok[j][1],
+    score_row<kThreads>(estage + (size_t)j * 2 * kC * r, vec, s_tok[j][0], s_tok[j][1],
               gate + j * 256, e_in, e_out, r, work, topv + (size_t)m * kC,
               scores + (size_t)m * kC * kC);
   }
@@ -467,8 +505,305 @@ __global__ void __launch_bounds__(kThreads)
   if (vec) gather_rows(st, s_tok, e_in, e_out, r);
   cp_async_wait_all();
   __syncthreads();
-  score_row(st, vec, s_tok[0], s_tok[1], g_row, e_in, e_out, r, work,
-            topv + (size_t)m * kC, scores + (size_t)m * kC * kC);
+  score_row<kThreads>(st, vec, s_tok[0], s_tok[1], g_row, e_in, e_out, r,
+                      work, topv + (size_t)m * kC,
+                      scores + (size_t)m * kC * kC);
+}
+
+// Merge of one row's nstrip strip lists staged in shared memory (sv/si
+// [nstrip][16], best first; sm/ss [nstrip] pairs) by a group of warps:
+// warp gw of ngw takes the lists gw, gw + ngw, ...: it sorts their best
+// entries (a warp bitonic sort) and folds the lists in that order with
+// bitonic merges, stopping at the first list whose best entry cannot enter
+// the top-16 (so at most 16 merges); then the group's first warp merges the
+// group's lists in warp order.  Same top-16 as topk_merge_kernel; lse may
+// differ in the last bits (another summation order).
+__device__ __forceinline__ void fold_lists_smem(const float* sv,
+                                                const int* si,
+                                                const float* sm,
+                                                const float* ss, int nstrip,
+                                                int gw, int ngw, float& tv,
+                                                int& ti, float& rm,
+                                                float& rs) {
+  const int lane = threadIdx.x & 31;
+  const int k = lane < kC ? lane : 31 - lane;  // lanes 16..31: reversed
+  const int nl = gw < nstrip ? (nstrip - gw + ngw - 1) / ngw : 0;  // lists
+  tv = -INFINITY;
+  ti = -1;
+  // pairs: each lane folds its lists in order, then lanes in a fixed tree
+  rm = -INFINITY;
+  rs = 0.f;
+  for (int j = lane; j < nl; j += 32) {
+    const int st = gw + ngw * j;
+    lse_combine(rm, rs, sm[st], ss[st], 1.f);
+  }
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float om = __shfl_down_sync(0xffffffffu, rm, o);
+    const float os = __shfl_down_sync(0xffffffffu, rs, o);
+    if (lane + o < 32) lse_combine(rm, rs, om, os, 1.f);
+  }
+  rm = __shfl_sync(0xffffffffu, rm, 0);
+  rs = __shfl_sync(0xffffffffu, rs, 0);
+  // top-16: 32 lists at a time, taken in the order of their best entries;
+  // once a list's best cannot enter the top-16, no later one can
+  for (int j0 = 0; j0 < nl; j0 += 32) {
+    const int j = j0 + lane;
+    float hv = -INFINITY;
+    int hi = -1, hs = -1;
+    if (j < nl) {
+      hs = gw + ngw * j;
+      hv = sv[hs * kC];
+      hi = si[hs * kC];
+    }
+    // bitonic sort of the 32 heads, best first
+#pragma unroll
+    for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+      for (int d = size >> 1; d; d >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, hv, d);
+        const int oi = __shfl_xor_sync(0xffffffffu, hi, d);
+        const int os = __shfl_xor_sync(0xffffffffu, hs, d);
+        const bool best_first = ((lane & size) == 0) || size == 32;
+        const bool lower = (lane & d) == 0;
+        const bool other_ahead = ranks_ahead(ov, oi, hv, hi);
+        const bool mine_ahead = ranks_ahead(hv, hi, ov, oi);
+        if ((lower == best_first) ? other_ahead : mine_ahead) {
+          hv = ov; hi = oi; hs = os;
+        }
+      }
+    }
+    for (int p = 0; p < 32; ++p) {
+      const float bv = __shfl_sync(0xffffffffu, hv, p);
+      const int bi = __shfl_sync(0xffffffffu, hi, p);
+      const int bs = __shfl_sync(0xffffffffu, hs, p);
+      if (bs < 0 ||
+          !ranks_ahead(bv, bi, __shfl_sync(0xffffffffu, tv, kC - 1),
+                       __shfl_sync(0xffffffffu, ti, kC - 1)))
+        break;
+      float v = lane < kC ? tv : sv[bs * kC + k];
+      int i = lane < kC ? ti : si[bs * kC + k];
+      bitonic_merge32(v, i, lane);
+      tv = v;
+      ti = i;
+    }
+  }
+}
+
+// The drafting steps after the LM head, for bf16 storage with the gate
+// precomputed by the conv launch: one CTA per row m = (b, t).
+//   1. one round of asynchronous copies: the gate row and the strip lists
+//      of rows m and m - 1 (the predecessors of row m are row m - 1's
+//      candidates; the anchor at t = 0);
+//   2. warps 0-3 merge row m (and write topv/topi/lse), warps 4-7 row m - 1;
+//   3. the 32 embedding rows by asynchronous copies; the 16 x 16 scores;
+//   4. the sequence's last row to finish (atomic ticket, zeroed by the conv
+//      launch) walks it: all K x 16 rows' step quantities are computed in
+//      parallel first, so the K serial steps are lookups.
+template <typename T>
+__global__ void __launch_bounds__(kThreads)
+    draft_tail_kernel(TopkPartials P, int nstrip,
+                      const int* __restrict__ anchor,
+                      const float* __restrict__ gate,
+                      const T* __restrict__ e_in, const T* __restrict__ e_out,
+                      int K, int V, int r, float Tt, float invT, uint64_t seed,
+                      uint64_t cycle, float* __restrict__ topv,
+                      int* __restrict__ topi, float* __restrict__ lse,
+                      float* __restrict__ scores, int* __restrict__ slot,
+                      int* __restrict__ draft, float* __restrict__ q,
+                      unsigned* __restrict__ tickets, int* err) {
+  extern __shared__ float4 smem4[];
+  float* g_row = reinterpret_cast<float*>(smem4);    // [256]
+  float* work = g_row + DFLASH_MAX_RANK;              // score tiles / walk
+  T* st = reinterpret_cast<T*>(work + 2 * kC * (DFLASH_MAX_RANK + 4));
+  float* lists = reinterpret_cast<float*>(st + 2 * kC * r);
+  // words of one row's lists, rounded to 16 bytes for the copies
+  const int lw = (nstrip * (2 * kC + 2) + 3) & ~3;
+  __shared__ int s_tok[2][kC];
+  __shared__ float s_topv[kC];
+  __shared__ int s_ids[DFLASH_MAX_K * kC];
+  __shared__ float s_tot[DFLASH_MAX_K * kC], s_mx[DFLASH_MAX_K * kC];
+  __shared__ int s_arg[DFLASH_MAX_K * kC];
+  __shared__ float s_mv[2][kWarps / 2][kC], s_mm[2][kWarps / 2],
+      s_ms[2][kWarps / 2];
+  __shared__ int s_mi[2][kWarps / 2][kC];
+  __shared__ int s_flag;
+  const int m = blockIdx.x, b = m / K, t = m % K;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const bool vec = (r * (int)sizeof(T)) % 16 == 0;
+
+  // ---- 1. gate row and strip lists ---------------------------------------
+  const float* grow = gate + (size_t)m * r;
+  if (r % 4 == 0) {
+    for (int c = tid; c < r / 4; c += kThreads)
+      cp_async16(g_row + 4 * c, grow + 4 * c, 16);
+  } else {
+    for (int k = tid; k < r; k += kThreads) g_row[k] = grow[k];
+  }
+  for (int j = 0; j < (t > 0 ? 2 : 1); ++j) {
+    const size_t base = (size_t)(m - j) * nstrip;
+    float* L = lists + j * lw;
+    for (int c = tid; c < nstrip * kC / 4; c += kThreads) {
+      cp_async16(L + 4 * c, P.v + base * kC + 4 * c, 16);
+      cp_async16(L + nstrip * kC + 4 * c, P.i + base * kC + 4 * c, 16);
+    }
+    for (int c = tid; c < nstrip; c += kThreads) {
+      cp_async4(L + 2 * nstrip * kC + c, P.m + base + c);
+      cp_async4(L + 2 * nstrip * kC + nstrip + c, P.s + base + c);
+    }
+  }
+  cp_async_wait_all();
+  __syncthreads();
+
+  // ---- 2. merges: warps 0-3 row m, warps 4-7 row m - 1 ------------------
+  {
+    constexpr int kG = kWarps / 2;  // warps per row
+    const int g = warp / kG, gw = warp % kG;
+    float tv = -INFINITY, rm = -INFINITY, rs = 0.f;
+    int ti = -1;
+    if (g == 0 || t > 0) {
+      const float* L = lists + g * lw;
+      fold_lists_smem(L, reinterpret_cast<const int*>(L + nstrip * kC),
+                      L + 2 * nstrip * kC, L + 2 * nstrip * kC + nstrip,
+                      nstrip, gw, kG, tv, ti, rm, rs);
+    }
+    if (lane < kC) { s_mv[g][gw][lane] = tv; s_mi[g][gw][lane] = ti; }
+    if (lane == 0) { s_mm[g][gw] = rm; s_ms[g][gw] = rs; }
+    __syncthreads();
+    if (gw == 0) {
+      if (g == 0 || t > 0) {
+        const int k = lane < kC ? lane : 31 - lane;
+        for (int w2 = 1; w2 < kG; ++w2) {
+          lse_combine(rm, rs, s_mm[g][w2], s_ms[g][w2], 1.f);
+          float v = lane < kC ? tv : s_mv[g][w2][k];
+          int i = lane < kC ? ti : s_mi[g][w2][k];
+          bitonic_merge32(v, i, lane);
+          tv = v;
+          ti = i;
+        }
+      } else {  // t = 0: every predecessor is the anchor
+        ti = anchor[b];
+        if (ti < -1 || ti >= V) {
+          if (lane == 0) raise_error(err, kErrBadIndex);
+          ti = -1;
+        }
+      }
+      if (g == 0) {
+        if (lane < kC) {
+          topv[(size_t)m * kC + lane] = tv;
+          topi[(size_t)m * kC + lane] = ti;
+          s_topv[lane] = tv;
+          s_tok[1][lane] = ti;
+        }
+        if (lane == 0) lse[m] = rm + logf(rs);
+      } else if (lane < kC) {
+        s_tok[0][lane] = ti;
+      }
+    }
+  }
+  __syncthreads();
+
+  // ---- 3. embedding rows and scores --------------------------------------
+  if (vec) gather_rows(st, s_tok, e_in, e_out, r);
+  cp_async_wait_all();
+  __syncthreads();
+  score_row<kThreads>(st, vec, s_tok[0], s_tok[1], g_row, e_in, e_out, r,
+                      work, s_topv, scores + (size_t)m * kC * kC);
+
+  // ---- 4. the last row of sequence b walks it -----------------------------
+  __syncthreads();
+  if (tid == 0) {
+    __threadfence();
+    s_flag = (atomicAdd(&tickets[b], 1u) == (unsigned)(K - 1));
+  }
+  __syncthreads();
+  if (!s_flag) return;
+  __threadfence();
+  // The quantities of every step the walk could take: for each position t
+  // and predecessor slot p (row t*16 + p of the sequence's scores), half a
+  // warp computes what the walk's step computes for that row — the argmax
+  // at T = 0, else the row max, the weights' prefix sums and total — in the
+  // same operations and order, so the serial walk below only looks them up
+  // (and recomputes the chosen row's 16 weights for q).
+  float* sc_s = work;                       // [K*16][16] scores
+  float* c_s = work + K * kC * kC;          // [K*16][16] prefix sums
+  {
+    const float4* src =
+        reinterpret_cast<const float4*>(scores + (size_t)b * K * kC * kC);
+    for (int i = tid; i < K * kC * kC / 4; i += kThreads)
+      reinterpret_cast<float4*>(sc_s)[i] = __ldcg(src + i);
+    for (int i = tid; i < K * kC; i += kThreads)
+      s_ids[i] = __ldcg(topi + (size_t)b * K * kC + i);
+  }
+  __syncthreads();
+  const int half = lane >> 4, hl = lane & 15;
+  for (int row = warp * 2 + half; row < K * kC; row += kWarps * 2) {
+    const float v = sc_s[row * kC + hl];
+    if (Tt == 0.f) {
+      float bv = v;
+      int bi = hl;
+#pragma unroll
+      for (int o = 8; o; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o, 16);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, o, 16);
+        if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
+      }
+      if (hl == 0) s_arg[row] = bi;
+    } else {
+      float mx = v;
+#pragma unroll
+      for (int o = 8; o; o >>= 1)
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o, 16));
+      const float wv = (v != -INFINITY) ? __expf((v - mx) * invT) : 0.f;
+      float cum = wv;
+#pragma unroll
+      for (int o = 1; o < 16; o <<= 1) {
+        const float n = __shfl_up_sync(0xffffffffu, cum, o, 16);
+        if (hl >= o) cum += n;
+      }
+      c_s[row * kC + hl] = cum;
+      if (hl == 15) { s_tot[row] = cum; s_mx[row] = mx; }
+    }
+  }
+  __syncthreads();
+  if (warp != 0) return;
+  // the walk: lane t draws position t's uniform up front
+  const float u_lane = (Tt > 0.f && lane < K)
+                           ? philox_uniform(seed, b, lane, kPurposeWalk, cycle)
+                           : 0.f;
+  int prev = 0;  // row 0 of position 0 is the anchor's row
+  for (int tt = 0; tt < K; ++tt) {
+    const int row = tt * kC + prev;
+    const int rowbase = (b * K + tt) * kC;
+    int j;
+    float qj;
+    if (Tt == 0.f) {
+      j = s_arg[row];
+      qj = (lane == j) ? 1.f : 0.f;
+    } else {
+      const float v = lane < kC ? sc_s[row * kC + lane] : -INFINITY;
+      const float mx = s_mx[row];
+      const float wv = (v != -INFINITY) ? __expf((v - mx) * invT) : 0.f;
+      const float cum = lane < kC ? c_s[row * kC + lane] : 0.f;
+      const float tot = s_tot[row];
+      const float u = __shfl_sync(0xffffffffu, u_lane, tt);
+      const float thr = u * tot;
+      const unsigned above = __ballot_sync(0xffffffffu, lane < kC && cum > thr);
+      const unsigned live = __ballot_sync(0xffffffffu, wv > 0.f);
+      if (above) j = __ffs(above) - 1;
+      else j = live ? 31 - __clz(live) : 0;  // u*tot rounded up to tot
+      if (!live && lane == 0) raise_error(err, kErrBadIndex);
+      qj = tot > 0.f ? wv / tot : 0.f;
+    }
+    if (lane < kC) q[rowbase + lane] = qj;
+    if (lane == 0) {
+      const int tok = s_ids[tt * kC + j];
+      slot[b * K + tt] = j;
+      draft[b * K + tt] = tok;
+      if (tok < 0) raise_error(err, kErrBadIndex);
+    }
+    prev = j;
+  }
 }
 
 }  // namespace
@@ -516,6 +851,36 @@ cudaError_t launch_pair_score_gated(const float* topv, const int* topi,
       topv, topi, anchor, gate, e_in, e_out, K, V, r, scores, err);
   return cudaGetLastError();
 }
+
+template <typename T>
+cudaError_t launch_draft_tail(TopkPartials P, int nstrip, const int* anchor,
+                              const float* gate, const T* e_in,
+                              const T* e_out, int B, int K, int V, int r,
+                              float T_, uint64_t seed, uint64_t cycle,
+                              float* topv, int* topi, float* lse,
+                              float* scores, int* slot, int* draft, float* q,
+                              unsigned* tickets, int* err, cudaStream_t s) {
+  const size_t smem =
+      (size_t)(DFLASH_MAX_RANK + 2 * kC * (DFLASH_MAX_RANK + 4)) *
+          sizeof(float) +
+      (size_t)2 * kC * r * sizeof(T) +
+      (size_t)2 * ((nstrip * (2 * kC + 2) + 3) & ~3) * sizeof(float);
+  cudaError_t e = cudaFuncSetAttribute(
+      draft_tail_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      (int)smem);
+  if (e != cudaSuccess) return e;
+  const float invT = T_ > 0.f ? 1.f / T_ : 0.f;
+  draft_tail_kernel<T><<<B * K, kThreads, smem, s>>>(
+      P, nstrip, anchor, gate, e_in, e_out, K, V, r, T_, invT, seed, cycle,
+      topv, topi, lse, scores, slot, draft, q, tickets, err);
+  return cudaGetLastError();
+}
+
+template cudaError_t launch_draft_tail<__nv_bfloat16>(
+    TopkPartials, int, const int*, const float*, const __nv_bfloat16*,
+    const __nv_bfloat16*, int, int, int, int, float, uint64_t, uint64_t,
+    float*, int*, float*, float*, int*, int*, float*, unsigned*, int*,
+    cudaStream_t);
 
 template cudaError_t launch_pair_score_gated<float>(
     const float*, const int*, const int*, const float*, const float*,

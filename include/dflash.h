@@ -200,20 +200,22 @@ dflash_status dflash_path_walk(const float* scores, const int32_t* topi,
  * "A Lightweight Path Selector" of "DFlash 2: Keep Drafting Parallel").
  * For bf16 storage with a conv, the context gate g_t = sigmoid(W_g h_t)
  * reads the same h tiles as the conv, so it is computed by the conv launch
- * on the tensor cores and kept in the workspace; the pair scores then only
- * gather embedding rows.  Otherwise the three steps run as the separate
- * calls do.
+ * on the tensor cores and kept in the workspace; after the LM head, one
+ * launch merges its partials, scores the pairs of each position (only
+ * gathering embedding rows) and walks each sequence.  Otherwise the three
+ * steps run as the separate calls do.
  *   inputs   h, conv_w (may be NULL: no conv), w_lm, w_gate, e_in, e_out,
  *            anchor, sizes, dt, T, seed, cycle: as in the three calls
  *   outputs  topv, topi, lse (dflash_lmhead_topk), scores
  *            (dflash_pair_score), slot, draft, q (dflash_path_walk)
  *   ws       >= dflash_workspace_bytes(2, B, K, H, V) bytes, 256-byte
- *            aligned, caller-owned; holds y, the LM-head partials and the
- *            gate.
+ *            aligned, caller-owned; holds y, the LM-head partials, the
+ *            gate and one walk ticket per sequence.
  * Requirements: the union of the three calls' (h, w_lm, w_gate, e_in,
  * e_out, scores 16-byte aligned; H % 8 == 0; 1 <= r <= 256; T >= 0).
  * Results equal the three calls' up to the order of fp32 accumulation in
- * the gate.
+ * the gate and in the logsumexp fold: the same candidates, lse and scores
+ * within fp32 rounding.
  */
 dflash_status dflash_draft(const void* h, const void* conv_w, const void* w_lm,
                            const void* w_gate, const void* e_in,
@@ -269,6 +271,9 @@ dflash_status dflash_philox4x32(const uint32_t* ctr, uint64_t seed,
  * `stage`:
  *   0 conv, 1 LM head with top-16 / logsumexp epilogue, 2 top-16 merge,
  *   3 pair score, 4 walk, 5 verify (row pass, accept tests and draw).
+ * In dflash_draft with bf16 storage and a conv, stage 0 is the conv with
+ * the context gate and stage 3 the one launch that merges, scores and
+ * walks (stages 2 and 4 are not recorded).
  * Pass NULL for both to stop.  Process-wide host state; set it from the
  * thread that makes the calls, not while other threads call the library.
  * Returns DFLASH_ERR_INVALID_ARG for an unknown stage or a lone NULL. */

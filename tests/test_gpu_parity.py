@@ -383,8 +383,9 @@ def test_fused_draft_fp32(lib, name, T):
 
 
 def test_fused_draft_matches_separate_calls(lib):
-    """Same LM head kernels: identical candidates; scores within the fp32
-    tolerance (the gate's accumulation order differs)."""
+    """Same LM head kernels: identical candidates; lse and scores within
+    fp32 rounding (the fused path folds the lse pairs and accumulates the
+    gate in other orders)."""
     w = synth.Workload("small", B=6, K=8, V=3001, H=256, r=256, dtype="bf16",
                        T=1.0, seed=5, w_lm_sd=0.1, conv_sd=0.05, sel_sd=0.1,
                        target=("affine", 0.9, 1.0))
@@ -399,7 +400,7 @@ def test_fused_draft_matches_separate_calls(lib):
     torch.cuda.synchronize()
     lib.dflash_check()
     assert torch.equal(a.topi, b.topi) and torch.equal(a.topv, b.topv)
-    assert torch.equal(a.lse, b.lse)
+    np.testing.assert_allclose(np_(b.lse), np_(a.lse), rtol=2e-6, atol=0)
     np.testing.assert_allclose(np_(b.scores), np_(a.scores), rtol=1e-5,
                                atol=1e-5)
 
