@@ -24,6 +24,44 @@ __device__ __forceinline__ void raise_error(int* err, int bit) {
   atomicOr(err, bit);
 }
 
+// Programmatic dependent launch: a kernel launched with the programmatic
+// stream serialization attribute may start while the previous kernel on the
+// stream is still running; pdl_wait() blocks the calling thread until that
+// kernel has completed and its memory is visible, pdl_trigger() lets the
+// next such kernel start.  Both are no-ops in a normal launch.
+__device__ __forceinline__ void pdl_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Launch configuration with programmatic stream serialization (plus an
+// optional cluster size).
+struct PdlLaunch {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[2];
+  PdlLaunch(dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+            int cluster_x = 0) {
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    int n = 1;
+    if (cluster_x > 0) {
+      attr[1].id = cudaLaunchAttributeClusterDimension;
+      attr[1].val.clusterDim.x = cluster_x;
+      attr[1].val.clusterDim.y = 1;
+      attr[1].val.clusterDim.z = 1;
+      n = 2;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = n;
+  }
+};
+
 __device__ __forceinline__ float to_f32(float x) { return x; }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 x) {
   return __bfloat162float(x);

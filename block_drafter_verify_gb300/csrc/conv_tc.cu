@@ -80,8 +80,6 @@ __global__ void __launch_bounds__(THREADS)
   const int mtile = blockIdx.y;
   const int kblocks = (H + BK - 1) / BK;
 
-  if (tickets && blockIdx.x == 0 && blockIdx.y == 0)
-    for (int i = threadIdx.x; i < ntickets; i += THREADS) tickets[i] = 0u;
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       tc::mbar_init(&bars->full[s], 1);
@@ -101,6 +99,11 @@ __global__ void __launch_bounds__(THREADS)
   tc::fence_after_sync();
   const uint32_t tmem = bars->tmem_base;
   volatile int* abort = &bars->abort;
+  // everything above is on-chip set-up; h may come from the previous launch
+  pdl_wait();
+  if (threadIdx.x == 0) pdl_trigger();
+  if (tickets && blockIdx.x == 0 && blockIdx.y == 0)
+    for (int i = threadIdx.x; i < ntickets; i += THREADS) tickets[i] = 0u;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -237,10 +240,10 @@ cudaError_t launch_conv_tc(const CUtensorMap& map_h, const CUtensorMap& map_wc,
   if (e != cudaSuccess) return e;
   const int gate_tiles = map_wg ? (r + 2 * BC - 1) / (2 * BC) : 0;
   const dim3 grid((H + BC - 1) / BC + gate_tiles, (M + BM - 1) / BM);
-  conv_tc_kernel<<<grid, THREADS, SMEM_BYTES, s>>>(
-      map_h, map_wc, map_wg ? *map_wg : map_wc, h, M, K, H, r, y, gate,
-      tickets, B, err);
-  return cudaGetLastError();
+  PdlLaunch L(grid, dim3(THREADS), SMEM_BYTES, s);
+  return cudaLaunchKernelEx(&L.cfg, conv_tc_kernel, map_h, map_wc,
+                            map_wg ? *map_wg : map_wc, h, M, K, H, r, y, gate,
+                            tickets, B, err);
 }
 
 }  // namespace dflash

@@ -207,30 +207,42 @@ __global__ void __launch_bounds__(THREADS, 1)
       int stage = 0;
       uint32_t phase = 0, issued = 0, last_par = 0;
       bool ok = true;
+      // The W tiles of the first stages go out before waiting for the
+      // launch that writes y (W_lm is an input no launch writes); each
+      // stage's full barrier already expects both of its tiles.
+      const int pre = min(STAGES, my_tiles * kblocks);
+      auto load_w = [&](int j, int s) {
+        const int vt = strip + (j / kblocks) * strips, kb = j % kblocks;
+        uint8_t* b_dst = sb + s * C::B_BYTES;
+        if constexpr (kPair) {
+          if (leader)
+            tc::mbar_arrive_expect_tx(&bars->full[s], 2 * C::STAGE_BYTES);
+          tc::tma_load_2d_pair(b_dst, &map_w, full0 + s * 8, kb * BK,
+                               vt * BN + rank * C::B_ROWS);
+        } else {
+          tc::mbar_arrive_expect_tx(&bars->full[s], C::STAGE_BYTES);
+          tc::tma_load_2d(b_dst, &map_w, &bars->full[s], kb * BK, vt * BN);
+        }
+      };
+      for (int j = 0; j < pre; ++j) load_w(j, j);
+      pdl_wait();
+      pdl_trigger();
+      int j = 0;
       for (int it = 0; it < my_tiles && ok; ++it) {
-        const int vt = strip + it * strips;
-        for (int kb = 0; kb < kblocks; ++kb) {
+        for (int kb = 0; kb < kblocks; ++kb, ++j) {
           if (!tc::mbar_wait_bounded(&bars->empty[stage], phase ^ 1, abort,
                                      WAIT_NS)) {
             ok = false;
             break;
           }
           uint8_t* a_dst = sa + stage * A_BYTES;
-          uint8_t* b_dst = sb + stage * C::B_BYTES;
+          if (j >= pre) load_w(j, stage);
           if constexpr (kPair) {
-            if (leader)
-              tc::mbar_arrive_expect_tx(&bars->full[stage],
-                                        2 * C::STAGE_BYTES);
-            const uint32_t fb = full0 + stage * 8;
-            tc::tma_load_2d_pair(a_dst, &map_y, fb, kb * BK, mtile * BM);
-            tc::tma_load_2d_pair(b_dst, &map_w, fb, kb * BK,
-                                 vt * BN + rank * C::B_ROWS);
+            tc::tma_load_2d_pair(a_dst, &map_y, full0 + stage * 8, kb * BK,
+                                 mtile * BM);
           } else {
-            tc::mbar_arrive_expect_tx(&bars->full[stage], C::STAGE_BYTES);
             tc::tma_load_2d(a_dst, &map_y, &bars->full[stage], kb * BK,
                             mtile * BM);
-            tc::tma_load_2d(b_dst, &map_w, &bars->full[stage], kb * BK,
-                            vt * BN);
           }
           issued |= 1u << stage;
           last_par = (last_par & ~(1u << stage)) | (phase << stage);
@@ -448,28 +460,17 @@ cudaError_t launch_lmhead_tc(const CUtensorMap& map_y, const CUtensorMap& map_w,
         lmhead_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
         (int)smem_bytes<false>());
     if (e != cudaSuccess) return e;
-    lmhead_tc_kernel<false><<<grid, THREADS, smem_bytes<false>(), s>>>(
-        map_y, map_w, M, H, V, rg, st, P, err);
-    return cudaGetLastError();
+    PdlLaunch L(dim3(grid), dim3(THREADS), smem_bytes<false>(), s);
+    return cudaLaunchKernelEx(&L.cfg, lmhead_tc_kernel<false>, map_y, map_w,
+                              M, H, V, rg, st, P, err);
   }
   cudaError_t e = cudaFuncSetAttribute(
       lmhead_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
       (int)smem_bytes<true>());
   if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(THREADS);
-  cfg.dynamicSmemBytes = smem_bytes<true>();
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, lmhead_tc_kernel<true>, map_y, map_w, M, H,
-                            V, rg, st, P, err);
+  PdlLaunch L(dim3(grid), dim3(THREADS), smem_bytes<true>(), s, 2);
+  return cudaLaunchKernelEx(&L.cfg, lmhead_tc_kernel<true>, map_y, map_w, M,
+                            H, V, rg, st, P, err);
 }
 
 }  // namespace dflash

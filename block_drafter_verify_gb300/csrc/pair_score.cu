@@ -631,6 +631,8 @@ __global__ void __launch_bounds__(kThreads)
   const int m = blockIdx.x, b = m / K, t = m % K;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const bool vec = (r * (int)sizeof(T)) % 16 == 0;
+  pdl_wait();  // the LM head's partials (and, before it, the gate)
+  if (tid == 0) pdl_trigger();
 
   // ---- 1. gate row and strip lists ---------------------------------------
   const float* grow = gate + (size_t)m * r;
@@ -870,10 +872,11 @@ cudaError_t launch_draft_tail(TopkPartials P, int nstrip, const int* anchor,
       (int)smem);
   if (e != cudaSuccess) return e;
   const float invT = T_ > 0.f ? 1.f / T_ : 0.f;
-  draft_tail_kernel<T><<<B * K, kThreads, smem, s>>>(
-      P, nstrip, anchor, gate, e_in, e_out, K, V, r, T_, invT, seed, cycle,
-      topv, topi, lse, scores, slot, draft, q, tickets, err);
-  return cudaGetLastError();
+  PdlLaunch L(dim3(B * K), dim3(kThreads), smem, s);
+  return cudaLaunchKernelEx(&L.cfg, draft_tail_kernel<T>, P, nstrip, anchor,
+                            gate, e_in, e_out, K, V, r, T_, invT, seed, cycle,
+                            topv, topi, lse, scores, slot, draft, q, tickets,
+                            err);
 }
 
 template cudaError_t launch_draft_tail<__nv_bfloat16>(
