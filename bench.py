@@ -52,6 +52,9 @@ def parse(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="bounded CPU work for the oracle baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sweep", default=None,
+                    help="time the sweep grid instead (one JSON line per "
+                         "point): 'all' or a comma list of point names")
     return ap.parse_args(argv)
 
 
@@ -307,6 +310,120 @@ def run_reference(args):
 
 
 # --------------------------------------------------------------------------
+# sweep: per-stage rooflines over the K x B x T grid
+# --------------------------------------------------------------------------
+def run_sweep(args):
+    """Each sweep point: cycles/s over CUDA-graph replays and per-stage
+    event times, one JSON line per point.  Inputs are drawn on the device
+    with seeded torch generators from the same distributions as synth (the
+    grid's 4.5 GB of target logits would take minutes to draw on the host);
+    the weights are shared by all points."""
+    import torch
+    import block_drafter_verify_gb300 as dv_mod
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    torch.backends.cuda.matmul.allow_tf32 = False
+    pts = synth.sweep_points()
+    if args.sweep != "all":
+        want = set(args.sweep.split(","))
+        pts = [p for p in pts if p.name in want]
+    g = torch.Generator(device=dev).manual_seed(pts[0].seed)
+    w0 = pts[0]
+
+    def normal(shape, sd, dt=torch.bfloat16):
+        return (torch.randn(shape, generator=g, device=dev) * sd).to(dt)
+    weights = {"w_conv": normal((2 * w0.H, w0.H), w0.conv_sd),
+               "w_lm": normal((w0.V, w0.H), w0.w_lm_sd),
+               "w_gate": normal((w0.r, w0.H), w0.sel_sd),
+               "e_in": normal((w0.V, w0.r), w0.sel_sd),
+               "e_out": normal((w0.V, w0.r), w0.sel_sd)}
+    pk = peaks()
+    for w in pts:
+        h_all = normal((w.B, w.K + 1, w.H), 1.0)
+        anchor = torch.randint(0, w.V, (w.B,), generator=g, device=dev,
+                               dtype=torch.int32)
+        # target = 0.9 * drafter logits + N(0, 1), drafter logits in fp32
+        hf = h_all.float()
+        wc = weights["w_conv"].float()
+        prev = torch.zeros_like(hf)
+        prev[:, 1:] = hf[:, :-1]
+        y = ((hf @ wc[:w.H].T) * hf + (hf @ wc[w.H:].T) * prev).to(
+            torch.bfloat16).float().reshape(-1, w.H)
+        L = torch.empty(y.shape[0], w.V, device=dev)
+        for v0 in range(0, w.V, 16384):
+            L[:, v0:v0 + 16384] = y @ weights["w_lm"][v0:v0 + 16384].float().T
+        L.mul_(w.target[1]).add_(torch.randn(L.shape, generator=g,
+                                             device=dev) * w.target[2])
+        L = L.reshape(w.B, w.K + 1, w.V)
+        del hf, prev, y
+        h = h_all[:, :w.K].contiguous()
+        dv = dv_mod.DraftVerify(w.B, w.K, w.H, w.V, w.r, weights, device=dev)
+        for i in range(3):
+            dv.cycle(h, anchor, L, w.T, w.seed, i)
+        torch.cuda.synchronize(dev)
+        dv_mod.dflash_check()
+        G, R = 20, 5
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr):
+            for i in range(G):
+                dv.cycle(h, anchor, L, w.T, w.seed, 3 + i)
+        gr.replay()
+        torch.cuda.synchronize(dev)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(R):
+            gr.replay()
+        e1.record()
+        torch.cuda.synchronize(dev)
+        ms = e0.elapsed_time(e1) / (G * R)
+        stages = dv_mod.STAGES
+        ev = [(torch.cuda.Event(enable_timing=True),
+               torch.cuda.Event(enable_timing=True)) for _ in stages]
+        for b_, e_ in ev:
+            b_.record()
+            e_.record()
+        tim = {n: [] for n in stages}
+        n_sum = 0
+        for i in range(5):
+            for si in range(len(stages)):
+                dv_mod.dflash_profile_stage(si, ev[si][0], ev[si][1])
+            dv.cycle(h, anchor, L, w.T, w.seed, 100 + i)
+            torch.cuda.synchronize(dev)
+            n_sum += int(dv.n.sum().item())
+            for si, n in enumerate(stages):
+                tim[n].append(ev[si][0].elapsed_time(ev[si][1]) * 1e3)
+        for si in range(len(stages)):
+            dv_mod.dflash_profile_stage(si, None, None)
+        dv_mod.dflash_check()
+        names = {"conv": "conv+gate", "lmhead": "lmhead",
+                 "pair_score": "merge+pair_score+walk", "verify": "verify"}
+        stage_us = {names[n]: float(np.mean(tim[n])) for n in names}
+        by, fl = lmhead_algorithmic(w)
+        t_lm = stage_us["lmhead"] * 1e-6
+        ridge = pk["bf16_tflops"] * 1e12 / (pk["hbm_gbs"] * 1e9)
+        lm = ({"bound": "hbm", "frac": by / t_lm / 1e9 / pk["hbm_gbs"],
+               "tensor_frac": fl / t_lm / 1e12 / pk["bf16_tflops"]}
+              if fl / by < ridge else
+              {"bound": "tensor", "frac": fl / t_lm / 1e12 / pk["bf16_tflops"],
+               "hbm_frac": by / t_lm / 1e9 / pk["hbm_gbs"]})
+        sb = stage_bytes(w, True)
+        line = {"sweep_point": w.name, "B": w.B, "K": w.K, "T": w.T,
+                "V": w.V, "H": w.H, "cycles_per_s": 1e3 / ms,
+                "ms_per_cycle": ms, "mean_accepted": n_sum / (5 * w.B),
+                "stage_us": stage_us, "lmhead": lm,
+                "stage_hbm_frac": {k: sb[k] / (stage_us[k] * 1e-6) / 1e9 /
+                                   pk["hbm_gbs"] for k in sb
+                                   if k in stage_us},
+                "data": "synthetic (device-drawn, same distributions)",
+                "peak_source": pk["source"]}
+        print(json.dumps(line), flush=True)
+        del dv, L, h, h_all, gr
+        torch.cuda.empty_cache()
+    return 0
+
+
+# --------------------------------------------------------------------------
 # our arm
 # --------------------------------------------------------------------------
 def run_ours(args):
@@ -366,13 +483,16 @@ def run_ours(args):
         graph_error = str(exc).splitlines()[0][:200]
     t_start = torch.cuda.Event(enable_timing=True)
     t_stop = torch.cuda.Event(enable_timing=True)
+    # an event after every graph replay: per-cycle time percentiles
+    marks = [torch.cuda.Event(enable_timing=True) for _ in graphs]
     barrier()
     torch.cuda.synchronize(dev)
     clk.mark_start()
     t_start.record(stream)
     if use_graph:
-        for g in graphs:
+        for g, mk_ in zip(graphs, marks):
             g.replay()
+            mk_.record(stream)
     else:
         for i in range(K):
             dv.cycle(h, anchor, L, w.T, seed, args.warmup + i)
@@ -385,7 +505,18 @@ def run_ours(args):
     secs = t_start.elapsed_time(t_stop) / 1e3
     secs_max = max_over_ranks(secs, dev)
     value, _ = aggregate(K, [secs_max], world)
-    n_hist = [float(dv.n.cpu().numpy().mean())]
+    cycle_ms = None
+    if use_graph and len(graphs) >= 2:
+        per = []
+        prev = t_start
+        for g, mk_ in zip(graphs, marks):
+            n_c = G if g is g_full else K % G
+            per.append(prev.elapsed_time(mk_) / n_c)
+            prev = mk_
+        q = np.percentile(per, [10, 50, 90])
+        cycle_ms = {"p10": float(q[0]), "p50": float(q[1]),
+                    "p90": float(q[2]), "graphs": len(per),
+                    "cycles_per_graph": G}
 
     # per-kernel times: CUDA events the library records around each launch,
     # on the launching stream, over eager cycles (not part of the timed K)
@@ -396,15 +527,18 @@ def run_ours(args):
         e.record(stream)
         return e
     ev = [[(mk(), mk()) for _ in stages] for _ in range(KS)]
+    n_sum = torch.zeros((), dtype=torch.int64, device=dev)
     torch.cuda.synchronize(dev)
     for i in range(KS):
         for si in range(len(stages)):
             dv_mod.dflash_profile_stage(si, ev[i][si][0], ev[i][si][1])
         dv.cycle(h, anchor, L, w.T, seed, args.warmup + i)
+        n_sum += dv.n.sum()
     torch.cuda.synchronize(dev)
     for si in range(len(stages)):
         dv_mod.dflash_profile_stage(si, None, None)
     dv_mod.dflash_check()
+    n_mean_cycles = float(n_sum.item()) / (KS * w.B)
     # dflash_draft with bf16 storage and a conv runs three kernels: the conv
     # (with the context gate), the LM head, and one launch that merges the
     # LM head's partials, scores the pairs and walks (recorded as the
@@ -451,6 +585,15 @@ def run_ours(args):
                 "peak_source": pk["source"], "kernel": "lmhead",
                 "hbm_frac": by / t_lm / 1e9 / pk["hbm_gbs"]}
 
+    # achieved bandwidth of the other stages (algorithmic bytes per launch
+    # / mean event time), against the measured HBM peak
+    stage_roof = {}
+    for name, nbytes in stage_bytes(w, fused).items():
+        if name in stage_us and stage_us[name] > 0:
+            gbs = nbytes / (stage_us[name] * 1e-6) / 1e9
+            stage_roof[name] = {"bytes": nbytes, "GB/s": gbs,
+                                "frac": gbs / pk["hbm_gbs"]}
+
     # end to end through the public API with host buffers
     e2e_steps = args.e2e_steps or max(3, min(K, 20))
     h_host = x["h"][:, :w.K].contiguous().pin_memory()
@@ -490,7 +633,7 @@ def run_ours(args):
         dist.destroy_process_group()
     if rank != 0:
         return 0
-    n_mean = float(np.mean(n_hist))
+    n_mean = n_mean_cycles
     launches_per_step = (4 if w.dtype == "bf16" and w.conv_sd is not None
                          else (3 if w.conv_sd is not None else 2) + 3)
     line = {
@@ -507,7 +650,10 @@ def run_ours(args):
                    "recipe": synth.describe(w)},
         "verified_tokens_per_s": value * w.B * (n_mean + 1),
         "mean_accepted": n_mean,
+        "mean_emitted": n_mean + 1,
+        "cycle_ms": cycle_ms,
         "stage_us": stage_us,
+        "stage_roofline": stage_roof,
         "clocks": clk.summary(),
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
@@ -517,6 +663,40 @@ def run_ours(args):
     }
     print(json.dumps(line))
     return 0
+
+
+def stage_bytes(w, fused):
+    """Algorithmic bytes per launch of the stages other than the LM head
+    (each input read once, each output written once)."""
+    M, H, V, r = w.B * w.K, w.H, w.V, w.r
+    e = 2 if w.dtype == "bf16" else 4
+    out = {}
+    if w.conv_sd is not None:
+        conv = 2 * H * H * e + M * H * e * 2
+        if fused:
+            conv += r * H * e + M * r * 4
+        out["conv+gate" if fused else "conv"] = conv
+    scores = M * 32 * r * e + M * 256 * 4 + M * 16 * 8
+    if fused:
+        # strip partials: one (16 values, 16 ids, max, sum) list per row and
+        # vocab strip, as many strips as the LM head's grid has units
+        strips = lmhead_strips(w)
+        out["merge+pair_score+walk"] = (M * strips * 136 + M * r * 4 +
+                                        scores + M * 16 * 4)
+    else:
+        out["pair_score"] = scores + M * H * e + r * H * e
+    out["verify"] = w.B * (w.K + 1) * V * 4
+    return out
+
+
+def lmhead_strips(w, sms=152):
+    """Vocab strips of the tensor-core LM head's grid (CTA pairs when the
+    rows span two or more 128-row tiles)."""
+    rt = (w.B * w.K + 127) // 128
+    vt = (w.V + 255) // 256
+    units = sms // 2 if rt >= 2 else sms
+    rg = (rt + 1) // 2 if rt >= 2 else rt
+    return max(1, min(units // rg, vt, 160))
 
 
 def lmhead_kernel_rev() -> str:
@@ -536,6 +716,8 @@ def main(argv=None):
     args = parse(argv)
     if args.impl == "reference":
         return run_reference(args)
+    if args.sweep:
+        return run_sweep(args)
     return run_ours(args)
 
 
