@@ -410,3 +410,74 @@ def test_fused_draft_full_size_b32k8(lib):
     x, L = _make(w)
     r = run_fused(lib, w, x, L, seed=w.seed, cycle=0)
     print("b32k8 fused ties", r["ties"], "mean accepted", r["n"].mean())
+
+
+def test_fused_full_size_b32k8cal(lib):
+    """The calibrated workload (mean 4.5 accepted drafts per cycle): the
+    accept tests and residual draws of every position are exercised."""
+    w = synth.get("b32k8cal")
+    x, L = _make(w)
+    r = run_fused(lib, w, x, L, seed=w.seed, cycle=0)
+    print("b32k8cal ties", r["ties"], "mean accepted", r["n"].mean())
+    assert r["n"].mean() > 2.0
+
+
+def _target_on_device(w, x):
+    """Target logits of every sequence from the drafter's logits computed
+    with torch fp32 ops on the device (input synthesis only; the oracle
+    checks below read the same tensor)."""
+    torch.backends.cuda.matmul.allow_tf32 = False
+    h = x["h"].cuda().float()
+    H = w.H
+    wc = x["w_conv"].cuda().float()
+    prev = torch.zeros_like(h)
+    prev[:, 1:] = h[:, :-1]
+    y = ((h @ wc[:H].T) * h + (h @ wc[H:].T) * prev).to(
+        torch.bfloat16).float().reshape(-1, H)
+    wl = x["w_lm"].cuda()
+    U = torch.empty(y.shape[0], w.V, device="cuda")
+    for v0 in range(0, w.V, 16384):
+        U[:, v0:v0 + 16384] = y @ wl[v0:v0 + 16384].float().T
+    d = U.reshape(w.B, w.K + 1, w.V).cpu().numpy()
+    return synth.target_logits(w, d)
+
+
+def test_fused_full_size_b128k16zipf_sampled(lib):
+    """B=128, K=16, H=2560, Zipf target: the whole cycle on the GPU, checked
+    against the oracle on the first four sequences (64 rows: conv, top-16
+    and lse, pair scores, walk and verify)."""
+    w = synth.get("b128k16zipf")
+    x = synth.make_inputs(w)
+    L = _target_on_device(w, x)
+    S, K, H, V = 4, w.K, w.H, w.V
+    seed, cycle = w.seed, 0
+    h = to_dev(x["h"][:, :K])
+    anchor = to_dev(x["anchor"])
+    dv = lib.DraftVerify(w.B, K, H, V, w.r, _weights(x))
+    dv.draft_all(h, anchor, w.T, seed, cycle)
+    dv.verify(to_dev(L), w.T, seed, cycle)
+    torch.cuda.synchronize()
+    lib.dflash_check()
+    rows = slice(0, S * K)
+    h64 = f64(h)[:S]
+    W = f64(x["w_conv"])
+    y = dv.y(fused=True)[:S]
+    check_y(y, oracle.conv2tap(h64, W), oracle.conv2tap(np.abs(h64),
+                                                        np.abs(W)), w.dtype)
+    y64 = f64(y).reshape(-1, H)
+    W_lm = f64(x["w_lm"])
+    ref = oracle.lmhead_topk(y64, W_lm, want_logits=True)
+    A = np.abs(y64) @ np.abs(W_lm).T
+    check_topk(dv.topv[rows], dv.topi[rows], dv.lse[rows], ref, A,
+               ERR_C[w.dtype])
+    topv = np_(dv.topv).reshape(w.B, K, C)[:S]
+    topi = np_(dv.topi).reshape(w.B, K, C)[:S]
+    g = oracle.gate(h64, f64(x["w_gate"]))
+    Sref = oracle.pair_score(topv, topi, np_(anchor)[:S], g, f64(x["e_in"]),
+                             f64(x["e_out"]))
+    check_scores(dv.scores[:S], Sref)
+    S32 = np_(dv.scores)[:S]
+    check_walk(dv.slot[:S], dv.draft[:S], dv.q[:S], S32, topi, w.T, seed,
+               cycle, 1e-5)
+    check_verify(dv.n[:S], dv.out[:S], np_(L)[:S], np_(dv.draft)[:S], topi,
+                 np_(dv.q)[:S], w.T, seed, cycle)
