@@ -24,14 +24,23 @@
 namespace dflash {
 namespace {
 
-constexpr int BM = 128, BC = 32, BK = 64, STAGES = 8;
+constexpr int BM = 128, BK = 64;
 constexpr int A_BYTES = BM * BK * 2;        // 16 KB
-constexpr int B_BYTES = 2 * BC * BK * 2;    // 8 KB (W0 part, then W1 part)
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int THREADS = 192;
-constexpr uint32_t TMEM_COLS = 64;
 constexpr uint64_t WAIT_NS = 2000000000ull;
 
+// BC channels per CTA: the B operand is BC rows of W0 over BC rows of W1
+// (MMA N = 2 BC).  32 for few rows (more CTAs), 128 when there are many
+// rows (M >= 1024), where the N = 64 tiles leave the tensor cores idle.
+template <int BC>
+struct ConvCfg {
+  static constexpr int STAGES = BC == 32 ? 8 : 4;
+  static constexpr int B_BYTES = 2 * BC * BK * 2;  // W0 part, then W1 part
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr uint32_t TMEM_COLS = 2 * BC;
+};
+
+template <int STAGES>
 struct Bars {
   uint64_t full[STAGES];
   uint64_t empty[STAGES];
@@ -40,7 +49,11 @@ struct Bars {
   uint32_t tmem_base;
   int abort;
 };
-constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + sizeof(Bars);
+template <int BC>
+constexpr size_t conv_smem_bytes() {
+  return 1024 + (size_t)ConvCfg<BC>::STAGES * ConvCfg<BC>::STAGE_BYTES +
+         sizeof(Bars<ConvCfg<BC>::STAGES>);
+}
 
 __device__ __forceinline__ bool wait_timeout(uint64_t* bar, uint32_t parity) {
   int never = 0;
@@ -57,6 +70,7 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4& u, float* f) {
   }
 }
 
+template <int BC>
 __global__ void __launch_bounds__(THREADS)
     conv_tc_kernel(const __grid_constant__ CUtensorMap map_h,
                    const __grid_constant__ CUtensorMap map_wc,
@@ -65,12 +79,17 @@ __global__ void __launch_bounds__(THREADS)
                    int r, __nv_bfloat16* __restrict__ y,
                    float* __restrict__ gate, unsigned* __restrict__ tickets,
                    int ntickets, int* err) {
+  constexpr int STAGES = ConvCfg<BC>::STAGES;
+  constexpr int B_BYTES = ConvCfg<BC>::B_BYTES;
+  constexpr int STAGE_BYTES = ConvCfg<BC>::STAGE_BYTES;
+  constexpr uint32_t TMEM_COLS = ConvCfg<BC>::TMEM_COLS;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sa = smem;
   uint8_t* sb = smem + STAGES * A_BYTES;
-  Bars* bars = reinterpret_cast<Bars*>(smem + STAGES * STAGE_BYTES);
+  Bars<STAGES>* bars =
+      reinterpret_cast<Bars<STAGES>*>(smem + STAGES * STAGE_BYTES);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // blocks [0, H/32): conv channel tiles; after them: 64-row gate tiles
   const int conv_tiles = (H + BC - 1) / BC;
@@ -166,50 +185,59 @@ __global__ void __launch_bounds__(THREADS)
     if (__all_sync(0xffffffffu, got)) {
       tc::fence_after_sync();
       const uint32_t tb = tmem + (static_cast<uint32_t>(q * 32) << 16);
-      float w0[32], w1[32];
-      tc::tmem_ld_x32(tb, w0);
-      tc::tmem_ld_x32(tb + BC, w1);
-      if (is_gate) {
-        // columns 0-63 of the accumulator are z for gate rows c0 .. c0+63
-        if (m < M) {
-          float* gr = gate + (size_t)m * r + c0;
-          float g[2 * BC];
+      const bool has_prev = (m % K) != 0;
+#pragma unroll 1
+      for (int cg = 0; cg < BC / 32; ++cg) {
+        float w0[32], w1[32];
+        tc::tmem_ld_x32(tb + cg * 32, w0);
+        tc::tmem_ld_x32(tb + BC + cg * 32, w1);
+        if (m >= M) continue;
+        if (is_gate) {
+          // columns [0, BC) are z of gate rows c0 .., [BC, 2 BC) of c0 + BC ..
 #pragma unroll
-          for (int j = 0; j < 2 * BC; ++j)
-            g[j] = 1.f / (1.f + __expf(-(j < BC ? w0[j] : w1[j - BC])));
-          if (r % 4 == 0 && c0 + 2 * BC <= r) {
+          for (int half = 0; half < 2; ++half) {
+            const int g0 = c0 + half * BC + cg * 32;
+            float* gr = gate + (size_t)m * r + g0;
+            float g[32];
 #pragma unroll
-            for (int j = 0; j < 2 * BC; j += 4)
-              *reinterpret_cast<float4*>(gr + j) =
-                  make_float4(g[j], g[j + 1], g[j + 2], g[j + 3]);
-          } else {
+            for (int j = 0; j < 32; ++j)
+              g[j] = 1.f / (1.f + __expf(-(half == 0 ? w0[j] : w1[j])));
+            if (r % 4 == 0 && g0 + 32 <= r) {
 #pragma unroll
-            for (int j = 0; j < 2 * BC; ++j)
-              if (c0 + j < r) gr[j] = g[j];
+              for (int j = 0; j < 32; j += 4)
+                *reinterpret_cast<float4*>(gr + j) =
+                    make_float4(g[j], g[j + 1], g[j + 2], g[j + 3]);
+            } else {
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                if (g0 + j < r) gr[j] = g[j];
+            }
           }
-        }
-      } else if (m < M) {
-        const bool has_prev = (m % K) != 0;
-        const __nv_bfloat16* hr = h + (size_t)m * H + c0;
-        __nv_bfloat16* yr = y + (size_t)m * H + c0;
+        } else {
+          const int cc = c0 + cg * 32;
+          const __nv_bfloat16* hr = h + (size_t)m * H + cc;
+          __nv_bfloat16* yr = y + (size_t)m * H + cc;
 #pragma unroll
-        for (int g = 0; g < BC / 8; ++g) {
-          if (c0 + g * 8 >= H) break;
-          float hc[8], hp[8];
-          bf16x8_to_f32(*reinterpret_cast<const uint4*>(hr + g * 8), hc);
-          if (has_prev)
-            bf16x8_to_f32(*reinterpret_cast<const uint4*>(hr - H + g * 8), hp);
-          uint4 out;
-          __nv_bfloat162* o = reinterpret_cast<__nv_bfloat162*>(&out);
+          for (int g = 0; g < 4; ++g) {
+            if (cc + g * 8 >= H) break;
+            float hc[8], hp[8];
+            bf16x8_to_f32(*reinterpret_cast<const uint4*>(hr + g * 8), hc);
+            if (has_prev)
+              bf16x8_to_f32(*reinterpret_cast<const uint4*>(hr - H + g * 8),
+                            hp);
+            uint4 out;
+            __nv_bfloat162* o = reinterpret_cast<__nv_bfloat162*>(&out);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int j = g * 8 + 2 * i;
-            const float y0 = w0[j] * hc[2 * i] + (has_prev ? w1[j] * hp[2 * i] : 0.f);
-            const float y1 = w0[j + 1] * hc[2 * i + 1] +
-                             (has_prev ? w1[j + 1] * hp[2 * i + 1] : 0.f);
-            o[i] = __floats2bfloat162_rn(y0, y1);
+            for (int i = 0; i < 4; ++i) {
+              const int j = g * 8 + 2 * i;
+              const float y0 =
+                  w0[j] * hc[2 * i] + (has_prev ? w1[j] * hp[2 * i] : 0.f);
+              const float y1 = w0[j + 1] * hc[2 * i + 1] +
+                               (has_prev ? w1[j + 1] * hp[2 * i + 1] : 0.f);
+              o[i] = __floats2bfloat162_rn(y0, y1);
+            }
+            *reinterpret_cast<uint4*>(yr + g * 8) = out;
           }
-          *reinterpret_cast<uint4*>(yr + g * 8) = out;
         }
       }
     } else {
@@ -228,22 +256,39 @@ __global__ void __launch_bounds__(THREADS)
 
 }  // namespace
 
-cudaError_t launch_conv_tc(const CUtensorMap& map_h, const CUtensorMap& map_wc,
+int conv_tc_bc(int M) { return M >= 1024 ? 128 : 32; }
+
+namespace {
+template <int BC>
+cudaError_t launch_conv_bc(const CUtensorMap& map_h, const CUtensorMap& map_wc,
                            const CUtensorMap* map_wg, const __nv_bfloat16* h,
                            int B, int K, int H, int r, __nv_bfloat16* y,
                            float* gate, unsigned* tickets, int* err,
                            cudaStream_t s) {
   const int M = B * K;
   cudaError_t e = cudaFuncSetAttribute(
-      conv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-      (int)SMEM_BYTES);
+      conv_tc_kernel<BC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      (int)conv_smem_bytes<BC>());
   if (e != cudaSuccess) return e;
   const int gate_tiles = map_wg ? (r + 2 * BC - 1) / (2 * BC) : 0;
   const dim3 grid((H + BC - 1) / BC + gate_tiles, (M + BM - 1) / BM);
-  PdlLaunch L(grid, dim3(THREADS), SMEM_BYTES, s);
-  return cudaLaunchKernelEx(&L.cfg, conv_tc_kernel, map_h, map_wc,
+  PdlLaunch L(grid, dim3(THREADS), conv_smem_bytes<BC>(), s);
+  return cudaLaunchKernelEx(&L.cfg, conv_tc_kernel<BC>, map_h, map_wc,
                             map_wg ? *map_wg : map_wc, h, M, K, H, r, y, gate,
                             tickets, B, err);
+}
+}  // namespace
+
+cudaError_t launch_conv_tc(const CUtensorMap& map_h, const CUtensorMap& map_wc,
+                           const CUtensorMap* map_wg, const __nv_bfloat16* h,
+                           int B, int K, int H, int r, __nv_bfloat16* y,
+                           float* gate, unsigned* tickets, int* err,
+                           cudaStream_t s) {
+  if (conv_tc_bc(B * K) == 128)
+    return launch_conv_bc<128>(map_h, map_wc, map_wg, h, B, K, H, r, y, gate,
+                               tickets, err, s);
+  return launch_conv_bc<32>(map_h, map_wc, map_wg, h, B, K, H, r, y, gate,
+                            tickets, err, s);
 }
 
 }  // namespace dflash

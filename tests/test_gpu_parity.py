@@ -364,6 +364,8 @@ def test_full_size_workload(lib, name):
     (9, 3, 128, 2051, 40, 1.5),     # r not a multiple of 64 (partial gate tile)
     (5, 3, 200, 1999, 48, 0.0),     # ragged K tail, greedy
     (20, 15, 136, 4099, 256, 1.0),  # M = 300: CTA pairs, full rank
+    (65, 16, 200, 3001, 200, 1.0),  # M = 1040: 128-channel conv tiles,
+                                    # ragged H and a partial gate tile
 ])
 def test_fused_draft_bf16(lib, B, K, H, V, r, T):
     w = synth.Workload("small", B=B, K=K, V=V, H=H, r=r, dtype="bf16", T=T,
