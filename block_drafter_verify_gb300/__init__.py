@@ -3,15 +3,17 @@
 The work happens in ``_build/libdflash.so`` (CUDA kernels behind the C ABI
 of include/dflash.h); this package is its ctypes binding.
 """
-from .binding import (BF16, C, FP32, STAGES, DFlashError, DraftVerify,
-                      EXPORTS, dflash_check, dflash_draft, dflash_lmhead_topk,
+from .binding import (BF16, C, COMMIT_STATS, FP32, STAGES, DFlashError,
+                      DraftVerify, EXPORTS, dflash_check, dflash_commit,
+                      dflash_draft, dflash_lmhead_topk,
                       dflash_pair_score, dflash_path_walk, dflash_philox4x32,
                       dflash_profile_stage, dflash_verify,
                       dflash_verify_noalloc, dflash_workspace_bytes,
                       library_path, load)
 
-__all__ = ["BF16", "C", "FP32", "STAGES", "DFlashError", "DraftVerify",
-           "EXPORTS", "dflash_check", "dflash_draft", "dflash_lmhead_topk",
+__all__ = ["BF16", "C", "COMMIT_STATS", "FP32", "STAGES", "DFlashError",
+           "DraftVerify", "EXPORTS", "dflash_check", "dflash_commit",
+           "dflash_draft", "dflash_lmhead_topk",
            "dflash_pair_score", "dflash_path_walk", "dflash_philox4x32",
            "dflash_profile_stage", "dflash_verify", "dflash_verify_noalloc",
            "dflash_workspace_bytes", "library_path", "load"]

@@ -21,7 +21,7 @@ STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported",
 
 EXPORTS = ("dflash_workspace_bytes", "dflash_lmhead_topk", "dflash_pair_score",
            "dflash_path_walk", "dflash_draft", "dflash_verify",
-           "dflash_verify_noalloc",
+           "dflash_verify_noalloc", "dflash_commit",
            "dflash_philox4x32", "dflash_profile_stage", "dflash_check",
            "dflash_status_string")
 STAGES = ("conv", "lmhead", "merge", "pair_score", "walk", "verify")
@@ -69,6 +69,7 @@ def load(path: str | None = None):
         "dflash_verify_noalloc": (i32, [vp, vp, vp, vp, i32, i32, i32, f32,
                                         u64, u64, vp, vp, vp]),
         "dflash_philox4x32": (i32, [vp, u64, vp, i64, vp]),
+        "dflash_commit": (i32, [vp, vp, i32, i32, vp, vp, vp, i32, vp, vp]),
         "dflash_profile_stage": (i32, [i32, vp, vp]),
         "dflash_check": (i32, [vp]),
         "dflash_status_string": (ctypes.c_char_p, [i32]),
@@ -208,6 +209,20 @@ def dflash_verify_noalloc(target_logits, draft, topi, q, T, seed, cycle,
           _ptr(n_accepted), _ptr(out_tok), _stream(stream))
 
 
+COMMIT_STATS = 3 + 16 + 1
+
+
+def dflash_commit(n_accepted, out_tok, anchor, tokens, length, stats,
+                  stream=None):
+    """n_accepted [B], out_tok [B,K+1] i32 (from dflash_verify); anchor [B]
+    i32 in/out; tokens [B,capacity] and length [B] i32 in/out; stats
+    [COMMIT_STATS] int64 in/out (accepted, passes, emitted, histogram)."""
+    B, K1 = out_tok.shape
+    _call("dflash_commit", _ptr(n_accepted), _ptr(out_tok), B, K1 - 1,
+          _ptr(anchor), _ptr(tokens), _ptr(length), tokens.shape[1],
+          _ptr(stats), _stream(stream))
+
+
 def dflash_philox4x32(ctr, seed, out, stream=None):
     """ctr [n,4] and out [n,4] int32 tensors holding uint32 words."""
     _call("dflash_philox4x32", _ptr(ctr), int(seed) & (2**64 - 1), _ptr(out),
@@ -296,6 +311,11 @@ class DraftVerify:
         self.draft_all(h, anchor, T, seed, cycle, stream)
         self.verify(L, T, seed, cycle, stream)
         return self.n, self.out
+
+    def commit(self, anchor, tokens, length, stats, stream=None):
+        """Commit the last verify's tokens; the anchor moves to the last
+        emitted token of each sequence."""
+        dflash_commit(self.n, self.out, anchor, tokens, length, stats, stream)
 
     def y(self, fused=False):
         """y written by the last lmhead (or, fused=True, draft_all) call:

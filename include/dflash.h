@@ -259,6 +259,38 @@ dflash_status dflash_verify_noalloc(const float* target_logits,
                                    int32_t* n_accepted, int32_t* out_tok,
                                    dflash_stream_t s);
 
+/*
+ * The step after verify in a draft-verify loop: commit each sequence's
+ * emitted tokens and hand the last one over as the next cycle's anchor.
+ *
+ * "What a block-diffusion drafter is" (2B-drafter page): the target
+ * verifies the whole run and the matching prefix is kept; "How many tokens
+ * survive": acceptance length is the mean number of draft tokens kept per
+ * verification pass.  For every sequence b, with n = n_accepted[b]:
+ *   tokens[b, length[b] .. length[b] + n] = out_tok[b, 0 .. n]
+ *   (the n accepted drafts, then the resampled or bonus token),
+ *   length[b] += n + 1, anchor[b] = out_tok[b, n];
+ *   stats[0] += n (accepted drafts), stats[1] += 1 (verification passes),
+ *   stats[2] += n + 1 (emitted tokens), stats[3 + n] += 1 (histogram).
+ * Mean acceptance length = stats[0] / stats[1].
+ *   n_accepted [B] int32, out_tok [B, K+1] int32   from dflash_verify
+ *   anchor     [B] int32 in/out      the next cycle's anchor
+ *   tokens     [B, capacity] int32 in/out, length [B] int32 in/out:
+ *              each sequence's committed tokens; a sequence whose buffer
+ *              is full keeps the tokens that fit, and the call flags
+ *              DFLASH_ERR_BAD_INDEX in the device error word (length still
+ *              advances, so a caller can tell how many were dropped)
+ *   stats      [DFLASH_COMMIT_STATS] int64 in/out, accumulated over calls
+ * All device memory, caller-owned; no workspace.  Requires 1 <= K <= 16,
+ * capacity >= 1.  An n_accepted outside [0, K] is flagged as
+ * DFLASH_ERR_BAD_INDEX and that sequence is left unchanged.
+ */
+#define DFLASH_COMMIT_STATS (3 + DFLASH_MAX_K + 1)
+dflash_status dflash_commit(const int32_t* n_accepted, const int32_t* out_tok,
+                            int B, int K, int32_t* anchor, int32_t* tokens,
+                            int32_t* length, int capacity, int64_t* stats,
+                            dflash_stream_t s);
+
 /* Philox4x32-10 of n counters (ctr [n, 4] uint32, device) under key
  * (seed lo, seed hi) into out [n, 4] uint32 (device): the generator the
  * walk and verify draw from, exposed so callers can reproduce draws. */

@@ -5,10 +5,10 @@ legs of ``bench.py`` may import this package.  The product path (the CUDA
 library and its Python binding) never does.
 """
 from . import philox
-from .dflash_oracle import (C, conv2tap, draft_verify_cycle, gate,
+from .dflash_oracle import (C, commit, conv2tap, draft_verify_cycle, gate,
                             lmhead_topk, pair_score, path_walk, round_bf16,
                             to_storage, verify)
 
-__all__ = ["philox", "C", "conv2tap", "draft_verify_cycle", "gate",
+__all__ = ["philox", "C", "commit", "conv2tap", "draft_verify_cycle", "gate",
            "lmhead_topk", "pair_score", "path_walk", "round_bf16",
            "to_storage", "verify"]

@@ -329,3 +329,31 @@ def draft_verify_cycle(h, w_conv, w_lm, w_gate, e_in, e_out, anchor, L,
     return {"y": y, "topv": topv, "topi": topi, "lse": lse.reshape(B, K),
             "g": g, "S": S32, "slot": slot, "draft": draft, "q": q32,
             "n": n, "out": out}
+
+
+def commit(n, out, anchor, tokens, length, stats):
+    """Commit each sequence's emitted tokens and hand the last one over as
+    the next anchor (in place; numpy arrays).
+
+    [2B] "What a block-diffusion drafter is": the target verifies the run
+    and the matching prefix is kept; "How many tokens survive": acceptance
+    length is the mean number of draft tokens kept per verification pass.
+    n [B] accepted drafts and out [B,K+1] from verify; anchor [B];
+    tokens [B,capacity] and length [B] the committed tokens; stats
+    [3+17]: accepted drafts, passes, emitted tokens, histogram of n.
+    Tokens past a sequence's capacity are dropped (its length still
+    advances).
+    """
+    B, cap = tokens.shape
+    for b in range(B):
+        nb = int(n[b])
+        for i in range(nb + 1):
+            pos = int(length[b]) + i
+            if pos < cap:
+                tokens[b, pos] = out[b, i]
+        length[b] += nb + 1
+        anchor[b] = out[b, nb]
+        stats[0] += nb
+        stats[1] += 1
+        stats[2] += nb + 1
+        stats[3 + nb] += 1

@@ -535,3 +535,37 @@ def test_tiny_cycle_runs_and_is_consistent():
     assert list(r["out"][0, :n]) == list(r["draft"][0, :n])
     # greedy: the emitted token after the accepted prefix is the argmax
     assert r["out"][0, n] == int(np.argmax(L[0, n]))
+
+
+# --------------------------------------------------------------------------
+# commit: the step after verify (hand-computed cases)
+def test_commit_keeps_the_prefix_and_moves_the_anchor():
+    n = np.array([1, 3, 0])
+    out = np.array([[5, 9, -1, -1], [1, 2, 3, 4], [7, -1, -1, -1]])
+    anchor = np.array([0, 0, 0])
+    tokens = np.full((3, 6), -9)
+    length = np.array([0, 2, 5])
+    stats = np.zeros(20, np.int64)
+    oracle.commit(n, out, anchor, tokens, length, stats)
+    assert anchor.tolist() == [9, 4, 7]
+    assert length.tolist() == [2, 6, 6]
+    assert tokens[0, :2].tolist() == [5, 9] and tokens[0, 2] == -9
+    assert tokens[1, 2:6].tolist() == [1, 2, 3, 4]
+    assert tokens[2, 5] == 7
+    # accepted drafts, passes, emitted, histogram of n (0, 1, 3 once each)
+    assert stats[:3].tolist() == [4, 3, 7]
+    assert stats[3:3 + 5].tolist() == [1, 1, 0, 1, 0]
+
+
+def test_commit_drops_tokens_past_capacity_and_accumulates():
+    n = np.array([2])
+    out = np.array([[1, 2, 3]])
+    anchor = np.array([0])
+    tokens = np.full((1, 4), -9)
+    length = np.array([0])
+    stats = np.zeros(20, np.int64)
+    oracle.commit(n, out, anchor, tokens, length, stats)
+    oracle.commit(n, out, anchor, tokens, length, stats)
+    assert tokens[0].tolist() == [1, 2, 3, 1]   # the 5th and 6th dropped
+    assert length.tolist() == [6] and anchor.tolist() == [3]
+    assert stats[0] / stats[1] == 2.0           # mean acceptance length
