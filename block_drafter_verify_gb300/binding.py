@@ -21,7 +21,8 @@ STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported",
 
 EXPORTS = ("dflash_workspace_bytes", "dflash_lmhead_topk", "dflash_pair_score",
            "dflash_path_walk", "dflash_draft", "dflash_verify",
-           "dflash_verify_noalloc", "dflash_commit",
+           "dflash_verify_noalloc", "dflash_commit", "dflash_path_viterbi",
+           "dflash_top16_recall",
            "dflash_philox4x32", "dflash_profile_stage", "dflash_check",
            "dflash_status_string")
 STAGES = ("conv", "lmhead", "merge", "pair_score", "walk", "verify")
@@ -70,6 +71,8 @@ def load(path: str | None = None):
                                         u64, u64, vp, vp, vp]),
         "dflash_philox4x32": (i32, [vp, u64, vp, i64, vp]),
         "dflash_commit": (i32, [vp, vp, i32, i32, vp, vp, vp, i32, vp, vp]),
+        "dflash_path_viterbi": (i32, [vp, vp, i32, i32, vp, vp, vp, vp]),
+        "dflash_top16_recall": (i32, [vp, vp, i32, i32, i32, vp, vp, vp]),
         "dflash_profile_stage": (i32, [i32, vp, vp]),
         "dflash_check": (i32, [vp]),
         "dflash_status_string": (ctypes.c_char_p, [i32]),
@@ -207,6 +210,38 @@ def dflash_verify_noalloc(target_logits, draft, topi, q, T, seed, cycle,
           _ptr(topi), _ptr(q), B, K1 - 1, V, float(T),
           int(seed) & (2**64 - 1), int(cycle) & (2**64 - 1),
           _ptr(n_accepted), _ptr(out_tok), _stream(stream))
+
+
+def dflash_path_viterbi(scores, topi, slot, draft, q, stream=None):
+    """scores [B,K,16,16] f32, topi [B,K,16] i32 -> slot, draft [B,K] i32,
+    q [B,K,16] f32 (one-hot): the global max-sum path (T = 0)."""
+    B, K = scores.shape[:2]
+    _call("dflash_path_viterbi", _ptr(scores), _ptr(topi), B, K, _ptr(slot),
+          _ptr(draft), _ptr(q), _stream(stream))
+
+
+def dflash_top16_recall(target_logits, topi, target_argmax, in_top16,
+                        stream=None):
+    """target_logits [B,K+1,V] f32, topi [B,K,16] -> target_argmax and
+    in_top16 [B,K] i32 for the K drafted positions."""
+    B, K1, V = target_logits.shape
+    _want(target_logits, torch.float32, "target_logits")
+    _call("dflash_top16_recall", _ptr(target_logits), _ptr(topi), B, K1 - 1,
+          V, _ptr(target_argmax), _ptr(in_top16), _stream(stream))
+
+
+def recall_by_position(in_top16):
+    """Recall@16 per drafted position, and the acceptance length a perfect
+    selector would reach under greedy verification (leading positions whose
+    target token is among the candidates), from dflash_top16_recall's
+    in_top16 [B,K] (host-side arithmetic on the kernel's flags)."""
+    f = in_top16.to(torch.int64)
+    recall = f.double().mean(dim=0)
+    miss = (f == 0)
+    first = torch.where(miss.any(dim=1), miss.int().argmax(dim=1),
+                        torch.full_like(miss[:, 0], f.shape[1],
+                                        dtype=torch.int64))
+    return recall, first.double().mean()
 
 
 COMMIT_STATS = 3 + 16 + 1

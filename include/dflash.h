@@ -291,6 +291,40 @@ dflash_status dflash_commit(const int32_t* n_accepted, const int32_t* out_tok,
                             int32_t* length, int capacity, int64_t* stats,
                             dflash_stream_t s);
 
+/*
+ * Selector variant: the global max-sum path through the K x 16 lattice
+ * (a Viterbi walk), for T = 0.  "What Comes Next" (Keep Drafting Parallel
+ * page): pairwise scoring is the simplest selector and there is room to
+ * explore; the pages' own greedy walk follows the best successor instead.
+ *   best_0(j) = scores[b,0,0,j],
+ *   best_t(j) = max_i best_{t-1}(i) + scores[b,t,i,j]  (t = 1..K-1),
+ * the path ends in the lowest j of maximal best_{K-1}(j), predecessors on
+ * ties are the lowest i, sums in fp32.  Outputs as dflash_path_walk: slot,
+ * draft = topi[b,t,slot], q one-hot.  scores 16-byte aligned; 1 <= K <= 16.
+ * A sequence with no path of finite score flags DFLASH_ERR_BAD_INDEX.
+ */
+dflash_status dflash_path_viterbi(const float* scores, const int32_t* topi,
+                                  int B, int K, int32_t* slot, int32_t* draft,
+                                  float* q, dflash_stream_t s);
+
+/*
+ * Diagnostic of the candidate lists ("What Comes Next", Keep Drafting
+ * Parallel page: recall of the 16 candidates by position, and the
+ * acceptance length an oracle that always picks the right candidate among
+ * them would reach).  For every drafted position (b, t), t < K:
+ *   target_argmax[b,t] = the first argmax over v of target_logits[b,t,v],
+ *   in_top16[b,t]      = 1 if that token is among topi[b,t,:], else 0.
+ * Recall@16 at position t is the mean of in_top16[:, t]; with greedy
+ * verification a perfect selector is accepted up to the first position
+ * whose in_top16 is 0.  Reads the K target rows once (B*K*V*4 bytes).
+ * target_logits [B, K+1, V] fp32; topi [B*K, 16]; outputs [B*K] int32.
+ * A NaN / +inf logit flags DFLASH_ERR_NONFINITE.
+ */
+dflash_status dflash_top16_recall(const float* target_logits,
+                                  const int32_t* topi, int B, int K, int V,
+                                  int32_t* target_argmax, int32_t* in_top16,
+                                  dflash_stream_t s);
+
 /* Philox4x32-10 of n counters (ctr [n, 4] uint32, device) under key
  * (seed lo, seed hi) into out [n, 4] uint32 (device): the generator the
  * walk and verify draw from, exposed so callers can reproduce draws. */

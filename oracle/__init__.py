@@ -6,9 +6,10 @@ library and its Python binding) never does.
 """
 from . import philox
 from .dflash_oracle import (C, commit, conv2tap, draft_verify_cycle, gate,
-                            lmhead_topk, pair_score, path_walk, round_bf16,
-                            to_storage, verify)
+                            lmhead_topk, pair_score, path_total,
+                            path_viterbi, path_walk, round_bf16, to_storage,
+                            top16_recall, verify)
 
 __all__ = ["philox", "C", "commit", "conv2tap", "draft_verify_cycle", "gate",
-           "lmhead_topk", "pair_score", "path_walk", "round_bf16",
-           "to_storage", "verify"]
+           "lmhead_topk", "pair_score", "path_total", "path_viterbi",
+           "path_walk", "round_bf16", "to_storage", "top16_recall", "verify"]

@@ -357,3 +357,69 @@ def commit(n, out, anchor, tokens, length, stats):
         stats[1] += 1
         stats[2] += nb + 1
         stats[3 + nb] += 1
+
+
+def path_viterbi(S, topi):
+    """Global max-sum path through the candidate lattice (T = 0 selector
+    variant; [KP] "What Comes Next": pairwise scoring is the simplest
+    selector, there is room to explore).
+
+    best_0(j) = S[b,0,0,j]; best_t(j) = max_i best_{t-1}(i) + S[b,t,i,j];
+    the path ends in the lowest j of maximal total and takes the lowest
+    predecessor i on ties (the sums in float64 of the given values).
+    Returns slot [B,K], draft [B,K], q one-hot [B,K,16] and the path's
+    total [B].
+    """
+    S = np.asarray(S, np.float64)
+    B, K = S.shape[:2]
+    slot = np.zeros((B, K), np.int32)
+    draft = np.zeros((B, K), np.int32)
+    q = np.zeros((B, K, C))
+    total = np.zeros(B)
+    for b in range(B):
+        best = S[b, 0, 0].copy()
+        back = np.zeros((K, C), np.int64)
+        for t in range(1, K):
+            cand = best[:, None] + S[b, t]          # [i, j]
+            back[t] = np.argmax(cand, axis=0)       # first maximum: lowest i
+            best = cand[back[t], np.arange(C)]
+        j = int(np.argmax(best))
+        total[b] = best[j]
+        for t in range(K - 1, -1, -1):
+            slot[b, t] = j
+            draft[b, t] = topi[b, t, j]
+            q[b, t, j] = 1.0
+            if t > 0:
+                j = int(back[t, j])
+    return slot, draft, q, total
+
+
+def path_total(S, slot):
+    """Sum of the scores along each sequence's path (float64)."""
+    S = np.asarray(S, np.float64)
+    B, K = slot.shape
+    tot = np.zeros(B)
+    for b in range(B):
+        prev = 0
+        for t in range(K):
+            tot[b] += S[b, t, prev, slot[b, t]]
+            prev = slot[b, t]
+    return tot
+
+
+def top16_recall(L, topi):
+    """For each drafted position (b, t), t < K: the target's first argmax
+    and whether it is among the 16 candidates ([KP] "What Comes Next":
+    recall of the candidate lists by position, and the oracle selector).
+    L [B,K+1,V]; topi [B,K,16].  Returns target_argmax [B,K], in_top16
+    [B,K] (0/1)."""
+    L = np.asarray(L)
+    B, K = topi.shape[:2]
+    arg = np.zeros((B, K), np.int64)
+    hit = np.zeros((B, K), np.int64)
+    for b in range(B):
+        for t in range(K):
+            a = int(np.argmax(L[b, t]))             # first maximum
+            arg[b, t] = a
+            hit[b, t] = int(a in set(int(v) for v in topi[b, t]))
+    return arg, hit

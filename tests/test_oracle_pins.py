@@ -569,3 +569,63 @@ def test_commit_drops_tokens_past_capacity_and_accumulates():
     assert tokens[0].tolist() == [1, 2, 3, 1]   # the 5th and 6th dropped
     assert length.tolist() == [6] and anchor.tolist() == [3]
     assert stats[0] / stats[1] == 2.0           # mean acceptance length
+
+
+# --------------------------------------------------------------------------
+# selector variants: the Viterbi walk against brute force over all paths
+def _paths16(K):
+    return np.array(np.meshgrid(*[np.arange(16)] * K, indexing="ij")).reshape(
+        K, -1).T
+
+
+@pytest.mark.parametrize("K,seed", [(1, 0), (2, 1), (3, 2), (3, 3)])
+def test_viterbi_equals_brute_force_max_sum(K, seed):
+    rng = np.random.default_rng(seed)
+    S = rng.normal(size=(3, K, 16, 16))
+    S[:, 0] = S[:, 0, :1]                      # position 0: the anchor's row
+    S[0, :, :, 5] = -np.inf                    # a padded candidate
+    topi = rng.integers(0, 1000, size=(3, K, 16))
+    slot, draft, q, total = oracle.path_viterbi(S, topi)
+    P = _paths16(K)
+    for b in range(3):
+        tot = np.zeros(len(P))
+        prev = np.zeros(len(P), int)
+        for t in range(K):
+            tot += S[b, t, prev, P[:, t]]
+            prev = P[:, t]
+        assert np.isclose(total[b], tot.max())
+        assert np.isclose(oracle.path_total(S, slot)[b], tot.max())
+        assert np.array_equal(draft[b], topi[b, np.arange(K), slot[b]])
+        assert np.all(q[b].sum(axis=1) == 1) and np.all(
+            q[b, np.arange(K), slot[b]] == 1)
+
+
+def test_viterbi_can_beat_the_greedy_walk():
+    """A lattice where the best first step leads into a poor row."""
+    S = np.zeros((1, 2, 16, 16))
+    S[0, 0, :, 0] = 2.0          # greedy takes slot 0 at t = 0 ...
+    S[0, 0, :, 1] = 1.0
+    S[0, 1, 0, :] = -5.0         # ... whose successors are all poor
+    S[0, 1, 1, 3] = 3.0          # slot 1 then 3: total 4 > greedy's -3
+    topi = np.arange(32).reshape(1, 2, 16)
+    slot, _, _, total = oracle.path_viterbi(S, topi)
+    g_slot, _, _, _ = oracle.path_walk(S, topi, 0.0, None)
+    assert slot[0].tolist() == [1, 3] and total[0] == 4.0
+    assert g_slot[0].tolist() == [0, 0]
+
+
+def test_top16_recall_hand_case():
+    L = np.zeros((2, 3, 10))
+    L[0, 0, 7] = 1.0
+    L[0, 1, 2] = 5.0
+    L[0, 1, 3] = 5.0             # tie: the first maximum, 2
+    L[1, 0, 9] = 1.0
+    L[1, 1, 4] = 1.0
+    topi = np.full((2, 2, 16), -1)
+    topi[0, 0, 3] = 7
+    topi[0, 1, 0] = 3            # 3 is not the first maximum
+    topi[1, 0, 15] = 9
+    topi[1, 1, 2] = 4
+    arg, hit = oracle.top16_recall(L, topi)
+    assert arg.tolist() == [[7, 2], [9, 4]]
+    assert hit.tolist() == [[1, 0], [1, 1]]
