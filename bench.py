@@ -620,6 +620,9 @@ def run_ours(args):
                 "with": "dflash_draft + dflash_verify + dflash_commit, "
                         "anchor handed over every cycle"}
 
+    sel = selector_report(dv_mod, dv, w, h, anchor, L, seed, stream, dev,
+                          pk)
+
     # achieved bandwidth of the other stages (algorithmic bytes per launch
     # / mean event time), against the measured HBM peak
     stage_roof = {}
@@ -688,6 +691,7 @@ def run_ours(args):
         "mean_emitted": n_mean + 1,
         "cycle_ms": cycle_ms,
         "loop": loop,
+        "selectors": sel,
         "stage_us": stage_us,
         "stage_roofline": stage_roof,
         "clocks": clk.summary(),
@@ -699,6 +703,59 @@ def run_ours(args):
     }
     print(json.dumps(line))
     return 0
+
+
+def selector_report(dv_mod, dv, w, h, anchor, L, seed, stream, dev, pk,
+                    reps=20):
+    """The T = 0 selector variants on the bench lattice, outside the timed
+    cycles: mean accepted drafts under greedy verification with the greedy
+    walk and with the Viterbi walk (same pair scores), recall@16 of the
+    target's argmax by position and the acceptance a perfect selector would
+    reach, and the two kernels' event times (recall: algorithmic bytes / time
+    against the HBM peak).  The recall launch follows dflash_draft, whose
+    W_lm stream has evicted the target logits from L2."""
+    import torch
+    B, K, C = w.B, w.K, 16
+    topi = dv.topi.view(B, K, C)
+    arg = torch.empty(B, K, dtype=torch.int32, device=dev)
+    hit = torch.empty_like(arg)
+    n_g = torch.zeros((), dtype=torch.int64, device=dev)
+    n_v = torch.zeros((), dtype=torch.int64, device=dev)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)]
+          for _ in range(reps)]
+    torch.cuda.synchronize(dev)
+    for i in range(reps):
+        c = 2 * 10**6 + i
+        dv.draft_all(h, anchor, 0.0, seed, c)
+        ev[i][0].record(stream)
+        dv_mod.dflash_top16_recall(L, topi, arg, hit)
+        ev[i][1].record(stream)
+        dv.verify(L, 0.0, seed, c)
+        n_g += dv.n.sum()
+        ev[i][2].record(stream)
+        dv_mod.dflash_path_viterbi(dv.scores, topi, dv.slot, dv.draft, dv.q)
+        ev[i][3].record(stream)
+        dv.verify(L, 0.0, seed, c)
+        n_v += dv.n.sum()
+    torch.cuda.synchronize(dev)
+    dv_mod.dflash_check()
+    t_rec = statistics.mean(e[0].elapsed_time(e[1]) for e in ev) * 1e3
+    t_vit = statistics.mean(e[2].elapsed_time(e[3]) for e in ev) * 1e3
+    rec_bytes = B * K * (w.V * 4 + C * 4 + 8)
+    vit_bytes = B * K * (C * C * 4 + C * 4 + 8 + C * 4)
+    recall, perfect = dv_mod.recall_by_position(hit)
+    gbs = rec_bytes / (t_rec * 1e-6) / 1e9
+    return {"T": 0.0,
+            "mean_accepted_greedy_walk": float(n_g.item()) / (reps * B),
+            "mean_accepted_viterbi_walk": float(n_v.item()) / (reps * B),
+            "mean_accepted_perfect_selector": float(perfect),
+            "recall16_by_position": [round(float(v), 4) for v in recall],
+            "viterbi_us": t_vit,
+            "viterbi_GB/s": vit_bytes / (t_vit * 1e-6) / 1e9,
+            "recall_us": t_rec,
+            "recall_roofline": {"bound": "hbm", "bytes": rec_bytes,
+                                "achieved": gbs, "peak": pk["hbm_gbs"],
+                                "unit": "GB/s", "frac": gbs / pk["hbm_gbs"]}}
 
 
 def stage_bytes(w, fused):

@@ -83,10 +83,13 @@ __global__ void __launch_bounds__(kViterbiWarps * 32)
   }
 }
 
-constexpr int kRecallThreads = 256;
+constexpr int kRecallThreads = 512;
+constexpr int kRecallUnroll = 4;  // float4 loads in flight per thread
 
 // Row (b, t), t < K, of the target logits: first argmax, and membership of
-// that token among topi[b, t, :].
+// that token among topi[b, t, :].  Each thread visits its indices in
+// increasing order and keeps the first maximum; the reductions prefer the
+// lower index on equal values.
 __global__ void __launch_bounds__(kRecallThreads)
     top16_recall_kernel(const float* __restrict__ L,
                         const int* __restrict__ topi, int K, int V, int vec4,
@@ -98,22 +101,34 @@ __global__ void __launch_bounds__(kRecallThreads)
   float bv = -INFINITY;
   int bi = 0x7fffffff;
   bool bad = false;
+  auto take = [&](float e, int v) {
+    bad |= (e != e) || e == INFINITY;
+    if (e > bv) { bv = e; bi = v; }
+  };
   if (vec4) {
-    for (int v = 4 * tid; v < V; v += 4 * kRecallThreads) {
-      const float4 f = *reinterpret_cast<const float4*>(x + v);
-      const float e[4] = {f.x, f.y, f.z, f.w};
+    const float4* x4 = reinterpret_cast<const float4*>(x);
+    const int n4 = V / 4;
+    constexpr int kStride = kRecallThreads * kRecallUnroll;
+    for (int base = tid; base < n4; base += kStride) {
+      float4 f[kRecallUnroll];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        bad |= (e[k] != e[k]) || e[k] == INFINITY;
-        if (e[k] > bv) { bv = e[k]; bi = v + k; }
+      for (int u = 0; u < kRecallUnroll; ++u) {
+        const int i = base + u * kRecallThreads;
+        f[u] = i < n4 ? __ldcs(x4 + i)
+                      : make_float4(-INFINITY, -INFINITY, -INFINITY,
+                                    -INFINITY);
+      }
+#pragma unroll
+      for (int u = 0; u < kRecallUnroll; ++u) {
+        const int v = 4 * (base + u * kRecallThreads);
+        take(f[u].x, v);
+        take(f[u].y, v + 1);
+        take(f[u].z, v + 2);
+        take(f[u].w, v + 3);
       }
     }
   } else {
-    for (int v = tid; v < V; v += kRecallThreads) {
-      const float e = x[v];
-      bad |= (e != e) || e == INFINITY;
-      if (e > bv) { bv = e; bi = v; }
-    }
+    for (int v = tid; v < V; v += kRecallThreads) take(x[v], v);
   }
 #pragma unroll
   for (int o = 16; o; o >>= 1) {
