@@ -5,11 +5,16 @@ legs of ``bench.py`` may import this package.  The product path (the CUDA
 library and its Python binding) never does.
 """
 from . import philox
-from .dflash_oracle import (C, commit, conv2tap, draft_verify_cycle, gate,
-                            lmhead_topk, pair_score, path_total,
-                            path_viterbi, path_walk, round_bf16, to_storage,
+from .dflash_oracle import (C, E4M3_MAX, commit, conv2tap,
+                            dequantize_e4m3_rows, draft_verify_cycle,
+                            e4m3_decode, e4m3_encode, gate, lmhead_topk,
+                            lmhead_topk_e4m3, pair_score, path_total,
+                            path_viterbi, path_walk, quantize_e4m3_rows,
+                            round_bf16, to_storage,
                             top16_recall, verify)
 
-__all__ = ["philox", "C", "commit", "conv2tap", "draft_verify_cycle", "gate",
-           "lmhead_topk", "pair_score", "path_total", "path_viterbi",
+__all__ = ["philox", "C", "E4M3_MAX", "commit", "conv2tap",
+           "dequantize_e4m3_rows", "draft_verify_cycle", "e4m3_decode",
+           "e4m3_encode", "gate", "lmhead_topk", "lmhead_topk_e4m3",
+           "quantize_e4m3_rows", "pair_score", "path_total", "path_viterbi",
            "path_walk", "round_bf16", "to_storage", "top16_recall", "verify"]

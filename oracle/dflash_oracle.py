@@ -127,6 +127,87 @@ def lmhead_topk(y: np.ndarray, w_lm: np.ndarray, want_logits=False):
 
 
 # --------------------------------------------------------------------------
+# a2 with 8-bit LM-head operands (quantized drafters: [2B] "What a
+# block-diffusion drafter is" and [KP] "What Comes Next" ship GGUF Q4_K_M
+# drafter builds and note that quantized kernels may prefer other block
+# sizes).  The format is OCP FP8 E4M3 ("e4m3fn"): 1 sign bit, 4 exponent
+# bits with bias 7, 3 mantissa bits, no infinities, S.1111.111 is NaN, the
+# largest finite magnitude is 448, subnormals are m/8 * 2^-6.
+# --------------------------------------------------------------------------
+E4M3_MAX = 448.0
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    """Values (float64) of E4M3 codes, NaN for the two NaN codes."""
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = (c & 0x7).astype(np.float64)
+    mag = np.where(e == 0, m / 8.0 * 2.0 ** -6,
+                   (1.0 + m / 8.0) * np.exp2(e.astype(np.float64) - 7.0))
+    mag = np.where((e == 15) & (m == 7), np.nan, mag)
+    return sign * mag
+
+
+def e4m3_encode(x) -> np.ndarray:
+    """Nearest E4M3 code of each finite float32 value (ties to the even
+    mantissa), magnitudes beyond 448 saturated to 448; the sign of zero is
+    kept.  Works on the exact float64 value of the float32 input: the
+    quantum at magnitude a is 2^(max(floor(log2 a), -6) - 3)."""
+    x = np.asarray(x, dtype=np.float32).astype(np.float64)
+    if not np.all(np.isfinite(x)):
+        raise ValueError("e4m3_encode: non-finite input")
+    neg = np.signbit(x)
+    a = np.abs(x)
+    _, E = np.frexp(np.where(a > 0, a, 1.0))     # a = f * 2^E, f in [0.5, 1)
+    e = np.maximum(E - 1, -6)                     # floor(log2 a), clamped
+    quantum = np.exp2((e - 3).astype(np.float64))
+    r = np.rint(a / quantum) * quantum            # rint: ties to even
+    r = np.minimum(np.where(a > 0, r, 0.0), E4M3_MAX)
+    # the code of the (representable) magnitude r
+    _, Er = np.frexp(np.where(r > 0, r, 1.0))
+    er = Er - 1
+    normal = r >= 2.0 ** -6
+    exp_field = np.where(normal, er + 7, 0)
+    mant = np.where(normal, r / np.exp2(er.astype(np.float64)) * 8 - 8,
+                    r / 2.0 ** -9)
+    code = (exp_field.astype(np.int64) << 3) | np.rint(mant).astype(np.int64)
+    code = np.where(r > 0, code, 0) | np.where(neg, 0x80, 0)
+    return code.astype(np.uint8)
+
+
+def quantize_e4m3_rows(X):
+    """Per-row scaled E4M3 codes of a matrix: X[i] ~ scale[i] * code[i].
+
+    In float32 arithmetic, as the CUDA kernel decides the codes:
+    amax = max |x| over the row, scale = amax / 448 (1 for an all-zero
+    row), code = e4m3(x / scale) with both divisions correctly rounded.
+    X: [R, H] (values of the storage dtype).  Returns codes uint8 [R, H]
+    and scale float32 [R]."""
+    X = np.asarray(X, dtype=np.float32)
+    amax = np.abs(X).max(axis=1)
+    scale = np.where(amax > 0, amax / np.float32(E4M3_MAX),
+                     np.float32(1.0)).astype(np.float32)
+    return e4m3_encode(X / scale[:, None]), scale
+
+
+def dequantize_e4m3_rows(codes, scale) -> np.ndarray:
+    """scale[i] * value(code[i, k]) in float64."""
+    return e4m3_decode(codes) * np.asarray(scale, np.float64)[:, None]
+
+
+def lmhead_topk_e4m3(y, w_codes, w_scale, want_logits=False):
+    """The LM head with 8-bit operands: y (the conv output, storage
+    values) is quantized per row, W_lm is given as per-row codes and
+    scales; U = (s_y q_y)(s_W q_W)^T exactly (float64), then logsumexp and
+    top-16 as in :func:`lmhead_topk`.  Also returns the y codes/scales."""
+    yc, ys = quantize_e4m3_rows(y)
+    out = lmhead_topk(dequantize_e4m3_rows(yc, ys),
+                      dequantize_e4m3_rows(w_codes, w_scale), want_logits)
+    return out + (yc, ys)
+
+
+# --------------------------------------------------------------------------
 # a3: context gate + low-rank bilinear pair scores
 # --------------------------------------------------------------------------
 def gate(h: np.ndarray, w_gate: np.ndarray) -> np.ndarray:
@@ -305,16 +386,23 @@ def verify(L, draft, topi, q, T: float, u_acc, u_res):
 # one whole draft-verify cycle
 # --------------------------------------------------------------------------
 def draft_verify_cycle(h, w_conv, w_lm, w_gate, e_in, e_out, anchor, L,
-                       T: float, seed: int, cycle: int, dtype: str):
+                       T: float, seed: int, cycle: int, dtype: str,
+                       w_lm_e4m3=None):
     """All five steps for B sequences, each stage fed by the previous one.
 
     h: [B,K,H] drafter hidden states (values of the storage dtype);
-    L: [B,K+1,V] target logits.  Returns a dict of every intermediate.
+    L: [B,K+1,V] target logits.  With ``w_lm_e4m3 = (codes, scale)`` the
+    LM head runs on 8-bit operands (:func:`lmhead_topk_e4m3`) and w_lm is
+    unused.  Returns a dict of every intermediate.
     """
     h = np.asarray(h, np.float64)
     B, K, H = h.shape
     y = to_storage(conv2tap(h, w_conv), dtype).astype(np.float64)
-    topv, topi, lse = lmhead_topk(y.reshape(B * K, H), w_lm)
+    if w_lm_e4m3 is not None:
+        topv, topi, lse, _, _ = lmhead_topk_e4m3(y.reshape(B * K, H),
+                                                 *w_lm_e4m3)
+    else:
+        topv, topi, lse = lmhead_topk(y.reshape(B * K, H), w_lm)
     topv = topv.reshape(B, K, C)
     topi = topi.reshape(B, K, C)
     g = gate(h, w_gate)

@@ -629,3 +629,88 @@ def test_top16_recall_hand_case():
     arg, hit = oracle.top16_recall(L, topi)
     assert arg.tolist() == [[7, 2], [9, 4]]
     assert hit.tolist() == [[1, 0], [1, 1]]
+
+
+# --------------------------------------------------------------------------
+# 8-bit LM-head operands: the E4M3 codec against torch's float8_e4m3fn (an
+# independent implementation) and the format's closed forms
+def test_e4m3_decode_matches_the_format_and_torch():
+    codes = np.arange(256, dtype=np.uint8)
+    v = oracle.e4m3_decode(codes)
+    assert np.isnan(v[0x7F]) and np.isnan(v[0xFF])
+    ok = ~np.isnan(v)
+    assert np.sum(ok) == 254
+    hand = {0x00: 0.0, 0x01: 2.0 ** -9, 0x07: 7 * 2.0 ** -9, 0x08: 2.0 ** -6,
+            0x38: 1.0, 0x39: 1.125, 0x40: 2.0, 0x7E: 448.0, 0xB8: -1.0,
+            0xFE: -448.0}
+    for c, x in hand.items():
+        assert v[c] == x, hex(c)
+    t = torch.from_numpy(codes).view(torch.float8_e4m3fn).float().numpy()
+    assert np.array_equal(v[ok], t[ok].astype(np.float64))
+
+
+def test_e4m3_encode_matches_torch_including_ties():
+    rng = np.random.default_rng(11)
+    mags = np.exp2(rng.uniform(-12, np.log2(448.0), size=20000))
+    x = (mags * rng.choice([-1, 1], size=mags.size)).astype(np.float32)
+    # every midpoint between neighbouring representable values (ties)
+    rep = np.unique(oracle.e4m3_decode(np.arange(0, 0x7F, dtype=np.uint8)))
+    mid = ((rep[1:] + rep[:-1]) / 2).astype(np.float32)
+    x = np.concatenate([x, mid, -mid, rep.astype(np.float32)])
+    ours = oracle.e4m3_encode(x)
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8)
+    assert np.array_equal(ours, ref.numpy())
+    # ties go to the even mantissa: 1 + 1/16 lies between 1 and 1.125
+    assert oracle.e4m3_encode(np.float32(1.0625)) == 0x38
+    assert oracle.e4m3_encode(np.float32(1.1875)) == 0x3A
+
+
+def test_e4m3_encode_saturates_and_keeps_the_sign_of_zero():
+    x = np.array([448.0, 463.9, 464.0, 500.0, 1e30, -1e30, 0.0, -0.0,
+                  2.0 ** -11, -(2.0 ** -11)], np.float32)
+    assert oracle.e4m3_encode(x).tolist() == [
+        0x7E, 0x7E, 0x7E, 0x7E, 0x7E, 0xFE, 0x00, 0x80, 0x00, 0x80]
+
+
+def test_quantize_rows_scale_amax_and_error_bound():
+    rng = np.random.default_rng(3)
+    X = (rng.standard_normal((40, 300)) * np.exp2(rng.uniform(
+        -8, 8, size=(40, 1)))).astype(np.float32)
+    X[7] = 0.0
+    codes, scale = oracle.quantize_e4m3_rows(X)
+    assert scale.dtype == np.float32 and scale[7] == 1.0
+    assert np.all(codes[7] == 0)
+    amax_col = np.abs(X).argmax(axis=1)
+    for i in range(40):
+        if i == 7:
+            continue
+        assert scale[i] == np.float32(np.abs(X[i]).max()) / np.float32(448)
+        assert codes[i, amax_col[i]] & 0x7F == 0x7E
+    D = oracle.dequantize_e4m3_rows(codes, scale)
+    # round to nearest: within half a quantum, 2^-4 of the magnitude for
+    # normal values and 2^-10 * scale below 2^-6 * scale
+    err = np.abs(D - X.astype(np.float64))
+    bound = np.maximum(np.abs(X) * 2.0 ** -4, scale[:, None] * 2.0 ** -10)
+    assert np.all(err <= bound * (1 + 1e-6))
+
+
+def test_lmhead_e4m3_equals_the_exact_product_of_the_codes():
+    """y rows whose maximum is 448 quantize with scale 1 and exact codes,
+    so U = sum_k y_k * s_v * value(code_vk) in closed form."""
+    V, H = 40, 8
+    y = np.zeros((2, H), np.float32)
+    y[0] = [448, 1, -2, 0.5, 0, 0, 3, -4]
+    y[1] = [-448, 0, 0, 0, 0, 0, 0, 0.125]
+    wc = np.zeros((V, H), np.uint8)
+    ws = np.ones(V, np.float32)
+    for v in range(V):
+        wc[v, v % H] = 0x38 + (v // H)        # 1.0, 1.125, ... at column v%H
+        ws[v] = 2.0 ** (v % 3)
+    topv, topi, lse, U, yc, ys = oracle.lmhead_topk_e4m3(y, wc, ws, True)
+    assert np.all(ys == 1.0)
+    for v in range(V):
+        c = v % H
+        exact = y[:, c].astype(np.float64) * (1 + (v // H) / 8) * ws[v]
+        assert np.array_equal(U[:, v], exact)
+    order = np.argsort(-U[0].astype(np.float32), kind="stable")[:16]
+    assert np.array_equal(topi[0], order)
