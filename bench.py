@@ -221,10 +221,13 @@ def synth_target_torch(w, x, dev):
 # --------------------------------------------------------------------------
 def lmhead_algorithmic(w):
     """Bytes and flops of one LM-head launch (the step's dominant kernel):
-    read W_lm and y once, write topv/topi/lse."""
-    es = 2 if w.dtype == "bf16" else 4
+    read W_lm and y once (as E4M3 codes plus row scales for the 8-bit
+    head), write topv/topi/lse."""
+    es = 1 if w.lm_e4m3 else (2 if w.dtype == "bf16" else 4)
     M = w.M
     by = w.V * w.H * es + M * w.H * es + M * (C * 8 + 4)
+    if w.lm_e4m3:
+        by += (w.V + M) * 4
     fl = 2.0 * M * w.V * w.H
     return by, fl
 
@@ -239,7 +242,16 @@ def verify_algorithmic(w, n_mean):
 # --------------------------------------------------------------------------
 # CPU oracle timing (bounded sample of the same workload)
 # --------------------------------------------------------------------------
-def time_oracle(w, x, L, seconds: float, seed: int):
+def oracle_w8(w, x):
+    """The oracle's E4M3 codes and scales of W_lm for an 8-bit-head
+    workload (weight preparation, done once, outside the timed sample)."""
+    if not w.lm_e4m3:
+        return None
+    import oracle
+    return oracle.quantize_e4m3_rows(x["w_lm"].float().numpy())
+
+
+def time_oracle(w, x, L, seconds: float, seed: int, w8=None):
     """Whole cycles of the oracle on the first sequences of the workload,
     one sequence at a time, until ``seconds`` of work; returns cycles/s
     scaled to the full batch, and a description of the sample."""
@@ -255,7 +267,7 @@ def time_oracle(w, x, L, seconds: float, seed: int):
         oracle.draft_verify_cycle(h[b:b + 1], W["w_conv"], W["w_lm"],
                                   W["w_gate"], W["e_in"], W["e_out"],
                                   anchor[b:b + 1], Lc[b:b + 1], w.T, seed, 0,
-                                  w.dtype)
+                                  w.dtype, w_lm_e4m3=w8)
         done += 1
         el = time.perf_counter() - t0
         if el >= seconds or done >= w.B:
@@ -290,9 +302,10 @@ def run_reference(args):
     d[:nseq] = U.reshape(nseq, w.K + 1, w.V)
     L = synth.target_logits(w, d)
     per = max(2.0, args.cpu_seconds / max(1, args.steps + args.warmup))
+    w8 = oracle_w8(w, x)
     for _ in range(args.warmup):
-        time_oracle(w, x, L, per, w.seed)
-    vals = [time_oracle(w, x, L, per, w.seed) for _ in range(args.steps)]
+        time_oracle(w, x, L, per, w.seed, w8)
+    vals = [time_oracle(w, x, L, per, w.seed, w8) for _ in range(args.steps)]
     v = statistics.median(r["value"] for r in vals)
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT,
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
@@ -446,7 +459,8 @@ def run_ours(args):
     anchor = x["anchor"].to(dev)
     L = L_cpu.to(dev)
     seed = rank_seed(w.seed, rank)
-    dv = dv_mod.DraftVerify(w.B, w.K, w.H, w.V, w.r, weights, device=dev)
+    dv = dv_mod.DraftVerify(w.B, w.K, w.H, w.V, w.r, weights, device=dev,
+                            lm_e4m3=w.lm_e4m3)
     stream = torch.cuda.current_stream(dev)
 
     # Warm-up, then the timed region: the K cycles are captured into CUDA
@@ -546,7 +560,9 @@ def run_ours(args):
     fused = w.dtype == "bf16" and w.conv_sd is not None
     names = ({"conv": "conv+gate", "lmhead": "lmhead",
               "pair_score": "merge+pair_score+walk", "verify": "verify"}
-             if fused else {n: n for n in stages})
+             if fused else {n: n for n in stages if n != "quant"})
+    if w.lm_e4m3:
+        names["quant"] = "quantize_y"
     stage_us = {}
     for si, name in enumerate(stages):
         if name == "conv" and w.conv_sd is None:
@@ -570,19 +586,26 @@ def run_ours(args):
         if tr.get("workload") == w.name and tr.get("kernel_rev") == \
                 lmhead_kernel_rev():
             traffic = tr.get("bytes_per_launch")
+    tensor_peak, tensor_src = pk["bf16_tflops"], pk["source"]
+    if w.lm_e4m3:   # E4M3 MMA: the measured bf16 rate x the nominal 2x
+        tensor_peak = 2.0 * pk["bf16_tflops"]
+        tensor_src = pk["source"] + " bf16 x 2 (nominal e4m3 / bf16 ratio)"
+        ridge = tensor_peak * 1e12 / (pk["hbm_gbs"] * 1e9)
+        hbm_bound = (fl / by) < ridge
     if hbm_bound:
         achieved = by / t_lm / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"],
                 "unit": "GB/s", "frac": achieved / pk["hbm_gbs"],
                 "traffic": traffic, "peak_source": pk["source"],
                 "kernel": "lmhead",
-                "tensor_frac": fl / t_lm / 1e12 / pk["bf16_tflops"]}
+                "tensor_frac": fl / t_lm / 1e12 / tensor_peak,
+                "tensor_peak_source": tensor_src}
     else:
         achieved = fl / t_lm / 1e12
         roof = {"bound": "tensor", "achieved": achieved,
-                "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": achieved / pk["bf16_tflops"], "traffic": traffic,
-                "peak_source": pk["source"], "kernel": "lmhead",
+                "peak": tensor_peak, "unit": "TFLOP/s",
+                "frac": achieved / tensor_peak, "traffic": traffic,
+                "peak_source": tensor_src, "kernel": "lmhead",
                 "hbm_frac": by / t_lm / 1e9 / pk["hbm_gbs"]}
 
     # the loop: cycles with the commit step, the anchor handed over from
@@ -663,7 +686,8 @@ def run_ours(args):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = time_oracle(w, x, L_cpu, args.cpu_seconds, seed)
+        cpu = time_oracle(w, x, L_cpu, args.cpu_seconds, seed,
+                          oracle_w8(w, x))
 
     if world > 1:
         import torch.distributed as dist
@@ -674,11 +698,14 @@ def run_ours(args):
     n_mean = n_mean_cycles
     launches_per_step = (4 if w.dtype == "bf16" and w.conv_sd is not None
                          else (3 if w.conv_sd is not None else 2) + 3)
+    if w.lm_e4m3:
+        launches_per_step += 1      # the quantization of y
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": 1e3 * secs_max / K,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": w.dtype, "data": "synthetic",
+        "dtype": w.dtype + ("+e4m3 LM head" if w.lm_e4m3 else ""),
+        "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "K": w.K, "V": w.V,
                    "H": w.H, "r": w.r, "T": w.T, "parallelism":
                    f"replicas x{world}",
@@ -779,6 +806,8 @@ def stage_bytes(w, fused):
     else:
         out["pair_score"] = scores + M * H * e + r * H * e
     out["verify"] = w.B * (w.K + 1) * V * 4
+    if w.lm_e4m3:
+        out["quantize_y"] = M * H * e + M * H + M * 4
     return out
 
 

@@ -22,10 +22,11 @@ STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported",
 EXPORTS = ("dflash_workspace_bytes", "dflash_lmhead_topk", "dflash_pair_score",
            "dflash_path_walk", "dflash_draft", "dflash_verify",
            "dflash_verify_noalloc", "dflash_commit", "dflash_path_viterbi",
-           "dflash_top16_recall",
-           "dflash_philox4x32", "dflash_profile_stage", "dflash_check",
+           "dflash_top16_recall", "dflash_quantize_e4m3_rows",
+           "dflash_draft_e4m3", "dflash_philox4x32", "dflash_profile_stage", "dflash_check",
            "dflash_status_string")
-STAGES = ("conv", "lmhead", "merge", "pair_score", "walk", "verify")
+STAGES = ("conv", "lmhead", "merge", "pair_score", "walk", "verify",
+          "quant")
 
 
 class DFlashError(RuntimeError):
@@ -73,6 +74,10 @@ def load(path: str | None = None):
         "dflash_commit": (i32, [vp, vp, i32, i32, vp, vp, vp, i32, vp, vp]),
         "dflash_path_viterbi": (i32, [vp, vp, i32, i32, vp, vp, vp, vp]),
         "dflash_top16_recall": (i32, [vp, vp, i32, i32, i32, vp, vp, vp]),
+        "dflash_quantize_e4m3_rows": (i32, [vp, i32, i32, vp, vp, vp]),
+        "dflash_draft_e4m3": (i32, [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32,
+                                    i32, i32, i32, f32, u64, u64, vp, vp, vp,
+                                    vp, vp, vp, vp, vp, sz, vp]),
         "dflash_profile_stage": (i32, [i32, vp, vp]),
         "dflash_check": (i32, [vp]),
         "dflash_status_string": (ctypes.c_char_p, [i32]),
@@ -188,6 +193,35 @@ def dflash_draft(h, conv_w, w_lm, w_gate, e_in, e_out, anchor, T, seed,
           _ptr(draft), _ptr(q), _ptr(ws), ws.numel(), _stream(stream))
 
 
+def dflash_quantize_e4m3_rows(x, codes, scale, stream=None):
+    """x [R,H] bf16 -> codes [R,H] uint8 (E4M3) and scale [R] f32."""
+    R, H = x.shape
+    _want(x, torch.bfloat16, "x")
+    _want(codes, torch.uint8, "codes")
+    _want(scale, torch.float32, "scale")
+    _call("dflash_quantize_e4m3_rows", _ptr(x), R, H, _ptr(codes),
+          _ptr(scale), _stream(stream))
+
+
+def dflash_draft_e4m3(h, conv_w, w_codes, w_scale, w_gate, e_in, e_out,
+                      anchor, T, seed, cycle, topv, topi, lse, scores, slot,
+                      draft, q, ws, stream=None):
+    """dflash_draft (bf16, with a conv) with the LM head on E4M3 codes:
+    w_codes [V,H] uint8 and w_scale [V] f32 from dflash_quantize_e4m3_rows;
+    ws uint8 (workspace kind 3)."""
+    B, K, H = h.shape
+    V = w_codes.shape[0]
+    r = w_gate.shape[0]
+    _want(h, torch.bfloat16, "h")
+    _want(w_codes, torch.uint8, "w_codes")
+    _call("dflash_draft_e4m3", _ptr(h), _ptr(conv_w), _ptr(w_codes),
+          _ptr(w_scale), _ptr(w_gate), _ptr(e_in), _ptr(e_out), _ptr(anchor),
+          B, K, H, V, r, float(T), int(seed) & (2**64 - 1),
+          int(cycle) & (2**64 - 1), _ptr(topv), _ptr(topi), _ptr(lse),
+          _ptr(scores), _ptr(slot), _ptr(draft), _ptr(q), _ptr(ws),
+          ws.numel(), _stream(stream))
+
+
 def dflash_verify(target_logits, draft, topi, q, T, seed, cycle, n_accepted,
                   out_tok, ws, stream=None):
     """target_logits [B,K+1,V] f32; draft [B,K]; topi/q [B,K,16];
@@ -290,11 +324,14 @@ class DraftVerify:
     tensors of one storage dtype.  ``cycle(h, anchor, L, T, seed, c)`` runs
     conv + LM head + top-16, pair scores, walk and verify on the current
     stream and returns the (device) n_accepted and out_tok tensors.
+    With ``lm_e4m3`` (bf16 with a conv) W_lm is quantized once to E4M3
+    codes and row scales, and draft_all runs dflash_draft_e4m3.
     """
 
-    def __init__(self, B, K, H, V, r, weights, device="cuda"):
+    def __init__(self, B, K, H, V, r, weights, device="cuda", lm_e4m3=False):
         self.B, self.K, self.H, self.V, self.r = B, K, H, V, r
         self.w = weights
+        self.lm_e4m3 = bool(lm_e4m3)
         dev = torch.device(device)
         M = B * K
         f32, i32 = torch.float32, torch.int32
@@ -311,8 +348,14 @@ class DraftVerify:
                                  dtype=torch.uint8, device=dev)
         self.ws_v = torch.empty(dflash_workspace_bytes(1, B, K, H, V),
                                 dtype=torch.uint8, device=dev)
-        self.ws_d = torch.empty(dflash_workspace_bytes(2, B, K, H, V),
-                                dtype=torch.uint8, device=dev)
+        self.ws_d = torch.empty(
+            dflash_workspace_bytes(3 if self.lm_e4m3 else 2, B, K, H, V),
+            dtype=torch.uint8, device=dev)
+        if self.lm_e4m3:
+            self.w_codes = torch.empty(V, H, dtype=torch.uint8, device=dev)
+            self.w_scale = torch.empty(V, dtype=f32, device=dev)
+            dflash_quantize_e4m3_rows(weights["w_lm"], self.w_codes,
+                                      self.w_scale)
 
     def lmhead(self, h, stream=None):
         dflash_lmhead_topk(h, self.w["w_conv"], self.w["w_lm"], self.topv,
@@ -335,7 +378,13 @@ class DraftVerify:
 
     def draft_all(self, h, anchor, T, seed, cycle, stream=None):
         """Steps a1-a4 in one dflash_draft call (gate inside the conv)."""
-        B, K = self.B, self.K
+        if self.lm_e4m3:
+            dflash_draft_e4m3(h, self.w["w_conv"], self.w_codes, self.w_scale,
+                              self.w["w_gate"], self.w["e_in"],
+                              self.w["e_out"], anchor, T, seed, cycle,
+                              self.topv, self.topi, self.lse, self.scores,
+                              self.slot, self.draft, self.q, self.ws_d, stream)
+            return
         dflash_draft(h, self.w["w_conv"], self.w["w_lm"], self.w["w_gate"],
                      self.w["e_in"], self.w["e_out"], anchor, T, seed, cycle,
                      self.topv, self.topi, self.lse, self.scores, self.slot,
@@ -360,3 +409,15 @@ class DraftVerify:
         ws = self.ws_d if fused else self.ws_lm
         return ws[: n * (2 if dt == torch.bfloat16 else 4)].view(
             dt).view(self.B, self.K, self.H)
+
+    def y_e4m3(self):
+        """y's E4M3 codes [B*K, H] and row scales [B*K] written by the last
+        draft_all with lm_e4m3: the workspace of kind 3 holds them after
+        the first dflash_workspace_bytes(2, ...) bytes, the scales from the
+        next 256-byte boundary after the codes."""
+        M, H = self.B * self.K, self.H
+        off = dflash_workspace_bytes(2, self.B, self.K, H, self.V)
+        off2 = off + (M * H + 255) // 256 * 256
+        codes = self.ws_d[off: off + M * H].view(M, H)
+        scale = self.ws_d[off2: off2 + 4 * M].view(torch.float32)
+        return codes, scale

@@ -45,7 +45,7 @@ dflash_status device_state(DeviceState** out) {
 
 // Caller-supplied timing events per stage (dflash_profile_stage).
 enum Stage { kStConv = 0, kStLmhead, kStMerge, kStPair, kStWalk, kStVerifyRows,
-             kNumStages };
+             kStQuant, kNumStages };
 cudaEvent_t g_prof[kNumStages][2] = {};
 
 struct StageTimer {
@@ -119,9 +119,31 @@ size_t draft_ws_layout(int B, int K, int H, int V, void* base, float** gate,
   return align256(lm + g + (size_t)B * sizeof(unsigned));
 }
 
+// Workspace of dflash_draft_e4m3: dflash_draft's, then the E4M3 codes of y
+// [B*K, H] and their row scales [B*K] fp32.
+size_t draft_e4m3_ws_layout(int B, int K, int H, int V, void* base,
+                            uint8_t** y_codes, float** y_scale) {
+  const size_t d = align256(draft_ws_layout(B, K, H, V, nullptr, nullptr));
+  const size_t c = align256((size_t)B * K * H);
+  char* p = static_cast<char*>(base);
+  if (y_codes) *y_codes = reinterpret_cast<uint8_t*>(p + d);
+  if (y_scale) *y_scale = reinterpret_cast<float*>(p + d + c);
+  return align256(d + c + (size_t)B * K * sizeof(float));
+}
+
+// 8-bit LM-head operands for lmhead_bf16: W_lm as E4M3 codes and row
+// scales, and where to put y's codes and scales.
+struct E4m3Head {
+  const uint8_t* w_codes;
+  const float* w_scale;
+  uint8_t* y_codes;
+  float* y_scale;
+};
+
 // bf16 storage: conv and LM head on the tensor cores (tcgen05 + TMA).  With
 // w_gate (and conv_w) the conv launch also writes the pair selector's gate
-// [B*K, r] fp32 to `gate`.
+// [B*K, r] fp32 to `gate`.  With q8 (and conv_w) y is quantized per row to
+// E4M3 and the LM head runs on the 8-bit operands (w_lm unused).
 dflash_status lmhead_bf16(const __nv_bfloat16* h, const __nv_bfloat16* conv_w,
                           const __nv_bfloat16* w_lm, int B, int K, int H,
                           int V, float* topv, int* topi, float* lse, void* ws,
@@ -129,7 +151,8 @@ dflash_status lmhead_bf16(const __nv_bfloat16* h, const __nv_bfloat16* conv_w,
                           const __nv_bfloat16* w_gate = nullptr, int r = 0,
                           float* gate = nullptr, unsigned* tickets = nullptr,
                           TopkPartials* P_out = nullptr,
-                          int* strips_out = nullptr) {
+                          int* strips_out = nullptr,
+                          const E4m3Head* q8 = nullptr) {
   void* yv = nullptr;
   TopkPartials P;
   lmhead_ws_layout(B, K, H, V, ws, &yv, &P);
@@ -154,13 +177,27 @@ dflash_status lmhead_bf16(const __nv_bfloat16* h, const __nv_bfloat16* conv_w,
     a = y;
   }
   CUtensorMap my, mw;
-  if (!make_tmap_bf16_2d(&my, a, H, M, 64, 128) ||
-      !make_tmap_bf16_2d(&mw, w_lm, H, V, 64, lmhead_tc_pairs(M) ? 128 : 256))
+  const uint32_t w_box = lmhead_tc_pairs(M) ? 128 : 256;
+  if (q8 && conv_w) {
+    {
+      StageTimer tm(kStQuant, s);
+      e = launch_quantize_e4m3_rows(a, M, H, q8->y_codes, q8->y_scale, d.err,
+                                    s);
+    }
+    if (e != cudaSuccess) return DFLASH_ERR_CUDA;
+    if (!make_tmap_u8_2d(&my, q8->y_codes, H, M, 128, 128) ||
+        !make_tmap_u8_2d(&mw, q8->w_codes, H, V, 128, w_box))
+      return DFLASH_ERR_CUDA;
+  } else if (!make_tmap_bf16_2d(&my, a, H, M, 64, 128) ||
+             !make_tmap_bf16_2d(&mw, w_lm, H, V, 64, w_box)) {
     return DFLASH_ERR_CUDA;
+  }
   int strips = 0;
   {
     StageTimer tm(kStLmhead, s);
-    e = launch_lmhead_tc(my, mw, M, H, V, d.sms, P, d.err, &strips, s);
+    e = launch_lmhead_tc(my, mw, M, H, V, d.sms, P, d.err, &strips, s,
+                         q8 && conv_w ? q8->y_scale : nullptr,
+                         q8 && conv_w ? q8->w_scale : nullptr);
   }
   if (e != cudaSuccess) return DFLASH_ERR_CUDA;
   if (P_out) {  // the caller merges (draft tail)
@@ -231,7 +268,26 @@ size_t dflash_workspace_bytes(int which, int B, int K, int H, int V) {
     if (H < 8) return 0;
     return draft_ws_layout(B, K, H, V, nullptr, nullptr);
   }
+  if (which == 3) {
+    if (H < 16) return 0;
+    return draft_e4m3_ws_layout(B, K, H, V, nullptr, nullptr, nullptr);
+  }
   return 0;
+}
+
+dflash_status dflash_quantize_e4m3_rows(const void* x, int R, int H,
+                                        uint8_t* codes, float* scale,
+                                        dflash_stream_t stream) {
+  REQUIRE(x && codes && scale);
+  REQUIRE(R >= 1 && H >= 16 && H % 16 == 0 &&
+          (long long)R * H <= (1LL << 40));
+  REQUIRE(aligned(x, 16) && aligned(codes, 16) && aligned(scale, 4));
+  DeviceState* d = nullptr;
+  dflash_status st = device_state(&d);
+  if (st != DFLASH_OK) return st;
+  return cuda_status(launch_quantize_e4m3_rows(
+      static_cast<const __nv_bfloat16*>(x), R, H, codes, scale, d->err,
+      reinterpret_cast<cudaStream_t>(stream)));
 }
 
 dflash_status dflash_lmhead_topk(const void* h, const void* conv_w,
@@ -368,6 +424,49 @@ dflash_status dflash_draft(const void* h, const void* conv_w, const void* w_lm,
   if (e != cudaSuccess) return DFLASH_ERR_CUDA;
   return dflash_path_walk(scores, topi, B, K, T, seed, cycle, slot, draft, q,
                           stream);
+}
+
+dflash_status dflash_draft_e4m3(
+    const void* h, const void* conv_w, const uint8_t* w_lm_codes,
+    const float* w_lm_scale, const void* w_gate, const void* e_in,
+    const void* e_out, const int32_t* anchor, int B, int K, int H, int V,
+    int r, float T, uint64_t seed, uint64_t cycle, float* topv,
+    int32_t* topi, float* lse, float* scores, int32_t* slot, int32_t* draft,
+    float* q, void* ws, size_t ws_bytes, dflash_stream_t stream) {
+  REQUIRE(h && conv_w && w_lm_codes && w_lm_scale && w_gate && e_in &&
+          e_out && anchor && topv && topi && lse && scores && slot && draft &&
+          q && ws);
+  REQUIRE(sizes_ok(B, K, H, V) && H >= 16 && H % 16 == 0 && r >= 1 &&
+          r <= DFLASH_MAX_RANK);
+  REQUIRE(T >= 0.f && T < INFINITY);
+  REQUIRE(aligned(ws, 256) && aligned(h, 16) && aligned(conv_w, 16) &&
+          aligned(w_lm_codes, 16) && aligned(w_lm_scale, 4) &&
+          aligned(w_gate, 16) && aligned(e_in, 16) && aligned(e_out, 16) &&
+          aligned(scores, 16));
+  REQUIRE(ws_bytes >=
+          draft_e4m3_ws_layout(B, K, H, V, nullptr, nullptr, nullptr));
+  DeviceState* d = nullptr;
+  dflash_status st = device_state(&d);
+  if (st != DFLASH_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  float* gate = nullptr;
+  unsigned* tickets = nullptr;
+  draft_ws_layout(B, K, H, V, ws, &gate, &tickets);
+  E4m3Head q8{w_lm_codes, w_lm_scale, nullptr, nullptr};
+  draft_e4m3_ws_layout(B, K, H, V, ws, &q8.y_codes, &q8.y_scale);
+  using bf = __nv_bfloat16;
+  TopkPartials P;
+  int strips = 0;
+  st = lmhead_bf16(static_cast<const bf*>(h), static_cast<const bf*>(conv_w),
+                   nullptr, B, K, H, V, topv, topi, lse, ws, *d, s,
+                   static_cast<const bf*>(w_gate), r, gate, tickets, &P,
+                   &strips, &q8);
+  if (st != DFLASH_OK) return st;
+  StageTimer tm(kStPair, s);
+  return cuda_status(launch_draft_tail<bf>(
+      P, strips, anchor, gate, static_cast<const bf*>(e_in),
+      static_cast<const bf*>(e_out), B, K, V, r, T, seed, cycle, topv, topi,
+      lse, scores, slot, draft, q, tickets, d->err, s));
 }
 
 dflash_status dflash_verify(const float* target_logits, const int32_t* draft,

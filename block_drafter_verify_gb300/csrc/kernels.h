@@ -30,14 +30,31 @@ cudaError_t launch_conv_tc(const CUtensorMap& map_h, const CUtensorMap& map_wc,
                            int B, int K, int H, int r, __nv_bfloat16* y,
                            float* gate, unsigned* tickets, int* err,
                            cudaStream_t s);
+// TMA descriptor of a row-major 8-bit [rows, inner] matrix, 128-byte
+// swizzle (inner a multiple of 16).
+bool make_tmap_u8_2d(CUtensorMap* map, const void* base, uint64_t inner,
+                     uint64_t rows, uint32_t box_inner, uint32_t box_rows);
 // map_y: y [M, H] box {64, 128}; map_w: w_lm [V, H] box {64, 256}, or
 // {64, 128} when lmhead_tc_pairs(M) (CTA pairs, two or more row tiles).
-// Writes `*strips` partial lists per row.
+// Writes `*strips` partial lists per row.  With y_scale and w_scale the
+// operands are E4M3 codes (maps from make_tmap_u8_2d, boxes of 128 codes
+// along H) and logit (m, v) = y_scale[m] * w_scale[v] * (codes' dot).
 cudaError_t launch_lmhead_tc(const CUtensorMap& map_y, const CUtensorMap& map_w,
                              int M, int H, int V, int num_sms, TopkPartials P,
-                             int* err, int* strips, cudaStream_t s);
+                             int* err, int* strips, cudaStream_t s,
+                             const float* y_scale = nullptr,
+                             const float* w_scale = nullptr);
+
+// quant_e4m3.cu: per-row E4M3 quantization of a bf16 [R, H] matrix
+// (H % 8 == 0): scale[i] = max_k |x_ik| / 448 (1 for a zero row), code =
+// e4m3(x / scale), round to nearest even, saturated.  Non-finite input
+// sets kErrNonfinite.  Launched with programmatic dependent launch.
+cudaError_t launch_quantize_e4m3_rows(const __nv_bfloat16* x, int R, int H,
+                                      uint8_t* codes, float* scale, int* err,
+                                      cudaStream_t s);
 bool lmhead_tc_pairs(int M);
-int lmhead_tc_grid(int M, int V, int num_sms, int* row_groups, int* strips);
+int lmhead_tc_grid(int M, int V, int num_sms, int* row_groups, int* strips,
+                   bool fp8 = false);
 
 // lmhead_simt.cu ----------------------------------------------------------
 template <typename T>

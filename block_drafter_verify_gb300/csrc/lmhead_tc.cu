@@ -1,6 +1,10 @@
 // Step a2 on the 5th-generation tensor cores: drafter LM head
 // U = y W_lm^T (bf16 x bf16 -> fp32) with an epilogue that keeps, per row,
 // an online logsumexp and the 16 largest logits, so U never reaches HBM.
+// The same kernel also runs with 8-bit operands: E4M3 codes of y and W_lm
+// with one fp32 scale per row each (kind::f8f6f4; a stage then holds 128
+// codes of every row instead of 64 bf16, the same bytes), and the epilogue
+// multiplies each logit by y_scale[m] * w_scale[v] before folding it.
 //
 // "Sixteen candidates per position" (DFlash 2: Block diffusion, wearing a
 // drafter's coat) and "A Lightweight Path Selector" (DFlash 2: Keep Drafting
@@ -40,8 +44,9 @@
 namespace dflash {
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 64;
-constexpr int A_BYTES = BM * BK * 2;  // 16 KB
+constexpr int BM = 128, BN = 256;
+constexpr int ROW_BYTES = 128;  // bytes of each operand row per stage
+constexpr int A_BYTES = BM * ROW_BYTES;  // 16 KB
 constexpr int THREADS = 192;
 constexpr uint32_t TMEM_COLS = 2 * BN;
 constexpr uint64_t WAIT_NS = 2000000000ull;  // 2 s: far beyond any real wait
@@ -51,9 +56,16 @@ template <bool kPair>
 struct Cfg {
   static constexpr int STAGES = kPair ? 6 : 4;
   static constexpr int B_ROWS = kPair ? BN / 2 : BN;  // W rows per CTA
-  static constexpr int B_BYTES = B_ROWS * BK * 2;
+  static constexpr int B_BYTES = B_ROWS * ROW_BYTES;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int CTAS = kPair ? 2 : 1;
+};
+// Elements of K per stage and per MMA: 64 and 16 for bf16, 128 and 32 for
+// E4M3; either way each MMA step advances 32 bytes along the row.
+template <bool kFp8>
+struct Elem {
+  static constexpr int BK = kFp8 ? 128 : 64;
+  static constexpr int MMA_K = kFp8 ? 32 : 16;
 };
 
 template <int STAGES>
@@ -68,10 +80,14 @@ struct Bars {
 };
 constexpr int XS_STRIDE = 33;  // padded row of the per-thread chunk stage
 constexpr size_t XS_BYTES = 4 * 32 * XS_STRIDE * sizeof(float);
-template <bool kPair>
+// 8-bit operands: each epilogue warp's copy of the current tile's BN
+// column scales.
+constexpr size_t WS_BYTES = 4 * BN * sizeof(float);
+template <bool kPair, bool kFp8>
 constexpr size_t smem_bytes() {
   return 1024 + (size_t)Cfg<kPair>::STAGES * Cfg<kPair>::STAGE_BYTES +
-         ((sizeof(Bars<Cfg<kPair>::STAGES>) + 15) & ~size_t(15)) + XS_BYTES;
+         ((sizeof(Bars<Cfg<kPair>::STAGES>) + 15) & ~size_t(15)) + XS_BYTES +
+         (kFp8 ? WS_BYTES : 0);
 }
 
 __device__ __forceinline__ bool wait_timeout(uint64_t* bar, uint32_t parity) {
@@ -132,14 +148,16 @@ __device__ __forceinline__ unsigned epilogue_chunk(float (&x)[32], int col0,
   return mask;
 }
 
-template <bool kPair>
+template <bool kPair, bool kFp8>
 __global__ void __launch_bounds__(THREADS, 1)
     lmhead_tc_kernel(const __grid_constant__ CUtensorMap map_y,
                      const __grid_constant__ CUtensorMap map_w, int M, int H,
                      int V, int row_groups, int strips, TopkPartials P,
-                     int* err) {
+                     const float* __restrict__ y_scale,
+                     const float* __restrict__ w_scale, int* err) {
   using C = Cfg<kPair>;
   constexpr int STAGES = C::STAGES;
+  constexpr int BK = Elem<kFp8>::BK;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -150,6 +168,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   float* xs_all = reinterpret_cast<float*>(
       smem + STAGES * C::STAGE_BYTES +
       ((sizeof(Bars<STAGES>) + 15) & ~size_t(15)));
+  float* ws_all = xs_all + XS_BYTES / sizeof(float);  // 8-bit operands only
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // a pair is a cluster of two consecutive blocks; rank 0 leads
   const int rank = kPair ? (int)(blockIdx.x & 1) : 0;
@@ -259,7 +278,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA
     if (lane == 0 && leader) {
-      constexpr uint32_t idesc = tc::idesc_bf16_f32(BM * C::CTAS, BN);
+      constexpr uint32_t idesc =
+          kFp8 ? tc::idesc_e4m3_f32(BM * C::CTAS, BN)
+               : tc::idesc_bf16_f32(BM * C::CTAS, BN);
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
@@ -282,11 +303,15 @@ __global__ void __launch_bounds__(THREADS, 1)
           const uint32_t a0 = tc::smem_u32(sa + stage * A_BYTES);
           const uint32_t b0 = tc::smem_u32(sb + stage * C::B_BYTES);
 #pragma unroll
-          for (int k = 0; k < BK / 16; ++k) {
+          for (int k = 0; k < BK / Elem<kFp8>::MMA_K; ++k) {
             const uint64_t ad = tc::sdesc_k_sw128(a0 + k * 32);
             const uint64_t bd = tc::sdesc_k_sw128(b0 + k * 32);
-            if constexpr (kPair)
+            if constexpr (kPair && kFp8)
+              tc::mma_e4m3_pair(d, ad, bd, idesc, (kb | k) != 0);
+            else if constexpr (kPair)
               tc::mma_bf16_pair(d, ad, bd, idesc, (kb | k) != 0);
+            else if constexpr (kFp8)
+              tc::mma_e4m3(d, ad, bd, idesc, (kb | k) != 0);
             else
               tc::mma_bf16(d, ad, bd, idesc, (kb | k) != 0);
           }
@@ -315,6 +340,12 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int m = mtile * BM + q * 32 + lane;
     float* xs = xs_all + ((warp - 2) * 32 + lane) * XS_STRIDE;
+    float* wsc = ws_all + (warp - 2) * BN;  // this warp's column scales
+    // y's row scales come from the previous launch: wait for it here too
+    // (only the producer waits in the bf16 form, whose epilogue reads
+    // nothing but TMEM)
+    if constexpr (kFp8) pdl_wait();
+    const float srow = kFp8 && m < M ? y_scale[m] : 1.f;
     // accumulator-free barriers of the MMA-issuing CTA
     const uint32_t tempty0 =
         kPair ? tc::mapa_shared(tc::smem_u32(&bars->tempty[0]), 0)
@@ -329,12 +360,26 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int vt = strip + it * strips;
       const int b = it & 1;
       const uint32_t aph = (it >> 1) & 1;
+      float wreg[BN / 32];
+      if constexpr (kFp8) {  // loads in flight during the wait
+#pragma unroll
+        for (int j = 0; j < BN / 32; ++j) {
+          const int v = vt * BN + j * 32 + lane;
+          wreg[j] = v < V ? __ldg(w_scale + v) : 0.f;
+        }
+      }
       const bool got = tc::mbar_wait_bounded(&bars->tfull[b], aph, abort,
                                              WAIT_NS);
       if (!__all_sync(0xffffffffu, got)) {
         *abort = 1;
         ok = false;
         break;
+      }
+      if constexpr (kFp8) {
+        __syncwarp();  // the previous tile's reads of wsc are done
+#pragma unroll
+        for (int j = 0; j < BN / 32; ++j) wsc[j * 32 + lane] = wreg[j];
+        __syncwarp();
       }
       tc::fence_after_sync();
       const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16) +
@@ -345,6 +390,17 @@ __global__ void __launch_bounds__(THREADS, 1)
         float x[32];
         tc::tmem_ld_x32(tbase + c * 32, x);
         const int col0 = vt * BN + c * 32;
+        if constexpr (kFp8) {
+          const float4* w4 = reinterpret_cast<const float4*>(wsc + c * 32);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float4 f = w4[i];
+            x[4 * i] *= srow * f.x;
+            x[4 * i + 1] *= srow * f.y;
+            x[4 * i + 2] *= srow * f.z;
+            x[4 * i + 3] *= srow * f.w;
+          }
+        }
         unsigned mask =
             epilogue_chunk(x, col0, V, tv[kC - 1], run_m, run_s, xs);
         // insert the chunk's candidates, every lane its own row in step
@@ -403,6 +459,7 @@ bool lmhead_tc_pairs(int M) { return (M + BM - 1) / BM >= 2; }
 
 namespace {
 // Pairs the device can hold at once (a pair needs two SMs of one TPC).
+template <bool kFp8>
 int max_resident_pairs(int num_sms) {
   static int cached[64] = {};
   int dev = 0;
@@ -412,7 +469,7 @@ int max_resident_pairs(int num_sms) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(num_sms);
   cfg.blockDim = dim3(THREADS);
-  cfg.dynamicSmemBytes = smem_bytes<true>();
+  cfg.dynamicSmemBytes = smem_bytes<true, kFp8>();
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
@@ -421,11 +478,11 @@ int max_resident_pairs(int num_sms) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaFuncSetAttribute(lmhead_tc_kernel<true>,
+  if (cudaFuncSetAttribute(lmhead_tc_kernel<true, kFp8>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)smem_bytes<true>()) != cudaSuccess ||
-      cudaOccupancyMaxActiveClusters(&n, lmhead_tc_kernel<true>, &cfg) !=
-          cudaSuccess ||
+                           (int)smem_bytes<true, kFp8>()) != cudaSuccess ||
+      cudaOccupancyMaxActiveClusters(&n, lmhead_tc_kernel<true, kFp8>,
+                                     &cfg) != cudaSuccess ||
       n < 1) {
     (void)cudaGetLastError();
     n = num_sms / 2;
@@ -435,13 +492,16 @@ int max_resident_pairs(int num_sms) {
 }
 }  // namespace
 
-int lmhead_tc_grid(int M, int V, int num_sms, int* row_groups, int* strips) {
+int lmhead_tc_grid(int M, int V, int num_sms, int* row_groups, int* strips,
+                   bool fp8) {
   const bool pairs = lmhead_tc_pairs(M);
   const int ctas = pairs ? 2 : 1;
   const int rt = (M + BM - 1) / BM;
   const int rg = (rt + ctas - 1) / ctas;  // units per vocab strip
   const int vt = (V + BN - 1) / BN;
-  const int units = pairs ? max_resident_pairs(num_sms) : num_sms;
+  const int units = !pairs ? num_sms
+                    : fp8  ? max_resident_pairs<true>(num_sms)
+                           : max_resident_pairs<false>(num_sms);
   int st = std::max(1, units / rg);
   st = std::min(std::min(st, vt), kMaxStrips);
   *row_groups = rg;
@@ -449,28 +509,46 @@ int lmhead_tc_grid(int M, int V, int num_sms, int* row_groups, int* strips) {
   return rg * st * ctas;
 }
 
-cudaError_t launch_lmhead_tc(const CUtensorMap& map_y, const CUtensorMap& map_w,
-                             int M, int H, int V, int num_sms, TopkPartials P,
-                             int* err, int* strips_out, cudaStream_t s) {
+namespace {
+template <bool kFp8>
+cudaError_t launch_variant(const CUtensorMap& map_y, const CUtensorMap& map_w,
+                           int M, int H, int V, int num_sms, TopkPartials P,
+                           int* err, int* strips_out, cudaStream_t s,
+                           const float* y_scale, const float* w_scale) {
   int rg = 0, st = 0;
-  const int grid = lmhead_tc_grid(M, V, num_sms, &rg, &st);
+  const int grid = lmhead_tc_grid(M, V, num_sms, &rg, &st, kFp8);
   *strips_out = st;
   if (!lmhead_tc_pairs(M)) {
     cudaError_t e = cudaFuncSetAttribute(
-        lmhead_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-        (int)smem_bytes<false>());
+        lmhead_tc_kernel<false, kFp8>,
+        cudaFuncAttributeMaxDynamicSharedMemorySize,
+        (int)smem_bytes<false, kFp8>());
     if (e != cudaSuccess) return e;
-    PdlLaunch L(dim3(grid), dim3(THREADS), smem_bytes<false>(), s);
-    return cudaLaunchKernelEx(&L.cfg, lmhead_tc_kernel<false>, map_y, map_w,
-                              M, H, V, rg, st, P, err);
+    PdlLaunch L(dim3(grid), dim3(THREADS), smem_bytes<false, kFp8>(), s);
+    return cudaLaunchKernelEx(&L.cfg, lmhead_tc_kernel<false, kFp8>, map_y,
+                              map_w, M, H, V, rg, st, P, y_scale, w_scale,
+                              err);
   }
   cudaError_t e = cudaFuncSetAttribute(
-      lmhead_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-      (int)smem_bytes<true>());
+      lmhead_tc_kernel<true, kFp8>,
+      cudaFuncAttributeMaxDynamicSharedMemorySize,
+      (int)smem_bytes<true, kFp8>());
   if (e != cudaSuccess) return e;
-  PdlLaunch L(dim3(grid), dim3(THREADS), smem_bytes<true>(), s, 2);
-  return cudaLaunchKernelEx(&L.cfg, lmhead_tc_kernel<true>, map_y, map_w, M,
-                            H, V, rg, st, P, err);
+  PdlLaunch L(dim3(grid), dim3(THREADS), smem_bytes<true, kFp8>(), s, 2);
+  return cudaLaunchKernelEx(&L.cfg, lmhead_tc_kernel<true, kFp8>, map_y,
+                            map_w, M, H, V, rg, st, P, y_scale, w_scale, err);
+}
+}  // namespace
+
+cudaError_t launch_lmhead_tc(const CUtensorMap& map_y, const CUtensorMap& map_w,
+                             int M, int H, int V, int num_sms, TopkPartials P,
+                             int* err, int* strips_out, cudaStream_t s,
+                             const float* y_scale, const float* w_scale) {
+  if (y_scale && w_scale)
+    return launch_variant<true>(map_y, map_w, M, H, V, num_sms, P, err,
+                                strips_out, s, y_scale, w_scale);
+  return launch_variant<false>(map_y, map_w, M, H, V, num_sms, P, err,
+                               strips_out, s, nullptr, nullptr);
 }
 
 }  // namespace dflash

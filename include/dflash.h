@@ -84,8 +84,9 @@ typedef enum { DFLASH_BF16 = 0, DFLASH_FP32 = 1 } dflash_dtype;
 #define DFLASH_MAX_RANK 256
 
 /* Workspace needed by dflash_lmhead_topk (which = 0), dflash_verify
- * (which = 1) or dflash_draft (which = 2) for these sizes, in bytes; an
- * upper bound over both dtypes and every r.  Returns 0 for invalid sizes. */
+ * (which = 1), dflash_draft (which = 2) or dflash_draft_e4m3 (which = 3)
+ * for these sizes, in bytes; an upper bound over both dtypes and every r.
+ * Returns 0 for invalid sizes. */
 size_t dflash_workspace_bytes(int which, int B, int K, int H, int V);
 
 /*
@@ -169,30 +170,6 @@ dflash_status dflash_path_walk(const float* scores, const int32_t* topi,
                                float* q, dflash_stream_t s);
 
 /*
- * Steps a5 + a6: rejection-sampling verify with residual or bonus draw.
- *
- * "Lossless, with conditions I did not used to state" (drafter's coat
- * page): accept a draft token x with probability min(1, p(x)/q(x)), and on
- * the first rejection resample from normalize(max(0, p - q)); the emitted
- * tokens then follow the target distribution exactly.  p_t =
- * softmax(L[b,t] / T).  For t = 0..K-1 in order, draft t is accepted iff
- * u_t * q_t(x) < p_t(x) (u_t = accept uniform (b, t)); n = the number
- * accepted before the first rejection.  If n < K the token at n is drawn
- * from max(0, p_n - q_n) (q_n zero off the candidates; p_n if that is all
- * zero); if n = K a bonus token is drawn from p_K.  A draw takes the
- * smallest token v whose running weight sum exceeds u * total (u =
- * residual uniform (b, K)).  T == 0: accept iff the draft equals
- * argmax L[b,t] (lowest id on ties) and emit argmax L[b,n].
- *
- *   target_logits [B, K+1, V] fp32   target model logits, rows 0..K
- *   draft [B, K], topi [B, K, 16], q [B, K, 16]   from the walk
- *   n_accepted [B] int32 out
- *   out_tok [B, K+1] int32 out   draft[0..n-1], the drawn token, then -1
- *   ws >= dflash_workspace_bytes(1, B, K, 0, V) bytes, 256-B aligned
- * Requirements: target_logits 16-byte aligned; T >= 0.  A NaN or +inf
- * target logit sets DFLASH_ERR_NONFINITE in the device error word.
- */
-/*
  * Steps a1-a4 in one call: dflash_lmhead_topk, dflash_pair_score and
  * dflash_path_walk with the same arguments and outputs as those three
  * calls, in that order ("Suffix-decay convolution" and "Sixteen candidates
@@ -226,6 +203,74 @@ dflash_status dflash_draft(const void* h, const void* conv_w, const void* w_lm,
                            int32_t* slot, int32_t* draft, float* q, void* ws,
                            size_t ws_bytes, dflash_stream_t s);
 
+/*
+ * 8-bit LM head (quantized drafters: "What a block-diffusion drafter is"
+ * of the 2B-drafter page and "What Comes Next" of "DFlash 2: Keep Drafting
+ * Parallel" ship GGUF-quantized drafter builds; this library's 8-bit form
+ * is OCP FP8 E4M3 with one fp32 scale per row, the operand type of the
+ * tensor cores' kind::f8f6f4 MMA).
+ *
+ * dflash_quantize_e4m3_rows: x [R, H] bf16 -> codes [R, H] uint8 (E4M3:
+ * bias 7, 3 mantissa bits, no infinities, 448 largest) and scale [R] fp32:
+ *     scale_i = max_k |x_ik| / 448 (1 for an all-zero row),
+ *     codes_ik = E4M3(x_ik / scale_i), nearest with ties to even, saturated,
+ * both divisions correctly rounded fp32.  Used once on W_lm when it is
+ * loaded; dflash_draft_e4m3 applies it to y every call.
+ * Requirements: H % 16 == 0; x and codes 16-byte aligned.  A non-finite
+ * input sets DFLASH_ERR_NONFINITE in the device error word.
+ */
+dflash_status dflash_quantize_e4m3_rows(const void* x, int R, int H,
+                                        uint8_t* codes, float* scale,
+                                        dflash_stream_t s);
+
+/*
+ * dflash_draft for bf16 storage with a conv, with the LM head on 8-bit
+ * operands: the conv output y is quantized per row
+ * (dflash_quantize_e4m3_rows) and U_t(v) = s_y[t] s_W[v] sum_k
+ * code_y[t,k] code_W[v,k] (fp32 accumulation; the codes' products are
+ * exact).  W_lm is given as codes [V, H] uint8 and row scales [V] fp32.
+ * Everything else (gate, candidates, lse, scores, walk, outputs) is as in
+ * dflash_draft with dt = DFLASH_BF16.
+ *   ws >= dflash_workspace_bytes(3, B, K, H, V) bytes, 256-byte aligned;
+ *        holds dflash_draft's workspace (its first
+ *        dflash_workspace_bytes(2, B, K, H, V) bytes, with y in bf16 at
+ *        offset 0), then y's codes [B*K, H] uint8, then from the next
+ *        256-byte boundary y's scales [B*K] fp32.
+ * Requirements: conv_w not NULL; H % 16 == 0; w_lm_codes 16-byte aligned;
+ * the rest as dflash_draft.
+ */
+dflash_status dflash_draft_e4m3(
+    const void* h, const void* conv_w, const uint8_t* w_lm_codes,
+    const float* w_lm_scale, const void* w_gate, const void* e_in,
+    const void* e_out, const int32_t* anchor, int B, int K, int H, int V,
+    int r, float T, uint64_t seed, uint64_t cycle, float* topv,
+    int32_t* topi, float* lse, float* scores, int32_t* slot, int32_t* draft,
+    float* q, void* ws, size_t ws_bytes, dflash_stream_t s);
+
+/*
+ * Steps a5 + a6: rejection-sampling verify with residual or bonus draw.
+ *
+ * "Lossless, with conditions I did not used to state" (drafter's coat
+ * page): accept a draft token x with probability min(1, p(x)/q(x)), and on
+ * the first rejection resample from normalize(max(0, p - q)); the emitted
+ * tokens then follow the target distribution exactly.  p_t =
+ * softmax(L[b,t] / T).  For t = 0..K-1 in order, draft t is accepted iff
+ * u_t * q_t(x) < p_t(x) (u_t = accept uniform (b, t)); n = the number
+ * accepted before the first rejection.  If n < K the token at n is drawn
+ * from max(0, p_n - q_n) (q_n zero off the candidates; p_n if that is all
+ * zero); if n = K a bonus token is drawn from p_K.  A draw takes the
+ * smallest token v whose running weight sum exceeds u * total (u =
+ * residual uniform (b, K)).  T == 0: accept iff the draft equals
+ * argmax L[b,t] (lowest id on ties) and emit argmax L[b,n].
+ *
+ *   target_logits [B, K+1, V] fp32   target model logits, rows 0..K
+ *   draft [B, K], topi [B, K, 16], q [B, K, 16]   from the walk
+ *   n_accepted [B] int32 out
+ *   out_tok [B, K+1] int32 out   draft[0..n-1], the drawn token, then -1
+ *   ws >= dflash_workspace_bytes(1, B, K, 0, V) bytes, 256-B aligned
+ * Requirements: target_logits 16-byte aligned; T >= 0.  A NaN or +inf
+ * target logit sets DFLASH_ERR_NONFINITE in the device error word.
+ */
 dflash_status dflash_verify(const float* target_logits, const int32_t* draft,
                             const int32_t* topi, const float* q, int B, int K,
                             int V, float T, uint64_t seed, uint64_t cycle,
@@ -336,7 +381,8 @@ dflash_status dflash_philox4x32(const uint32_t* ctr, uint64_t seed,
  * call's stream right before and right after it launches the kernel of
  * `stage`:
  *   0 conv, 1 LM head with top-16 / logsumexp epilogue, 2 top-16 merge,
- *   3 pair score, 4 walk, 5 verify (row pass, accept tests and draw).
+ *   3 pair score, 4 walk, 5 verify (row pass, accept tests and draw),
+ *   6 E4M3 quantization of y (dflash_draft_e4m3).
  * In dflash_draft with bf16 storage and a conv, stage 0 is the conv with
  * the context gate and stage 3 the one launch that merges, scores and
  * walks (stages 2 and 4 are not recorded).

@@ -188,7 +188,11 @@ def quantize_e4m3_rows(X):
     amax = np.abs(X).max(axis=1)
     scale = np.where(amax > 0, amax / np.float32(E4M3_MAX),
                      np.float32(1.0)).astype(np.float32)
-    return e4m3_encode(X / scale[:, None]), scale
+    codes = np.empty(X.shape, np.uint8)
+    for i in range(0, X.shape[0], 4096):        # row blocks: bounded memory
+        codes[i:i + 4096] = e4m3_encode(X[i:i + 4096] /
+                                        scale[i:i + 4096, None])
+    return codes, scale
 
 
 def dequantize_e4m3_rows(codes, scale) -> np.ndarray:

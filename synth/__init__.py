@@ -67,6 +67,7 @@ class Workload:
     conv_sd: Optional[float]
     sel_sd: float
     target: tuple
+    lm_e4m3: bool = False   # LM head on E4M3 codes (W_lm quantized per row)
 
     @property
     def M(self) -> int:
@@ -104,6 +105,17 @@ CONFIGS = {
                          dtype="bf16", T=1.0, seed=2, w_lm_sd=0.113137,
                          conv_sd=0.05, sel_sd=0.1,
                          target=("affine", 0.9, 1.0)),
+    # b32k8 and b32k8cal with the LM head on 8-bit operands: W_lm and y
+    # quantized per row to E4M3 (the target is still built from the bf16
+    # drafter's logits)
+    "b32k8e4m3": Workload("b32k8e4m3", B=32, K=8, V=151936, H=2048, r=256,
+                          dtype="bf16", T=1.0, seed=2, w_lm_sd=0.02,
+                          conv_sd=0.05, sel_sd=0.1,
+                          target=("affine", 0.9, 1.0), lm_e4m3=True),
+    "b32k8cale4m3": Workload("b32k8cale4m3", B=32, K=8, V=151936, H=2048,
+                             r=256, dtype="bf16", T=1.0, seed=2,
+                             w_lm_sd=0.113137, conv_sd=0.05, sel_sd=0.1,
+                             target=("affine", 0.9, 1.0), lm_e4m3=True),
     "b128k16zipf": Workload("b128k16zipf", B=128, K=16, V=151936, H=2560,
                             r=256, dtype="bf16", T=1.0, seed=3,
                             w_lm_sd=0.02, conv_sd=0.05, sel_sd=0.1,
@@ -196,7 +208,8 @@ def describe(w: Workload) -> str:
     kind, a, sd = w.target
     tgt = (f"{a}*draft+N(0,{sd})" if kind == "affine"
            else f"-{a}*log(rank)+N(0,{sd})")
-    return (f"B={w.B} K={w.K} V={w.V} H={w.H} r={w.r} {w.dtype} T={w.T} "
-            f"seed={w.seed} h~N(0,1) W_lm~N(0,{w.w_lm_sd}) conv={conv} "
-            f"sel~N(0,{w.sel_sd}) target={tgt}")
+    head = " LM head E4M3 (per-row scales)" if w.lm_e4m3 else ""
+    return (f"B={w.B} K={w.K} V={w.V} H={w.H} r={w.r} {w.dtype}{head} "
+            f"T={w.T} seed={w.seed} h~N(0,1) W_lm~N(0,{w.w_lm_sd}) "
+            f"conv={conv} sel~N(0,{w.sel_sd}) target={tgt}")
 
