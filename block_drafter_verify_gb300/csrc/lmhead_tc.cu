@@ -47,14 +47,20 @@ namespace {
 constexpr int BM = 128, BN = 256;
 constexpr int ROW_BYTES = 128;  // bytes of each operand row per stage
 constexpr int A_BYTES = BM * ROW_BYTES;  // 16 KB
-constexpr int THREADS = 192;
 constexpr uint32_t TMEM_COLS = 2 * BN;
 constexpr uint64_t WAIT_NS = 2000000000ull;  // 2 s: far beyond any real wait
 constexpr float LOG2E = 1.4426950408889634f;
 
-template <bool kPair>
+// EPI_WARPS epilogue warps: 4 (thread = row, all BN columns of a tile),
+// or 8 for CTA pairs with 8-bit operands, whose W tiles arrive twice as
+// fast: then two warps share each TMEM lane quarter and take half of the
+// tile's columns each, and the two halves' lists are merged at the end.
+template <bool kPair, bool kFp8>
 struct Cfg {
-  static constexpr int STAGES = kPair ? 6 : 4;
+  static constexpr int EPI_WARPS = kPair && kFp8 ? 8 : 4;
+  static constexpr int HALVES = EPI_WARPS / 4;
+  static constexpr int THREADS = 64 + 32 * EPI_WARPS;
+  static constexpr int STAGES = !kPair ? 4 : (EPI_WARPS == 8 ? 5 : 6);
   static constexpr int B_ROWS = kPair ? BN / 2 : BN;  // W rows per CTA
   static constexpr int B_BYTES = B_ROWS * ROW_BYTES;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
@@ -79,15 +85,23 @@ struct Bars {
   int abort;
 };
 constexpr int XS_STRIDE = 33;  // padded row of the per-thread chunk stage
-constexpr size_t XS_BYTES = 4 * 32 * XS_STRIDE * sizeof(float);
-// 8-bit operands: each epilogue warp's copy of the current tile's BN
-// column scales.
-constexpr size_t WS_BYTES = 4 * BN * sizeof(float);
+// Shared memory after the stages and barriers: the per-thread chunk
+// stage, (8-bit operands) each epilogue warp's copy of its columns'
+// scales for the current tile, and (two halves) the second half's lists
+// for the final merge (16 values, 16 ids, max, sum per row).
+template <bool kPair, bool kFp8>
+struct Smem {
+  using C = Cfg<kPair, kFp8>;
+  static constexpr size_t XS = (size_t)C::EPI_WARPS * 32 * XS_STRIDE * 4;
+  static constexpr size_t WS = kFp8 ? (size_t)4 * BN * 4 : 0;
+  static constexpr size_t MERGE = C::HALVES == 2 ? (size_t)BM * 34 * 4 : 0;
+  static constexpr size_t BARS = (sizeof(Bars<C::STAGES>) + 15) & ~size_t(15);
+  static constexpr size_t TOTAL =
+      1024 + (size_t)C::STAGES * C::STAGE_BYTES + BARS + XS + WS + MERGE;
+};
 template <bool kPair, bool kFp8>
 constexpr size_t smem_bytes() {
-  return 1024 + (size_t)Cfg<kPair>::STAGES * Cfg<kPair>::STAGE_BYTES +
-         ((sizeof(Bars<Cfg<kPair>::STAGES>) + 15) & ~size_t(15)) + XS_BYTES +
-         (kFp8 ? WS_BYTES : 0);
+  return Smem<kPair, kFp8>::TOTAL;
 }
 
 __device__ __forceinline__ bool wait_timeout(uint64_t* bar, uint32_t parity) {
@@ -108,40 +122,105 @@ __device__ __forceinline__ void topk_insert(float (&tv)[kC], int (&ti)[kC],
   if (xv > tv[0]) { tv[0] = xv; ti[0] = xi; }
 }
 
-// Fold 32 logits (columns col0..col0+31) of this thread's row into its
-// running (max, sum exp); returns the bitmask of columns that beat the
-// row's current 16th value (their values are staged in xs).
-__device__ __forceinline__ unsigned epilogue_chunk(float (&x)[32], int col0,
-                                                   int V, float thr,
-                                                   float& run_m, float& run_s,
-                                                   float* xs) {
+// Insert (xv, xi) into the sorted list, ordered by value descending and
+// then by id ascending (for merging lists whose ids interleave).
+__device__ __forceinline__ bool topk_before(float xv, int xi, float tv,
+                                            int ti) {
+  return xv > tv || (xv == tv && xi < ti);
+}
+__device__ __forceinline__ void topk_insert_any(float (&tv)[kC],
+                                                int (&ti)[kC], float xv,
+                                                int xi) {
+  if (!topk_before(xv, xi, tv[kC - 1], ti[kC - 1])) return;
+#pragma unroll
+  for (int p = kC - 1; p >= 1; --p) {
+    const bool shift = topk_before(xv, xi, tv[p - 1], ti[p - 1]);
+    const bool here = !shift && topk_before(xv, xi, tv[p], ti[p]);
+    tv[p] = shift ? tv[p - 1] : (here ? xv : tv[p]);
+    ti[p] = shift ? ti[p - 1] : (here ? xi : ti[p]);
+  }
+  if (topk_before(xv, xi, tv[0], ti[0])) { tv[0] = xv; ti[0] = xi; }
+}
+
+// The 16th largest of 32 values: both halves sorted descending by bitonic
+// networks of min/max steps, then max(a[i], b[15-i]) is the top 16 of the
+// union (in some order), whose minimum is returned.
+__device__ __forceinline__ float kth16_of_32(float (&g)[32]) {
+#pragma unroll
+  for (int h = 0; h < 32; h += 16)
+#pragma unroll
+    for (int k = 2; k <= 16; k <<= 1)
+#pragma unroll
+      for (int j = k >> 1; j > 0; j >>= 1)
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int l = i ^ j;
+          if (l > i) {
+            const float a = g[h + i], b = g[h + l];
+            const bool desc = (i & k) == 0;
+            g[h + i] = desc ? fmaxf(a, b) : fminf(a, b);
+            g[h + l] = desc ? fminf(a, b) : fmaxf(a, b);
+          }
+        }
+  float lo = INFINITY;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) lo = fminf(lo, fmaxf(g[i], g[31 - i]));
+  return lo;
+}
+
+// Columns at or beyond V take no part in the row.
+__device__ __forceinline__ void mask_tail(float (&x)[32], int col0, int V) {
   if (col0 + 32 > V) {
 #pragma unroll
     for (int i = 0; i < 32; ++i)
       if (col0 + i >= V) x[i] = -INFINITY;
   }
-  float t16[16];
+}
+
+// Fold 32 logits of this thread's row into its running (max, sum exp), the
+// exponent taken as 2^(l2e * x) (l2e = log2 e times the row's positive
+// scale).  Returns the chunk maximum.
+// With gmax, also the maxima of the chunk's kG column groups (kG = 8:
+// columns {i, i+8, .., i+24}; kG = 4: {i, i+4, .., i+28}).
+template <int kG = 0>
+__device__ __forceinline__ float fold_chunk(const float (&x)[32], float l2e,
+                                            float& run_m, float& run_s,
+                                            float* gmax = nullptr) {
+  float t[16];
 #pragma unroll
-  for (int i = 0; i < 16; ++i) t16[i] = fmaxf(x[i], x[i + 16]);
+  for (int i = 0; i < 16; ++i) t[i] = fmaxf(x[i], x[i + 16]);
 #pragma unroll
-  for (int w = 8; w >= 1; w >>= 1)
+  for (int w = 8; w >= 1; w >>= 1) {
 #pragma unroll
-    for (int i = 0; i < w; ++i) t16[i] = fmaxf(t16[i], t16[i + w]);
-  const float cm = t16[0];
+    for (int i = 0; i < w; ++i) t[i] = fmaxf(t[i], t[i + w]);
+    if (kG == w) {
+#pragma unroll
+      for (int i = 0; i < w; ++i) gmax[i] = t[i];
+    }
+  }
+  const float cm = t[0];
   if (cm > run_m) {
-    run_s *= tc::ex2_approx((run_m - cm) * LOG2E);
+    run_s *= tc::ex2_approx((run_m - cm) * l2e);
     run_m = cm;
   }
-  const float nb = -run_m * LOG2E;
+  const float nb = -run_m * l2e;
   float s[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-  for (int i = 0; i < 32; ++i) s[i & 3] += tc::ex2_approx(fmaf(x[i], LOG2E, nb));
+  for (int i = 0; i < 32; ++i) s[i & 3] += tc::ex2_approx(fmaf(x[i], l2e, nb));
   run_s += (s[0] + s[1]) + (s[2] + s[3]);
+  return cm;
+}
+
+// Bitmask of the columns that beat the row's current 16th value thr and
+// reach lo (their values are staged in xs); cm is the chunk maximum.
+__device__ __forceinline__ unsigned chunk_candidates(const float (&x)[32],
+                                                     float cm, float thr,
+                                                     float lo, float* xs) {
   unsigned mask = 0;
-  if (cm > thr) {
+  if (cm > thr && cm >= lo) {
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
-      mask |= (x[i] > thr ? 1u : 0u) << i;
+      mask |= (x[i] > thr && x[i] >= lo ? 1u : 0u) << i;
       xs[i] = x[i];
     }
   }
@@ -149,13 +228,14 @@ __device__ __forceinline__ unsigned epilogue_chunk(float (&x)[32], int col0,
 }
 
 template <bool kPair, bool kFp8>
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __launch_bounds__(Cfg<kPair, kFp8>::THREADS, 1)
     lmhead_tc_kernel(const __grid_constant__ CUtensorMap map_y,
                      const __grid_constant__ CUtensorMap map_w, int M, int H,
                      int V, int row_groups, int strips, TopkPartials P,
                      const float* __restrict__ y_scale,
                      const float* __restrict__ w_scale, int* err) {
-  using C = Cfg<kPair>;
+  using C = Cfg<kPair, kFp8>;
+  using SM = Smem<kPair, kFp8>;
   constexpr int STAGES = C::STAGES;
   constexpr int BK = Elem<kFp8>::BK;
   extern __shared__ uint8_t smem_raw[];
@@ -165,10 +245,10 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint8_t* sb = smem + STAGES * A_BYTES;
   Bars<STAGES>* bars =
       reinterpret_cast<Bars<STAGES>*>(smem + STAGES * C::STAGE_BYTES);
-  float* xs_all = reinterpret_cast<float*>(
-      smem + STAGES * C::STAGE_BYTES +
-      ((sizeof(Bars<STAGES>) + 15) & ~size_t(15)));
-  float* ws_all = xs_all + XS_BYTES / sizeof(float);  // 8-bit operands only
+  float* xs_all =
+      reinterpret_cast<float*>(smem + STAGES * C::STAGE_BYTES + SM::BARS);
+  float* ws_all = xs_all + SM::XS / 4;     // 8-bit operands only
+  float* mg_all = ws_all + SM::WS / 4;     // two halves only
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // a pair is a cluster of two consecutive blocks; rank 0 leads
   const int rank = kPair ? (int)(blockIdx.x & 1) : 0;
@@ -188,7 +268,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     for (int b = 0; b < 2; ++b) {
       tc::mbar_init(&bars->tfull[b], 1);
-      tc::mbar_init(&bars->tempty[b], 4 * C::CTAS);
+      tc::mbar_init(&bars->tempty[b], C::EPI_WARPS * C::CTAS);
     }
     tc::mbar_init(&bars->drain, 1);
     bars->abort = 0;
@@ -337,15 +417,22 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
+    constexpr int CH = BN / 32 / C::HALVES;  // 32-column chunks per warp
+    const int ew = warp - 2;
     const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int half = ew >> 2;  // which part of each tile's columns
     const int m = mtile * BM + q * 32 + lane;
-    float* xs = xs_all + ((warp - 2) * 32 + lane) * XS_STRIDE;
-    float* wsc = ws_all + (warp - 2) * BN;  // this warp's column scales
+    float* xs = xs_all + (ew * 32 + lane) * XS_STRIDE;
+    float* wsc = ws_all + ew * (BN / C::HALVES);  // this warp's col scales
     // y's row scales come from the previous launch: wait for it here too
     // (only the producer waits in the bf16 form, whose epilogue reads
     // nothing but TMEM)
     if constexpr (kFp8) pdl_wait();
+    // 8-bit operands: logit = srow * (acc * w_scale); the row factor is
+    // positive, so candidates are ranked on acc * w_scale and srow enters
+    // the exponent's scale and the final values only
     const float srow = kFp8 && m < M ? y_scale[m] : 1.f;
+    const float l2e = kFp8 ? srow * LOG2E : LOG2E;
     // accumulator-free barriers of the MMA-issuing CTA
     const uint32_t tempty0 =
         kPair ? tc::mapa_shared(tc::smem_u32(&bars->tempty[0]), 0)
@@ -360,11 +447,11 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int vt = strip + it * strips;
       const int b = it & 1;
       const uint32_t aph = (it >> 1) & 1;
-      float wreg[BN / 32];
+      float wreg[CH];
       if constexpr (kFp8) {  // loads in flight during the wait
 #pragma unroll
-        for (int j = 0; j < BN / 32; ++j) {
-          const int v = vt * BN + j * 32 + lane;
+        for (int j = 0; j < CH; ++j) {
+          const int v = vt * BN + (half * CH + j) * 32 + lane;
           wreg[j] = v < V ? __ldg(w_scale + v) : 0.f;
         }
       }
@@ -378,32 +465,31 @@ __global__ void __launch_bounds__(THREADS, 1)
       if constexpr (kFp8) {
         __syncwarp();  // the previous tile's reads of wsc are done
 #pragma unroll
-        for (int j = 0; j < BN / 32; ++j) wsc[j * 32 + lane] = wreg[j];
+        for (int j = 0; j < CH; ++j) wsc[j * 32 + lane] = wreg[j];
         __syncwarp();
       }
       tc::fence_after_sync();
       const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16) +
                              static_cast<uint32_t>(b * BN);
-#pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
-        __syncwarp();
-        float x[32];
-        tc::tmem_ld_x32(tbase + c * 32, x);
-        const int col0 = vt * BN + c * 32;
+      // chunk c of this warp's columns: TMEM -> registers, scaled, tail
+      auto load_chunk = [&](int c, float (&x)[32]) {
+        const int cc = half * CH + c;
+        tc::tmem_ld_x32(tbase + cc * 32, x);
         if constexpr (kFp8) {
           const float4* w4 = reinterpret_cast<const float4*>(wsc + c * 32);
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             const float4 f = w4[i];
-            x[4 * i] *= srow * f.x;
-            x[4 * i + 1] *= srow * f.y;
-            x[4 * i + 2] *= srow * f.z;
-            x[4 * i + 3] *= srow * f.w;
+            x[4 * i] *= f.x;
+            x[4 * i + 1] *= f.y;
+            x[4 * i + 2] *= f.z;
+            x[4 * i + 3] *= f.w;
           }
         }
-        unsigned mask =
-            epilogue_chunk(x, col0, V, tv[kC - 1], run_m, run_s, xs);
-        // insert the chunk's candidates, every lane its own row in step
+        mask_tail(x, vt * BN + cc * 32, V);
+      };
+      // insert the chunk's candidates, every lane its own row in step
+      auto insert = [&](unsigned mask, int col0) {
         while (__any_sync(0xffffffffu, mask != 0)) {
           if (mask) {
             const int i = __ffs(mask) - 1;
@@ -412,6 +498,41 @@ __global__ void __launch_bounds__(THREADS, 1)
             if (xv > tv[kC - 1]) topk_insert(tv, ti, xv, col0 + i);
           }
         }
+      };
+      float lo = -INFINITY;
+      if (it == 0) {
+        // First tile: the list is empty, so most columns would be inserted
+        // one by one.  A first pass folds (max, sum) and keeps the maxima
+        // of 32 column groups; lo, the 16th largest of them, is reached by
+        // at least 16 of the tile's values, so no value below lo can make
+        // the top 16, and the second pass inserts only values >= lo.
+#pragma unroll 1
+        for (int c = 0; c < CH; ++c) {
+          __syncwarp();
+          float x[32];
+          load_chunk(c, x);
+          fold_chunk<32 / CH>(x, l2e, run_m, run_s, xs + c * (32 / CH));
+        }
+        float gm[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) gm[i] = xs[i];
+        lo = kth16_of_32(gm);
+      }
+#pragma unroll 1
+      for (int c = 0; c < CH; ++c) {
+        __syncwarp();
+        float x[32];
+        load_chunk(c, x);
+        float cm;
+        if (it == 0) {  // folded above
+          cm = x[0];
+#pragma unroll
+          for (int i = 1; i < 32; ++i) cm = fmaxf(cm, x[i]);
+        } else {
+          cm = fold_chunk(x, l2e, run_m, run_s);
+        }
+        insert(chunk_candidates(x, cm, tv[kC - 1], lo, xs),
+               vt * BN + (half * CH + c) * 32);
       }
       tc::fence_before_sync();
       __syncwarp();
@@ -422,7 +543,39 @@ __global__ void __launch_bounds__(THREADS, 1)
           tc::mbar_arrive(&bars->tempty[b]);
       }
     }
-    if (ok && m < M) {
+    if constexpr (C::HALVES == 2) {
+      // the second half's warps hand their lists to the first half's; every
+      // epilogue thread reaches both barriers once (also after a timeout)
+      float* mg = mg_all + (q * 32 + lane) * 34;
+      if (half == 1) {
+#pragma unroll
+        for (int k = 0; k < kC; ++k) {
+          mg[k] = tv[k];
+          mg[kC + k] = __int_as_float(ti[k]);
+        }
+        mg[32] = run_m;
+        mg[33] = run_s;
+      }
+      asm volatile("bar.sync 1, %0;" ::"n"(C::EPI_WARPS * 32) : "memory");
+      if (half == 0) {
+#pragma unroll 1
+        for (int k = 0; k < kC; ++k)
+          topk_insert_any(tv, ti, mg[k], __float_as_int(mg[kC + k]));
+        const float m1 = mg[32], s1 = mg[33];
+        const float mm = fmaxf(run_m, m1);
+        if (mm != -INFINITY)
+          run_s = run_s * tc::ex2_approx((run_m - mm) * l2e) +
+                  s1 * tc::ex2_approx((m1 - mm) * l2e);
+        run_m = mm;
+      }
+      asm volatile("bar.sync 1, %0;" ::"n"(C::EPI_WARPS * 32) : "memory");
+    }
+    if (ok && half == 0 && !*abort && m < M) {
+      if constexpr (kFp8) {
+#pragma unroll
+        for (int k = 0; k < kC; ++k) tv[k] *= srow;
+        run_m *= srow;
+      }
       const size_t pr = (size_t)m * strips + strip;
       float4* pv = reinterpret_cast<float4*>(P.v + pr * kC);
       int4* pi = reinterpret_cast<int4*>(P.i + pr * kC);
@@ -468,7 +621,7 @@ int max_resident_pairs(int num_sms) {
   if (cached[dev] > 0) return cached[dev];
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(num_sms);
-  cfg.blockDim = dim3(THREADS);
+  cfg.blockDim = dim3(Cfg<true, kFp8>::THREADS);
   cfg.dynamicSmemBytes = smem_bytes<true, kFp8>();
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -524,7 +677,8 @@ cudaError_t launch_variant(const CUtensorMap& map_y, const CUtensorMap& map_w,
         cudaFuncAttributeMaxDynamicSharedMemorySize,
         (int)smem_bytes<false, kFp8>());
     if (e != cudaSuccess) return e;
-    PdlLaunch L(dim3(grid), dim3(THREADS), smem_bytes<false, kFp8>(), s);
+    PdlLaunch L(dim3(grid), dim3(Cfg<false, kFp8>::THREADS),
+                smem_bytes<false, kFp8>(), s);
     return cudaLaunchKernelEx(&L.cfg, lmhead_tc_kernel<false, kFp8>, map_y,
                               map_w, M, H, V, rg, st, P, y_scale, w_scale,
                               err);
@@ -534,7 +688,8 @@ cudaError_t launch_variant(const CUtensorMap& map_y, const CUtensorMap& map_w,
       cudaFuncAttributeMaxDynamicSharedMemorySize,
       (int)smem_bytes<true, kFp8>());
   if (e != cudaSuccess) return e;
-  PdlLaunch L(dim3(grid), dim3(THREADS), smem_bytes<true, kFp8>(), s, 2);
+  PdlLaunch L(dim3(grid), dim3(Cfg<true, kFp8>::THREADS),
+              smem_bytes<true, kFp8>(), s, 2);
   return cudaLaunchKernelEx(&L.cfg, lmhead_tc_kernel<true, kFp8>, map_y,
                             map_w, M, H, V, rg, st, P, y_scale, w_scale, err);
 }
