@@ -80,10 +80,11 @@ bool sizes_ok(int B, int K, int H, int V) {
          M * (long long)(H > 0 ? H : 1) <= (1LL << 40);
 }
 
-// Workspace of dflash_lmhead_topk: y (room for fp32), then the per-strip
-// top-16 partials of every row.
+// Workspace of dflash_lmhead_topk: y (room for fp32), the per-strip top-16
+// partials of every row, then the LM head's shared row bounds
+// [B*K, kBoundSlots] fp32.
 size_t lmhead_ws_layout(int B, int K, int H, int V, void* base, void** y,
-                        TopkPartials* P) {
+                        TopkPartials* P, float** row_bound = nullptr) {
   (void)V;
   const size_t M = (size_t)B * K;
   char* p = static_cast<char*>(base);
@@ -100,8 +101,10 @@ size_t lmhead_ws_layout(int B, int K, int H, int V, void* base, void** y,
   pp.i = reinterpret_cast<int*>(take((size_t)kMaxStrips * M * kC * sizeof(int)));
   pp.m = reinterpret_cast<float*>(take((size_t)kMaxStrips * M * sizeof(float)));
   pp.s = reinterpret_cast<float*>(take((size_t)kMaxStrips * M * sizeof(float)));
+  float* rb = reinterpret_cast<float*>(take(M * kBoundSlots * sizeof(float)));
   if (y) *y = yy;
   if (P) *P = pp;
+  if (row_bound) *row_bound = rb;
   return align256(off);
 }
 
@@ -155,10 +158,14 @@ dflash_status lmhead_bf16(const __nv_bfloat16* h, const __nv_bfloat16* conv_w,
                           const E4m3Head* q8 = nullptr) {
   void* yv = nullptr;
   TopkPartials P;
-  lmhead_ws_layout(B, K, H, V, ws, &yv, &P);
+  float* row_bound = nullptr;
+  lmhead_ws_layout(B, K, H, V, ws, &yv, &P, &row_bound);
   const int M = B * K;
   const __nv_bfloat16* a = h;
   cudaError_t e;
+  // the conv launch resets the LM head's shared row bounds; without a conv
+  // the LM head runs without them
+  if (!conv_w) row_bound = nullptr;
   if (conv_w) {
     CUtensorMap mh, mw, mg;
     if (!make_tmap_bf16_2d(&mh, h, H, M, 64, 128) ||
@@ -171,7 +178,7 @@ dflash_status lmhead_bf16(const __nv_bfloat16* h, const __nv_bfloat16* conv_w,
     {
       StageTimer tm(kStConv, s);
       e = launch_conv_tc(mh, mw, w_gate ? &mg : nullptr, h, B, K, H, r, y,
-                         gate, tickets, d.err, s);
+                         gate, tickets, row_bound, M * kBoundSlots, d.err, s);
     }
     if (e != cudaSuccess) return DFLASH_ERR_CUDA;
     a = y;
@@ -197,7 +204,7 @@ dflash_status lmhead_bf16(const __nv_bfloat16* h, const __nv_bfloat16* conv_w,
     StageTimer tm(kStLmhead, s);
     e = launch_lmhead_tc(my, mw, M, H, V, d.sms, P, d.err, &strips, s,
                          q8 && conv_w ? q8->y_scale : nullptr,
-                         q8 && conv_w ? q8->w_scale : nullptr);
+                         q8 && conv_w ? q8->w_scale : nullptr, row_bound);
   }
   if (e != cudaSuccess) return DFLASH_ERR_CUDA;
   if (P_out) {  // the caller merges (draft tail)

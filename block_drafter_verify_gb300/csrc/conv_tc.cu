@@ -78,7 +78,8 @@ __global__ void __launch_bounds__(THREADS)
                    const __nv_bfloat16* __restrict__ h, int M, int K, int H,
                    int r, __nv_bfloat16* __restrict__ y,
                    float* __restrict__ gate, unsigned* __restrict__ tickets,
-                   int ntickets, int* err) {
+                   int ntickets, float* __restrict__ row_bound, int nbound,
+                   int* err) {
   constexpr int STAGES = ConvCfg<BC>::STAGES;
   constexpr int B_BYTES = ConvCfg<BC>::B_BYTES;
   constexpr int STAGE_BYTES = ConvCfg<BC>::STAGE_BYTES;
@@ -123,6 +124,12 @@ __global__ void __launch_bounds__(THREADS)
   if (threadIdx.x == 0) pdl_trigger();
   if (tickets && blockIdx.x == 0 && blockIdx.y == 0)
     for (int i = threadIdx.x; i < ntickets; i += THREADS) tickets[i] = 0u;
+  if (row_bound) {  // the next launch's shared row bounds start unset
+    const int lin = blockIdx.y * gridDim.x + blockIdx.x;
+    for (int i = lin * THREADS + threadIdx.x; i < nbound;
+         i += gridDim.x * gridDim.y * THREADS)
+      row_bound[i] = -INFINITY;
+  }
 
   if (warp == 0) {
     if (lane == 0) {
@@ -263,8 +270,8 @@ template <int BC>
 cudaError_t launch_conv_bc(const CUtensorMap& map_h, const CUtensorMap& map_wc,
                            const CUtensorMap* map_wg, const __nv_bfloat16* h,
                            int B, int K, int H, int r, __nv_bfloat16* y,
-                           float* gate, unsigned* tickets, int* err,
-                           cudaStream_t s) {
+                           float* gate, unsigned* tickets, float* row_bound,
+                           int nbound, int* err, cudaStream_t s) {
   const int M = B * K;
   cudaError_t e = cudaFuncSetAttribute(
       conv_tc_kernel<BC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -275,20 +282,20 @@ cudaError_t launch_conv_bc(const CUtensorMap& map_h, const CUtensorMap& map_wc,
   PdlLaunch L(grid, dim3(THREADS), conv_smem_bytes<BC>(), s);
   return cudaLaunchKernelEx(&L.cfg, conv_tc_kernel<BC>, map_h, map_wc,
                             map_wg ? *map_wg : map_wc, h, M, K, H, r, y, gate,
-                            tickets, B, err);
+                            tickets, B, row_bound, nbound, err);
 }
 }  // namespace
 
 cudaError_t launch_conv_tc(const CUtensorMap& map_h, const CUtensorMap& map_wc,
                            const CUtensorMap* map_wg, const __nv_bfloat16* h,
                            int B, int K, int H, int r, __nv_bfloat16* y,
-                           float* gate, unsigned* tickets, int* err,
-                           cudaStream_t s) {
+                           float* gate, unsigned* tickets, float* row_bound,
+                           int nbound, int* err, cudaStream_t s) {
   if (conv_tc_bc(B * K) == 128)
     return launch_conv_bc<128>(map_h, map_wc, map_wg, h, B, K, H, r, y, gate,
-                               tickets, err, s);
+                               tickets, row_bound, nbound, err, s);
   return launch_conv_bc<32>(map_h, map_wc, map_wg, h, B, K, H, r, y, gate,
-                            tickets, err, s);
+                            tickets, row_bound, nbound, err, s);
 }
 
 }  // namespace dflash

@@ -23,13 +23,14 @@ bool make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner,
 // with BC = conv_tc_bc(B*K) channels per CTA (map_wg likewise).
 // With map_wg (w_gate [r, H], box {64, 32}) the launch also writes the pair
 // selector's gate g = sigmoid(W_g h) as gate [B*K, r] fp32.  tickets (B
-// words, may be NULL) are zeroed for a later launch of the same call.
+// words, may be NULL) are zeroed and row_bound (nbound floats, may be NULL)
+// set to -inf for later launches of the same call.
 int conv_tc_bc(int M);
 cudaError_t launch_conv_tc(const CUtensorMap& map_h, const CUtensorMap& map_wc,
                            const CUtensorMap* map_wg, const __nv_bfloat16* h,
                            int B, int K, int H, int r, __nv_bfloat16* y,
-                           float* gate, unsigned* tickets, int* err,
-                           cudaStream_t s);
+                           float* gate, unsigned* tickets, float* row_bound,
+                           int nbound, int* err, cudaStream_t s);
 // TMA descriptor of a row-major 8-bit [rows, inner] matrix, 128-byte
 // swizzle (inner a multiple of 16).
 bool make_tmap_u8_2d(CUtensorMap* map, const void* base, uint64_t inner,
@@ -39,11 +40,17 @@ bool make_tmap_u8_2d(CUtensorMap* map, const void* base, uint64_t inner,
 // Writes `*strips` partial lists per row.  With y_scale and w_scale the
 // operands are E4M3 codes (maps from make_tmap_u8_2d, boxes of 128 codes
 // along H) and logit (m, v) = y_scale[m] * w_scale[v] * (codes' dot).
+// row_bound (M * kBoundSlots floats set to -inf by an earlier launch of
+// the same stream, may be NULL) is where units share their rows' running
+// maxima, from which every unit prunes values that cannot reach a row's
+// top 16.
+constexpr int kBoundSlots = 16;
 cudaError_t launch_lmhead_tc(const CUtensorMap& map_y, const CUtensorMap& map_w,
                              int M, int H, int V, int num_sms, TopkPartials P,
                              int* err, int* strips, cudaStream_t s,
                              const float* y_scale = nullptr,
-                             const float* w_scale = nullptr);
+                             const float* w_scale = nullptr,
+                             float* row_bound = nullptr);
 
 // quant_e4m3.cu: per-row E4M3 quantization of a bf16 [R, H] matrix
 // (H % 8 == 0): scale[i] = max_k |x_ik| / 448 (1 for a zero row), code =

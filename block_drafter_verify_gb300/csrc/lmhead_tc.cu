@@ -233,7 +233,8 @@ __global__ void __launch_bounds__(Cfg<kPair, kFp8>::THREADS, 1)
                      const __grid_constant__ CUtensorMap map_w, int M, int H,
                      int V, int row_groups, int strips, TopkPartials P,
                      const float* __restrict__ y_scale,
-                     const float* __restrict__ w_scale, int* err) {
+                     const float* __restrict__ w_scale,
+                     float* __restrict__ row_bound, int* err) {
   using C = Cfg<kPair, kFp8>;
   using SM = Smem<kPair, kFp8>;
   constexpr int STAGES = C::STAGES;
@@ -424,10 +425,9 @@ __global__ void __launch_bounds__(Cfg<kPair, kFp8>::THREADS, 1)
     const int m = mtile * BM + q * 32 + lane;
     float* xs = xs_all + (ew * 32 + lane) * XS_STRIDE;
     float* wsc = ws_all + ew * (BN / C::HALVES);  // this warp's col scales
-    // y's row scales come from the previous launch: wait for it here too
-    // (only the producer waits in the bf16 form, whose epilogue reads
-    // nothing but TMEM)
-    if constexpr (kFp8) pdl_wait();
+    // y's row scales come from the previous launch, which also reset the
+    // shared row bounds: wait for it here too (the producer waits anyway)
+    if (kFp8 || row_bound) pdl_wait();
     // 8-bit operands: logit = srow * (acc * w_scale); the row factor is
     // positive, so candidates are ranked on acc * w_scale and srow enters
     // the exponent's scale and the final values only
@@ -443,6 +443,31 @@ __global__ void __launch_bounds__(Cfg<kPair, kFp8>::THREADS, 1)
     for (int k = 0; k < kC; ++k) { tv[k] = -INFINITY; ti[k] = -1; }
     float run_m = -INFINITY, run_s = 0.f;
     bool ok = true;
+    // Shared row bounds: the lists of kBoundSlots units (strips 0.. of the
+    // row group, each half of a tile's columns its own slot) publish their
+    // running maxima; these are values of distinct columns, so a value
+    // below the smallest of them cannot make the row's top 16 and no unit
+    // needs to insert it.  Unset slots hold -inf; reads may be stale,
+    // which only weakens the bound.
+    const int bslot = strip * C::HALVES + half;
+    float* rb = row_bound && m < M ? row_bound + (size_t)m * kBoundSlots
+                                   : nullptr;
+    auto publish = [&]() {
+      if (rb && bslot < kBoundSlots) rb[bslot] = run_m;
+    };
+    auto read_bound = [&]() {
+      float bd = -INFINITY;
+      if (rb) {
+        const float4* r4 = reinterpret_cast<const float4*>(rb);
+        bd = INFINITY;
+#pragma unroll
+        for (int k = 0; k < kBoundSlots / 4; ++k) {
+          const float4 f = __ldcg(r4 + k);
+          bd = fminf(bd, fminf(fminf(f.x, f.y), fminf(f.z, f.w)));
+        }
+      }
+      return bd;
+    };
     for (int it = 0; it < my_tiles; ++it) {
       const int vt = strip + it * strips;
       const int b = it & 1;
@@ -517,7 +542,9 @@ __global__ void __launch_bounds__(Cfg<kPair, kFp8>::THREADS, 1)
 #pragma unroll
         for (int i = 0; i < 32; ++i) gm[i] = xs[i];
         lo = kth16_of_32(gm);
+        publish();
       }
+      lo = fmaxf(lo, read_bound());
 #pragma unroll 1
       for (int c = 0; c < CH; ++c) {
         __syncwarp();
@@ -534,6 +561,7 @@ __global__ void __launch_bounds__(Cfg<kPair, kFp8>::THREADS, 1)
         insert(chunk_candidates(x, cm, tv[kC - 1], lo, xs),
                vt * BN + (half * CH + c) * 32);
       }
+      if (it > 0) publish();
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) {
@@ -667,7 +695,8 @@ template <bool kFp8>
 cudaError_t launch_variant(const CUtensorMap& map_y, const CUtensorMap& map_w,
                            int M, int H, int V, int num_sms, TopkPartials P,
                            int* err, int* strips_out, cudaStream_t s,
-                           const float* y_scale, const float* w_scale) {
+                           const float* y_scale, const float* w_scale,
+                           float* row_bound) {
   int rg = 0, st = 0;
   const int grid = lmhead_tc_grid(M, V, num_sms, &rg, &st, kFp8);
   *strips_out = st;
@@ -681,7 +710,7 @@ cudaError_t launch_variant(const CUtensorMap& map_y, const CUtensorMap& map_w,
                 smem_bytes<false, kFp8>(), s);
     return cudaLaunchKernelEx(&L.cfg, lmhead_tc_kernel<false, kFp8>, map_y,
                               map_w, M, H, V, rg, st, P, y_scale, w_scale,
-                              err);
+                              row_bound, err);
   }
   cudaError_t e = cudaFuncSetAttribute(
       lmhead_tc_kernel<true, kFp8>,
@@ -691,19 +720,21 @@ cudaError_t launch_variant(const CUtensorMap& map_y, const CUtensorMap& map_w,
   PdlLaunch L(dim3(grid), dim3(Cfg<true, kFp8>::THREADS),
               smem_bytes<true, kFp8>(), s, 2);
   return cudaLaunchKernelEx(&L.cfg, lmhead_tc_kernel<true, kFp8>, map_y,
-                            map_w, M, H, V, rg, st, P, y_scale, w_scale, err);
+                            map_w, M, H, V, rg, st, P, y_scale, w_scale,
+                            row_bound, err);
 }
 }  // namespace
 
 cudaError_t launch_lmhead_tc(const CUtensorMap& map_y, const CUtensorMap& map_w,
                              int M, int H, int V, int num_sms, TopkPartials P,
                              int* err, int* strips_out, cudaStream_t s,
-                             const float* y_scale, const float* w_scale) {
+                             const float* y_scale, const float* w_scale,
+                             float* row_bound) {
   if (y_scale && w_scale)
     return launch_variant<true>(map_y, map_w, M, H, V, num_sms, P, err,
-                                strips_out, s, y_scale, w_scale);
+                                strips_out, s, y_scale, w_scale, row_bound);
   return launch_variant<false>(map_y, map_w, M, H, V, num_sms, P, err,
-                               strips_out, s, nullptr, nullptr);
+                               strips_out, s, nullptr, nullptr, row_bound);
 }
 
 }  // namespace dflash
