@@ -583,9 +583,10 @@ def run_ours(args):
     if os.path.exists(tr_file):
         with open(tr_file) as f:
             tr = json.load(f)
-        if tr.get("workload") == w.name and tr.get("kernel_rev") == \
-                lmhead_kernel_rev():
-            traffic = tr.get("bytes_per_launch")
+        for e in (tr if isinstance(tr, list) else [tr]):
+            if e.get("workload") == w.name and e.get("kernel_rev") == \
+                    lmhead_kernel_rev():
+                traffic = e.get("bytes_per_launch")
     tensor_peak, tensor_src = pk["bf16_tflops"], pk["source"]
     if w.lm_e4m3:   # E4M3 MMA: the measured bf16 rate x the nominal 2x
         tensor_peak = 2.0 * pk["bf16_tflops"]
