@@ -109,17 +109,21 @@ __device__ __forceinline__ bool wait_timeout(uint64_t* bar, uint32_t parity) {
   return tc::mbar_wait_bounded(bar, parity, &never, WAIT_NS);
 }
 
-// Insert xv (> tv[15], id larger than every held id) into the sorted list.
+// Insert xv (> tv[15], id larger than every held id) into the sorted list:
+// entry p becomes max(tv[p], min(xv, tv[p-1])), and the ids follow the
+// comparisons of xv with the old entries (an equal value keeps its place).
 __device__ __forceinline__ void topk_insert(float (&tv)[kC], int (&ti)[kC],
                                             float xv, int xi) {
+  bool c[kC];
+#pragma unroll
+  for (int p = 0; p < kC; ++p) c[p] = xv > tv[p];
 #pragma unroll
   for (int p = kC - 1; p >= 1; --p) {
-    const bool shift = xv > tv[p - 1];
-    const bool here = !shift && (xv > tv[p]);
-    tv[p] = shift ? tv[p - 1] : (here ? xv : tv[p]);
-    ti[p] = shift ? ti[p - 1] : (here ? xi : ti[p]);
+    ti[p] = c[p - 1] ? ti[p - 1] : (c[p] ? xi : ti[p]);
+    tv[p] = fmaxf(tv[p], fminf(xv, tv[p - 1]));
   }
-  if (xv > tv[0]) { tv[0] = xv; ti[0] = xi; }
+  ti[0] = c[0] ? xi : ti[0];
+  tv[0] = fmaxf(tv[0], xv);
 }
 
 // Insert (xv, xi) into the sorted list, ordered by value descending and
