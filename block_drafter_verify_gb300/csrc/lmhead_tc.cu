@@ -520,12 +520,12 @@ __global__ void __launch_bounds__(Cfg<kPair, kFp8>::THREADS, 1)
       // insert the chunk's candidates, every lane its own row in step
       auto insert = [&](unsigned mask, int col0) {
         while (__any_sync(0xffffffffu, mask != 0)) {
-          if (mask) {
-            const int i = __ffs(mask) - 1;
-            mask &= mask - 1;
-            const float xv = xs[i];
-            if (xv > tv[kC - 1]) topk_insert(tv, ti, xv, col0 + i);
-          }
+          // straight-line for every lane: a lane without a candidate
+          // inserts -inf, which changes nothing
+          const int i = max(__ffs(mask) - 1, 0);
+          const float xv = mask ? xs[i] : -INFINITY;
+          mask &= mask - 1;
+          topk_insert(tv, ti, xv, col0 + i);
         }
       };
       float lo = -INFINITY;
