@@ -483,3 +483,40 @@ def test_fused_full_size_b128k16zipf_sampled(lib):
                cycle, 1e-5)
     check_verify(dv.n[:S], dv.out[:S], np_(L)[:S], np_(dv.draft)[:S], topi,
                  np_(dv.q)[:S], w.T, seed, cycle)
+
+
+@pytest.mark.parametrize("e4m3", [False, True])
+def test_fused_draft_exact_ties_across_strips(lib, e4m3):
+    """W_lm built from 40 distinct rows repeated over V = 5003 tokens: every
+    logit value occurs about 125 times, spread over all vocab strips, so the
+    top 16 of a row are 16 copies of its largest value and must be the 16
+    lowest ids that carry it (ties to the lower id through the first-tile
+    threshold, the shared row maxima and the merge of the strips)."""
+    import synth as _s
+    w = _s.Workload("ties", B=4, K=4, V=5003, H=128, r=32, dtype="bf16",
+                    T=1.0, seed=77, w_lm_sd=0.1, conv_sd=0.05, sel_sd=0.1,
+                    target=("affine", 0.9, 1.0))
+    x = _s.make_inputs(w)
+    base = x["w_lm"][:40].clone()
+    x["w_lm"] = base.repeat((w.V + 39) // 40, 1)[: w.V].contiguous()
+    dv = lib.DraftVerify(w.B, w.K, w.H, w.V, w.r, _weights(x), lm_e4m3=e4m3)
+    h = to_dev(x["h"][:, : w.K])
+    dv.draft_all(h, to_dev(x["anchor"]), w.T, 5, 0)
+    torch.cuda.synchronize()
+    lib.dflash_check()
+    if e4m3:
+        yc, ys = dv.y_e4m3()
+        wc, ws = oracle.quantize_e4m3_rows(x["w_lm"].float().numpy())
+        y64 = oracle.dequantize_e4m3_rows(np_(yc), np_(ys))
+        W64 = oracle.dequantize_e4m3_rows(wc, ws)
+    else:
+        y64 = f64(dv.y(fused=True)).reshape(-1, w.H)
+        W64 = f64(x["w_lm"])
+    _, o_i, _ = oracle.lmhead_topk(y64, W64)
+    gi = np_(dv.topi)
+    for m in range(w.M):
+        # the GPU's 16 values are equal copies of one logit (same W rows,
+        # same accumulation order), so the ids must be the lowest 16
+        gv = np_(dv.topv)[m]
+        assert np.all(gv == gv[0]), f"row {m}: values differ {gv}"
+        assert np.array_equal(gi[m], o_i[m]), f"row {m}: {gi[m]} vs {o_i[m]}"
