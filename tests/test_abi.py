@@ -68,3 +68,40 @@ def test_binding_fails_loudly_without_library(tmp_path):
     import block_drafter_verify_gb300.binding as b
     with pytest.raises(RuntimeError):
         b.load(str(tmp_path / "missing.so"))
+
+
+def test_argument_checks_come_before_any_device_work(so):
+    """Invalid arguments are refused on the host (DFLASH_ERR_INVALID_ARG)
+    before the library looks for a device, so these run without a GPU."""
+    vp, i32, f32, u64, sz = (ctypes.c_void_p, ctypes.c_int, ctypes.c_float,
+                             ctypes.c_uint64, ctypes.c_size_t)
+    fake = ctypes.c_void_p(0x100000)   # never dereferenced: checks fail first
+    q = so.dflash_quantize_e4m3_rows
+    q.restype, q.argtypes = i32, [vp, i32, i32, vp, vp, vp]
+    assert q(None, 4, 32, fake, fake, None) == 1            # no input
+    assert q(fake, 4, 24, fake, fake, None) == 1            # H % 16 != 0
+    assert q(fake, 0, 32, fake, fake, None) == 1            # no rows
+    d = so.dflash_draft_e4m3
+    d.restype = i32
+    d.argtypes = [vp] * 8 + [i32] * 5 + [f32, u64, u64] + [vp] * 8 + [sz, vp]
+    args = [fake, None, fake, fake, fake, fake, fake, fake,   # conv_w NULL
+            2, 4, 64, 1000, 32, 1.0, 1, 0] + [fake] * 8 + [1 << 30, None]
+    assert d(*args) == 1
+    args[1] = fake
+    args[10] = 40                                             # H % 16 != 0
+    assert d(*args) == 1
+    so.dflash_workspace_bytes.restype = sz
+    so.dflash_workspace_bytes.argtypes = [i32] * 5
+    w2 = so.dflash_workspace_bytes(2, 32, 8, 2048, 151936)
+    w3 = so.dflash_workspace_bytes(3, 32, 8, 2048, 151936)
+    assert w3 >= w2 + 32 * 8 * 2048 + 32 * 8 * 4
+    assert so.dflash_workspace_bytes(3, 1, 4, 8, 100) == 0   # H < 16
+    v = so.dflash_path_viterbi
+    v.restype, v.argtypes = i32, [vp, vp, i32, i32, vp, vp, vp, vp]
+    assert v(fake, fake, 2, 17, fake, fake, fake, None) == 1  # K > 16
+    r = so.dflash_top16_recall
+    r.restype, r.argtypes = i32, [vp, vp, i32, i32, i32, vp, vp, vp]
+    assert r(None, fake, 2, 4, 100, fake, fake, None) == 1
+    c = so.dflash_commit
+    c.restype, c.argtypes = i32, [vp, vp, i32, i32, vp, vp, vp, i32, vp, vp]
+    assert c(fake, fake, 2, 4, fake, fake, fake, 0, fake, None) == 1  # cap 0
