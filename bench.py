@@ -244,11 +244,13 @@ def verify_algorithmic(w, n_mean):
 # --------------------------------------------------------------------------
 def oracle_w8(w, x):
     """The oracle's E4M3 codes and scales of W_lm for an 8-bit-head
-    workload (weight preparation, done once, outside the timed sample)."""
+    workload and their dequantized matrix (weight preparation, done once,
+    outside the timed sample, as the CUDA path quantizes W_lm once)."""
     if not w.lm_e4m3:
         return None
     import oracle
-    return oracle.quantize_e4m3_rows(x["w_lm"].float().numpy())
+    codes, scale = oracle.quantize_e4m3_rows(x["w_lm"].float().numpy())
+    return codes, scale, oracle.dequantize_e4m3_rows(codes, scale)
 
 
 def time_oracle(w, x, L, seconds: float, seed: int, w8=None):

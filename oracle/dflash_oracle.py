@@ -200,14 +200,17 @@ def dequantize_e4m3_rows(codes, scale) -> np.ndarray:
     return e4m3_decode(codes) * np.asarray(scale, np.float64)[:, None]
 
 
-def lmhead_topk_e4m3(y, w_codes, w_scale, want_logits=False):
+def lmhead_topk_e4m3(y, w_codes, w_scale, want_logits=False, w_deq=None):
     """The LM head with 8-bit operands: y (the conv output, storage
     values) is quantized per row, W_lm is given as per-row codes and
     scales; U = (s_y q_y)(s_W q_W)^T exactly (float64), then logsumexp and
-    top-16 as in :func:`lmhead_topk`.  Also returns the y codes/scales."""
+    top-16 as in :func:`lmhead_topk`.  Also returns the y codes/scales.
+    ``w_deq``: dequantize_e4m3_rows(w_codes, w_scale), if the caller keeps
+    it (weight preparation done once)."""
     yc, ys = quantize_e4m3_rows(y)
-    out = lmhead_topk(dequantize_e4m3_rows(yc, ys),
-                      dequantize_e4m3_rows(w_codes, w_scale), want_logits)
+    if w_deq is None:
+        w_deq = dequantize_e4m3_rows(w_codes, w_scale)
+    out = lmhead_topk(dequantize_e4m3_rows(yc, ys), w_deq, want_logits)
     return out + (yc, ys)
 
 
@@ -397,14 +400,16 @@ def draft_verify_cycle(h, w_conv, w_lm, w_gate, e_in, e_out, anchor, L,
     h: [B,K,H] drafter hidden states (values of the storage dtype);
     L: [B,K+1,V] target logits.  With ``w_lm_e4m3 = (codes, scale)`` the
     LM head runs on 8-bit operands (:func:`lmhead_topk_e4m3`) and w_lm is
-    unused.  Returns a dict of every intermediate.
+    unused; a third element, if present, is their dequantized matrix.
+    Returns a dict of every intermediate.
     """
     h = np.asarray(h, np.float64)
     B, K, H = h.shape
     y = to_storage(conv2tap(h, w_conv), dtype).astype(np.float64)
     if w_lm_e4m3 is not None:
-        topv, topi, lse, _, _ = lmhead_topk_e4m3(y.reshape(B * K, H),
-                                                 *w_lm_e4m3)
+        topv, topi, lse, _, _ = lmhead_topk_e4m3(
+            y.reshape(B * K, H), w_lm_e4m3[0], w_lm_e4m3[1],
+            w_deq=w_lm_e4m3[2] if len(w_lm_e4m3) > 2 else None)
     else:
         topv, topi, lse = lmhead_topk(y.reshape(B * K, H), w_lm)
     topv = topv.reshape(B, K, C)

@@ -520,3 +520,17 @@ def test_fused_draft_exact_ties_across_strips(lib, e4m3):
         gv = np_(dv.topv)[m]
         assert np.all(gv == gv[0]), f"row {m}: values differ {gv}"
         assert np.array_equal(gi[m], o_i[m]), f"row {m}: {gi[m]} vs {o_i[m]}"
+
+
+@pytest.mark.parametrize("B,K", [(3, 5), (20, 15)])
+def test_bf16_without_conv(lib, B, K):
+    """bf16 storage with no conv (y = h): the tensor-core LM head runs
+    without the shared row maxima (nothing resets them), single CTAs at
+    M = 15 and CTA pairs at M = 300, through the separate calls and
+    through dflash_draft."""
+    w = synth.Workload("noconv", B=B, K=K, V=4099, H=136, r=64,
+                       dtype="bf16", T=1.0, seed=13 + B, w_lm_sd=0.1,
+                       conv_sd=None, sel_sd=0.1, target=("affine", 0.9, 1.0))
+    x, L = _make(w)
+    run_stagewise(lib, w, x, L)
+    run_fused(lib, w, x, L)
