@@ -825,15 +825,20 @@ def lmhead_strips(w, sms=152):
 
 
 def lmhead_kernel_rev() -> str:
-    """Revision tag of the LM-head kernel source (hash of its file), so that
-    a stored ncu traffic figure is only used for the kernel it measured."""
+    """Revision tag of the LM-head kernel source (hash of its files with
+    comments and blank space removed), so that a stored ncu traffic figure
+    is only used for the code it measured."""
     import hashlib
+    import re
     p = os.path.join(ROOT, "block_drafter_verify_gb300", "csrc")
     h = hashlib.sha1()
     for name in sorted(os.listdir(p)):
         if name.startswith("lmhead"):
-            with open(os.path.join(p, name), "rb") as f:
-                h.update(f.read())
+            with open(os.path.join(p, name)) as f:
+                src = f.read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            src = re.sub(r"//[^\n]*", "", src)
+            h.update(" ".join(src.split()).encode())
     return h.hexdigest()[:12]
 
 

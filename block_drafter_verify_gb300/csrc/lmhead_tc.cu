@@ -3,39 +3,49 @@
 // an online logsumexp and the 16 largest logits, so U never reaches HBM.
 // The same kernel also runs with 8-bit operands: E4M3 codes of y and W_lm
 // with one fp32 scale per row each (kind::f8f6f4; a stage then holds 128
-// codes of every row instead of 64 bf16, the same bytes), and the epilogue
-// multiplies each logit by y_scale[m] * w_scale[v] before folding it.
+// codes of every row instead of 64 bf16, the same bytes); the epilogue
+// multiplies each logit by its column's scale and applies the row's scale
+// in the exponent and to the outputs.
 //
 // "Sixteen candidates per position" (DFlash 2: Block diffusion, wearing a
 // drafter's coat) and "A Lightweight Path Selector" (DFlash 2: Keep Drafting
 // Parallel): U_t is the drafter's own logit; 16 candidates are kept per slot.
 //
-// Persistent kernel, one CTA per SM, 192 threads:
-//   warp 0      TMA producer: y tile [128 x 64] and W tile per stage,
-//               128-byte swizzle;
-//   warp 1      MMA issuer (one thread): tcgen05.mma N=256 K=16 into one of
-//               two TMEM accumulators (2 x 256 fp32 columns);
-//   warps 2-5   epilogue: thread = one row (TMEM lane), reads 32 columns at
+// Persistent kernel, one CTA per SM, 64 + 32 * EPI_WARPS threads:
+//   warp 0      TMA producer: y tile [128 rows x 128 bytes] and W tile per
+//               stage, 128-byte swizzle;
+//   warp 1      MMA issuer (one thread): tcgen05.mma N=256 into one of two
+//               TMEM accumulators (2 x 256 fp32 columns);
+//   warps 2..   epilogue: thread = one row (TMEM lane), reads 32 columns at
 //               a time with tcgen05.ld, folds them into (max, sum exp) and a
 //               register-resident sorted top-16, while the MMA fills the
-//               other accumulator.
+//               other accumulator.  Four warps, or eight for the 8-bit pair
+//               variant (two per lane quarter, half of the columns each,
+//               their lists merged at the end).
 // Two variants:
-//   single  (one row tile, M <= 128): W tile [256 x 64] per stage, 4 stages,
-//           M=128 MMAs (cta_group::1);
+//   single  (one row tile, M <= 128): W tile [256 rows] per stage, 4
+//           stages, M=128 MMAs (cta_group::1);
 //   pair    (two or more row tiles): a cluster of two CTAs computes the rows
 //           of two row tiles against one W tile with M=256 MMAs
 //           (cta_group::2).  Each CTA loads its own y tile and one half
-//           [128 x 64] of the W tile, so W crosses L2 -> SM once per pair
-//           instead of once per row tile and a stage is 32 KB: 6 stages.
+//           [128 rows] of the W tile, so W crosses L2 -> SM once per pair
+//           instead of once per row tile and a stage is 32 KB: 6 stages
+//           (5 for the 8-bit variant, whose epilogue needs more room).
 //           The even CTA issues the MMAs; its full barriers count both
 //           CTAs' copies, and its commits arrive on both CTAs' barriers.
 // Unit u (a CTA, or a pair) owns row group (u mod row_groups) and the vocab
 // tiles strip, strip + strips, ... (strip = u / row_groups), so the units
 // that share a vocab tile run it at the same time and W_lm is read from HBM
 // about once.  Each CTA writes one top-16 / (max, sum) partial per row;
-// topk_merge folds them.  Every wait is time-bounded; on a timeout the CTA
-// stops issuing, drains its copies and MMAs, frees TMEM, flags the error
-// word and exits.
+// topk_merge (or the draft tail) folds them.
+// Candidate insertions dominate the epilogue.  They are pruned twice: in a
+// unit's first tile, where the list is empty, by the 16th largest of 32
+// column-group maxima (at least 16 of the tile's values reach it), and in
+// every tile by the running maxima that 16 units of the row group publish
+// in the workspace (16 values of distinct columns, so a value below their
+// minimum cannot make the row's top 16).
+// Every wait is time-bounded; on a timeout the CTA stops issuing, drains
+// its copies and MMAs, frees TMEM, flags the error word and exits.
 #include <algorithm>
 
 #include "kernels.h"
