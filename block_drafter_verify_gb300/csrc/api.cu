@@ -134,7 +134,7 @@ size_t draft_e4m3_ws_layout(int B, int K, int H, int V, void* base,
   return align256(d + c + (size_t)B * K * sizeof(float));
 }
 
-// 8-bit LM-head operands for lmhead_bf16: W_lm as E4M3 codes and row
+// 8-bit LM-head operands for lmhead_tc_path: W_lm as E4M3 codes and row
 // scales, and where to put y's codes and scales.
 struct E4m3Head {
   const uint8_t* w_codes;
@@ -147,15 +147,17 @@ struct E4m3Head {
 // w_gate (and conv_w) the conv launch also writes the pair selector's gate
 // [B*K, r] fp32 to `gate`.  With q8 (and conv_w) y is quantized per row to
 // E4M3 and the LM head runs on the 8-bit operands (w_lm unused).
-dflash_status lmhead_bf16(const __nv_bfloat16* h, const __nv_bfloat16* conv_w,
-                          const __nv_bfloat16* w_lm, int B, int K, int H,
-                          int V, float* topv, int* topi, float* lse, void* ws,
-                          const DeviceState& d, cudaStream_t s,
-                          const __nv_bfloat16* w_gate = nullptr, int r = 0,
-                          float* gate = nullptr, unsigned* tickets = nullptr,
-                          TopkPartials* P_out = nullptr,
-                          int* strips_out = nullptr,
-                          const E4m3Head* q8 = nullptr) {
+dflash_status lmhead_tc_path(const __nv_bfloat16* h,
+                            const __nv_bfloat16* conv_w,
+                            const __nv_bfloat16* w_lm, int B, int K, int H,
+                            int V, float* topv, int* topi, float* lse,
+                            void* ws, const DeviceState& d, cudaStream_t s,
+                            const __nv_bfloat16* w_gate = nullptr, int r = 0,
+                            float* gate = nullptr,
+                            unsigned* tickets = nullptr,
+                            TopkPartials* P_out = nullptr,
+                            int* strips_out = nullptr,
+                            const E4m3Head* q8 = nullptr) {
   void* yv = nullptr;
   TopkPartials P;
   float* row_bound = nullptr;
@@ -317,7 +319,7 @@ dflash_status dflash_lmhead_topk(const void* h, const void* conv_w,
                               static_cast<const float*>(conv_w),
                               static_cast<const float*>(w_lm), B, K, H, V,
                               topv, topi, lse, ws, *d, s);
-  return lmhead_bf16(static_cast<const __nv_bfloat16*>(h),
+  return lmhead_tc_path(static_cast<const __nv_bfloat16*>(h),
                      static_cast<const __nv_bfloat16*>(conv_w),
                      static_cast<const __nv_bfloat16*>(w_lm), B, K, H, V, topv,
                      topi, lse, ws, *d, s);
@@ -409,7 +411,7 @@ dflash_status dflash_draft(const void* h, const void* conv_w, const void* w_lm,
     using bf = __nv_bfloat16;
     TopkPartials P;
     int strips = 0;
-    st = lmhead_bf16(static_cast<const bf*>(h), static_cast<const bf*>(conv_w),
+    st = lmhead_tc_path(static_cast<const bf*>(h), static_cast<const bf*>(conv_w),
                      static_cast<const bf*>(w_lm), B, K, H, V, topv, topi, lse,
                      ws, *d, s, static_cast<const bf*>(w_gate), r, gate,
                      tickets, &P, &strips);
@@ -464,7 +466,7 @@ dflash_status dflash_draft_e4m3(
   using bf = __nv_bfloat16;
   TopkPartials P;
   int strips = 0;
-  st = lmhead_bf16(static_cast<const bf*>(h), static_cast<const bf*>(conv_w),
+  st = lmhead_tc_path(static_cast<const bf*>(h), static_cast<const bf*>(conv_w),
                    nullptr, B, K, H, V, topv, topi, lse, ws, *d, s,
                    static_cast<const bf*>(w_gate), r, gate, tickets, &P,
                    &strips, &q8);
