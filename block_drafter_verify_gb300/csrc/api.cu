@@ -320,9 +320,9 @@ dflash_status dflash_lmhead_topk(const void* h, const void* conv_w,
                               static_cast<const float*>(w_lm), B, K, H, V,
                               topv, topi, lse, ws, *d, s);
   return lmhead_tc_path(static_cast<const __nv_bfloat16*>(h),
-                     static_cast<const __nv_bfloat16*>(conv_w),
-                     static_cast<const __nv_bfloat16*>(w_lm), B, K, H, V, topv,
-                     topi, lse, ws, *d, s);
+                        static_cast<const __nv_bfloat16*>(conv_w),
+                        static_cast<const __nv_bfloat16*>(w_lm), B, K, H, V,
+                        topv, topi, lse, ws, *d, s);
 }
 
 dflash_status dflash_pair_score(const float* topv, const int32_t* topi,
@@ -411,10 +411,11 @@ dflash_status dflash_draft(const void* h, const void* conv_w, const void* w_lm,
     using bf = __nv_bfloat16;
     TopkPartials P;
     int strips = 0;
-    st = lmhead_tc_path(static_cast<const bf*>(h), static_cast<const bf*>(conv_w),
-                     static_cast<const bf*>(w_lm), B, K, H, V, topv, topi, lse,
-                     ws, *d, s, static_cast<const bf*>(w_gate), r, gate,
-                     tickets, &P, &strips);
+    st = lmhead_tc_path(static_cast<const bf*>(h),
+                        static_cast<const bf*>(conv_w),
+                        static_cast<const bf*>(w_lm), B, K, H, V, topv, topi,
+                        lse, ws, *d, s, static_cast<const bf*>(w_gate), r,
+                        gate, tickets, &P, &strips);
     if (st != DFLASH_OK) return st;
     StageTimer tm(kStPair, s);
     return cuda_status(launch_draft_tail<bf>(
@@ -466,10 +467,11 @@ dflash_status dflash_draft_e4m3(
   using bf = __nv_bfloat16;
   TopkPartials P;
   int strips = 0;
-  st = lmhead_tc_path(static_cast<const bf*>(h), static_cast<const bf*>(conv_w),
-                   nullptr, B, K, H, V, topv, topi, lse, ws, *d, s,
-                   static_cast<const bf*>(w_gate), r, gate, tickets, &P,
-                   &strips, &q8);
+  st = lmhead_tc_path(static_cast<const bf*>(h),
+                      static_cast<const bf*>(conv_w), nullptr, B, K, H, V,
+                      topv, topi, lse, ws, *d, s,
+                      static_cast<const bf*>(w_gate), r, gate, tickets, &P,
+                      &strips, &q8);
   if (st != DFLASH_OK) return st;
   StageTimer tm(kStPair, s);
   return cuda_status(launch_draft_tail<bf>(
