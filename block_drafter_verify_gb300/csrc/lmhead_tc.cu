@@ -217,7 +217,10 @@ __device__ __forceinline__ float fold_chunk(const float (&x)[32], float l2e,
     run_s *= tc::ex2_approx((run_m - cm) * l2e);
     run_m = cm;
   }
-  const float nb = -run_m * l2e;
+  // a warp whose columns so far are all beyond V (the second half of a
+  // last tile) still has run_m = -inf: its terms are exactly 0, not
+  // 2^(-inf + inf)
+  const float nb = run_m == -INFINITY ? 0.f : -run_m * l2e;
   float s[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
   for (int i = 0; i < 32; ++i) s[i & 3] += tc::ex2_approx(fmaf(x[i], l2e, nb));

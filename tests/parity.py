@@ -78,7 +78,7 @@ def check_topk(topv, topi, lse, ref, A, c):
     _, o_i, o_lse, U = ref
     M, V = U.shape
     lse_tol = c * A.max(axis=1) + 1e-6 * np.abs(o_lse)
-    bad = np.abs(lse - o_lse) > lse_tol
+    bad = ~(np.abs(lse - o_lse) <= lse_tol)   # NaN counts as bad
     assert not bad.any(), (f"lse rows {np.nonzero(bad)[0][:5]}: "
                            f"{lse[bad][:5]} vs {o_lse[bad][:5]}")
     n = min(C, V)
