@@ -35,6 +35,15 @@ design notes):
   * decisions (ranking, argmax, accept, inverse CDF) compare their operands
     rounded to fp32, the precision the CUDA kernels decide in; the operands
     themselves are computed in float64 from the exact input values.
+  * 8-bit LM head (the pages name quantized drafter builds, not a format):
+    OCP FP8 E4M3 codes with one fp32 scale per row for y and W_lm, scale =
+    max|x| / 448, codes rounded to nearest even and saturated, both
+    divisions in fp32 (the codes are decisions taken in fp32); the logits
+    are the exact products of the dequantized operands.
+  * selector variants (beyond the pages' greedy and sampled walks): the
+    Viterbi walk maximises the sum of pair scores along the path, ties to
+    the lowest slot; recall@16 is measured against the target's first
+    argmax.
 """
 from __future__ import annotations
 
