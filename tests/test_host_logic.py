@@ -1,0 +1,56 @@
+"""Host-side arithmetic of the benchmark and the binding (no GPU): the
+algorithmic byte counts the roofline divides by, the workloads' shapes, and
+the recall/acceptance summary computed from the kernels' flags."""
+import torch
+
+import bench
+import synth
+
+
+def test_lmhead_algorithmic_bytes():
+    by, fl = bench.lmhead_algorithmic(synth.get("b32k8"))
+    # W_lm + y in bf16, top-16 values/ids and lse of 256 rows
+    assert by == 151936 * 2048 * 2 + 256 * 2048 * 2 + 256 * (16 * 8 + 4)
+    assert fl == 2.0 * 256 * 151936 * 2048
+    by8, fl8 = bench.lmhead_algorithmic(synth.get("b32k8e4m3"))
+    # codes of W_lm and y, their fp32 row scales, the same outputs
+    assert by8 == (151936 * 2048 + 256 * 2048 + 256 * (16 * 8 + 4) +
+                   (151936 + 256) * 4)
+    assert fl8 == fl
+
+
+def test_stage_bytes_of_the_fused_cycle():
+    w = synth.get("b32k8")
+    sb = bench.stage_bytes(w, fused=True)
+    assert set(sb) == {"conv+gate", "merge+pair_score+walk", "verify"}
+    assert sb["verify"] == 32 * 9 * 151936 * 4
+    sb8 = bench.stage_bytes(synth.get("b32k8e4m3"), fused=True)
+    assert sb8["quantize_y"] == 256 * 2048 * (2 + 1) + 256 * 4
+
+
+def test_lmhead_strips_match_the_pair_grid():
+    # 256 rows: two row tiles, CTA pairs, 76 pairs in one row group
+    assert bench.lmhead_strips(synth.get("b32k8")) == 76
+    # 8 rows: one row tile, single CTAs, one strip per SM
+    assert bench.lmhead_strips(synth.get("b1k8")) == 152
+
+
+def test_workloads():
+    for name in ("b32k8e4m3", "b32k8cale4m3"):
+        w = synth.get(name)
+        assert w.lm_e4m3 and w.dtype == "bf16" and (w.B, w.K) == (32, 8)
+        assert "E4M3" in synth.describe(w)
+    assert not synth.get("b32k8").lm_e4m3
+    assert bench.aggregate(100, [0.5, 0.4], 2) == (400.0, 0.5)
+    assert bench.rank_seed(2, 0) != bench.rank_seed(2, 1)
+
+
+def test_recall_by_position_on_flags():
+    from block_drafter_verify_gb300 import recall_by_position
+    flags = torch.tensor([[1, 1, 0, 1],
+                          [1, 1, 1, 1],
+                          [0, 1, 1, 1]], dtype=torch.int32)
+    recall, accept = recall_by_position(flags)
+    assert recall.tolist() == [2 / 3, 1.0, 2 / 3, 1.0]
+    # leading runs of candidates that hold the target token: 2, 4, 0
+    assert float(accept) == 2.0
