@@ -137,3 +137,17 @@ def test_draft_e4m3_full_size_b32k8cal(lib):
     x, L = _make(w)
     r = run_e4m3(lib, w, x, L, seed=w.seed, cycle=0)
     print("b32k8cal e4m3 ties", r["ties"], "mean accepted", r["n"].mean())
+
+
+def test_draft_e4m3_vocab_smaller_than_candidates(lib):
+    """V = 10 < 16: every list ends in (-inf, -1) padding, one vocab tile
+    whose columns beyond V take no part (and no unit publishes to most
+    shared-maxima slots)."""
+    w = synth.Workload("v10", B=2, K=3, V=10, H=32, r=8, dtype="bf16",
+                       T=1.0, seed=5, w_lm_sd=0.5, conv_sd=0.05, sel_sd=0.1,
+                       target=("affine", 1.0, 0.3))
+    x, L = _make(w)
+    r = run_e4m3(lib, w, x, L)
+    topi = np_(r["dv"].topi)
+    assert np.all(topi[:, 10:] == -1)
+    assert np.all(np.isneginf(np_(r["dv"].topv)[:, 10:]))

@@ -534,3 +534,15 @@ def test_bf16_without_conv(lib, B, K):
     x, L = _make(w)
     run_stagewise(lib, w, x, L)
     run_fused(lib, w, x, L)
+
+
+def test_vocab_smaller_than_candidates_tensor_cores(lib):
+    """V = 10 < 16 on the bf16 tensor-core path (conv, LM head, draft
+    tail): lists padded with (-inf, -1), scores of padded candidates -inf."""
+    w = synth.Workload("v10bf", B=2, K=3, V=10, H=32, r=8, dtype="bf16",
+                       T=1.0, seed=6, w_lm_sd=0.5, conv_sd=0.05, sel_sd=0.1,
+                       target=("affine", 1.0, 0.3))
+    x, L = _make(w)
+    run_stagewise(lib, w, x, L)
+    r = run_fused(lib, w, x, L)
+    assert np.all(np_(r["dv"].topi)[:, 10:] == -1)
