@@ -48,14 +48,25 @@ enum Stage { kStConv = 0, kStLmhead, kStMerge, kStPair, kStWalk, kStVerifyRows,
              kStQuant, kNumStages };
 cudaEvent_t g_prof[kNumStages][2] = {};
 
+// Inside a stream capture the records become event-record nodes of the
+// graph (cudaEventRecordExternal), so that a replay stamps the events.
+inline void record_stage_event(cudaEvent_t ev, cudaStream_t s) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cs) == cudaSuccess &&
+      cs == cudaStreamCaptureStatusActive)
+    cudaEventRecordWithFlags(ev, s, cudaEventRecordExternal);
+  else
+    cudaEventRecord(ev, s);
+}
+
 struct StageTimer {
   int st;
   cudaStream_t s;
   StageTimer(int stage, cudaStream_t stream) : st(stage), s(stream) {
-    if (g_prof[st][0]) cudaEventRecord(g_prof[st][0], s);
+    if (g_prof[st][0]) record_stage_event(g_prof[st][0], s);
   }
   ~StageTimer() {
-    if (g_prof[st][1]) cudaEventRecord(g_prof[st][1], s);
+    if (g_prof[st][1]) record_stage_event(g_prof[st][1], s);
   }
 };
 

@@ -386,6 +386,8 @@ dflash_status dflash_philox4x32(const uint32_t* ctr, uint64_t seed,
  * In dflash_draft with bf16 storage and a conv, stage 0 is the conv with
  * the context gate and stage 3 the one launch that merges, scores and
  * walks (stages 2 and 4 are not recorded).
+ * Calls captured into a CUDA graph record the events as event-record
+ * nodes (cudaEventRecordExternal), stamped at every replay.
  * Pass NULL for both to stop.  Process-wide host state; set it from the
  * thread that makes the calls, not while other threads call the library.
  * Returns DFLASH_ERR_INVALID_ARG for an unknown stage or a lone NULL. */
