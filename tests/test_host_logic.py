@@ -54,3 +54,27 @@ def test_recall_by_position_on_flags():
     assert recall.tolist() == [2 / 3, 1.0, 2 / 3, 1.0]
     # leading runs of candidates that hold the target token: 2, 4, 0
     assert float(accept) == 2.0
+
+
+def test_reference_arm_prints_one_json_line():
+    """bench.py --impl reference (the oracle on the host cores) keeps the
+    line's contract: metric, value, unit, impl, cpu_baseline and e2e."""
+    import json
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run(
+        [sys.executable, os.path.join(root, "bench.py"), "--impl",
+         "reference", "--config", "tiny", "--steps", "1", "--warmup", "0",
+         "--cpu-seconds", "1"], capture_output=True, text=True, timeout=600,
+        cwd=root)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["value"] > 0
+    assert d["unit"] == "cycles/s" and d["higher_is_better"] is True
+    assert d["cpu_baseline"]["kind"] == "oracle"
+    assert d["e2e"]["h2d_bytes_per_step"] == 0
+    assert d["config"]["workload"] == "tiny"
