@@ -224,6 +224,73 @@ def lmhead_topk_e4m3(y, w_codes, w_scale, want_logits=False, w_deq=None):
 
 
 # --------------------------------------------------------------------------
+# a2 with 4-bit LM-head operands (NVFP4 reading; the CUDA kernel is not
+# built yet).  Elements are E2M1 (1 sign, 2 exponent, 1 mantissa bit:
+# magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6); each block of 16 consecutive
+# elements of a row carries an E4M3 scale, and the whole matrix one fp32
+# scale, so that x ~ g * value(block scale) * value(code).
+# --------------------------------------------------------------------------
+E2M1_MAG = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+NVFP4_BLOCK = 16
+
+
+def e2m1_decode(codes) -> np.ndarray:
+    """Values (float64) of 4-bit E2M1 codes (bit 3 = sign)."""
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    return np.where(c & 8, -1.0, 1.0) * E2M1_MAG[c & 7]
+
+
+def e2m1_encode(x) -> np.ndarray:
+    """Nearest E2M1 code of each finite value, ties to the even code (the
+    one whose mantissa bit is 0), magnitudes beyond 6 saturated to 6, the
+    sign of zero kept."""
+    x = np.asarray(x, dtype=np.float64)
+    if not np.all(np.isfinite(x)):
+        raise ValueError("e2m1_encode: non-finite input")
+    a = np.minimum(np.abs(x), 6.0)
+    d = np.abs(a[..., None] - E2M1_MAG)              # distance to each
+    best = d.min(axis=-1, keepdims=True)
+    tie = np.isclose(d, best, rtol=0, atol=0)        # exact ties only
+    # among equally near codes take the even one (lowest bit 0)
+    pref = np.where(tie, (np.arange(8) & 1) * 8 + np.arange(8), 99)
+    code = np.argmin(pref, axis=-1)
+    return (code | np.where(np.signbit(x), 8, 0)).astype(np.uint8)
+
+
+def quantize_nvfp4_rows(X):
+    """Two-level 4-bit quantization of a matrix [R, H] (H % 16 == 0), in
+    float32 arithmetic: g = max|X| / (448 * 6) (1 for a zero matrix);
+    per block of 16 elements b: scale code s_b = E4M3(max|x_b| / (6 g)),
+    d_b its value; element codes E2M1(x / (d_b * g)) (0 where d_b = 0).
+    Returns (codes uint8 [R, H], block scale codes uint8 [R, H/16], g)."""
+    X = np.asarray(X, dtype=np.float32)
+    R, H = X.shape
+    if H % NVFP4_BLOCK:
+        raise ValueError("H must be a multiple of 16")
+    amax = np.float32(np.abs(X).max()) if X.size else np.float32(0)
+    g = np.float32(amax / np.float32(448.0 * 6.0)) if amax > 0 else \
+        np.float32(1.0)
+    Xb = X.reshape(R, H // NVFP4_BLOCK, NVFP4_BLOCK)
+    bmax = np.abs(Xb).max(axis=2).astype(np.float32)
+    sc = e4m3_encode((bmax / (np.float32(6.0) * g)).astype(np.float32))
+    d = e4m3_decode(sc).astype(np.float32)
+    den = (d * g).astype(np.float32)[..., None]
+    safe = np.where(den > 0, den, np.float32(1.0))
+    q = np.where(den > 0, (Xb / safe).astype(np.float32), np.float32(0.0))
+    codes = e2m1_encode(q).reshape(R, H)
+    return codes, sc, g
+
+
+def dequantize_nvfp4_rows(codes, scale_codes, g) -> np.ndarray:
+    """value(code) * value(block scale) * g in float64."""
+    codes = np.asarray(codes)
+    R, H = codes.shape
+    d = e4m3_decode(scale_codes) * np.float64(g)
+    return (e2m1_decode(codes).reshape(R, H // NVFP4_BLOCK, NVFP4_BLOCK) *
+            d[..., None]).reshape(R, H)
+
+
+# --------------------------------------------------------------------------
 # a3: context gate + low-rank bilinear pair scores
 # --------------------------------------------------------------------------
 def gate(h: np.ndarray, w_gate: np.ndarray) -> np.ndarray:

@@ -714,3 +714,71 @@ def test_lmhead_e4m3_equals_the_exact_product_of_the_codes():
         assert np.array_equal(U[:, v], exact)
     order = np.argsort(-U[0].astype(np.float32), kind="stable")[:16]
     assert np.array_equal(topi[0], order)
+
+
+# --------------------------------------------------------------------------
+# 4-bit operands (NVFP4 reading): the E2M1 codec in closed form and the
+# two-level scaling
+def test_e2m1_decode_table():
+    v = oracle.e2m1_decode(np.arange(16, dtype=np.uint8))
+    mags = [0, 0.5, 1, 1.5, 2, 3, 4, 6]
+    # exponent field e (2 bits), mantissa m (1 bit): e = 0 is subnormal
+    # (m * 0.5), else (1 + m/2) * 2^(e-1)
+    for c in range(8):
+        e, m = c >> 1, c & 1
+        closed = m * 0.5 if e == 0 else (1 + m / 2) * 2.0 ** (e - 1)
+        assert v[c] == closed == mags[c]
+        assert v[c | 8] == -closed
+    assert np.signbit(v[8])
+
+
+def test_e2m1_encode_nearest_ties_to_even_and_saturation():
+    mags = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6])
+    # brute force: the nearest magnitude, ties to the code with mantissa 0
+    xs = np.concatenate([np.linspace(-8, 8, 3201), (mags[1:] + mags[:-1]) / 2,
+                         -(mags[1:] + mags[:-1]) / 2])
+    got = oracle.e2m1_encode(xs)
+    for x, c in zip(xs, got):
+        a = min(abs(x), 6.0)
+        d = np.abs(mags - a)
+        cand = np.nonzero(d == d.min())[0]
+        even = [k for k in cand if k % 2 == 0]
+        k = even[0] if even else cand[0]
+        assert (c & 7) == k, (x, c)
+        assert bool(c & 8) == bool(np.signbit(x)), (x, c)
+
+
+def test_nvfp4_two_level_scales():
+    rng = np.random.default_rng(8)
+    X = (rng.standard_normal((6, 64)) * np.exp2(rng.uniform(
+        -6, 6, size=(6, 4)).repeat(16, axis=1))).astype(np.float32)
+    X[2, 16:32] = 0.0                                  # an all-zero block
+    codes, sc, g = oracle.quantize_nvfp4_rows(X)
+    assert codes.shape == (6, 64) and sc.shape == (6, 4)
+    assert g == np.float32(np.abs(X).max()) / np.float32(448 * 6)
+    assert sc[2, 1] == 0 and np.all(codes[2, 16:32] == 0)
+    D = oracle.dequantize_nvfp4_rows(codes, sc, g)
+    # each element within half of E2M1's widest gap (2 at the top) of its
+    # block's scale, plus the block scale's own E4M3 rounding
+    d = oracle.e4m3_decode(sc) * np.float64(g)
+    bound = np.repeat(d, 16, axis=1) * 1.0 + 1e-30
+    assert np.all(np.abs(D - X) <= bound)
+    # the largest element of a block maps to 4 or 6 (the scale is rounded
+    # to E4M3, so the block maximum lands within 1/16 of 6)
+    Xb = np.abs(X.reshape(6, 4, 16))
+    top = np.take_along_axis(codes.reshape(6, 4, 16) & 7,
+                             Xb.argmax(axis=2)[..., None], axis=2)[..., 0]
+    nz = Xb.max(axis=2) > 0
+    assert np.all(np.isin(top[nz], [6, 7]))
+
+
+def test_nvfp4_exact_closed_form():
+    """A matrix whose blocks are E2M1 values times a power of two scale is
+    reproduced exactly: g and the block scales divide out."""
+    vals = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6, -6, -4, -3, -2, -1.5, -1,
+                     -0.5, 0], np.float32)
+    X = np.stack([vals * np.float32(2.0 ** k) for k in (-3, 0, 5)])
+    X = np.concatenate([X, X], axis=1)                 # two blocks per row
+    codes, sc, g = oracle.quantize_nvfp4_rows(X)
+    D = oracle.dequantize_nvfp4_rows(codes, sc, g)
+    assert np.allclose(D, X, rtol=1e-6, atol=0)
