@@ -290,6 +290,19 @@ def dequantize_nvfp4_rows(codes, scale_codes, g) -> np.ndarray:
             d[..., None]).reshape(R, H)
 
 
+def lmhead_topk_nvfp4(y, w_codes, w_scale_codes, w_g, want_logits=False):
+    """The LM head with 4-bit operands: y (the conv output) quantized by
+    :func:`quantize_nvfp4_rows`, W_lm given in the same form; U is the
+    exact product of the dequantized operands (float64), then logsumexp
+    and top-16 as in :func:`lmhead_topk`.  Also returns y's codes, block
+    scale codes and matrix scale."""
+    yc, ysc, yg = quantize_nvfp4_rows(y)
+    out = lmhead_topk(dequantize_nvfp4_rows(yc, ysc, yg),
+                      dequantize_nvfp4_rows(w_codes, w_scale_codes, w_g),
+                      want_logits)
+    return out + (yc, ysc, yg)
+
+
 # --------------------------------------------------------------------------
 # a3: context gate + low-rank bilinear pair scores
 # --------------------------------------------------------------------------

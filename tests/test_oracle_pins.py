@@ -782,3 +782,20 @@ def test_nvfp4_exact_closed_form():
     codes, sc, g = oracle.quantize_nvfp4_rows(X)
     D = oracle.dequantize_nvfp4_rows(codes, sc, g)
     assert np.allclose(D, X, rtol=1e-6, atol=0)
+
+
+def test_lmhead_nvfp4_equals_the_product_of_exact_operands():
+    """Operands built from E2M1 values (one block of 16 per row, scales that
+    divide out) are reproduced exactly, so U is their plain product."""
+    vals = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6, -6, -4, -3, -2, -1.5, -1,
+                     -0.5, 0], np.float32)
+    y = np.stack([np.roll(vals, k) for k in range(3)])          # [3, 16]
+    W = np.stack([np.roll(vals, 2 * k + 1) * np.float32(0.5 ** (k % 3))
+                  for k in range(40)])                          # [40, 16]
+    wc, wsc, wg = oracle.quantize_nvfp4_rows(W)
+    topv, topi, lse, U, yc, ysc, yg = oracle.lmhead_topk_nvfp4(
+        y, wc, wsc, wg, want_logits=True)
+    exact = y.astype(np.float64) @ W.astype(np.float64).T
+    assert np.allclose(U, exact, rtol=1e-6, atol=1e-9)
+    order = np.argsort(-U[0].astype(np.float32), kind="stable")[:16]
+    assert np.array_equal(topi[0], order)
