@@ -27,7 +27,26 @@ import sys
 import tempfile
 import time
 
-import numpy as np
+
+def _set_blas_threads(argv):
+    """The oracle's BLAS thread count, fixed before numpy loads: the value
+    after --oracle-threads, else every host core for the oracle runs
+    (--impl reference, --oracle-sample)."""
+    n = None
+    if "--oracle-threads" in argv:
+        n = argv[argv.index("--oracle-threads") + 1]
+    elif "reference" in argv or "--oracle-sample" in argv:
+        n = str(os.cpu_count())
+    if n is not None:
+        for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS",
+                    "MKL_NUM_THREADS"):
+            os.environ[var] = n
+
+
+if __name__ == "__main__":
+    _set_blas_threads(sys.argv)
+
+import numpy as np  # noqa: E402
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
@@ -52,6 +71,11 @@ def parse(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="bounded CPU work for the oracle baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--oracle-sample", action="store_true",
+                    help="(internal) time the oracle on a sample of the "
+                         "workload and print its JSON; run as a child "
+                         "process so that its thread count is its own")
+    ap.add_argument("--oracle-threads", type=int, default=None)
     ap.add_argument("--sweep", default=None,
                     help="time the sweep grid instead (one JSON line per "
                          "point): 'all' or a comma list of point names")
@@ -216,6 +240,14 @@ def synth_target_torch(w, x, dev):
     return synth.target_logits(w, d)
 
 
+def bench_config(w, world: int) -> dict:
+    """The workload as both arms report it (same keys and values)."""
+    return {"workload": w.name, "B": w.B, "K": w.K, "V": w.V, "H": w.H,
+            "r": w.r, "T": w.T, "parallelism": f"replicas x{world}",
+            "l2": "inputs larger than L2 (W_lm streamed each cycle)",
+            "recipe": synth.describe(w)}
+
+
 # --------------------------------------------------------------------------
 # algorithmic bytes and flops per launch
 # --------------------------------------------------------------------------
@@ -233,10 +265,12 @@ def lmhead_algorithmic(w):
 
 
 def verify_algorithmic(w, n_mean):
-    """Bytes the verify needs: target rows 0..n of each sequence, the draw
-    row once more, plus the small draft arrays."""
-    rows_needed = w.B * (n_mean + 1)
-    return rows_needed * w.V * 4 * (2 if w.T > 0 else 1) + w.M * C * 8
+    """Bytes the verify needs: target rows 0..n of each sequence (n
+    accepted drafts), at T > 0 the draw row once more (the inverse CDF
+    walks it after its total is known), plus the drafts, candidates and
+    q."""
+    rows = w.B * (n_mean + 1) + (w.B if w.T > 0 else 0)
+    return rows * w.V * 4 + w.M * C * 8 + w.M * 4
 
 
 # --------------------------------------------------------------------------
@@ -276,9 +310,69 @@ def time_oracle(w, x, L, seconds: float, seed: int, w8=None):
             break
     seq_per_s = done / el
     return {"value": seq_per_s / w.B, "unit": UNIT,
-            "cores": os.cpu_count(), "kind": "oracle",
+            "cores": oracle_threads(), "kind": "oracle",
             "sample": (f"{done} of {w.B} sequences of one cycle ({el:.1f} s, "
                        f"float64 numpy; cycles/s = sequences/s / B)")}
+
+
+def oracle_threads() -> int:
+    """Threads the oracle's BLAS runs on in this process (set by
+    _set_blas_threads before numpy loaded; else every core)."""
+    v = os.environ.get("OPENBLAS_NUM_THREADS")
+    return int(v) if v and v.isdigit() else os.cpu_count()
+
+
+def reference_inputs(w):
+    """The workload's inputs, with the target logits of the first
+    sequences (those a bounded sample reaches) from the oracle's own
+    drafter logits; the rest of the target rows are zero."""
+    import oracle
+    x = synth.make_inputs(w)
+    f64 = lambda t: None if t is None else t.float().numpy().astype(np.float64)
+    nseq = max(1, min(w.B, 4))
+    h = f64(x["h"][:nseq])
+    y = oracle.to_storage(oracle.conv2tap(h, f64(x["w_conv"])), w.dtype)
+    _, _, _, U = oracle.lmhead_topk(
+        y.reshape(-1, w.H).astype(np.float64), f64(x["w_lm"]),
+        want_logits=True)
+    d = np.zeros((w.B, w.K + 1, w.V), np.float32)
+    d[:nseq] = U.reshape(nseq, w.K + 1, w.V)
+    return x, synth.target_logits(w, d)
+
+
+def run_oracle_sample(args):
+    """Child process of the CPU baseline: the oracle on a bounded sample of
+    the workload, with its own BLAS thread count; prints one JSON dict."""
+    w = synth.get(args.config)
+    x, L = reference_inputs(w)
+    r = time_oracle(w, x, L, args.cpu_seconds, w.seed, oracle_w8(w, x))
+    print(json.dumps(r))
+    return 0
+
+
+def cpu_baseline(args):
+    """The oracle timed on the host cores in child processes: all cores
+    (the reported value) and one thread."""
+    out = {}
+    for name, n in (("all", os.cpu_count()), ("one", 1)):
+        cmd = [sys.executable, os.path.abspath(__file__), "--oracle-sample",
+               "--config", args.config, "--cpu-seconds",
+               str(args.cpu_seconds / 2), "--oracle-threads", str(n)]
+        env = dict(os.environ)
+        for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS",
+                    "MKL_NUM_THREADS"):
+            env[var] = str(n)
+        try:
+            r = subprocess.run(cmd, capture_output=True, text=True,
+                               env=env, timeout=600)
+            out[name] = json.loads(r.stdout.strip().splitlines()[-1])
+        except (subprocess.SubprocessError, ValueError, IndexError) as exc:
+            out[name] = {"error": str(exc)[:200]}
+    res = dict(out["all"])
+    res["single_thread"] = out["one"]
+    res["threads_how"] = ("BLAS threads fixed by OPENBLAS_NUM_THREADS / "
+                          "OMP_NUM_THREADS in a child process")
+    return res
 
 
 # --------------------------------------------------------------------------
@@ -289,20 +383,7 @@ def run_reference(args):
     if rank != 0:
         return 0
     w = synth.get(args.config)
-    x = synth.make_inputs(w)
-    import oracle
-    from oracle import dflash_oracle as _o  # noqa: F401
-    f64 = lambda t: None if t is None else t.float().numpy().astype(np.float64)
-    h_all = f64(x["h"])
-    y = oracle.to_storage(oracle.conv2tap(h_all, f64(x["w_conv"])), w.dtype)
-    # the target logits of the sampled sequences only
-    nseq = max(1, min(w.B, 2))
-    _, _, _, U = oracle.lmhead_topk(
-        y[:nseq].reshape(-1, w.H).astype(np.float64), f64(x["w_lm"]),
-        want_logits=True)
-    d = np.zeros((w.B, w.K + 1, w.V), np.float32)
-    d[:nseq] = U.reshape(nseq, w.K + 1, w.V)
-    L = synth.target_logits(w, d)
+    x, L = reference_inputs(w)
     per = max(2.0, args.cpu_seconds / max(1, args.steps + args.warmup))
     w8 = oracle_w8(w, x)
     for _ in range(args.warmup):
@@ -313,8 +394,7 @@ def run_reference(args):
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 / v, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": w.name,
-                                            "recipe": synth.describe(w)},
+            "data": "synthetic", "config": bench_config(w, ws),
             "cpu_baseline": {"value": v, "unit": UNIT,
                              "cores": vals[0]["cores"], "kind": "oracle",
                              "sample": vals[0]["sample"]},
@@ -427,8 +507,8 @@ def run_sweep(args):
                 "V": w.V, "H": w.H, "cycles_per_s": 1e3 / ms,
                 "ms_per_cycle": ms, "mean_accepted": n_sum / (5 * w.B),
                 "stage_us": stage_us,
-        "stage_us_eager": stage_us_eager,
-        "stage_timing": stage_timing, "lmhead": lm,
+                "stage_timing": "events around each kernel, 5 eager cycles",
+                "lmhead": lm,
                 "stage_hbm_frac": {k: sb[k] / (stage_us[k] * 1e-6) / 1e9 /
                                    pk["hbm_gbs"] for k in sb
                                    if k in stage_us},
@@ -694,6 +774,18 @@ def run_ours(args):
             gbs = nbytes / (stage_us[name] * 1e-6) / 1e9
             stage_roof[name] = {"bytes": nbytes, "GB/s": gbs,
                                 "frac": gbs / pk["hbm_gbs"]}
+    if "verify" in stage_roof:
+        # the design reads every target row; the algorithm needs rows
+        # 0..n of each sequence (n accepted drafts) and the draw row again
+        vb = verify_algorithmic(w, n_mean_cycles)
+        vgbs = vb / (stage_us["verify"] * 1e-6) / 1e9
+        stage_roof["verify"].update({
+            "design_bytes": stage_roof["verify"]["bytes"],
+            "algorithmic_bytes": vb, "algorithmic_GB/s": vgbs,
+            "frac_algorithmic": vgbs / pk["hbm_gbs"],
+            "note": "frac is of the bytes the design reads (all B*(K+1) "
+                    "target rows); frac_algorithmic of the rows the "
+                    "accepted lengths need"})
 
     # end to end through the public API with host buffers
     e2e_steps = args.e2e_steps or max(3, min(K, 20))
@@ -702,20 +794,35 @@ def run_ours(args):
     L_host = L_cpu.pin_memory()
     n_host = torch.empty(w.B, dtype=torch.int32).pin_memory()
     o_host = torch.empty(w.B, w.K + 1, dtype=torch.int32).pin_memory()
-    h_d, a_d, L_d = torch.empty_like(h), torch.empty_like(anchor), \
-        torch.empty_like(L)
+    # two sets of device inputs: the copies of step i + 1 (on their own
+    # stream) run while step i computes; a set is refilled only after the
+    # cycle that read it
+    bufs = [(torch.empty_like(h), torch.empty_like(anchor),
+             torch.empty_like(L)) for _ in range(2)]
+    copy_s = torch.cuda.Stream(dev)
+    copied = [torch.cuda.Event() for _ in range(2)]
+    freed = [torch.cuda.Event() for _ in range(2)]
     barrier()
     torch.cuda.synchronize(dev)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
+    copy_s.wait_stream(stream)
     for i in range(e2e_steps):
-        h_d.copy_(h_host, non_blocking=True)
-        a_d.copy_(a_host, non_blocking=True)
-        L_d.copy_(L_host, non_blocking=True)
+        j = i % 2
+        h_d, a_d, L_d = bufs[j]
+        with torch.cuda.stream(copy_s):
+            if i >= 2:
+                copy_s.wait_event(freed[j])
+            h_d.copy_(h_host, non_blocking=True)
+            a_d.copy_(a_host, non_blocking=True)
+            L_d.copy_(L_host, non_blocking=True)
+            copied[j].record(copy_s)
+        stream.wait_event(copied[j])
         n, out = dv.cycle(h_d, a_d, L_d, w.T, seed, 10**6 + i)
         n_host.copy_(n, non_blocking=True)
         o_host.copy_(out, non_blocking=True)
+        freed[j].record(stream)
     e1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_secs = max_over_ranks(e0.elapsed_time(e1) / 1e3, dev)
@@ -726,8 +833,7 @@ def run_ours(args):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = time_oracle(w, x, L_cpu, args.cpu_seconds, seed,
-                          oracle_w8(w, x))
+        cpu = cpu_baseline(args)
 
     if world > 1:
         import torch.distributed as dist
@@ -746,13 +852,9 @@ def run_ours(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": w.dtype + ("+e4m3 LM head" if w.lm_e4m3 else ""),
         "data": "synthetic",
-        "config": {"workload": w.name, "B": w.B, "K": w.K, "V": w.V,
-                   "H": w.H, "r": w.r, "T": w.T, "parallelism":
-                   f"replicas x{world}",
-                   "l2": "inputs larger than L2 (W_lm streamed each cycle)",
-                   "timing": ("CUDA graph replay of the K cycles" if use_graph
-                              else "eager calls: " + graph_error),
-                   "recipe": synth.describe(w)},
+        "config": bench_config(w, world),
+        "timing": ("CUDA graph replay of the K cycles" if use_graph
+                   else "eager calls: " + graph_error),
         "verified_tokens_per_s": value * w.B * (n_mean + 1),
         "mean_accepted": n_mean,
         "mean_emitted": n_mean + 1,
@@ -765,7 +867,10 @@ def run_ours(args):
         "stage_roofline": stage_roof,
         "clocks": clk.summary(),
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                "h2d_GB/s": h2d * e2e_steps / e2e_secs / 1e9,
+                "overlap": "inputs of the next cycle copied on a second "
+                           "stream (double-buffered) while the cycle runs"},
         "gpu_launches": launches_per_step * K,
         "roofline": roof,
         "cpu_baseline": cpu,
@@ -883,6 +988,8 @@ def lmhead_kernel_rev() -> str:
 
 def main(argv=None):
     args = parse(argv)
+    if args.oracle_sample:
+        return run_oracle_sample(args)
     if args.impl == "reference":
         return run_reference(args)
     if args.sweep:

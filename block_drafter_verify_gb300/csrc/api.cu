@@ -273,6 +273,35 @@ dflash_status current_device_info(int* sms, int** err) {
   *err = d->err;
   return DFLASH_OK;
 }
+
+// The checks dflash_verify and dflash_verify_noalloc share (everything but
+// the scratch memory): pointers, sizes, temperature, alignment.
+bool verify_args_ok(const float* target_logits, const int32_t* draft,
+                    const int32_t* topi, const float* q, int B, int K, int V,
+                    float T, const int32_t* n_accepted,
+                    const int32_t* out_tok) {
+  return target_logits && draft && topi && q && n_accepted && out_tok &&
+         sizes_ok(B, K, 0, V) && T >= 0.f && T < INFINITY &&
+         aligned(target_logits, 16);
+}
+
+// Zero the tickets of workspace w, then launch the verify kernel on the
+// current device, inside the verify stage's profiling events.
+dflash_status verify_run(const float* target_logits, const int32_t* draft,
+                         const int32_t* topi, const float* q, int B, int K,
+                         int V, float T, uint64_t seed, uint64_t cycle,
+                         int32_t* n_accepted, int32_t* out_tok,
+                         const VerifyWs& w, cudaStream_t s) {
+  DeviceState* d = nullptr;
+  dflash_status st = device_state(&d);
+  if (st != DFLASH_OK) return st;
+  if (cudaMemsetAsync(w.counters, 0, w.counter_bytes, s) != cudaSuccess)
+    return DFLASH_ERR_CUDA;
+  StageTimer tm(kStVerifyRows, s);
+  return cuda_status(launch_verify(target_logits, draft, topi, q, B, K, V, T,
+                                   seed, cycle, n_accepted, out_tok, w, d->sms,
+                                   d->err, s));
+}
 }  // namespace dflash
 
 extern "C" {
@@ -496,23 +525,15 @@ dflash_status dflash_verify(const float* target_logits, const int32_t* draft,
                             int V, float T, uint64_t seed, uint64_t cycle,
                             int32_t* n_accepted, int32_t* out_tok, void* ws,
                             size_t ws_bytes, dflash_stream_t stream) {
-  REQUIRE(target_logits && draft && topi && q && n_accepted && out_tok && ws);
-  REQUIRE(sizes_ok(B, K, 0, V));
-  REQUIRE(T >= 0.f && T < INFINITY);
-  REQUIRE(aligned(ws, 256) && aligned(target_logits, 16));
+  REQUIRE(verify_args_ok(target_logits, draft, topi, q, B, K, V, T,
+                         n_accepted, out_tok));
+  REQUIRE(ws && aligned(ws, 256));
   REQUIRE(ws_bytes >= verify_ws_layout(B, K, V, nullptr, nullptr));
-  DeviceState* d = nullptr;
-  dflash_status st = device_state(&d);
-  if (st != DFLASH_OK) return st;
   VerifyWs w;
   verify_ws_layout(B, K, V, ws, &w);
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(w.counters, 0, w.counter_bytes, s) != cudaSuccess)
-    return DFLASH_ERR_CUDA;
-  StageTimer tm(kStVerifyRows, s);
-  return cuda_status(launch_verify(target_logits, draft, topi, q, B, K, V, T,
-                                   seed, cycle, n_accepted, out_tok, w, d->sms,
-                                   d->err, s));
+  return verify_run(target_logits, draft, topi, q, B, K, V, T, seed, cycle,
+                    n_accepted, out_tok, w,
+                    reinterpret_cast<cudaStream_t>(stream));
 }
 
 dflash_status dflash_philox4x32(const uint32_t* ctr, uint64_t seed,

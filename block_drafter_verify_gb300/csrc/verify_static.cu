@@ -32,8 +32,18 @@
 
 namespace dflash {
 
-// SM count and device error word of the current device (api.cu).
-dflash_status current_device_info(int* sms, int** err);
+// Shared with dflash_verify (api.cu): the argument checks other than the
+// scratch memory, and the launch (tickets zeroed, profiling events of the
+// verify stage).
+bool verify_args_ok(const float* target_logits, const int32_t* draft,
+                    const int32_t* topi, const float* q, int B, int K, int V,
+                    float T, const int32_t* n_accepted,
+                    const int32_t* out_tok);
+dflash_status verify_run(const float* target_logits, const int32_t* draft,
+                         const int32_t* topi, const float* q, int B, int K,
+                         int V, float T, uint64_t seed, uint64_t cycle,
+                         int32_t* n_accepted, int32_t* out_tok,
+                         const VerifyWs& w, cudaStream_t s);
 
 namespace {
 
@@ -62,10 +72,6 @@ dflash_status scratch_address(void** out) {
   return DFLASH_OK;
 }
 
-inline bool aligned16(const void* p) {
-  return (reinterpret_cast<uintptr_t>(p) & 15) == 0;
-}
-
 }  // namespace
 }  // namespace dflash
 
@@ -75,29 +81,18 @@ extern "C" dflash_status dflash_verify_noalloc(
     uint64_t cycle, int32_t* n_accepted, int32_t* out_tok,
     dflash_stream_t stream) {
   using namespace dflash;
-  if (!(target_logits && draft && topi && q && n_accepted && out_tok))
-    return DFLASH_ERR_INVALID_ARG;
-  if (B < 1 || K < 1 || K > DFLASH_MAX_K || V < 1 || (long long)B * K > (1 << 20))
-    return DFLASH_ERR_INVALID_ARG;
-  if (!(T >= 0.f && T < INFINITY) || !aligned16(target_logits))
+  if (!verify_args_ok(target_logits, draft, topi, q, B, K, V, T, n_accepted,
+                      out_tok))
     return DFLASH_ERR_INVALID_ARG;
   // sizes whose scratch does not fit the fixed array are refused
   if (verify_ws_layout(B, K, V, nullptr, nullptr) > kStaticScratchBytes)
     return DFLASH_ERR_UNSUPPORTED;
-  int sms = 0;
-  int* err = nullptr;
-  dflash_status st = current_device_info(&sms, &err);
-  if (st != DFLASH_OK) return st;
   void* base = nullptr;
-  st = scratch_address(&base);
+  const dflash_status st = scratch_address(&base);
   if (st != DFLASH_OK) return st;
   VerifyWs w;
   verify_ws_layout(B, K, V, base, &w);
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(w.counters, 0, w.counter_bytes, s) != cudaSuccess)
-    return DFLASH_ERR_CUDA;
-  const cudaError_t e =
-      launch_verify(target_logits, draft, topi, q, B, K, V, T, seed, cycle,
-                    n_accepted, out_tok, w, sms, err, s);
-  return e == cudaSuccess ? DFLASH_OK : DFLASH_ERR_CUDA;
+  return verify_run(target_logits, draft, topi, q, B, K, V, T, seed, cycle,
+                    n_accepted, out_tok, w,
+                    reinterpret_cast<cudaStream_t>(stream));
 }

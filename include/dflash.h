@@ -285,14 +285,15 @@ dflash_status dflash_verify(const float* target_logits, const int32_t* draft,
  * callers with no allocator of their own.  This entry point has no
  * counterpart in the pages; it exists for those callers only.
  *
- * Same arguments, semantics and results as dflash_verify, minus ws and
- * ws_bytes.  The scratch is a fixed 4 MiB array the library holds in device
- * memory on every GPU that loads it, until the process exits; sizes whose
- * scratch (dflash_workspace_bytes(1, B, K, 0, V)) exceeds 4 MiB are refused
- * with DFLASH_ERR_UNSUPPORTED (B = 256 with K = 16 fits; B = 512 with
- * K = 16 does not).  The first call on a device looks up the array's device
- * address
- * (so make that first call before any stream capture).  All calls share the
+ * Same arguments, checks, semantics, results and profiling stage as
+ * dflash_verify, minus ws and ws_bytes.  The scratch is a fixed 4 MiB array
+ * the library holds in device memory on every GPU that loads it, until the
+ * process exits; sizes whose scratch, dflash_workspace_bytes(1, B, K, 0, V)
+ * (about B*(K+1)*ceil(V/2048)*8 bytes), exceeds 4 MiB are refused with
+ * DFLASH_ERR_UNSUPPORTED.  At V = 151936, B = 256 with K = 16 fits (2.7 MB)
+ * and K = 16 fits up to B = 402; at V = 262144, B = 256 fits up to K = 14.
+ * The first call on a device looks up the array's device address (so make
+ * that first call before any stream capture).  All calls share the
  * array: each clears what must start at zero itself, and calls whose
  * kernels overlap on the GPU (several streams or threads on one device)
  * race on it and must be serialised by the caller.  Allocates nothing.

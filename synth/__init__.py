@@ -155,9 +155,34 @@ def _normal(seed, tensor, shape, sd, dtype) -> torch.Tensor:
     return t.to(torch.bfloat16) if dtype == "bf16" else t
 
 
-def make_inputs(w: Workload) -> dict:
-    """All drafter-side inputs of workload ``w`` as CPU torch tensors."""
+def make_inputs(w: Workload, tensors=None) -> dict:
+    """All drafter-side inputs of workload ``w`` as CPU torch tensors (only
+    the names in ``tensors``, if given; the others are None).  Each tensor
+    has its own stream, so a subset draws exactly the same values."""
     B, K, V, H, r = w.B, w.K, w.V, w.H, w.r
+    if tensors is not None:
+        want = set(tensors)
+        full = {}
+        if "h" in want:
+            full["h"] = _normal(w.seed, "h", (B, K + 1, H), 1.0, w.dtype)
+        if "w_lm" in want:
+            full["w_lm"] = _normal(w.seed, "w_lm", (V, H), w.w_lm_sd,
+                                   w.dtype)
+        if "w_gate" in want:
+            full["w_gate"] = _normal(w.seed, "w_gate", (r, H), w.sel_sd,
+                                     w.dtype)
+        for name in ("e_in", "e_out"):
+            if name in want:
+                full[name] = _normal(w.seed, name, (V, r), w.sel_sd, w.dtype)
+        if "anchor" in want:
+            full["anchor"] = torch.from_numpy(
+                _rng(w.seed, "anchor").integers(0, V, size=B).astype(
+                    np.int32))
+        if "w_conv" in want and w.conv_sd is not None:
+            full["w_conv"] = _normal(w.seed, "w_conv", (2 * H, H),
+                                     w.conv_sd, w.dtype)
+        return {k: full.get(k) for k in ("h", "w_lm", "w_gate", "e_in",
+                                         "e_out", "anchor", "w_conv")}
     out = {
         "h": _normal(w.seed, "h", (B, K + 1, H), 1.0, w.dtype),
         "w_lm": _normal(w.seed, "w_lm", (V, H), w.w_lm_sd, w.dtype),

@@ -107,12 +107,18 @@ def check_scores(S_gpu, S_ref, rtol=1e-5, atol=1e-5):
     np.testing.assert_allclose(g[~inf_g], S_ref[~inf_o], rtol=rtol, atol=atol)
 
 
-def check_walk(slot, draft, q, S32, topi, T, seed, cycle, eps):
+def check_walk(slot, draft, q, S32, topi, T, seed, cycle, eps, bidx=None):
     """Oracle walk on the CUDA scores; identical slots except near-ties
-    (after which the rest of that sequence is not comparable)."""
+    (after which the rest of that sequence is not comparable).  ``bidx``:
+    the batch indices of the given sequences (their Philox streams), when
+    they are a sample of a larger batch."""
     slot, draft, q = np_(slot), np_(draft), np_(q)
     B, K = slot.shape
-    u = philox.walk_uniforms(seed, cycle, B, K) if T > 0 else None
+    u = None
+    if T > 0:
+        bi = np.arange(B) if bidx is None else np.asarray(bidx)
+        u = philox.uniforms(seed, cycle, bi[:, None], np.arange(K)[None, :],
+                            philox.PURPOSE_WALK)
     o_slot, o_draft, o_q, margin = oracle.path_walk(S32, topi, T, u)
     ties = 0
     for b in range(B):
@@ -129,14 +135,19 @@ def check_walk(slot, draft, q, S32, topi, T, seed, cycle, eps):
     return ties
 
 
-def check_verify(n, out, L, draft, topi, q, T, seed, cycle):
+def check_verify(n, out, L, draft, topi, q, T, seed, cycle, bidx=None):
     """Oracle verify on the CUDA drafts; identical n and tokens except at
-    near-tie accept tests or draws."""
+    near-tie accept tests or draws.  ``bidx`` as in check_walk."""
     n, out = np_(n), np_(out)
     B, K1, V = L.shape
     K = K1 - 1
-    ua = philox.accept_uniforms(seed, cycle, B, K) if T > 0 else None
-    ur = philox.resample_uniforms(seed, cycle, B, K) if T > 0 else None
+    ua = ur = None
+    if T > 0:
+        bi = np.arange(B) if bidx is None else np.asarray(bidx)
+        ua = philox.uniforms(seed, cycle, bi[:, None], np.arange(K)[None, :],
+                             philox.PURPOSE_ACCEPT)
+        ur = philox.uniforms(seed, cycle, bi, np.full(B, K),
+                             philox.PURPOSE_RESAMPLE)
     o_n, o_out, mg = oracle.verify(L, draft, topi, q, T, ua, ur)
     ties = 0
     for b in range(B):

@@ -105,3 +105,52 @@ def test_argument_checks_come_before_any_device_work(so):
     c = so.dflash_commit
     c.restype, c.argtypes = i32, [vp, vp, i32, i32, vp, vp, vp, i32, vp, vp]
     assert c(fake, fake, 2, 4, fake, fake, fake, 0, fake, None) == 1  # cap 0
+
+
+def test_noalloc_verify_refuses_bad_arguments_on_the_host(so):
+    """dflash_verify_noalloc shares dflash_verify's host-side checks: a
+    null pointer, T < 0, target logits not 16-byte aligned and K > 16 are
+    refused before any device work (no GPU needed)."""
+    vp, i32, f32, u64 = (ctypes.c_void_p, ctypes.c_int, ctypes.c_float,
+                         ctypes.c_uint64)
+    fake = ctypes.c_void_p(0x100000)
+    f = so.dflash_verify_noalloc
+    f.restype = i32
+    f.argtypes = [vp, vp, vp, vp, i32, i32, i32, f32, u64, u64, vp, vp, vp]
+    ok = [fake, fake, fake, fake, 2, 4, 100, 1.0, 1, 0, fake, fake, None]
+
+    def call(**kw):
+        a = list(ok)
+        for k, v in kw.items():
+            a[{"L": 0, "draft": 1, "topi": 2, "q": 3, "B": 4, "K": 5,
+               "V": 6, "T": 7, "n": 10, "out": 11}[k]] = v
+        return f(*a)
+    assert call(L=None) == 1
+    assert call(q=None) == 1
+    assert call(out=None) == 1
+    assert call(T=-1.0) == 1
+    assert call(T=float("inf")) == 1
+    assert call(L=ctypes.c_void_p(0x100004)) == 1     # not 16-byte aligned
+    assert call(K=17) == 1
+    assert call(K=0) == 1
+    assert call(B=0) == 1
+    assert call(V=0) == 1
+    # the same checks in dflash_verify (its workspace present and large)
+    g = so.dflash_verify
+    g.restype = i32
+    g.argtypes = [vp, vp, vp, vp, i32, i32, i32, f32, u64, u64, vp, vp, vp,
+                  ctypes.c_size_t, vp]
+    big = ctypes.c_void_p(0x200000)
+    base = [fake, fake, fake, fake, 2, 4, 100, 1.0, 1, 0, fake, fake, big,
+            1 << 30, None]
+    for i, v in ((0, None), (7, -1.0), (0, ctypes.c_void_p(0x100004)),
+                 (5, 17)):
+        a = list(base)
+        a[i] = v
+        assert g(*a) == 1
+    a = list(base)
+    a[12] = ctypes.c_void_p(0x200010)                 # ws not 256-aligned
+    assert g(*a) == 1
+    a = list(base)
+    a[13] = 16                                        # ws too small
+    assert g(*a) == 1

@@ -99,6 +99,26 @@ def test_philox_matches_independent_implementation(tmp_path):
     assert np.array_equal(got, ref)
 
 
+def _philox_kat():
+    import json
+    with open(os.path.join(os.path.dirname(__file__), "golden",
+                           "philox_kat.json")) as f:
+        fx = json.load(f)
+    h = lambda ws: [int(w, 16) for w in ws]
+    return [(h(v["ctr"]), h(v["key"]), h(v["out"])) for v in fx["vectors"]]
+
+
+def test_philox_published_known_answers():
+    """The generator's own published known-answer vectors (Random123,
+    Philox4x32-10): counter 0 under key 0, all-ones, and the digits of pi;
+    scalar and vectorised forms."""
+    for ctr, key, out in _philox_kat():
+        assert list(philox.philox_scalar(ctr, key)) == out
+        got = philox.philox4x32_10(np.array([ctr], np.uint64),
+                                   np.array([key], np.uint64))
+        assert [int(x) for x in got[0]] == out
+
+
 def test_philox_vector_and_scalar_agree():
     rng = np.random.default_rng(2)
     ctr = rng.integers(0, 2**32, size=(64, 4), dtype=np.uint64)
@@ -492,6 +512,38 @@ def test_verify_is_lossless_chi_square():
     sel = n >= 1
     c1 = np.bincount(out[sel, 1], minlength=V)
     assert stats.chisquare(c1, p1 * sel.sum()).pvalue > 1e-3
+
+
+def _all_accepted(B, K, V):
+    """Drafts that every accept test takes with certainty: position t
+    drafts token t (q one-hot on it) and the target puts all its mass on
+    token t (logit 0, the rest -inf), so p = q = 1 exactly."""
+    draft = np.tile(np.arange(K, dtype=np.int32), (B, 1))
+    topi = np.full((B, K, C), -1, np.int32)
+    topi[:, :, 0] = draft
+    q = np.zeros((B, K, C), np.float32)
+    q[:, :, 0] = 1.0
+    L = np.full((B, K + 1, V), -np.inf, np.float32)
+    L[:, np.arange(K), np.arange(K)] = 0.0
+    return draft, topi, q, L
+
+
+def test_verify_bonus_draw_follows_target_row_K():
+    """All K drafts accepted: the bonus token is drawn from row K,
+    p_K = softmax(L[:, K] / T), and not from row K-1 or its residual (both
+    put all their mass on token K-1).  chi-square at V = 8."""
+    V, B, K, T = 8, 40000, 2, 0.7
+    rng = np.random.default_rng(15)
+    pK = rng.dirichlet(np.ones(V) * 0.5)
+    draft, topi, q, L = _all_accepted(B, K, V)
+    L[:, K] = T * np.log(pK)
+    n, out, _ = oracle.verify(L, draft, topi, q, T,
+                              philox.accept_uniforms(19, 0, B, K),
+                              philox.resample_uniforms(19, 0, B, K))
+    assert np.all(n == K)
+    assert np.array_equal(out[:, :K], draft)
+    cK = np.bincount(out[:, K], minlength=V)
+    assert stats.chisquare(cK, pK * B).pvalue > 1e-3
 
 
 def test_verify_output_layout():

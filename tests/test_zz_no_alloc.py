@@ -54,6 +54,52 @@ def test_noalloc_verify_matches_verify_on_consecutive_calls(lib, T):
         assert np.array_equal(np_(out), np_(out_ref))
 
 
+def _valid_inputs(B, K, V, seed):
+    """Target logits and drafts of the right shapes on the device (drafts
+    among their candidates, q a distribution over them)."""
+    g = torch.Generator(device="cuda").manual_seed(seed)
+    L = torch.randn(B, K + 1, V, generator=g, device="cuda")
+    topi = torch.randint(0, V, (B, K, C), generator=g, device="cuda",
+                         dtype=torch.int32)
+    q = torch.rand(B, K, C, generator=g, device="cuda") + 0.01
+    q /= q.sum(-1, keepdim=True)
+    draft = topi[:, :, 0].contiguous()
+    return L, draft, topi, q
+
+
+LIMIT = 4 << 20
+
+
+@pytest.mark.parametrize("V,K,B", [
+    (151936, 16, 402),     # the largest batch whose scratch fits, K = 16
+    (151936, 16, 403),     # one sequence more: over the limit
+    (262144, 14, 256),     # B = 256 fits up to K = 14 at V = 262144
+    (262144, 15, 256),     # ... and not at K = 15
+])
+def test_noalloc_verify_at_the_scratch_limit(lib, V, K, B):
+    """Just inside the 4 MiB limit the call runs and matches dflash_verify;
+    just outside it is refused with DFLASH_ERR_UNSUPPORTED."""
+    need = lib.dflash_workspace_bytes(1, B, K, 0, V)
+    L, draft, topi, q = _valid_inputs(B, K, V, seed=B + K)
+    i32 = dict(dtype=torch.int32, device="cuda")
+    n = torch.full((B,), -7, **i32)
+    out = torch.full((B, K + 1), -7, **i32)
+    if need > LIMIT:
+        with pytest.raises(lib.DFlashError) as e:
+            lib.dflash_verify_noalloc(L, draft, topi, q, 1.0, 3, 1, n, out)
+        assert e.value.status == 2      # DFLASH_ERR_UNSUPPORTED
+        assert int(n.min()) == -7       # nothing launched
+        return
+    n_ref = torch.empty(B, **i32)
+    out_ref = torch.empty(B, K + 1, **i32)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    lib.dflash_verify(L, draft, topi, q, 1.0, 3, 1, n_ref, out_ref, ws)
+    lib.dflash_verify_noalloc(L, draft, topi, q, 1.0, 3, 1, n, out)
+    torch.cuda.synchronize()
+    lib.dflash_check()
+    assert torch.equal(n, n_ref) and torch.equal(out, out_ref)
+
+
 def test_noalloc_verify_refuses_sizes_beyond_its_scratch(lib):
     # 278,528 target rows: their per-row results and tickets alone outgrow
     # the 4 MiB array
