@@ -110,7 +110,9 @@ struct VerifyWs {
   int* row_acc;        // [rows] accept decision of position t (t < K)
   int* row_tok;        // [rows] token emitted if t is the first rejection
                        // (t = K: the bonus token)
-  unsigned* counters;  // rows + B tickets, zeroed before every launch
+  unsigned* counters;  // rows + B tickets and B rejection masks, zeroed
+                       // before every launch
+  unsigned* rejmask;   // [B] bit t: position t rejected (in counters)
   size_t counter_bytes;
 };
 constexpr int kVerifyMaxChunks = 64;  // row chunks (CTAs) per target row

@@ -39,6 +39,24 @@ __device__ __forceinline__ void bitonic_merge32(float& v, int& i, int lane) {
   }
 }
 
+// Best-first bitonic sort of 32 (value, id) pairs, one per lane: larger
+// value first, lower id first among equal values.
+__device__ __forceinline__ void warp_sort32(float& v, int& i, int lane) {
+#pragma unroll
+  for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+    for (int d = size >> 1; d; d >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, v, d);
+      const int oi = __shfl_xor_sync(0xffffffffu, i, d);
+      const bool best_first = ((lane & size) == 0) || size == 32;
+      const bool lower = (lane & d) == 0;
+      const bool other_ahead = ranks_ahead(ov, oi, v, i);
+      const bool mine_ahead = ranks_ahead(v, i, ov, oi);
+      if ((lower == best_first) ? other_ahead : mine_ahead) { v = ov; i = oi; }
+    }
+  }
+}
+
 // Phase 1, warp gw (0..kMergeWarps-1) of the group merging row m: fold the
 // strips gw, gw + 8, ... of the row.  Returns the warp's top-16 on lanes
 // 0..15 (tv, ti) and its (max, sum exp) pair (rm, rs).

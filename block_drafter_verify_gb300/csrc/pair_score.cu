@@ -391,6 +391,118 @@ __device__ __forceinline__ void gather_rows(T* st, const int (*tok)[kC],
   }
 }
 
+// Row stride (bf16 elements) of the staged embedding rows of the
+// tensor-core scores: r rounded up to whole k-steps of 16, plus 8 so that
+// the fragment loads of 8 rows x 4 columns hit 32 distinct banks.
+__host__ __device__ constexpr int mma_ld(int r) { return (r + 15) / 16 * 16 + 8; }
+
+// As gather_rows, into rows of stride ld, with the elements [r, ld - 8)
+// zeroed (r % 8 == 0).
+__device__ __forceinline__ void gather_rows_ld(__nv_bfloat16* st, int ld,
+                                               const int (*tok)[kC],
+                                               const __nv_bfloat16* e_in,
+                                               const __nv_bfloat16* e_out,
+                                               int r) {
+  const int cpr = r / 8;                    // 16-byte chunks per row
+  const int cpad = (ld - 8) / 8;            // chunks up to the k-step
+  for (int idx = threadIdx.x; idx < 2 * kC * cpad; idx += kThreads) {
+    const int rowi = idx / cpad, ch = idx % cpad;
+    __nv_bfloat16* dst = st + (size_t)rowi * ld + ch * 8;
+    if (ch >= cpr) {
+      *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
+      continue;
+    }
+    const int tab = rowi / kC;
+    const int t = tok[tab][rowi % kC];
+    const __nv_bfloat16* src = (tab == 0 ? e_in : e_out) + (size_t)max(t, 0) * r;
+    cp_async16(dst, src + ch * 8, t >= 0 ? 16 : 0);
+  }
+}
+
+// bf16 splitting of an fp32 value x = hi + mid + lo + e, |e| <= 2^-24 |x|
+// (each step keeps the next 8 significant bits; the differences are exact
+// in fp32).
+__device__ __forceinline__ void split3_bf16(float x, __nv_bfloat16& hi,
+                                            __nv_bfloat16& mid,
+                                            __nv_bfloat16& lo) {
+  hi = __float2bfloat16_rn(x);
+  const float r1 = x - __bfloat162float(hi);
+  mid = __float2bfloat16_rn(r1);
+  lo = __float2bfloat16_rn(r1 - __bfloat162float(mid));
+}
+
+// The 16 x 16 scores of one row (b, t) on the tensor cores, whole CTA
+// (256 threads), from the staged raw rows st ([table][16][ld], 0 = E_in,
+// padded with zeros to the k-step):
+//   S[i][j] = topv[j] + sum_k E_in[pred_i, k] X[j, k],
+//   X[j, k] = g[k] E_out[cand_j, k]  (fp32),
+// with X split into three bf16 parts so that every product of the
+// mma.sync m16n8k16 (bf16 x bf16 -> fp32) is exact and the sum matches
+// fp32 evaluation: E_in is bf16 already, X = X_hi + X_mid + X_lo to 2^-24.
+// Warp w takes column block w & 1 (8 candidates) and every fourth k-step
+// from w >> 1; the four partial tiles are added in a fixed order.
+// work: >= 3 * 16 * ld bf16 + 4 * 256 fp32.
+__device__ __forceinline__ void score_row_mma(
+    const __nv_bfloat16* st, int ld, const int* pred, const int* cand,
+    const float* g_row, int r, float* work, const float* topv_row,
+    float* __restrict__ out) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int kp = ld - 8;                        // padded k extent
+  __nv_bfloat16* xs = reinterpret_cast<__nv_bfloat16*>(work);  // [3][16][ld]
+  float* part = work + (3 * kC * ld + 1) / 2;   // [4][16][16]
+  const __nv_bfloat16* eo = st + (size_t)kC * ld;
+  const int cpr = kp / 8;
+  for (int idx = tid; idx < kC * cpr; idx += kThreads) {
+    const int j = idx / cpr, ch = idx % cpr;
+    float f[8];
+    Vec16<__nv_bfloat16>::to_f32(
+        *reinterpret_cast<const uint4*>(eo + (size_t)j * ld + ch * 8), f);
+    __align__(16) __nv_bfloat16 h8[8], m8[8], l8[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const int k = ch * 8 + e;
+      const float x = k < r ? f[e] * g_row[k] : 0.f;
+      split3_bf16(x, h8[e], m8[e], l8[e]);
+    }
+    const size_t o = (size_t)j * ld + ch * 8;
+    *reinterpret_cast<uint4*>(xs + o) = *reinterpret_cast<const uint4*>(h8);
+    *reinterpret_cast<uint4*>(xs + kC * ld + o) =
+        *reinterpret_cast<const uint4*>(m8);
+    *reinterpret_cast<uint4*>(xs + 2 * kC * ld + o) =
+        *reinterpret_cast<const uint4*>(l8);
+  }
+  __syncthreads();
+  {
+    const int g = lane >> 2, c = lane & 3;
+    const int nt = warp & 1, kq = warp >> 1;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    const __nv_bfloat16* ea = st + g * ld + 2 * c;
+    const __nv_bfloat16* xb = xs + (nt * 8 + g) * ld + 2 * c;
+    for (int k0 = kq * 16; k0 < kp; k0 += 64) {
+      const uint32_t a0 = ld_b32(ea + k0);
+      const uint32_t a1 = ld_b32(ea + 8 * ld + k0);
+      const uint32_t a2 = ld_b32(ea + k0 + 8);
+      const uint32_t a3 = ld_b32(ea + 8 * ld + k0 + 8);
+#pragma unroll
+      for (int pp = 0; pp < 3; ++pp) {
+        const __nv_bfloat16* xr = xb + pp * kC * ld + k0;
+        mma_16816(acc, a0, a1, a2, a3, ld_b32(xr), ld_b32(xr + 8));
+      }
+    }
+    float* pq = part + kq * kC * kC;
+    const int col = nt * 8 + 2 * c;
+    pq[g * kC + col] = acc[0];
+    pq[g * kC + col + 1] = acc[1];
+    pq[(g + 8) * kC + col] = acc[2];
+    pq[(g + 8) * kC + col + 1] = acc[3];
+  }
+  __syncthreads();
+  const int i = tid / kC, j = tid % kC;  // kThreads == 256 == 16 x 16
+  const float v = ((part[tid] + part[256 + tid]) + part[512 + tid]) +
+                  part[768 + tid];
+  out[tid] = (pred[i] >= 0 && cand[j] >= 0) ? topv_row[j] + v : -INFINITY;
+}
+
 template <typename T>
 __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads)
     pair_score_kernel(const float* __restrict__ topv,
@@ -518,19 +630,14 @@ __global__ void __launch_bounds__(kThreads)
 // the top-16 (so at most 16 merges); then the group's first warp merges the
 // group's lists in warp order.  Same top-16 as topk_merge_kernel; lse may
 // differ in the last bits (another summation order).
-__device__ __forceinline__ void fold_lists_smem(const float* sv,
-                                                const int* si,
-                                                const float* sm,
+// (max, sum exp) pairs of the strips gw, gw + ngw, ... of one row, folded
+// by a warp: each lane its strips in order, then the lanes in a fixed tree.
+__device__ __forceinline__ void fold_pairs_smem(const float* sm,
                                                 const float* ss, int nstrip,
-                                                int gw, int ngw, float& tv,
-                                                int& ti, float& rm,
+                                                int gw, int ngw, float& rm,
                                                 float& rs) {
   const int lane = threadIdx.x & 31;
-  const int k = lane < kC ? lane : 31 - lane;  // lanes 16..31: reversed
   const int nl = gw < nstrip ? (nstrip - gw + ngw - 1) / ngw : 0;  // lists
-  tv = -INFINITY;
-  ti = -1;
-  // pairs: each lane folds its lists in order, then lanes in a fixed tree
   rm = -INFINITY;
   rs = 0.f;
   for (int j = lane; j < nl; j += 32) {
@@ -545,6 +652,21 @@ __device__ __forceinline__ void fold_lists_smem(const float* sv,
   }
   rm = __shfl_sync(0xffffffffu, rm, 0);
   rs = __shfl_sync(0xffffffffu, rs, 0);
+}
+
+__device__ __forceinline__ void fold_lists_smem(const float* sv,
+                                                const int* si,
+                                                const float* sm,
+                                                const float* ss, int nstrip,
+                                                int gw, int ngw, float& tv,
+                                                int& ti, float& rm,
+                                                float& rs) {
+  const int lane = threadIdx.x & 31;
+  const int k = lane < kC ? lane : 31 - lane;  // lanes 16..31: reversed
+  const int nl = gw < nstrip ? (nstrip - gw + ngw - 1) / ngw : 0;  // lists
+  tv = -INFINITY;
+  ti = -1;
+  fold_pairs_smem(sm, ss, nstrip, gw, ngw, rm, rs);
   // top-16: 32 lists at a time, taken in the order of their best entries;
   // once a list's best cannot enter the top-16, no later one can
   for (int j0 = 0; j0 < nl; j0 += 32) {
@@ -616,7 +738,7 @@ __global__ void __launch_bounds__(kThreads)
   float* g_row = reinterpret_cast<float*>(smem4);    // [256]
   float* work = g_row + DFLASH_MAX_RANK;              // score tiles / walk
   T* st = reinterpret_cast<T*>(work + 2 * kC * (DFLASH_MAX_RANK + 4));
-  float* lists = reinterpret_cast<float*>(st + 2 * kC * r);
+  float* lists = reinterpret_cast<float*>(st + 2 * kC * mma_ld(r));
   // words of one row's lists, rounded to 16 bytes for the copies
   const int lw = (nstrip * (2 * kC + 2) + 3) & ~3;
   __shared__ int s_tok[2][kC];
@@ -627,6 +749,8 @@ __global__ void __launch_bounds__(kThreads)
   __shared__ float s_mv[2][kWarps / 2][kC], s_mm[2][kWarps / 2],
       s_ms[2][kWarps / 2];
   __shared__ int s_mi[2][kWarps / 2][kC];
+  __shared__ float s_th[2], s_sv[2][64];
+  __shared__ int s_wt[2][kWarps / 2], s_si[2][64];
   __shared__ int s_flag;
   const int m = blockIdx.x, b = m / K, t = m % K;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -658,30 +782,113 @@ __global__ void __launch_bounds__(kThreads)
   __syncthreads();
 
   // ---- 2. merges: warps 0-3 row m, warps 4-7 row m - 1 ------------------
+  // The row's top 16 come from few of its strip lists.  A bound th, the
+  // 16th largest of 32 lane maxima of the lists' best entries (each lane
+  // owns distinct strips, so at least 16 values of distinct columns reach
+  // th), is at most the row's 16th value: no entry below it can make the
+  // top 16.  The entries >= th of every list (a prefix of each sorted
+  // list; usually a few dozen in all) are gathered and sorted once.  When
+  // more than kCap survive (many equal values), the lists are folded
+  // whole by bitonic merges instead.
   {
     constexpr int kG = kWarps / 2;  // warps per row
-    const int g = warp / kG, gw = warp % kG;
-    float tv = -INFINITY, rm = -INFINITY, rs = 0.f;
-    int ti = -1;
-    if (g == 0 || t > 0) {
-      const float* L = lists + g * lw;
-      fold_lists_smem(L, reinterpret_cast<const int*>(L + nstrip * kC),
-                      L + 2 * nstrip * kC, L + 2 * nstrip * kC + nstrip,
-                      nstrip, gw, kG, tv, ti, rm, rs);
+    constexpr int kGT = kG * 32;    // threads per row
+    constexpr int kCap = 64;
+    const int g = warp / kG, gw = warp % kG, lt = tid % kGT;
+    const bool act = g == 0 || t > 0;  // row m - 1 exists
+    const float* L = lists + g * lw;
+    const float* sv = L;
+    const int* si = reinterpret_cast<const int*>(L + nstrip * kC);
+    const float* sm = L + 2 * nstrip * kC;
+    const float* ss = sm + nstrip;
+    float rm = -INFINITY, rs = 0.f;
+    if (gw == 0) {
+      float mx = -INFINITY;
+      if (act)
+        for (int q = lane; q < nstrip; q += 32) mx = fmaxf(mx, sv[q * kC]);
+      int dummy = lane;
+      warp_sort32(mx, dummy, lane);
+      if (lane == 0) s_th[g] = __shfl_sync(0xffffffffu, mx, kC - 1);
     }
-    if (lane < kC) { s_mv[g][gw][lane] = tv; s_mi[g][gw][lane] = ti; }
+    if (act) fold_pairs_smem(sm, ss, nstrip, gw, kG, rm, rs);
     if (lane == 0) { s_mm[g][gw] = rm; s_ms[g][gw] = rs; }
     __syncthreads();
+    // survivors of lists lt, lt + kGT, ... (nstrip <= 160 < 2 kGT)
+    const float th = s_th[g];
+    int c0 = 0, c1 = 0;
+    if (act) {
+      if (lt < nstrip)
+        while (c0 < kC && sv[lt * kC + c0] >= th) ++c0;
+      if (lt + kGT < nstrip)
+        while (c1 < kC && sv[(lt + kGT) * kC + c1] >= th) ++c1;
+    }
+    const int cnt = c0 + c1;
+    int incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += n;
+    }
+    if (lane == 31) s_wt[g][gw] = incl;
+    __syncthreads();
+    int pos = incl - cnt, total = 0;
+#pragma unroll
+    for (int w2 = 0; w2 < kG; ++w2) {
+      const int x = s_wt[g][w2];
+      if (w2 < gw) pos += x;
+      total += x;
+    }
+    const bool direct = total <= kCap;
+    if (act && direct) {
+      for (int k = 0; k < c0; ++k, ++pos) {
+        s_sv[g][pos] = sv[lt * kC + k];
+        s_si[g][pos] = si[lt * kC + k];
+      }
+      for (int k = 0; k < c1; ++k, ++pos) {
+        s_sv[g][pos] = sv[(lt + kGT) * kC + k];
+        s_si[g][pos] = si[(lt + kGT) * kC + k];
+      }
+      for (int p2 = total + lt; p2 < kCap; p2 += kGT) {
+        s_sv[g][p2] = -INFINITY;
+        s_si[g][p2] = -1;
+      }
+    }
+    float tv = -INFINITY;
+    int ti = -1;
+    if (act && !direct) {
+      float rm2, rs2;  // the pairs are folded above
+      fold_lists_smem(sv, si, sm, ss, nstrip, gw, kG, tv, ti, rm2, rs2);
+    }
+    if (lane < kC) { s_mv[g][gw][lane] = tv; s_mi[g][gw][lane] = ti; }
+    __syncthreads();
     if (gw == 0) {
-      if (g == 0 || t > 0) {
-        const int k = lane < kC ? lane : 31 - lane;
-        for (int w2 = 1; w2 < kG; ++w2) {
+      if (act) {
+        for (int w2 = 1; w2 < kG; ++w2)
           lse_combine(rm, rs, s_mm[g][w2], s_ms[g][w2], 1.f);
-          float v = lane < kC ? tv : s_mv[g][w2][k];
-          int i = lane < kC ? ti : s_mi[g][w2][k];
-          bitonic_merge32(v, i, lane);
-          tv = v;
-          ti = i;
+        if (direct) {
+          // sort both halves of the 64 survivors, then keep the best 16
+          // of their union (a: lanes 0-15; b reversed: lanes 16-31)
+          float va = s_sv[g][lane], vb = s_sv[g][lane + 32];
+          int ia = s_si[g][lane], ib = s_si[g][lane + 32];
+          warp_sort32(va, ia, lane);
+          if (total > 32) {
+            warp_sort32(vb, ib, lane);
+            const float bv = __shfl_sync(0xffffffffu, vb, 31 - lane);
+            const int bi = __shfl_sync(0xffffffffu, ib, 31 - lane);
+            if (lane >= kC) { va = bv; ia = bi; }
+            bitonic_merge32(va, ia, lane);
+          }
+          tv = va;
+          ti = ia;
+        } else {
+          const int k = lane < kC ? lane : 31 - lane;
+          for (int w2 = 1; w2 < kG; ++w2) {
+            float v = lane < kC ? tv : s_mv[g][w2][k];
+            int i = lane < kC ? ti : s_mi[g][w2][k];
+            bitonic_merge32(v, i, lane);
+            tv = v;
+            ti = i;
+          }
         }
       } else {  // t = 0: every predecessor is the anchor
         ti = anchor[b];
@@ -706,11 +913,26 @@ __global__ void __launch_bounds__(kThreads)
   __syncthreads();
 
   // ---- 3. embedding rows and scores --------------------------------------
-  if (vec) gather_rows(st, s_tok, e_in, e_out, r);
+  // bf16 rows of whole 16-byte chunks: tensor-core scores; otherwise the
+  // fp32 dot products
+  constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
+  const bool tc_scores = kBf16 && r % 8 == 0;
+  if (tc_scores) {
+    if constexpr (kBf16)
+      gather_rows_ld(st, mma_ld(r), s_tok, e_in, e_out, r);
+  } else if (vec) {
+    gather_rows(st, s_tok, e_in, e_out, r);
+  }
   cp_async_wait_all();
   __syncthreads();
-  score_row<kThreads>(st, vec, s_tok[0], s_tok[1], g_row, e_in, e_out, r,
-                      work, s_topv, scores + (size_t)m * kC * kC);
+  if (tc_scores) {
+    if constexpr (kBf16)
+      score_row_mma(st, mma_ld(r), s_tok[0], s_tok[1], g_row, r, work,
+                    s_topv, scores + (size_t)m * kC * kC);
+  } else {
+    score_row<kThreads>(st, vec, s_tok[0], s_tok[1], g_row, e_in, e_out, r,
+                        work, s_topv, scores + (size_t)m * kC * kC);
+  }
 
   // ---- 4. the last row of sequence b walks it -----------------------------
   __syncthreads();
@@ -865,7 +1087,7 @@ cudaError_t launch_draft_tail(TopkPartials P, int nstrip, const int* anchor,
   const size_t smem =
       (size_t)(DFLASH_MAX_RANK + 2 * kC * (DFLASH_MAX_RANK + 4)) *
           sizeof(float) +
-      (size_t)2 * kC * r * sizeof(T) +
+      (size_t)2 * kC * mma_ld(r) * sizeof(T) +
       (size_t)2 * ((nstrip * (2 * kC + 2) + 3) & ~3) * sizeof(float);
   cudaError_t e = cudaFuncSetAttribute(
       draft_tail_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -21,7 +21,11 @@
 //               residual max(0, p - q) over the <= 16 candidates) or, for
 //               t = K, the bonus draw from p.  All draws of sequence b share
 //               its one resample uniform, so drawing every row ahead of time
-//               gives the same token as drawing only the rejected one.  The
+//               gives the same token as drawing only the rejected one.  A
+//               row that cannot be emitted skips its draw: its draft was
+//               accepted, or an earlier position of the sequence already
+//               recorded a rejection in the sequence's mask (for t = K: any
+//               rejection).  The
 //               drafter's inputs of row t (draft, candidates, q and the
 //               target logits at those tokens) are fetched at the start of
 //               the CTA, so none of this waits on another launch or row.
@@ -111,7 +115,7 @@ __global__ void __launch_bounds__(kThreads)
 
   __shared__ float s_a[kWarps];
   __shared__ int s_i[kWarps];
-  __shared__ int s_flag, s_seg, s_use_raw, s_acc;
+  __shared__ int s_flag, s_seg, s_use_raw, s_acc, s_need;
   __shared__ float s_W[kWarps], s_rem, s_m;
   __shared__ int s_ci[kC];
   __shared__ float s_qz[kC], s_corr[kC];
@@ -307,11 +311,23 @@ __global__ void __launch_bounds__(kThreads)
       if (lane == 0) {
         s_m = ra;
         s_acc = acc;
+        // Row t's token is emitted only if t is the first rejection (t < K)
+        // or nothing is rejected (t = K): a row whose draft was accepted,
+        // or that follows a rejection already recorded in the sequence's
+        // mask, skips its draw.  A stale mask only costs a draw.
+        const unsigned below = (1u << t) - 1u;
+        if (has_draft)
+          s_need = !acc &&
+                   !(atomicOr(&ws.rejmask[b], 1u << t) & below);
+        else
+          s_need = atomicOr(&ws.rejmask[b], 0u) == 0u;
       }
     }
   }
   if (!greedy) {
     __syncthreads();
+  }
+  if (!greedy && s_need) {
     // ---- draw of row (b, t): residual max(0, p - q), or p for t = K ------
     // Warp 0 locates the segment.  Lane l owns the contiguous segments
     // l*per .. l*per+per-1; a segment's weight is its (max, sum) pair
@@ -436,8 +452,8 @@ __global__ void __launch_bounds__(kThreads)
       ws.row_tok[row] = pick >= 0 ? pick : last;
       __threadfence();  // before the sequence ticket below
     }
-    if (tid == 0) ws.row_acc[row] = s_acc;
   }
+  if (!greedy && tid == 0) ws.row_acc[row] = s_acc;
 
   // ---- ticket of sequence b; its last row emits the tokens --------------
   __syncthreads();
@@ -490,8 +506,11 @@ size_t verify_ws_layout(int B, int K, int V, void* base, VerifyWs* o) {
   w.part = reinterpret_cast<float2*>(take(rows * nseg * sizeof(float2)));
   w.row_acc = reinterpret_cast<int*>(take(rows * sizeof(int)));
   w.row_tok = reinterpret_cast<int*>(take(rows * sizeof(int)));
-  w.counter_bytes = (rows + (size_t)B) * sizeof(unsigned);
+  // tickets of rows and sequences, then each sequence's mask of rejected
+  // positions, all zeroed together before a launch
+  w.counter_bytes = (rows + 2 * (size_t)B) * sizeof(unsigned);
   w.counters = reinterpret_cast<unsigned*>(take(w.counter_bytes));
+  w.rejmask = w.counters ? w.counters + rows + B : nullptr;
   if (o) *o = w;
   return align256(off);
 }

@@ -97,11 +97,13 @@ def conv2tap(h: np.ndarray, w_conv) -> np.ndarray:
     W0, W1 = W[:H], W[H:]
     y = np.empty_like(h)
     for b in range(B):
-        for t in range(K):
-            w0 = W0 @ h[b, t]            # dynamic tap weights from h_t
-            w1 = W1 @ h[b, t]
-            prev = h[b, t - 1] if t > 0 else np.zeros(H)
-            y[b, t] = w0 * h[b, t] + w1 * prev
+        # the dynamic tap weights of every position of the sequence at once:
+        # row t of w0 is W0 h_t, row t of w1 is W1 h_t
+        w0 = h[b] @ W0.T
+        w1 = h[b] @ W1.T
+        prev = np.zeros((K, H))          # h_{t-1}, zero before the block
+        prev[1:] = h[b, :-1]
+        y[b] = w0 * h[b] + w1 * prev
     return y
 
 

@@ -24,10 +24,14 @@ EPS_ACCEPT = 1e-5
 def f64(t):
     if t is None:
         return None
+    if isinstance(t, np.ndarray):
+        return t.astype(np.float64)
     return t.detach().float().cpu().numpy().astype(np.float64)
 
 
 def np_(t):
+    if isinstance(t, np.ndarray):
+        return t
     return t.detach().cpu().numpy()
 
 
