@@ -917,7 +917,7 @@ def selector_report(dv_mod, dv, w, h, anchor, L, seed, stream, dev, pk,
     t_vit = statistics.mean(e[2].elapsed_time(e[3]) for e in ev) * 1e3
     rec_bytes = B * K * (w.V * 4 + C * 4 + 8)
     vit_bytes = B * K * (C * C * 4 + C * 4 + 8 + C * 4)
-    recall, perfect = dv_mod.recall_by_position(hit)
+    recall, perfect = recall_by_position(hit)
     gbs = rec_bytes / (t_rec * 1e-6) / 1e9
     return {"T": 0.0,
             "mean_accepted_greedy_walk": float(n_g.item()) / (reps * B),
@@ -930,6 +930,22 @@ def selector_report(dv_mod, dv, w, h, anchor, L, seed, stream, dev, pk,
             "recall_roofline": {"bound": "hbm", "bytes": rec_bytes,
                                 "achieved": gbs, "peak": pk["hbm_gbs"],
                                 "unit": "GB/s", "frac": gbs / pk["hbm_gbs"]}}
+
+
+def recall_by_position(in_top16):
+    """Recall@16 per drafted position, and the acceptance length a perfect
+    selector would reach under greedy verification (leading positions whose
+    target token is among the candidates), from dflash_top16_recall's
+    in_top16 [B,K] (a report of the diagnostic's flags, not a step of
+    the path)."""
+    import torch
+    f = in_top16.to(torch.int64)
+    recall = f.double().mean(dim=0)
+    miss = (f == 0)
+    first = torch.where(miss.any(dim=1), miss.int().argmax(dim=1),
+                        torch.full_like(miss[:, 0], f.shape[1],
+                                        dtype=torch.int64))
+    return recall, first.double().mean()
 
 
 def stage_bytes(w, fused):

@@ -7,7 +7,7 @@ from .binding import (BF16, C, COMMIT_STATS, FP32, STAGES, DFlashError,
                       DraftVerify, EXPORTS, dflash_check, dflash_commit,
                       dflash_draft, dflash_draft_e4m3, dflash_lmhead_topk,
                       dflash_path_viterbi, dflash_quantize_e4m3_rows,
-                      dflash_top16_recall, recall_by_position,
+                      dflash_top16_recall, dflash_set_wait_limit_ns,
                       dflash_pair_score, dflash_path_walk, dflash_philox4x32,
                       dflash_profile_stage, dflash_verify,
                       dflash_verify_noalloc, dflash_workspace_bytes,
@@ -17,7 +17,7 @@ __all__ = ["BF16", "C", "COMMIT_STATS", "FP32", "STAGES", "DFlashError",
            "DraftVerify", "EXPORTS", "dflash_check", "dflash_commit",
            "dflash_draft", "dflash_draft_e4m3", "dflash_lmhead_topk",
            "dflash_path_viterbi", "dflash_quantize_e4m3_rows",
-           "dflash_top16_recall", "recall_by_position",
+           "dflash_top16_recall", "dflash_set_wait_limit_ns",
            "dflash_pair_score", "dflash_path_walk", "dflash_philox4x32",
            "dflash_profile_stage", "dflash_verify", "dflash_verify_noalloc",
            "dflash_workspace_bytes", "library_path", "load"]

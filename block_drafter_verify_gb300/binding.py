@@ -23,8 +23,8 @@ EXPORTS = ("dflash_workspace_bytes", "dflash_lmhead_topk", "dflash_pair_score",
            "dflash_path_walk", "dflash_draft", "dflash_verify",
            "dflash_verify_noalloc", "dflash_commit", "dflash_path_viterbi",
            "dflash_top16_recall", "dflash_quantize_e4m3_rows",
-           "dflash_draft_e4m3", "dflash_philox4x32", "dflash_profile_stage", "dflash_check",
-           "dflash_status_string")
+           "dflash_draft_e4m3", "dflash_philox4x32", "dflash_profile_stage",
+           "dflash_set_wait_limit_ns", "dflash_check", "dflash_status_string")
 STAGES = ("conv", "lmhead", "merge", "pair_score", "walk", "verify",
           "quant")
 
@@ -79,6 +79,7 @@ def load(path: str | None = None):
                                     i32, i32, i32, f32, u64, u64, vp, vp, vp,
                                     vp, vp, vp, vp, vp, sz, vp]),
         "dflash_profile_stage": (i32, [i32, vp, vp]),
+        "dflash_set_wait_limit_ns": (i32, [u64]),
         "dflash_check": (i32, [vp]),
         "dflash_status_string": (ctypes.c_char_p, [i32]),
     }
@@ -264,20 +265,6 @@ def dflash_top16_recall(target_logits, topi, target_argmax, in_top16,
           V, _ptr(target_argmax), _ptr(in_top16), _stream(stream))
 
 
-def recall_by_position(in_top16):
-    """Recall@16 per drafted position, and the acceptance length a perfect
-    selector would reach under greedy verification (leading positions whose
-    target token is among the candidates), from dflash_top16_recall's
-    in_top16 [B,K] (host-side arithmetic on the kernel's flags)."""
-    f = in_top16.to(torch.int64)
-    recall = f.double().mean(dim=0)
-    miss = (f == 0)
-    first = torch.where(miss.any(dim=1), miss.int().argmax(dim=1),
-                        torch.full_like(miss[:, 0], f.shape[1],
-                                        dtype=torch.int64))
-    return recall, first.double().mean()
-
-
 COMMIT_STATS = 3 + 16 + 1
 
 
@@ -307,6 +294,12 @@ def dflash_profile_stage(stage, begin=None, end=None):
     b = None if begin is None else ctypes.c_void_p(begin.cuda_event)
     e = None if end is None else ctypes.c_void_p(end.cuda_event)
     _call("dflash_profile_stage", int(stage), b, e)
+
+
+def dflash_set_wait_limit_ns(ns):
+    """Limit of the tensor-core kernels' bounded waits in later launches
+    (0 = the default 2 s); for tests of the timeout path."""
+    _call("dflash_set_wait_limit_ns", int(ns))
 
 
 def dflash_check(stream=None):

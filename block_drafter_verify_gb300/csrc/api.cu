@@ -2,6 +2,7 @@
 // workspace carving and kernel launches.  Nothing here allocates memory.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "kernels.h"
@@ -42,6 +43,10 @@ dflash_status device_state(DeviceState** out) {
   *out = &d;
   return DFLASH_OK;
 }
+
+// Limit of the tensor-core kernels' bounded waits for later launches
+// (dflash_set_wait_limit_ns).
+std::atomic<uint64_t> g_wait_ns{kWaitLimitNs};
 
 // Caller-supplied timing events per stage (dflash_profile_stage).
 enum Stage { kStConv = 0, kStLmhead, kStMerge, kStPair, kStWalk, kStVerifyRows,
@@ -191,7 +196,8 @@ dflash_status lmhead_tc_path(const __nv_bfloat16* h,
     {
       StageTimer tm(kStConv, s);
       e = launch_conv_tc(mh, mw, w_gate ? &mg : nullptr, h, B, K, H, r, y,
-                         gate, tickets, row_bound, M * kBoundSlots, d.err, s);
+                         gate, tickets, row_bound, M * kBoundSlots, d.err, s,
+                         g_wait_ns.load());
     }
     if (e != cudaSuccess) return DFLASH_ERR_CUDA;
     a = y;
@@ -217,7 +223,8 @@ dflash_status lmhead_tc_path(const __nv_bfloat16* h,
     StageTimer tm(kStLmhead, s);
     e = launch_lmhead_tc(my, mw, M, H, V, d.sms, P, d.err, &strips, s,
                          q8 && conv_w ? q8->y_scale : nullptr,
-                         q8 && conv_w ? q8->w_scale : nullptr, row_bound);
+                         q8 && conv_w ? q8->w_scale : nullptr, row_bound,
+                         g_wait_ns.load());
   }
   if (e != cudaSuccess) return DFLASH_ERR_CUDA;
   if (P_out) {  // the caller merges (draft tail)
@@ -546,6 +553,11 @@ dflash_status dflash_philox4x32(const uint32_t* ctr, uint64_t seed,
   if (st != DFLASH_OK) return st;
   return cuda_status(launch_philox(ctr, seed, out, n,
                                    reinterpret_cast<cudaStream_t>(stream)));
+}
+
+dflash_status dflash_set_wait_limit_ns(uint64_t ns) {
+  g_wait_ns.store(ns ? ns : kWaitLimitNs);
+  return DFLASH_OK;
 }
 
 dflash_status dflash_profile_stage(int stage, void* begin, void* end) {

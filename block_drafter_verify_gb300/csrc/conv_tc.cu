@@ -27,6 +27,8 @@ namespace {
 constexpr int BM = 128, BK = 64;
 constexpr int A_BYTES = BM * BK * 2;        // 16 KB
 constexpr int THREADS = 192;
+// Limit of the drain waits after a give-up (copies and MMAs in flight
+// complete in microseconds); the other waits take the launch's wait_ns.
 constexpr uint64_t WAIT_NS = 2000000000ull;
 
 // BC channels per CTA: the B operand is BC rows of W0 over BC rows of W1
@@ -79,7 +81,7 @@ __global__ void __launch_bounds__(THREADS)
                    int r, __nv_bfloat16* __restrict__ y,
                    float* __restrict__ gate, unsigned* __restrict__ tickets,
                    int ntickets, float* __restrict__ row_bound, int nbound,
-                   int* err) {
+                   int* err, uint64_t wait_ns) {
   constexpr int STAGES = ConvCfg<BC>::STAGES;
   constexpr int B_BYTES = ConvCfg<BC>::B_BYTES;
   constexpr int STAGE_BYTES = ConvCfg<BC>::STAGE_BYTES;
@@ -137,7 +139,7 @@ __global__ void __launch_bounds__(THREADS)
       uint32_t phase = 0, issued = 0, last_par = 0;
       for (int kb = 0; kb < kblocks; ++kb) {
         if (!tc::mbar_wait_bounded(&bars->empty[stage], phase ^ 1, abort,
-                                   WAIT_NS))
+                                   wait_ns))
           break;
         tc::mbar_arrive_expect_tx(&bars->full[stage], STAGE_BYTES);
         uint8_t* b = sb + stage * B_BYTES;
@@ -167,7 +169,7 @@ __global__ void __launch_bounds__(THREADS)
       bool ok = true;
       for (int kb = 0; kb < kblocks; ++kb) {
         if (!tc::mbar_wait_bounded(&bars->full[stage], phase, abort,
-                                   WAIT_NS)) {
+                                   wait_ns)) {
           ok = false;
           break;
         }
@@ -188,7 +190,7 @@ __global__ void __launch_bounds__(THREADS)
   } else {
     const int q = warp & 3;
     const int m = mtile * BM + q * 32 + lane;
-    const bool got = tc::mbar_wait_bounded(&bars->tfull, 0, abort, WAIT_NS);
+    const bool got = tc::mbar_wait_bounded(&bars->tfull, 0, abort, wait_ns);
     if (__all_sync(0xffffffffu, got)) {
       tc::fence_after_sync();
       const uint32_t tb = tmem + (static_cast<uint32_t>(q * 32) << 16);
@@ -271,7 +273,8 @@ cudaError_t launch_conv_bc(const CUtensorMap& map_h, const CUtensorMap& map_wc,
                            const CUtensorMap* map_wg, const __nv_bfloat16* h,
                            int B, int K, int H, int r, __nv_bfloat16* y,
                            float* gate, unsigned* tickets, float* row_bound,
-                           int nbound, int* err, cudaStream_t s) {
+                           int nbound, int* err, cudaStream_t s,
+                           uint64_t wait_ns) {
   const int M = B * K;
   cudaError_t e = cudaFuncSetAttribute(
       conv_tc_kernel<BC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -282,7 +285,7 @@ cudaError_t launch_conv_bc(const CUtensorMap& map_h, const CUtensorMap& map_wc,
   PdlLaunch L(grid, dim3(THREADS), conv_smem_bytes<BC>(), s);
   return cudaLaunchKernelEx(&L.cfg, conv_tc_kernel<BC>, map_h, map_wc,
                             map_wg ? *map_wg : map_wc, h, M, K, H, r, y, gate,
-                            tickets, B, row_bound, nbound, err);
+                            tickets, B, row_bound, nbound, err, wait_ns);
 }
 }  // namespace
 
@@ -290,12 +293,13 @@ cudaError_t launch_conv_tc(const CUtensorMap& map_h, const CUtensorMap& map_wc,
                            const CUtensorMap* map_wg, const __nv_bfloat16* h,
                            int B, int K, int H, int r, __nv_bfloat16* y,
                            float* gate, unsigned* tickets, float* row_bound,
-                           int nbound, int* err, cudaStream_t s) {
+                           int nbound, int* err, cudaStream_t s,
+                           uint64_t wait_ns) {
   if (conv_tc_bc(B * K) == 128)
     return launch_conv_bc<128>(map_h, map_wc, map_wg, h, B, K, H, r, y, gate,
-                               tickets, row_bound, nbound, err, s);
+                               tickets, row_bound, nbound, err, s, wait_ns);
   return launch_conv_bc<32>(map_h, map_wc, map_wg, h, B, K, H, r, y, gate,
-                            tickets, row_bound, nbound, err, s);
+                            tickets, row_bound, nbound, err, s, wait_ns);
 }
 
 }  // namespace dflash

@@ -10,6 +10,11 @@
 
 namespace dflash {
 
+// Default limit of the tensor-core kernels' bounded waits (2 s, far beyond
+// any real wait); dflash_set_wait_limit_ns changes it for later launches of
+// the conv and of the single-CTA LM head.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
 // conv.cu -----------------------------------------------------------------
 template <typename T>
 cudaError_t launch_conv_simt(const T* h, const T* w_conv, int B, int K, int H,
@@ -30,7 +35,8 @@ cudaError_t launch_conv_tc(const CUtensorMap& map_h, const CUtensorMap& map_wc,
                            const CUtensorMap* map_wg, const __nv_bfloat16* h,
                            int B, int K, int H, int r, __nv_bfloat16* y,
                            float* gate, unsigned* tickets, float* row_bound,
-                           int nbound, int* err, cudaStream_t s);
+                           int nbound, int* err, cudaStream_t s,
+                           uint64_t wait_ns = kWaitLimitNs);
 // TMA descriptor of a row-major 8-bit [rows, inner] matrix, 128-byte
 // swizzle (inner a multiple of 16).
 bool make_tmap_u8_2d(CUtensorMap* map, const void* base, uint64_t inner,
@@ -50,7 +56,8 @@ cudaError_t launch_lmhead_tc(const CUtensorMap& map_y, const CUtensorMap& map_w,
                              int* err, int* strips, cudaStream_t s,
                              const float* y_scale = nullptr,
                              const float* w_scale = nullptr,
-                             float* row_bound = nullptr);
+                             float* row_bound = nullptr,
+                             uint64_t wait_ns = kWaitLimitNs);
 
 // quant_e4m3.cu: per-row E4M3 quantization of a bf16 [R, H] matrix
 // (H % 8 == 0): scale[i] = max_k |x_ik| / 448 (1 for a zero row), code =

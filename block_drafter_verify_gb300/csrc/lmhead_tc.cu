@@ -58,7 +58,10 @@ constexpr int BM = 128, BN = 256;
 constexpr int ROW_BYTES = 128;  // bytes of each operand row per stage
 constexpr int A_BYTES = BM * ROW_BYTES;  // 16 KB
 constexpr uint32_t TMEM_COLS = 2 * BN;
-constexpr uint64_t WAIT_NS = 2000000000ull;  // 2 s: far beyond any real wait
+// 2 s: far beyond any real wait.  The limit of the drain waits after a
+// give-up, and of every wait of the CTA-pair variant; the single-CTA
+// variant's other waits take the launch's wait_ns.
+constexpr uint64_t WAIT_NS = 2000000000ull;
 constexpr float LOG2E = 1.4426950408889634f;
 
 // EPI_WARPS epilogue warps: 4 (thread = row, all BN columns of a tile),
@@ -251,8 +254,13 @@ __global__ void __launch_bounds__(Cfg<kPair, kFp8>::THREADS, 1)
                      int V, int row_groups, int strips, TopkPartials P,
                      const float* __restrict__ y_scale,
                      const float* __restrict__ w_scale,
-                     float* __restrict__ row_bound, int* err) {
+                     float* __restrict__ row_bound, int* err,
+                     uint64_t wait_ns) {
   using C = Cfg<kPair, kFp8>;
+  // the launch's limit for the work waits; CTA pairs keep the long one (an
+  // early give-up there could leave one CTA's last copy in flight, counted
+  // on the other CTA's barrier, when the pair exits)
+  const uint64_t lim = kPair ? WAIT_NS : wait_ns;
   using SM = Smem<kPair, kFp8>;
   constexpr int STAGES = C::STAGES;
   constexpr int BK = Elem<kFp8>::BK;
@@ -348,7 +356,7 @@ __global__ void __launch_bounds__(Cfg<kPair, kFp8>::THREADS, 1)
       for (int it = 0; it < my_tiles && ok; ++it) {
         for (int kb = 0; kb < kblocks; ++kb, ++j) {
           if (!tc::mbar_wait_bounded(&bars->empty[stage], phase ^ 1, abort,
-                                     WAIT_NS)) {
+                                     lim)) {
             ok = false;
             break;
           }
@@ -385,7 +393,7 @@ __global__ void __launch_bounds__(Cfg<kPair, kFp8>::THREADS, 1)
       for (int it = 0; it < my_tiles && ok; ++it) {
         const int b = it & 1;
         const uint32_t aph = (it >> 1) & 1;
-        if (!tc::mbar_wait_bounded(&bars->tempty[b], aph ^ 1, abort, WAIT_NS)) {
+        if (!tc::mbar_wait_bounded(&bars->tempty[b], aph ^ 1, abort, lim)) {
           ok = false;
           break;
         }
@@ -393,7 +401,7 @@ __global__ void __launch_bounds__(Cfg<kPair, kFp8>::THREADS, 1)
         const uint32_t d = tmem + b * BN;
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!tc::mbar_wait_bounded(&bars->full[stage], phase, abort,
-                                     WAIT_NS)) {
+                                     lim)) {
             ok = false;
             break;
           }
@@ -498,7 +506,7 @@ __global__ void __launch_bounds__(Cfg<kPair, kFp8>::THREADS, 1)
         }
       }
       const bool got = tc::mbar_wait_bounded(&bars->tfull[b], aph, abort,
-                                             WAIT_NS);
+                                             lim);
       if (!__all_sync(0xffffffffu, got)) {
         *abort = 1;
         ok = false;
@@ -713,7 +721,7 @@ cudaError_t launch_variant(const CUtensorMap& map_y, const CUtensorMap& map_w,
                            int M, int H, int V, int num_sms, TopkPartials P,
                            int* err, int* strips_out, cudaStream_t s,
                            const float* y_scale, const float* w_scale,
-                           float* row_bound) {
+                           float* row_bound, uint64_t wait_ns) {
   int rg = 0, st = 0;
   const int grid = lmhead_tc_grid(M, V, num_sms, &rg, &st, kFp8);
   *strips_out = st;
@@ -727,7 +735,7 @@ cudaError_t launch_variant(const CUtensorMap& map_y, const CUtensorMap& map_w,
                 smem_bytes<false, kFp8>(), s);
     return cudaLaunchKernelEx(&L.cfg, lmhead_tc_kernel<false, kFp8>, map_y,
                               map_w, M, H, V, rg, st, P, y_scale, w_scale,
-                              row_bound, err);
+                              row_bound, err, wait_ns);
   }
   cudaError_t e = cudaFuncSetAttribute(
       lmhead_tc_kernel<true, kFp8>,
@@ -738,7 +746,7 @@ cudaError_t launch_variant(const CUtensorMap& map_y, const CUtensorMap& map_w,
               smem_bytes<true, kFp8>(), s, 2);
   return cudaLaunchKernelEx(&L.cfg, lmhead_tc_kernel<true, kFp8>, map_y,
                             map_w, M, H, V, rg, st, P, y_scale, w_scale,
-                            row_bound, err);
+                            row_bound, err, wait_ns);
 }
 }  // namespace
 
@@ -746,12 +754,14 @@ cudaError_t launch_lmhead_tc(const CUtensorMap& map_y, const CUtensorMap& map_w,
                              int M, int H, int V, int num_sms, TopkPartials P,
                              int* err, int* strips_out, cudaStream_t s,
                              const float* y_scale, const float* w_scale,
-                             float* row_bound) {
+                             float* row_bound, uint64_t wait_ns) {
   if (y_scale && w_scale)
     return launch_variant<true>(map_y, map_w, M, H, V, num_sms, P, err,
-                                strips_out, s, y_scale, w_scale, row_bound);
+                                strips_out, s, y_scale, w_scale, row_bound,
+                                wait_ns);
   return launch_variant<false>(map_y, map_w, M, H, V, num_sms, P, err,
-                               strips_out, s, nullptr, nullptr, row_bound);
+                               strips_out, s, nullptr, nullptr, row_bound,
+                               wait_ns);
 }
 
 }  // namespace dflash

@@ -808,7 +808,8 @@ __global__ void __launch_bounds__(kThreads)
         for (int q = lane; q < nstrip; q += 32) mx = fmaxf(mx, sv[q * kC]);
       int dummy = lane;
       warp_sort32(mx, dummy, lane);
-      if (lane == 0) s_th[g] = __shfl_sync(0xffffffffu, mx, kC - 1);
+      const float th16 = __shfl_sync(0xffffffffu, mx, kC - 1);  // whole warp
+      if (lane == 0) s_th[g] = th16;
     }
     if (act) fold_pairs_smem(sm, ss, nstrip, gw, kG, rm, rs);
     if (lane == 0) { s_mm[g][gw] = rm; s_ms[g][gw] = rs; }
@@ -896,6 +897,13 @@ __global__ void __launch_bounds__(kThreads)
           if (lane == 0) raise_error(err, kErrBadIndex);
           ti = -1;
         }
+      }
+      // the lists come from the LM head; after a failed launch they may
+      // hold anything, and the ids index the embedding tables below
+      if (act && lane < kC && (ti < -1 || ti >= V)) {
+        raise_error(err, kErrBadIndex);
+        ti = -1;
+        tv = -INFINITY;
       }
       if (g == 0) {
         if (lane < kC) {

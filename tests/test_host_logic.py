@@ -46,7 +46,7 @@ def test_workloads():
 
 
 def test_recall_by_position_on_flags():
-    from block_drafter_verify_gb300 import recall_by_position
+    from bench import recall_by_position
     flags = torch.tensor([[1, 1, 0, 1],
                           [1, 1, 1, 1],
                           [0, 1, 1, 1]], dtype=torch.int32)
