@@ -11,6 +11,9 @@ from .binding import (BF16, C, COMMIT_STATS, FP32, STAGES, DFlashError,
                       dflash_pair_score, dflash_path_walk, dflash_philox4x32,
                       dflash_profile_stage, dflash_verify,
                       dflash_verify_noalloc, dflash_workspace_bytes,
+                      dflash_lmhead_topk_shard, dflash_topk_merge_shards,
+                      dflash_verify_shard_stats, dflash_verify_shard_decide,
+                      dflash_verify_shard_draw, SHARD_STATS, SHARD_PLAN,
                       library_path, load)
 
 __all__ = ["BF16", "C", "COMMIT_STATS", "FP32", "STAGES", "DFlashError",
@@ -20,4 +23,7 @@ __all__ = ["BF16", "C", "COMMIT_STATS", "FP32", "STAGES", "DFlashError",
            "dflash_top16_recall", "dflash_set_wait_limit_ns",
            "dflash_pair_score", "dflash_path_walk", "dflash_philox4x32",
            "dflash_profile_stage", "dflash_verify", "dflash_verify_noalloc",
-           "dflash_workspace_bytes", "library_path", "load"]
+           "dflash_workspace_bytes", "dflash_lmhead_topk_shard",
+           "dflash_topk_merge_shards", "dflash_verify_shard_stats",
+           "dflash_verify_shard_decide", "dflash_verify_shard_draw",
+           "SHARD_STATS", "SHARD_PLAN", "library_path", "load"]

@@ -24,7 +24,10 @@ EXPORTS = ("dflash_workspace_bytes", "dflash_lmhead_topk", "dflash_pair_score",
            "dflash_verify_noalloc", "dflash_commit", "dflash_path_viterbi",
            "dflash_top16_recall", "dflash_quantize_e4m3_rows",
            "dflash_draft_e4m3", "dflash_philox4x32", "dflash_profile_stage",
-           "dflash_set_wait_limit_ns", "dflash_check", "dflash_status_string")
+           "dflash_set_wait_limit_ns", "dflash_lmhead_topk_shard",
+           "dflash_topk_merge_shards", "dflash_verify_shard_stats",
+           "dflash_verify_shard_decide", "dflash_verify_shard_draw",
+           "dflash_check", "dflash_status_string")
 STAGES = ("conv", "lmhead", "merge", "pair_score", "walk", "verify",
           "quant")
 
@@ -80,6 +83,18 @@ def load(path: str | None = None):
                                     vp, vp, vp, vp, vp, sz, vp]),
         "dflash_profile_stage": (i32, [i32, vp, vp]),
         "dflash_set_wait_limit_ns": (i32, [u64]),
+        "dflash_lmhead_topk_shard": (i32, [vp, vp, vp, i32, i32, i32, i32,
+                                           i32, i32, vp, vp, vp, vp, vp, sz,
+                                           vp]),
+        "dflash_topk_merge_shards": (i32, [vp, vp, vp, vp, i32, i32, vp, vp,
+                                           vp, vp]),
+        "dflash_verify_shard_stats": (i32, [vp, vp, vp, i32, i32, i32, i32,
+                                            i32, f32, vp, vp, sz, vp]),
+        "dflash_verify_shard_decide": (i32, [vp, i32, vp, vp, vp, i32, i32,
+                                             i32, f32, u64, u64, vp, vp, vp,
+                                             vp]),
+        "dflash_verify_shard_draw": (i32, [vp, vp, vp, vp, i32, i32, i32,
+                                           i32, i32, f32, vp, vp, sz, vp]),
         "dflash_check": (i32, [vp]),
         "dflash_status_string": (ctypes.c_char_p, [i32]),
     }
@@ -300,6 +315,67 @@ def dflash_set_wait_limit_ns(ns):
     """Limit of the tensor-core kernels' bounded waits in later launches
     (0 = the default 2 s); for tests of the timeout path."""
     _call("dflash_set_wait_limit_ns", int(ns))
+
+
+SHARD_STATS, SHARD_PLAN = 20, 8
+
+
+def dflash_lmhead_topk_shard(h, conv_w, w_lm_shard, v0, part_v, part_i,
+                             part_m, part_s, ws, stream=None):
+    """h [B,K,H]; conv_w [2H,H] or None; w_lm_shard [V_shard,H] (rows of
+    the vocabulary from v0); outputs part_v [B*K,16] f32, part_i [B*K,16]
+    i32 (global ids), part_m, part_s [B*K] f32; ws uint8 (kind 0 for
+    V_shard)."""
+    B, K, H = h.shape
+    Vs = w_lm_shard.shape[0]
+    _want(part_i, torch.int32, "part_i")
+    _call("dflash_lmhead_topk_shard", _ptr(h), _ptr(conv_w), _ptr(w_lm_shard),
+          B, K, H, Vs, int(v0), _dtype(h), _ptr(part_v), _ptr(part_i),
+          _ptr(part_m), _ptr(part_s), _ptr(ws), ws.numel(), _stream(stream))
+
+
+def dflash_topk_merge_shards(part_v, part_i, part_m, part_s, topv, topi, lse,
+                             stream=None):
+    """part_v, part_i [S,M,16]; part_m, part_s [S,M] -> topv, topi [M,16],
+    lse [M]."""
+    S, M = part_m.shape
+    _call("dflash_topk_merge_shards", _ptr(part_v), _ptr(part_i),
+          _ptr(part_m), _ptr(part_s), S, M, _ptr(topv), _ptr(topi), _ptr(lse),
+          _stream(stream))
+
+
+def dflash_verify_shard_stats(target_shard, draft, topi, v0, V, T, stats, ws,
+                              stream=None):
+    """target_shard [B,K+1,V_shard] f32 (ids from v0 of V); draft [B,K];
+    topi [B,K,16] -> stats [B*(K+1), SHARD_STATS] f32; ws uint8 (kind 1
+    for V_shard), kept for dflash_verify_shard_draw."""
+    B, K1, Vs = target_shard.shape
+    _want(target_shard, torch.float32, "target_shard")
+    _call("dflash_verify_shard_stats", _ptr(target_shard), _ptr(draft),
+          _ptr(topi), B, K1 - 1, Vs, int(v0), int(V), float(T), _ptr(stats),
+          _ptr(ws), ws.numel(), _stream(stream))
+
+
+def dflash_verify_shard_decide(stats, draft, topi, q, V, T, seed, cycle,
+                               n_accepted, out_tok, plan, stream=None):
+    """stats [S, B*(K+1), SHARD_STATS] -> n_accepted [B], out_tok [B,K+1],
+    plan [B, SHARD_PLAN] f32."""
+    S = stats.shape[0]
+    B, K = draft.shape
+    _call("dflash_verify_shard_decide", _ptr(stats), S, _ptr(draft),
+          _ptr(topi), _ptr(q), B, K, int(V), float(T),
+          int(seed) & (2**64 - 1), int(cycle) & (2**64 - 1),
+          _ptr(n_accepted), _ptr(out_tok), _ptr(plan), _stream(stream))
+
+
+def dflash_verify_shard_draw(target_shard, plan, topi, q, shard, v0, T,
+                             out_tok, ws, stream=None):
+    """The draws the plan gives to shard `shard` (its target_shard and the
+    ws of its stats call) into out_tok."""
+    B, K1, Vs = target_shard.shape
+    _call("dflash_verify_shard_draw", _ptr(target_shard), _ptr(plan),
+          _ptr(topi), _ptr(q), int(shard), B, K1 - 1, Vs, int(v0), float(T),
+          _ptr(out_tok), _ptr(ws), ws.numel(), _stream(stream))
 
 
 def dflash_check(stream=None):

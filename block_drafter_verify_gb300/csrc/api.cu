@@ -241,7 +241,8 @@ template <typename T>
 dflash_status lmhead_impl(const T* h, const T* conv_w, const T* w_lm, int B,
                           int K, int H, int V, float* topv, int* topi,
                           float* lse, void* ws, const DeviceState& d,
-                          cudaStream_t s) {
+                          cudaStream_t s, TopkPartials* P_out = nullptr,
+                          int* strips_out = nullptr) {
   void* yv = nullptr;
   TopkPartials P;
   lmhead_ws_layout(B, K, H, V, ws, &yv, &P);
@@ -263,6 +264,11 @@ dflash_status lmhead_impl(const T* h, const T* conv_w, const T* w_lm, int B,
     e = launch_lmhead_simt<T>(a, w_lm, M, H, V, ns, P, s);
   }
   if (e != cudaSuccess) return DFLASH_ERR_CUDA;
+  if (P_out) {  // the caller merges
+    *P_out = P;
+    *strips_out = ns;
+    return DFLASH_OK;
+  }
   StageTimer tm(kStMerge, s);
   return cuda_status(launch_topk_merge(P, ns, M, topv, topi, lse, s));
 }
@@ -541,6 +547,130 @@ dflash_status dflash_verify(const float* target_logits, const int32_t* draft,
   return verify_run(target_logits, draft, topi, q, B, K, V, T, seed, cycle,
                     n_accepted, out_tok, w,
                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+dflash_status dflash_lmhead_topk_shard(const void* h, const void* conv_w,
+                                       const void* w_lm_shard, int B, int K,
+                                       int H, int V_shard, int v0,
+                                       dflash_dtype dt, float* part_v,
+                                       int32_t* part_i, float* part_m,
+                                       float* part_s, void* ws,
+                                       size_t ws_bytes,
+                                       dflash_stream_t stream) {
+  REQUIRE(h && w_lm_shard && part_v && part_i && part_m && part_s && ws);
+  REQUIRE(sizes_ok(B, K, H, V_shard) && H >= 8 && H % 8 == 0);
+  REQUIRE(v0 >= 0 && (long long)v0 + V_shard <= (1LL << 30));
+  REQUIRE(dt == DFLASH_BF16 || dt == DFLASH_FP32);
+  REQUIRE(aligned(ws, 256) && aligned(h, 16) && aligned(w_lm_shard, 16));
+  REQUIRE(!conv_w || aligned(conv_w, 16));
+  REQUIRE(ws_bytes >=
+          lmhead_ws_layout(B, K, H, V_shard, nullptr, nullptr, nullptr));
+  DeviceState* d = nullptr;
+  dflash_status st = device_state(&d);
+  if (st != DFLASH_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  TopkPartials P;
+  int strips = 0;
+  if (dt == DFLASH_FP32)
+    st = lmhead_impl<float>(static_cast<const float*>(h),
+                            static_cast<const float*>(conv_w),
+                            static_cast<const float*>(w_lm_shard), B, K, H,
+                            V_shard, nullptr, nullptr, nullptr, ws, *d, s, &P,
+                            &strips);
+  else
+    st = lmhead_tc_path(static_cast<const __nv_bfloat16*>(h),
+                        static_cast<const __nv_bfloat16*>(conv_w),
+                        static_cast<const __nv_bfloat16*>(w_lm_shard), B, K,
+                        H, V_shard, nullptr, nullptr, nullptr, ws, *d, s,
+                        nullptr, 0, nullptr, nullptr, &P, &strips);
+  if (st != DFLASH_OK) return st;
+  StageTimer tm(kStMerge, s);
+  return cuda_status(launch_topk_merge(P, strips, B * K, part_v, part_i,
+                                       nullptr, s, v0, part_m, part_s));
+}
+
+dflash_status dflash_topk_merge_shards(const float* part_v,
+                                       const int32_t* part_i,
+                                       const float* part_m,
+                                       const float* part_s, int S, int M,
+                                       float* topv, int32_t* topi, float* lse,
+                                       dflash_stream_t stream) {
+  REQUIRE(part_v && part_i && part_m && part_s && topv && topi && lse);
+  REQUIRE(S >= 1 && S <= DFLASH_MAX_SHARDS && M >= 1 && M <= (1 << 20));
+  DeviceState* d = nullptr;
+  dflash_status st = device_state(&d);
+  if (st != DFLASH_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  StageTimer tm(kStMerge, s);
+  return cuda_status(launch_shard_merge(part_v, part_i, part_m, part_s, S, M,
+                                        topv, topi, lse, s));
+}
+
+dflash_status dflash_verify_shard_stats(const float* target_shard,
+                                        const int32_t* draft,
+                                        const int32_t* topi, int B, int K,
+                                        int V_shard, int v0, int V, float T,
+                                        float* stats, void* ws,
+                                        size_t ws_bytes,
+                                        dflash_stream_t stream) {
+  REQUIRE(target_shard && draft && topi && stats && ws);
+  REQUIRE(sizes_ok(B, K, 0, V_shard) && sizes_ok(B, K, 0, V));
+  REQUIRE(v0 >= 0 && (long long)v0 + V_shard <= V);
+  REQUIRE(T >= 0.f && T < INFINITY);
+  REQUIRE(aligned(ws, 256) && aligned(target_shard, 16) && aligned(stats, 4));
+  REQUIRE(ws_bytes >= verify_ws_layout(B, K, V_shard, nullptr, nullptr));
+  DeviceState* d = nullptr;
+  dflash_status st = device_state(&d);
+  if (st != DFLASH_OK) return st;
+  VerifyWs w;
+  verify_ws_layout(B, K, V_shard, ws, &w);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(w.counters, 0, w.counter_bytes, s) != cudaSuccess)
+    return DFLASH_ERR_CUDA;
+  StageTimer tm(kStVerifyRows, s);
+  return cuda_status(launch_verify(target_shard, draft, topi, nullptr, B, K,
+                                   V_shard, T, 0, 0, nullptr, nullptr, w,
+                                   d->sms, d->err, s, v0, stats));
+}
+
+dflash_status dflash_verify_shard_decide(
+    const float* stats, int S, const int32_t* draft, const int32_t* topi,
+    const float* q, int B, int K, int V, float T, uint64_t seed,
+    uint64_t cycle, int32_t* n_accepted, int32_t* out_tok, float* plan,
+    dflash_stream_t stream) {
+  REQUIRE(stats && draft && topi && q && n_accepted && out_tok && plan);
+  REQUIRE(S >= 1 && S <= DFLASH_MAX_SHARDS && sizes_ok(B, K, 0, V));
+  REQUIRE(T >= 0.f && T < INFINITY);
+  DeviceState* d = nullptr;
+  dflash_status st = device_state(&d);
+  if (st != DFLASH_OK) return st;
+  return cuda_status(launch_verify_shard_decide(
+      stats, S, draft, topi, q, B, K, V, T, seed, cycle, n_accepted, out_tok,
+      plan, d->err, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+dflash_status dflash_verify_shard_draw(const float* target_shard,
+                                       const float* plan,
+                                       const int32_t* topi, const float* q,
+                                       int shard, int B, int K, int V_shard,
+                                       int v0, float T, int32_t* out_tok,
+                                       void* ws, size_t ws_bytes,
+                                       dflash_stream_t stream) {
+  REQUIRE(target_shard && plan && topi && q && out_tok && ws);
+  REQUIRE(shard >= 0 && shard < DFLASH_MAX_SHARDS);
+  REQUIRE(sizes_ok(B, K, 0, V_shard) && v0 >= 0 &&
+          (long long)v0 + V_shard <= (1LL << 30));
+  REQUIRE(T >= 0.f && T < INFINITY);
+  REQUIRE(aligned(ws, 256) && aligned(target_shard, 16));
+  REQUIRE(ws_bytes >= verify_ws_layout(B, K, V_shard, nullptr, nullptr));
+  DeviceState* d = nullptr;
+  dflash_status st = device_state(&d);
+  if (st != DFLASH_OK) return st;
+  VerifyWs w;
+  verify_ws_layout(B, K, V_shard, ws, &w);
+  return cuda_status(launch_verify_shard_draw(
+      target_shard, plan, topi, q, shard, B, K, V_shard, v0, T, out_tok, w,
+      d->err, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 dflash_status dflash_philox4x32(const uint32_t* ctr, uint64_t seed,

@@ -75,8 +75,16 @@ template <typename T>
 cudaError_t launch_lmhead_simt(const T* y, const T* w_lm, int M, int H, int V,
                                int nstrip, TopkPartials P, cudaStream_t s);
 int lmhead_simt_strips(int M, int V, int num_sms);
+// With out_m / out_s (a vocabulary shard whose ids start at id_off): ids
+// offset by id_off, the rows' (max, sum) pairs instead of lse.
 cudaError_t launch_topk_merge(TopkPartials P, int nstrip, int M, float* topv,
-                              int* topi, float* lse, cudaStream_t s);
+                              int* topi, float* lse, cudaStream_t s,
+                              int id_off = 0, float* out_m = nullptr,
+                              float* out_s = nullptr);
+// S shards' partials [S][M][16] + [S][M] pairs -> topv, topi, lse.
+cudaError_t launch_shard_merge(const float* pv, const int* pi, const float* pm,
+                               const float* ps, int S, int M, float* topv,
+                               int* topi, float* lse, cudaStream_t s);
 
 // pair_score.cu -----------------------------------------------------------
 // After the LM head, for a precomputed gate [B*K, r] fp32: merge of the
@@ -124,12 +132,35 @@ struct VerifyWs {
 };
 constexpr int kVerifyMaxChunks = 64;  // row chunks (CTAs) per target row
 size_t verify_ws_layout(int B, int K, int V, void* base, VerifyWs* out);
-// The caller zeroes ws.counters on stream s first.
+// The caller zeroes ws.counters on stream s first.  With `stats` (a
+// vocabulary shard [v0, v0 + V) of the rows): the rows' shard statistics
+// (kShardStats words per row) instead of the accept tests and draws, and
+// the segment pairs kept in ws for the shard's draw.
+constexpr int kShardStats = DFLASH_SHARD_STATS;
+constexpr int kShardPlan = DFLASH_SHARD_PLAN;
 cudaError_t launch_verify(const float* L, const int* draft, const int* topi,
                           const float* q, int B, int K, int V, float T,
                           uint64_t seed, uint64_t cycle, int* n_accepted,
                           int* out_tok, const VerifyWs& ws, int num_sms,
-                          int* err, cudaStream_t s);
+                          int* err, cudaStream_t s, int v0 = 0,
+                          float* stats = nullptr);
+// Every shard's statistics [S][B*(K+1)][kShardStats] -> n, the emitted
+// tokens (at T > 0 the drawn one is left -1 for the owner shard's draw) and
+// each sequence's draw plan [B][kShardPlan].
+cudaError_t launch_verify_shard_decide(const float* stats, int S,
+                                       const int* draft, const int* topi,
+                                       const float* q, int B, int K, int V,
+                                       float T, uint64_t seed, uint64_t cycle,
+                                       int* n_accepted, int* out_tok,
+                                       float* plan, int* err, cudaStream_t s);
+// The draws the plan gives to shard `shard` (its logits L [B*(K+1), V],
+// ids v0..v0+V-1, ws from its statistics launch).
+cudaError_t launch_verify_shard_draw(const float* L, const float* plan,
+                                     const int* topi, const float* q,
+                                     int shard, int B, int K, int V, int v0,
+                                     float T, int* out_tok,
+                                     const VerifyWs& ws, int* err,
+                                     cudaStream_t s);
 
 // philox --------------------------------------------------------------------
 cudaError_t launch_philox(const uint32_t* ctr, uint64_t seed, uint32_t* out,

@@ -98,10 +98,13 @@ __global__ void __launch_bounds__(kThreads)
   }
 }
 
-// One CTA of eight warps per row: the merge of merge.cuh.
+// One CTA of eight warps per row: the merge of merge.cuh.  With out_m
+// (a vocabulary shard whose first id is id_off): ids offset by id_off and
+// the row's (max, sum) pair written to out_m / out_s instead of lse.
 __global__ void __launch_bounds__(kMergeWarps * 32)
     topk_merge_kernel(TopkPartials P, int nstrip, int M, float* topv,
-                      int* topi, float* lse) {
+                      int* topi, float* lse, int id_off, float* out_m,
+                      float* out_s) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int m = blockIdx.x;
   __shared__ float s_v[kMergeWarps][kC], s_m[kMergeWarps], s_s[kMergeWarps];
@@ -114,6 +117,51 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
   __syncthreads();
   if (warp != 0) return;
   merge_combine(s_v, s_i, s_m, s_s, lane, tv, ti, rm, rs);
+  if (lane < kC) {
+    topv[(size_t)m * kC + lane] = tv;
+    topi[(size_t)m * kC + lane] = ti >= 0 ? ti + id_off : -1;
+  }
+  if (lane == 0) {
+    if (out_m) {
+      out_m[m] = rm;
+      out_s[m] = rs;
+    } else {
+      lse[m] = rm + logf(rs);
+    }
+  }
+}
+
+// Merge of S shards' partials [S][M][16] (global ids) and [S][M] pairs into
+// the rows' top-16 and logsumexp: one warp per row, shards in order, each
+// list folded by one bitonic merge (skipped when its best entry cannot
+// enter the top 16).
+__global__ void shard_merge_kernel(const float* __restrict__ pv,
+                                   const int* __restrict__ pi,
+                                   const float* __restrict__ pm,
+                                   const float* __restrict__ ps, int S,
+                                   int M, float* __restrict__ topv,
+                                   int* __restrict__ topi,
+                                   float* __restrict__ lse) {
+  const int lane = threadIdx.x & 31;
+  const int m = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+  if (m >= M) return;
+  const int k = lane < kC ? lane : 31 - lane;  // lanes 16..31: reversed
+  float tv = -INFINITY, rm = -INFINITY, rs = 0.f;
+  int ti = -1;
+  for (int sh = 0; sh < S; ++sh) {
+    const size_t r = (size_t)sh * M + m;
+    lse_combine(rm, rs, pm[r], ps[r], 1.f);
+    const float bv = pv[r * kC];
+    const int bi = pi[r * kC];
+    if (!ranks_ahead(bv, bi, __shfl_sync(0xffffffffu, tv, kC - 1),
+                     __shfl_sync(0xffffffffu, ti, kC - 1)))
+      continue;
+    float v = lane < kC ? tv : pv[r * kC + k];
+    int i = lane < kC ? ti : pi[r * kC + k];
+    bitonic_merge32(v, i, lane);
+    tv = v;
+    ti = i;
+  }
   if (lane < kC) {
     topv[(size_t)m * kC + lane] = tv;
     topi[(size_t)m * kC + lane] = ti;
@@ -147,9 +195,19 @@ cudaError_t launch_lmhead_simt(const T* y, const T* w_lm, int M, int H, int V,
 }
 
 cudaError_t launch_topk_merge(TopkPartials P, int nstrip, int M, float* topv,
-                              int* topi, float* lse, cudaStream_t s) {
+                              int* topi, float* lse, cudaStream_t s,
+                              int id_off, float* out_m, float* out_s) {
   topk_merge_kernel<<<M, kMergeWarps * 32, 0, s>>>(P, nstrip, M, topv, topi,
-                                                   lse);
+                                                   lse, id_off, out_m, out_s);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_shard_merge(const float* pv, const int* pi, const float* pm,
+                               const float* ps, int S, int M, float* topv,
+                               int* topi, float* lse, cudaStream_t s) {
+  const int per_cta = 8;
+  shard_merge_kernel<<<(M + per_cta - 1) / per_cta, 32 * per_cta, 0, s>>>(
+      pv, pi, pm, ps, S, M, topv, topi, lse);
   return cudaGetLastError();
 }
 

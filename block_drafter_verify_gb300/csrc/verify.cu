@@ -97,12 +97,174 @@ __device__ __forceinline__ void load_segment(const float* x, int base, int V,
   }
 }
 
+// Shared memory of one row's draw (row_draw).
+struct DrawSmem {
+  int seg, use_raw, pick, last;
+  float rem;
+  float W[kWarps];
+};
+
+// The inverse-CDF draw inside one target row x[0, V), by every thread of
+// the CTA.  Token v weighs w(v) = 2^((x_v - m) s2) minus, unless raw, the
+// correction of the candidate it is (s_ci / s_qz: w = max(0, w - q Z));
+// the row's 2048-token segments weigh their (max, sum) pair (s_pair)
+// rescaled to m plus the corrections of the candidates inside them
+// (s_corr), clamped at zero.  Target theta: u * (the row's total) when
+// theta_abs < 0, where a zero residual total switches to raw weights;
+// else theta_abs with raw = raw_given.  Warp 0 locates the segment (lane l
+// owns segments l*per .. l*per+per-1: one inclusive scan of the lane
+// totals and a ballot); the CTA then takes the smallest token of the
+// segment whose running sum exceeds theta (8 contiguous tokens per thread,
+// block scan in a fixed tree).  Returns the token on every thread (the
+// segment's last token of positive weight if rounding leaves the target at
+// the segment's end), or -1 if no segment has weight.
+__device__ __forceinline__ int row_draw(
+    const float* __restrict__ x, int V, int nseg, const float2* s_pair,
+    const int* s_ci, const float* s_qz, const float* s_corr, float m,
+    float s2, float u, float theta_abs, bool raw_given, DrawSmem& sm,
+    int* err) {
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const float nb = -m * s2;
+  if (wid == 0) {
+    const int per = (nseg + 31) / 32;
+    auto seg_weight = [&](int k, bool raw) -> float {
+      if (k >= nseg) return 0.f;
+      const float2 p = s_pair[k];
+      float w = (p.x == -INFINITY) ? 0.f : p.y * ex2f((p.x - m) * s2);
+      if (!raw) {
+#pragma unroll
+        for (int j = 0; j < kC; ++j)
+          if (s_ci[j] >= 0 && s_ci[j] / kSegTokens == k) w += s_corr[j];
+      }
+      return fmaxf(w, 0.f);
+    };
+    int f_seg = -1, f_raw = 0;
+    float f_rem = 0.f;
+    const int raw0 = theta_abs >= 0.f ? (raw_given ? 1 : 0) : 0;
+    const int raw1 = theta_abs >= 0.f ? raw0 : 1;
+    for (int raw = raw0; raw <= raw1 && f_seg < 0; ++raw) {
+      float ltot = 0.f;
+      for (int i = 0; i < per; ++i) ltot += seg_weight(lane * per + i, raw);
+      float incl = ltot;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float tt = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += tt;
+      }
+      const float total = __shfl_sync(0xffffffffu, incl, 31);
+      if (!(total > 0.f)) continue;  // degenerate residual: draw from p
+      const float theta = theta_abs >= 0.f ? theta_abs : u * total;
+      const unsigned hit = __ballot_sync(0xffffffffu, ltot > 0.f && incl > theta);
+      const unsigned live = __ballot_sync(0xffffffffu, ltot > 0.f);
+      // theta rounded up to the total: the last lane with weight
+      const int Ls = hit ? __ffs(hit) - 1 : 31 - __clz(live);
+      if (lane == Ls) {
+        float a = incl - ltot;
+        int last = -1;
+        for (int i = 0; i < per; ++i) {
+          const float w = seg_weight(lane * per + i, raw);
+          if (w > 0.f) last = lane * per + i;
+          if (w > 0.f && a + w > theta) {
+            f_seg = lane * per + i;
+            f_rem = theta - a;
+            break;
+          }
+          a += w;
+        }
+        if (f_seg < 0) {
+          f_seg = last;
+          f_rem = INFINITY;
+        }
+      }
+      f_seg = __shfl_sync(0xffffffffu, f_seg, Ls);
+      f_rem = __shfl_sync(0xffffffffu, f_rem, Ls);
+      f_raw = raw;
+    }
+    if (lane == 0) {
+      sm.seg = f_seg;
+      sm.rem = f_rem;
+      sm.use_raw = f_raw;
+      sm.pick = -1;
+      sm.last = -1;
+    }
+  }
+  __syncthreads();
+  const int seg = sm.seg;
+  if (seg < 0) {  // no weight anywhere (the row maximum has weight 1)
+    if (tid == 0) raise_error(err, kErrBadIndex);
+    return -1;
+  }
+  // the 2048 tokens of the segment: 8 contiguous tokens per thread
+  const bool use_raw = sm.use_raw;
+  const int t0 = seg * kSegTokens + tid * 8;
+  float w8[8];
+  float tsum = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int v = t0 + i;
+    float wv = 0.f;
+    if (v < V) {
+      wv = weight(x[v], s2, nb);
+      if (!use_raw) {
+#pragma unroll
+        for (int j = 0; j < kC; ++j)
+          if (s_ci[j] == v) wv = fmaxf(wv - s_qz[j], 0.f);
+      }
+    }
+    w8[i] = wv;
+    tsum += wv;
+  }
+  // block exclusive scan of tsum (fixed tree)
+  float incl = tsum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float tt = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += tt;
+  }
+  if (lane == 31) sm.W[wid] = incl;
+  __syncthreads();
+  float pre = 0.f, segtot = 0.f;
+  for (int w = 0; w < kWarps; ++w) {
+    if (w < wid) pre += sm.W[w];
+    segtot += sm.W[w];
+  }
+  const float excl = pre + incl - tsum;
+  // rounding may leave the target at or past the recomputed total
+  const float rem = fminf(sm.rem, segtot * (1.f - 0x1p-22f));
+  int last = -1;
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    if (w8[i] > 0.f) last = t0 + i;
+  if (last >= 0) atomicMax(&sm.last, last);
+  if (tsum > 0.f && excl <= rem && rem < excl + tsum) {
+    float a = excl;
+    int pick = -1;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      a += w8[i];
+      if (pick < 0 && a > rem) pick = t0 + i;
+    }
+    atomicMax(&sm.pick, pick >= 0 ? pick : last);
+  }
+  __syncthreads();
+  return sm.pick >= 0 ? sm.pick : sm.last;
+}
+
+// kStats: the row statistics of one vocabulary shard [v0, v0 + V) (the
+// rows hold the shard's V logits; token ids are global): the main pass
+// keeps its segment pairs in the workspace for the shard's later draw, and
+// the row's last CTA writes the row's entry of `stats` (kShardStats words:
+// max and sum, or max and argmax at T = 0; the logits of the candidates
+// and of the draft the shard holds; a mask of which it holds) instead of
+// the accept test and draw.
+template <bool kStats>
 __global__ void __launch_bounds__(kThreads)
     verify_kernel(const float* __restrict__ L, const int* __restrict__ draft,
                   const int* __restrict__ topi, const float* __restrict__ q,
                   int B, int K, int V, int nchunk, int bpc, float T, float s2,
                   uint64_t seed, uint64_t cycle, int* __restrict__ n_accepted,
-                  int* __restrict__ out_tok, VerifyWs ws, int* err, int vec4) {
+                  int* __restrict__ out_tok, VerifyWs ws, int* err, int vec4,
+                  int v0, float* __restrict__ stats) {
   const int row = blockIdx.x, c = blockIdx.y, tid = threadIdx.x;
   const int lane = tid & 31, wid = tid >> 5;
   const int K1 = K + 1, rows = B * K1;
@@ -115,8 +277,9 @@ __global__ void __launch_bounds__(kThreads)
 
   __shared__ float s_a[kWarps];
   __shared__ int s_i[kWarps];
-  __shared__ int s_flag, s_seg, s_use_raw, s_acc, s_need;
-  __shared__ float s_W[kWarps], s_rem, s_m;
+  __shared__ int s_flag, s_acc, s_need;
+  __shared__ float s_m;
+  __shared__ DrawSmem s_draw;
   __shared__ int s_ci[kC];
   __shared__ float s_qz[kC], s_corr[kC];
 
@@ -129,7 +292,7 @@ __global__ void __launch_bounds__(kThreads)
   if (wid == 0 && has_draft) {
     if (lane < kC) {
       r_tok = topi[(b * K + t) * kC + lane];
-      r_q = q[(b * K + t) * kC + lane];
+      r_q = kStats ? 0.f : q[(b * K + t) * kC + lane];
     } else if (lane == kC) {
       r_tok = draft[b * K + t];
     }
@@ -144,12 +307,14 @@ __global__ void __launch_bounds__(kThreads)
   const int sc1 = min(nseg, (c + 1) * bpc * kWarps);
   const int nmine = sc0 + wid < sc1 ? (sc1 - (sc0 + wid) + kWarps - 1) / kWarps : 0;
   float r_x = 0.f;  // target logit at r_tok (fetched after the first segment)
+  // the row holds r_tok (a shard holds ids v0 .. v0 + V - 1)
+  const bool r_own = r_tok >= v0 && r_tok - v0 < V;
   for (int j = 0; j < nmine; ++j) {
     const int seg = sc0 + wid + kWarps * j;
     const int base = seg * kSegTokens;
     float4 f[16];
     load_segment(x, base, V, lane, vec4, f);
-    if (j == 0 && wid == 0 && r_tok >= 0 && r_tok < V) r_x = x[r_tok];
+    if (j == 0 && wid == 0 && r_own) r_x = x[r_tok - v0];
     if (greedy) {
       float chk = 0.f;
 #pragma unroll
@@ -186,11 +351,11 @@ __global__ void __launch_bounds__(kThreads)
       if (lane == 0) {
         const float2 pr = make_float2(mx, sum);
         if (nchunk == 1) s_pair[seg] = pr;
-        else ws.part[(size_t)row * nseg + seg] = pr;
+        if (nchunk > 1 || kStats) ws.part[(size_t)row * nseg + seg] = pr;
       }
     }
   }
-  if (wid == 0 && nmine == 0 && r_tok >= 0 && r_tok < V) r_x = x[r_tok];
+  if (wid == 0 && nmine == 0 && r_own) r_x = x[r_tok - v0];
   if (__any_sync(0xffffffffu, bad) && lane == 0) raise_error(err, kErrNonfinite);
   if (greedy) {  // chunk argmax: lanes, then warps, in a fixed tree
 #pragma unroll
@@ -264,6 +429,19 @@ __global__ void __launch_bounds__(kThreads)
         fold_lse(ra, rs, oa, os, s2);
       }
     }
+    if constexpr (kStats) {
+      // a shard may hold no mass of a row: (-inf, 0) folds to nothing
+      float* st = stats + (size_t)row * kShardStats;
+      const unsigned own = __ballot_sync(0xffffffffu, lane <= kC && r_own);
+      if (lane == 0) {
+        st[0] = ra;
+        st[1] = greedy ? __int_as_float(ri == 0x7fffffff ? -1 : v0 + ri) : rs;
+        st[kShardStats - 1] = __uint_as_float(own);
+      }
+      if (lane < kC) st[2 + lane] = r_own ? r_x : 0.f;
+      if (lane == kC) st[2 + kC] = r_own ? r_x : 0.f;
+      return;
+    }
     if (ra == -INFINITY) {  // every logit of the row is -inf
       if (lane == 0) raise_error(err, kErrNonfinite);
       ri = 0; ra = 0.f; rs = 1.f;
@@ -324,134 +502,16 @@ __global__ void __launch_bounds__(kThreads)
       }
     }
   }
+  if constexpr (kStats) return;  // warp 0 wrote the row's statistics
   if (!greedy) {
     __syncthreads();
   }
   if (!greedy && s_need) {
     // ---- draw of row (b, t): residual max(0, p - q), or p for t = K ------
-    // Warp 0 locates the segment.  Lane l owns the contiguous segments
-    // l*per .. l*per+per-1; a segment's weight is its (max, sum) pair
-    // rescaled to the row max, plus the corrections of the candidates
-    // inside it (in candidate order), clamped at zero.  One inclusive scan
-    // of the lane totals and one ballot find the lane, which walks its
-    // segments.  A zero residual total switches to p itself.
-    const float m = s_m;
-    const float nb = -m * s2;
-    if (wid == 0) {
-      const int per = (nseg + 31) / 32;
-      const float u = philox_uniform(seed, b, K, kPurposeResample, cycle);
-      auto seg_weight = [&](int k, bool raw) -> float {
-        if (k >= nseg) return 0.f;
-        const float2 p = s_pair[k];
-        float w = (p.x == -INFINITY) ? 0.f : p.y * ex2f((p.x - m) * s2);
-        if (!raw) {
-#pragma unroll
-          for (int j = 0; j < kC; ++j)
-            if (s_ci[j] >= 0 && s_ci[j] / kSegTokens == k) w += s_corr[j];
-        }
-        return fmaxf(w, 0.f);
-      };
-      int f_seg = -1, f_raw = 0;
-      float f_rem = 0.f;
-      for (int raw = 0; raw < 2 && f_seg < 0; ++raw) {
-        float ltot = 0.f;
-        for (int i = 0; i < per; ++i) ltot += seg_weight(lane * per + i, raw);
-        float incl = ltot;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const float tt = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += tt;
-        }
-        const float total = __shfl_sync(0xffffffffu, incl, 31);
-        if (!(total > 0.f)) continue;  // degenerate residual: draw from p
-        const float theta = u * total;
-        const unsigned hit = __ballot_sync(0xffffffffu, ltot > 0.f && incl > theta);
-        const unsigned live = __ballot_sync(0xffffffffu, ltot > 0.f);
-        // u * total rounded up to the total: the last lane with weight
-        const int Ls = hit ? __ffs(hit) - 1 : 31 - __clz(live);
-        if (lane == Ls) {
-          float a = incl - ltot;
-          int last = -1;
-          for (int i = 0; i < per; ++i) {
-            const float w = seg_weight(lane * per + i, raw);
-            if (w > 0.f) last = lane * per + i;
-            if (w > 0.f && a + w > theta) {
-              f_seg = lane * per + i;
-              f_rem = theta - a;
-              break;
-            }
-            a += w;
-          }
-          if (f_seg < 0) {
-            f_seg = last;
-            f_rem = INFINITY;
-          }
-        }
-        f_seg = __shfl_sync(0xffffffffu, f_seg, Ls);
-        f_rem = __shfl_sync(0xffffffffu, f_rem, Ls);
-        f_raw = raw;
-      }
-      if (lane == 0) {
-        s_seg = f_seg;
-        s_rem = f_rem;
-        s_use_raw = f_raw;
-      }
-    }
-    __syncthreads();
-    int seg = s_seg;
-    if (seg < 0) {  // cannot happen: the row maximum has weight 1
-      if (tid == 0) raise_error(err, kErrBadIndex);
-      seg = 0;
-    }
-    // the 2048 tokens of the segment: 8 contiguous tokens per thread
-    const bool use_raw = s_use_raw;
-    const int t0 = seg * kSegTokens + tid * 8;
-    float w8[8];
-    float tsum = 0.f;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int v = t0 + i;
-      float wv = 0.f;
-      if (v < V) {
-        wv = weight(x[v], s2, nb);
-        if (!use_raw) {
-#pragma unroll
-          for (int j = 0; j < kC; ++j)
-            if (s_ci[j] == v) wv = fmaxf(wv - s_qz[j], 0.f);
-        }
-      }
-      w8[i] = wv;
-      tsum += wv;
-    }
-    // block exclusive scan of tsum (fixed tree)
-    float incl = tsum;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const float tt = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += tt;
-    }
-    if (lane == 31) s_W[wid] = incl;
-    __syncthreads();
-    float pre = 0.f, segtot = 0.f;
-    for (int w = 0; w < kWarps; ++w) {
-      if (w < wid) pre += s_W[w];
-      segtot += s_W[w];
-    }
-    const float excl = pre + incl - tsum;
-    // rounding may leave the target at or past the recomputed total
-    const float rem = fminf(s_rem, segtot * (1.f - 0x1p-22f));
-    if (tsum > 0.f && excl <= rem && rem < excl + tsum) {
-      float a = excl;
-      int pick = -1, last = -1;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        if (w8[i] > 0.f) last = t0 + i;
-        a += w8[i];
-        if (pick < 0 && a > rem) pick = t0 + i;
-      }
-      ws.row_tok[row] = pick >= 0 ? pick : last;
-      __threadfence();  // before the sequence ticket below
-    }
+    const float u = philox_uniform(seed, b, K, kPurposeResample, cycle);
+    const int tok = row_draw(x, V, nseg, s_pair, s_ci, s_qz, s_corr, s_m, s2,
+                             u, -1.f, false, s_draw, err);
+    if (tid == 0) ws.row_tok[row] = tok;
   }
   if (!greedy && tid == 0) ws.row_acc[row] = s_acc;
 
@@ -474,6 +534,174 @@ __global__ void __launch_bounds__(kThreads)
     else if (lane == n) tok = __ldcg(&ws.row_tok[b * K1 + n]);
     out_tok[b * K1 + lane] = tok;
   }
+}
+
+// ---- vocabulary shards: decide and draw ----------------------------------
+// Plan of one sequence's draw (kShardPlan words): [0] owner shard (int,
+// -1: none), [1] target theta within the owner's residual (or p) weights,
+// [2] the row's global max m, [3] its Z = sum 2^((x - m) s2), [4] raw
+// weights (int), [5] the row n (int).
+
+// One warp per sequence, lane t = row t (t <= K): the rows' shard
+// statistics folded in shard order (global max and Z, or the argmax), the
+// accept tests with the draft's logit from the shard that holds it, n, the
+// emitted prefix, and for T > 0 the draw plan of row n: each shard's
+// residual mass (its rescaled sum plus the corrections of the candidates it
+// holds, clamped at zero; raw sums when the total residual is zero or
+// n = K), theta = u * total, the first shard whose running mass exceeds
+// theta and the remainder within it.
+__global__ void verify_shard_decide_kernel(
+    const float* __restrict__ stats, int S, const int* __restrict__ draft,
+    const int* __restrict__ topi, const float* __restrict__ q, int B, int K,
+    int V, float T, float s2, uint64_t seed, uint64_t cycle,
+    int* __restrict__ n_accepted, int* __restrict__ out_tok,
+    float* __restrict__ plan, int* err) {
+  const int lane = threadIdx.x & 31;
+  const int b = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+  if (b >= B) return;
+  const int K1 = K + 1, rows = B * K1;
+  const bool greedy = T == 0.f;
+  const int t = lane;
+  const int row = b * K1 + min(t, K);
+  float m = -INFINITY, Z = 0.f, xd = 0.f;
+  int bi = 0x7fffffff;
+  bool have_d = false;
+  for (int sh = 0; sh < S; ++sh) {
+    const float* st = stats + ((size_t)sh * rows + row) * kShardStats;
+    if (greedy) {
+      const int id = __float_as_int(st[1]);
+      if (id >= 0 && arg_better(st[0], id, m, bi)) { m = st[0]; bi = id; }
+    } else {
+      fold_lse(m, Z, st[0], st[1], s2);
+    }
+    if ((__float_as_uint(st[kShardStats - 1]) >> kC) & 1u) {
+      xd = st[2 + kC];
+      have_d = true;
+    }
+  }
+  if (t <= K && (m == -INFINITY || (greedy && bi == 0x7fffffff))) {
+    raise_error(err, kErrNonfinite);  // every logit of the row is -inf
+    m = 0.f; Z = 1.f; bi = 0;
+  }
+  int acc = 1;
+  int d = -1;
+  if (t < K) {
+    d = draft[b * K + t];
+    if (d < 0 || d >= V || !have_d) {
+      raise_error(err, kErrBadIndex);
+      acc = 0;
+    } else if (greedy) {
+      acc = d == bi;
+    } else {
+      float qd = 0.f;
+      int j = 0;
+      for (; j < kC; ++j)
+        if (topi[(b * K + t) * kC + j] == d) { qd = q[(b * K + t) * kC + j]; break; }
+      if (j == kC) raise_error(err, kErrBadIndex);
+      const float pd = weight(xd, s2, -m * s2) / Z;
+      const float u = philox_uniform(seed, b, t, kPurposeAccept, cycle);
+      acc = u * qd < pd;
+    }
+  }
+  const unsigned rej = __ballot_sync(0xffffffffu, t < K && !acc);
+  const int n = rej ? __ffs(rej) - 1 : K;
+  if (lane == 0) n_accepted[b] = n;
+  if (t <= K) out_tok[b * K1 + t] = t < n ? d : (t == n && greedy ? bi : -1);
+  if (t != n) return;
+  float* pl = plan + (size_t)b * kShardPlan;
+  pl[0] = __int_as_float(-1);
+  pl[5] = __int_as_float(n);
+  if (greedy) return;
+  // row n's draw: residual masses per shard (raw for the bonus row)
+  const float u = philox_uniform(seed, b, K, kPurposeResample, cycle);
+  float tot_res = 0.f, tot_raw = 0.f;
+  auto shard_mass = [&](int sh, bool raw) -> float {
+    const float* st = stats + ((size_t)sh * rows + row) * kShardStats;
+    float w = st[0] == -INFINITY ? 0.f : st[1] * ex2f((st[0] - m) * s2);
+    if (!raw && n < K) {
+      const unsigned own = __float_as_uint(st[kShardStats - 1]);
+      for (int j = 0; j < kC; ++j)
+        if ((own >> j) & 1u) {
+          const float qz = q[(b * K + n) * kC + j] * Z;
+          w -= fminf(weight(st[2 + j], s2, -m * s2), qz);
+        }
+    }
+    return fmaxf(w, 0.f);
+  };
+  for (int sh = 0; sh < S; ++sh) {
+    tot_res += shard_mass(sh, false);
+    tot_raw += shard_mass(sh, true);
+  }
+  const bool raw = !(tot_res > 0.f) || n == K;
+  const float total = raw ? tot_raw : tot_res;
+  const float theta = u * total;
+  int owner = -1, last = -1;
+  float a = 0.f, rem = 0.f;
+  for (int sh = 0; sh < S; ++sh) {
+    const float w = shard_mass(sh, raw);
+    if (w > 0.f) last = sh;
+    if (w > 0.f && a + w > theta) { owner = sh; rem = theta - a; break; }
+    a += w;
+  }
+  if (owner < 0) {  // theta rounded up to the total: the last shard's end
+    owner = last;
+    rem = INFINITY;
+  }
+  if (owner < 0) raise_error(err, kErrBadIndex);  // no mass anywhere
+  pl[0] = __int_as_float(owner);
+  pl[1] = rem;
+  pl[2] = m;
+  pl[3] = Z;
+  pl[4] = __int_as_float(raw ? 1 : 0);
+}
+
+// The draw of each sequence whose plan names this shard, one CTA per
+// sequence: the shard's segment pairs of row n (left in its workspace by
+// the statistics launch), the corrections of the candidates it holds, and
+// row_draw with the plan's target, max, Z and weights.
+__global__ void __launch_bounds__(kThreads)
+    verify_shard_draw_kernel(const float* __restrict__ L,
+                             const float* __restrict__ plan,
+                             const int* __restrict__ topi,
+                             const float* __restrict__ q, int shard, int B,
+                             int K, int V, int v0, float s2,
+                             int* __restrict__ out_tok, VerifyWs ws,
+                             int* err) {
+  const int b = blockIdx.x, tid = threadIdx.x;
+  const int K1 = K + 1;
+  const int nseg = (V + kSegTokens - 1) / kSegTokens;
+  const float* pl = plan + (size_t)b * kShardPlan;
+  if (__float_as_int(pl[0]) != shard) return;
+  const int n = __float_as_int(pl[5]);
+  const float theta = pl[1], m = pl[2], Z = pl[3];
+  const bool raw = __float_as_int(pl[4]) != 0;
+  const int row = b * K1 + n;
+  const float* x = L + (size_t)row * V;
+  extern __shared__ float2 s_pair[];
+  __shared__ int s_ci[kC];
+  __shared__ float s_qz[kC], s_corr[kC];
+  __shared__ DrawSmem s_draw;
+  for (int k = tid; k < nseg; k += kThreads)
+    s_pair[k] = __ldcg(&ws.part[(size_t)row * nseg + k]);
+  if (tid < kC) {
+    int ci = -1;
+    float qz = 0.f, corr = 0.f;
+    if (n < K) {
+      const int c = topi[(b * K + n) * kC + tid];
+      if (c >= v0 && c - v0 < V) {
+        ci = c - v0;
+        qz = q[(b * K + n) * kC + tid] * Z;
+        corr = -fminf(weight(x[ci], s2, -m * s2), qz);
+      }
+    }
+    s_ci[tid] = ci;
+    s_qz[tid] = qz;
+    s_corr[tid] = corr;
+  }
+  __syncthreads();
+  const int tok = row_draw(x, V, nseg, s_pair, s_ci, s_qz, s_corr, m, s2,
+                           0.f, fmaxf(theta, 0.f), raw, s_draw, err);
+  if (tid == 0) out_tok[b * K1 + n] = tok >= 0 ? v0 + tok : -1;
 }
 
 __global__ void philox_kernel(const uint32_t* __restrict__ ctr, uint64_t seed,
@@ -520,7 +748,7 @@ cudaError_t launch_verify(const float* L, const int* draft, const int* topi,
                           const float* q, int B, int K, int V, float T,
                           uint64_t seed, uint64_t cycle, int* n_accepted,
                           int* out_tok, const VerifyWs& ws, int num_sms,
-                          int* err, cudaStream_t s) {
+                          int* err, cudaStream_t s, int v0, float* stats) {
   const int rows = B * (K + 1);
   const int nseg = (V + kSegTokens - 1) / kSegTokens;
   const int blocks_per_row = (V + kBlockTokens - 1) / kBlockTokens;
@@ -537,14 +765,51 @@ cudaError_t launch_verify(const float* L, const int* draft, const int* topi,
   const int nchunk = (blocks_per_row + bpc - 1) / bpc;
   const float s2 = T > 0.f ? kLog2e / T : 0.f;
   const size_t smem = (size_t)nseg * sizeof(float2);
+  auto kern = stats ? verify_kernel<true> : verify_kernel<false>;
   if (smem > 48 * 1024) {
     const cudaError_t e = cudaFuncSetAttribute(
-        verify_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
-  verify_kernel<<<dim3(rows, nchunk), kThreads, smem, s>>>(
+  kern<<<dim3(rows, nchunk), kThreads, smem, s>>>(
       L, draft, topi, q, B, K, V, nchunk, bpc, T, s2, seed, cycle, n_accepted,
-      out_tok, ws, err, vec4);
+      out_tok, ws, err, vec4, v0, stats);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_verify_shard_decide(const float* stats, int S,
+                                       const int* draft, const int* topi,
+                                       const float* q, int B, int K, int V,
+                                       float T, uint64_t seed, uint64_t cycle,
+                                       int* n_accepted, int* out_tok,
+                                       float* plan, int* err, cudaStream_t s) {
+  const float s2 = T > 0.f ? kLog2e / T : 0.f;
+  const int per_cta = 4;  // warps (sequences) per CTA
+  verify_shard_decide_kernel<<<(B + per_cta - 1) / per_cta, 32 * per_cta, 0,
+                               s>>>(stats, S, draft, topi, q, B, K, V, T, s2,
+                                    seed, cycle, n_accepted, out_tok, plan,
+                                    err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_verify_shard_draw(const float* L, const float* plan,
+                                     const int* topi, const float* q,
+                                     int shard, int B, int K, int V, int v0,
+                                     float T, int* out_tok,
+                                     const VerifyWs& ws, int* err,
+                                     cudaStream_t s) {
+  if (!(T > 0.f)) return cudaSuccess;  // T = 0: decided with the argmax
+  const float s2 = kLog2e / T;
+  const int nseg = (V + kSegTokens - 1) / kSegTokens;
+  const size_t smem = (size_t)nseg * sizeof(float2);
+  if (smem > 48 * 1024) {
+    const cudaError_t e = cudaFuncSetAttribute(
+        verify_shard_draw_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  verify_shard_draw_kernel<<<B, kThreads, smem, s>>>(
+      L, plan, topi, q, shard, B, K, V, v0, s2, out_tok, ws, err);
   return cudaGetLastError();
 }
 

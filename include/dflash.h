@@ -82,6 +82,9 @@ typedef enum { DFLASH_BF16 = 0, DFLASH_FP32 = 1 } dflash_dtype;
 #define DFLASH_CANDIDATES 16
 #define DFLASH_MAX_K 16
 #define DFLASH_MAX_RANK 256
+#define DFLASH_MAX_SHARDS 64   /* vocabulary shards of one merge / decide */
+#define DFLASH_SHARD_STATS 20  /* words per target row of shard statistics */
+#define DFLASH_SHARD_PLAN 8    /* words per sequence of a shard draw plan */
 
 /* Workspace needed by dflash_lmhead_topk (which = 0), dflash_verify
  * (which = 1), dflash_draft (which = 2) or dflash_draft_e4m3 (which = 3)
@@ -370,6 +373,94 @@ dflash_status dflash_top16_recall(const float* target_logits,
                                   const int32_t* topi, int B, int K, int V,
                                   int32_t* target_argmax, int32_t* in_top16,
                                   dflash_stream_t s);
+
+/*
+ * Vocabulary shards.  With the vocabulary split into S contiguous ranges
+ * [v0, v0 + V_shard) (an LM head and target logits too large for one
+ * device, or a target that is itself split by vocabulary), each shard
+ * computes what depends on its range only, the shards' small summaries are
+ * gathered (S x a few words per row), and a merge gives exactly what the
+ * whole-vocabulary calls give: the same candidates and tokens, logsumexp
+ * and probabilities within fp32 rounding of another summation order.  The
+ * pages have no sharded form; the decomposition follows from the
+ * definitions of the top-16, the logsumexp, the accept test and the
+ * inverse CDF (each a fold over the vocabulary).  Every call runs on the
+ * caller's device and stream; moving the summaries between devices (an
+ * all-gather) is the caller's, and one device can run all shards in turn.
+ *
+ * dflash_lmhead_topk_shard: steps a1 + a2 of dflash_lmhead_topk on the
+ * shard's LM-head rows w_lm_shard [V_shard, H] (the conv is recomputed on
+ * every shard; it is small).  Writes the shard's partial of every row:
+ *   part_v, part_i [B*K, 16]  the shard's 16 best logits and their global
+ *                             ids (v0 + row of w_lm_shard), descending,
+ *                             ties to the lower id, padding (-inf, -1)
+ *   part_m, part_s [B*K]      the shard's max of U_t and sum exp(U_t - max)
+ *   ws >= dflash_workspace_bytes(0, B, K, H, V_shard) bytes.
+ * Requirements as dflash_lmhead_topk; v0 >= 0.
+ */
+dflash_status dflash_lmhead_topk_shard(const void* h, const void* conv_w,
+                                       const void* w_lm_shard, int B, int K,
+                                       int H, int V_shard, int v0,
+                                       dflash_dtype dt, float* part_v,
+                                       int32_t* part_i, float* part_m,
+                                       float* part_s, void* ws,
+                                       size_t ws_bytes, dflash_stream_t s);
+
+/* The S shards' partials gathered in shard order (part_v, part_i
+ * [S, M, 16]; part_m, part_s [S, M]; M = B*K) merged into topv, topi
+ * [M, 16] and lse [M], as dflash_lmhead_topk writes them.  1 <= S <= 64. */
+dflash_status dflash_topk_merge_shards(const float* part_v,
+                                       const int32_t* part_i,
+                                       const float* part_m,
+                                       const float* part_s, int S, int M,
+                                       float* topv, int32_t* topi, float* lse,
+                                       dflash_stream_t s);
+
+/*
+ * Steps a5 + a6 by vocabulary shard, in three calls.
+ *
+ * 1. dflash_verify_shard_stats, on each shard: the shard's target logits
+ *    target_shard [B, K+1, V_shard] (ids v0 .. v0 + V_shard - 1 of a
+ *    vocabulary of V) -> stats [B*(K+1), DFLASH_SHARD_STATS] fp32 words,
+ *    per target row: [0] the shard's max logit, [1] at T > 0 its sum of
+ *    exp((x - max) / T), at T = 0 its first argmax (global id, int bits),
+ *    [2..17] the logits of the row's 16 candidates the shard holds,
+ *    [18] that of the draft, [19] a mask (uint bits) of which it holds
+ *    (bit j: candidate j, bit 16: the draft).  The shard's segment sums
+ *    stay in ws (>= dflash_workspace_bytes(1, B, K, 0, V_shard) bytes) for
+ *    step 3.
+ * 2. dflash_verify_shard_decide, with every shard's stats gathered in
+ *    shard order ([S, B*(K+1), DFLASH_SHARD_STATS]): each row's max and Z
+ *    (or argmax), the accept tests as dflash_verify takes them, n_accepted
+ *    and out_tok; at T = 0 out_tok is final.  At T > 0 the token at n is
+ *    drawn in step 3 (out_tok holds -1 there until then) from the plan
+ *    [B, DFLASH_SHARD_PLAN]: the shard whose part of the residual (or of p)
+ *    holds the draw, and the remaining mass within it.
+ * 3. dflash_verify_shard_draw, on each shard (index `shard`, with its ws
+ *    from step 1): the draws the plan gives to that shard, written to
+ *    out_tok.  Nothing to do at T = 0.
+ * Same uniforms, tests and draws as dflash_verify ("Lossless, with
+ * conditions I did not used to state", drafter's coat page); the sums are
+ * folded per shard, then over shards in shard order.
+ */
+dflash_status dflash_verify_shard_stats(const float* target_shard,
+                                        const int32_t* draft,
+                                        const int32_t* topi, int B, int K,
+                                        int V_shard, int v0, int V, float T,
+                                        float* stats, void* ws,
+                                        size_t ws_bytes, dflash_stream_t s);
+dflash_status dflash_verify_shard_decide(
+    const float* stats, int S, const int32_t* draft, const int32_t* topi,
+    const float* q, int B, int K, int V, float T, uint64_t seed,
+    uint64_t cycle, int32_t* n_accepted, int32_t* out_tok, float* plan,
+    dflash_stream_t s);
+dflash_status dflash_verify_shard_draw(const float* target_shard,
+                                       const float* plan,
+                                       const int32_t* topi, const float* q,
+                                       int shard, int B, int K, int V_shard,
+                                       int v0, float T, int32_t* out_tok,
+                                       void* ws, size_t ws_bytes,
+                                       dflash_stream_t s);
 
 /* Philox4x32-10 of n counters (ctr [n, 4] uint32, device) under key
  * (seed lo, seed hi) into out [n, 4] uint32 (device): the generator the
