@@ -125,17 +125,24 @@ size_t lmhead_ws_layout(int B, int K, int H, int V, void* base, void** y,
 }
 
 // Workspace of dflash_draft: the LM-head workspace, then the gate
-// [B*K, DFLASH_MAX_RANK] fp32, then one walk ticket per sequence.
+// [B*K, DFLASH_MAX_RANK] fp32, one walk ticket per sequence, and every
+// row's walk step from each predecessor slot: the chosen slot [B*K, 16]
+// int32 and q [B*K, 16, 16] fp32.
 size_t draft_ws_layout(int B, int K, int H, int V, void* base, float** gate,
-                       unsigned** tickets = nullptr) {
+                       unsigned** tickets = nullptr, int** walk_j = nullptr,
+                       float** walk_q = nullptr) {
+  const size_t M = (size_t)B * K;
   const size_t lm = align256(lmhead_ws_layout(B, K, H, V, nullptr, nullptr,
                                               nullptr));
-  const size_t g = align256((size_t)B * K * DFLASH_MAX_RANK * sizeof(float));
-  if (gate)
-    *gate = reinterpret_cast<float*>(static_cast<char*>(base) + lm);
-  if (tickets)
-    *tickets = reinterpret_cast<unsigned*>(static_cast<char*>(base) + lm + g);
-  return align256(lm + g + (size_t)B * sizeof(unsigned));
+  const size_t g = align256(M * DFLASH_MAX_RANK * sizeof(float));
+  const size_t tk = align256((size_t)B * sizeof(unsigned));
+  const size_t wj = align256(M * kC * sizeof(int));
+  char* p = static_cast<char*>(base);
+  if (gate) *gate = reinterpret_cast<float*>(p + lm);
+  if (tickets) *tickets = reinterpret_cast<unsigned*>(p + lm + g);
+  if (walk_j) *walk_j = reinterpret_cast<int*>(p + lm + g + tk);
+  if (walk_q) *walk_q = reinterpret_cast<float*>(p + lm + g + tk + wj);
+  return align256(lm + g + tk + wj + M * kC * kC * sizeof(float));
 }
 
 // Workspace of dflash_draft_e4m3: dflash_draft's, then the E4M3 codes of y
@@ -455,7 +462,9 @@ dflash_status dflash_draft(const void* h, const void* conv_w, const void* w_lm,
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   float* gate = nullptr;
   unsigned* tickets = nullptr;
-  draft_ws_layout(B, K, H, V, ws, &gate, &tickets);
+  int* walk_j = nullptr;
+  float* walk_q = nullptr;
+  draft_ws_layout(B, K, H, V, ws, &gate, &tickets, &walk_j, &walk_q);
   cudaError_t e;
   if (dt == DFLASH_BF16 && conv_w) {
     // The gate rides along with the conv (which also zeroes the walk
@@ -474,7 +483,7 @@ dflash_status dflash_draft(const void* h, const void* conv_w, const void* w_lm,
     return cuda_status(launch_draft_tail<bf>(
         P, strips, anchor, gate, static_cast<const bf*>(e_in),
         static_cast<const bf*>(e_out), B, K, V, r, T, seed, cycle, topv, topi,
-        lse, scores, slot, draft, q, tickets, d->err, s));
+        lse, scores, slot, draft, q, tickets, walk_j, walk_q, d->err, s));
   } else {
     st = dflash_lmhead_topk(h, conv_w, w_lm, B, K, H, V, dt, topv, topi, lse,
                             ws, ws_bytes, stream);
@@ -514,7 +523,9 @@ dflash_status dflash_draft_e4m3(
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   float* gate = nullptr;
   unsigned* tickets = nullptr;
-  draft_ws_layout(B, K, H, V, ws, &gate, &tickets);
+  int* walk_j = nullptr;
+  float* walk_q = nullptr;
+  draft_ws_layout(B, K, H, V, ws, &gate, &tickets, &walk_j, &walk_q);
   E4m3Head q8{w_lm_codes, w_lm_scale, nullptr, nullptr};
   draft_e4m3_ws_layout(B, K, H, V, ws, &q8.y_codes, &q8.y_scale);
   using bf = __nv_bfloat16;
@@ -530,7 +541,7 @@ dflash_status dflash_draft_e4m3(
   return cuda_status(launch_draft_tail<bf>(
       P, strips, anchor, gate, static_cast<const bf*>(e_in),
       static_cast<const bf*>(e_out), B, K, V, r, T, seed, cycle, topv, topi,
-      lse, scores, slot, draft, q, tickets, d->err, s));
+      lse, scores, slot, draft, q, tickets, walk_j, walk_q, d->err, s));
 }
 
 dflash_status dflash_verify(const float* target_logits, const int32_t* draft,

@@ -89,7 +89,8 @@ cudaError_t launch_shard_merge(const float* pv, const int* pi, const float* pm,
 // pair_score.cu -----------------------------------------------------------
 // After the LM head, for a precomputed gate [B*K, r] fp32: merge of the
 // strip partials, pair scores and walk in one launch (tickets [B], zeroed
-// by the conv launch, pick each sequence's walker).
+// by the conv launch, pick each sequence's walker; walk_j [B*K, 16] and
+// walk_q [B*K, 16, 16] hold every row's step from each predecessor slot).
 template <typename T>
 cudaError_t launch_draft_tail(TopkPartials P, int nstrip, const int* anchor,
                               const float* gate, const T* e_in,
@@ -97,7 +98,8 @@ cudaError_t launch_draft_tail(TopkPartials P, int nstrip, const int* anchor,
                               float T_, uint64_t seed, uint64_t cycle,
                               float* topv, int* topi, float* lse,
                               float* scores, int* slot, int* draft, float* q,
-                              unsigned* tickets, int* err, cudaStream_t s);
+                              unsigned* tickets, int* walk_j, float* walk_q,
+                              int* err, cudaStream_t s);
 // Pair scores from a precomputed gate [B*K, r] fp32 (gathers + bilinear).
 template <typename T>
 cudaError_t launch_pair_score_gated(const float* topv, const int* topi,

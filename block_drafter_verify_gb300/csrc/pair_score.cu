@@ -273,7 +273,8 @@ __device__ __forceinline__ void score_row(
     const T* st, bool vec, const int* pred, const int* cand,
     const float* g_row, const T* __restrict__ e_in,
     const T* __restrict__ e_out, int r, float* work,
-    const float* __restrict__ topv_row, float* __restrict__ out) {
+    const float* __restrict__ topv_row, float* __restrict__ out,
+    float* s_out = nullptr) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   // fp32 tiles with 16-byte aligned rows when r allows (float4 reads)
   const bool r4 = (r % 4) == 0;
@@ -352,8 +353,14 @@ __device__ __forceinline__ void score_row(
   }
   const float tj = topv_row[jj];
   const bool cj = cand[jj] >= 0;
-  out[i * kC + jj] = (pred[i] >= 0 && cj) ? tj + sc : -INFINITY;
-  out[(i + 8) * kC + jj] = (pred[i + 8] >= 0 && cj) ? tj + sd : -INFINITY;
+  const float o0 = (pred[i] >= 0 && cj) ? tj + sc : -INFINITY;
+  const float o1 = (pred[i + 8] >= 0 && cj) ? tj + sd : -INFINITY;
+  out[i * kC + jj] = o0;
+  out[(i + 8) * kC + jj] = o1;
+  if (s_out) {
+    s_out[i * kC + jj] = o0;
+    s_out[(i + 8) * kC + jj] = o1;
+  }
 }
 
 // Token of (table, slot i) for row m: candidates topi[m, i] (table 1) or
@@ -445,7 +452,7 @@ __device__ __forceinline__ void split3_bf16(float x, __nv_bfloat16& hi,
 __device__ __forceinline__ void score_row_mma(
     const __nv_bfloat16* st, int ld, const int* pred, const int* cand,
     const float* g_row, int r, float* work, const float* topv_row,
-    float* __restrict__ out) {
+    float* __restrict__ out, float* s_out) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int kp = ld - 8;                        // padded k extent
   __nv_bfloat16* xs = reinterpret_cast<__nv_bfloat16*>(work);  // [3][16][ld]
@@ -500,7 +507,9 @@ __device__ __forceinline__ void score_row_mma(
   const int i = tid / kC, j = tid % kC;  // kThreads == 256 == 16 x 16
   const float v = ((part[tid] + part[256 + tid]) + part[512 + tid]) +
                   part[768 + tid];
-  out[tid] = (pred[i] >= 0 && cand[j] >= 0) ? topv_row[j] + v : -INFINITY;
+  const float o = (pred[i] >= 0 && cand[j] >= 0) ? topv_row[j] + v : -INFINITY;
+  out[tid] = o;
+  s_out[tid] = o;
 }
 
 template <typename T>
@@ -733,7 +742,9 @@ __global__ void __launch_bounds__(kThreads)
                       int* __restrict__ topi, float* __restrict__ lse,
                       float* __restrict__ scores, int* __restrict__ slot,
                       int* __restrict__ draft, float* __restrict__ q,
-                      unsigned* __restrict__ tickets, int* err) {
+                      unsigned* __restrict__ tickets,
+                      int* __restrict__ walk_j, float* __restrict__ walk_q,
+                      int* err) {
   extern __shared__ float4 smem4[];
   float* g_row = reinterpret_cast<float*>(smem4);    // [256]
   float* work = g_row + DFLASH_MAX_RANK;              // score tiles / walk
@@ -744,13 +755,14 @@ __global__ void __launch_bounds__(kThreads)
   __shared__ int s_tok[2][kC];
   __shared__ float s_topv[kC];
   __shared__ int s_ids[DFLASH_MAX_K * kC];
-  __shared__ float s_tot[DFLASH_MAX_K * kC], s_mx[DFLASH_MAX_K * kC];
   __shared__ int s_arg[DFLASH_MAX_K * kC];
+  __shared__ float s_S[kC * kC];
+  __shared__ int s_prev[DFLASH_MAX_K], s_pick[DFLASH_MAX_K];
   __shared__ float s_mv[2][kWarps / 2][kC], s_mm[2][kWarps / 2],
       s_ms[2][kWarps / 2];
   __shared__ int s_mi[2][kWarps / 2][kC];
-  __shared__ float s_th[2], s_sv[2][64];
-  __shared__ int s_wt[2][kWarps / 2], s_si[2][64];
+  __shared__ float s_th[2], s_sv[2][64], s_lm[2][32], s_bv[2][kC];
+  __shared__ int s_wt[2][kWarps / 2], s_si[2][64], s_bi[2][kC];
   __shared__ int s_flag;
   const int m = blockIdx.x, b = m / K, t = m % K;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -803,13 +815,20 @@ __global__ void __launch_bounds__(kThreads)
     const float* ss = sm + nstrip;
     float rm = -INFINITY, rs = 0.f;
     if (gw == 0) {
+      // th: the lane maximum ranked 16th (values descending, lanes
+      // ascending on equal values), by counting the maxima ranked ahead
       float mx = -INFINITY;
       if (act)
         for (int q = lane; q < nstrip; q += 32) mx = fmaxf(mx, sv[q * kC]);
-      int dummy = lane;
-      warp_sort32(mx, dummy, lane);
-      const float th16 = __shfl_sync(0xffffffffu, mx, kC - 1);  // whole warp
-      if (lane == 0) s_th[g] = th16;
+      s_lm[g][lane] = mx;
+      __syncwarp();
+      int ahead = 0;
+#pragma unroll 8
+      for (int k = 0; k < 32; ++k) {
+        const float o = s_lm[g][k];
+        ahead += (o > mx || (o == mx && k < lane)) ? 1 : 0;
+      }
+      if (ahead == kC - 1) s_th[g] = mx;
     }
     if (act) fold_pairs_smem(sm, ss, nstrip, gw, kG, rm, rs);
     if (lane == 0) { s_mm[g][gw] = rm; s_ms[g][gw] = rs; }
@@ -862,25 +881,34 @@ __global__ void __launch_bounds__(kThreads)
     }
     if (lane < kC) { s_mv[g][gw][lane] = tv; s_mi[g][gw][lane] = ti; }
     __syncthreads();
+    // the survivors' top 16: survivor lt goes to its rank (the number of
+    // survivors ranked ahead of it, so every rank below 16 is taken once)
+    if (act && direct) {
+      if (lt < total) {
+        const float v = s_sv[g][lt];
+        const int i = s_si[g][lt];
+        int ahead = 0;  // equal entries (padding: -inf, -1) in list order
+        for (int k = 0; k < total; ++k) {
+          const float ov = s_sv[g][k];
+          const int oi = s_si[g][k];
+          ahead += (ranks_ahead(ov, oi, v, i) ||
+                    (ov == v && oi == i && k < lt)) ? 1 : 0;
+        }
+        if (ahead < kC) { s_bv[g][ahead] = v; s_bi[g][ahead] = i; }
+      }
+      if (total + lt < kC) {  // fewer than 16 survivors: padding
+        s_bv[g][total + lt] = -INFINITY;
+        s_bi[g][total + lt] = -1;
+      }
+    }
+    __syncthreads();
     if (gw == 0) {
       if (act) {
         for (int w2 = 1; w2 < kG; ++w2)
           lse_combine(rm, rs, s_mm[g][w2], s_ms[g][w2], 1.f);
-        if (direct) {
-          // sort both halves of the 64 survivors, then keep the best 16
-          // of their union (a: lanes 0-15; b reversed: lanes 16-31)
-          float va = s_sv[g][lane], vb = s_sv[g][lane + 32];
-          int ia = s_si[g][lane], ib = s_si[g][lane + 32];
-          warp_sort32(va, ia, lane);
-          if (total > 32) {
-            warp_sort32(vb, ib, lane);
-            const float bv = __shfl_sync(0xffffffffu, vb, 31 - lane);
-            const int bi = __shfl_sync(0xffffffffu, ib, 31 - lane);
-            if (lane >= kC) { va = bv; ia = bi; }
-            bitonic_merge32(va, ia, lane);
-          }
-          tv = va;
-          ti = ia;
+        if (direct) {  // placed by rank below
+          tv = s_bv[g][lane & (kC - 1)];
+          ti = s_bi[g][lane & (kC - 1)];
         } else {
           const int k = lane < kC ? lane : 31 - lane;
           for (int w2 = 1; w2 < kG; ++w2) {
@@ -936,51 +964,38 @@ __global__ void __launch_bounds__(kThreads)
   if (tc_scores) {
     if constexpr (kBf16)
       score_row_mma(st, mma_ld(r), s_tok[0], s_tok[1], g_row, r, work,
-                    s_topv, scores + (size_t)m * kC * kC);
+                    s_topv, scores + (size_t)m * kC * kC, s_S);
   } else {
     score_row<kThreads>(st, vec, s_tok[0], s_tok[1], g_row, e_in, e_out, r,
-                        work, s_topv, scores + (size_t)m * kC * kC);
+                        work, s_topv, scores + (size_t)m * kC * kC, s_S);
   }
+  __syncthreads();
 
-  // ---- 4. the last row of sequence b walks it -----------------------------
-  __syncthreads();
-  if (tid == 0) {
-    __threadfence();
-    s_flag = (atomicAdd(&tickets[b], 1u) == (unsigned)(K - 1));
-  }
-  __syncthreads();
-  if (!s_flag) return;
-  __threadfence();
-  // The quantities of every step the walk could take: for each position t
-  // and predecessor slot p (row t*16 + p of the sequence's scores), half a
-  // warp computes what the walk's step computes for that row — the argmax
-  // at T = 0, else the row max, the weights' prefix sums and total — in the
-  // same operations and order, so the serial walk below only looks them up
-  // (and recomputes the chosen row's 16 weights for q).
-  float* sc_s = work;                       // [K*16][16] scores
-  float* c_s = work + K * kC * kC;          // [K*16][16] prefix sums
+  // ---- 3b. the walk's step from every predecessor slot of this row ------
+  // Half-warp i takes predecessor slot i (the 16 scores S[i][.]): the
+  // argmax at T = 0 (lowest slot on ties), else the weights
+  // w = exp((S - max) / T), their running sums and total, and the slot the
+  // walk's uniform of position t selects (the first running sum above
+  // u * total; the last slot of positive weight if rounding leaves none;
+  // -1 if no slot has weight), and q = w / total.  The uniform depends on
+  // (b, t) only, so every predecessor's step is known here and the walk
+  // itself only follows the chosen slots.
   {
-    const float4* src =
-        reinterpret_cast<const float4*>(scores + (size_t)b * K * kC * kC);
-    for (int i = tid; i < K * kC * kC / 4; i += kThreads)
-      reinterpret_cast<float4*>(sc_s)[i] = __ldcg(src + i);
-    for (int i = tid; i < K * kC; i += kThreads)
-      s_ids[i] = __ldcg(topi + (size_t)b * K * kC + i);
-  }
-  __syncthreads();
-  const int half = lane >> 4, hl = lane & 15;
-  for (int row = warp * 2 + half; row < K * kC; row += kWarps * 2) {
-    const float v = sc_s[row * kC + hl];
+    const int i = tid / kC, jj = tid % kC;
+    const float v = s_S[tid];
+    int jstar;
+    float qv;
     if (Tt == 0.f) {
       float bv = v;
-      int bi = hl;
+      int bi = jj;
 #pragma unroll
       for (int o = 8; o; o >>= 1) {
         const float ov = __shfl_xor_sync(0xffffffffu, bv, o, 16);
         const int oi = __shfl_xor_sync(0xffffffffu, bi, o, 16);
         if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
       }
-      if (hl == 0) s_arg[row] = bi;
+      jstar = bi;
+      qv = jj == bi ? 1.f : 0.f;
     } else {
       float mx = v;
 #pragma unroll
@@ -991,50 +1006,65 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
       for (int o = 1; o < 16; o <<= 1) {
         const float n = __shfl_up_sync(0xffffffffu, cum, o, 16);
-        if (hl >= o) cum += n;
+        if (jj >= o) cum += n;
       }
-      c_s[row * kC + hl] = cum;
-      if (hl == 15) { s_tot[row] = cum; s_mx[row] = mx; }
+      const float tot = __shfl_sync(0xffffffffu, cum, 15, 16);
+      const float u = philox_uniform(seed, b, t, kPurposeWalk, cycle);
+      const int sh = lane & 16;  // this half-warp's lanes in the ballots
+      const unsigned above =
+          (__ballot_sync(0xffffffffu, cum > u * tot) >> sh) & 0xFFFFu;
+      const unsigned live =
+          (__ballot_sync(0xffffffffu, wv > 0.f) >> sh) & 0xFFFFu;
+      jstar = above ? __ffs(above) - 1 : (live ? 31 - __clz(live) : -1);
+      qv = tot > 0.f ? wv / tot : 0.f;
+    }
+    walk_q[(size_t)m * kC * kC + tid] = qv;
+    if (jj == 0) walk_j[(size_t)m * kC + i] = jstar;
+  }
+
+  // ---- 4. the last row of sequence b walks it -----------------------------
+  // (the barrier orders the CTA's score and walk-step stores before thread
+  // 0's fence, which makes them visible before its ticket)
+  __syncthreads();
+  if (tid == 0) {
+    __threadfence();
+    s_flag = (atomicAdd(&tickets[b], 1u) == (unsigned)(K - 1));
+  }
+  __syncthreads();
+  if (!s_flag) return;
+  __threadfence();
+  // every row's steps are known: follow the chosen slots from the anchor's
+  // row (slot 0 of position 0), then write each position's q, slot, draft
+  for (int i2 = tid; i2 < K * kC; i2 += kThreads) {
+    s_arg[i2] = __ldcg(walk_j + (size_t)b * K * kC + i2);
+    s_ids[i2] = __ldcg(topi + (size_t)b * K * kC + i2);
+  }
+  __syncthreads();
+  if (tid == 0) {
+    int prev = 0;
+    for (int tt = 0; tt < K; ++tt) {
+      int j = s_arg[tt * kC + prev];
+      if (j < 0) {  // the walk reached a slot with no weight
+        raise_error(err, kErrBadIndex);
+        j = 0;
+      }
+      s_prev[tt] = prev;
+      s_pick[tt] = j;
+      prev = j;
     }
   }
   __syncthreads();
-  if (warp != 0) return;
-  // the walk: lane t draws position t's uniform up front
-  const float u_lane = (Tt > 0.f && lane < K)
-                           ? philox_uniform(seed, b, lane, kPurposeWalk, cycle)
-                           : 0.f;
-  int prev = 0;  // row 0 of position 0 is the anchor's row
-  for (int tt = 0; tt < K; ++tt) {
-    const int row = tt * kC + prev;
-    const int rowbase = (b * K + tt) * kC;
-    int j;
-    float qj;
-    if (Tt == 0.f) {
-      j = s_arg[row];
-      qj = (lane == j) ? 1.f : 0.f;
-    } else {
-      const float v = lane < kC ? sc_s[row * kC + lane] : -INFINITY;
-      const float mx = s_mx[row];
-      const float wv = (v != -INFINITY) ? __expf((v - mx) * invT) : 0.f;
-      const float cum = lane < kC ? c_s[row * kC + lane] : 0.f;
-      const float tot = s_tot[row];
-      const float u = __shfl_sync(0xffffffffu, u_lane, tt);
-      const float thr = u * tot;
-      const unsigned above = __ballot_sync(0xffffffffu, lane < kC && cum > thr);
-      const unsigned live = __ballot_sync(0xffffffffu, wv > 0.f);
-      if (above) j = __ffs(above) - 1;
-      else j = live ? 31 - __clz(live) : 0;  // u*tot rounded up to tot
-      if (!live && lane == 0) raise_error(err, kErrBadIndex);
-      qj = tot > 0.f ? wv / tot : 0.f;
-    }
-    if (lane < kC) q[rowbase + lane] = qj;
-    if (lane == 0) {
-      const int tok = s_ids[tt * kC + j];
-      slot[b * K + tt] = j;
-      draft[b * K + tt] = tok;
-      if (tok < 0) raise_error(err, kErrBadIndex);
-    }
-    prev = j;
+  for (int i2 = tid; i2 < K * kC; i2 += kThreads) {
+    const int tt = i2 / kC, jj = i2 % kC;
+    const size_t rr = (size_t)b * K + tt;
+    q[rr * kC + jj] = __ldcg(walk_q + (rr * kC + s_prev[tt]) * kC + jj);
+  }
+  if (tid < K) {
+    const int j = s_pick[tid];
+    const int tok = s_ids[tid * kC + j];
+    slot[b * K + tid] = j;
+    draft[b * K + tid] = tok;
+    if (tok < 0) raise_error(err, kErrBadIndex);
   }
 }
 
@@ -1091,7 +1121,8 @@ cudaError_t launch_draft_tail(TopkPartials P, int nstrip, const int* anchor,
                               float T_, uint64_t seed, uint64_t cycle,
                               float* topv, int* topi, float* lse,
                               float* scores, int* slot, int* draft, float* q,
-                              unsigned* tickets, int* err, cudaStream_t s) {
+                              unsigned* tickets, int* walk_j, float* walk_q,
+                              int* err, cudaStream_t s) {
   const size_t smem =
       (size_t)(DFLASH_MAX_RANK + 2 * kC * (DFLASH_MAX_RANK + 4)) *
           sizeof(float) +
@@ -1106,14 +1137,14 @@ cudaError_t launch_draft_tail(TopkPartials P, int nstrip, const int* anchor,
   return cudaLaunchKernelEx(&L.cfg, draft_tail_kernel<T>, P, nstrip, anchor,
                             gate, e_in, e_out, K, V, r, T_, invT, seed, cycle,
                             topv, topi, lse, scores, slot, draft, q, tickets,
-                            err);
+                            walk_j, walk_q, err);
 }
 
 template cudaError_t launch_draft_tail<__nv_bfloat16>(
     TopkPartials, int, const int*, const float*, const __nv_bfloat16*,
     const __nv_bfloat16*, int, int, int, int, float, uint64_t, uint64_t,
     float*, int*, float*, float*, int*, int*, float*, unsigned*, int*,
-    cudaStream_t);
+    float*, int*, cudaStream_t);
 
 template cudaError_t launch_pair_score_gated<float>(
     const float*, const int*, const int*, const float*, const float*,
