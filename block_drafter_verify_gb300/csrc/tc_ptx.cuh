@@ -41,35 +41,39 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar,
                "r"(bytes)
                : "memory");
 }
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+// Test for the completion of phase `parity`; the thread may be suspended
+// for at most about hint_ns while the phase is incomplete.
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity,
+                                              uint32_t hint_ns) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}\n"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
       : "memory");
   return ok != 0;
 }
 
 // Wait for phase `parity` of `bar` to complete.  Gives up after `limit_ns`
 // (or as soon as *abort is set by another role), sets *abort and returns
-// false; the caller then stops issuing work.
+// false; the caller then stops issuing work.  Each test suspends for at
+// most min(limit, 1 us), so the limit holds to about a microsecond.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar,
                                                   uint32_t parity,
                                                   volatile int* abort,
                                                   uint64_t limit_ns) {
-  if (mbar_try_wait(bar, parity)) return true;
+  const uint32_t hint =
+      (uint32_t)(limit_ns < 1000ull ? (limit_ns > 0 ? limit_ns : 1) : 1000ull);
+  if (mbar_try_wait(bar, parity, hint)) return true;
   const uint64_t t0 = globaltimer_ns();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63) == 0) {
-      if (*abort) return false;
-      if (globaltimer_ns() - t0 > limit_ns) {
-        *abort = 1;
-        return false;
-      }
+  for (;;) {
+    if (mbar_try_wait(bar, parity, hint)) return true;
+    if (*abort) return false;
+    if (globaltimer_ns() - t0 > limit_ns) {
+      *abort = 1;
+      return false;
     }
   }
 }
@@ -99,6 +103,21 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src,
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes "
       "[%0], [%1], %2, [%3];" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// 2-D tiled load delivered to every CTA of the cluster in cta_mask, at the
+// same shared-memory offset in each; each destination counts the bytes on
+// its mbarrier at the offset of `bar`.
+__device__ __forceinline__ void tma_load_2d_mc(void* dst, const CUtensorMap* m,
+                                               uint64_t* bar, int x, int y,
+                                               uint16_t cta_mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::"
+      "bytes.multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(
+          smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(smem_u32(bar)),
+      "h"(cta_mask)
       : "memory");
 }
 
@@ -159,6 +178,18 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 "
       "[%0];" ::"r"(smem_u32(bar))
+      : "memory");
+}
+
+// Arrive once on the mbarrier at this offset in every CTA of cta_mask when
+// the tcgen05 operations this thread issued so far have completed
+// (single-CTA MMAs).
+__device__ __forceinline__ void mma_commit_mc(uint64_t* bar,
+                                              uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster."
+      "multicast::cluster.b64 [%0], %1;" ::"r"(smem_u32(bar)),
+      "h"(cta_mask)
       : "memory");
 }
 
