@@ -193,8 +193,7 @@ dflash_status lmhead_tc_path(const __nv_bfloat16* h,
   if (!conv_w) row_bound = nullptr;
   if (conv_w) {
     CUtensorMap mh, mw, mg;
-    const int mc = conv_tc_cluster(M, H, w_gate ? r : 0);
-    if (!make_tmap_bf16_2d(&mh, h, H, M, 64, 128 / mc) ||
+    if (!make_tmap_bf16_2d(&mh, h, H, M, 64, 128) ||
         !make_tmap_bf16_2d(&mw, conv_w, H, 2 * (uint64_t)H, 64,
                            conv_tc_bc(M)))
       return DFLASH_ERR_CUDA;
@@ -203,7 +202,7 @@ dflash_status lmhead_tc_path(const __nv_bfloat16* h,
     __nv_bfloat16* y = static_cast<__nv_bfloat16*>(yv);
     {
       StageTimer tm(kStConv, s);
-      e = launch_conv_tc(mh, mc, mw, w_gate ? &mg : nullptr, h, B, K, H, r, y,
+      e = launch_conv_tc(mh, mw, w_gate ? &mg : nullptr, h, B, K, H, r, y,
                          gate, tickets, row_bound, M * kBoundSlots, d.err, s,
                          g_wait_ns.load());
     }

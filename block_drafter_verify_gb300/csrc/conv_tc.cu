@@ -72,12 +72,7 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4& u, float* f) {
   }
 }
 
-// MC CTAs of consecutive channel tiles (a cluster along x, one row tile)
-// share the h tile: each loads MC-th of its rows and multicasts them to the
-// MC CTAs, so the cluster reads the h tile from L2 once instead of MC
-// times.  A stage is then free only when all MC CTAs' MMAs have read it:
-// every CTA's MMA commit arrives on the empty barriers of all MC CTAs.
-template <int BC, int MC>
+template <int BC>
 __global__ void __launch_bounds__(THREADS)
     conv_tc_kernel(const __grid_constant__ CUtensorMap map_h,
                    const __grid_constant__ CUtensorMap map_wc,
@@ -110,7 +105,7 @@ __global__ void __launch_bounds__(THREADS)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       tc::mbar_init(&bars->full[s], 1);
-      tc::mbar_init(&bars->empty[s], MC);
+      tc::mbar_init(&bars->empty[s], 1);
     }
     tc::mbar_init(&bars->tfull, 1);
     tc::mbar_init(&bars->drain, 1);
@@ -122,18 +117,10 @@ __global__ void __launch_bounds__(THREADS)
     tc::tmem_relinquish();
   }
   tc::fence_before_sync();
-  if constexpr (MC > 1)
-    tc::cluster_sync();  // every CTA's barriers exist before a copy lands
-  else
-    __syncthreads();
+  __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = bars->tmem_base;
   volatile int* abort = &bars->abort;
-  const uint32_t crank = MC > 1 ? (uint32_t)(blockIdx.x % MC) : 0u;
-  constexpr uint16_t kMask = (uint16_t)((1u << MC) - 1u);
-  // clusters keep the long limit: a CTA that gave up early could leave
-  // while a peer's copy into its shared memory is still in flight
-  wait_ns = MC > 1 ? WAIT_NS : wait_ns;
   // everything above is on-chip set-up; h may come from the previous launch
   pdl_wait();
   if (threadIdx.x == 0) pdl_trigger();
@@ -156,13 +143,8 @@ __global__ void __launch_bounds__(THREADS)
           break;
         tc::mbar_arrive_expect_tx(&bars->full[stage], STAGE_BYTES);
         uint8_t* b = sb + stage * B_BYTES;
-        if constexpr (MC > 1)  // this CTA's rows of the h tile, to all MC
-          tc::tma_load_2d_mc(sa + stage * A_BYTES + crank * (A_BYTES / MC),
-                             &map_h, &bars->full[stage], kb * BK,
-                             mtile * BM + crank * (BM / MC), kMask);
-        else
-          tc::tma_load_2d(sa + stage * A_BYTES, &map_h, &bars->full[stage],
-                          kb * BK, mtile * BM);
+        tc::tma_load_2d(sa + stage * A_BYTES, &map_h, &bars->full[stage],
+                        kb * BK, mtile * BM);
         if (is_gate) {
           tc::tma_load_2d(b, &map_wg, &bars->full[stage], kb * BK, c0);
           tc::tma_load_2d(b + BC * BK * 2, &map_wg, &bars->full[stage],
@@ -198,10 +180,7 @@ __global__ void __launch_bounds__(THREADS)
         for (int k = 0; k < BK / 16; ++k)
           tc::mma_bf16(tmem, tc::sdesc_k_sw128(a0 + k * 32),
                        tc::sdesc_k_sw128(b0 + k * 32), idesc, (kb | k) != 0);
-        if constexpr (MC > 1)
-          tc::mma_commit_mc(&bars->empty[stage], kMask);
-        else
-          tc::mma_commit(&bars->empty[stage]);
+        tc::mma_commit(&bars->empty[stage]);
         if (++stage == STAGES) { stage = 0; phase ^= 1; }
       }
       if (ok) tc::mma_commit(&bars->tfull);
@@ -276,11 +255,7 @@ __global__ void __launch_bounds__(THREADS)
   }
 
   tc::fence_before_sync();
-  if constexpr (MC > 1)
-    tc::cluster_sync();  // no CTA leaves while a peer's copies or commits
-                         // may still reach its shared memory
-  else
-    __syncthreads();
+  __syncthreads();
   if (warp == 1) {
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, TMEM_COLS);
@@ -293,111 +268,38 @@ __global__ void __launch_bounds__(THREADS)
 int conv_tc_bc(int M) { return M >= 1024 ? 128 : 32; }
 
 namespace {
-// Clusters of MC conv CTAs the device can hold at once (cached per device).
-template <int BC, int MC>
-int max_conv_clusters() {
-  static int cached[64] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-  if (cached[dev] != 0) return cached[dev];
-  if (cudaFuncSetAttribute(conv_tc_kernel<BC, MC>,
-                           cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)conv_smem_bytes<BC>()) != cudaSuccess) {
-    (void)cudaGetLastError();
-    return cached[dev] = -1;
-  }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(MC);
-  cfg.blockDim = dim3(THREADS);
-  cfg.dynamicSmemBytes = conv_smem_bytes<BC>();
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = MC;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, conv_tc_kernel<BC, MC>, &cfg) !=
-          cudaSuccess ||
-      n < 1) {
-    (void)cudaGetLastError();
-    n = -1;
-  }
-  return cached[dev] = n;
-}
-
-template <int BC, int MC>
-cudaError_t launch_conv_mc(const CUtensorMap& map_h, const CUtensorMap& map_wc,
-                           const CUtensorMap* map_wg, const __nv_bfloat16* h,
-                           int M, int K, int H, int r, __nv_bfloat16* y,
-                           float* gate, unsigned* tickets, int ntickets,
-                           float* row_bound, int nbound, int* err,
-                           cudaStream_t s, uint64_t wait_ns) {
-  cudaError_t e = cudaFuncSetAttribute(
-      conv_tc_kernel<BC, MC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-      (int)conv_smem_bytes<BC>());
-  if (e != cudaSuccess) return e;
-  const int gate_tiles = map_wg ? (r + 2 * BC - 1) / (2 * BC) : 0;
-  const dim3 grid((H + BC - 1) / BC + gate_tiles, (M + BM - 1) / BM);
-  PdlLaunch L(grid, dim3(THREADS), conv_smem_bytes<BC>(), s,
-              MC > 1 ? MC : 0);
-  return cudaLaunchKernelEx(&L.cfg, conv_tc_kernel<BC, MC>, map_h, map_wc,
-                            map_wg ? *map_wg : map_wc, h, M, K, H, r, y, gate,
-                            tickets, ntickets, row_bound, nbound, err,
-                            wait_ns);
-}
-
 template <int BC>
-int cluster_for(int M, int H, int r) {
-  const int gate_tiles = r > 0 ? (r + 2 * BC - 1) / (2 * BC) : 0;
-  const int tiles = (H + BC - 1) / BC + gate_tiles;
-  const int ctas = tiles * ((M + BM - 1) / BM);
-  // every cluster resident at once (the CTAs of one launch all run
-  // together), and the channel tiles a whole number of clusters
-  if (tiles % 4 == 0 && max_conv_clusters<BC, 4>() * 4 >= ctas) return 4;
-  if (tiles % 2 == 0 && max_conv_clusters<BC, 2>() * 2 >= ctas) return 2;
-  return 1;
-}
-}  // namespace
-
-int conv_tc_cluster(int M, int H, int r) {
-  return conv_tc_bc(M) == 128 ? cluster_for<128>(M, H, r)
-                              : cluster_for<32>(M, H, r);
-}
-
-cudaError_t launch_conv_tc(const CUtensorMap& map_h, int mc,
-                           const CUtensorMap& map_wc,
+cudaError_t launch_conv_bc(const CUtensorMap& map_h, const CUtensorMap& map_wc,
                            const CUtensorMap* map_wg, const __nv_bfloat16* h,
                            int B, int K, int H, int r, __nv_bfloat16* y,
                            float* gate, unsigned* tickets, float* row_bound,
                            int nbound, int* err, cudaStream_t s,
                            uint64_t wait_ns) {
   const int M = B * K;
-  if (conv_tc_bc(M) == 128) {
-    if (mc == 4)
-      return launch_conv_mc<128, 4>(map_h, map_wc, map_wg, h, M, K, H, r, y,
-                                    gate, tickets, B, row_bound, nbound, err,
-                                    s, wait_ns);
-    if (mc == 2)
-      return launch_conv_mc<128, 2>(map_h, map_wc, map_wg, h, M, K, H, r, y,
-                                    gate, tickets, B, row_bound, nbound, err,
-                                    s, wait_ns);
-    return launch_conv_mc<128, 1>(map_h, map_wc, map_wg, h, M, K, H, r, y,
-                                  gate, tickets, B, row_bound, nbound, err, s,
-                                  wait_ns);
-  }
-  if (mc == 4)
-    return launch_conv_mc<32, 4>(map_h, map_wc, map_wg, h, M, K, H, r, y,
-                                 gate, tickets, B, row_bound, nbound, err, s,
-                                 wait_ns);
-  if (mc == 2)
-    return launch_conv_mc<32, 2>(map_h, map_wc, map_wg, h, M, K, H, r, y,
-                                 gate, tickets, B, row_bound, nbound, err, s,
-                                 wait_ns);
-  return launch_conv_mc<32, 1>(map_h, map_wc, map_wg, h, M, K, H, r, y, gate,
-                               tickets, B, row_bound, nbound, err, s,
-                               wait_ns);
+  cudaError_t e = cudaFuncSetAttribute(
+      conv_tc_kernel<BC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      (int)conv_smem_bytes<BC>());
+  if (e != cudaSuccess) return e;
+  const int gate_tiles = map_wg ? (r + 2 * BC - 1) / (2 * BC) : 0;
+  const dim3 grid((H + BC - 1) / BC + gate_tiles, (M + BM - 1) / BM);
+  PdlLaunch L(grid, dim3(THREADS), conv_smem_bytes<BC>(), s);
+  return cudaLaunchKernelEx(&L.cfg, conv_tc_kernel<BC>, map_h, map_wc,
+                            map_wg ? *map_wg : map_wc, h, M, K, H, r, y, gate,
+                            tickets, B, row_bound, nbound, err, wait_ns);
+}
+}  // namespace
+
+cudaError_t launch_conv_tc(const CUtensorMap& map_h, const CUtensorMap& map_wc,
+                           const CUtensorMap* map_wg, const __nv_bfloat16* h,
+                           int B, int K, int H, int r, __nv_bfloat16* y,
+                           float* gate, unsigned* tickets, float* row_bound,
+                           int nbound, int* err, cudaStream_t s,
+                           uint64_t wait_ns) {
+  if (conv_tc_bc(B * K) == 128)
+    return launch_conv_bc<128>(map_h, map_wc, map_wg, h, B, K, H, r, y, gate,
+                               tickets, row_bound, nbound, err, s, wait_ns);
+  return launch_conv_bc<32>(map_h, map_wc, map_wg, h, B, K, H, r, y, gate,
+                            tickets, row_bound, nbound, err, s, wait_ns);
 }
 
 }  // namespace dflash

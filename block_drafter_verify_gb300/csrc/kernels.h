@@ -24,19 +24,14 @@ cudaError_t launch_conv_simt(const T* h, const T* w_conv, int B, int K, int H,
 // TMA descriptor of a row-major bf16 [rows, inner] matrix, 128-byte swizzle.
 bool make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner,
                        uint64_t rows, uint32_t box_inner, uint32_t box_rows);
-// map_h: h [B*K, H] box {64, 128 / mc}; map_wc: conv_w [2H, H] box {64, BC}
+// map_h: h [B*K, H] box {64, 128}; map_wc: conv_w [2H, H] box {64, BC}
 // with BC = conv_tc_bc(B*K) channels per CTA (map_wg likewise).
 // With map_wg (w_gate [r, H], box {64, 32}) the launch also writes the pair
 // selector's gate g = sigmoid(W_g h) as gate [B*K, r] fp32.  tickets (B
 // words, may be NULL) are zeroed and row_bound (nbound floats, may be NULL)
 // set to -inf for later launches of the same call.
 int conv_tc_bc(int M);
-// Cluster size (4, 2 or 1) of the conv launch for these sizes (r = 0: no
-// gate tiles): clusters of consecutive channel tiles share each h tile by
-// multicast.  map_h's boxes are then {64, 128 / cluster} rows.
-int conv_tc_cluster(int M, int H, int r);
-cudaError_t launch_conv_tc(const CUtensorMap& map_h, int mc,
-                           const CUtensorMap& map_wc,
+cudaError_t launch_conv_tc(const CUtensorMap& map_h, const CUtensorMap& map_wc,
                            const CUtensorMap* map_wg, const __nv_bfloat16* h,
                            int B, int K, int H, int r, __nv_bfloat16* y,
                            float* gate, unsigned* tickets, float* row_bound,

@@ -106,21 +106,6 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src,
       : "memory");
 }
 
-// 2-D tiled load delivered to every CTA of the cluster in cta_mask, at the
-// same shared-memory offset in each; each destination counts the bytes on
-// its mbarrier at the offset of `bar`.
-__device__ __forceinline__ void tma_load_2d_mc(void* dst, const CUtensorMap* m,
-                                               uint64_t* bar, int x, int y,
-                                               uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::"
-      "bytes.multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(
-          smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(smem_u32(bar)),
-      "h"(cta_mask)
-      : "memory");
-}
-
 // ---- TMEM -----------------------------------------------------------------
 __device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
   asm volatile(
@@ -178,18 +163,6 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 "
       "[%0];" ::"r"(smem_u32(bar))
-      : "memory");
-}
-
-// Arrive once on the mbarrier at this offset in every CTA of cta_mask when
-// the tcgen05 operations this thread issued so far have completed
-// (single-CTA MMAs).
-__device__ __forceinline__ void mma_commit_mc(uint64_t* bar,
-                                              uint16_t cta_mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster."
-      "multicast::cluster.b64 [%0], %1;" ::"r"(smem_u32(bar)),
-      "h"(cta_mask)
       : "memory");
 }
 

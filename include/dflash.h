@@ -486,13 +486,12 @@ dflash_status dflash_philox4x32(const uint32_t* ctr, uint64_t seed,
 dflash_status dflash_profile_stage(int stage, void* begin, void* end);
 
 /* Limit, in nanoseconds, of the bounded waits inside the tensor-core
- * kernels of later launches: the conv when its CTAs are not clustered
- * (channel tiles in no multiple of 2) and the single-CTA LM head (one row
+ * kernels of later launches: the conv and the single-CTA LM head (one row
  * tile, B*K <= 128) give up on a wait that runs longer, stop issuing work,
  * let their copies and MMAs in flight complete, free their TMEM and set
  * DFLASH_ERR_DEVICE_TIMEOUT in the device error word (their results are
  * then invalid).  0 restores the default of 2 s, far beyond any real wait;
- * clustered conv launches and the CTA-pair LM head always use it.  Process-wide host state,
+ * the CTA-pair LM head always uses it.  Process-wide host state,
  * meant for tests of that failure path ("Failure detection": a wait that
  * never completes must end in a status the host reads, not a hang).
  * Always returns DFLASH_OK. */

@@ -14,10 +14,9 @@ pytestmark = pytest.mark.gpu
 
 
 def _workload():
-    # one row tile (B*K = 32): single-CTA LM head; 63 channel tiles (H =
-    # 2016): the conv's CTAs are not clustered; 32 k-steps per tile, so the
-    # epilogue's accumulator waits last microseconds
-    return synth.Workload("timeout", B=4, K=8, V=151936, H=2016, r=32,
+    # one row tile (B*K = 32): single-CTA LM head; 32 k-steps per tile, so
+    # the epilogue's accumulator waits last microseconds
+    return synth.Workload("timeout", B=4, K=8, V=151936, H=2048, r=32,
                           dtype="bf16", T=1.0, seed=51, w_lm_sd=0.02,
                           conv_sd=0.05, sel_sd=0.1,
                           target=("affine", 0.9, 1.0))

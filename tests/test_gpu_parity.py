@@ -414,10 +414,8 @@ def test_full_size_workload(lib, name):
     (20, 15, 136, 4099, 256, 1.0),  # M = 300: CTA pairs, full rank
     (65, 16, 200, 3001, 200, 1.0),  # M = 1040: 128-channel conv tiles,
                                     # ragged H and a partial gate tile
-    (6, 5, 224, 3001, 32, 1.0),     # 7 + 1 channel tiles: conv clusters
-                                    # of 4 sharing h by multicast, ragged K
-    (20, 15, 256, 4099, 128, 0.7),  # 8 + 2 tiles, 3 row tiles: clusters
-                                    # of 2
+    (6, 5, 224, 3001, 32, 1.0),     # ragged K (224 = 3.5 k-blocks)
+    (20, 15, 256, 4099, 128, 0.7),  # M = 300, two gate tiles
 ])
 def test_fused_draft_bf16(lib, B, K, H, V, r, T):
     w = synth.Workload("small", B=B, K=K, V=V, H=H, r=r, dtype="bf16", T=T,
