@@ -139,24 +139,11 @@ __device__ __forceinline__ void topk_insert(float (&tv)[kC], int (&ti)[kC],
   tv[0] = fmaxf(tv[0], xv);
 }
 
-// Insert (xv, xi) into the sorted list, ordered by value descending and
-// then by id ascending (for merging lists whose ids interleave).
+// Order of the lists: value descending, then id ascending (for merging
+// lists whose ids interleave).
 __device__ __forceinline__ bool topk_before(float xv, int xi, float tv,
                                             int ti) {
   return xv > tv || (xv == tv && xi < ti);
-}
-__device__ __forceinline__ void topk_insert_any(float (&tv)[kC],
-                                                int (&ti)[kC], float xv,
-                                                int xi) {
-  if (!topk_before(xv, xi, tv[kC - 1], ti[kC - 1])) return;
-#pragma unroll
-  for (int p = kC - 1; p >= 1; --p) {
-    const bool shift = topk_before(xv, xi, tv[p - 1], ti[p - 1]);
-    const bool here = !shift && topk_before(xv, xi, tv[p], ti[p]);
-    tv[p] = shift ? tv[p - 1] : (here ? xv : tv[p]);
-    ti[p] = shift ? ti[p - 1] : (here ? xi : ti[p]);
-  }
-  if (topk_before(xv, xi, tv[0], ti[0])) { tv[0] = xv; ti[0] = xi; }
 }
 
 // The 16th largest of 32 values: both halves sorted descending by bitonic
@@ -611,9 +598,34 @@ __global__ void __launch_bounds__(Cfg<kPair, kFp8>::THREADS, 1)
       }
       asm volatile("bar.sync 1, %0;" ::"n"(C::EPI_WARPS * 32) : "memory");
       if (half == 0) {
-#pragma unroll 1
-        for (int k = 0; k < kC; ++k)
-          topk_insert_any(tv, ti, mg[k], __float_as_int(mg[kC + k]));
+        // Merge of two sorted lists: the better of entry k and the other
+        // list's entry 15 - k are the top 16 of both, in bitonic order,
+        // which four rounds of compare-exchanges (distance 8, 4, 2, 1)
+        // sort best first.
+#pragma unroll
+        for (int k = 0; k < kC; ++k) {
+          const float bv = mg[kC - 1 - k];
+          const int bi = __float_as_int(mg[2 * kC - 1 - k]);
+          if (topk_before(bv, bi, tv[k], ti[k])) {
+            tv[k] = bv;
+            ti[k] = bi;
+          }
+        }
+#pragma unroll
+        for (int dd = kC / 2; dd; dd >>= 1) {
+#pragma unroll
+          for (int k = 0; k < kC; ++k) {
+            const int l = k ^ dd;
+            if (l > k && topk_before(tv[l], ti[l], tv[k], ti[k])) {
+              const float fv = tv[k];
+              const int fi = ti[k];
+              tv[k] = tv[l];
+              ti[k] = ti[l];
+              tv[l] = fv;
+              ti[l] = fi;
+            }
+          }
+        }
         const float m1 = mg[32], s1 = mg[33];
         const float mm = fmaxf(run_m, m1);
         if (mm != -INFINITY)
