@@ -124,11 +124,11 @@ cudaError_t launch_path_walk(const float* scores, const int* topi, int B,
 struct VerifyWs {
   float2* part;        // [rows][segments]: segment (max, sum) pairs at
                        // T > 0, chunk (max, argmax) at T = 0
-  int* row_acc;        // [rows] accept decision of position t (t < K)
   int* row_tok;        // [rows] token emitted if t is the first rejection
                        // (t = K: the bonus token)
-  unsigned* counters;  // rows + B tickets and B rejection masks, zeroed
-                       // before every launch
+  unsigned* counters;  // [rows] tickets, [B] sequence words (arrivals << 16
+                       // | rejected positions), [B] masks of rejections
+                       // seen by the draws; zeroed before every launch
   unsigned* rejmask;   // [B] bit t: position t rejected (in counters)
   size_t counter_bytes;
 };

@@ -278,6 +278,7 @@ __global__ void __launch_bounds__(kThreads)
   __shared__ float s_a[kWarps];
   __shared__ int s_i[kWarps];
   __shared__ int s_flag, s_acc, s_need;
+  __shared__ unsigned s_rej;
   __shared__ float s_m;
   __shared__ DrawSmem s_draw;
   __shared__ int s_ci[kC];
@@ -297,6 +298,14 @@ __global__ void __launch_bounds__(kThreads)
       r_tok = draft[b * K + t];
     }
   }
+  // the row's accept uniform and the sequence's resample uniform, computed
+  // now rather than after the pass, where the row's work waits on them
+  const bool draws = !kStats && !greedy;
+  const float u_acc =
+      draws && has_draft ? philox_uniform(seed, b, t, kPurposeAccept, cycle)
+                         : 0.f;
+  const float u_res =
+      draws ? philox_uniform(seed, b, K, kPurposeResample, cycle) : 0.f;
 
   // ---- main pass ------------------------------------------------------
   // Segments of this chunk: sc0 .. sc1-1; warp w takes sc0 + w + 8 j.
@@ -397,6 +406,9 @@ __global__ void __launch_bounds__(kThreads)
     __syncthreads();
   }
   if (wid == 0) {
+    // the sequence's rejection mask so far, in flight during the fold
+    unsigned seen = 0;
+    if (!kStats && !greedy && lane == 0) seen = __ldcg(&ws.rejmask[b]);
     float ra = -INFINITY, rs = 0.f;
     int ri = 0x7fffffff;
     if (greedy) {
@@ -462,13 +474,12 @@ __global__ void __launch_bounds__(kThreads)
         const float qd = hit ? __shfl_sync(0xffffffffu, r_q, __ffs(hit) - 1) : 0.f;
         if (!hit && lane == 0) raise_error(err, kErrBadIndex);
         const float pd = weight(xd, s2, -ra * s2) / rs;
-        const float u = philox_uniform(seed, b, t, kPurposeAccept, cycle);
-        acc = (u * qd < pd);
+        acc = (u_acc * qd < pd);
       }
     }
     if (greedy) {
       if (lane == 0) {
-        ws.row_acc[row] = acc;
+        s_acc = acc;
         ws.row_tok[row] = ri;
       }
     } else {
@@ -491,14 +502,16 @@ __global__ void __launch_bounds__(kThreads)
         s_acc = acc;
         // Row t's token is emitted only if t is the first rejection (t < K)
         // or nothing is rejected (t = K): a row whose draft was accepted,
-        // or that follows a rejection already recorded in the sequence's
-        // mask, skips its draw.  A stale mask only costs a draw.
+        // or that follows a rejection already in the sequence's mask (read
+        // before the fold), skips its draw.  A stale mask only costs a
+        // draw.  The row's own rejection is added without waiting.
         const unsigned below = (1u << t) - 1u;
-        if (has_draft)
-          s_need = !acc &&
-                   !(atomicOr(&ws.rejmask[b], 1u << t) & below);
-        else
-          s_need = atomicOr(&ws.rejmask[b], 0u) == 0u;
+        if (has_draft) {
+          s_need = !acc && !(seen & below);
+          if (!acc) atomicOr(&ws.rejmask[b], 1u << t);
+        } else {
+          s_need = seen == 0u;
+        }
       }
     }
   }
@@ -508,24 +521,25 @@ __global__ void __launch_bounds__(kThreads)
   }
   if (!greedy && s_need) {
     // ---- draw of row (b, t): residual max(0, p - q), or p for t = K ------
-    const float u = philox_uniform(seed, b, K, kPurposeResample, cycle);
     const int tok = row_draw(x, V, nseg, s_pair, s_ci, s_qz, s_corr, s_m, s2,
-                             u, -1.f, false, s_draw, err);
+                             u_res, -1.f, false, s_draw, err);
     if (tid == 0) ws.row_tok[row] = tok;
   }
-  if (!greedy && tid == 0) ws.row_acc[row] = s_acc;
 
-  // ---- ticket of sequence b; its last row emits the tokens --------------
+  // ---- the sequence's word: arrivals (bits 16..) and rejected positions;
+  // its last row emits the tokens ------------------------------------------
   __syncthreads();
   if (tid == 0) {
-    __threadfence();
-    s_flag = (atomicAdd(&ws.counters[rows + b], 1u) == (unsigned)K);
+    const unsigned mine = (1u << 16) | (has_draft && !s_acc ? 1u << t : 0u);
+    __threadfence();  // the row's token before its arrival
+    const unsigned old = atomicAdd(&ws.counters[rows + b], mine);
+    s_flag = (old >> 16) == (unsigned)K;
+    s_rej = (old + mine) & 0xffffu;
   }
   __syncthreads();
   if (!s_flag || wid != 0) return;
   __threadfence();
-  const int acc = lane < K ? __ldcg(&ws.row_acc[b * K1 + lane]) : 1;
-  const unsigned rej = __ballot_sync(0xffffffffu, lane < K && !acc);
+  const unsigned rej = s_rej;
   const int n = rej ? __ffs(rej) - 1 : K;
   if (lane == 0) n_accepted[b] = n;
   if (lane <= K) {
@@ -732,10 +746,10 @@ size_t verify_ws_layout(int B, int K, int V, void* base, VerifyWs* o) {
   VerifyWs w{};
   // per row: segment pairs (T > 0) or chunk argmaxes (T = 0, <= nseg)
   w.part = reinterpret_cast<float2*>(take(rows * nseg * sizeof(float2)));
-  w.row_acc = reinterpret_cast<int*>(take(rows * sizeof(int)));
   w.row_tok = reinterpret_cast<int*>(take(rows * sizeof(int)));
-  // tickets of rows and sequences, then each sequence's mask of rejected
-  // positions, all zeroed together before a launch
+  // tickets of rows (chunks done), the sequences' words (arrivals and
+  // rejected positions), then each sequence's mask of rejections seen by
+  // the draws, all zeroed together before a launch
   w.counter_bytes = (rows + 2 * (size_t)B) * sizeof(unsigned);
   w.counters = reinterpret_cast<unsigned*>(take(w.counter_bytes));
   w.rejmask = w.counters ? w.counters + rows + B : nullptr;

@@ -294,7 +294,7 @@ dflash_status dflash_verify(const float* target_logits, const int32_t* draft,
  * process exits; sizes whose scratch, dflash_workspace_bytes(1, B, K, 0, V)
  * (about B*(K+1)*ceil(V/2048)*8 bytes), exceeds 4 MiB are refused with
  * DFLASH_ERR_UNSUPPORTED.  At V = 151936, B = 256 with K = 16 fits (2.7 MB)
- * and K = 16 fits up to B = 402; at V = 262144, B = 256 fits up to K = 14.
+ * and K = 16 fits up to B = 405; at V = 262144, B = 256 fits up to K = 14.
  * The first call on a device looks up the array's device address (so make
  * that first call before any stream capture).  All calls share the
  * array: each clears what must start at zero itself, and calls whose

@@ -71,8 +71,8 @@ LIMIT = 4 << 20
 
 
 @pytest.mark.parametrize("V,K,B", [
-    (151936, 16, 402),     # the largest batch whose scratch fits, K = 16
-    (151936, 16, 403),     # one sequence more: over the limit
+    (151936, 16, 405),     # the largest batch whose scratch fits, K = 16
+    (151936, 16, 406),     # one sequence more: over the limit
     (262144, 14, 256),     # B = 256 fits up to K = 14 at V = 262144
     (262144, 15, 256),     # ... and not at K = 15
 ])
