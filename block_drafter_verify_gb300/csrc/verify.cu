@@ -109,34 +109,39 @@ struct DrawSmem {
 // correction of the candidate it is (s_ci / s_qz: w = max(0, w - q Z));
 // the row's 2048-token segments weigh their (max, sum) pair (s_pair)
 // rescaled to m plus the corrections of the candidates inside them
-// (s_corr), clamped at zero.  Target theta: u * (the row's total) when
-// theta_abs < 0, where a zero residual total switches to raw weights;
-// else theta_abs with raw = raw_given.  Warp 0 locates the segment (lane l
-// owns segments l*per .. l*per+per-1: one inclusive scan of the lane
-// totals and a ballot); the CTA then takes the smallest token of the
+// (s_corr), clamped at zero; every thread computes some segments' two
+// weights (residual, raw), which replace their pairs in s_pair.  Target
+// theta: u * (the row's total) when theta_abs < 0, where a zero residual
+// total switches to raw weights; else theta_abs with raw = raw_given.
+// Warp 0 locates the segment (lane l owns segments l*per .. l*per+per-1:
+// one inclusive scan of the lane totals and a ballot); the CTA then takes
+// the smallest token of the
 // segment whose running sum exceeds theta (8 contiguous tokens per thread,
 // block scan in a fixed tree).  Returns the token on every thread (the
 // segment's last token of positive weight if rounding leaves the target at
 // the segment's end), or -1 if no segment has weight.
 __device__ __forceinline__ int row_draw(
-    const float* __restrict__ x, int V, int nseg, const float2* s_pair,
+    const float* __restrict__ x, int V, int nseg, float2* s_pair,
     const int* s_ci, const float* s_qz, const float* s_corr, float m,
     float s2, float u, float theta_abs, bool raw_given, DrawSmem& sm,
     int* err) {
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const float nb = -m * s2;
+  for (int k = tid; k < nseg; k += kThreads) {
+    const float2 p = s_pair[k];
+    const float wr = (p.x == -INFINITY) ? 0.f : p.y * ex2f((p.x - m) * s2);
+    float w = wr;
+#pragma unroll
+    for (int j = 0; j < kC; ++j)
+      if (s_ci[j] >= 0 && s_ci[j] / kSegTokens == k) w += s_corr[j];
+    s_pair[k] = make_float2(fmaxf(w, 0.f), fmaxf(wr, 0.f));
+  }
+  __syncthreads();
   if (wid == 0) {
     const int per = (nseg + 31) / 32;
     auto seg_weight = [&](int k, bool raw) -> float {
       if (k >= nseg) return 0.f;
-      const float2 p = s_pair[k];
-      float w = (p.x == -INFINITY) ? 0.f : p.y * ex2f((p.x - m) * s2);
-      if (!raw) {
-#pragma unroll
-        for (int j = 0; j < kC; ++j)
-          if (s_ci[j] >= 0 && s_ci[j] / kSegTokens == k) w += s_corr[j];
-      }
-      return fmaxf(w, 0.f);
+      return raw ? s_pair[k].y : s_pair[k].x;
     };
     int f_seg = -1, f_raw = 0;
     float f_rem = 0.f;
@@ -197,6 +202,12 @@ __device__ __forceinline__ int row_draw(
   // the 2048 tokens of the segment: 8 contiguous tokens per thread
   const bool use_raw = sm.use_raw;
   const int t0 = seg * kSegTokens + tid * 8;
+  unsigned own = 0;  // the candidates among this thread's tokens
+  if (!use_raw) {
+#pragma unroll
+    for (int j = 0; j < kC; ++j)
+      if ((unsigned)(s_ci[j] - t0) < 8u) own |= 1u << j;
+  }
   float w8[8];
   float tsum = 0.f;
 #pragma unroll
@@ -205,10 +216,9 @@ __device__ __forceinline__ int row_draw(
     float wv = 0.f;
     if (v < V) {
       wv = weight(x[v], s2, nb);
-      if (!use_raw) {
-#pragma unroll
-        for (int j = 0; j < kC; ++j)
-          if (s_ci[j] == v) wv = fmaxf(wv - s_qz[j], 0.f);
+      for (unsigned mm = own; mm; mm &= mm - 1) {
+        const int j = __ffs(mm) - 1;  // candidate order, as in the weights
+        if (s_ci[j] == v) wv = fmaxf(wv - s_qz[j], 0.f);
       }
     }
     w8[i] = wv;
