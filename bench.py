@@ -760,7 +760,7 @@ def run_ours(args):
         loop = {"cycles": G, "cycles_per_s": G / lsecs,
                 "emitted_tokens_per_s": float(st_[2]) / lsecs,
                 "mean_acceptance_length": float(st_[0]) / float(st_[1]),
-                "with": "dflash_draft + dflash_verify + dflash_commit, "
+                "with": "dflash_cycle + dflash_commit, "
                         "anchor handed over every cycle"}
 
     sel = selector_report(dv_mod, dv, w, h, anchor, L, seed, stream, dev,

@@ -5,7 +5,7 @@ of include/dflash.h); this package is its ctypes binding.
 """
 from .binding import (BF16, C, COMMIT_STATS, FP32, STAGES, DFlashError,
                       DraftVerify, EXPORTS, dflash_check, dflash_commit,
-                      dflash_draft, dflash_draft_e4m3, dflash_lmhead_topk,
+                      dflash_cycle, dflash_draft, dflash_draft_e4m3, dflash_lmhead_topk,
                       dflash_path_viterbi, dflash_quantize_e4m3_rows,
                       dflash_top16_recall, dflash_set_wait_limit_ns,
                       dflash_pair_score, dflash_path_walk, dflash_philox4x32,
@@ -18,7 +18,7 @@ from .binding import (BF16, C, COMMIT_STATS, FP32, STAGES, DFlashError,
 
 __all__ = ["BF16", "C", "COMMIT_STATS", "FP32", "STAGES", "DFlashError",
            "DraftVerify", "EXPORTS", "dflash_check", "dflash_commit",
-           "dflash_draft", "dflash_draft_e4m3", "dflash_lmhead_topk",
+           "dflash_cycle", "dflash_draft", "dflash_draft_e4m3", "dflash_lmhead_topk",
            "dflash_path_viterbi", "dflash_quantize_e4m3_rows",
            "dflash_top16_recall", "dflash_set_wait_limit_ns",
            "dflash_pair_score", "dflash_path_walk", "dflash_philox4x32",

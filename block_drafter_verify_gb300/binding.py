@@ -20,7 +20,7 @@ STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported",
           5: "device wait timed out", 6: "token index out of range"}
 
 EXPORTS = ("dflash_workspace_bytes", "dflash_lmhead_topk", "dflash_pair_score",
-           "dflash_path_walk", "dflash_draft", "dflash_verify",
+           "dflash_path_walk", "dflash_draft", "dflash_verify", "dflash_cycle",
            "dflash_verify_noalloc", "dflash_commit", "dflash_path_viterbi",
            "dflash_top16_recall", "dflash_quantize_e4m3_rows",
            "dflash_draft_e4m3", "dflash_philox4x32", "dflash_profile_stage",
@@ -71,6 +71,9 @@ def load(path: str | None = None):
                                vp, vp, vp, sz, vp]),
         "dflash_verify": (i32, [vp, vp, vp, vp, i32, i32, i32, f32, u64, u64,
                                 vp, vp, vp, sz, vp]),
+        "dflash_cycle": (i32, [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32,
+                               i32, i32, i32, i32, f32, u64, u64, vp, vp, vp,
+                               vp, vp, vp, vp, vp, vp, vp, sz, vp, sz, vp]),
         "dflash_verify_noalloc": (i32, [vp, vp, vp, vp, i32, i32, i32, f32,
                                         u64, u64, vp, vp, vp]),
         "dflash_philox4x32": (i32, [vp, u64, vp, i64, vp]),
@@ -248,6 +251,31 @@ def dflash_verify(target_logits, draft, topi, q, T, seed, cycle, n_accepted,
           _ptr(q), B, K1 - 1, V, float(T), int(seed) & (2**64 - 1),
           int(cycle) & (2**64 - 1), _ptr(n_accepted), _ptr(out_tok),
           _ptr(ws), ws.numel(), _stream(stream))
+
+
+def dflash_cycle(h, conv_w, w_lm, w_scale, w_gate, e_in, e_out, anchor,
+                 target_logits, T, seed, cycle, topv, topi, lse, scores, slot,
+                 draft, q, n_accepted, out_tok, ws_draft, ws_verify,
+                 stream=None):
+    """One whole cycle: dflash_draft (w_scale None; else dflash_draft_e4m3
+    with w_lm the E4M3 codes [V,H] uint8 and w_scale [V] f32) and
+    dflash_verify of its draft; the arguments and outputs of the two calls,
+    ws_draft (workspace kind 2, or 3 with w_scale) and ws_verify (kind 1)."""
+    B, K, H = h.shape
+    V = w_lm.shape[0]
+    r = w_gate.shape[0]
+    _want(target_logits, torch.float32, "target_logits")
+    if w_scale is not None:
+        _want(h, torch.bfloat16, "h")
+        _want(w_lm, torch.uint8, "w_lm")
+    _call("dflash_cycle", _ptr(h), _ptr(conv_w), _ptr(w_lm), _ptr(w_scale),
+          _ptr(w_gate), _ptr(e_in), _ptr(e_out), _ptr(anchor),
+          _ptr(target_logits), B, K, H, V, r, _dtype(h), float(T),
+          int(seed) & (2**64 - 1), int(cycle) & (2**64 - 1), _ptr(topv),
+          _ptr(topi), _ptr(lse), _ptr(scores), _ptr(slot), _ptr(draft),
+          _ptr(q), _ptr(n_accepted), _ptr(out_tok), _ptr(ws_draft),
+          ws_draft.numel(), _ptr(ws_verify), ws_verify.numel(),
+          _stream(stream))
 
 
 def dflash_verify_noalloc(target_logits, draft, topi, q, T, seed, cycle,
@@ -460,9 +488,16 @@ class DraftVerify:
                      self.draft, self.q, self.ws_d, stream)
 
     def cycle(self, h, anchor, L, T, seed, cycle, stream=None):
-        """One draft-verify cycle: dflash_draft + dflash_verify."""
-        self.draft_all(h, anchor, T, seed, cycle, stream)
-        self.verify(L, T, seed, cycle, stream)
+        """One draft-verify cycle in one dflash_cycle call (dflash_draft +
+        dflash_verify, the verify's tickets zeroed by the conv launch)."""
+        e4 = self.lm_e4m3
+        dflash_cycle(h, self.w["w_conv"],
+                     self.w_codes if e4 else self.w["w_lm"],
+                     self.w_scale if e4 else None, self.w["w_gate"],
+                     self.w["e_in"], self.w["e_out"], anchor, L, T, seed,
+                     cycle, self.topv, self.topi, self.lse, self.scores,
+                     self.slot, self.draft, self.q, self.n, self.out,
+                     self.ws_d, self.ws_v, stream)
         return self.n, self.out
 
     def commit(self, anchor, tokens, length, stats, stream=None):

@@ -180,7 +180,8 @@ dflash_status lmhead_tc_path(const __nv_bfloat16* h,
                             unsigned* tickets = nullptr,
                             TopkPartials* P_out = nullptr,
                             int* strips_out = nullptr,
-                            const E4m3Head* q8 = nullptr) {
+                            const E4m3Head* q8 = nullptr,
+                            unsigned* vz = nullptr, int nvz = 0) {
   void* yv = nullptr;
   TopkPartials P;
   float* row_bound = nullptr;
@@ -204,7 +205,7 @@ dflash_status lmhead_tc_path(const __nv_bfloat16* h,
       StageTimer tm(kStConv, s);
       e = launch_conv_tc(mh, mw, w_gate ? &mg : nullptr, h, B, K, H, r, y,
                          gate, tickets, row_bound, M * kBoundSlots, d.err, s,
-                         g_wait_ns.load());
+                         g_wait_ns.load(), vz, nvz);
     }
     if (e != cudaSuccess) return DFLASH_ERR_CUDA;
     a = y;
@@ -305,17 +306,19 @@ bool verify_args_ok(const float* target_logits, const int32_t* draft,
          aligned(target_logits, 16);
 }
 
-// Zero the tickets of workspace w, then launch the verify kernel on the
-// current device, inside the verify stage's profiling events.
+// Zero the tickets of workspace w (unless an earlier launch of the same
+// call did: zeroed), then launch the verify kernel on the current device,
+// inside the verify stage's profiling events.
 dflash_status verify_run(const float* target_logits, const int32_t* draft,
                          const int32_t* topi, const float* q, int B, int K,
                          int V, float T, uint64_t seed, uint64_t cycle,
                          int32_t* n_accepted, int32_t* out_tok,
-                         const VerifyWs& w, cudaStream_t s) {
+                         const VerifyWs& w, cudaStream_t s, bool zeroed) {
   DeviceState* d = nullptr;
   dflash_status st = device_state(&d);
   if (st != DFLASH_OK) return st;
-  if (cudaMemsetAsync(w.counters, 0, w.counter_bytes, s) != cudaSuccess)
+  if (!zeroed &&
+      cudaMemsetAsync(w.counters, 0, w.counter_bytes, s) != cudaSuccess)
     return DFLASH_ERR_CUDA;
   StageTimer tm(kStVerifyRows, s);
   return cuda_status(launch_verify(target_logits, draft, topi, q, B, K, V, T,
@@ -437,14 +440,57 @@ dflash_status dflash_path_walk(const float* scores, const int32_t* topi,
                                       slot, draft, q, d->err, s));
 }
 
-dflash_status dflash_draft(const void* h, const void* conv_w, const void* w_lm,
-                           const void* w_gate, const void* e_in,
-                           const void* e_out, const int32_t* anchor, int B,
-                           int K, int H, int V, int r, dflash_dtype dt,
-                           float T, uint64_t seed, uint64_t cycle, float* topv,
-                           int32_t* topi, float* lse, float* scores,
-                           int32_t* slot, int32_t* draft, float* q, void* ws,
-                           size_t ws_bytes, dflash_stream_t stream) {
+}  // extern "C"
+
+namespace dflash {
+namespace {
+
+// Steps a1-a4 on the tensor cores (bf16 storage with a conv; q8: the
+// 8-bit LM head): the gate rides along with the conv, which also zeroes the
+// walk tickets (and vz, nvz words: the cycle's verify tickets); one launch
+// after the LM head merges its partials, scores the pairs and walks each
+// sequence.
+dflash_status draft_tc(const void* h, const void* conv_w, const void* w_lm,
+                       const E4m3Head* q8, const void* w_gate,
+                       const void* e_in, const void* e_out,
+                       const int32_t* anchor, int B, int K, int H, int V,
+                       int r, float T, uint64_t seed, uint64_t cycle,
+                       float* topv, int32_t* topi, float* lse, float* scores,
+                       int32_t* slot, int32_t* draft, float* q, void* ws,
+                       const DeviceState& d, cudaStream_t s, unsigned* vz,
+                       int nvz) {
+  using bf = __nv_bfloat16;
+  float* gate = nullptr;
+  unsigned* tickets = nullptr;
+  int* walk_j = nullptr;
+  float* walk_q = nullptr;
+  draft_ws_layout(B, K, H, V, ws, &gate, &tickets, &walk_j, &walk_q);
+  TopkPartials P;
+  int strips = 0;
+  const dflash_status st = lmhead_tc_path(
+      static_cast<const bf*>(h), static_cast<const bf*>(conv_w),
+      static_cast<const bf*>(w_lm), B, K, H, V, topv, topi, lse, ws, d, s,
+      static_cast<const bf*>(w_gate), r, gate, tickets, &P, &strips, q8, vz,
+      nvz);
+  if (st != DFLASH_OK) return st;
+  StageTimer tm(kStPair, s);
+  return cuda_status(launch_draft_tail<bf>(
+      P, strips, anchor, gate, static_cast<const bf*>(e_in),
+      static_cast<const bf*>(e_out), B, K, V, r, T, seed, cycle, topv, topi,
+      lse, scores, slot, draft, q, tickets, walk_j, walk_q, d.err, s));
+}
+
+// dflash_draft; with vz (nvz words) the tensor-core path also zeroes them
+// and sets *zeroed.
+dflash_status draft_call(const void* h, const void* conv_w, const void* w_lm,
+                         const void* w_gate, const void* e_in,
+                         const void* e_out, const int32_t* anchor, int B,
+                         int K, int H, int V, int r, dflash_dtype dt, float T,
+                         uint64_t seed, uint64_t cycle, float* topv,
+                         int32_t* topi, float* lse, float* scores,
+                         int32_t* slot, int32_t* draft, float* q, void* ws,
+                         size_t ws_bytes, dflash_stream_t stream,
+                         unsigned* vz, int nvz, bool* zeroed) {
   REQUIRE(h && w_lm && w_gate && e_in && e_out && anchor && topv && topi &&
           lse && scores && slot && draft && q && ws);
   REQUIRE(sizes_ok(B, K, H, V) && H >= 8 && H % 8 == 0 && r >= 1 &&
@@ -460,51 +506,32 @@ dflash_status dflash_draft(const void* h, const void* conv_w, const void* w_lm,
   dflash_status st = device_state(&d);
   if (st != DFLASH_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  float* gate = nullptr;
-  unsigned* tickets = nullptr;
-  int* walk_j = nullptr;
-  float* walk_q = nullptr;
-  draft_ws_layout(B, K, H, V, ws, &gate, &tickets, &walk_j, &walk_q);
-  cudaError_t e;
   if (dt == DFLASH_BF16 && conv_w) {
-    // The gate rides along with the conv (which also zeroes the walk
-    // tickets); one launch after the LM head merges its partials, scores
-    // the pairs and walks each sequence.
-    using bf = __nv_bfloat16;
-    TopkPartials P;
-    int strips = 0;
-    st = lmhead_tc_path(static_cast<const bf*>(h),
-                        static_cast<const bf*>(conv_w),
-                        static_cast<const bf*>(w_lm), B, K, H, V, topv, topi,
-                        lse, ws, *d, s, static_cast<const bf*>(w_gate), r,
-                        gate, tickets, &P, &strips);
-    if (st != DFLASH_OK) return st;
-    StageTimer tm(kStPair, s);
-    return cuda_status(launch_draft_tail<bf>(
-        P, strips, anchor, gate, static_cast<const bf*>(e_in),
-        static_cast<const bf*>(e_out), B, K, V, r, T, seed, cycle, topv, topi,
-        lse, scores, slot, draft, q, tickets, walk_j, walk_q, d->err, s));
-  } else {
-    st = dflash_lmhead_topk(h, conv_w, w_lm, B, K, H, V, dt, topv, topi, lse,
-                            ws, ws_bytes, stream);
-    if (st != DFLASH_OK) return st;
-    st = dflash_pair_score(topv, topi, anchor, h, w_gate, e_in, e_out, B, K, H,
-                           V, r, dt, scores, stream);
-    if (st != DFLASH_OK) return st;
-    e = cudaSuccess;
+    if (zeroed) *zeroed = vz != nullptr;
+    return draft_tc(h, conv_w, w_lm, nullptr, w_gate, e_in, e_out, anchor, B,
+                    K, H, V, r, T, seed, cycle, topv, topi, lse, scores, slot,
+                    draft, q, ws, *d, s, vz, nvz);
   }
-  if (e != cudaSuccess) return DFLASH_ERR_CUDA;
+  if (zeroed) *zeroed = false;
+  st = dflash_lmhead_topk(h, conv_w, w_lm, B, K, H, V, dt, topv, topi, lse,
+                          ws, ws_bytes, stream);
+  if (st != DFLASH_OK) return st;
+  st = dflash_pair_score(topv, topi, anchor, h, w_gate, e_in, e_out, B, K, H,
+                         V, r, dt, scores, stream);
+  if (st != DFLASH_OK) return st;
   return dflash_path_walk(scores, topi, B, K, T, seed, cycle, slot, draft, q,
                           stream);
 }
 
-dflash_status dflash_draft_e4m3(
+// dflash_draft_e4m3; with vz (nvz words) the conv launch also zeroes them.
+dflash_status draft_e4m3_call(
     const void* h, const void* conv_w, const uint8_t* w_lm_codes,
     const float* w_lm_scale, const void* w_gate, const void* e_in,
     const void* e_out, const int32_t* anchor, int B, int K, int H, int V,
     int r, float T, uint64_t seed, uint64_t cycle, float* topv,
     int32_t* topi, float* lse, float* scores, int32_t* slot, int32_t* draft,
-    float* q, void* ws, size_t ws_bytes, dflash_stream_t stream) {
+    float* q, void* ws, size_t ws_bytes, dflash_stream_t stream,
+    unsigned* vz, int nvz) {
   REQUIRE(h && conv_w && w_lm_codes && w_lm_scale && w_gate && e_in &&
           e_out && anchor && topv && topi && lse && scores && slot && draft &&
           q && ws);
@@ -518,30 +545,81 @@ dflash_status dflash_draft_e4m3(
   REQUIRE(ws_bytes >=
           draft_e4m3_ws_layout(B, K, H, V, nullptr, nullptr, nullptr));
   DeviceState* d = nullptr;
-  dflash_status st = device_state(&d);
+  const dflash_status st = device_state(&d);
   if (st != DFLASH_OK) return st;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  float* gate = nullptr;
-  unsigned* tickets = nullptr;
-  int* walk_j = nullptr;
-  float* walk_q = nullptr;
-  draft_ws_layout(B, K, H, V, ws, &gate, &tickets, &walk_j, &walk_q);
   E4m3Head q8{w_lm_codes, w_lm_scale, nullptr, nullptr};
   draft_e4m3_ws_layout(B, K, H, V, ws, &q8.y_codes, &q8.y_scale);
-  using bf = __nv_bfloat16;
-  TopkPartials P;
-  int strips = 0;
-  st = lmhead_tc_path(static_cast<const bf*>(h),
-                      static_cast<const bf*>(conv_w), nullptr, B, K, H, V,
-                      topv, topi, lse, ws, *d, s,
-                      static_cast<const bf*>(w_gate), r, gate, tickets, &P,
-                      &strips, &q8);
+  return draft_tc(h, conv_w, nullptr, &q8, w_gate, e_in, e_out, anchor, B, K,
+                  H, V, r, T, seed, cycle, topv, topi, lse, scores, slot,
+                  draft, q, ws, *d, reinterpret_cast<cudaStream_t>(stream),
+                  vz, nvz);
+}
+
+}  // namespace
+}  // namespace dflash
+
+extern "C" {
+
+dflash_status dflash_draft(const void* h, const void* conv_w, const void* w_lm,
+                           const void* w_gate, const void* e_in,
+                           const void* e_out, const int32_t* anchor, int B,
+                           int K, int H, int V, int r, dflash_dtype dt,
+                           float T, uint64_t seed, uint64_t cycle, float* topv,
+                           int32_t* topi, float* lse, float* scores,
+                           int32_t* slot, int32_t* draft, float* q, void* ws,
+                           size_t ws_bytes, dflash_stream_t stream) {
+  return draft_call(h, conv_w, w_lm, w_gate, e_in, e_out, anchor, B, K, H, V,
+                    r, dt, T, seed, cycle, topv, topi, lse, scores, slot,
+                    draft, q, ws, ws_bytes, stream, nullptr, 0, nullptr);
+}
+
+dflash_status dflash_draft_e4m3(
+    const void* h, const void* conv_w, const uint8_t* w_lm_codes,
+    const float* w_lm_scale, const void* w_gate, const void* e_in,
+    const void* e_out, const int32_t* anchor, int B, int K, int H, int V,
+    int r, float T, uint64_t seed, uint64_t cycle, float* topv,
+    int32_t* topi, float* lse, float* scores, int32_t* slot, int32_t* draft,
+    float* q, void* ws, size_t ws_bytes, dflash_stream_t stream) {
+  return draft_e4m3_call(h, conv_w, w_lm_codes, w_lm_scale, w_gate, e_in,
+                         e_out, anchor, B, K, H, V, r, T, seed, cycle, topv,
+                         topi, lse, scores, slot, draft, q, ws, ws_bytes,
+                         stream, nullptr, 0);
+}
+
+dflash_status dflash_cycle(
+    const void* h, const void* conv_w, const void* w_lm,
+    const float* w_lm_scale, const void* w_gate, const void* e_in,
+    const void* e_out, const int32_t* anchor, const float* target_logits,
+    int B, int K, int H, int V, int r, dflash_dtype dt, float T,
+    uint64_t seed, uint64_t cycle, float* topv, int32_t* topi, float* lse,
+    float* scores, int32_t* slot, int32_t* draft, float* q,
+    int32_t* n_accepted, int32_t* out_tok, void* ws_draft,
+    size_t ws_draft_bytes, void* ws_verify, size_t ws_verify_bytes,
+    dflash_stream_t stream) {
+  REQUIRE(verify_args_ok(target_logits, draft, topi, q, B, K, V, T,
+                         n_accepted, out_tok));
+  REQUIRE(ws_verify && aligned(ws_verify, 256));
+  REQUIRE(ws_verify_bytes >= verify_ws_layout(B, K, V, nullptr, nullptr));
+  REQUIRE(!w_lm_scale || dt == DFLASH_BF16);
+  VerifyWs w;
+  verify_ws_layout(B, K, V, ws_verify, &w);
+  const int nvz = (int)(w.counter_bytes / sizeof(unsigned));
+  bool zeroed = true;
+  dflash_status st =
+      w_lm_scale
+          ? draft_e4m3_call(h, conv_w, static_cast<const uint8_t*>(w_lm),
+                            w_lm_scale, w_gate, e_in, e_out, anchor, B, K, H,
+                            V, r, T, seed, cycle, topv, topi, lse, scores,
+                            slot, draft, q, ws_draft, ws_draft_bytes, stream,
+                            w.counters, nvz)
+          : draft_call(h, conv_w, w_lm, w_gate, e_in, e_out, anchor, B, K, H,
+                       V, r, dt, T, seed, cycle, topv, topi, lse, scores,
+                       slot, draft, q, ws_draft, ws_draft_bytes, stream,
+                       w.counters, nvz, &zeroed);
   if (st != DFLASH_OK) return st;
-  StageTimer tm(kStPair, s);
-  return cuda_status(launch_draft_tail<bf>(
-      P, strips, anchor, gate, static_cast<const bf*>(e_in),
-      static_cast<const bf*>(e_out), B, K, V, r, T, seed, cycle, topv, topi,
-      lse, scores, slot, draft, q, tickets, walk_j, walk_q, d->err, s));
+  return verify_run(target_logits, draft, topi, q, B, K, V, T, seed, cycle,
+                    n_accepted, out_tok, w,
+                    reinterpret_cast<cudaStream_t>(stream), zeroed);
 }
 
 dflash_status dflash_verify(const float* target_logits, const int32_t* draft,
@@ -557,7 +635,7 @@ dflash_status dflash_verify(const float* target_logits, const int32_t* draft,
   verify_ws_layout(B, K, V, ws, &w);
   return verify_run(target_logits, draft, topi, q, B, K, V, T, seed, cycle,
                     n_accepted, out_tok, w,
-                    reinterpret_cast<cudaStream_t>(stream));
+                    reinterpret_cast<cudaStream_t>(stream), false);
 }
 
 dflash_status dflash_lmhead_topk_shard(const void* h, const void* conv_w,

@@ -81,7 +81,8 @@ __global__ void __launch_bounds__(THREADS)
                    int r, __nv_bfloat16* __restrict__ y,
                    float* __restrict__ gate, unsigned* __restrict__ tickets,
                    int ntickets, float* __restrict__ row_bound, int nbound,
-                   int* err, uint64_t wait_ns) {
+                   int* err, uint64_t wait_ns, unsigned* __restrict__ tickets2,
+                   int ntickets2) {
   constexpr int STAGES = ConvCfg<BC>::STAGES;
   constexpr int B_BYTES = ConvCfg<BC>::B_BYTES;
   constexpr int STAGE_BYTES = ConvCfg<BC>::STAGE_BYTES;
@@ -126,6 +127,12 @@ __global__ void __launch_bounds__(THREADS)
   if (threadIdx.x == 0) pdl_trigger();
   if (tickets && blockIdx.x == 0 && blockIdx.y == 0)
     for (int i = threadIdx.x; i < ntickets; i += THREADS) tickets[i] = 0u;
+  if (tickets2) {  // a later launch's tickets (the cycle's verify)
+    const int lin = blockIdx.y * gridDim.x + blockIdx.x;
+    for (int i = lin * THREADS + threadIdx.x; i < ntickets2;
+         i += gridDim.x * gridDim.y * THREADS)
+      tickets2[i] = 0u;
+  }
   if (row_bound) {  // the next launch's shared row bounds start unset
     const int lin = blockIdx.y * gridDim.x + blockIdx.x;
     for (int i = lin * THREADS + threadIdx.x; i < nbound;
@@ -274,7 +281,8 @@ cudaError_t launch_conv_bc(const CUtensorMap& map_h, const CUtensorMap& map_wc,
                            int B, int K, int H, int r, __nv_bfloat16* y,
                            float* gate, unsigned* tickets, float* row_bound,
                            int nbound, int* err, cudaStream_t s,
-                           uint64_t wait_ns) {
+                           uint64_t wait_ns, unsigned* tickets2,
+                           int ntickets2) {
   const int M = B * K;
   cudaError_t e = cudaFuncSetAttribute(
       conv_tc_kernel<BC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -285,7 +293,8 @@ cudaError_t launch_conv_bc(const CUtensorMap& map_h, const CUtensorMap& map_wc,
   PdlLaunch L(grid, dim3(THREADS), conv_smem_bytes<BC>(), s);
   return cudaLaunchKernelEx(&L.cfg, conv_tc_kernel<BC>, map_h, map_wc,
                             map_wg ? *map_wg : map_wc, h, M, K, H, r, y, gate,
-                            tickets, B, row_bound, nbound, err, wait_ns);
+                            tickets, B, row_bound, nbound, err, wait_ns,
+                            tickets2, ntickets2);
 }
 }  // namespace
 
@@ -294,12 +303,15 @@ cudaError_t launch_conv_tc(const CUtensorMap& map_h, const CUtensorMap& map_wc,
                            int B, int K, int H, int r, __nv_bfloat16* y,
                            float* gate, unsigned* tickets, float* row_bound,
                            int nbound, int* err, cudaStream_t s,
-                           uint64_t wait_ns) {
+                           uint64_t wait_ns, unsigned* tickets2,
+                           int ntickets2) {
   if (conv_tc_bc(B * K) == 128)
     return launch_conv_bc<128>(map_h, map_wc, map_wg, h, B, K, H, r, y, gate,
-                               tickets, row_bound, nbound, err, s, wait_ns);
+                               tickets, row_bound, nbound, err, s, wait_ns,
+                               tickets2, ntickets2);
   return launch_conv_bc<32>(map_h, map_wc, map_wg, h, B, K, H, r, y, gate,
-                            tickets, row_bound, nbound, err, s, wait_ns);
+                            tickets, row_bound, nbound, err, s, wait_ns,
+                            tickets2, ntickets2);
 }
 
 }  // namespace dflash

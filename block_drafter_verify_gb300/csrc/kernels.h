@@ -29,14 +29,16 @@ bool make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner,
 // With map_wg (w_gate [r, H], box {64, 32}) the launch also writes the pair
 // selector's gate g = sigmoid(W_g h) as gate [B*K, r] fp32.  tickets (B
 // words, may be NULL) are zeroed and row_bound (nbound floats, may be NULL)
-// set to -inf for later launches of the same call.
+// set to -inf for later launches of the same call; so are tickets2
+// (ntickets2 words, may be NULL: the tickets of the cycle's verify).
 int conv_tc_bc(int M);
 cudaError_t launch_conv_tc(const CUtensorMap& map_h, const CUtensorMap& map_wc,
                            const CUtensorMap* map_wg, const __nv_bfloat16* h,
                            int B, int K, int H, int r, __nv_bfloat16* y,
                            float* gate, unsigned* tickets, float* row_bound,
                            int nbound, int* err, cudaStream_t s,
-                           uint64_t wait_ns = kWaitLimitNs);
+                           uint64_t wait_ns = kWaitLimitNs,
+                           unsigned* tickets2 = nullptr, int ntickets2 = 0);
 // TMA descriptor of a row-major 8-bit [rows, inner] matrix, 128-byte
 // swizzle (inner a multiple of 16).
 bool make_tmap_u8_2d(CUtensorMap* map, const void* base, uint64_t inner,

@@ -43,7 +43,7 @@ dflash_status verify_run(const float* target_logits, const int32_t* draft,
                          const int32_t* topi, const float* q, int B, int K,
                          int V, float T, uint64_t seed, uint64_t cycle,
                          int32_t* n_accepted, int32_t* out_tok,
-                         const VerifyWs& w, cudaStream_t s);
+                         const VerifyWs& w, cudaStream_t s, bool zeroed);
 
 namespace {
 
@@ -94,5 +94,5 @@ extern "C" dflash_status dflash_verify_noalloc(
   verify_ws_layout(B, K, V, base, &w);
   return verify_run(target_logits, draft, topi, q, B, K, V, T, seed, cycle,
                     n_accepted, out_tok, w,
-                    reinterpret_cast<cudaStream_t>(stream));
+                    reinterpret_cast<cudaStream_t>(stream), false);
 }

@@ -281,6 +281,41 @@ dflash_status dflash_verify(const float* target_logits, const int32_t* draft,
                             size_t ws_bytes, dflash_stream_t s);
 
 /*
+ * One whole cycle, steps a1-a6: dflash_draft (or, with w_lm_scale,
+ * dflash_draft_e4m3 with w_lm as the E4M3 codes) followed by dflash_verify
+ * of its draft, topi and q, with the same arguments, outputs and results
+ * as those two calls.  On the tensor-core paths (bf16 storage with a conv)
+ * the conv launch also zeroes the verify's tickets, which dflash_verify
+ * otherwise zeroes with a copy-engine fill of its own before its launch;
+ * that fill and its gap before the verify launch cost about 4.5 us of a
+ * b32k8 cycle (B = 32, K = 8, V = 151936).
+ *   inputs   h, conv_w, w_lm, w_lm_scale (NULL: bf16 LM head; else w_lm
+ *            holds [V, H] uint8 codes and w_lm_scale [V] fp32 scales from
+ *            dflash_quantize_e4m3_rows), w_gate, e_in, e_out, anchor, the
+ *            sizes, dt, T, seed, cycle: as in dflash_draft(_e4m3);
+ *            target_logits [B, K+1, V] fp32 as in dflash_verify
+ *   outputs  topv, topi, lse, scores, slot, draft, q (the draft call's),
+ *            n_accepted, out_tok (the verify's)
+ *   ws_draft >= dflash_workspace_bytes(2, ...) bytes (3 with w_lm_scale),
+ *            ws_verify >= dflash_workspace_bytes(1, B, K, 0, V) bytes, both
+ *            256-byte aligned and caller-owned; ws_verify's contents need
+ *            no zeroing by the caller.
+ * Requirements: the union of the two calls'; w_lm_scale only with
+ * dt == DFLASH_BF16.  Every argument is checked before anything is
+ * launched.
+ */
+dflash_status dflash_cycle(
+    const void* h, const void* conv_w, const void* w_lm,
+    const float* w_lm_scale, const void* w_gate, const void* e_in,
+    const void* e_out, const int32_t* anchor, const float* target_logits,
+    int B, int K, int H, int V, int r, dflash_dtype dt, float T,
+    uint64_t seed, uint64_t cycle, float* topv, int32_t* topi, float* lse,
+    float* scores, int32_t* slot, int32_t* draft, float* q,
+    int32_t* n_accepted, int32_t* out_tok, void* ws_draft,
+    size_t ws_draft_bytes, void* ws_verify, size_t ws_verify_bytes,
+    dflash_stream_t s);
+
+/*
  * dflash_verify without any caller-provided scratch, for callers that
  * cannot allocate device memory at the time they verify: serving loops whose
  * device memory belongs to another engine's allocator, code running where

@@ -154,3 +154,38 @@ def test_noalloc_verify_refuses_bad_arguments_on_the_host(so):
     a = list(base)
     a[13] = 16                                        # ws too small
     assert g(*a) == 1
+
+
+def test_cycle_refuses_bad_arguments_on_the_host(so):
+    """dflash_cycle checks the verify's arguments, then the draft's, before
+    any launch: a null target, a misaligned or too small verify workspace,
+    the 8-bit head with fp32 storage and a draft-side size error are all
+    refused on the host (no GPU needed)."""
+    vp, i32, f32, u64, sz = (ctypes.c_void_p, ctypes.c_int, ctypes.c_float,
+                             ctypes.c_uint64, ctypes.c_size_t)
+    fake = ctypes.c_void_p(0x100000)
+    f = so.dflash_cycle
+    f.restype = i32
+    f.argtypes = ([vp] * 9 + [i32] * 6 + [f32, u64, u64] + [vp] * 9 +
+                  [vp, sz, vp, sz, vp])
+    names = ["h", "conv_w", "w_lm", "w_scale", "w_gate", "e_in", "e_out",
+             "anchor", "L", "B", "K", "H", "V", "r", "dt", "T", "seed",
+             "cycle", "topv", "topi", "lse", "scores", "slot", "draft", "q",
+             "n", "out", "wsd", "wsd_bytes", "wsv", "wsv_bytes", "stream"]
+    ok = dict(zip(names, [fake, fake, fake, None, fake, fake, fake, fake,
+                          fake, 2, 4, 64, 1000, 32, 0, 1.0, 1, 0] +
+                  [fake] * 9 + [fake, 1 << 30, fake, 1 << 30, None]))
+
+    def call(**kw):
+        a = dict(ok)
+        a.update(kw)
+        return f(*[a[k] for k in names])
+    assert call(L=None) == 1                               # no target
+    assert call(n=None) == 1                               # no output
+    assert call(wsv=None) == 1
+    assert call(wsv=ctypes.c_void_p(0x100010)) == 1        # not 256-aligned
+    assert call(wsv_bytes=16) == 1                         # too small
+    assert call(w_scale=fake, dt=1) == 1                   # 8-bit, fp32
+    assert call(H=60) == 1                                 # H % 8 != 0
+    assert call(K=17) == 1
+    assert call(T=-1.0) == 1
