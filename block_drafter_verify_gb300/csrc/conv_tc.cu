@@ -197,11 +197,24 @@ __global__ void __launch_bounds__(THREADS)
   } else {
     const int q = warp & 3;
     const int m = mtile * BM + q * 32 + lane;
+    const bool has_prev = (m % K) != 0;
+    // h_t and h_{t-1} of the first 32 channels, loaded while the MMAs run
+    uint4 hc0[4], hp0[4];
+    const bool pre = !is_gate && m < M;
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      hc0[g] = make_uint4(0u, 0u, 0u, 0u);
+      hp0[g] = hc0[g];
+      if (pre && c0 + g * 8 < H) {
+        const __nv_bfloat16* hr = h + (size_t)m * H + c0 + g * 8;
+        hc0[g] = *reinterpret_cast<const uint4*>(hr);
+        if (has_prev) hp0[g] = *reinterpret_cast<const uint4*>(hr - H);
+      }
+    }
     const bool got = tc::mbar_wait_bounded(&bars->tfull, 0, abort, wait_ns);
     if (__all_sync(0xffffffffu, got)) {
       tc::fence_after_sync();
       const uint32_t tb = tmem + (static_cast<uint32_t>(q * 32) << 16);
-      const bool has_prev = (m % K) != 0;
 #pragma unroll 1
       for (int cg = 0; cg < BC / 32; ++cg) {
         float w0[32], w1[32];
@@ -237,10 +250,14 @@ __global__ void __launch_bounds__(THREADS)
           for (int g = 0; g < 4; ++g) {
             if (cc + g * 8 >= H) break;
             float hc[8], hp[8];
-            bf16x8_to_f32(*reinterpret_cast<const uint4*>(hr + g * 8), hc);
+            bf16x8_to_f32(cg == 0 ? hc0[g]
+                                  : *reinterpret_cast<const uint4*>(hr + g * 8),
+                          hc);
             if (has_prev)
-              bf16x8_to_f32(*reinterpret_cast<const uint4*>(hr - H + g * 8),
-                            hp);
+              bf16x8_to_f32(
+                  cg == 0 ? hp0[g]
+                          : *reinterpret_cast<const uint4*>(hr - H + g * 8),
+                  hp);
             uint4 out;
             __nv_bfloat162* o = reinterpret_cast<__nv_bfloat162*>(&out);
 #pragma unroll
