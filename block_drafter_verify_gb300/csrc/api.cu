@@ -196,9 +196,10 @@ dflash_status lmhead_tc_path(const __nv_bfloat16* h,
     CUtensorMap mh, mw, mg;
     if (!make_tmap_bf16_2d(&mh, h, H, M, 64, 128) ||
         !make_tmap_bf16_2d(&mw, conv_w, H, 2 * (uint64_t)H, 64,
-                           conv_tc_bc(M)))
+                           conv_tc_bc(M, H)))
       return DFLASH_ERR_CUDA;
-    if (w_gate && !make_tmap_bf16_2d(&mg, w_gate, H, r, 64, conv_tc_bc(M)))
+    if (w_gate &&
+        !make_tmap_bf16_2d(&mg, w_gate, H, r, 64, conv_tc_bc(M, H)))
       return DFLASH_ERR_CUDA;
     __nv_bfloat16* y = static_cast<__nv_bfloat16*>(yv);
     {

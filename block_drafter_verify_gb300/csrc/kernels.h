@@ -25,13 +25,13 @@ cudaError_t launch_conv_simt(const T* h, const T* w_conv, int B, int K, int H,
 bool make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner,
                        uint64_t rows, uint32_t box_inner, uint32_t box_rows);
 // map_h: h [B*K, H] box {64, 128}; map_wc: conv_w [2H, H] box {64, BC}
-// with BC = conv_tc_bc(B*K) channels per CTA (map_wg likewise).
+// with BC = conv_tc_bc(B*K, H) channels per tile (map_wg likewise).
 // With map_wg (w_gate [r, H], box {64, 32}) the launch also writes the pair
 // selector's gate g = sigmoid(W_g h) as gate [B*K, r] fp32.  tickets (B
 // words, may be NULL) are zeroed and row_bound (nbound floats, may be NULL)
 // set to -inf for later launches of the same call; so are tickets2
 // (ntickets2 words, may be NULL: the tickets of the cycle's verify).
-int conv_tc_bc(int M);
+int conv_tc_bc(int M, int H);
 cudaError_t launch_conv_tc(const CUtensorMap& map_h, const CUtensorMap& map_wc,
                            const CUtensorMap* map_wg, const __nv_bfloat16* h,
                            int B, int K, int H, int r, __nv_bfloat16* y,

@@ -215,6 +215,47 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
           cluster_addr)
       : "memory");
 }
+// Test for phase `parity` with acquire semantics at cluster scope (for
+// arrivals that release writes made by another CTA of the cluster).
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar,
+                                                      uint32_t parity,
+                                                      uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, "
+      "%3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+// mbar_wait_bounded with cluster-scope acquire.
+__device__ __forceinline__ bool mbar_wait_cluster_bounded(
+    uint64_t* bar, uint32_t parity, volatile int* abort, uint64_t limit_ns) {
+  const uint32_t hint =
+      (uint32_t)(limit_ns < 1000ull ? (limit_ns > 0 ? limit_ns : 1) : 1000ull);
+  if (mbar_try_wait_cluster(bar, parity, hint)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    if (mbar_try_wait_cluster(bar, parity, hint)) return true;
+    if (*abort) return false;
+    if (globaltimer_ns() - t0 > limit_ns) {
+      *abort = 1;
+      return false;
+    }
+  }
+}
+// 16 bytes into the shared memory of a CTA of the cluster (cluster address).
+__device__ __forceinline__ void st_cluster_v4(uint32_t cluster_addr,
+                                              float a, float b, float c,
+                                              float d) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(
+                   cluster_addr),
+               "f"(a), "f"(b), "f"(c), "f"(d)
+               : "memory");
+}
 // All threads of every CTA of the cluster; orders shared and TMEM state.
 __device__ __forceinline__ void cluster_sync() {
   asm volatile(
