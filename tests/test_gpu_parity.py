@@ -415,7 +415,12 @@ def test_full_size_workload(lib, name):
     (65, 16, 200, 3001, 200, 1.0),  # M = 1040: 128-channel conv tiles,
                                     # ragged H and a partial gate tile
     (6, 5, 224, 3001, 32, 1.0),     # ragged K (224 = 3.5 k-blocks)
-    (20, 15, 256, 4099, 128, 0.7),  # M = 300, two gate tiles
+    (20, 15, 256, 4099, 128, 0.7),  # M = 300, one full 128-row gate tile
+    (17, 9, 200, 3001, 200, 1.0),   # M = 153: conv K split over a cluster
+                                    # with ragged H, a ragged second row
+                                    # tile and a partial gate tile
+    (9, 16, 128, 2051, 40, 0.0),    # M = 144: K split into single blocks,
+                                    # one partial gate tile, greedy
 ])
 def test_fused_draft_bf16(lib, B, K, H, V, r, T):
     w = synth.Workload("small", B=B, K=K, V=V, H=H, r=r, dtype="bf16", T=T,
