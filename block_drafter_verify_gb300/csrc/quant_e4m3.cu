@@ -9,8 +9,8 @@
 //   code_ik = e4m3(x_ik / scale_i), round to nearest even, saturated
 //
 // Both divisions are correctly rounded fp32 divisions, so the codes are a
-// deterministic function of the input.  One warp per row; rows up to 4096
-// wide stay in the lanes' registers between the maximum and the
+// deterministic function of the input.  One CTA of four warps per row;
+// rows up to 4096 wide stay in registers between the maximum and the
 // conversion, wider rows are read twice (the second time from L1).
 #include <cuda_fp8.h>
 
@@ -19,7 +19,7 @@
 namespace dflash {
 namespace {
 
-constexpr int kQuantWarps = 8;
+constexpr int kQuantWarps = 4;  // warps per row (one CTA per row)
 constexpr float kE4m3Max = 448.f;
 
 __device__ __forceinline__ void unpack8(const uint4& u, float (&f)[8]) {
@@ -56,9 +56,12 @@ __device__ __forceinline__ void fold8(const float (&f)[8], float& amax,
   }
 }
 
-// kChunks > 0: each lane holds its kChunks 8-element chunks of the row in
-// registers (all loads in flight at once, no second read); 0: two passes
-// over the row, the second from L1.
+// One CTA of kQuantWarps warps per row; the row's 8-element chunks are
+// dealt to the CTA's threads in turn (chunk i to thread i mod 128).
+// kChunks > 0: each thread holds its kChunks chunks in registers (all
+// loads in flight at once, no second read); 0: two passes over the row,
+// the second from L1.  The row's max |x| is reduced over the warps
+// through shared memory; max and the divisions do not depend on the order.
 template <int kChunks>
 __global__ void __launch_bounds__(kQuantWarps * 32)
     quantize_e4m3_rows_kernel(const __nv_bfloat16* __restrict__ x, int R,
@@ -68,9 +71,11 @@ __global__ void __launch_bounds__(kQuantWarps * 32)
   // before it reads the codes.
   pdl_trigger();
   pdl_wait();  // x may be written by the previous launch
-  const int lane = threadIdx.x & 31;
-  const long long row =
-      (long long)blockIdx.x * kQuantWarps + (threadIdx.x >> 5);
+  constexpr int kT = kQuantWarps * 32;
+  __shared__ float s_amax[kQuantWarps];
+  __shared__ int s_bad;
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const long long row = blockIdx.x;
   if (row >= R) return;
   const uint4* src = reinterpret_cast<const uint4*>(x + row * H);
   uint2* dst = reinterpret_cast<uint2*>(codes + row * H);
@@ -81,7 +86,7 @@ __global__ void __launch_bounds__(kQuantWarps * 32)
   if constexpr (kChunks > 0) {
 #pragma unroll
     for (int j = 0; j < kChunks; ++j) {
-      const int i = lane + 32 * j;
+      const int i = tid + kT * j;
       v[j] = i < n8 ? src[i] : make_uint4(0u, 0u, 0u, 0u);
     }
 #pragma unroll
@@ -91,23 +96,27 @@ __global__ void __launch_bounds__(kQuantWarps * 32)
       fold8(f, amax, bad);
     }
   } else {
-    for (int i = lane; i < n8; i += 32) {
+    for (int i = tid; i < n8; i += kT) {
       float f[8];
       unpack8(src[i], f);
       fold8(f, amax, bad);
     }
   }
+  if (tid == 0) s_bad = 0;
 #pragma unroll
   for (int o = 16; o; o >>= 1)
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-  if (__any_sync(0xffffffffu, bad)) {
-    if (lane == 0) raise_error(err, kErrNonfinite);
-  }
-  const float s = amax > 0.f ? __fdiv_rn(amax, kE4m3Max) : 1.f;
+  if (lane == 0) s_amax[wid] = amax;
+  __syncthreads();
+  if (bad) s_bad = 1;
+  float m = s_amax[0];
+#pragma unroll
+  for (int w = 1; w < kQuantWarps; ++w) m = fmaxf(m, s_amax[w]);
+  const float s = m > 0.f ? __fdiv_rn(m, kE4m3Max) : 1.f;
   if constexpr (kChunks > 0) {
 #pragma unroll
     for (int j = 0; j < kChunks; ++j) {
-      const int i = lane + 32 * j;
+      const int i = tid + kT * j;
       if (i < n8) {
         float f[8];
         unpack8(v[j], f);
@@ -115,13 +124,17 @@ __global__ void __launch_bounds__(kQuantWarps * 32)
       }
     }
   } else {
-    for (int i = lane; i < n8; i += 32) {
+    for (int i = tid; i < n8; i += kT) {
       float f[8];
       unpack8(src[i], f);
       dst[i] = encode8(f, s);
     }
   }
-  if (lane == 0) scale[row] = s;
+  __syncthreads();
+  if (tid == 0) {
+    scale[row] = s;
+    if (s_bad) raise_error(err, kErrNonfinite);
+  }
 }
 
 }  // namespace
@@ -129,15 +142,15 @@ __global__ void __launch_bounds__(kQuantWarps * 32)
 cudaError_t launch_quantize_e4m3_rows(const __nv_bfloat16* x, int R, int H,
                                       uint8_t* codes, float* scale, int* err,
                                       cudaStream_t s) {
-  const long long blocks = ((long long)R + kQuantWarps - 1) / kQuantWarps;
-  if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
-  PdlLaunch L(dim3((unsigned)blocks), dim3(kQuantWarps * 32), 0, s);
+  if (R > 0x7fffffff) return cudaErrorInvalidValue;
+  PdlLaunch L(dim3((unsigned)R), dim3(kQuantWarps * 32), 0, s);
   const int n8 = H / 8;
-  if (n8 <= 32 * 8)
-    return cudaLaunchKernelEx(&L.cfg, quantize_e4m3_rows_kernel<8>, x, R, H,
+  constexpr int kT = kQuantWarps * 32;
+  if (n8 <= kT * 2)
+    return cudaLaunchKernelEx(&L.cfg, quantize_e4m3_rows_kernel<2>, x, R, H,
                               codes, scale, err);
-  if (n8 <= 32 * 16)
-    return cudaLaunchKernelEx(&L.cfg, quantize_e4m3_rows_kernel<16>, x, R, H,
+  if (n8 <= kT * 4)
+    return cudaLaunchKernelEx(&L.cfg, quantize_e4m3_rows_kernel<4>, x, R, H,
                               codes, scale, err);
   return cudaLaunchKernelEx(&L.cfg, quantize_e4m3_rows_kernel<0>, x, R, H,
                             codes, scale, err);
