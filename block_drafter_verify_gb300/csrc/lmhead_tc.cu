@@ -569,11 +569,14 @@ __global__ void __launch_bounds__(Cfg<kPair, kFp8>::THREADS, 1)
           for (int i = 1; i < 32; ++i) cm = fmaxf(cm, x[i]);
         } else {
           cm = fold_chunk(x, l2e, run_m, run_s);
+          // the tile's running maximum is final: publish it now, so the
+          // store is done before the accumulator is handed back (that
+          // arrive's release would wait for it)
+          if (c == CH - 1) publish();
         }
         insert(chunk_candidates(x, cm, tv[kC - 1], lo, xs),
                vt * BN + (half * CH + c) * 32);
       }
-      if (it > 0) publish();
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) {
