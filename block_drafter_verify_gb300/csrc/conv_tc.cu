@@ -25,9 +25,9 @@
 //
 // Optionally the same launch also computes the pair selector's context gate
 // g_t = sigmoid(W_g h_t) ("A Lightweight Path Selector", DFlash 2: Keep
-// Drafting Parallel), which reads the same h tiles: extra CTAs after the
-// channel tiles take 64 gate rows each as their B operand (W_g rows
-// [g0, g0+64) in two 32-row boxes) and write g in fp32.
+// Drafting Parallel), which reads the same h tiles: extra tiles after the
+// channel tiles take 2BC gate rows each as their B operand (W_g rows
+// [g0, g0+2BC) in two BC-row boxes) and write g in fp32.
 #include "kernels.h"
 #include "tc_ptx.cuh"
 

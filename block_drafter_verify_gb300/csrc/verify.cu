@@ -23,14 +23,17 @@
 //               its one resample uniform, so drawing every row ahead of time
 //               gives the same token as drawing only the rejected one.  A
 //               row that cannot be emitted skips its draw: its draft was
-//               accepted, or an earlier position of the sequence already
-//               recorded a rejection in the sequence's mask (for t = K: any
-//               rejection).  The
-//               drafter's inputs of row t (draft, candidates, q and the
-//               target logits at those tokens) are fetched at the start of
-//               the CTA, so none of this waits on another launch or row.
-//   sequence    the last row of a sequence to finish keeps the prefix before
-//               the first rejection n and emits row n's token.
+//               accepted, or an earlier position of the sequence had already
+//               recorded a rejection in the sequence's mask when the row
+//               read it (for t = K: any rejection).  The drafter's inputs of
+//               row t (draft, candidates, q and the target logits at those
+//               tokens) are fetched at the start of the CTA, and the row's
+//               uniforms drawn then, so none of this waits on another launch
+//               or row.
+//   sequence    each row adds one arrival and, if its draft was rejected,
+//               its position's bit to the sequence's word; the row whose
+//               arrival is the last keeps the prefix before the first
+//               rejection n and emits row n's token.
 // "Last CTA" is an atomic ticket; nothing ever waits.  All folds and sums
 // run in a fixed order, so results are identical run to run.
 #include <algorithm>
