@@ -51,8 +51,8 @@ bool make_tmap_u8_2d(CUtensorMap* map, const void* base, uint64_t inner,
 // row_bound (M * kBoundSlots floats set to -inf by an earlier launch of
 // the same stream, may be NULL) is where units share their rows' running
 // maxima, from which every unit prunes values that cannot reach a row's
-// top 16 (room for 32 slots per row; CTA pairs use 16 per row, rows 16
-// floats apart).
+// top 16 (room for 32 slots per row; 16 per row, rows 16 floats apart,
+// except for at most 8 rows).
 constexpr int kBoundSlots = 32;
 cudaError_t launch_lmhead_tc(const CUtensorMap& map_y, const CUtensorMap& map_w,
                              int M, int H, int V, int num_sms, TopkPartials P,

@@ -41,10 +41,9 @@
 // Candidate insertions dominate the epilogue.  They are pruned twice: in a
 // unit's first tile, where the list is empty, by the 16th largest of 32
 // column-group maxima (at least 16 of the tile's values reach it), and in
-// every tile by the running maxima that 16 (CTA pairs) or 32 (single
-// CTAs) units of the row group publish in the workspace (values of
-// distinct columns, so a value below 16 of them cannot make the row's top
-// 16).
+// every tile by the running maxima that 16 (32 for at most 8 rows) units
+// of the row group publish in the workspace (values of distinct columns,
+// so a value below 16 of them cannot make the row's top 16).
 // Every wait is time-bounded; on a timeout the CTA stops issuing, drains
 // its copies and MMAs, frees TMEM, flags the error word and exits.
 #include <algorithm>
@@ -456,29 +455,29 @@ __global__ void __launch_bounds__(Cfg<kPair, kFp8>::THREADS, 1)
     for (int k = 0; k < kC; ++k) { tv[k] = -INFINITY; ti[k] = -1; }
     float run_m = -INFINITY, run_s = 0.f;
     bool ok = true;
-    // Shared row bounds: the lists of kSlots units (strips 0.. of the row
+    // Shared row bounds: the lists of nslots units (strips 0.. of the row
     // group, each half of a tile's columns its own slot) publish their
     // running maxima; these are values of distinct columns, so a value
     // below 16 of them cannot make the row's top 16 and no unit needs to
-    // insert it.  CTA pairs (every thread a row) take the smallest of 16
-    // slots; single CTAs (at most 128 rows, so few threads read) the 16th
-    // largest of 32, a tighter bound that costs 32 loads and a sorting
-    // network per tile.  Unset slots hold -inf; reads may be stale, which
-    // only weakens the bound.
-    constexpr int kSlots = kPair ? 16 : 32;
-    static_assert(kSlots <= kBoundSlots, "row bound slots");
+    // insert it.  Usually the bound is the smallest of 16 slots; for at
+    // most 8 rows (single CTAs, so only a few threads per CTA read it) the
+    // 16th largest of 32, a tighter bound that costs 32 loads and a
+    // sorting network per tile.  Unset slots hold -inf; reads may be
+    // stale, which only weakens the bound.
+    const bool wide = !kPair && M <= 8;
+    const int nslots = wide ? 32 : 16;
     const int bslot = strip * C::HALVES + half;
-    // rows kSlots floats apart, so a CTA pair's rows stay packed
-    float* rb = row_bound && m < M ? row_bound + (size_t)m * kSlots
+    // rows nslots floats apart, so many rows stay packed
+    float* rb = row_bound && m < M ? row_bound + (size_t)m * nslots
                                    : nullptr;
     auto publish = [&]() {
-      if (rb && bslot < kSlots) rb[bslot] = run_m;
+      if (rb && bslot < nslots) rb[bslot] = run_m;
     };
     auto read_bound = [&]() {
       float bd = -INFINITY;
       if (rb) {
         const float4* r4 = reinterpret_cast<const float4*>(rb);
-        if constexpr (kSlots == 16) {
+        if (!wide) {
           bd = INFINITY;
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
