@@ -50,10 +50,12 @@ struct ConvCfg {
   static constexpr int B_BYTES = 2 * BC * BK * 2;  // W0 part, then W1 part
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr uint32_t TMEM_COLS = 2 * BC;
-  // K split: the 64 partial sums per row received from the other CTA
-  // (rows padded to 68 words, so 8 lanes' 16-byte stores hit 32 banks)
-  static constexpr int XSTRIDE = 68;
-  static constexpr int XBUF_BYTES = KS == 2 ? BM * XSTRIDE * 4 : 0;
+  // K split: the 64 partial sums per row received from the other CTA, as
+  // 16 columns of 128 rows of float4 (one warp's remote store, and later
+  // its load, of a column covers 512 contiguous bytes: a scattered layout,
+  // a row's 64 sums together, made each remote store 32 separate pieces
+  // and the send took 4k SM cycles)
+  static constexpr int XBUF_BYTES = KS == 2 ? BM * 64 * 4 : 0;
 };
 
 template <int STAGES>
@@ -93,7 +95,7 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4& u, float* f) {
 }
 
 template <int BC, int KS>
-__global__ void __launch_bounds__(THREADS)
+__global__ void __launch_bounds__(THREADS, 1)
     conv_tc_kernel(const __grid_constant__ CUtensorMap map_h,
                    const __grid_constant__ CUtensorMap map_wc,
                    const __grid_constant__ CUtensorMap map_wg,
@@ -197,7 +199,8 @@ __global__ void __launch_bounds__(THREADS)
         if (++stage == STAGES) { stage = 0; phase ^= 1; }
       }
       for (int s = 0; s < STAGES; ++s)
-        if ((issued >> s) & 1) wait_timeout(&bars->full[s], (last_par >> s) & 1);
+        if ((issued >> s) & 1)
+          wait_timeout(&bars->full[s], (last_par >> s) & 1);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -247,12 +250,17 @@ __global__ void __launch_bounds__(THREADS)
         if (has_prev) hp0[g] = *reinterpret_cast<const uint4*>(hr - H);
       }
     }
-    // gate rows [g0, g0 + 32) of this row from 32 pre-activations
+    // gate rows [g0, g0 + 32) of this row from 32 pre-activations.  The
+    // fast reciprocal divide (within 2 ulp; 0 for divisors past 2^126, the
+    // sigmoid's limit there): the correctly rounded divide's per-value
+    // latency chain, 64 values per thread in a warp per scheduler, made the
+    // gate tiles' epilogue 9k SM cycles and them the launch's last CTAs
     auto write_gate = [&](int g0, const float (&z)[32]) {
       float* gr = gate + (size_t)m * r + g0;
       float g[32];
 #pragma unroll
-      for (int j = 0; j < 32; ++j) g[j] = 1.f / (1.f + __expf(-z[j]));
+      for (int j = 0; j < 32; ++j)
+        g[j] = __fdividef(1.f, 1.f + __expf(-z[j]));
       if (r % 4 == 0 && g0 + 32 <= r) {
 #pragma unroll
         for (int j = 0; j < 32; j += 4)
@@ -310,25 +318,26 @@ __global__ void __launch_bounds__(THREADS)
         tc::tmem_ld_x32(tb + o0, w0);
         tc::tmem_ld_x32(tb + o1, w1);
         const uint32_t peer = (uint32_t)(kh ^ 1);
-        const uint32_t xr = tc::mapa_shared(
-            tc::smem_u32(xbuf + row * Cf::XSTRIDE), peer);
+        const uint32_t xr =
+            tc::mapa_shared(tc::smem_u32(xbuf) + row * 16, peer);
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          tc::st_cluster_v4(xr + 16 * j, w0[4 * j], w0[4 * j + 1],
+          tc::st_cluster_v4(xr + j * (BM * 16), w0[4 * j], w0[4 * j + 1],
                             w0[4 * j + 2], w0[4 * j + 3]);
-          tc::st_cluster_v4(xr + 128 + 16 * j, w1[4 * j], w1[4 * j + 1],
-                            w1[4 * j + 2], w1[4 * j + 3]);
+          tc::st_cluster_v4(xr + (8 + j) * (BM * 16), w1[4 * j],
+                            w1[4 * j + 1], w1[4 * j + 2], w1[4 * j + 3]);
         }
         tc::mbar_arrive_cluster(
             tc::mapa_shared(tc::smem_u32(&bars->xbar), peer));
         tc::tmem_ld_x32(tb + m0, w0);
         tc::tmem_ld_x32(tb + m1, w1);
-        if (tc::mbar_wait_cluster_bounded(&bars->xbar, 0, abort, wait_ns)) {
-          const float4* xs =
-              reinterpret_cast<const float4*>(xbuf + row * Cf::XSTRIDE);
+        const bool xok =
+            tc::mbar_wait_cluster_bounded(&bars->xbar, 0, abort, wait_ns);
+        if (__all_sync(0xffffffffu, xok)) {
+          const float4* xs = reinterpret_cast<const float4*>(xbuf) + row;
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
-            const float4 a = xs[j], b = xs[8 + j];
+            const float4 a = xs[j * BM], b = xs[(8 + j) * BM];
             w0[4 * j] += a.x;
             w0[4 * j + 1] += a.y;
             w0[4 * j + 2] += a.z;
