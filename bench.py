@@ -775,17 +775,23 @@ def run_ours(args):
             stage_roof[name] = {"bytes": nbytes, "GB/s": gbs,
                                 "frac": gbs / pk["hbm_gbs"]}
     if "verify" in stage_roof:
-        # the design reads every target row; the algorithm needs rows
-        # 0..n of each sequence (n accepted drafts) and the draw row again
+        # The verify reads rows 0..n of each sequence (n accepted drafts),
+        # the draw row again, and of the later rows only what it streams
+        # before the earlier rejection is known: the main figure is the
+        # bytes the accepted lengths need; every target row's bytes (what
+        # a verify reading all rows would move in the same time) beside it
+        ab = stage_roof["verify"]["bytes"]
         vb = verify_algorithmic(w, n_mean_cycles)
         vgbs = vb / (stage_us["verify"] * 1e-6) / 1e9
-        stage_roof["verify"].update({
-            "design_bytes": stage_roof["verify"]["bytes"],
-            "algorithmic_bytes": vb, "algorithmic_GB/s": vgbs,
-            "frac_algorithmic": vgbs / pk["hbm_gbs"],
-            "note": "frac is of the bytes the design reads (all B*(K+1) "
-                    "target rows); frac_algorithmic of the rows the "
-                    "accepted lengths need"})
+        stage_roof["verify"] = {
+            "bytes": vb, "GB/s": vgbs, "frac": vgbs / pk["hbm_gbs"],
+            "all_rows_bytes": ab,
+            "all_rows_GB/s": stage_roof["verify"]["GB/s"],
+            "frac_all_rows": stage_roof["verify"]["frac"],
+            "note": "rows after a sequence's first rejection stop being "
+                    "read once it is known; bytes = rows 0..n of each "
+                    "sequence and the draw row again; all_rows_bytes = "
+                    "every B*(K+1) target row"}
 
     # end to end through the public API with host buffers
     e2e_steps = args.e2e_steps or max(3, min(K, 20))

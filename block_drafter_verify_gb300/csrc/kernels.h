@@ -129,13 +129,19 @@ struct VerifyWs {
                        // T > 0, chunk (max, argmax) at T = 0
   int* row_tok;        // [rows] token emitted if t is the first rejection
                        // (t = K: the bonus token)
-  unsigned* counters;  // [rows] tickets, [B] sequence words (arrivals << 16
-                       // | rejected positions), [B] masks of rejections
-                       // seen by the draws; zeroed before every launch
-  unsigned* rejmask;   // [B] bit t: position t rejected (in counters)
+  unsigned* counters;  // zeroed before every launch: the sequences' words,
+                       // then the rows' tickets
+  unsigned long long* seq;  // [B] (in counters): bit t (t < K) position t
+                            // rejected, bit 32 + t row t decided
+  unsigned* tickets;   // [rows] (in counters): chunks of the row done
   size_t counter_bytes;
 };
 constexpr int kVerifyMaxChunks = 64;  // row chunks (CTAs) per target row
+// The verify grid: positions t < t_split in nchunk0 chunks of bpc0 blocks
+// per row, later positions in nchunk1 chunks of bpc1 blocks.
+struct VerifyGrid {
+  int nchunk0, bpc0, nchunk1, bpc1, t_split;
+};
 size_t verify_ws_layout(int B, int K, int V, void* base, VerifyWs* out);
 // The caller zeroes ws.counters on stream s first.  With `stats` (a
 // vocabulary shard [v0, v0 + V) of the rows): the rows' shard statistics

@@ -4,15 +4,26 @@
 // diffusion, wearing a drafter's coat): accept a draft token with
 // probability min(1, p/q) and resample from the residual on rejection.
 //
-// One launch, grid (B*(K+1) target rows, chunks of each row), 256 threads:
+// One launch over the B*(K+1) target rows, each in chunks, 256 threads:
+//   order       the CTAs go in position order (all sequences' chunks of
+//               position 0, then position 1, ...), the chunks sized so that
+//               position 0 alone fills the GPU (about two CTAs per SM).
+//               Only rows 0..n of a sequence matter (n its first
+//               rejection): once the sequence's word shows a rejection
+//               before t, the chunks of row t stop reading and leave
+//               without arriving anywhere (a chunk that starts after it
+//               reads nothing).  At low acceptance most of the later rows
+//               are never read; at high acceptance every row is needed and
+//               read, as before.
 //   main pass   a CTA walks its chunk in blocks of 16384 tokens; warp w of
 //               the CTA owns the contiguous 2048-token segment w of each
 //               block and reads it with 16-byte loads straight into
-//               registers (lane l holds the words 4l + 128u, u < 16).  No
-//               shared-memory staging: every CTA of the grid is resident
-//               at once and keeps its loads in flight.  At T > 0 a warp
-//               reduces a segment to (max, sum 2^((x-max)/T log2 e)); at
-//               T = 0 the CTA keeps the first argmax.
+//               registers (lane l holds the words 4l + 128u, u < 16), with
+//               no shared-memory staging.  Before each segment a warp
+//               checks the sequence's mask, read one segment ahead.  At
+//               T > 0 a warp reduces a segment to (max, sum
+//               2^((x-max)/T log2 e)); at T = 0 the CTA keeps the first
+//               argmax.
 //   row work    the last CTA to finish row (b, t) (atomic ticket) folds the
 //               row in a fixed tree (row max, Z, argmax) and then settles
 //               everything that depends on that row alone: the accept test
@@ -30,10 +41,13 @@
 //               tokens) are fetched at the start of the CTA, and the row's
 //               uniforms drawn then, so none of this waits on another launch
 //               or row.
-//   sequence    each row adds one arrival and, if its draft was rejected,
-//               its position's bit to the sequence's word; the row whose
-//               arrival is the last keeps the prefix before the first
-//               rejection n and emits row n's token.
+//   sequence    a rejected row sets its position's bit in the sequence's
+//               64-bit word right after its test; every tested row then
+//               sets its decided bit (after its draw).  The row whose bit
+//               completes rows 0..n, n the lowest rejected position (K if
+//               none), keeps the prefix before n and emits row n's token.
+//               A row that stopped early is never among rows 0..n: it
+//               stopped on a rejection before it.
 // "Last CTA" is an atomic ticket; nothing ever waits.  All folds and sums
 // run in a fixed order, so results are identical run to run.
 #include <algorithm>
@@ -53,6 +67,18 @@ __device__ __forceinline__ float ex2f(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// A sequence's result is known once rows 0..n are decided, n its first
+// rejected position (K if none): w holds the rejected positions in its low
+// word and the decided rows in its high word.  A row's rejection bit goes
+// in before its decided bit, so once rows 0..n are decided no bit below n
+// can still appear, and the state never turns back.
+__device__ __forceinline__ bool seq_settled(unsigned long long w, int K) {
+  const unsigned rej = (unsigned)w;
+  const int n = rej ? __ffs(rej) - 1 : K;
+  const unsigned need = (2u << n) - 1u;  // rows 0..n (n <= 16)
+  return ((unsigned)(w >> 32) & need) == need;
 }
 
 __device__ __forceinline__ bool arg_better(float v1, int i1, float v2,
@@ -271,17 +297,29 @@ __device__ __forceinline__ int row_draw(
 // and of the draft the shard holds; a mask of which it holds) instead of
 // the accept test and draw.
 template <bool kStats>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 2)  // two CTAs per SM
     verify_kernel(const float* __restrict__ L, const int* __restrict__ draft,
                   const int* __restrict__ topi, const float* __restrict__ q,
-                  int B, int K, int V, int nchunk, int bpc, float T, float s2,
+                  int B, int K, int V, VerifyGrid g, float T, float s2,
                   uint64_t seed, uint64_t cycle, int* __restrict__ n_accepted,
                   int* __restrict__ out_tok, VerifyWs ws, int* err, int vec4,
                   int v0, float* __restrict__ stats) {
-  const int row = blockIdx.x, c = blockIdx.y, tid = threadIdx.x;
+  // CTAs in position order: the rows of positions t < g.t_split (enough to
+  // fill the GPU) in g.nchunk0 chunks each, chunk c of row (b, t) being CTA
+  // (t B + b) nchunk0 + c; after them the later positions' rows, in
+  // g.nchunk1 chunks each, in the same order
+  const int tid = threadIdx.x;
   const int lane = tid & 31, wid = tid >> 5;
-  const int K1 = K + 1, rows = B * K1;
-  const int b = row / K1, t = row % K1;
+  const int K1 = K + 1;
+  const unsigned n_early = (unsigned)(g.t_split * B * g.nchunk0);
+  const bool early = blockIdx.x < n_early;
+  const int nchunk = early ? g.nchunk0 : g.nchunk1;
+  const int bpc = early ? g.bpc0 : g.bpc1;
+  const unsigned xi = early ? blockIdx.x : blockIdx.x - n_early;
+  const int c = (int)(xi % (unsigned)nchunk);
+  const int rt = (int)(xi / (unsigned)nchunk);
+  const int t = (early ? 0 : g.t_split) + rt / B, b = rt % B;
+  const int row = b * K1 + t;
   const int nseg = (V + kSegTokens - 1) / kSegTokens;
   const float* x = L + (size_t)row * V;
   const bool greedy = (T == 0.f);
@@ -296,6 +334,16 @@ __global__ void __launch_bounds__(kThreads)
   __shared__ DrawSmem s_draw;
   __shared__ int s_ci[kC];
   __shared__ float s_qz[kC], s_corr[kC];
+
+  // A row after its sequence's first rejection is never emitted: once the
+  // sequence's mask shows a rejection before t, a warp stops reading.  The
+  // mask is read first (a CTA that starts after such a rejection reads no
+  // segment; the inputs below cover the read's latency), then one segment
+  // ahead.
+  const bool may_skip = !kStats && t > 0;
+  const unsigned before = (1u << t) - 1u;
+  unsigned mk = 0;
+  if (may_skip && lane == 0) mk = (unsigned)__ldcg(&ws.seq[b]);
 
   // ---- the drafter's inputs of this row, in flight during the main pass --
   // lanes 0-15 of warp 0: candidate j (token, q, target logit); lane 16:
@@ -322,6 +370,7 @@ __global__ void __launch_bounds__(kThreads)
 
   // ---- main pass ------------------------------------------------------
   // Segments of this chunk: sc0 .. sc1-1; warp w takes sc0 + w + 8 j.
+  bool skipped = false;
   bool bad = false;
   float ga = -INFINITY;   // T = 0: this thread's best value ...
   int gi = 0x7fffffff;    // ... and its (first) index
@@ -332,10 +381,15 @@ __global__ void __launch_bounds__(kThreads)
   // the row holds r_tok (a shard holds ids v0 .. v0 + V - 1)
   const bool r_own = r_tok >= v0 && r_tok - v0 < V;
   for (int j = 0; j < nmine; ++j) {
+    if (may_skip && (__shfl_sync(0xffffffffu, mk, 0) & before)) {
+      skipped = true;
+      break;
+    }
     const int seg = sc0 + wid + kWarps * j;
     const int base = seg * kSegTokens;
     float4 f[16];
     load_segment(x, base, V, lane, vec4, f);
+    if (may_skip && lane == 0) mk = (unsigned)__ldcg(&ws.seq[b]);
     if (j == 0 && wid == 0 && r_own) r_x = x[r_tok - v0];
     if (greedy) {
       float chk = 0.f;
@@ -388,7 +442,9 @@ __global__ void __launch_bounds__(kThreads)
     }
     if (lane == 0) { s_a[wid] = ga; s_i[wid] = gi; }
   }
-  __syncthreads();
+  // a CTA that stopped early leaves without arriving: its row is after the
+  // sequence's first rejection, and no result depends on it
+  if (__syncthreads_or(skipped)) return;
   if (tid == 0) {
     if (greedy) {
       float ra = s_a[0];
@@ -402,7 +458,7 @@ __global__ void __launch_bounds__(kThreads)
     }
     if (nchunk > 1) {
       __threadfence();
-      s_flag = (atomicAdd(&ws.counters[row], 1u) == (unsigned)(nchunk - 1));
+      s_flag = (atomicAdd(&ws.tickets[row], 1u) == (unsigned)(nchunk - 1));
     } else {
       s_flag = 1;
     }
@@ -421,7 +477,7 @@ __global__ void __launch_bounds__(kThreads)
   if (wid == 0) {
     // the sequence's rejection mask so far, in flight during the fold
     unsigned seen = 0;
-    if (!kStats && !greedy && lane == 0) seen = __ldcg(&ws.rejmask[b]);
+    if (!kStats && !greedy && lane == 0) seen = (unsigned)__ldcg(&ws.seq[b]);
     float ra = -INFINITY, rs = 0.f;
     int ri = 0x7fffffff;
     if (greedy) {
@@ -494,6 +550,7 @@ __global__ void __launch_bounds__(kThreads)
       if (lane == 0) {
         s_acc = acc;
         ws.row_tok[row] = ri;
+        if (has_draft && !acc) atomicOr(&ws.seq[b], 1ull << t);
       }
     } else {
       // residual corrections of the candidates: -min(p_j Z, q_j Z)
@@ -521,7 +578,7 @@ __global__ void __launch_bounds__(kThreads)
         const unsigned below = (1u << t) - 1u;
         if (has_draft) {
           s_need = !acc && !(seen & below);
-          if (!acc) atomicOr(&ws.rejmask[b], 1u << t);
+          if (!acc) atomicOr(&ws.seq[b], 1ull << t);
         } else {
           s_need = seen == 0u;
         }
@@ -539,15 +596,17 @@ __global__ void __launch_bounds__(kThreads)
     if (tid == 0) ws.row_tok[row] = tok;
   }
 
-  // ---- the sequence's word: arrivals (bits 16..) and rejected positions;
-  // its last row emits the tokens ------------------------------------------
+  // ---- the sequence's word: the row is decided (and, rejected, its
+  // position's bit); the row whose bit completes rows 0..n (n the first
+  // rejection) emits the tokens ------------------------------------------
   __syncthreads();
   if (tid == 0) {
-    const unsigned mine = (1u << 16) | (has_draft && !s_acc ? 1u << t : 0u);
-    __threadfence();  // the row's token before its arrival
-    const unsigned old = atomicAdd(&ws.counters[rows + b], mine);
-    s_flag = (old >> 16) == (unsigned)K;
-    s_rej = (old + mine) & 0xffffu;
+    const unsigned long long mine =
+        (1ull << (32 + t)) | (has_draft && !s_acc ? 1ull << t : 0ull);
+    __threadfence();  // the row's token before its bit
+    const unsigned long long old = atomicOr(&ws.seq[b], mine);
+    s_flag = !seq_settled(old, K) && seq_settled(old | mine, K);
+    s_rej = (unsigned)(old | mine);
   }
   __syncthreads();
   if (!s_flag || wid != 0) return;
@@ -760,12 +819,13 @@ size_t verify_ws_layout(int B, int K, int V, void* base, VerifyWs* o) {
   // per row: segment pairs (T > 0) or chunk argmaxes (T = 0, <= nseg)
   w.part = reinterpret_cast<float2*>(take(rows * nseg * sizeof(float2)));
   w.row_tok = reinterpret_cast<int*>(take(rows * sizeof(int)));
-  // tickets of rows (chunks done), the sequences' words (arrivals and
-  // rejected positions), then each sequence's mask of rejections seen by
-  // the draws, all zeroed together before a launch
-  w.counter_bytes = (rows + 2 * (size_t)B) * sizeof(unsigned);
+  // the sequences' 64-bit words (rejected positions, decided rows; first,
+  // so they are 8-byte aligned), then the rows' tickets (chunks done), all
+  // zeroed together before a launch
+  w.counter_bytes = (2 * (size_t)B + rows) * sizeof(unsigned);
   w.counters = reinterpret_cast<unsigned*>(take(w.counter_bytes));
-  w.rejmask = w.counters ? w.counters + rows + B : nullptr;
+  w.seq = reinterpret_cast<unsigned long long*>(w.counters);
+  w.tickets = w.counters ? w.counters + 2 * B : nullptr;
   if (o) *o = w;
   return align256(off);
 }
@@ -780,16 +840,38 @@ cudaError_t launch_verify(const float* L, const int* draft, const int* topi,
   const int nseg = (V + kSegTokens - 1) / kSegTokens;
   const int blocks_per_row = (V + kBlockTokens - 1) / kBlockTokens;
   const int vec4 = (V % 4 == 0) && ((reinterpret_cast<uintptr_t>(L) & 15) == 0);
-  // chunks of whole 16384-token blocks: about two CTAs per SM in total (so
-  // a large batch keeps one chunk per row and its pairs in shared memory),
-  // at most kVerifyMaxChunks per row
-  const long long per_sm = 2;
-  const long long total_blocks = (long long)rows * blocks_per_row;
-  int bpc = (int)std::max<long long>(
-      1, (total_blocks + per_sm * num_sms - 1) / (per_sm * num_sms));
-  bpc = std::max(bpc, (blocks_per_row + kVerifyMaxChunks - 1) / kVerifyMaxChunks);
-  bpc = std::min(bpc, blocks_per_row);
-  const int nchunk = (blocks_per_row + bpc - 1) / bpc;
+  // Chunks of whole 16384-token blocks, at most kVerifyMaxChunks per row,
+  // equal to within a block: for `nrows` rows, about two CTAs per SM.
+  const long long per_sm = 2, slots = per_sm * num_sms;
+  auto chunking = [&](long long nrows, int* nchunk, int* bpc) {
+    const long long blocks = nrows * blocks_per_row;
+    int b = (int)std::max<long long>(1, (blocks + slots - 1) / slots);
+    b = std::max(b, (blocks_per_row + kVerifyMaxChunks - 1) / kVerifyMaxChunks);
+    b = std::min(b, blocks_per_row);
+    *nchunk = (blocks_per_row + b - 1) / b;
+    *bpc = (blocks_per_row + *nchunk - 1) / *nchunk;
+  };
+  // The CTAs run in position order and rows after a sequence's first
+  // rejection stop early.  The first positions (enough to fill the GPU)
+  // get chunks sized so that position 0 alone makes about two CTAs per SM;
+  // the later positions get chunks sized over all their rows, so that few
+  // CTAs have to start (and, at low acceptance, leave at once).  Shard
+  // statistics read every row: one chunking over all rows.
+  VerifyGrid g{};
+  const int K1 = K + 1;
+  if (stats) {
+    chunking(rows, &g.nchunk0, &g.bpc0);
+    g.t_split = K1;
+  } else {
+    chunking(B, &g.nchunk0, &g.bpc0);
+    const long long per_pos = (long long)B * g.nchunk0;
+    g.t_split = (int)std::min<long long>(K1, (slots + per_pos - 1) / per_pos);
+  }
+  g.nchunk1 = g.nchunk0;
+  g.bpc1 = g.bpc0;
+  if (g.t_split < K1) chunking((long long)(K1 - g.t_split) * B, &g.nchunk1, &g.bpc1);
+  const long long ctas = (long long)g.t_split * B * g.nchunk0 +
+                         (long long)(K1 - g.t_split) * B * g.nchunk1;
   const float s2 = T > 0.f ? kLog2e / T : 0.f;
   const size_t smem = (size_t)nseg * sizeof(float2);
   auto kern = stats ? verify_kernel<true> : verify_kernel<false>;
@@ -798,8 +880,8 @@ cudaError_t launch_verify(const float* L, const int* draft, const int* topi,
         kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
-  kern<<<dim3(rows, nchunk), kThreads, smem, s>>>(
-      L, draft, topi, q, B, K, V, nchunk, bpc, T, s2, seed, cycle, n_accepted,
+  kern<<<(unsigned)ctas, kThreads, smem, s>>>(
+      L, draft, topi, q, B, K, V, g, T, s2, seed, cycle, n_accepted,
       out_tok, ws, err, vec4, v0, stats);
   return cudaGetLastError();
 }

@@ -273,6 +273,10 @@ dflash_status dflash_draft_e4m3(
  *   ws >= dflash_workspace_bytes(1, B, K, 0, V) bytes, 256-B aligned
  * Requirements: target_logits 16-byte aligned; T >= 0.  A NaN or +inf
  * target logit sets DFLASH_ERR_NONFINITE in the device error word.
+ * Rows are read in position order, and a row after its sequence's first
+ * rejection (which no result depends on) stops being read once that
+ * rejection is known: a non-finite logit there may go unreported.  Rows
+ * 0..n of every sequence are always read in full.
  */
 dflash_status dflash_verify(const float* target_logits, const int32_t* draft,
                             const int32_t* topi, const float* q, int B, int K,

@@ -359,9 +359,11 @@ def test_invalid_arguments_are_rejected(lib):
 
 
 def test_nonfinite_target_logit_is_reported(lib):
+    # in row 0, which is always read (rows after a sequence's first
+    # rejection may stop being read once it is known)
     B, K, V = 1, 2, 64
     L = torch.zeros(B, K + 1, V, device="cuda")
-    L[0, 1, 5] = float("nan")
+    L[0, 0, 5] = float("nan")
     draft = torch.zeros(B, K, dtype=torch.int32, device="cuda")
     topi = torch.zeros(B, K, C, dtype=torch.int32, device="cuda")
     topi[:, :, 1:] = -1
