@@ -313,6 +313,43 @@ def test_bonus_draw_follows_target_row_K_on_gpu(lib):
     assert stats.chisquare(cK, pK * B).pvalue > 1e-3
 
 
+
+@pytest.mark.parametrize("T", [1.0, 0.0])
+def test_verify_position_order_with_mixed_acceptance(lib, T):
+    """Rows run in position order and a row after a known rejection stops
+    reading.  B = 64, V = 40000 (3 blocks per row): positions 0-1 go in 3
+    chunks per row, the later ones in 1, so both chunkings and the stops
+    meet.  Sequence b accepts about m_b drafts (m_b spread over 0..K: the
+    target puts nearly all its mass on drafts 0..m_b-1 and almost none on
+    draft m_b); every sequence's n and tokens must match the oracle."""
+    B, K, V = 64, 8, 40000
+    rng = np.random.default_rng(71)
+    L = rng.standard_normal((B, K + 1, V)).astype(np.float32)
+    m = rng.integers(0, K + 1, size=B)
+    draft = rng.integers(0, V, size=(B, K)).astype(np.int32)
+    for b in range(B):
+        for t in range(K):
+            if t < m[b]:
+                L[b, t, draft[b, t]] = 20.0
+            else:
+                L[b, t, draft[b, t]] = -20.0
+    topi = np.full((B, K, C), -1, np.int32)
+    topi[:, :, 0] = draft
+    q = np.zeros((B, K, C), np.float32)
+    q[:, :, 0] = 1.0
+    d = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    n = torch.empty(B, dtype=torch.int32, device="cuda")
+    out = torch.empty(B, K + 1, dtype=torch.int32, device="cuda")
+    ws = torch.empty(lib.dflash_workspace_bytes(1, B, K, 0, V),
+                     dtype=torch.uint8, device="cuda")
+    lib.dflash_verify(d(L), d(draft), d(topi), d(q), T, 13, 2, n, out, ws)
+    torch.cuda.synchronize()
+    lib.dflash_check()
+    _, o_n, _ = check_verify(n, out, L, draft, topi, q, T, 13, 2)
+    assert np.array_equal(np_(n), o_n)
+    # the construction spreads the accepted lengths over 0..K
+    assert len(set(np_(n).tolist())) >= K - 1
+
 def test_p_equals_q_accepts_all(lib):
     V, K, B = 12, 4, 512
     rng = np.random.default_rng(5)
