@@ -6,8 +6,10 @@
 //
 // One launch over the B*(K+1) target rows, each in chunks, 256 threads:
 //   order       the CTAs go in position order (all sequences' chunks of
-//               position 0, then position 1, ...), the chunks sized so that
-//               position 0 alone fills the GPU (about two CTAs per SM).
+//               position 0, then position 1, ...).  The first positions,
+//               as many as fill the GPU, get chunks sized so that position
+//               0 alone makes about two CTAs per SM; the later ones get
+//               chunks sized over all their rows, so that few CTAs start.
 //               Only rows 0..n of a sequence matter (n its first
 //               rejection): once the sequence's word shows a rejection
 //               before t, the chunks of row t stop reading and leave
@@ -20,7 +22,8 @@
 //               block and reads it with 16-byte loads straight into
 //               registers (lane l holds the words 4l + 128u, u < 16), with
 //               no shared-memory staging.  Before each segment a warp
-//               checks the sequence's mask, read one segment ahead.  At
+//               checks the sequence's word (rejected positions), read at
+//               the CTA's start and then one segment ahead.  At
 //               T > 0 a warp reduces a segment to (max, sum
 //               2^((x-max)/T log2 e)); at T = 0 the CTA keeps the first
 //               argmax.
@@ -35,7 +38,7 @@
 //               gives the same token as drawing only the rejected one.  A
 //               row that cannot be emitted skips its draw: its draft was
 //               accepted, or an earlier position of the sequence had already
-//               recorded a rejection in the sequence's mask when the row
+//               recorded a rejection in the sequence's word when the row
 //               read it (for t = K: any rejection).  The drafter's inputs of
 //               row t (draft, candidates, q and the target logits at those
 //               tokens) are fetched at the start of the CTA, and the row's
@@ -336,8 +339,8 @@ __global__ void __launch_bounds__(kThreads, 2)  // two CTAs per SM
   __shared__ float s_qz[kC], s_corr[kC];
 
   // A row after its sequence's first rejection is never emitted: once the
-  // sequence's mask shows a rejection before t, a warp stops reading.  The
-  // mask is read first (a CTA that starts after such a rejection reads no
+  // sequence's word shows a rejection before t, a warp stops reading.  The
+  // word is read first (a CTA that starts after such a rejection reads no
   // segment; the inputs below cover the read's latency), then one segment
   // ahead.
   const bool may_skip = !kStats && t > 0;
@@ -475,7 +478,7 @@ __global__ void __launch_bounds__(kThreads, 2)  // two CTAs per SM
     __syncthreads();
   }
   if (wid == 0) {
-    // the sequence's rejection mask so far, in flight during the fold
+    // the sequence's rejections so far, in flight during the fold
     unsigned seen = 0;
     if (!kStats && !greedy && lane == 0) seen = (unsigned)__ldcg(&ws.seq[b]);
     float ra = -INFINITY, rs = 0.f;
@@ -572,8 +575,8 @@ __global__ void __launch_bounds__(kThreads, 2)  // two CTAs per SM
         s_acc = acc;
         // Row t's token is emitted only if t is the first rejection (t < K)
         // or nothing is rejected (t = K): a row whose draft was accepted,
-        // or that follows a rejection already in the sequence's mask (read
-        // before the fold), skips its draw.  A stale mask only costs a
+        // or that follows a rejection already in the sequence's word (read
+        // before the fold), skips its draw.  A stale word only costs a
         // draw.  The row's own rejection is added without waiting.
         const unsigned below = (1u << t) - 1u;
         if (has_draft) {
