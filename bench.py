@@ -503,15 +503,23 @@ def run_sweep(args):
               {"bound": "tensor", "frac": fl / t_lm / 1e12 / pk["bf16_tflops"],
                "hbm_frac": by / t_lm / 1e9 / pk["hbm_gbs"]})
         sb = stage_bytes(w, True)
+        n_mean = n_sum / (5 * w.B)
+        # the verify reads rows 0..n of each sequence (and the draw row),
+        # not every target row: its fraction is of those bytes
+        all_rows = sb["verify"]
+        sb["verify"] = verify_algorithmic(w, n_mean)
         line = {"sweep_point": w.name, "B": w.B, "K": w.K, "T": w.T,
                 "V": w.V, "H": w.H, "cycles_per_s": 1e3 / ms,
-                "ms_per_cycle": ms, "mean_accepted": n_sum / (5 * w.B),
+                "ms_per_cycle": ms, "mean_accepted": n_mean,
                 "stage_us": stage_us,
                 "stage_timing": "events around each kernel, 5 eager cycles",
                 "lmhead": lm,
                 "stage_hbm_frac": {k: sb[k] / (stage_us[k] * 1e-6) / 1e9 /
                                    pk["hbm_gbs"] for k in sb
                                    if k in stage_us},
+                "verify_all_rows_frac": all_rows / (stage_us["verify"] *
+                                                    1e-6) / 1e9 /
+                                        pk["hbm_gbs"],
                 "data": "synthetic (device-drawn, same distributions)",
                 "peak_source": pk["source"]}
         print(json.dumps(line), flush=True)
