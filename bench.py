@@ -264,6 +264,26 @@ def lmhead_algorithmic(w):
     return by, fl
 
 
+def verify_roofline(w, n_mean, verify_us, hbm_gbs):
+    """The verify stage against the HBM rate.  It reads rows 0..n of each
+    sequence (n accepted drafts), the draw row again, and of the later rows
+    only what it streams before the earlier rejection is known: the main
+    figure is the bytes the accepted lengths need; every target row's bytes
+    (what a verify reading all rows would move in the same time) beside
+    it."""
+    vb = verify_algorithmic(w, n_mean)
+    ab = w.B * (w.K + 1) * w.V * 4
+    t = verify_us * 1e-6
+    return {"bytes": vb, "GB/s": vb / t / 1e9,
+            "frac": vb / t / 1e9 / hbm_gbs,
+            "all_rows_bytes": ab, "all_rows_GB/s": ab / t / 1e9,
+            "frac_all_rows": ab / t / 1e9 / hbm_gbs,
+            "note": "rows after a sequence's first rejection stop being "
+                    "read once it is known; bytes = rows 0..n of each "
+                    "sequence and the draw row again; all_rows_bytes = "
+                    "every B*(K+1) target row"}
+
+
 def verify_algorithmic(w, n_mean):
     """Bytes the verify needs: target rows 0..n of each sequence (n
     accepted drafts), at T > 0 the draw row once more (the inverse CDF
@@ -783,23 +803,9 @@ def run_ours(args):
             stage_roof[name] = {"bytes": nbytes, "GB/s": gbs,
                                 "frac": gbs / pk["hbm_gbs"]}
     if "verify" in stage_roof:
-        # The verify reads rows 0..n of each sequence (n accepted drafts),
-        # the draw row again, and of the later rows only what it streams
-        # before the earlier rejection is known: the main figure is the
-        # bytes the accepted lengths need; every target row's bytes (what
-        # a verify reading all rows would move in the same time) beside it
-        ab = stage_roof["verify"]["bytes"]
-        vb = verify_algorithmic(w, n_mean_cycles)
-        vgbs = vb / (stage_us["verify"] * 1e-6) / 1e9
-        stage_roof["verify"] = {
-            "bytes": vb, "GB/s": vgbs, "frac": vgbs / pk["hbm_gbs"],
-            "all_rows_bytes": ab,
-            "all_rows_GB/s": stage_roof["verify"]["GB/s"],
-            "frac_all_rows": stage_roof["verify"]["frac"],
-            "note": "rows after a sequence's first rejection stop being "
-                    "read once it is known; bytes = rows 0..n of each "
-                    "sequence and the draw row again; all_rows_bytes = "
-                    "every B*(K+1) target row"}
+        stage_roof["verify"] = verify_roofline(w, n_mean_cycles,
+                                               stage_us["verify"],
+                                               pk["hbm_gbs"])
 
     # end to end through the public API with host buffers
     e2e_steps = args.e2e_steps or max(3, min(K, 20))

@@ -28,6 +28,25 @@ def test_stage_bytes_of_the_fused_cycle():
     assert sb8["quantize_y"] == 256 * 2048 * (2 + 1) + 256 * 4
 
 
+def test_verify_roofline_counts_the_rows_the_accepted_lengths_need():
+    w = synth.get("b32k8")                      # T = 1: the draw row again
+    row = 151936 * 4
+    side = 256 * 16 * 8 + 256 * 4               # candidates, q, drafts
+    assert bench.verify_algorithmic(w, 0.0) == 32 * 2 * row + side
+    assert bench.verify_algorithmic(w, 3.0) == 32 * 5 * row + side
+    g = synth.get("b1k8")                       # T = 0: no draw row
+    assert bench.verify_algorithmic(g, 1.0) == 1 * 2 * row + 8 * 16 * 8 + 8 * 4
+    r = bench.verify_roofline(w, 0.5, 25.0, 6791.4)
+    assert r["bytes"] == bench.verify_algorithmic(w, 0.5)
+    assert r["all_rows_bytes"] == 32 * 9 * row
+    assert abs(r["GB/s"] - r["bytes"] / 25e-6 / 1e9) < 1e-6
+    assert abs(r["frac"] * 6791.4 - r["GB/s"]) < 1e-6
+    # fewer bytes needed than all rows until every draft is accepted
+    assert r["frac"] < r["frac_all_rows"]
+    full = bench.verify_roofline(w, 8.0, 25.0, 6791.4)
+    assert full["bytes"] > full["all_rows_bytes"]   # all rows + draw rows
+
+
 def test_lmhead_strips_match_the_pair_grid():
     # 256 rows: two row tiles, CTA pairs, 76 pairs in one row group
     assert bench.lmhead_strips(synth.get("b32k8")) == 76
