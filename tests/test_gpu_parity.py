@@ -350,6 +350,47 @@ def test_verify_position_order_with_mixed_acceptance(lib, T):
     # the construction spreads the accepted lengths over 0..K
     assert len(set(np_(n).tolist())) >= K - 1
 
+
+@pytest.mark.parametrize("T", [1.0, 0.0])
+def test_verify_rows_after_the_first_rejection_do_not_matter(lib, T):
+    """Rows after a sequence's first rejection are never emitted (the CUDA
+    verify stops reading them once the rejection is known): replacing them
+    with other finite values leaves n and every token identical, bit for
+    bit, whichever of them the launch happened to read."""
+    B, K, V = 64, 8, 40000
+    rng = np.random.default_rng(73)
+    L = rng.standard_normal((B, K + 1, V)).astype(np.float32)
+    m = rng.integers(0, K + 1, size=B)
+    draft = rng.integers(0, V, size=(B, K)).astype(np.int32)
+    for b in range(B):
+        for t in range(K):
+            L[b, t, draft[b, t]] = 20.0 if t < m[b] else -20.0
+    topi = np.full((B, K, C), -1, np.int32)
+    topi[:, :, 0] = draft
+    q = np.zeros((B, K, C), np.float32)
+    q[:, :, 0] = 1.0
+    d = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    ws = torch.empty(lib.dflash_workspace_bytes(1, B, K, 0, V),
+                     dtype=torch.uint8, device="cuda")
+
+    def run(Lx):
+        n = torch.empty(B, dtype=torch.int32, device="cuda")
+        out = torch.empty(B, K + 1, dtype=torch.int32, device="cuda")
+        lib.dflash_verify(d(Lx), d(draft), d(topi), d(q), T, 21, 4, n, out,
+                          ws)
+        torch.cuda.synchronize()
+        lib.dflash_check()
+        return np_(n).copy(), np_(out).copy()
+
+    n1, o1 = run(L)
+    L2 = L.copy()
+    for b in range(B):
+        L2[b, n1[b] + 1:] = rng.standard_normal((K - n1[b], V)) * 4
+    n2, o2 = run(L2)
+    assert len(set(n1.tolist())) >= K - 1
+    assert np.array_equal(n1, n2)
+    assert np.array_equal(o1, o2)
+
 def test_p_equals_q_accepts_all(lib):
     V, K, B = 12, 4, 512
     rng = np.random.default_rng(5)

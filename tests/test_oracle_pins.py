@@ -564,6 +564,39 @@ def test_verify_output_layout():
         assert np.all(out[b, n[b] + 1:] == -1)
 
 
+
+@pytest.mark.parametrize("T", [0.8, 0.0])
+def test_verify_ignores_rows_after_the_first_rejection(T):
+    """The result of sequence b depends only on its target rows 0..n (n its
+    first rejection; the bonus row when n = K): the accept tests stop at the
+    first rejection and the draw uses row n alone ("Lossless, with
+    conditions...", DFlash 2: Block diffusion, wearing a drafter's coat).
+    Rows after n replaced by other finite values leave n and every emitted
+    token unchanged.  (The CUDA verify stops reading such rows.)"""
+    V, K, B = 40, 6, 200
+    rng = np.random.default_rng(31)
+    L = rng.standard_normal((B, K + 1, V)).astype(np.float32) * 2
+    topi = np.stack([np.stack([rng.choice(V, C, replace=False)
+                               for _ in range(K)]) for _ in range(B)])
+    q = rng.dirichlet(np.ones(C), size=(B, K)).astype(np.float32)
+    slot = rng.integers(0, C, (B, K))
+    draft = np.take_along_axis(topi, slot[..., None], 2)[..., 0]
+    # make some drafts likely to be accepted, so n spreads over 0..K
+    for b in range(B):
+        for t in range(int(rng.integers(0, K + 1))):
+            L[b, t, draft[b, t]] += 8.0
+    ua = philox.accept_uniforms(5, 7, B, K) if T > 0 else None
+    ur = philox.resample_uniforms(5, 7, B, K) if T > 0 else None
+    ti = topi.astype(np.int32)
+    n, out, _ = oracle.verify(L, draft, ti, q, T, ua, ur)
+    assert len(set(n.tolist())) >= 4
+    L2 = L.copy()
+    for b in range(B):
+        L2[b, n[b] + 1:] = rng.standard_normal((K - n[b], V)) * 5
+    n2, out2, _ = oracle.verify(L2, draft, ti, q, T, ua, ur)
+    assert np.array_equal(n, n2)
+    assert np.array_equal(out, out2)
+
 # --------------------------------------------------------------------------
 # whole cycle on the tiny workload
 # --------------------------------------------------------------------------
